@@ -1,0 +1,81 @@
+"""Scaled-FP8 GEMM over dequantized operands, in float64.
+
+Test infrastructure only (see ``oracle/__init__``).
+
+Whatever the granularity, the scaled-FP8 product is the plain matrix product
+of the dequantized operands:
+
+    C[m, n] = sum_k decode(qa[m, k]) * sa(m, k) * decode(qb[n, k]) * sb(n, k)
+
+where sa(m, k) / sb(n, k) is the scale that covers element (m, k) / (n, k):
+
+* per tensor: one scalar each; the Flax guide (section 2.2) contracts the
+  codes with fp32 accumulation and multiplies by ``a_scale * b_scale``
+  afterwards, which is the same sum.
+* per K group (Transformers fine-grained FP8, 一): sa[m, k // 128] times
+  sb[n // 128, k // 128].
+* two-level (MOSS blog, section 4): S_a * r_a[m, k // 32] times
+  S_b * r_b[n, k // 32].
+
+Both operands are stored [rows, K] with K contiguous ("A row-major, B
+column-major", the TN layout of the nanochat module, "核心原语").  ``b`` is
+therefore [N, K], the layout of ``nn.Linear.weight``.
+
+Alongside C the oracle returns the error budget of each element,
+``E[m, n] = sum_k |a_deq[m, k]| * |b_deq[n, k]|``; an FP32-accumulated result
+is accepted when ``|gpu - C| <= 1e-3 * E`` (plus one output ulp of |C| for a
+bf16 output).
+
+Pins (``tests/test_oracle_gemm.py``): exact rational brute force on tiny
+shapes (products of two 8-bit floats and their short sums are exact), the
+scale = 1 case against an integer matmul on the code grid, and a transposed
+operand / dropped scale / sign flip each failing the check.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .formats import decode
+
+
+def dequant_operand(q, fmt, scale_full) -> np.ndarray:
+    """decode(q) * scale, float64; ``scale_full`` broadcasts against q."""
+    return decode(q, fmt) * np.asarray(scale_full, dtype=np.float64)
+
+
+def gemm(a_deq, b_deq):
+    """C = A @ B^T and E = |A| @ |B|^T, float64; A [M,K], B [N,K]."""
+    a = np.asarray(a_deq, dtype=np.float64)
+    b = np.asarray(b_deq, dtype=np.float64)
+    return a @ b.T, np.abs(a) @ np.abs(b).T
+
+
+def gemm_sampled(a_deq, b_deq, rows, cols):
+    """C and E at the (rows[i], cols[i]) output positions only."""
+    a = np.asarray(a_deq, dtype=np.float64)[np.asarray(rows)]
+    b = np.asarray(b_deq, dtype=np.float64)[np.asarray(cols)]
+    return np.sum(a * b, axis=1), np.sum(np.abs(a) * np.abs(b), axis=1)
+
+
+def bf16_ulp(v) -> np.ndarray:
+    """Spacing of bf16 values (8 significant bits) at |v|."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    _, ex = np.frexp(a)
+    ulp = np.ldexp(1.0, ex - 8)
+    return np.where(a > 0, ulp, np.ldexp(1.0, -133))
+
+
+def tolerance(c_ref, e_ref, out_dtype: str, rel: float = 1e-3) -> np.ndarray:
+    tol = rel * np.asarray(e_ref, dtype=np.float64)
+    if out_dtype == "bf16":
+        tol = tol + bf16_ulp(c_ref)
+    return tol
+
+
+def check(c_gpu, c_ref, e_ref, out_dtype: str, rel: float = 1e-3):
+    """Returns (ok, worst ratio |err| / tol)."""
+    err = np.abs(np.asarray(c_gpu, dtype=np.float64) - np.asarray(c_ref, dtype=np.float64))
+    tol = tolerance(c_ref, e_ref, out_dtype, rel)
+    ratio = err / tol
+    worst = float(np.max(ratio)) if ratio.size else 0.0
+    return bool(np.all(err <= tol)), worst

@@ -1,0 +1,129 @@
+"""Pins for the float64 dequantized GEMM (oracle/gemm.py) and its tolerance.
+
+Evidence: exact rational arithmetic (fractions.Fraction over values decoded by
+torch's float8 dtypes) on tiny shapes, an integer matmul on the E4M3 code grid
+for unit scales, and plausible mistakes (a transposed operand, a dropped scale,
+a sign flip, a per-group scale applied to the wrong group) each failing the
+acceptance check.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import gemm as G
+from oracle import quantize as Q
+
+F32 = np.float32
+
+
+def torch_decode(codes, name):
+    dt = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[name]
+    return torch.tensor(np.asarray(codes, dtype=np.uint8)).view(dt).to(torch.float64).numpy()
+
+
+def finite_codes(rng, shape, name):
+    c = rng.integers(0, 256, shape).astype(np.uint8)
+    bad = np.isnan(torch_decode(c, name)) | np.isinf(torch_decode(c, name))
+    c[bad] = 0x38 if name == "e4m3" else 0x3C
+    return c
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (3, 5, 7), (8, 8, 8), (2, 7, 4)])
+@pytest.mark.parametrize("names", [("e4m3", "e4m3"), ("e5m2", "e4m3")])
+def test_exact_rational_brute_force(shape, names):
+    m, n, k = shape
+    rng = np.random.default_rng(m * 100 + n * 10 + k)
+    qa, qb = finite_codes(rng, (m, k), names[0]), finite_codes(rng, (n, k), names[1])
+    sa, sb = F32(rng.uniform(1e-3, 10)), F32(rng.uniform(1e-3, 10))
+    c, e = G.gemm(G.dequant_operand(qa, names[0], sa), G.dequant_operand(qb, names[1], sb))
+    av, bv = torch_decode(qa, names[0]), torch_decode(qb, names[1])
+    for i in range(m):
+        for j in range(n):
+            exact = sum(Fraction(av[i, t]) * Fraction(bv[j, t]) for t in range(k))
+            exact *= Fraction(float(sa)) * Fraction(float(sb))
+            mag = sum(abs(Fraction(av[i, t]) * Fraction(bv[j, t])) for t in range(k))
+            mag *= Fraction(float(sa)) * Fraction(float(sb))
+            assert abs(Fraction(c[i, j]) - exact) <= Fraction(2, 10 ** 15) * (mag + 1)
+            assert abs(Fraction(e[i, j]) - mag) <= Fraction(2, 10 ** 15) * (mag + 1)
+
+
+def test_unit_scale_equals_integer_grid_matmul():
+    # every finite E4M3 value is an integer multiple of 2^-9
+    rng = np.random.default_rng(1)
+    qa, qb = finite_codes(rng, (16, 32), "e4m3"), finite_codes(rng, (64, 32), "e4m3")
+    ia = (torch_decode(qa, "e4m3") * 512).astype(np.int64)
+    ib = (torch_decode(qb, "e4m3") * 512).astype(np.int64)
+    c, _ = G.gemm(G.dequant_operand(qa, "e4m3", 1.0), G.dequant_operand(qb, "e4m3", 1.0))
+    assert np.array_equal(c * 512 * 512, (ia @ ib.T).astype(np.float64))
+
+
+def test_group_scales_brute_force():
+    rng = np.random.default_rng(5)
+    m, n, k = 3, 130, 256
+    qa, qb = finite_codes(rng, (m, k), "e4m3"), finite_codes(rng, (n, k), "e4m3")
+    sa = rng.uniform(0.5, 2, (m, 2)).astype(F32)
+    sb = rng.uniform(0.5, 2, (2, 2)).astype(F32)
+    a = G.dequant_operand(qa, "e4m3", Q.expand(sa, m, k, 1, 128))
+    b = G.dequant_operand(qb, "e4m3", Q.expand(sb, n, k, 128, 128))
+    c, _ = G.gemm(a, b)
+    av, bv = torch_decode(qa, "e4m3"), torch_decode(qb, "e4m3")
+    for i in range(m):
+        for j in (0, 127, 128, 129):
+            ref = 0.0
+            for g in range(2):
+                part = sum(av[i, t] * bv[j, t] for t in range(128 * g, 128 * g + 128))
+                ref += float(sa[i, g]) * float(sb[j // 128, g]) * part
+            assert abs(c[i, j] - ref) <= 1e-12 * (abs(ref) + 1)
+
+
+def test_sampled_matches_full():
+    rng = np.random.default_rng(2)
+    a = rng.standard_normal((40, 64))
+    b = rng.standard_normal((50, 64))
+    c, e = G.gemm(a, b)
+    rows, cols = rng.integers(0, 40, 30), rng.integers(0, 50, 30)
+    cs, es = G.gemm_sampled(a, b, rows, cols)
+    assert np.allclose(cs, c[rows, cols], rtol=0, atol=1e-12)
+    assert np.allclose(es, e[rows, cols], rtol=0, atol=1e-12)
+
+
+def test_tolerance_catches_plausible_mistakes():
+    x, w, _ = workloads.float8_linear(tokens=64, d_in=256, d_out=48)
+    xf, wf = x.float().numpy(), w.float().numpy()
+    qa, sa = Q.quantize_tensor(xf, "e4m3")
+    qb, sb = Q.quantize_tensor(wf, "e4m3")
+    a = G.dequant_operand(qa, "e4m3", sa)
+    b = G.dequant_operand(qb, "e4m3", sb)
+    c, e = G.gemm(a, b)
+    # an fp32-accumulated result passes
+    c32 = (a.astype(F32) @ b.astype(F32).T).astype(np.float64)
+    assert G.check(c32, c, e, "f32")[0]
+    # a dropped scale fails
+    assert not G.check(c / float(sb), c, e, "f32")[0]
+    # a sign flip fails
+    assert not G.check(-c, c, e, "f32")[0]
+    # a transposed operand (square case) fails
+    sq = b[:48, :48]
+    c2, e2 = G.gemm(a[:, :48], sq)
+    wrong, _ = G.gemm(a[:, :48], sq.T)
+    assert not G.check(wrong, c2, e2, "f32")[0]
+    # a group scale applied to the neighbouring group fails
+    sg = np.array([[1.0, 4.0]])
+    ag = a[:, :256] * Q.expand(np.repeat(sg, 64, 0), 64, 256, 1, 128)
+    ag_wrong = a[:, :256] * Q.expand(np.repeat(sg[:, ::-1], 64, 0), 64, 256, 1, 128)
+    cg, eg = G.gemm(ag, b[:, :256])
+    cw, _ = G.gemm(ag_wrong, b[:, :256])
+    assert not G.check(cw, cg, eg, "f32")[0]
+
+
+def test_bf16_ulp():
+    assert G.bf16_ulp(1.0) == 2.0 ** -7
+    assert G.bf16_ulp(1.5) == 2.0 ** -7
+    assert G.bf16_ulp(-3.0) == 2.0 ** -6
+    # one bf16 ulp is exactly the gap torch's bf16 grid has at that value
+    v = torch.tensor([1.0, 3.0, 1000.0], dtype=torch.bfloat16)
+    nxt = torch.nextafter(v, torch.tensor(float("inf"), dtype=torch.bfloat16))
+    assert np.array_equal((nxt - v).double().numpy(), G.bf16_ulp(v.double().numpy()))

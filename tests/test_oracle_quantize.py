@@ -1,0 +1,176 @@
+"""Pins for the oracle's quantizers (oracle/quantize.py).
+
+Evidence independent of the oracle's own code: hand encodings, torch's float8
+cast (a library routine) applied to values scaled by an exact power of two,
+the defining property that the amax element lands on +-MAX, and the MOSS
+two-level invariants.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from golden.fixtures import load
+from oracle import formats as F
+from oracle import quantize as Q
+
+CONST = load("format_constants.txt")
+F32 = np.float32
+
+
+def torch_cast(vals_f32, name):
+    dt = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[name]
+    return torch.tensor(np.asarray(vals_f32, dtype=F32)).to(dt).view(torch.uint8).numpy()
+
+
+def test_hand_per_tensor():
+    # amax 448 -> scale exactly 1.0 -> 1.0, -448, 0.5 encode as by hand
+    q, s = Q.quantize_tensor(np.array([1.0, -448.0, 0.5], F32), "e4m3")
+    assert s == 1.0 and list(q) == [0x38, 0xFE, 0x30]
+    # amax 7 -> scale 7/448 = 1/64 -> 3.5 * 64 = 224 = 0.1110.110
+    q, s = Q.quantize_tensor(np.array([3.5, -7.0, 0.0], F32), "e4m3")
+    assert s == 1.0 / 64 and list(q) == [0x76, 0xFE, 0x00]
+    # E5M2 gradient: amax 57344 * 2 -> scale 2 -> 1.0 encodes as 0.01111.00
+    q, s = Q.quantize_tensor(np.array([2.0, -114688.0], F32), "e5m2")
+    assert s == 2.0 and list(q) == [0x3C, 0xFB]
+
+
+@pytest.mark.parametrize("name", ["e4m3", "e5m2"])
+def test_amax_element_hits_max(name):
+    x = workloads.normal((64, 96), 3.0, seed=11).numpy()
+    q, s = Q.quantize_tensor(x, name)
+    i = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert abs(F.decode(q[i], name)) == F.fmt_of(name).max
+    assert np.all(np.isfinite(F.decode(q, name)))
+
+
+@pytest.mark.parametrize("name", ["e4m3", "e5m2"])
+def test_roundtrip_within_half_step(name):
+    f = F.fmt_of(name)
+    x = workloads.normal((128, 64), 1.0, seed=5).numpy()
+    q, s = Q.quantize_tensor(x, name)
+    y = np.abs(x.astype(np.float64) / float(s))
+    e = np.maximum(np.floor(np.log2(np.maximum(y, 1e-300))), f.min_normal_exp)
+    half_step = np.ldexp(0.5, (e - f.mbits).astype(int)) * float(s)
+    err = np.abs(Q.dequantize(q, name, s) - x)
+    assert np.all(err <= half_step * (1 + 1e-6) + 1e-30)
+
+
+def test_zero_and_signed_zero():
+    q, s = Q.quantize_tensor(np.zeros((4, 4), F32), "e4m3")
+    assert s == 1.0 and not q.any()
+    q, s = Q.quantize_tensor(np.array([-0.0, 1.0], F32), "e4m3")
+    assert q[0] == 0x80
+
+
+def test_pow2_scale_matches_library_cast():
+    # with a power-of-two scale the division is exact, so quantization is
+    # torch's cast of x * 2^-e (clipped): independent of the oracle's division
+    x = workloads.normal((33, 130), 10.0, seed=9).numpy()
+    for e in (-3, 0, 4):
+        q = Q.quantize_with_scale(x, F32(2.0 ** e), "e4m3")
+        ref = torch_cast(np.clip(x * F32(2.0 ** -e), -448, 448), "e4m3")
+        assert np.array_equal(q, ref)
+
+
+def _group_views(x, q, rows, cols):
+    for r0 in range(0, x.shape[0], rows):
+        for c0 in range(0, x.shape[1], cols):
+            yield (r0 // rows, c0 // cols), x[r0:r0 + rows, c0:c0 + cols], q[r0:r0 + rows, c0:c0 + cols]
+
+
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_token_group_properties(sfmt):
+    x = workloads.normal((5, 300), 1.0, seed=21).numpy()   # ragged last group (44 wide)
+    x[2, 130] = 80.0                                     # outlier in one group only
+    x[3, 128:256] = 0.0                                  # an all-zero group
+    q, sc = Q.quantize_token_group(x, "e4m3", sfmt)
+    assert sc.shape == (5, 3)
+    vals = Q.group_scale_values(sc, sfmt)
+    for (i, j), xg, qg in _group_views(x, q, 1, 128):
+        am = float(np.max(np.abs(xg)))
+        mag = np.max(np.abs(F.decode(qg, "e4m3")))
+        if am == 0:
+            assert vals[i, j] == 1.0 and not qg.any()
+            continue
+        if sfmt == "f32":
+            assert vals[i, j] == np.float32(np.float32(am) / np.float32(448.0))
+            assert mag == 448.0
+        else:
+            e = int(np.log2(vals[i, j]))
+            assert vals[i, j] == 2.0 ** e
+            assert 2.0 ** (e - 1) < am / 448.0 <= 2.0 ** e * (1 + 2 ** -23)
+            assert 224.0 <= mag <= 448.0
+            assert np.array_equal(qg, torch_cast(np.clip(xg * F32(2.0 ** -e), -448, 448), "e4m3"))
+    # the outlier only moves its own group's scale
+    x2 = x.copy()
+    x2[2, 130] = 1.0
+    q2, sc2 = Q.quantize_token_group(x2, "e4m3", sfmt)
+    diff = np.argwhere(np.asarray(sc) != np.asarray(sc2))
+    assert [tuple(d) for d in diff] == [(2, 1)]
+
+
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_block_properties_and_transpose(sfmt):
+    w = workloads.normal((200, 260), 0.02, seed=22).numpy()   # ragged in both dims
+    q, sc = Q.quantize_block(w, "e4m3", sfmt)
+    assert sc.shape == (2, 3)
+    vals = Q.group_scale_values(sc, sfmt)
+    for (i, j), wb, qb in _group_views(w, q, 128, 128):
+        am = np.float32(np.max(np.abs(wb)))
+        if sfmt == "f32":
+            assert vals[i, j] == np.float32(am / np.float32(448.0))
+            assert np.max(np.abs(F.decode(qb, "e4m3"))) == 448.0
+        else:
+            assert 224.0 <= np.max(np.abs(F.decode(qb, "e4m3"))) <= 448.0
+    qt, sct = Q.quantize_block(w.T.copy(), "e4m3", sfmt)
+    assert np.array_equal(qt, q.T) and np.array_equal(np.asarray(sct), np.asarray(sc).T)
+
+
+def test_two_level_invariants():
+    a, _ = workloads.two_level(m=64, n=8, k=512)
+    x = a.float().numpy()
+    q, local, big_s = Q.quantize_two_level(x, "e4m3")
+    assert local.shape == (64, 16)
+    s_i = (np.max(np.abs(x.reshape(64, 16, 32)), axis=2) / F32(448)).astype(F32)
+    # global factor = max of the 1x32 fp32 scales = fl32(tensor amax / MAX)
+    assert big_s == np.max(s_i) == np.float32(np.float32(np.max(np.abs(x))) / F32(448))
+    r = F.e8m0_decode(local)
+    assert np.all((r > 0) & (r <= 1))
+    assert np.all(np.log2(r) == np.round(np.log2(r)))
+    assert np.all(float(big_s) * r >= s_i.astype(np.float64))
+    # r is the smallest such power of two
+    assert np.all(float(big_s) * r / 2 < s_i.astype(np.float64))
+    d = F.decode(q, "e4m3")
+    assert np.all(np.isfinite(d)) and np.max(np.abs(d)) <= 448.0
+    y = x.reshape(64, 16, 32) / (float(big_s) * r)[:, :, None]
+    assert np.max(np.abs(y)) <= 448.0 * (1 + 2 ** -22)
+
+
+def test_two_level_reduces_to_per_tensor():
+    # equal block amaxes -> every r_i = 1 -> per-tensor quantization
+    x = workloads.normal((4, 128), 1.0, seed=31).numpy()
+    x.reshape(4, 4, 32)[:, :, 0] = 5.0
+    q, local, big_s = Q.quantize_two_level(x, "e4m3")
+    assert np.all(local == 127)
+    qt, st = Q.quantize_tensor(x, "e4m3")
+    assert big_s == st and np.array_equal(q, qt)
+
+
+def test_two_level_rescues_small_blocks():
+    # half the 1x32 blocks are 2^-16 smaller: per-tensor scaling pushes them into
+    # E4M3 subnormals, the E8M0 local factors lift them back into the normal range
+    from oracle.snr import snr_db
+    x = workloads.normal((64, 256), 1.0, seed=41).numpy()
+    xb = x.reshape(64, 8, 32)
+    xb[:, 1::2, :] *= np.float32(2.0 ** -16)
+    q2, l2, s2 = Q.quantize_two_level(x, "e4m3")
+    d2 = F.decode(q2, "e4m3") * Q.expand(Q.two_level_scale_values(l2, float(s2)), 64, 256, 1, 32)
+    qt, st = Q.quantize_tensor(x, "e4m3")
+    dt = Q.dequantize(qt, "e4m3", st)
+    small = np.zeros_like(xb, dtype=bool)
+    small[:, 1::2, :] = True
+    small = small.reshape(64, 256)
+    assert snr_db(x[small], d2[small]) > snr_db(x[small], dt[small]) + 20.0
+    # on the large blocks both schemes agree exactly
+    assert np.array_equal(d2[~small], dt[~small])
