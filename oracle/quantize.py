@@ -166,8 +166,9 @@ def quantize_two_level(x, fmt, block=32):
     if not big_s > 0:
         big_s = F32(1.0)
     ratio = (s_i / big_s).astype(F32)                       # step 3
+    # all-zero block: r = 1; a positive block whose ratio underflows: 2^-127
+    e = np.where(s_i > 0, -127, 0).astype(np.int64)
     pos = ratio > 0
-    e = np.zeros(ratio.shape, dtype=np.int64)
     if np.any(pos):
         e[pos] = np.maximum(ceil_log2_f32(ratio[pos]), -127)
     r_i = np.ldexp(F32(1.0), e).astype(F32)
