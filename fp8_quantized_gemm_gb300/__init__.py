@@ -1,0 +1,195 @@
+"""Thin Python binding of libfp8gemm.so (the C ABI in include/fp8gemm.h).
+
+Argument marshalling only: each function takes torch CUDA tensors, passes
+their device pointers, sizes and the current CUDA stream to the C entry point
+of the same name, and raises ``Fp8Error`` on a non-zero status.  Every step of
+the computation runs in the library's CUDA kernels; there is no CPU path.
+
+The library must have been built (``python -c "import __graft_entry__ as g;
+g.build()"`` or ``python fp8_quantized_gemm_gb300/build.py``); importing this
+package without it raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8gemm.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libfp8gemm.so is not built (%s); run fp8_quantized_gemm_gb300/build.py" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# enums (include/fp8gemm.h)
+FP8_OK, FP8_ERR_INVALID_ARG, FP8_ERR_MISALIGNED = 0, -1, -2
+FP8_ERR_UNSUPPORTED, FP8_ERR_CUDA, FP8_ERR_TIMEOUT, FP8_ERR_NO_DEVICE = -3, -4, -5, -6
+IN_BF16, IN_F32 = 0, 1
+E4M3, E5M2 = 0, 1
+SCALE_F32, SCALE_UE8M0 = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
+
+_vp, _i64, _int, _f = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+_SIGS = {
+    "fp8_amax": [_vp, _int, _i64, _vp, _vp],
+    "fp8_quantize_tensor": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "fp8_quantize_token_group": [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp],
+    "fp8_quantize_block": [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp],
+    "fp8_quantize_mx": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp],
+    "fp8_gemm_tensor": [_vp, _int, _vp, _int, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp],
+    "fp8_gemm_group": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
+    "fp8_gemm_mx": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp],
+    "fp8_delayed_state_update": [_vp, _vp, _vp, _i64, _int, _vp],
+    "fp8_swiglu_forward": [_vp, _vp, _vp, _i64, _vp],
+    "fp8_swiglu_backward": [_vp, _vp, _vp, _vp, _vp, _i64, _vp],
+    "fp8_adamw_step": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f, _f, _f, _f, _f, _vp],
+    "fp8_get_last_device_error": [ctypes.POINTER(ctypes.c_int), _vp],
+}
+for _name, _args in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = ctypes.c_int
+_lib.fp8_status_string.argtypes = [_int]
+_lib.fp8_status_string.restype = ctypes.c_char_p
+_lib.fp8_version.argtypes = []
+_lib.fp8_version.restype = ctypes.c_char_p
+
+EXPORTED = tuple(_SIGS) + ("fp8_status_string", "fp8_version")
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, name: str, status: int):
+        super().__init__("%s failed: %s (%d)" % (name, status_string(status), status))
+        self.status = status
+
+
+def status_string(status: int) -> str:
+    return _lib.fp8_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return _lib.fp8_version().decode()
+
+
+def _p(t):
+    """Device pointer of a CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _call(name, *args):
+    rc = getattr(_lib, name)(*args)
+    if rc != FP8_OK:
+        raise Fp8Error(name, rc)
+
+
+def _in_dt(t) -> int:
+    if t.dtype == torch.bfloat16:
+        return IN_BF16
+    if t.dtype == torch.float32:
+        return IN_F32
+    raise ValueError("input must be bf16 or fp32")
+
+
+# ----------------------------------------------------------------- calls --
+
+def fp8_amax(x, amax_out, stream=None):
+    _call("fp8_amax", _p(x), _in_dt(x), x.numel(), _p(amax_out), _stream(stream))
+
+
+def fp8_quantize_tensor(x, fmt, q, *, amax_in=None, scale=None, scale_out=None, q_t=None,
+                        amax_out=None, stream=None):
+    rows, cols = x.shape
+    _call("fp8_quantize_tensor", _p(x), _in_dt(x), rows, cols, fmt, _p(amax_in), _p(scale),
+          _p(scale_out), _p(q), _p(q_t), _p(amax_out), _stream(stream))
+
+
+def fp8_quantize_token_group(x, fmt, sfmt, q, scales, stream=None):
+    m, k = x.shape
+    _call("fp8_quantize_token_group", _p(x), _in_dt(x), m, k, fmt, sfmt, _p(q), _p(scales),
+          _stream(stream))
+
+
+def fp8_quantize_block(w, fmt, sfmt, q, scales, stream=None):
+    n, k = w.shape
+    _call("fp8_quantize_block", _p(w), _in_dt(w), n, k, fmt, sfmt, _p(q), _p(scales),
+          _stream(stream))
+
+
+def fp8_quantize_mx(x, fmt, amax, global_out, q, local, stream=None):
+    r, k = x.shape
+    _call("fp8_quantize_mx", _p(x), _in_dt(x), r, k, fmt, _p(amax), _p(global_out), _p(q),
+          _p(local), _stream(stream))
+
+
+def fp8_gemm_tensor(a, fa, b, fb, sa, sb, out, *, out_dt=None, accumulate=False, stream=None):
+    m, k = a.shape
+    n = b.shape[0]
+    if out_dt is None:
+        out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    _call("fp8_gemm_tensor", _p(a), fa, _p(b), fb, _p(sa), _p(sb), m, n, k, out_dt, _p(out),
+          out.stride(0), int(bool(accumulate)), _stream(stream))
+
+
+def fp8_gemm_group(a, sa, b, sb, sfmt, out, stream=None):
+    m, k = a.shape
+    n = b.shape[0]
+    _call("fp8_gemm_group", _p(a), _p(sa), _p(b), _p(sb), sfmt, m, n, k, _p(out), out.stride(0),
+          _stream(stream))
+
+
+def fp8_gemm_mx(a, la, ga, b, lb, gb, out, *, out_dt=None, stream=None):
+    m, k = a.shape
+    n = b.shape[0]
+    if out_dt is None:
+        out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    _call("fp8_gemm_mx", _p(a), _p(la), _p(ga), _p(b), _p(lb), _p(gb), m, n, k, out_dt, _p(out),
+          out.stride(0), _stream(stream))
+
+
+def fp8_delayed_state_update(hist, scale, amax_cur, fmt, stream=None):
+    _call("fp8_delayed_state_update", _p(hist), _p(scale), _p(amax_cur), hist.numel(), fmt,
+          _stream(stream))
+
+
+def fp8_swiglu_forward(h, u, a, stream=None):
+    _call("fp8_swiglu_forward", _p(h), _p(u), _p(a), h.numel(), _stream(stream))
+
+
+def fp8_swiglu_backward(da, h, u, dh, du, stream=None):
+    _call("fp8_swiglu_backward", _p(da), _p(h), _p(u), _p(dh), _p(du), h.numel(), _stream(stream))
+
+
+def fp8_adamw_step(p, g, m, v, p_bf16, step, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8,
+                   weight_decay=0.01, stream=None):
+    _call("fp8_adamw_step", _p(p), _p(g), _p(m), _p(v), _p(p_bf16), p.numel(), int(step), lr,
+          beta1, beta2, eps, weight_decay, _stream(stream))
+
+
+def fp8_get_last_device_error(stream=None):
+    """(status, where): status 0 or FP8_ERR_TIMEOUT; clears the word."""
+    where = ctypes.c_int(0)
+    rc = _lib.fp8_get_last_device_error(ctypes.byref(where), _stream(stream))
+    return rc, where.value
+
+
+# ------------------------------------------------------------ allocation --
+
+def mx_local_words(rows: int, k: int, device="cuda"):
+    """Buffer for fp8_quantize_mx's packed local factors: uint32 [K/128, R_pad]."""
+    rpad = (rows + 127) // 128 * 128
+    return torch.empty((k // 128, rpad), dtype=torch.int32, device=device)

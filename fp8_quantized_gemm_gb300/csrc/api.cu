@@ -1,0 +1,316 @@
+// C ABI of libfp8gemm.so (declared in include/fp8gemm.h): argument
+// validation, TMA descriptor encoding, per-device setup and launches.
+//
+// The library links the CUDA runtime statically and reaches the driver's
+// cuTensorMapEncodeTiled through cudaGetDriverEntryPointByVersion, so the
+// shared object loads on a machine without a GPU driver (only the calls need
+// a device).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "fp8gemm.h"
+#include "kernels.h"
+#include "support.h"
+
+namespace {
+
+using fp8k::GemmArgs;
+
+// Device error word: [0] first error code (positive), [1] where.
+__device__ uint32_t g_device_error[2];
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  uint32_t *err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+// Per-device setup, once per device with that device current.
+int device_state(DeviceState **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FP8_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) return FP8_ERR_NO_DEVICE;  // built for sm_103a only
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FP8_ERR_CUDA;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return FP8_ERR_CUDA;
+    d.err = static_cast<uint32_t *>(p);
+    if (g_encode == nullptr) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FP8_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return FP8_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_fmt(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }
+bool valid_in(int d) { return d == FP8_IN_BF16 || d == FP8_IN_F32; }
+constexpr int64_t kMaxDim = (int64_t)1 << 31;
+
+// 2-D uint8 operand [rows, k] with row pitch k bytes; box {128, box_rows},
+// 128-byte swizzle (the layout the UMMA shared-memory descriptor expects).
+int encode_operand(CUtensorMap *map, const void *base, int64_t k, int64_t rows, int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)k};
+  const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
+int check_output(const void *c, int64_t N, int64_t ldc, int out_dt) {
+  if (c == nullptr) return FP8_ERR_INVALID_ARG;
+  if (out_dt != FP8_OUT_F32 && out_dt != FP8_OUT_BF16) return FP8_ERR_INVALID_ARG;
+  if (ldc < N) return FP8_ERR_INVALID_ARG;
+  const int64_t es = out_dt == FP8_OUT_F32 ? 4 : 2;
+  if (!aligned16(c) || (ldc * es) % 16 != 0) return FP8_ERR_MISALIGNED;
+  return FP8_OK;
+}
+
+int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaStream_t st) {
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  args.err = d->err;
+  CUtensorMap tma, tmb;
+  if ((rc = encode_operand(&tma, a, args.K, args.M, 128)) != FP8_OK) return rc;
+  if ((rc = encode_operand(&tmb, b, args.K, args.N, fp8k::gemm_tile_n(mode))) != FP8_OK) return rc;
+  return to_status(fp8k::launch_gemm(mode, tma, tmb, args, d->sms, st));
+}
+
+int check_gemm_common(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
+                      int64_t kgran) {
+  if (a == nullptr || b == nullptr) return FP8_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+    return FP8_ERR_INVALID_ARG;
+  if (K % kgran != 0 || !aligned16(a) || !aligned16(b)) return FP8_ERR_MISALIGNED;
+  return FP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8_amax(const void *x, int in_dt, int64_t n, float *amax_out, fp8_stream_t stream) {
+  if (amax_out == nullptr || n < 0 || !valid_in(in_dt) || (n > 0 && x == nullptr))
+    return FP8_ERR_INVALID_ARG;
+  if (n > 0 && !aligned16(x)) return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_amax(x, in_dt, n, amax_out, d->sms, (cudaStream_t)stream));
+}
+
+int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, int fmt,
+                        const float *amax_in, const float *scale, float *scale_out, uint8_t *q,
+                        uint8_t *q_t, float *amax_out, fp8_stream_t stream) {
+  if (x == nullptr || q == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (amax_in == nullptr && scale == nullptr) return FP8_ERR_INVALID_ARG;
+  if (rows < 1 || cols < 1 || rows >= kMaxDim || cols >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (cols % 8 != 0 || !aligned16(x) || !aligned16(q) || (q_t != nullptr && !aligned16(q_t)))
+    return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_quant_tensor(x, in_dt, rows, cols, fmt, amax_in, scale,
+                                             scale_out, q, q_t, amax_out, d->sms,
+                                             (cudaStream_t)stream));
+}
+
+int fp8_quantize_token_group(const void *x, int in_dt, int64_t M, int64_t K, int fmt, int sfmt,
+                             uint8_t *q, void *scales, fp8_stream_t stream) {
+  if (x == nullptr || q == nullptr || scales == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
+  if (M < 1 || K < 1 || M >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || !aligned16(x) || !aligned16(q)) return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_quant_group(x, in_dt, M, K, fmt, sfmt, q, scales, d->sms,
+                                            (cudaStream_t)stream));
+}
+
+int fp8_quantize_block(const void *w, int in_dt, int64_t N, int64_t K, int fmt, int sfmt,
+                       uint8_t *q, void *scales, fp8_stream_t stream) {
+  if (w == nullptr || q == nullptr || scales == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || N >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if ((N + 127) / 128 > 65535) return FP8_ERR_UNSUPPORTED;
+  if (K % 16 != 0 || !aligned16(w) || !aligned16(q)) return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(
+      fp8k::launch_quant_block(w, in_dt, N, K, fmt, sfmt, q, scales, (cudaStream_t)stream));
+}
+
+int fp8_quantize_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt, const float *amax,
+                    float *global_out, uint8_t *q, uint32_t *local, fp8_stream_t stream) {
+  if (x == nullptr || amax == nullptr || q == nullptr || local == nullptr || !valid_in(in_dt) ||
+      !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (R < 1 || K < 1 || R >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (K % 128 != 0 || !aligned16(x) || !aligned16(q) || !aligned16(local))
+    return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_quant_mx(x, in_dt, R, K, fmt, amax, global_out, q, local, d->sms,
+                                         (cudaStream_t)stream));
+}
+
+int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, const float *sa,
+                    const float *sb, int64_t M, int64_t N, int64_t K, int out_dt, void *c,
+                    int64_t ldc, int accumulate, fp8_stream_t stream) {
+  int rc = check_gemm_common(a, b, M, N, K, 16);
+  if (rc != FP8_OK) return rc;
+  if (sa == nullptr || sb == nullptr || !valid_fmt(fa) || !valid_fmt(fb)) return FP8_ERR_INVALID_ARG;
+  if ((rc = check_output(c, N, ldc, out_dt)) != FP8_OK) return rc;
+  if (accumulate != 0 && (accumulate != 1 || out_dt != FP8_OUT_F32)) return FP8_ERR_UNSUPPORTED;
+  GemmArgs args{};
+  args.M = M; args.N = N; args.K = K; args.fa = fa; args.fb = fb;
+  args.out_dt = out_dt; args.accumulate = accumulate; args.ldc = ldc; args.c = c;
+  args.sa = sa; args.sb = sb;
+  return run_gemm(fp8k::kScaleTensor, a, b, args, (cudaStream_t)stream);
+}
+
+int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb, int sfmt,
+                   int64_t M, int64_t N, int64_t K, void *c, int64_t ldc, fp8_stream_t stream) {
+  int rc = check_gemm_common(a, b, M, N, K, 128);
+  if (rc != FP8_OK) return rc;
+  if (sa == nullptr || sb == nullptr) return FP8_ERR_INVALID_ARG;
+  if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
+  if ((rc = check_output(c, N, ldc, FP8_OUT_BF16)) != FP8_OK) return rc;
+  GemmArgs args{};
+  args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
+  args.out_dt = FP8_OUT_BF16; args.ldc = ldc; args.c = c; args.sa = sa; args.sb = sb;
+  const int mode = sfmt == FP8_SCALE_F32 ? fp8k::kScaleGroupF32 : fp8k::kScaleGroupUe8m0;
+  return run_gemm(mode, a, b, args, (cudaStream_t)stream);
+}
+
+int fp8_gemm_mx(const uint8_t *a, const uint32_t *la, const float *ga, const uint8_t *b,
+                const uint32_t *lb, const float *gb, int64_t M, int64_t N, int64_t K, int out_dt,
+                void *c, int64_t ldc, fp8_stream_t stream) {
+  int rc = check_gemm_common(a, b, M, N, K, 128);
+  if (rc != FP8_OK) return rc;
+  if (la == nullptr || lb == nullptr || ga == nullptr || gb == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(la) || !aligned16(lb)) return FP8_ERR_MISALIGNED;
+  if ((rc = check_output(c, N, ldc, out_dt)) != FP8_OK) return rc;
+  GemmArgs args{};
+  args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
+  args.out_dt = out_dt; args.ldc = ldc; args.c = c; args.sa = la; args.sb = lb;
+  args.ga = ga; args.gb = gb;
+  return run_gemm(fp8k::kScaleMx, a, b, args, (cudaStream_t)stream);
+}
+
+int fp8_delayed_state_update(float *hist, float *scale, const float *amax_cur, int64_t L,
+                             int fmt, fp8_stream_t stream) {
+  if (hist == nullptr || scale == nullptr || amax_cur == nullptr || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (L < 1 || L > 32768) return FP8_ERR_INVALID_ARG;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_delayed_update(hist, scale, amax_cur, L, fmt, (cudaStream_t)stream));
+}
+
+int fp8_swiglu_forward(const void *h, const void *u, void *a, int64_t n, fp8_stream_t stream) {
+  if (h == nullptr || u == nullptr || a == nullptr || n < 0) return FP8_ERR_INVALID_ARG;
+  if (n % 8 != 0 || !aligned16(h) || !aligned16(u) || !aligned16(a)) return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  if (n == 0) return FP8_OK;
+  return to_status(fp8k::launch_swiglu_fwd(h, u, a, n, d->sms, (cudaStream_t)stream));
+}
+
+int fp8_swiglu_backward(const void *da, const void *h, const void *u, void *dh, void *du,
+                        int64_t n, fp8_stream_t stream) {
+  if (da == nullptr || h == nullptr || u == nullptr || dh == nullptr || du == nullptr || n < 0)
+    return FP8_ERR_INVALID_ARG;
+  if (n % 8 != 0 || !aligned16(da) || !aligned16(h) || !aligned16(u) || !aligned16(dh) ||
+      !aligned16(du))
+    return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  if (n == 0) return FP8_OK;
+  return to_status(fp8k::launch_swiglu_bwd(da, h, u, dh, du, n, d->sms, (cudaStream_t)stream));
+}
+
+int fp8_adamw_step(float *p, const float *g, float *m, float *v, void *p_bf16, int64_t n,
+                   int64_t step, float lr, float beta1, float beta2, float eps,
+                   float weight_decay, fp8_stream_t stream) {
+  if (p == nullptr || g == nullptr || m == nullptr || v == nullptr || n < 0 || step < 1)
+    return FP8_ERR_INVALID_ARG;
+  if (n % 4 != 0 || !aligned16(p) || !aligned16(g) || !aligned16(m) || !aligned16(v) ||
+      (p_bf16 != nullptr && (reinterpret_cast<uintptr_t>(p_bf16) & 7u) != 0))
+    return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  if (n == 0) return FP8_OK;
+  return to_status(fp8k::launch_adamw(p, g, m, v, p_bf16, n, step, lr, beta1, beta2, eps,
+                                      weight_decay, d->sms, (cudaStream_t)stream));
+}
+
+const char *fp8_status_string(int status) {
+  switch (status) {
+    case FP8_OK: return "ok";
+    case FP8_ERR_INVALID_ARG: return "invalid argument";
+    case FP8_ERR_MISALIGNED: return "misaligned pointer, stride or K granularity";
+    case FP8_ERR_UNSUPPORTED: return "unsupported format combination or shape";
+    case FP8_ERR_CUDA: return "CUDA runtime error";
+    case FP8_ERR_TIMEOUT: return "device-side wait timed out";
+    case FP8_ERR_NO_DEVICE: return "no sm_103 device is current";
+    default: return "unknown status";
+  }
+}
+
+int fp8_get_last_device_error(int *where_out, fp8_stream_t stream) {
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FP8_ERR_CUDA;
+  uint32_t h[2] = {0, 0};
+  if (cudaMemcpy(h, d->err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FP8_ERR_CUDA;
+  if (h[0] != 0) {
+    const uint32_t z[2] = {0, 0};
+    if (cudaMemcpy(d->err, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FP8_ERR_CUDA;
+  }
+  if (where_out != nullptr) *where_out = (int)h[1];
+  return -(int)h[0];
+}
+
+const char *fp8_version(void) { return "fp8gemm 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,301 @@
+// Shared device helpers for the sm_103a kernels: inline-PTX wrappers for
+// mbarriers, TMA (cp.async.bulk.tensor), tcgen05 (TMEM alloc, MMA, commit,
+// ld/st, cp) and FP8 conversion, plus the bounded-wait policy.
+//
+// Every spin on an mbarrier is bounded by %globaltimer: after kWaitLimitNs the
+// waiter records FP8_ERR_TIMEOUT in the library's device error word, raises a
+// CTA-wide abort flag in shared memory (so the other roles stop waiting too)
+// and returns false; the kernel then runs its normal teardown (TMEM dealloc)
+// and exits.  Nothing here traps.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8k {
+
+constexpr float kE4M3Max = 448.0f;
+constexpr float kE5M2Max = 57344.0f;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+constexpr uint32_t kErrTimeout = 5;               // stored as -FP8_ERR_TIMEOUT
+
+__device__ __forceinline__ float fmt_max(int fmt) { return fmt == 0 ? kE4M3Max : kE5M2Max; }
+
+// ------------------------------------------------------------ error word --
+struct DevErr {
+  uint32_t *word;  // [0] = first error code (positive), [1] = where
+};
+
+__device__ __forceinline__ void record_error(DevErr e, uint32_t code, uint32_t where) {
+  if (e.word != nullptr && atomicCAS(e.word, 0u, code) == 0u) e.word[1] = where;
+}
+
+// ----------------------------------------------------------------- misc --
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// -------------------------------------------------------------- mbarrier --
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with parity `parity` to complete.
+// Returns false (after recording the timeout and raising *abort) when the
+// limit expires, or when another role has already raised *abort.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          DevErr err, uint32_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0u) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        record_error(err, kErrTimeout, where);
+        return false;
+      }
+    }
+  }
+}
+
+// -------------------------------------------------------------------- TMA --
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                            int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// --------------------------------------------------------------- tcgen05 --
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// with 128-byte swizzling: rows of 128 bytes, 8-row atoms of 1024 bytes.
+// Fields: start address >> 4 (bits 0-13), leading byte offset >> 4 (16-29,
+// unused for swizzled K-major, set to 1), stride byte offset >> 4 (32-45:
+// 1024 bytes between 8-row atoms), descriptor version 1 (bits 46-47),
+// base offset 0 (tile base 1024-aligned), layout SWIZZLE_128B = 2 (61-63).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
+  return (uint64_t)((smem_addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Descriptor of an unswizzled K-major source for tcgen05.cp: 8-row x 16-byte
+// core matrices stored contiguously (row stride 16 bytes, 128 bytes apart).
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t smem_addr) {
+  return (uint64_t)((smem_addr >> 4) & 0x3FFFu) | ((uint64_t)(128 >> 4) << 16) |
+         ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor, kind::f8f6f4 (dense): D = f32 (bits 4-5 = 1),
+// A/B formats at bits 7-9 / 10-12 (E4M3 = 0, E5M2 = 1), both K-major,
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t m, uint32_t n, uint32_t fa,
+                                                    uint32_t fb) {
+  return (1u << 4) | (fa << 7) | (fb << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: B scale-factor
+// id at bits 4-5, formats at 7-9 / 10-12, N >> 3 at 17-22, scale type UE8M0
+// (bit 23 = 1), M >> 4 at 24-28, A scale-factor id at bits 29-30.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t m, uint32_t n, uint32_t fa,
+                                                      uint32_t fb, uint32_t sfa_id,
+                                                      uint32_t sfb_id) {
+  return (sfb_id << 4) | (fa << 7) | (fb << 10) | ((n >> 3) << 17) | (1u << 23) |
+         ((m >> 4) << 24) | (sfa_id << 29);
+}
+
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa_tmem,
+                                             uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` when every tcgen05 op this thread issued so far completes.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// smem (32 rows x 16 bytes) -> TMEM 32 lanes x 4 columns, replicated into all
+// four 32-lane sub-partitions.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+#define FP8K_TMEM_LD_X32(taddr, r)                                                            \
+  asm volatile(                                                                               \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"       \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),   \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),            \
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),         \
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),         \
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),         \
+        "=r"(r[31])                                                                           \
+      : "r"(taddr))
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------ conversion --
+// Two fp32 -> two FP8 codes, round to nearest even, saturating to +-MAX.
+// PTX places the first source operand in the UPPER byte, so `hi` is the
+// element at the higher address.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint16_t cvt_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint16_t cvt_fp8x2(int fmt, float lo, float hi) {
+  return fmt == 0 ? cvt_e4m3x2(lo, hi) : cvt_e5m2x2(lo, hi);
+}
+
+// Quantize one value: fl32(x / s), clipped to +-MAX (the cast then rounds).
+__device__ __forceinline__ float q_prep(float x, float s, float mx) {
+  float y = __fdiv_rn(x, s);
+  return fminf(fmaxf(y, -mx), mx);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// |x| as an order-preserving uint32 key (non-negative floats order like uints).
+__device__ __forceinline__ uint32_t abs_key(float x) { return __float_as_uint(x) & 0x7FFFFFFFu; }
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// fp32 scale from an amax: fl32(amax / MAX), or 1.0 for amax == 0.
+__device__ __forceinline__ float scale_from_amax(float amax, float mx) {
+  return amax > 0.0f ? __fdiv_rn(amax, mx) : 1.0f;
+}
+
+// Exact ceil(log2(s)) for finite s > 0 (normal or subnormal fp32).
+__device__ __forceinline__ int ceil_log2_pos(float s) {
+  const uint32_t b = __float_as_uint(s);
+  const int ef = (int)(b >> 23);
+  const uint32_t man = b & 0x7FFFFFu;
+  if (ef != 0) return (ef - 127) + (man != 0u ? 1 : 0);
+  // subnormal: s = man * 2^-149; ceil(log2) = floor(log2(man)) - 149 (+1 unless pow2)
+  const int fl = 31 - __clz((int)man);
+  return fl - 149 + ((man & (man - 1u)) != 0u ? 1 : 0);
+}
+
+// 2^e as fp32 for e in [-149, 127].
+__device__ __forceinline__ float exp2_int(int e) {
+  if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
+  return __uint_as_float(1u << (e + 149));
+}
+
+}  // namespace fp8k

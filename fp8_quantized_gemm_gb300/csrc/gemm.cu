@@ -1,0 +1,384 @@
+// Scaled-FP8 GEMM kernels on the 5th-generation tensor cores (tcgen05).
+//
+// One CTA computes one 128 x BN output tile, K-major operands for both A
+// ([M, K]) and B ([N, K]), 128-byte K slices:
+//
+//   warp 0        TMA producer: A and B tiles (128-byte swizzle) into a ring
+//                 of shared-memory stages; for the block-scaled modes also
+//                 the scale-factor words of the stage.
+//   warp 1        allocates TMEM; one elected thread issues tcgen05.mma
+//                 (4 x K=32 per stage) and tcgen05.commit's each stage back
+//                 to the producer.
+//   warps 2..     epilogue: tcgen05.ld the FP32 accumulator, apply the
+//                 scales, convert, store.
+//
+// Scale placement (the four modes of kernels.h):
+//   per tensor   (Flax guide 2.2)  alpha = sa * sb once in the epilogue.
+//   two level    (MOSS blog, 4)    E8M0 local factors as block scale factors
+//                                  of kind::mxf8f6f4 (one per 1x32 K block,
+//                                  scale_vec::1X), FP32 S_a * S_b in the
+//                                  epilogue.
+//   group UE8M0  (Transformers 七) the per-128 power-of-two scales, replicated
+//                                  over the four 1x32 blocks, as block scale
+//                                  factors: no promotion at all.
+//   group FP32   (Transformers 一) every 128-wide K slice is contracted into
+//                                  its own TMEM buffer (4 buffers in a ring);
+//                                  the epilogue warps promote
+//                                  acc += sa[m,g] * sb[n/128,g] * partial
+//                                  while the tensor cores run the next slice.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8k {
+
+constexpr uint32_t pow2_cols(uint32_t c) {
+  uint32_t p = 32;
+  while (p < c) p <<= 1;
+  return p;
+}
+
+template <int MODE, int BN, int STAGES>
+struct Cfg {
+  static constexpr int BM = 128, BK = 128;
+  static constexpr bool kBlockScaled = (MODE == kScaleMx || MODE == kScaleGroupUe8m0);
+  static constexpr bool kPromote = (MODE == kScaleGroupF32);
+  static constexpr int kEpiWarps = kPromote ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr uint32_t kABytes = BM * BK, kBBytes = BN * BK;
+  static constexpr uint32_t kSfaBytes = kBlockScaled ? BM * 4 : 0;
+  static constexpr uint32_t kSfbBytes = kBlockScaled ? BN * 4 : 0;
+  static constexpr uint32_t kTileBytes = STAGES * (kABytes + kBBytes);
+  static constexpr uint32_t kSfBytes = STAGES * (kSfaBytes + kSfbBytes);
+  static constexpr int kAccBufs = kPromote ? 4 : 1;
+  static constexpr uint32_t kAccCols = kAccBufs * BN;
+  static constexpr uint32_t kSfColsPerStage = kBlockScaled ? 4 + BN / 32 : 0;
+  static constexpr uint32_t kTmemCols = pow2_cols(kAccCols + STAGES * kSfColsPerStage);
+  static constexpr int kNumBars = 2 * STAGES + 2 * kAccBufs + 1;  // + drain
+  static constexpr uint32_t kSmem = 1024 + kTileBytes + kSfBytes + 8 * kNumBars + 16;
+  static_assert(kTmemCols <= 512, "TMEM budget");
+  static_assert(kSmem <= 227 * 1024, "shared-memory budget");
+  static_assert(BN % 32 == 0 && BN <= 256, "tile N");
+};
+
+// Store 32 consecutive results of one output row (already scaled).
+__device__ __forceinline__ void store_row32(const GemmArgs &a, int64_t row, int64_t col0,
+                                            const float (&v)[32]) {
+  if (row >= a.M || col0 >= a.N) return;
+  const bool full = (col0 + 32 <= a.N);
+  if (a.out_dt == 1) {
+    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.c) + row * a.ldc + col0;
+    if (full) {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+      }
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else {
+      for (int i = 0; i < 32 && col0 + i < a.N; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+    }
+  } else {
+    float *dst = static_cast<float *>(a.c) + row * a.ldc + col0;
+    if (full) {
+      float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float4 o = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        if (a.accumulate) {
+          const float4 p = d4[i];
+          o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
+        }
+        d4[i] = o;
+      }
+    } else {
+      for (int i = 0; i < 32 && col0 + i < a.N; ++i) dst[i] = a.accumulate ? dst[i] + v[i] : v[i];
+    }
+  }
+}
+
+// Short non-abortable wait used only on the abort path (drains async work
+// before the CTA exits).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > 20000000ull) break;  // 20 ms
+  }
+}
+
+template <int MODE, int BN, int STAGES>
+__global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
+                const GemmArgs args) {
+  using C = Cfg<MODE, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *tiles = smem;
+  uint8_t *sf = smem + C::kTileBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sf + C::kSfBytes);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const DevErr err{args.err};
+
+  auto sA = [&](int s) { return smem_u32(tiles + s * (C::kABytes + C::kBBytes)); };
+  auto sB = [&](int s) { return smem_u32(tiles + s * (C::kABytes + C::kBBytes) + C::kABytes); };
+  auto sSfa = [&](int s) { return sf + s * (C::kSfaBytes + C::kSfbBytes); };
+  auto sSfb = [&](int s) { return sf + s * (C::kSfaBytes + C::kSfbBytes) + C::kSfaBytes; };
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
+  auto accf_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + b]); };
+  auto acce_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + C::kAccBufs + b]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 2 * C::kAccBufs]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), C::kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma);
+    tma_prefetch_desc(&tmb);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int64_t m0 = (int64_t)blockIdx.y * C::BM;
+  const int64_t n0 = (int64_t)blockIdx.x * BN;
+  const int KB = (int)((args.K + C::BK - 1) / C::BK);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t round = (uint32_t)(kb / STAGES);
+      if (!mbar_wait(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) break;
+      uint32_t tx = C::kABytes + C::kBBytes;
+      if constexpr (MODE == kScaleGroupUe8m0) {
+        // per-128 UE8M0 byte -> word with the byte in all four 1x32 slots;
+        // word for row 32c + l of a 128-row chunk sits at index 4l + c
+        const uint8_t *sa8 = static_cast<const uint8_t *>(args.sa);
+        const uint8_t *sb8 = static_cast<const uint8_t *>(args.sb);
+        const int64_t G = args.K / 128;
+        uint32_t *wa = reinterpret_cast<uint32_t *>(sSfa(s));
+        uint32_t *wb = reinterpret_cast<uint32_t *>(sSfb(s));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int64_t m = m0 + 32 * c + lane;
+          const uint32_t b = m < args.M ? sa8[(int64_t)kb * args.M + m] : 127u;
+          wa[4 * lane + c] = b * 0x01010101u;
+        }
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          const int64_t n = n0 + 32 * c + lane;
+          const uint32_t b = n < args.N ? sb8[(n >> 7) * G + kb] : 127u;
+          wb[(c >> 2) * 128 + 4 * lane + (c & 3)] = b * 0x01010101u;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (elect_one()) {
+        uint32_t sfb_bytes = 0;
+        if constexpr (MODE == kScaleMx) {
+          const int64_t npad = (args.N + 127) / 128 * 128;
+          const int64_t rows = (npad - n0) < BN ? (npad - n0) : BN;
+          sfb_bytes = (uint32_t)rows * 4u;
+          tx += C::kSfaBytes + sfb_bytes;
+        }
+        mbar_arrive_expect_tx(full_bar(s), tx);
+        tma_load_2d(sA(s), &tma, full_bar(s), kb * C::BK, (int32_t)m0);
+        tma_load_2d(sB(s), &tmb, full_bar(s), kb * C::BK, (int32_t)n0);
+        if constexpr (MODE == kScaleMx) {
+          const int64_t mpad = (args.M + 127) / 128 * 128;
+          const int64_t npad = (args.N + 127) / 128 * 128;
+          const uint32_t *la = static_cast<const uint32_t *>(args.sa) + (int64_t)kb * mpad + m0;
+          const uint32_t *lb = static_cast<const uint32_t *>(args.sb) + (int64_t)kb * npad + n0;
+          bulk_load(smem_u32(sSfa(s)), la, C::kSfaBytes, full_bar(s));
+          bulk_load(smem_u32(sSfb(s)), lb, sfb_bytes, full_bar(s));
+        }
+      }
+      __syncwarp();
+      ++issued;
+    }
+    if (*abort_flag) {
+      // let the copies already in flight land before the CTA can exit
+      if (lane == 0) {
+        const int first = issued > STAGES ? issued - STAGES : 0;
+        for (int i = first; i < issued; ++i)
+          drain_wait(full_bar(i % STAGES), (uint32_t)(i / STAGES) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (elect_one()) {
+      bool ok = true;
+      for (int kb = 0; kb < KB && ok; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t round = (uint32_t)(kb / STAGES);
+        if (!mbar_wait(full_bar(s), round & 1u, abort_flag, err, 2)) {
+          ok = false;
+          break;
+        }
+        uint32_t d = tmem;
+        if constexpr (C::kPromote) {
+          const int buf = kb & 3;
+          const uint32_t use = (uint32_t)(kb >> 2);
+          if (!mbar_wait(acce_bar(buf), (use & 1u) ^ 1u, abort_flag, err, 2)) {
+            ok = false;
+            break;
+          }
+          d = tmem + (uint32_t)(buf * BN);
+        }
+        tc_fence_after();
+        const uint64_t adesc = sdesc_sw128(sA(s));
+        const uint64_t bdesc = sdesc_sw128(sB(s));
+        if constexpr (C::kBlockScaled) {
+          const uint32_t sfa_col = C::kAccCols + (uint32_t)s * C::kSfColsPerStage;
+          const uint32_t sfb_col = sfa_col + 4;
+          tmem_cp_32x128b_warpx4(tmem + sfa_col, sdesc_plain(smem_u32(sSfa(s))));
+#pragma unroll
+          for (int j = 0; j < BN / 128; ++j)
+            tmem_cp_32x128b_warpx4(tmem + sfb_col + 4 * j, sdesc_plain(smem_u32(sSfb(s)) + 512 * j));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t idesc = idesc_mxf8f6f4(128, BN, args.fa, args.fb, k, k);
+            mma_mxf8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + sfa_col,
+                         tmem + sfb_col, (kb | k) != 0 ? 1u : 0u);
+          }
+        } else {
+          const uint32_t idesc = idesc_f8f6f4(128, BN, args.fa, args.fb);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t acc = C::kPromote ? (k != 0) : ((kb | k) != 0);
+            mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc ? 1u : 0u);
+          }
+        }
+        mma_commit(empty_bar(s));
+        if constexpr (C::kPromote) mma_commit(accf_bar(kb & 3));
+      }
+      if (ok) {
+        if constexpr (!C::kPromote) mma_commit(accf_bar(0));
+      } else {
+        mma_commit(drain_bar);
+        drain_wait(drain_bar, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t q = warp & 3u;
+    const int64_t row = m0 + 32 * q + lane;
+    const uint32_t lane_base = tmem + ((32u * q) << 16);
+    if constexpr (!C::kPromote) {
+      if (mbar_wait(accf_bar(0), 0, abort_flag, err, 3)) {
+        tc_fence_after();
+        float alpha = 1.0f;
+        if constexpr (MODE == kScaleTensor)
+          alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
+        if constexpr (MODE == kScaleMx) alpha = *args.ga * *args.gb;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          FP8K_TMEM_LD_X32(lane_base + (uint32_t)c, r);
+          tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
+          store_row32(args, row, n0 + c, v);
+        }
+      }
+    } else {
+      const int h = (int)(warp - 2) >> 2;  // column half of the 128-wide tile
+      const float *sa = static_cast<const float *>(args.sa);
+      const float *sb = static_cast<const float *>(args.sb);
+      const int64_t G = args.K / 128;
+      const float *sb_row = sb + (n0 >> 7) * G;
+      float acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+      float sa_next = row < args.M ? __ldg(sa + row) : 0.0f;
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int buf = kb & 3;
+        const float s_cur = sa_next * __ldg(sb_row + kb);
+        if (kb + 1 < KB) sa_next = row < args.M ? __ldg(sa + (int64_t)(kb + 1) * args.M + row) : 0.0f;
+        if (!mbar_wait(accf_bar(buf), (uint32_t)(kb >> 2) & 1u, abort_flag, err, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        const uint32_t col = (uint32_t)(buf * BN + h * 64);
+        FP8K_TMEM_LD_X32(lane_base + col, r0);
+        FP8K_TMEM_LD_X32(lane_base + col + 32, r1);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(buf));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          acc[i] = fmaf(s_cur, __uint_as_float(r0[i]), acc[i]);
+          acc[32 + i] = fmaf(s_cur, __uint_as_float(r1[i]), acc[32 + i]);
+        }
+      }
+      if (ok) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = acc[i];
+        store_row32(args, row, n0 + h * 64, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = acc[32 + i];
+        store_row32(args, row, n0 + h * 64 + 32, v);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int MODE, int BN, int STAGES>
+static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
+                       cudaStream_t st) {
+  using C = Cfg<MODE, BN, STAGES>;
+  auto kern = gemm_kernel<MODE, BN, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((args.N + BN - 1) / BN), (unsigned)((args.M + C::BM - 1) / C::BM));
+  kern<<<grid, C::kThreads, C::kSmem, st>>>(tma, tmb, args);
+  return cudaGetLastError();
+}
+
+int gemm_tile_n(int mode) { return mode == kScaleGroupF32 ? 128 : 256; }
+
+cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,
+                        const GemmArgs &args, int sms, cudaStream_t st) {
+  (void)sms;
+  switch (mode) {
+    case kScaleTensor: return run<kScaleTensor, 256, 4>(tma, tmb, args, st);
+    case kScaleMx: return run<kScaleMx, 256, 4>(tma, tmb, args, st);
+    case kScaleGroupUe8m0: return run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, st);
+    case kScaleGroupF32: return run<kScaleGroupF32, 128, 6>(tma, tmb, args, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fp8k

@@ -1,0 +1,53 @@
+// Host-side launch entry points of the device kernels (internal to the
+// library; the public C ABI is include/fp8gemm.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8k {
+
+cudaError_t launch_amax(const void *x, int in_dt, int64_t n, float *out, int sms,
+                        cudaStream_t st);
+cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, int fmt,
+                                const float *amax_in, const float *scale, float *scale_out,
+                                uint8_t *q, uint8_t *qt, float *amax_out, int sms,
+                                cudaStream_t st);
+cudaError_t launch_quant_group(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
+                               int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st);
+cudaError_t launch_quant_block(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
+                               int sfmt, uint8_t *q, void *scales, cudaStream_t st);
+cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
+                            const float *amax, float *global_out, uint8_t *q, uint32_t *local,
+                            int sms, cudaStream_t st);
+cudaError_t launch_delayed_update(float *hist, float *scale, const float *amax_cur, int64_t L,
+                                  int fmt, cudaStream_t st);
+
+// GEMM family.  Scale modes of the epilogue / main loop:
+enum GemmScaleMode : int {
+  kScaleTensor = 0,      // per-tensor: alpha = sa[0] * sb[0] in the epilogue
+  kScaleMx = 1,          // block-scaled MMA, packed E8M0 words; alpha = ga[0] * gb[0]
+  kScaleGroupUe8m0 = 2,  // block-scaled MMA, per-128 UE8M0 bytes replicated in-kernel
+  kScaleGroupF32 = 3     // per-128 fp32 scales promoted on the CUDA cores
+};
+
+struct GemmArgs {
+  int64_t M, N, K;
+  int fa, fb;          // operand formats: 0 = E4M3, 1 = E5M2
+  int out_dt;          // 0 = f32, 1 = bf16
+  int accumulate;      // f32 output only
+  int64_t ldc;
+  void *c;
+  const void *sa, *sb;         // scale operands (meaning depends on the mode)
+  const float *ga, *gb;        // global factors (kScaleMx)
+  uint32_t *err;               // device error word
+};
+
+// Output-tile width (N) of each mode; the B tensor map's box uses it.
+int gemm_tile_n(int mode);
+
+cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,
+                        const GemmArgs &args, int sms, cudaStream_t st);
+
+}  // namespace fp8k

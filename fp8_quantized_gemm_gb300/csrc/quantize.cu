@@ -1,0 +1,543 @@
+// Amax and quantization kernels (HBM-bound, CUDA cores).
+//
+// Every kernel reads its input with 16-byte vector loads, reduces |x| with
+// warp shuffles on order-preserving uint32 keys (exact: max is order
+// independent), and casts on store with cvt.rn.satfinite after the
+// fl32(x / s) division and the +-MAX clip of the Flax guide's `quantize`
+// (section 2.2).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8k {
+
+// ---------------------------------------------------------------- loads --
+// Eight consecutive input elements as fp32 (bf16: one 16-byte load; f32: two).
+template <typename T>
+struct Vec8;
+
+template <>
+struct Vec8<__nv_bfloat16> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  static __device__ __forceinline__ void load_stream(const __nv_bfloat16 *p, float (&v)[8]) {
+    const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+};
+
+template <>
+struct Vec8<float> {
+  static __device__ __forceinline__ void load(const float *p, float (&v)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  static __device__ __forceinline__ void load_stream(const float *p, float (&v)[8]) {
+    const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ float load1(const T *p);
+template <>
+__device__ __forceinline__ float load1<__nv_bfloat16>(const __nv_bfloat16 *p) {
+  return __bfloat162float(*p);
+}
+template <>
+__device__ __forceinline__ float load1<float>(const float *p) { return *p; }
+
+// 8 values -> 8 codes packed little-endian into a uint2.
+__device__ __forceinline__ uint2 pack8(int fmt, const float (&y)[8]) {
+  const uint32_t c0 = cvt_fp8x2(fmt, y[0], y[1]), c1 = cvt_fp8x2(fmt, y[2], y[3]);
+  const uint32_t c2 = cvt_fp8x2(fmt, y[4], y[5]), c3 = cvt_fp8x2(fmt, y[6], y[7]);
+  return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+}
+
+// Block-wide max of a uint32 key, then one atomicMax per block.
+__device__ __forceinline__ void block_max_to(uint32_t key, uint32_t *dst) {
+  __shared__ uint32_t red[32];
+  key = warp_max_u32(key);
+  const int w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  if (lane_id() == 0) red[w] = key;
+  __syncthreads();
+  if (w == 0) {
+    uint32_t k = lane_id() < (uint32_t)nw ? red[lane_id()] : 0u;
+    k = warp_max_u32(k);
+    if (lane_id() == 0 && k != 0u) atomicMax(dst, k);
+  }
+}
+
+// ------------------------------------------------------------------ amax --
+template <typename T>
+__global__ void __launch_bounds__(512) amax_kernel(const T *__restrict__ x, int64_t n,
+                                                   uint32_t *__restrict__ out) {
+  uint32_t key = 0;
+  const int64_t nvec = n / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    float v[8];
+    Vec8<T>::load(x + i * 8, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
+  }
+  for (int64_t i = nvec * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    key = max(key, abs_key(load1(x + i)));
+  block_max_to(key, out);
+}
+
+// ------------------------------------------------------- quantize tensor --
+__device__ __forceinline__ float resolve_scale(const float *amax_in, const float *scale_in,
+                                               float mx) {
+  return amax_in != nullptr ? scale_from_amax(*amax_in, mx) : *scale_in;
+}
+
+// Row-major output only: grid-stride over 8-element vectors.
+template <typename T>
+__global__ void __launch_bounds__(512)
+    quant_tensor_kernel(const T *__restrict__ x, int64_t n, int fmt, const float *amax_in,
+                        const float *scale_in, float *scale_out, uint8_t *__restrict__ q,
+                        uint32_t *amax_out) {
+  const float mx = fmt_max(fmt);
+  const float s = resolve_scale(amax_in, scale_in, mx);
+  if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+  uint32_t key = 0;
+  const int64_t nvec = n / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    float v[8], y[8];
+    Vec8<T>::load_stream(x + i * 8, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      key = max(key, abs_key(v[j]));
+      y[j] = q_prep(v[j], s, mx);
+    }
+    reinterpret_cast<uint2 *>(q)[i] = pack8(fmt, y);
+  }
+  if (amax_out != nullptr) block_max_to(key, amax_out);
+}
+
+// Row-major output plus the transposed copy q_t [cols, rows], in 128 x 128
+// tiles staged through shared memory.  The 8-byte chunk c of tile row r is
+// stored at chunk c ^ (r / 8), so that both the row-wise writes and the 8x8
+// byte-block reads of the transpose are free of bank conflicts.
+constexpr int kTT = 128;
+constexpr int kTPitch = kTT;
+__device__ __forceinline__ int tchunk(int r, int c8) { return ((c8 ^ (r >> 3)) & 15) * 8; }
+
+__device__ __forceinline__ uint64_t transpose8x8(const uint64_t (&r)[8], int j) {
+  // byte j of every row r[i] -> byte i of the result
+  uint64_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out |= ((r[i] >> (8 * j)) & 0xFFull) << (8 * i);
+  return out;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    quant_tensor_t_kernel(const T *__restrict__ x, int64_t rows, int64_t cols, int fmt,
+                          const float *amax_in, const float *scale_in, float *scale_out,
+                          uint8_t *__restrict__ q, uint8_t *__restrict__ qt,
+                          uint32_t *amax_out) {
+  __shared__ __align__(16) uint8_t tile[kTT * kTPitch];
+  const float mx = fmt_max(fmt);
+  const float s = resolve_scale(amax_in, scale_in, mx);
+  if (scale_out != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    *scale_out = s;
+  const int64_t r0 = (int64_t)blockIdx.y * kTT, c0 = (int64_t)blockIdx.x * kTT;
+  const int t = threadIdx.x;
+  uint32_t key = 0;
+  // phase 1: 16 vectors of 8 per tile row; 256 threads cover 16 rows per pass
+#pragma unroll 2
+  for (int pass = 0; pass < kTT / 16; ++pass) {
+    const int lr = pass * 16 + (t >> 4), lc = (t & 15) * 8;
+    const int64_t r = r0 + lr, c = c0 + lc;
+    uint2 packed = make_uint2(0u, 0u);
+    if (r < rows && c < cols) {
+      float v[8], y[8];
+      Vec8<T>::load_stream(x + r * cols + c, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        key = max(key, abs_key(v[j]));
+        y[j] = q_prep(v[j], s, mx);
+      }
+      packed = pack8(fmt, y);
+      *reinterpret_cast<uint2 *>(q + r * cols + c) = packed;
+    }
+    *reinterpret_cast<uint2 *>(&tile[lr * kTPitch + tchunk(lr, lc >> 3)]) = packed;
+  }
+  __syncthreads();
+  // phase 2: thread -> one 8x8 byte block; 16 threads per q_t row segment
+  const int rb = t & 15, cb = t >> 4;
+  uint64_t rr[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    rr[i] = *reinterpret_cast<const uint64_t *>(&tile[(rb * 8 + i) * kTPitch + tchunk(rb * 8 + i, cb)]);
+  const int64_t orow0 = c0 + cb * 8;  // q_t row = input column
+  const int64_t ocol = r0 + rb * 8;   // q_t column = input row
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t orow = orow0 + j;
+    if (orow >= cols) break;
+    const uint64_t w = transpose8x8(rr, j);
+    uint8_t *dst = qt + orow * rows + ocol;
+    if (ocol + 8 <= rows && (rows & 7) == 0) {
+      *reinterpret_cast<uint64_t *>(dst) = w;
+    } else {
+      for (int i = 0; i < 8 && ocol + i < rows; ++i) dst[i] = (uint8_t)(w >> (8 * i));
+    }
+  }
+  if (amax_out != nullptr) block_max_to(key, amax_out);
+}
+
+// --------------------------------------------------- token group (1x128) --
+// One warp per (row, pair of 128-wide K groups); lane l holds elements
+// [8l, 8l+8) of the 256-wide window, so lanes 0-15 form group 2p and lanes
+// 16-31 group 2p+1.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    quant_group_kernel(const T *__restrict__ x, int64_t M, int64_t K, int fmt, int sfmt,
+                       uint8_t *__restrict__ q, void *scales) {
+  const float mx = fmt_max(fmt);
+  const int64_t G = (K + 127) / 128, pairs = (G + 1) / 2;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t l = lane_id();
+  for (int64_t task = warp; task < M * pairs; task += nwarps) {
+    const int64_t m = task / pairs, p = task % pairs;
+    const int64_t k = p * 256 + l * 8;
+    float v[8];
+    const bool valid = k < K;
+    if (valid) {
+      Vec8<T>::load_stream(x + m * K + k, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+    }
+    uint32_t key = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+    const float amax = __uint_as_float(key);
+    float s = scale_from_amax(amax, mx);
+    uint8_t e8 = 127;
+    if (sfmt == 1 && amax > 0.0f) {
+      const int e = min(max(ceil_log2_pos(s), -127), 127);
+      s = exp2_int(e);
+      e8 = (uint8_t)(e + 127);
+    } else if (sfmt == 1) {
+      s = 1.0f;
+    }
+    const int64_t g = p * 2 + (l >> 4);
+    if ((l & 15) == 0 && g < G) {
+      if (sfmt == 0)
+        reinterpret_cast<float *>(scales)[g * M + m] = s;
+      else
+        reinterpret_cast<uint8_t *>(scales)[g * M + m] = e8;
+    }
+    if (valid) {
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) y[j] = q_prep(v[j], s, mx);
+      *reinterpret_cast<uint2 *>(q + m * K + k) = pack8(fmt, y);
+    }
+  }
+}
+
+// --------------------------------------------------- weight block 128x128 --
+// One CTA per block: thread t covers row t/2, columns (t%2)*64 .. +64.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    quant_block_kernel(const T *__restrict__ w, int64_t N, int64_t K, int fmt, int sfmt,
+                       uint8_t *__restrict__ q, void *scales) {
+  __shared__ uint32_t red[8];
+  __shared__ uint32_t amax_key;
+  const float mx = fmt_max(fmt);
+  const int64_t bn = blockIdx.y, bk = blockIdx.x, KB = (K + 127) / 128;
+  const int t = threadIdx.x;
+  const int64_t r = bn * 128 + (t >> 1);
+  const int64_t cbase = bk * 128 + (t & 1) * 64;
+  float v[64];
+  uint32_t key = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t c = cbase + i * 8;
+    float tmp[8];
+    if (r < N && c < K) {
+      Vec8<T>::load(w + r * K + c, tmp);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tmp[j] = 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[i * 8 + j] = tmp[j];
+      key = max(key, abs_key(tmp[j]));
+    }
+  }
+  key = warp_max_u32(key);
+  if (lane_id() == 0) red[t >> 5] = key;
+  __syncthreads();
+  if (t < 32) {
+    uint32_t k2 = t < 8 ? red[t] : 0u;
+    k2 = warp_max_u32(k2);
+    if (t == 0) amax_key = k2;
+  }
+  __syncthreads();
+  const float amax = __uint_as_float(amax_key);
+  float s = scale_from_amax(amax, mx);
+  uint8_t e8 = 127;
+  if (sfmt == 1) {
+    if (amax > 0.0f) {
+      const int e = min(max(ceil_log2_pos(s), -127), 127);
+      s = exp2_int(e);
+      e8 = (uint8_t)(e + 127);
+    } else {
+      s = 1.0f;
+    }
+  }
+  if (t == 0) {
+    if (sfmt == 0)
+      reinterpret_cast<float *>(scales)[bn * KB + bk] = s;
+    else
+      reinterpret_cast<uint8_t *>(scales)[bn * KB + bk] = e8;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t c = cbase + i * 8;
+    if (r < N && c < K) {
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) y[j] = q_prep(v[i * 8 + j], s, mx);
+      *reinterpret_cast<uint2 *>(q + r * K + c) = pack8(fmt, y);
+    }
+  }
+}
+
+// ------------------------------------------------------ two-level (MOSS) --
+// One warp per (row, pair of 128-wide K slices); lane l holds elements
+// [8l, 8l+8): the 1x32 block of lane l is l/4 (four lanes per block).
+// Index of the packed local-factor word for (row r, slice g).
+__device__ __forceinline__ int64_t mx_word_index(int64_t r, int64_t g, int64_t rpad) {
+  return g * rpad + (r & ~(int64_t)127) + 4 * (r & 31) + ((r & 127) >> 5);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    quant_mx_kernel(const T *__restrict__ x, int64_t R, int64_t K, int fmt,
+                    const float *amax_in, float *global_out, uint8_t *__restrict__ q,
+                    uint32_t *__restrict__ local) {
+  const float mx = fmt_max(fmt);
+  const float S = scale_from_amax(*amax_in, mx);  // == max_i fl32(amax_i / MAX)
+  if (global_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *global_out = S;
+  const int64_t G = K / 128, pairs = (G + 1) / 2;
+  const int64_t rpad = (R + 127) / 128 * 128;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t l = lane_id();
+  for (int64_t task = warp; task < rpad * pairs; task += nwarps) {
+    const int64_t r = task / pairs, p = task % pairs;
+    const int64_t g = p * 2 + (l >> 4);
+    const int64_t k = p * 256 + l * 8;
+    if (r >= R) {  // padding rows: factor 1 (byte 127)
+      if ((l & 15) == 0 && g < G) local[mx_word_index(r, g, rpad)] = 0x7F7F7F7Fu;
+      continue;
+    }
+    const bool valid = k < K;
+    float v[8];
+    if (valid) {
+      Vec8<T>::load_stream(x + r * K + k, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+    }
+    uint32_t key = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
+    key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
+    key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
+    const float amax_i = __uint_as_float(key);
+    const float s_i = __fdiv_rn(amax_i, mx);     // step 1
+    int e = 0;
+    if (s_i > 0.0f) {
+      const float ratio = __fdiv_rn(s_i, S);     // step 3
+      e = ratio > 0.0f ? max(ceil_log2_pos(ratio), -127) : -127;
+    }
+    const float eff = S * exp2_int(e);           // step 4: S * r_i
+    if (valid) {
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) y[j] = q_prep(v[j], eff, mx);
+      *reinterpret_cast<uint2 *>(q + r * K + k) = pack8(fmt, y);
+    }
+    // gather the four block bytes of each 128-wide slice into one word
+    uint32_t b = (uint32_t)(e + 127) & 0xFFu;
+    const uint32_t b1 = __shfl_down_sync(0xffffffffu, b, 4);
+    const uint32_t b2 = __shfl_down_sync(0xffffffffu, b, 8);
+    const uint32_t b3 = __shfl_down_sync(0xffffffffu, b, 12);
+    if ((l & 15) == 0 && g < G) local[mx_word_index(r, g, rpad)] = b | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  }
+}
+
+// ------------------------------------------------- delayed-state update --
+// One CTA: roll the history by -1, write the new amax at index 0, then take
+// max(history) (NaN propagates, as a max over the array does) and update the
+// scale when it is positive and finite.
+__global__ void __launch_bounds__(1024)
+    delayed_update_kernel(float *hist, float *scale, const float *amax_cur, int64_t L, int fmt) {
+  extern __shared__ float old[];
+  __shared__ uint32_t red_key[32];
+  __shared__ int red_nan[32];
+  for (int64_t i = threadIdx.x; i < L; i += blockDim.x) old[i] = hist[i];
+  __syncthreads();
+  const float a = *amax_cur;
+  uint32_t key = 0;
+  int nan_seen = 0;
+  for (int64_t i = threadIdx.x; i < L; i += blockDim.x) {
+    const float v = (i == 0) ? a : old[(i + 1) % L];
+    hist[i] = v;
+    if (v != v) nan_seen = 1;
+    // keys of non-negative floats order like uints; +inf is the largest
+    else key = max(key, v > 0.0f ? __float_as_uint(v) : 0u);
+  }
+  key = warp_max_u32(key);
+  nan_seen = __any_sync(0xffffffffu, nan_seen);
+  if (lane_id() == 0) {
+    red_key[threadIdx.x >> 5] = key;
+    red_nan[threadIdx.x >> 5] = nan_seen;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int nw = (blockDim.x + 31) >> 5;
+    uint32_t k = threadIdx.x < (uint32_t)nw ? red_key[threadIdx.x] : 0u;
+    int nn = threadIdx.x < (uint32_t)nw ? red_nan[threadIdx.x] : 0;
+    k = warp_max_u32(k);
+    nn = __any_sync(0xffffffffu, nn);
+    if (threadIdx.x == 0) {
+      const float m = __uint_as_float(k);
+      if (!nn && m > 0.0f && m <= 3.402823466e38f) *scale = __fdiv_rn(m, fmt_max(fmt));
+    }
+  }
+}
+
+// ----------------------------------------------------------- launchers --
+static int grid_for(int64_t work, int threads, int per_sm_blocks, int sms) {
+  const int64_t need = (work + threads - 1) / threads;
+  const int64_t cap = (int64_t)sms * per_sm_blocks;
+  return (int)(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+cudaError_t launch_amax(const void *x, int in_dt, int64_t n, float *out, int sms,
+                        cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), st);
+  if (e != cudaSuccess || n == 0) return e;
+  const int threads = 512, blocks = grid_for((n + 7) / 8, threads, 4, sms);
+  if (in_dt == 0)
+    amax_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(x), n, reinterpret_cast<uint32_t *>(out));
+  else
+    amax_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float *>(x), n,
+                                                    reinterpret_cast<uint32_t *>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, int fmt,
+                                const float *amax_in, const float *scale, float *scale_out,
+                                uint8_t *q, uint8_t *qt, float *amax_out, int sms,
+                                cudaStream_t st) {
+  if (amax_out != nullptr) {
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  uint32_t *ao = reinterpret_cast<uint32_t *>(amax_out);
+  if (qt == nullptr) {
+    const int64_t n = rows * cols;
+    const int threads = 512, blocks = grid_for(n / 8, threads, 4, sms);
+    if (in_dt == 0)
+      quant_tensor_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
+          static_cast<const __nv_bfloat16 *>(x), n, fmt, amax_in, scale, scale_out, q, ao);
+    else
+      quant_tensor_kernel<float><<<blocks, threads, 0, st>>>(
+          static_cast<const float *>(x), n, fmt, amax_in, scale, scale_out, q, ao);
+  } else {
+    dim3 grid((unsigned)((cols + kTT - 1) / kTT), (unsigned)((rows + kTT - 1) / kTT));
+    if (in_dt == 0)
+      quant_tensor_t_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+          static_cast<const __nv_bfloat16 *>(x), rows, cols, fmt, amax_in, scale, scale_out,
+          q, qt, ao);
+    else
+      quant_tensor_t_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(x), rows,
+                                                          cols, fmt, amax_in, scale, scale_out,
+                                                          q, qt, ao);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_group(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
+                               int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st) {
+  const int64_t G = (K + 127) / 128, pairs = (G + 1) / 2;
+  const int threads = 256, blocks = grid_for(M * pairs * 32, threads, 8, sms);
+  if (in_dt == 0)
+    quant_group_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(x), M, K, fmt, sfmt, q, scales);
+  else
+    quant_group_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float *>(x), M, K,
+                                                          fmt, sfmt, q, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_block(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
+                               int sfmt, uint8_t *q, void *scales, cudaStream_t st) {
+  dim3 grid((unsigned)((K + 127) / 128), (unsigned)((N + 127) / 128));
+  if (in_dt == 0)
+    quant_block_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(w), N, K, fmt, sfmt, q, scales);
+  else
+    quant_block_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(w), N, K, fmt,
+                                                     sfmt, q, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
+                            const float *amax, float *global_out, uint8_t *q, uint32_t *local,
+                            int sms, cudaStream_t st) {
+  const int64_t G = K / 128, pairs = (G + 1) / 2, rpad = (R + 127) / 128 * 128;
+  const int threads = 256, blocks = grid_for(rpad * pairs * 32, threads, 8, sms);
+  if (in_dt == 0)
+    quant_mx_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(x), R, K, fmt, amax, global_out, q, local);
+  else
+    quant_mx_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float *>(x), R, K, fmt,
+                                                       amax, global_out, q, local);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_delayed_update(float *hist, float *scale, const float *amax_cur, int64_t L,
+                                  int fmt, cudaStream_t st) {
+  const size_t smem = (size_t)L * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(delayed_update_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  delayed_update_kernel<<<1, 1024, smem, st>>>(hist, scale, amax_cur, L, fmt);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8k

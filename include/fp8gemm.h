@@ -1,0 +1,247 @@
+/*
+ * fp8gemm.h -- C ABI of the scaled-FP8 GEMM library (libfp8gemm.so), sm_103a.
+ *
+ * The library quantizes operands to E4M3 / E5M2 and contracts them on the
+ * tcgen05 tensor cores with FP32 accumulation, applying the scales in one of
+ * four places: per tensor in the epilogue (current or delayed scaling), per
+ * K group in the main loop (1x128 x 128x128, FP32 or UE8M0 scales), or two
+ * level (E8M0 local factors inside block-scaled MMA, an FP32 global factor in
+ * the epilogue).
+ *
+ * Sources (web pages, by title and section):
+ *   [Flax]   "Flax FP8 量化实战指南" -- 1 (Q/DQ), 2.2 (current scaling,
+ *            quantize/dequantize), 2.3 (delayed scaling, amax history),
+ *            3.3 (E4M3 forward / E5M2 gradients), 5.1 (meta state).
+ *   [Nano]   "Nanochat的FP8训练模块" -- "核心原语" (_scaled_mm, TN layout),
+ *            "实现" (forward / backward GEMMs, E5M2 max 57344).
+ *   [HF]     "Transformers 中的细粒度 FP8 量化配置..." -- 一 (128x128 weight
+ *            blocks, 1x128 token groups, weight_scale_inv shape), 四
+ *            (scale_fmt float | ue8m0), 七 (UE8M0 rounded up, quantize with it).
+ *   [MOSS]   "MOSS: 高效、精确的 FP8 LLM 训练" -- 4 (two-level microscaling,
+ *            steps 1-4).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All data pointers are DEVICE pointers on the current CUDA device; the
+ *   caller owns every buffer (allocates and frees it).  The library never
+ *   frees or retains a caller pointer past the call.
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *   default stream).  A return of FP8_OK means the work was enqueued.
+ * - A "scale" is always the DEQUANT multiplier amax / MAX ([Flax] 1, 2.2):
+ *   quantize divides by it, dequantize multiplies by it.
+ * - Matrices are row-major.  GEMM operands are both stored [rows, K] with K
+ *   contiguous ("A row-major, B column-major", the TN layout of [Nano]
+ *   "核心原语"); b is [N, K], the layout of nn.Linear.weight.
+ * - Quantization is bit-exact: y = fl32(x / s) (IEEE division), clipped to
+ *   +-MAX, then one round-to-nearest-even cast ([Flax] 2.2 quantize).
+ * - Errors: calls return an fp8_status_t.  Device-side errors (a bounded wait
+ *   that expired) are recorded in a library-wide device error word and read
+ *   with fp8_get_last_device_error().
+ */
+#ifndef FP8GEMM_H
+#define FP8GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8_API __attribute__((visibility("default")))
+#else
+#define FP8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *fp8_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  FP8_OK = 0,
+  FP8_ERR_INVALID_ARG = -1, /* null pointer, non-positive or too-large size, bad enum */
+  FP8_ERR_MISALIGNED = -2,  /* pointer/stride alignment or K granularity violated */
+  FP8_ERR_UNSUPPORTED = -3, /* format combination or shape the kernels do not cover */
+  FP8_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+  FP8_ERR_TIMEOUT = -5,     /* a device-side bounded wait expired (device error word) */
+  FP8_ERR_NO_DEVICE = -6    /* no sm_103 device is current */
+} fp8_status_t;
+
+typedef enum { FP8_IN_BF16 = 0, FP8_IN_F32 = 1 } fp8_in_dtype_t;
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_fmt_t; /* E4M3fn max 448, E5M2 max 57344 */
+typedef enum { FP8_SCALE_F32 = 0, FP8_SCALE_UE8M0 = 1 } fp8_scale_fmt_t;
+typedef enum { FP8_OUT_F32 = 0, FP8_OUT_BF16 = 1 } fp8_out_dtype_t;
+
+/* ------------------------------------------------------------------ amax --
+ * fp8_amax: amax_out[0] = max |x[i]| over i < n ([Flax] 1: "amax is the max
+ * absolute value of the tensor").  x: n elements of in_dt, 16-byte aligned.
+ * amax_out: one fp32, overwritten (the call clears it first).  Exact (max is
+ * order independent).  n == 0 gives 0.
+ */
+FP8_API int fp8_amax(const void *x, int in_dt, int64_t n, float *amax_out, fp8_stream_t stream);
+
+/* ------------------------------------------------------- quantize tensor --
+ * fp8_quantize_tensor: per-tensor quantization ([Flax] 2.2 quantize; 2.3
+ * in_q for delayed scaling).
+ *   x       [rows, cols] of in_dt, row-major, 16-byte aligned, cols % 8 == 0.
+ *   fmt     FP8_E4M3 (activations, weights) or FP8_E5M2 (gradients).
+ *   amax_in nullable.  CURRENT scaling: when non-null the scale is
+ *           s = fl32(amax_in[0] / MAX) (1.0 if amax_in[0] == 0), typically the
+ *           output of fp8_amax on the same x.
+ *   scale   DELAYED scaling: used when amax_in is null; s = scale[0] (the
+ *           scale fp8_delayed_state_update left for this step).
+ *   scale_out nullable; receives s (fp32), e.g. for the GEMM epilogue.
+ *   q       [rows, cols] uint8 codes, row-major.
+ *   q_t     nullable; [cols, rows] uint8 codes: the transposed copy that the
+ *           backward GEMMs read as a K-contiguous operand.
+ *   amax_out nullable; receives max |x| (cleared first), the amax that the
+ *           delayed-scaling history takes for this step.
+ */
+FP8_API int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, int fmt,
+                        const float *amax_in, const float *scale, float *scale_out,
+                        uint8_t *q, uint8_t *q_t, float *amax_out, fp8_stream_t stream);
+
+/* -------------------------------------------------- quantize token group --
+ * fp8_quantize_token_group: dynamic per-token activation quantization in
+ * 1 x 128 K groups ([HF] 一; scale formats [HF] 四/七).
+ *   x      [M, K] of in_dt, row-major, 16-byte aligned, K % 16 == 0 (the last
+ *          group may be ragged: its amax covers the valid elements only).
+ *   sfmt   FP8_SCALE_F32: scales are fp32 amax/MAX (1.0 for an all-zero group).
+ *          FP8_SCALE_UE8M0: scales are bytes e + 127 with 2^e = amax/MAX
+ *          rounded UP to a power of two (byte 127 for an all-zero group), and
+ *          the group is quantized WITH 2^e ([HF] 七).
+ *   q      [M, K] uint8 codes.
+ *   scales GROUP-MAJOR: [ceil(K/128), M] (fp32 or uint8): scales[g * M + m] is
+ *          the scale of row m, K group g.
+ */
+FP8_API int fp8_quantize_token_group(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
+                             int sfmt, uint8_t *q, void *scales, fp8_stream_t stream);
+
+/* -------------------------------------------------------- quantize block --
+ * fp8_quantize_block: 128 x 128 weight-block quantization ([HF] 一: one scale
+ * per block, weight_scale_inv of shape (ceil(N/128), ceil(K/128))).
+ *   w      [N, K] of in_dt, row-major, 16-byte aligned, K % 16 == 0.
+ *   sfmt   as for fp8_quantize_token_group.
+ *   q      [N, K] uint8 codes.
+ *   scales [ceil(N/128), ceil(K/128)] row-major (fp32 or uint8).
+ */
+FP8_API int fp8_quantize_block(const void *w, int in_dt, int64_t N, int64_t K, int fmt, int sfmt,
+                       uint8_t *q, void *scales, fp8_stream_t stream);
+
+/* ----------------------------------------------------------- quantize mx --
+ * fp8_quantize_mx: MOSS two-level microscaling ([MOSS] 4, steps 1-4).
+ *   x      [R, K] of in_dt, row-major, 16-byte aligned, K % 128 == 0.
+ *   amax   device fp32: max |x| over the whole tensor (from fp8_amax).  The
+ *          global factor is S = max_i s_i with s_i = fl32(amax_i / MAX) over
+ *          the 1x32 blocks; since fp32 rounding is monotone this equals
+ *          fl32(amax / MAX), which is how it is evaluated (1.0 if amax == 0).
+ *   global_out device fp32: receives S (the FP32 factor the GEMM epilogue
+ *          applies).
+ *   q      [R, K] uint8 codes, quantized with the effective scale S * r_i.
+ *   local  E8M0 local factors r_i = 2^ceil(log2(fl32(s_i / S))) in (0, 1],
+ *          byte e + 127 (byte 127 for an all-zero block; e clamped at -127).
+ *          Layout (the block-scaled GEMM's operand layout): R_pad = R rounded
+ *          up to 128; local is uint32 [K/128][R_pad]; the word for row r and
+ *          128-wide K slice g holds in byte j the factor of the 1x32 block
+ *          4g + j, and sits at index g * R_pad + (r & ~127) + 4 * (r % 32) +
+ *          (r % 128) / 32.  Words of padding rows are written as 127 bytes.
+ *          Size: 4 * (K/128) * R_pad bytes.
+ */
+FP8_API int fp8_quantize_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
+                    const float *amax, float *global_out, uint8_t *q, uint32_t *local,
+                    fp8_stream_t stream);
+
+/* ------------------------------------------------------ GEMM, per tensor --
+ * fp8_gemm_tensor: C = (sa * sb) * (A_q . B_q^T) with FP32 accumulation in
+ * TMEM and the scales applied in the epilogue ([Flax] 2.2: dot with
+ * preferred_element_type = f32, then dequantize by a_scale * b_scale; [Nano]
+ * "实现": out_dtype bf16).
+ *   a  [M, K] uint8 codes of format fa; b [N, K] codes of format fb.
+ *      E4M3 x E4M3 (forward) and E5M2 x E4M3 (gradient GEMMs) are the uses;
+ *      every E4M3/E5M2 pairing is accepted.
+ *   sa, sb  device fp32 scalars (dequant scales).
+ *   K % 16 == 0; a, b 16-byte aligned.  M, N >= 1 (ragged tiles are masked).
+ *   out_dt  FP8_OUT_F32 or FP8_OUT_BF16 (RNE); c [M, ldc] row-major,
+ *           16-byte aligned, ldc >= N, ldc * elemsize % 16 == 0.
+ *   accumulate  0: C = result.  1 (FP8_OUT_F32 only): C += result.
+ */
+FP8_API int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, const float *sa,
+                    const float *sb, int64_t M, int64_t N, int64_t K, int out_dt, void *c,
+                    int64_t ldc, int accumulate, fp8_stream_t stream);
+
+/* ---------------------------------------------------- GEMM, per K group --
+ * fp8_gemm_group: C[m,n] = sum_g sa[g,m] * sb[n/128, g] * sum_{k in g} a.b
+ * ([HF] 一: 1x128 activation groups times 128x128 weight blocks), output
+ * bf16.  The per-group scales are applied in the main loop.
+ *   a  [M, K] E4M3 codes, sa GROUP-MAJOR [K/128, M] (fp8_quantize_token_group).
+ *   b  [N, K] E4M3 codes, sb [ceil(N/128), K/128] (fp8_quantize_block).
+ *   sfmt FP8_SCALE_F32: fp32 scales, partial sums promoted per 128-K group on
+ *        the CUDA cores.  FP8_SCALE_UE8M0: byte scales, applied by the tensor
+ *        core as block scale factors (no promotion).
+ *   K % 128 == 0.  c [M, ldc] bf16 as for fp8_gemm_tensor.
+ */
+FP8_API int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
+                   int sfmt, int64_t M, int64_t N, int64_t K, void *c, int64_t ldc,
+                   fp8_stream_t stream);
+
+/* ----------------------------------------------------- GEMM, two level --
+ * fp8_gemm_mx: C = S_a * S_b * sum_i r_a[m,i] r_b[n,i] sum_{k in i} a.b
+ * ([MOSS] 4, step 4): the E8M0 local factors are block scale factors of the
+ * MMA (kind::mxf8f6f4, one per 1x32), the FP32 global factors are applied
+ * once in the epilogue.
+ *   a [M, K], b [N, K] E4M3 codes; la, lb local factors in the layout written
+ *   by fp8_quantize_mx (R_pad = M or N rounded up to 128); ga, gb device fp32
+ *   global factors.  K % 128 == 0.  out_dt / c / ldc as for fp8_gemm_tensor.
+ */
+FP8_API int fp8_gemm_mx(const uint8_t *a, const uint32_t *la, const float *ga, const uint8_t *b,
+                const uint32_t *lb, const float *gb, int64_t M, int64_t N, int64_t K,
+                int out_dt, void *c, int64_t ldc, fp8_stream_t stream);
+
+/* -------------------------------------------------- delayed-state update --
+ * fp8_delayed_state_update: one amax-history step of delayed scaling
+ * ([Flax] 2.3 compute_amax_history / update_fp8_meta), on device, no host
+ * synchronisation.  In order:
+ *   1. hist <- roll(hist, -1); hist[0] <- amax_cur[0]   (element 0 is newest)
+ *   2. m = max(hist); scale[0] <- fl32(m / MAX) if m > 0 and finite, else
+ *      scale[0] is kept.
+ * hist [L] fp32 (L >= 1), scale [1] fp32, amax_cur [1] fp32 (the fused amax
+ * fp8_quantize_tensor wrote for this step).  After the call scale[0] is the
+ * scale the NEXT step quantizes with; starting from the guide's initial state
+ * (zeros, 1.0) this reproduces in_q's order exactly (the guide computes the
+ * scale from the history before pushing the current amax, [Flax] 2.3).
+ */
+FP8_API int fp8_delayed_state_update(float *hist, float *scale, const float *amax_cur, int64_t L,
+                             int fmt, fp8_stream_t stream);
+
+/* -------------------------------------------- SwiGLU / AdamW (support) --
+ * Support kernels of the FP8 SwiGLU training step.  Not described on the
+ * pages; plain definitions: silu(z) = z / (1 + exp(-z)) in fp32.
+ * fp8_swiglu_forward: a = silu(h) * u (bf16 in, bf16 out), n elements.
+ * fp8_swiglu_backward: dh = da * u * silu'(h), du = da * silu(h), bf16.
+ * fp8_adamw_step: decoupled-weight-decay Adam on fp32 master weights p with
+ *   moments m, v (fp32), gradient g (fp32); writes the bf16 copy p_bf16
+ *   (nullable).  step counts from 1.  All buffers 16-byte aligned.
+ */
+FP8_API int fp8_swiglu_forward(const void *h, const void *u, void *a, int64_t n, fp8_stream_t stream);
+FP8_API int fp8_swiglu_backward(const void *da, const void *h, const void *u, void *dh, void *du,
+                        int64_t n, fp8_stream_t stream);
+FP8_API int fp8_adamw_step(float *p, const float *g, float *m, float *v, void *p_bf16, int64_t n,
+                   int64_t step, float lr, float beta1, float beta2, float eps,
+                   float weight_decay, fp8_stream_t stream);
+
+/* ---------------------------------------------------------------- status --
+ * fp8_status_string: static text for a status code.
+ * fp8_get_last_device_error: synchronises `stream`, then returns (and clears)
+ * the first device-side error recorded since the last read: 0 for none,
+ * FP8_ERR_TIMEOUT when a bounded wait expired; *where_out (nullable) receives
+ * a small code naming the wait (1 producer, 2 MMA, 3 epilogue).
+ * fp8_version: library version string.
+ */
+FP8_API const char *fp8_status_string(int status);
+FP8_API int fp8_get_last_device_error(int *where_out, fp8_stream_t stream);
+FP8_API const char *fp8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8GEMM_H */

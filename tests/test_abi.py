@@ -1,0 +1,99 @@
+"""The C-ABI library: it loads, exports every entry point include/fp8gemm.h
+declares, and rejects bad arguments on the host (no GPU needed: validation
+runs before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8gemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_quantized_gemm_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_symbols():
+    text = open(HEADER, encoding="utf-8").read()
+    return sorted(set(re.findall(r"^FP8_API[^;(]*?\b(fp8_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("fp8_amax", "fp8_quantize_tensor", "fp8_quantize_token_group", "fp8_quantize_block",
+              "fp8_quantize_mx", "fp8_gemm_tensor", "fp8_gemm_group", "fp8_gemm_mx",
+              "fp8_delayed_state_update"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    import fp8_quantized_gemm_gb300 as F
+    assert set(F.EXPORTED) == set(declared_symbols())
+
+
+def test_status_strings(lib):
+    lib.fp8_status_string.restype = ctypes.c_char_p
+    assert lib.fp8_status_string(0) == b"ok"
+    assert b"misaligned" in lib.fp8_status_string(-2)
+    lib.fp8_version.restype = ctypes.c_char_p
+    assert b"sm_103a" in lib.fp8_version()
+
+
+def _gemm(lib, a=16, b=16, sa=16, sb=16, M=128, N=128, K=128, out_dt=1, c=256, ldc=128, acc=0,
+          fa=0, fb=0):
+    f = lib.fp8_gemm_tensor
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    return f(a, fa, b, fb, sa, sb, M, N, K, out_dt, c, ldc, acc, None)
+
+
+def test_gemm_argument_validation(lib):
+    assert _gemm(lib, a=None) == -1                 # null operand
+    assert _gemm(lib, M=0) == -1                    # empty
+    assert _gemm(lib, K=17) == -2                   # K % 16
+    assert _gemm(lib, a=24) == -2                   # misaligned operand
+    assert _gemm(lib, ldc=100) == -1                # ldc < N
+    assert _gemm(lib, N=100, ldc=100) == -2         # row pitch not 16-byte multiple (bf16)
+    assert _gemm(lib, acc=1, out_dt=1) == -3        # accumulate needs f32 output
+    assert _gemm(lib, fa=2) == -1                   # bad format enum
+    # a well-formed call reaches the device check: no GPU here
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except Exception:
+        has_gpu = False
+    if not has_gpu:
+        assert _gemm(lib) == -6
+
+
+def test_group_and_mx_need_k_multiple_of_128(lib):
+    g = lib.fp8_gemm_group
+    g.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_int64] * 3 + [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    assert g(16, 16, 16, 16, 0, 128, 128, 144, 256, 128, None) == -2
+    assert g(16, 16, 16, 16, 7, 128, 128, 128, 256, 128, None) == -1
+    q = lib.fp8_quantize_mx
+    q.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert q(16, 0, 4, 96, 0, 16, 16, 16, 16, None) == -2
+
+
+def test_quantize_validation(lib):
+    f = lib.fp8_quantize_tensor
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int] + \
+        [ctypes.c_void_p] * 7
+    assert f(16, 0, 4, 12, 0, 16, None, None, 16, None, None, None) == -2   # cols % 8
+    assert f(16, 0, 4, 16, 0, None, None, None, 16, None, None, None) == -1  # no scale source
+    assert f(16, 3, 4, 16, 0, 16, None, None, 16, None, None, None) == -1    # bad input dtype
+    d = lib.fp8_delayed_state_update
+    d.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    assert d(16, 16, 16, 0, 0, None) == -1
+    assert d(16, 16, 16, 1 << 20, 0, None) == -1

@@ -1,0 +1,199 @@
+"""GPU parity of the scaled-FP8 GEMMs against the float64 oracle.
+
+Operands are quantized by the ORACLE on the CPU and uploaded, so each GEMM is
+checked on its own.  Acceptance per output element:
+|gpu - oracle| <= 1e-3 * sum_k |a_deq| |b_deq| (+ one bf16 ulp of |oracle| for a
+bf16 output)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import FMT, lib, mx_pack, sample_positions
+from oracle import gemm as OG
+from oracle import quantize as OQ
+
+pytestmark = pytest.mark.gpu
+
+
+def dev_u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def dev_f32(v):
+    return torch.tensor(np.atleast_1d(np.asarray(v, dtype=np.float32)), device="cuda")
+
+
+def per_tensor_operands(m, n, k, fa, fb, seed):
+    sa_std = 1.0 if fa == "e4m3" else 1e-3
+    x = workloads.normal((m, k), sa_std, seed).to(torch.bfloat16).float().numpy()
+    w = workloads.normal((n, k), 0.02, seed + 1).to(torch.bfloat16).float().numpy()
+    qa, sa = OQ.quantize_tensor(x, fa)
+    qb, sb = OQ.quantize_tensor(w, fb)
+    return qa, sa, qb, sb
+
+
+def run_tensor(qa, fa, sa, qb, fb, sb, out_dtype, accumulate_into=None):
+    F = lib()
+    m, n = qa.shape[0], qb.shape[0]
+    if accumulate_into is not None:
+        out = accumulate_into
+    else:
+        out = torch.empty((m, n), dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float32,
+                          device="cuda")
+    F.fp8_gemm_tensor(dev_u8(qa), FMT[fa], dev_u8(qb), FMT[fb], dev_f32(sa), dev_f32(sb), out,
+                      accumulate=accumulate_into is not None)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+SHAPES = [(128, 256, 128), (1, 64, 32), (16, 64, 32), (129, 300, 272), (300, 520, 1024),
+          (256, 512, 4096), (1000, 130, 16)]
+
+
+@pytest.mark.parametrize("mnk", SHAPES)
+@pytest.mark.parametrize("fmts", [("e4m3", "e4m3"), ("e5m2", "e4m3")])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_gemm_tensor(mnk, fmts, out_dtype):
+    m, n, k = mnk
+    fa, fb = fmts
+    qa, sa, qb, sb = per_tensor_operands(m, n, k, fa, fb, seed=m + n + k)
+    got = run_tensor(qa, fa, sa, qb, fb, sb, out_dtype)
+    c, e = OG.gemm(OG.dequant_operand(qa, fa, sa), OG.dequant_operand(qb, fb, sb))
+    ok, worst = OG.check(got, c, e, out_dtype)
+    assert ok, worst
+
+
+def test_gemm_tensor_accumulate():
+    m, n, k = 200, 384, 256
+    qa, sa, qb, sb = per_tensor_operands(m, n, k, "e5m2", "e4m3", seed=3)
+    qa2, sa2, qb2, sb2 = per_tensor_operands(m, n, k, "e5m2", "e4m3", seed=9)
+    out = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+    run_tensor(qa, "e5m2", sa, qb, "e4m3", sb, "f32", accumulate_into=out)
+    got = run_tensor(qa2, "e5m2", sa2, qb2, "e4m3", sb2, "f32", accumulate_into=out)
+    c1, e1 = OG.gemm(OG.dequant_operand(qa, "e5m2", sa), OG.dequant_operand(qb, "e4m3", sb))
+    c2, e2 = OG.gemm(OG.dequant_operand(qa2, "e5m2", sa2), OG.dequant_operand(qb2, "e4m3", sb2))
+    ok, worst = OG.check(got, c1 + c2, e1 + e2, "f32")
+    assert ok, worst
+
+
+def test_tiny_per_tensor_example():
+    """The Flax guide's 16x32 . 32x64 example (section 2.2), current scaling,
+    fp32 output; b is passed as b^T [64, 32]."""
+    F = lib()
+    a, b = workloads.tiny_per_tensor()
+    ad, btd = a.cuda(), b.t().contiguous().cuda()
+    qa = torch.empty((16, 32), dtype=torch.uint8, device="cuda")
+    qb = torch.empty((64, 32), dtype=torch.uint8, device="cuda")
+    am, bm = torch.empty(1, device="cuda"), torch.empty(1, device="cuda")
+    sa, sb = torch.empty(1, device="cuda"), torch.empty(1, device="cuda")
+    F.fp8_amax(ad, am)
+    F.fp8_amax(btd, bm)
+    F.fp8_quantize_tensor(ad, 0, qa, amax_in=am, scale_out=sa)
+    F.fp8_quantize_tensor(btd, 0, qb, amax_in=bm, scale_out=sb)
+    out = torch.empty((16, 64), dtype=torch.float32, device="cuda")
+    F.fp8_gemm_tensor(qa, 0, qb, 0, sa, sb, out)
+    ra, rsa = OQ.quantize_tensor(a.numpy(), "e4m3")
+    rb, rsb = OQ.quantize_tensor(b.t().contiguous().numpy(), "e4m3")
+    assert np.array_equal(qa.cpu().numpy(), ra) and np.array_equal(qb.cpu().numpy(), rb)
+    assert sa.item() == float(rsa) and sb.item() == float(rsb)
+    c, e = OG.gemm(OG.dequant_operand(ra, "e4m3", rsa), OG.dequant_operand(rb, "e4m3", rsb))
+    ok, worst = OG.check(out.cpu().numpy(), c, e, "f32")
+    assert ok, worst
+
+
+# ------------------------------------------------------------ per K group --
+
+def group_operands(m, n, k, sfmt, seed):
+    act, w = workloads.fine_grained(m, seed=seed, k=k, n=n)
+    qa, sa = OQ.quantize_token_group(act.float().numpy(), "e4m3", sfmt)
+    qb, sb = OQ.quantize_block(w.float().numpy(), "e4m3", sfmt)
+    return qa, sa, qb, sb
+
+
+def group_reference(qa, sa, qb, sb, sfmt, rows=None, cols=None):
+    m, k = qa.shape
+    n = qb.shape[0]
+    a = OG.dequant_operand(qa, "e4m3", OQ.expand(OQ.group_scale_values(sa, sfmt), m, k, 1, 128))
+    b = OG.dequant_operand(qb, "e4m3", OQ.expand(OQ.group_scale_values(sb, sfmt), n, k, 128, 128))
+    if rows is None:
+        return OG.gemm(a, b)
+    return OG.gemm_sampled(a, b, rows, cols)
+
+
+def run_group(qa, sa, qb, sb, sfmt):
+    F = lib()
+    m, n = qa.shape[0], qb.shape[0]
+    sa_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sa).T)).cuda()   # [G, M]
+    sb_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sb))).cuda()     # [N/128, G]
+    out = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    F.fp8_gemm_group(dev_u8(qa), sa_dev, dev_u8(qb), sb_dev, 0 if sfmt == "f32" else 1, out)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("mnk", [(1, 256, 512), (128, 128, 128), (200, 384, 1024),
+                                 (130, 2048, 7168), (513, 200, 384)])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_gemm_group(mnk, sfmt):
+    m, n, k = mnk
+    qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=2)
+    got = run_group(qa, sa, qb, sb, sfmt)
+    c, e = group_reference(qa, sa, qb, sb, sfmt)
+    ok, worst = OG.check(got, c, e, "bf16")
+    assert ok, worst
+
+
+# -------------------------------------------------------------- two level --
+
+def mx_operands(m, n, k, seed):
+    a, b = workloads.two_level(seed=seed, m=m, n=n, k=k)
+    qa, la, ga = OQ.quantize_two_level(a.float().numpy(), "e4m3")
+    qb, lb, gb = OQ.quantize_two_level(b.float().numpy(), "e4m3")
+    return qa, la, ga, qb, lb, gb
+
+
+def mx_reference(qa, la, ga, qb, lb, gb, rows=None, cols=None):
+    m, k = qa.shape
+    n = qb.shape[0]
+    a = OG.dequant_operand(qa, "e4m3", OQ.expand(OQ.two_level_scale_values(la, ga), m, k, 1, 32))
+    b = OG.dequant_operand(qb, "e4m3", OQ.expand(OQ.two_level_scale_values(lb, gb), n, k, 1, 32))
+    if rows is None:
+        return OG.gemm(a, b)
+    return OG.gemm_sampled(a, b, rows, cols)
+
+
+def run_mx(qa, la, ga, qb, lb, gb, out_dtype="bf16"):
+    F = lib()
+    m, n = qa.shape[0], qb.shape[0]
+    out = torch.empty((m, n), dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float32,
+                      device="cuda")
+    F.fp8_gemm_mx(dev_u8(qa), torch.from_numpy(mx_pack(la)).cuda(), dev_f32(ga), dev_u8(qb),
+                  torch.from_numpy(mx_pack(lb)).cuda(), dev_f32(gb), out)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("mnk", [(128, 256, 128), (200, 384, 512), (1, 128, 256), (300, 1000, 1024)])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_gemm_mx(mnk, out_dtype):
+    m, n, k = mnk
+    qa, la, ga, qb, lb, gb = mx_operands(m, n, k, seed=3)
+    got = run_mx(qa, la, ga, qb, lb, gb, out_dtype)
+    c, e = mx_reference(qa, la, ga, qb, lb, gb)
+    ok, worst = OG.check(got, c, e, out_dtype)
+    assert ok, worst
+
+
+def test_gemm_mx_distinct_local_factors():
+    """Every 1x32 block of both operands gets its own power-of-two factor, so a
+    factor applied to the wrong block or row shows up."""
+    m, n, k = 256, 256, 512
+    rng = np.random.default_rng(11)
+    qa, la, ga, qb, lb, gb = mx_operands(m, n, k, seed=5)
+    la = (127 - rng.integers(0, 6, la.shape)).astype(np.uint8)
+    lb = (127 - rng.integers(0, 6, lb.shape)).astype(np.uint8)
+    got = run_mx(qa, la, ga, qb, lb, gb, "f32")
+    c, e = mx_reference(qa, la, ga, qb, lb, gb)
+    ok, worst = OG.check(got, c, e, "f32")
+    assert ok, worst

@@ -1,0 +1,208 @@
+"""GPU parity of the quantization kernels against the CPU oracle.
+
+Quantized bytes and scales must match bit for bit (the kernel and the oracle
+both take the fp32 x / s decision, then round to nearest even)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import FMT, f32_bits, lib, mx_unpack, to_np_u8
+from oracle import delayed as OD
+from oracle import quantize as OQ
+
+pytestmark = pytest.mark.gpu
+
+
+def special_input(shape, std, seed, dtype, fmt):
+    """Normal draws plus hand-placed edge values: zeros, -0.0, tiny values that
+    land in the FP8 subnormal range, and the element that sets the amax."""
+    x = workloads.normal(shape, std, seed)
+    flat = x.view(-1)
+    n = flat.numel()
+    if n >= 8:
+        flat[0] = 0.0
+        flat[1] = -0.0
+        flat[2] = std * 1e-3
+        flat[3] = -std * 3e-4
+        flat[n // 2] = std * 7.0
+        flat[n - 1] = -std * 6.5
+    return x.to(dtype)
+
+
+SHAPES = [(1, 8), (7, 24), (128, 128), (300, 520), (513, 1032)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("transpose", [False, True])
+def test_current_scaling(shape, fmt, dt, transpose):
+    F = lib()
+    std = 1.0 if fmt == "e4m3" else 1e-3
+    x = special_input(shape, std, 10 + shape[0], dt, fmt)
+    xf = x.float().numpy()
+    xd = x.cuda()
+    amax = torch.empty(1, device="cuda")
+    F.fp8_amax(xd, amax)
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    qt = torch.empty((shape[1], shape[0]), dtype=torch.uint8, device="cuda") if transpose else None
+    s_out = torch.empty(1, device="cuda")
+    F.fp8_quantize_tensor(xd, FMT[fmt], q, amax_in=amax, scale_out=s_out, q_t=qt)
+    ref_q, ref_s = OQ.quantize_tensor(xf, fmt)
+    assert f32_bits(amax.item()) == f32_bits(OQ.amax(xf))
+    assert f32_bits(s_out.item()) == f32_bits(ref_s)
+    assert np.array_equal(to_np_u8(q), ref_q)
+    if transpose:
+        assert np.array_equal(to_np_u8(qt), ref_q.T)
+
+
+@pytest.mark.parametrize("shape", [(64, 96), (257, 136)])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_given_scale_with_clip_and_fused_amax(shape, fmt):
+    F = lib()
+    x = special_input(shape, 1.0, 77, torch.bfloat16, fmt)
+    xf = x.float().numpy()
+    # a scale small enough that the largest values clip at +-MAX
+    from oracle.formats import fmt_of
+    scale = np.float32(np.float32(OQ.amax(xf)) / np.float32(fmt_of(fmt).max) / np.float32(3.0))
+    sd = torch.tensor([float(scale)], dtype=torch.float32, device="cuda")
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    qt = torch.empty((shape[1], shape[0]), dtype=torch.uint8, device="cuda")
+    amax_out = torch.full((1,), 123.0, device="cuda")
+    F.fp8_quantize_tensor(x.cuda(), FMT[fmt], q, scale=sd, q_t=qt, amax_out=amax_out)
+    ref = OQ.quantize_with_scale(xf, scale, fmt)
+    assert np.array_equal(to_np_u8(q), ref)
+    assert np.array_equal(to_np_u8(qt), ref.T)
+    assert f32_bits(amax_out.item()) == f32_bits(OQ.amax(xf))
+
+
+def test_amax_sizes_and_zero():
+    F = lib()
+    for n in (1, 7, 8, 1000, 1 << 20):
+        x = workloads.normal((n,), 2.0, n)
+        out = torch.empty(1, device="cuda")
+        F.fp8_amax(x.cuda(), out)
+        assert out.item() == float(np.max(np.abs(x.numpy())))
+    z = torch.zeros(4096, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((1,), 5.0, device="cuda")
+    F.fp8_amax(z, out)
+    assert out.item() == 0.0
+    q = torch.empty((64, 64), dtype=torch.uint8, device="cuda")
+    s = torch.empty(1, device="cuda")
+    F.fp8_quantize_tensor(z.view(64, 64), 0, q, amax_in=out, scale_out=s)
+    assert s.item() == 1.0 and not q.any()
+
+
+@pytest.mark.parametrize("shape", [(1, 128), (5, 304), (130, 1024), (64, 7168)])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_token_group(shape, sfmt, dt):
+    F = lib()
+    m, k = shape
+    act, _ = workloads.fine_grained(m, k=k, n=128)
+    x = act.to(dt)
+    if m > 2:
+        x[2, : min(128, k)] = 0.0  # an all-zero group
+    xf = x.float().numpy()
+    g = (k + 127) // 128
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    sc = torch.empty((g, m), dtype=torch.float32 if sfmt == "f32" else torch.uint8, device="cuda")
+    F.fp8_quantize_token_group(x.cuda(), 0, 0 if sfmt == "f32" else 1, q, sc)
+    ref_q, ref_s = OQ.quantize_token_group(xf, "e4m3", sfmt)
+    assert np.array_equal(to_np_u8(q), ref_q)
+    got = sc.cpu().numpy().T
+    if sfmt == "f32":
+        assert np.array_equal(got.view(np.uint32), np.asarray(ref_s, np.float32).view(np.uint32))
+    else:
+        assert np.array_equal(got, ref_s)
+
+
+@pytest.mark.parametrize("shape", [(200, 272), (256, 512), (2048, 7168)])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_block(shape, sfmt):
+    F = lib()
+    n, k = shape
+    _, w = workloads.fine_grained(1, k=k, n=n)
+    wf = w.float().numpy()
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    bn, bk = (n + 127) // 128, (k + 127) // 128
+    sc = torch.empty((bn, bk), dtype=torch.float32 if sfmt == "f32" else torch.uint8, device="cuda")
+    F.fp8_quantize_block(w.cuda(), 0, 0 if sfmt == "f32" else 1, q, sc)
+    ref_q, ref_s = OQ.quantize_block(wf, "e4m3", sfmt)
+    assert np.array_equal(to_np_u8(q), ref_q)
+    got = sc.cpu().numpy()
+    if sfmt == "f32":
+        assert np.array_equal(got.view(np.uint32), np.asarray(ref_s, np.float32).view(np.uint32))
+    else:
+        assert np.array_equal(got, ref_s)
+
+
+@pytest.mark.parametrize("shape", [(1, 128), (130, 512), (256, 1024), (333, 2048)])
+def test_two_level(shape):
+    F = lib()
+    r, k = shape
+    a, _ = workloads.two_level(m=r, n=8, k=k)
+    x = a.clone()
+    x[0, 32:64] = 0.0  # an all-zero 1x32 block
+    xf = x.float().numpy()
+    xd = x.cuda()
+    amax = torch.empty(1, device="cuda")
+    F.fp8_amax(xd, amax)
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    words = F.mx_local_words(r, k)
+    words.fill_(0)
+    glob = torch.empty(1, device="cuda")
+    F.fp8_quantize_mx(xd, 0, amax, glob, q, words)
+    ref_q, ref_l, ref_s = OQ.quantize_two_level(xf, "e4m3")
+    assert f32_bits(glob.item()) == f32_bits(ref_s)
+    assert np.array_equal(to_np_u8(q), ref_q)
+    w = words.cpu().numpy()
+    assert np.array_equal(mx_unpack(w, r, k), ref_l)
+    rpad = (r + 127) // 128 * 128
+    if rpad > r:  # padding rows hold factor 1
+        rows = np.arange(r, rpad)
+        pos = (rows & ~127) + 4 * (rows % 32) + (rows % 128) // 32
+        assert np.all(w.view(np.uint32)[:, pos] == 0x7F7F7F7F)
+
+
+@pytest.mark.parametrize("length", [4, 1024])
+def test_delayed_scaling_sequence(length):
+    """GPU quantize + fp8_delayed_state_update over 20 steps against the
+    guide's in_q order (scale from the previous history, then push)."""
+    F = lib()
+    hist = torch.zeros(length, device="cuda")
+    scale = torch.ones(1, device="cuda")
+    amax_cur = torch.empty(1, device="cuda")
+    st = OD.DelayedState.initial(length)
+    for t in range(20):
+        x = workloads.normal((64, 128), 2.0 ** ((t * 3) % 11 - 5), 500 + t).to(torch.bfloat16)
+        if t == 4:
+            x.zero_()
+        xf = x.float().numpy()
+        q = torch.empty((64, 128), dtype=torch.uint8, device="cuda")
+        used = scale.item()
+        F.fp8_quantize_tensor(x.cuda(), 0, q, scale=scale, amax_out=amax_cur)
+        F.fp8_delayed_state_update(hist, scale, amax_cur, 0)
+        ref_q, ref_scale, st = OD.in_q(xf, "e4m3", st)
+        assert f32_bits(used) == f32_bits(ref_scale), t
+        assert np.array_equal(to_np_u8(q), ref_q), t
+        assert np.array_equal(hist.cpu().numpy().view(np.uint32), st.history.view(np.uint32)), t
+
+
+def test_delayed_update_keeps_scale_on_nonfinite():
+    F = lib()
+    hist = torch.zeros(8, device="cuda")
+    hist[3] = float("inf")
+    scale = torch.tensor([0.5], device="cuda")
+    F.fp8_delayed_state_update(hist, scale, torch.tensor([2.0], device="cuda"), 0)
+    assert scale.item() == 0.5
+    hist[:] = 0.0
+    hist[5] = float("nan")
+    F.fp8_delayed_state_update(hist, scale, torch.tensor([2.0], device="cuda"), 0)
+    assert scale.item() == 0.5
+    hist[:] = 0.0
+    F.fp8_delayed_state_update(hist, scale, torch.tensor([0.0], device="cuda"), 1)
+    assert scale.item() == 0.5
+    F.fp8_delayed_state_update(hist, scale, torch.tensor([57344.0 * 4], device="cuda"), 1)
+    assert scale.item() == 4.0
