@@ -10,6 +10,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import hashlib
 import os
+import platform
 import shutil
 import subprocess
 
@@ -45,6 +46,7 @@ def _deps_digest() -> str:
                 with open(os.path.join(d, f), "rb") as fh:
                     h.update(f.encode() + fh.read())
     h.update(" ".join(NVCC_FLAGS).encode())
+    h.update(platform.machine().encode())  # host objects differ per architecture
     return h.hexdigest()[:16]
 
 
@@ -69,7 +71,7 @@ def build(verbose: bool = False) -> str:
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(lambda s: _compile(nvcc, s, digest), srcs))
-    stamp = hashlib.sha256("".join(objs).encode()).hexdigest()[:16]
+    stamp = hashlib.sha256(("".join(objs) + platform.machine()).encode()).hexdigest()[:16]
     stamp_file = os.path.join(BUILD, "lib.stamp")
     if os.path.exists(LIB) and os.path.exists(stamp_file):
         with open(stamp_file) as fh:

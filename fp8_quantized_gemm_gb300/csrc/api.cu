@@ -88,9 +88,15 @@ int check_output(const void *c, int64_t N, int64_t ldc, int out_dt) {
   if (c == nullptr) return FP8_ERR_INVALID_ARG;
   if (out_dt != FP8_OUT_F32 && out_dt != FP8_OUT_BF16) return FP8_ERR_INVALID_ARG;
   if (ldc < N) return FP8_ERR_INVALID_ARG;
-  const int64_t es = out_dt == FP8_OUT_F32 ? 4 : 2;
-  if (!aligned16(c) || (ldc * es) % 16 != 0) return FP8_ERR_MISALIGNED;
+  const uintptr_t es = out_dt == FP8_OUT_F32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(c) & (es - 1)) != 0) return FP8_ERR_MISALIGNED;
   return FP8_OK;
+}
+
+// 16-byte vector stores need an aligned base and a row pitch of 16-byte multiples.
+int vector_store_ok(const void *c, int64_t ldc, int out_dt) {
+  const int64_t es = out_dt == FP8_OUT_F32 ? 4 : 2;
+  return aligned16(c) && (ldc * es) % 16 == 0 ? 1 : 0;
 }
 
 int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaStream_t st) {
@@ -98,6 +104,7 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
   int rc = device_state(&d);
   if (rc != FP8_OK) return rc;
   args.err = d->err;
+  args.vec_store = vector_store_ok(args.c, args.ldc, args.out_dt);
   CUtensorMap tma, tmb;
   if ((rc = encode_operand(&tma, a, args.K, args.M, 128)) != FP8_OK) return rc;
   if ((rc = encode_operand(&tmb, b, args.K, args.N, fp8k::gemm_tile_n(mode))) != FP8_OK) return rc;
@@ -133,6 +140,7 @@ int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, in
   if (x == nullptr || q == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
   if (amax_in == nullptr && scale == nullptr) return FP8_ERR_INVALID_ARG;
+  if (amax_out != nullptr && (amax_out == amax_in || amax_out == scale)) return FP8_ERR_INVALID_ARG;
   if (rows < 1 || cols < 1 || rows >= kMaxDim || cols >= kMaxDim) return FP8_ERR_INVALID_ARG;
   if (cols % 8 != 0 || !aligned16(x) || !aligned16(q) || (q_t != nullptr && !aligned16(q_t)))
     return FP8_ERR_MISALIGNED;

@@ -64,7 +64,7 @@ struct Cfg {
 __device__ __forceinline__ void store_row32(const GemmArgs &a, int64_t row, int64_t col0,
                                             const float (&v)[32]) {
   if (row >= a.M || col0 >= a.N) return;
-  const bool full = (col0 + 32 <= a.N);
+  const bool full = (col0 + 32 <= a.N) && a.vec_store;
   if (a.out_dt == 1) {
     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.c) + row * a.ldc + col0;
     if (full) {

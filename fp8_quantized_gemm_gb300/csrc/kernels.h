@@ -37,6 +37,7 @@ struct GemmArgs {
   int fa, fb;          // operand formats: 0 = E4M3, 1 = E5M2
   int out_dt;          // 0 = f32, 1 = bf16
   int accumulate;      // f32 output only
+  int vec_store;       // 1: c and ldc allow 16-byte vector stores
   int64_t ldc;
   void *c;
   const void *sa, *sb;         // scale operands (meaning depends on the mode)

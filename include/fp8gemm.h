@@ -94,7 +94,8 @@ FP8_API int fp8_amax(const void *x, int in_dt, int64_t n, float *amax_out, fp8_s
  *   q_t     nullable; [cols, rows] uint8 codes: the transposed copy that the
  *           backward GEMMs read as a K-contiguous operand.
  *   amax_out nullable; receives max |x| (cleared first), the amax that the
- *           delayed-scaling history takes for this step.
+ *           delayed-scaling history takes for this step.  Must not alias
+ *           amax_in or scale (INVALID_ARG).
  */
 FP8_API int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, int fmt,
                         const float *amax_in, const float *scale, float *scale_out,
@@ -161,7 +162,8 @@ FP8_API int fp8_quantize_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
  *   sa, sb  device fp32 scalars (dequant scales).
  *   K % 16 == 0; a, b 16-byte aligned.  M, N >= 1 (ragged tiles are masked).
  *   out_dt  FP8_OUT_F32 or FP8_OUT_BF16 (RNE); c [M, ldc] row-major,
- *           16-byte aligned, ldc >= N, ldc * elemsize % 16 == 0.
+ *           aligned to its element size, ldc >= N.  (A 16-byte aligned c with
+ *           ldc * elemsize % 16 == 0 takes the vector-store path.)
  *   accumulate  0: C = result.  1 (FP8_OUT_F32 only): C += result.
  */
 FP8_API int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, const float *sa,

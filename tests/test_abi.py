@@ -13,8 +13,8 @@ HEADER = os.path.join(ROOT, "include", "fp8gemm.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from fp8_quantized_gemm_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
     return ctypes.CDLL(path)
 
 
@@ -61,7 +61,7 @@ def test_gemm_argument_validation(lib):
     assert _gemm(lib, K=17) == -2                   # K % 16
     assert _gemm(lib, a=24) == -2                   # misaligned operand
     assert _gemm(lib, ldc=100) == -1                # ldc < N
-    assert _gemm(lib, N=100, ldc=100) == -2         # row pitch not 16-byte multiple (bf16)
+    assert _gemm(lib, c=257) == -2                  # output not aligned to its element
     assert _gemm(lib, acc=1, out_dt=1) == -3        # accumulate needs f32 output
     assert _gemm(lib, fa=2) == -1                   # bad format enum
     # a well-formed call reaches the device check: no GPU here
