@@ -234,3 +234,368 @@ class Float8Linear:
         flops = 3 * 2.0 * rows * self.din * self.dout
         return flops, dt, "first %d of %d token rows (x, g), full W; 3 quantizes + 3 GEMMs" % (
             rows, self.T)
+
+
+# ----------------------------------------------------------- distributed --
+
+def setup_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return torch.device("cuda", torch.cuda.current_device()), rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_digest(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel
+    source has not changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh).get(kernel)
+    if not rec:
+        return None
+    if rec.get("source_digest") != source_digest(rec["sources"]):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+# ------------------------------------------------------------- our arm --
+
+def time_workload(wl, steps, warmup, world, flush, stream):
+    launches = wl.launches()
+    for _ in range(warmup):
+        for _, fn in launches:
+            fn()
+    torch.cuda.synchronize()
+    timer = StepTimer()
+    barrier(world)
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        flush.zero_()  # write 512 MiB: evicts the 129 MB L2 between steps
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for label, fn in launches:
+            timer.launch(label, fn, stream)
+        e.record(stream)
+        timer.steps.append((s, e))
+    torch.cuda.synchronize()
+    barrier(world)
+    return timer, len(launches)
+
+
+def time_e2e(wl, steps, flush, stream):
+    launches = wl.launches()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        wl.upload(stream)
+        for _, fn in launches:
+            fn()
+        wl.download(stream)
+        e.record(stream)
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e))
+    return times
+
+
+def cpu_baseline(wl, rows):
+    flops, dt, sample = wl.oracle_sample(rows)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "seconds": round(dt, 3)}
+
+
+def roofline_entry(bound, achieved, peak, unit, traffic, note):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": note}
+
+
+def run_ours(args):
+    import fp8_quantized_gemm_gb300 as F
+    peaks = load_peaks()
+    dev, rank, world = setup_dist()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    wl = Float8Linear(dev)
+    with ClockSampler(dev.index) as clk:
+        timer, n_launch = time_workload(wl, args.steps, args.warmup, world, flush, stream)
+    rc, where = F.fp8_get_last_device_error()
+    if rc != 0:
+        raise RuntimeError("device error %d (where %d) during the timed region" % (rc, where))
+    step_ms = timer.step_ms()
+    total_ms = max_over_ranks(sum(step_ms), world)
+    value = wl.flops * args.steps * world / (total_ms / 1e3) / 1e12
+    per = timer.per_label_ms()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # dense FP8 = 2 x bf16 (nominal ratio)
+    gemm_ms = sum(per["gemm"]) / len(per["gemm"])
+    gemm_tflops = (wl.flops / 3) / (gemm_ms / 1e3) / 1e12
+    q_ms = sum(per["quantize"])
+    q_gbs = wl.bytes["quantize"] * len(per["quantize"]) / (q_ms / 1e3) / 1e9
+    a_ms = sum(per["amax"])
+    a_gbs = wl.bytes["amax"] * len(per["amax"]) / (a_ms / 1e3) / 1e9
+    src = "MEASURED_PEAKS.json (%s)" % peaks["source"]
+    line = {
+        "metric": "FP8 scaled-GEMM TFLOP/s incl. quantize, % of FP8 peak; quantize GB/s % HBM",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8 e4m3/e5m2, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": wl.T, "d_in": wl.din, "d_out": wl.dout,
+                   "scaling": "per-tensor current", "inputs": "bf16, seeded (workloads.py)",
+                   "l2": "flushed between timed steps (512 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "fraction_of_fp8_peak": round(value / fp8_peak, 4),
+        "roofline": roofline_entry("tensor", gemm_tflops, fp8_peak, "TFLOP/s",
+                                   recorded_traffic("gemm_tensor"),
+                                   "dense FP8 = 2 x measured bf16 burst (%s)" % src),
+        "quantize_roofline": roofline_entry("hbm", q_gbs, peaks["hbm_gbs"], "GB/s",
+                                            recorded_traffic("quantize_tensor_t"),
+                                            "measured HBM copy (%s)" % src),
+        "amax_roofline": roofline_entry("hbm", a_gbs, peaks["hbm_gbs"], "GB/s",
+                                        recorded_traffic("amax"), "measured HBM copy (%s)" % src),
+        "kernel_ms": {k: round(sum(v) / len(v), 4) for k, v in per.items()},
+        "gpu_launches": n_launch * args.steps,
+        "clocks": clk.summary(),
+    }
+    e2e = time_e2e(wl, max(3, min(args.steps, 10)), flush, stream)
+    e2e_ms = max_over_ranks(sum(e2e) / len(e2e), world)
+    line["e2e"] = {"value": round(wl.flops * world / (e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h,
+                   "ms_per_step": round(e2e_ms, 4)}
+    if not args.no_extras and rank == 0:
+        line["rows"] = run_extras(dev, flush, stream, peaks)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The CPU oracle on the same workload: each step is a bounded sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = Float8Linear.__new__(Float8Linear)
+    wl.T, wl.din, wl.dout = 8192, 2048, 2048
+    x, w, g = workloads.float8_linear()
+    wl.host_in = [x, w, g]
+    wl.name = Float8Linear.name
+    for _ in range(args.warmup and 1):
+        wl.oracle_sample(64)
+    flops_total, secs, sample = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        f, dt, sample = wl.oracle_sample(args.cpu_rows)
+        flops_total += f
+        secs += dt
+    value = flops_total / secs / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {
+        "impl": "reference",
+        "metric": "FP8 scaled-GEMM TFLOP/s incl. quantize, % of FP8 peak; quantize GB/s % HBM",
+        "value": value, "unit": "TFLOP/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (oracle over fp8 codes)", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": 8192, "d_in": 2048, "d_out": 2048,
+                   "scaling": "per-tensor current"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------- other workloads --
+
+def time_launches(fns, iters, flush, stream, warmup=3):
+    """Mean ms per label and per pass of `fns`, L2 flushed before each pass."""
+    for _ in range(warmup):
+        for _, fn in fns:
+            fn()
+    torch.cuda.synchronize()
+    timer = StepTimer()
+    for _ in range(iters):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for label, fn in fns:
+            timer.launch(label, fn, stream)
+        e.record(stream)
+        timer.steps.append((s, e))
+    torch.cuda.synchronize()
+    per = {k: sum(v) / len(v) for k, v in timer.per_label_ms().items()}
+    steps = timer.step_ms()
+    return per, sum(steps) / len(steps)
+
+
+def snr_db_dev(x, xhat):
+    d = (x.double() - xhat.double())
+    return float(10.0 * torch.log10((x.double() ** 2).sum() / (d * d).sum()))
+
+
+def run_extras(dev, flush, stream, peaks, iters=10):
+    import fp8_quantized_gemm_gb300 as F
+    fp8_peak, hbm = 2.0 * peaks["bf16_tflops"], peaks["hbm_gbs"]
+    out = {}
+    # per-K-group GEMM (1x128 activations x 128x128 weight blocks), K 7168, N 2048
+    K, N = 7168, 2048
+    _, w = workloads.fine_grained(1, k=K, n=N)
+    wd = w.to(dev)
+    for sname, sfmt in (("f32", F.SCALE_F32), ("ue8m0", F.SCALE_UE8M0)):
+        sdt = torch.float32 if sfmt == F.SCALE_F32 else torch.uint8
+        wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        ws = torch.empty((N // 128, K // 128), dtype=sdt, device=dev)
+        F.fp8_quantize_block(wd, F.E4M3, sfmt, wq, ws)  # offline weight quantization
+        for m in (1, 128, 4096):
+            act, _ = workloads.fine_grained(m, k=K, n=8)
+            ad = act.to(dev)
+            aq = torch.empty((m, K), dtype=torch.uint8, device=dev)
+            asc = torch.empty((K // 128, m), dtype=sdt, device=dev)
+            y = torch.empty((m, N), dtype=torch.bfloat16, device=dev)
+            fns = [("quantize", lambda: F.fp8_quantize_token_group(ad, F.E4M3, sfmt, aq, asc)),
+                   ("gemm", lambda: F.fp8_gemm_group(aq, asc, wq, ws, sfmt, y))]
+            per, step = time_launches(fns, iters, flush, stream)
+            flops = 2.0 * m * N * K
+            gemm_bytes = N * K + m * K + m * N * 2 + ws.numel() * ws.element_size() + \
+                asc.numel() * asc.element_size()
+            out["group_%s_m%d" % (sname, m)] = {
+                "tflops_incl_quantize": round(flops / (step / 1e3) / 1e12, 2),
+                "gemm_tflops": round(flops / (per["gemm"] / 1e3) / 1e12, 2),
+                "gemm_frac_fp8_peak": round(flops / (per["gemm"] / 1e3) / 1e12 / fp8_peak, 4),
+                "gemm_gbs": round(gemm_bytes / (per["gemm"] / 1e3) / 1e9, 1),
+                "gemm_frac_hbm": round(gemm_bytes / (per["gemm"] / 1e3) / 1e9 / hbm, 4),
+                "quantize_gbs": round((m * K * 3 + asc.numel() * asc.element_size())
+                                      / (per["quantize"] / 1e3) / 1e9, 1),
+                "ms": {k: round(v, 4) for k, v in per.items()}}
+    del wd
+    # two-level microscaling GEMM, M = N = K = 8192
+    M = N = K = 8192
+    a, b = workloads.two_level(m=M, n=N, k=K)
+    ad, bd = a.to(dev), b.to(dev)
+    bufs = []
+    for t in (ad, bd):
+        bufs.append((t, torch.empty(1, device=dev), torch.empty(1, device=dev),
+                     torch.empty((M, K), dtype=torch.uint8, device=dev), F.mx_local_words(M, K, dev)))
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    fns = []
+    for t, am, gl, q, lw in bufs:
+        fns.append(("amax", lambda t=t, am=am: F.fp8_amax(t, am)))
+        fns.append(("quantize", lambda t=t, am=am, gl=gl, q=q, lw=lw:
+                    F.fp8_quantize_mx(t, F.E4M3, am, gl, q, lw)))
+    fns.append(("gemm", lambda: F.fp8_gemm_mx(bufs[0][3], bufs[0][4], bufs[0][2], bufs[1][3],
+                                              bufs[1][4], bufs[1][2], y)))
+    per, step = time_launches(fns, max(3, iters // 2), flush, stream)
+    flops = 2.0 * M * N * K
+    row = {"tflops_incl_quantize": round(flops / (step / 1e3) / 1e12, 2),
+           "gemm_tflops": round(flops / (per["gemm"] / 1e3) / 1e12, 2),
+           "gemm_frac_fp8_peak": round(flops / (per["gemm"] / 1e3) / 1e12 / fp8_peak, 4),
+           "quantize_gbs": round(M * K * (3 + 1 / 32) / (per["quantize"] / 1e3) / 1e9, 1),
+           "amax_gbs": round(M * K * 2 / (per["amax"] / 1e3) / 1e9, 1),
+           "ms": {k: round(v, 4) for k, v in per.items()}}
+    # SNR of A under the three granularities (dequantized from the kernels' codes)
+    e4 = torch.float8_e4m3fn
+    x = ad.float()
+    t, am, gl, q, lw = bufs[0]
+    loc = lw.view(torch.uint8).view(K // 128, -1, 4)  # [G, Rpad, 4] bytes in word order
+    rows_ = torch.arange(M, device=dev)
+    pos = (rows_ & ~127) + 4 * (rows_ % 32) + (rows_ % 128) // 32
+    r = loc[:, pos, :].permute(1, 0, 2).reshape(M, K // 32).float()
+    deq2 = q.view(e4).float().view(M, K // 32, 32) * (gl * torch.exp2(r - 127.0))[:, :, None]
+    qt = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    st = torch.empty(1, device=dev)
+    F.fp8_quantize_tensor(ad, F.E4M3, qt, amax_in=am, scale_out=st)
+    qg = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sg = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    F.fp8_quantize_token_group(ad, F.E4M3, F.SCALE_F32, qg, sg)
+    deqg = qg.view(e4).float().view(M, K // 128, 128) * sg.t()[:, :, None]
+    row["snr_db"] = {"per_tensor": round(snr_db_dev(x, qt.view(e4).float() * st), 3),
+                     "per_group_1x128": round(snr_db_dev(x, deqg.view(M, K)), 3),
+                     "two_level": round(snr_db_dev(x, deq2.view(M, K)), 3)}
+    out["two_level_8192"] = row
+    del ad, bd, bufs, x, deq2, deqg
+    # delayed-state update (1024-entry history)
+    hist = torch.zeros(1024, device=dev)
+    sc = torch.ones(1, device=dev)
+    cur = torch.full((1,), 3.0, device=dev)
+    per, _ = time_launches([("update", lambda: F.fp8_delayed_state_update(hist, sc, cur, F.E4M3))],
+                           iters, flush, stream)
+    out["delayed_state_update_L1024"] = {"us": round(per["update"] * 1e3, 2)}
+    return out
+
+
+def run_profile(args):
+    """The workload's launch sequence only (warmup + steps passes, no flush
+    buffer, no extras, no baselines): the command ncu captures use."""
+    import fp8_quantized_gemm_gb300 as F
+    dev, _, _ = setup_dist()
+    wl = Float8Linear(dev)
+    for _ in range(args.warmup + args.steps):
+        for _, fn in wl.launches():
+            fn()
+    torch.cuda.synchronize()
+    rc, where = F.fp8_get_last_device_error()
+    if rc != 0:
+        raise RuntimeError("device error %d (where %d)" % (rc, where))
+    print("profile run: %d passes of %d launches" % (args.warmup + args.steps, len(wl.launches())))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--profile", action="store_true",
+                    help="run the launch sequence only (for ncu captures); prints no bench line")
+    args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
