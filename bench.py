@@ -314,6 +314,39 @@ def time_workload(wl, steps, warmup, world, flush, stream):
     return timer, len(launches)
 
 
+def time_graph(wl, steps, world, flush):
+    """The same step captured once as a CUDA graph and replayed: the kernels
+    and their order are unchanged, the host launch gaps between them go."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _, fn in wl.launches():  # warm the capture stream
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _, fn in wl.launches():
+            fn()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    times = []
+    barrier(world)
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        graph.replay()
+        e.record(stream)
+        times.append((s, e))
+    torch.cuda.synchronize()
+    barrier(world)
+    return [s.elapsed_time(e) for s, e in times]
+
+
 def time_e2e(wl, steps, flush, stream):
     launches = wl.launches()
     times = []
@@ -357,8 +390,15 @@ def run_ours(args):
     if rc != 0:
         raise RuntimeError("device error %d (where %d) during the timed region" % (rc, where))
     step_ms = timer.step_ms()
-    total_ms = max_over_ranks(sum(step_ms), world)
-    value = wl.flops * args.steps * world / (total_ms / 1e3) / 1e12
+    eager_total_ms = max_over_ranks(sum(step_ms), world)
+    eager_value = wl.flops * args.steps * world / (eager_total_ms / 1e3) / 1e12
+    if args.eager:
+        total_ms, value = eager_total_ms, eager_value
+    else:
+        with ClockSampler(dev.index) as clk:
+            graph_ms = time_graph(wl, args.steps, world, flush)
+        total_ms = max_over_ranks(sum(graph_ms), world)
+        value = wl.flops * args.steps * world / (total_ms / 1e3) / 1e12
     per = timer.per_label_ms()
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # dense FP8 = 2 x bf16 (nominal ratio)
     gemm_ms = sum(per["gemm"]) / len(per["gemm"])
@@ -387,6 +427,9 @@ def run_ours(args):
                                             "measured HBM copy (%s)" % src),
         "amax_roofline": roofline_entry("hbm", a_gbs, peaks["hbm_gbs"], "GB/s",
                                         recorded_traffic("amax"), "measured HBM copy (%s)" % src),
+        "launch": "eager (one API call per kernel)" if args.eager else
+                  "CUDA graph of the step's API calls, replayed",
+        "eager": {"value": round(eager_value, 2), "ms_per_step": round(eager_total_ms / args.steps, 4)},
         "kernel_ms": {k: round(sum(v) / len(v), 4) for k, v in per.items()},
         "gpu_launches": n_launch * args.steps,
         "clocks": clk.summary(),
@@ -414,11 +457,13 @@ def run_reference(args):
     x, w, g = workloads.float8_linear()
     wl.host_in = [x, w, g]
     wl.name = Float8Linear.name
-    for _ in range(args.warmup and 1):
-        wl.oracle_sample(64)
+    # calibrate: size each step's sample so that the whole run takes ~2 min
+    _, dt_cal, _ = wl.oracle_sample(256)
+    per_row = dt_cal / 256
+    rows = int(min(8192, max(64, 120.0 / max(args.steps, 1) / per_row)) // 64 * 64)
     flops_total, secs, sample = 0.0, 0.0, ""
     for _ in range(args.steps):
-        f, dt, sample = wl.oracle_sample(args.cpu_rows)
+        f, dt, sample = wl.oracle_sample(rows)
         flops_total += f
         secs += dt
     value = flops_total / secs / 1e12
@@ -577,12 +622,13 @@ def run_profile(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager launches, not a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--profile", action="store_true",
                     help="run the launch sequence only (for ncu captures); prints no bench line")
     args = ap.parse_args()

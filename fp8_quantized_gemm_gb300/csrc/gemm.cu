@@ -49,7 +49,11 @@ struct Cfg {
   static constexpr uint32_t kSfbBytes = kBlockScaled ? BN * 4 : 0;
   static constexpr uint32_t kTileBytes = STAGES * (kABytes + kBBytes);
   static constexpr uint32_t kSfBytes = STAGES * (kSfaBytes + kSfbBytes);
-  static constexpr int kAccBufs = kPromote ? 4 : 1;
+  // TMEM accumulators: per-tensor mode double-buffers whole tiles (epilogue of
+  // one tile overlaps the MMAs of the next); the promotion mode rings four
+  // per-K-slice buffers; the block-scaled modes keep one tile buffer next to
+  // their per-stage scale-factor columns.
+  static constexpr int kAccBufs = kPromote ? 4 : (MODE == kScaleTensor ? 2 : 1);
   static constexpr uint32_t kAccCols = kAccBufs * BN;
   static constexpr uint32_t kSfColsPerStage = kBlockScaled ? 4 + BN / 32 : 0;
   static constexpr uint32_t kTmemCols = pow2_cols(kAccCols + STAGES * kSfColsPerStage);
@@ -159,123 +163,167 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int64_t m0 = (int64_t)blockIdx.y * C::BM;
-  const int64_t n0 = (int64_t)blockIdx.x * BN;
+  // Persistent tile loop: tile t covers rows (t / tiles_n) * 128 and columns
+  // (t % tiles_n) * BN; CTA b takes tiles b, b + gridDim.x, ...  Consecutive
+  // CTAs share an A row block (L2 reuse of A; B is read by every row block).
+  const int64_t tiles_n = (args.N + BN - 1) / BN;
+  const int64_t num_tiles = ((args.M + C::BM - 1) / C::BM) * tiles_n;
   const int KB = (int)((args.K + C::BK - 1) / C::BK);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int issued = 0;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t round = (uint32_t)(kb / STAGES);
-      if (!mbar_wait(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) break;
-      uint32_t tx = C::kABytes + C::kBBytes;
+    uint32_t it = 0;  // stage iterations issued, across tiles
+    bool ok = true;
+    // group-UE8M0 mode: the per-128 scale bytes of the NEXT stage are loaded
+    // into registers before waiting on the current stage, so their latency
+    // hides behind the wait instead of stalling every stage.
+    uint32_t sfa_cur[4] = {}, sfb_cur[BN / 32] = {}, sfa_nxt[4] = {}, sfb_nxt[BN / 32] = {};
+    auto load_sf = [&](int64_t t, int kb, uint32_t (&fa)[4], uint32_t (&fb)[BN / 32]) {
       if constexpr (MODE == kScaleGroupUe8m0) {
-        // per-128 UE8M0 byte -> word with the byte in all four 1x32 slots;
-        // word for row 32c + l of a 128-row chunk sits at index 4l + c
         const uint8_t *sa8 = static_cast<const uint8_t *>(args.sa);
         const uint8_t *sb8 = static_cast<const uint8_t *>(args.sb);
         const int64_t G = args.K / 128;
-        uint32_t *wa = reinterpret_cast<uint32_t *>(sSfa(s));
-        uint32_t *wb = reinterpret_cast<uint32_t *>(sSfb(s));
+        const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int64_t m = m0 + 32 * c + lane;
-          const uint32_t b = m < args.M ? sa8[(int64_t)kb * args.M + m] : 127u;
-          wa[4 * lane + c] = b * 0x01010101u;
+          fa[c] = m < args.M ? (uint32_t)__ldg(sa8 + (int64_t)kb * args.M + m) : 127u;
         }
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           const int64_t n = n0 + 32 * c + lane;
-          const uint32_t b = n < args.N ? sb8[(n >> 7) * G + kb] : 127u;
-          wb[(c >> 2) * 128 + 4 * lane + (c & 3)] = b * 0x01010101u;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      if (elect_one()) {
-        uint32_t sfb_bytes = 0;
-        if constexpr (MODE == kScaleMx) {
-          const int64_t npad = (args.N + 127) / 128 * 128;
-          const int64_t rows = (npad - n0) < BN ? (npad - n0) : BN;
-          sfb_bytes = (uint32_t)rows * 4u;
-          tx += C::kSfaBytes + sfb_bytes;
-        }
-        mbar_arrive_expect_tx(full_bar(s), tx);
-        tma_load_2d(sA(s), &tma, full_bar(s), kb * C::BK, (int32_t)m0);
-        tma_load_2d(sB(s), &tmb, full_bar(s), kb * C::BK, (int32_t)n0);
-        if constexpr (MODE == kScaleMx) {
-          const int64_t mpad = (args.M + 127) / 128 * 128;
-          const int64_t npad = (args.N + 127) / 128 * 128;
-          const uint32_t *la = static_cast<const uint32_t *>(args.sa) + (int64_t)kb * mpad + m0;
-          const uint32_t *lb = static_cast<const uint32_t *>(args.sb) + (int64_t)kb * npad + n0;
-          bulk_load(smem_u32(sSfa(s)), la, C::kSfaBytes, full_bar(s));
-          bulk_load(smem_u32(sSfb(s)), lb, sfb_bytes, full_bar(s));
+          fb[c] = n < args.N ? (uint32_t)__ldg(sb8 + (n >> 7) * G + kb) : 127u;
         }
       }
-      __syncwarp();
-      ++issued;
+    };
+    if constexpr (MODE == kScaleGroupUe8m0) {
+      if ((int64_t)blockIdx.x < num_tiles) load_sf(blockIdx.x, 0, sfa_cur, sfb_cur);
     }
-    if (*abort_flag) {
-      // let the copies already in flight land before the CTA can exit
-      if (lane == 0) {
-        const int first = issued > STAGES ? issued - STAGES : 0;
-        for (int i = first; i < issued; ++i)
-          drain_wait(full_bar(i % STAGES), (uint32_t)(i / STAGES) & 1u);
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = (int)(it % STAGES);
+        const uint32_t round = it / STAGES;
+        if constexpr (MODE == kScaleGroupUe8m0) {
+          const int64_t tn = kb + 1 < KB ? t : t + gridDim.x;
+          if (tn < num_tiles) load_sf(tn, kb + 1 < KB ? kb + 1 : 0, sfa_nxt, sfb_nxt);
+        }
+        if (!mbar_wait(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) {
+          ok = false;
+          break;
+        }
+        uint32_t tx = C::kABytes + C::kBBytes;
+        if constexpr (MODE == kScaleGroupUe8m0) {
+          // byte -> word with the byte in all four 1x32 slots; the word for
+          // row 32c + l of a 128-row chunk sits at index 4l + c
+          uint32_t *wa = reinterpret_cast<uint32_t *>(sSfa(s));
+          uint32_t *wb = reinterpret_cast<uint32_t *>(sSfb(s));
+#pragma unroll
+          for (int c = 0; c < 4; ++c) wa[4 * lane + c] = sfa_cur[c] * 0x01010101u;
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+            wb[(c >> 2) * 128 + 4 * lane + (c & 3)] = sfb_cur[c] * 0x01010101u;
+          fence_proxy_async_smem();
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) sfa_cur[c] = sfa_nxt[c];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) sfb_cur[c] = sfb_nxt[c];
+        }
+        if (elect_one()) {
+          uint32_t sfb_bytes = 0;
+          if constexpr (MODE == kScaleMx) {
+            const int64_t npad = (args.N + 127) / 128 * 128;
+            const int64_t rows = (npad - n0) < BN ? (npad - n0) : BN;
+            sfb_bytes = (uint32_t)rows * 4u;
+            tx += C::kSfaBytes + sfb_bytes;
+          }
+          mbar_arrive_expect_tx(full_bar(s), tx);
+          tma_load_2d(sA(s), &tma, full_bar(s), kb * C::BK, (int32_t)m0);
+          tma_load_2d(sB(s), &tmb, full_bar(s), kb * C::BK, (int32_t)n0);
+          if constexpr (MODE == kScaleMx) {
+            const int64_t mpad = (args.M + 127) / 128 * 128;
+            const int64_t npad = (args.N + 127) / 128 * 128;
+            const uint32_t *la = static_cast<const uint32_t *>(args.sa) + (int64_t)kb * mpad + m0;
+            const uint32_t *lb = static_cast<const uint32_t *>(args.sb) + (int64_t)kb * npad + n0;
+            bulk_load(smem_u32(sSfa(s)), la, C::kSfaBytes, full_bar(s));
+            bulk_load(smem_u32(sSfb(s)), lb, sfb_bytes, full_bar(s));
+          }
+        }
+        __syncwarp();
+        ++it;
       }
+    }
+    if (!ok && lane == 0) {
+      // let the copies already in flight land before the CTA can exit
+      const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+      for (uint32_t i = first; i < it; ++i) drain_wait(full_bar(i % STAGES), (i / STAGES) & 1u);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (elect_one()) {
+      uint32_t it = 0, j = 0;
       bool ok = true;
-      for (int kb = 0; kb < KB && ok; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t round = (uint32_t)(kb / STAGES);
-        if (!mbar_wait(full_bar(s), round & 1u, abort_flag, err, 2)) {
-          ok = false;
-          break;
-        }
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++j) {
         uint32_t d = tmem;
-        if constexpr (C::kPromote) {
-          const int buf = kb & 3;
-          const uint32_t use = (uint32_t)(kb >> 2);
-          if (!mbar_wait(acce_bar(buf), (use & 1u) ^ 1u, abort_flag, err, 2)) {
+        uint32_t tile_buf = 0;
+        if constexpr (!C::kPromote) {
+          tile_buf = j % C::kAccBufs;
+          const uint32_t use = j / C::kAccBufs;
+          if (!mbar_wait(acce_bar(tile_buf), (use & 1u) ^ 1u, abort_flag, err, 2)) {
             ok = false;
             break;
           }
-          d = tmem + (uint32_t)(buf * BN);
+          d = tmem + tile_buf * BN;
         }
-        tc_fence_after();
-        const uint64_t adesc = sdesc_sw128(sA(s));
-        const uint64_t bdesc = sdesc_sw128(sB(s));
-        if constexpr (C::kBlockScaled) {
-          const uint32_t sfa_col = C::kAccCols + (uint32_t)s * C::kSfColsPerStage;
-          const uint32_t sfb_col = sfa_col + 4;
-          tmem_cp_32x128b_warpx4(tmem + sfa_col, sdesc_plain(smem_u32(sSfa(s))));
-#pragma unroll
-          for (int j = 0; j < BN / 128; ++j)
-            tmem_cp_32x128b_warpx4(tmem + sfb_col + 4 * j, sdesc_plain(smem_u32(sSfb(s)) + 512 * j));
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t idesc = idesc_mxf8f6f4(128, BN, args.fa, args.fb, k, k);
-            mma_mxf8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + sfa_col,
-                         tmem + sfb_col, (kb | k) != 0 ? 1u : 0u);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          const uint32_t round = it / STAGES;
+          if (!mbar_wait(full_bar(s), round & 1u, abort_flag, err, 2)) {
+            ok = false;
+            break;
           }
-        } else {
-          const uint32_t idesc = idesc_f8f6f4(128, BN, args.fa, args.fb);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t acc = C::kPromote ? (k != 0) : ((kb | k) != 0);
-            mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc ? 1u : 0u);
+          if constexpr (C::kPromote) {
+            // one TMEM buffer per 128-wide K slice, four in a ring
+            const uint32_t buf = it & 3u, use = it >> 2;
+            if (!mbar_wait(acce_bar(buf), (use & 1u) ^ 1u, abort_flag, err, 2)) {
+              ok = false;
+              break;
+            }
+            d = tmem + buf * BN;
           }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_sw128(sA(s));
+          const uint64_t bdesc = sdesc_sw128(sB(s));
+          if constexpr (C::kBlockScaled) {
+            const uint32_t sfa_col = C::kAccCols + (uint32_t)s * C::kSfColsPerStage;
+            const uint32_t sfb_col = sfa_col + 4;
+            tmem_cp_32x128b_warpx4(tmem + sfa_col, sdesc_plain(smem_u32(sSfa(s))));
+#pragma unroll
+            for (int jj = 0; jj < BN / 128; ++jj)
+              tmem_cp_32x128b_warpx4(tmem + sfb_col + 4 * jj,
+                                     sdesc_plain(smem_u32(sSfb(s)) + 512 * jj));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t idesc = idesc_mxf8f6f4(128, BN, args.fa, args.fb, k, k);
+              mma_mxf8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + sfa_col,
+                           tmem + sfb_col, (kb | k) != 0 ? 1u : 0u);
+            }
+          } else {
+            const uint32_t idesc = idesc_f8f6f4(128, BN, args.fa, args.fb);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const bool acc = C::kPromote ? (k != 0) : ((kb | k) != 0);
+              mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc ? 1u : 0u);
+            }
+          }
+          mma_commit(empty_bar(s));
+          if constexpr (C::kPromote) mma_commit(accf_bar(it & 3u));
         }
-        mma_commit(empty_bar(s));
-        if constexpr (C::kPromote) mma_commit(accf_bar(kb & 3));
+        if (!ok) break;
+        if constexpr (!C::kPromote) mma_commit(accf_bar(tile_buf));
       }
-      if (ok) {
-        if constexpr (!C::kPromote) mma_commit(accf_bar(0));
-      } else {
+      if (!ok) {
         mma_commit(drain_bar);
         drain_wait(drain_bar, 0);
       }
@@ -284,20 +332,29 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const uint32_t q = warp & 3u;
-    const int64_t row = m0 + 32 * q + lane;
     const uint32_t lane_base = tmem + ((32u * q) << 16);
     if constexpr (!C::kPromote) {
-      if (mbar_wait(accf_bar(0), 0, abort_flag, err, 3)) {
+      float alpha = 1.0f;
+      if constexpr (MODE == kScaleTensor)
+        alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
+      if constexpr (MODE == kScaleMx) alpha = *args.ga * *args.gb;
+      uint32_t j = 0;
+      for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
+        const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
+        const int64_t row = m0 + 32 * q + lane;
+        const uint32_t buf = j % C::kAccBufs, use = j / C::kAccBufs;
+        if (!mbar_wait(accf_bar(buf), use & 1u, abort_flag, err, 3)) break;
         tc_fence_after();
-        float alpha = 1.0f;
-        if constexpr (MODE == kScaleTensor)
-          alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
-        if constexpr (MODE == kScaleMx) alpha = *args.ga * *args.gb;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
-          FP8K_TMEM_LD_X32(lane_base + (uint32_t)c, r);
+          FP8K_TMEM_LD_X32(lane_base + buf * BN + (uint32_t)c, r);
           tmem_ld_wait();
+          if (c + 32 == BN) {  // accumulator fully read: hand it back to the MMA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(buf));
+          }
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
@@ -309,36 +366,41 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       const float *sa = static_cast<const float *>(args.sa);
       const float *sb = static_cast<const float *>(args.sb);
       const int64_t G = args.K / 128;
-      const float *sb_row = sb + (n0 >> 7) * G;
-      float acc[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-      float sa_next = row < args.M ? __ldg(sa + row) : 0.0f;
+      uint32_t it = 0;
       bool ok = true;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int buf = kb & 3;
-        const float s_cur = sa_next * __ldg(sb_row + kb);
-        if (kb + 1 < KB) sa_next = row < args.M ? __ldg(sa + (int64_t)(kb + 1) * args.M + row) : 0.0f;
-        if (!mbar_wait(accf_bar(buf), (uint32_t)(kb >> 2) & 1u, abort_flag, err, 3)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t r0[32], r1[32];
-        const uint32_t col = (uint32_t)(buf * BN + h * 64);
-        FP8K_TMEM_LD_X32(lane_base + col, r0);
-        FP8K_TMEM_LD_X32(lane_base + col + 32, r1);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acce_bar(buf));
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
+        const int64_t row = m0 + 32 * q + lane;
+        const float *sb_row = sb + (n0 >> 7) * G;
+        float acc[64];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          acc[i] = fmaf(s_cur, __uint_as_float(r0[i]), acc[i]);
-          acc[32 + i] = fmaf(s_cur, __uint_as_float(r1[i]), acc[32 + i]);
+        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        float sa_next = row < args.M ? __ldg(sa + row) : 0.0f;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const uint32_t buf = it & 3u, use = it >> 2;
+          const float s_cur = sa_next * __ldg(sb_row + kb);
+          if (kb + 1 < KB)
+            sa_next = row < args.M ? __ldg(sa + (int64_t)(kb + 1) * args.M + row) : 0.0f;
+          if (!mbar_wait(accf_bar(buf), use & 1u, abort_flag, err, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t r0[32], r1[32];
+          const uint32_t col = buf * BN + (uint32_t)(h * 64);
+          FP8K_TMEM_LD_X32(lane_base + col, r0);
+          FP8K_TMEM_LD_X32(lane_base + col + 32, r1);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acce_bar(buf));
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            acc[i] = fmaf(s_cur, __uint_as_float(r0[i]), acc[i]);
+            acc[32 + i] = fmaf(s_cur, __uint_as_float(r1[i]), acc[32 + i]);
+          }
         }
-      }
-      if (ok) {
+        if (!ok) break;
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = acc[i];
@@ -357,12 +419,22 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
 
 template <int MODE, int BN, int STAGES>
 static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
-                       cudaStream_t st) {
+                       int sms, cudaStream_t st) {
   using C = Cfg<MODE, BN, STAGES>;
   auto kern = gemm_kernel<MODE, BN, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+  // the shared-memory opt-in is set once per device (not inside a capture)
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((args.N + BN - 1) / BN), (unsigned)((args.M + C::BM - 1) / C::BM));
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int64_t tiles = ((args.M + C::BM - 1) / C::BM) * ((args.N + BN - 1) / BN);
+  const int grid = (int)(tiles < sms ? tiles : sms);
   kern<<<grid, C::kThreads, C::kSmem, st>>>(tma, tmb, args);
   return cudaGetLastError();
 }
@@ -371,12 +443,11 @@ int gemm_tile_n(int mode) { return mode == kScaleGroupF32 ? 128 : 256; }
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,
                         const GemmArgs &args, int sms, cudaStream_t st) {
-  (void)sms;
   switch (mode) {
-    case kScaleTensor: return run<kScaleTensor, 256, 4>(tma, tmb, args, st);
-    case kScaleMx: return run<kScaleMx, 256, 4>(tma, tmb, args, st);
-    case kScaleGroupUe8m0: return run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, st);
-    case kScaleGroupF32: return run<kScaleGroupF32, 128, 6>(tma, tmb, args, st);
+    case kScaleTensor: return run<kScaleTensor, 256, 4>(tma, tmb, args, sms, st);
+    case kScaleMx: return run<kScaleMx, 256, 4>(tma, tmb, args, sms, st);
+    case kScaleGroupUe8m0: return run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, sms, st);
+    case kScaleGroupF32: return run<kScaleGroupF32, 128, 6>(tma, tmb, args, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -53,6 +53,40 @@ struct Vec8<float> {
   }
 };
 
+// Raw 16-byte vectors holding 8 elements (bf16: one uint4; f32: two), kept
+// undecoded in registers until used.
+template <typename T>
+struct Raw8 {
+  static constexpr int kWords = sizeof(T) * 8 / 16;
+  uint4 w[kWords];
+  __device__ __forceinline__ void load_stream(const T *p) {
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) w[i] = __ldcs(reinterpret_cast<const uint4 *>(p) + i);
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __device__ __forceinline__ void decode(float (&v)[8]) const {
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t u[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(u[i] << 16);
+        v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        v[4 * i] = __uint_as_float(w[i].x);
+        v[4 * i + 1] = __uint_as_float(w[i].y);
+        v[4 * i + 2] = __uint_as_float(w[i].z);
+        v[4 * i + 3] = __uint_as_float(w[i].w);
+      }
+    }
+  }
+};
+
 template <typename T>
 __device__ __forceinline__ float load1(const T *p);
 template <>
@@ -90,7 +124,18 @@ __global__ void __launch_bounds__(512) amax_kernel(const T *__restrict__ x, int6
   uint32_t key = 0;
   const int64_t nvec = n / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // four independent 16-byte loads in flight per thread
+  for (; i + 3 * stride < nvec; i += 4 * stride) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) Vec8<T>::load(x + (i + u * stride) * 8, v[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[u][j]));
+  }
+  for (; i < nvec; i += stride) {
     float v[8];
     Vec8<T>::load(x + i * 8, v);
 #pragma unroll
@@ -119,7 +164,23 @@ __global__ void __launch_bounds__(512)
   uint32_t key = 0;
   const int64_t nvec = n / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < nvec; i += 4 * stride) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) Vec8<T>::load_stream(x + (i + u * stride) * 8, v[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        key = max(key, abs_key(v[u][j]));
+        y[j] = q_prep(v[u][j], s, mx);
+      }
+      reinterpret_cast<uint2 *>(q)[i + u * stride] = pack8(fmt, y);
+    }
+  }
+  for (; i < nvec; i += stride) {
     float v[8], y[8];
     Vec8<T>::load_stream(x + i * 8, v);
 #pragma unroll
@@ -162,23 +223,32 @@ __global__ void __launch_bounds__(256)
   const int64_t r0 = (int64_t)blockIdx.y * kTT, c0 = (int64_t)blockIdx.x * kTT;
   const int t = threadIdx.x;
   uint32_t key = 0;
-  // phase 1: 16 vectors of 8 per tile row; 256 threads cover 16 rows per pass
-#pragma unroll 2
-  for (int pass = 0; pass < kTT / 16; ++pass) {
-    const int lr = pass * 16 + (t >> 4), lc = (t & 15) * 8;
-    const int64_t r = r0 + lr, c = c0 + lc;
-    uint2 packed = make_uint2(0u, 0u);
-    if (r < rows && c < cols) {
-      float v[8], y[8];
-      Vec8<T>::load_stream(x + r * cols + c, v);
+  // phase 1: 16 vectors of 8 per tile row; 256 threads cover 16 rows per
+  // pass.  All eight loads of the thread are issued before any is used.
+  const int lc = (t & 15) * 8;
+  const int64_t c = c0 + lc;
+  Raw8<T> raw[kTT / 16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        key = max(key, abs_key(v[j]));
-        y[j] = q_prep(v[j], s, mx);
-      }
-      packed = pack8(fmt, y);
-      *reinterpret_cast<uint2 *>(q + r * cols + c) = packed;
+  for (int pass = 0; pass < kTT / 16; ++pass) {
+    const int64_t r = r0 + pass * 16 + (t >> 4);
+    if (r < rows && c < cols)
+      raw[pass].load_stream(x + r * cols + c);
+    else
+      raw[pass].zero();
+  }
+#pragma unroll
+  for (int pass = 0; pass < kTT / 16; ++pass) {
+    const int lr = pass * 16 + (t >> 4);
+    const int64_t r = r0 + lr;
+    float v[8], y[8];
+    raw[pass].decode(v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      key = max(key, abs_key(v[j]));
+      y[j] = q_prep(v[j], s, mx);
     }
+    const uint2 packed = pack8(fmt, y);
+    if (r < rows && c < cols) *reinterpret_cast<uint2 *>(q + r * cols + c) = packed;
     *reinterpret_cast<uint2 *>(&tile[lr * kTPitch + tchunk(lr, lc >> 3)]) = packed;
   }
   __syncthreads();
