@@ -71,7 +71,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -206,6 +206,33 @@ class Float8Linear:
                                                self.dw)),
         ]
 
+    def capture_branches(self):
+        """The step as a graph with independent branches on forked streams:
+        the three amax -> quantize chains run side by side, then y, dx and dW
+        (each needs two of the quantized operands) run side by side."""
+        L = dict((i, fn) for i, (_, fn) in enumerate(self.launches()))
+        main = torch.cuda.current_stream()
+        side = [torch.cuda.Stream() for _ in range(2)]
+        for st in side:
+            st.wait_stream(main)
+        # quantize chains: x on main, W and g on the side streams
+        L[0](); L[3]()
+        with torch.cuda.stream(side[0]):
+            L[1](); L[4]()
+        with torch.cuda.stream(side[1]):
+            L[2](); L[5]()
+        for st in side:
+            main.wait_stream(st)
+            st.wait_stream(main)
+        # GEMMs: y on main, dx and dW on the side streams
+        with torch.cuda.stream(side[0]):
+            L[7]()
+        with torch.cuda.stream(side[1]):
+            L[8]()
+        L[6]()
+        for st in side:
+            main.wait_stream(st)
+
     def upload(self, stream):
         for h, d in zip(self.host_in, (self.x, self.w, self.g)):
             d.copy_(h, non_blocking=True)
@@ -314,6 +341,24 @@ def time_workload(wl, steps, warmup, world, flush, stream):
     return timer, len(launches)
 
 
+def time_isolated(wl, reps, flush, stream):
+    """Device time of each launch on its own: the 512 MiB flush queued before
+    every launch keeps the GPU busy while the host enqueues the launch, so the
+    events bracket the kernel alone, on a cold L2."""
+    per = {}
+    launches = wl.launches()
+    for _ in range(reps):
+        for label, fn in launches:
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            per.setdefault(label, []).append((s, e))
+    torch.cuda.synchronize()
+    return {k: [s.elapsed_time(e) for s, e in v] for k, v in per.items()}
+
+
 def time_graph(wl, steps, world, flush):
     """The same step captured once as a CUDA graph and replayed: the kernels
     and their order are unchanged, the host launch gaps between them go."""
@@ -326,8 +371,11 @@ def time_graph(wl, steps, world, flush):
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        for _, fn in wl.launches():
-            fn()
+        if hasattr(wl, "capture_branches"):
+            wl.capture_branches()
+        else:
+            for _, fn in wl.launches():
+                fn()
     for _ in range(3):
         graph.replay()
     torch.cuda.synchronize()
@@ -365,8 +413,12 @@ def time_e2e(wl, steps, flush, stream):
     return times
 
 
-def cpu_baseline(wl, rows):
-    flops, dt, sample = wl.oracle_sample(rows)
+def cpu_baseline(wl, rows, min_seconds=10.0, max_reps=8):
+    flops, dt, reps = 0.0, 0.0, 0
+    while reps < max_reps and (dt < min_seconds or reps == 0):
+        f, d, sample = wl.oracle_sample(rows)
+        flops, dt, reps = flops + f, dt + d, reps + 1
+    sample = "%s; %d repetition(s)" % (sample, reps)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": sample, "seconds": round(dt, 3)}
@@ -399,7 +451,7 @@ def run_ours(args):
             graph_ms = time_graph(wl, args.steps, world, flush)
         total_ms = max_over_ranks(sum(graph_ms), world)
         value = wl.flops * args.steps * world / (total_ms / 1e3) / 1e12
-    per = timer.per_label_ms()
+    per = time_isolated(wl, 10, flush, stream)
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # dense FP8 = 2 x bf16 (nominal ratio)
     gemm_ms = sum(per["gemm"]) / len(per["gemm"])
     gemm_tflops = (wl.flops / 3) / (gemm_ms / 1e3) / 1e12
@@ -431,6 +483,7 @@ def run_ours(args):
                   "CUDA graph of the step's API calls, replayed",
         "eager": {"value": round(eager_value, 2), "ms_per_step": round(eager_total_ms / args.steps, 4)},
         "kernel_ms": {k: round(sum(v) / len(v), 4) for k, v in per.items()},
+        "kernel_timing": "each launch alone after a 512 MiB flush (cold L2), CUDA events",
         "gpu_launches": n_launch * args.steps,
         "clocks": clk.summary(),
     }
@@ -488,24 +541,30 @@ def run_reference(args):
 # ------------------------------------------------------- other workloads --
 
 def time_launches(fns, iters, flush, stream, warmup=3):
-    """Mean ms per label and per pass of `fns`, L2 flushed before each pass."""
+    """Mean device ms of each launch, each timed alone after a 512 MiB flush
+    (cold L2; the host enqueues the launch while the flush runs), and their
+    sum as the time of one pass."""
     for _ in range(warmup):
         for _, fn in fns:
             fn()
     torch.cuda.synchronize()
-    timer = StepTimer()
+    rec = {}
     for _ in range(iters):
-        flush.zero_()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
         for label, fn in fns:
-            timer.launch(label, fn, stream)
-        e.record(stream)
-        timer.steps.append((s, e))
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            rec.setdefault(label, []).append((s, e))
     torch.cuda.synchronize()
-    per = {k: sum(v) / len(v) for k, v in timer.per_label_ms().items()}
-    steps = timer.step_ms()
-    return per, sum(steps) / len(steps)
+    per = {k: sum(s.elapsed_time(e) for s, e in v) / len(v) for k, v in rec.items()}
+    count = {}
+    for label, _ in fns:
+        count[label] = count.get(label, 0) + 1
+    per = {k: v for k, v in per.items()}
+    step = sum(per[k] * count[k] for k in per)
+    return per, step
 
 
 def snr_db_dev(x, xhat):
@@ -622,7 +681,7 @@ def run_profile(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")

@@ -7,7 +7,9 @@
 // a device).
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "fp8gemm.h"
 #include "kernels.h"
@@ -29,6 +31,18 @@ struct DeviceState {
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+
+// Split-K scratch of the small-M GEMM path, one per (device, stream) so that
+// calls on different streams never share it.  Layout: uint32 arrival
+// counters (one per output tile, zero between calls) in the first
+// kCounterBytes, then the fp32 partials [ksplit][M][N].  Allocated (zeroed) on
+// first need and grown by doubling; never inside a stream capture.
+constexpr size_t kCounterBytes = 64 * 1024;
+struct Workspace {
+  void *ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
@@ -99,11 +113,46 @@ int vector_store_ok(const void *c, int64_t ldc, int out_dt) {
   return aligned16(c) && (ldc * es) % 16 == 0 ? 1 : 0;
 }
 
+int get_workspace(cudaStream_t st, size_t need, void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP8_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace &w = g_ws[std::make_pair(dev, st)];
+  if (w.bytes < need) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return FP8_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return FP8_ERR_UNSUPPORTED;  // warm up before capture
+    if (w.ptr != nullptr) {
+      if (cudaStreamSynchronize(st) != cudaSuccess || cudaFree(w.ptr) != cudaSuccess)
+        return FP8_ERR_CUDA;
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    size_t bytes = need > 2 * w.bytes ? need : 2 * w.bytes;
+    bytes = (bytes + (1u << 20) - 1) & ~(size_t)((1u << 20) - 1);
+    if (cudaMalloc(&w.ptr, bytes) != cudaSuccess) return FP8_ERR_CUDA;
+    if (cudaMemset(w.ptr, 0, bytes) != cudaSuccess) return FP8_ERR_CUDA;
+    w.bytes = bytes;
+  }
+  *out = w.ptr;
+  return FP8_OK;
+}
+
 int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaStream_t st) {
   DeviceState *d = nullptr;
   int rc = device_state(&d);
   if (rc != FP8_OK) return rc;
   args.err = d->err;
+  args.ksplit = fp8k::gemm_ksplit(mode, args.M, args.N, args.K, d->sms);
+  args.ws = nullptr;
+  args.counters = nullptr;
+  if (args.ksplit > 1) {
+    const size_t need = kCounterBytes + (size_t)args.ksplit * args.M * args.N * sizeof(float);
+    void *w = nullptr;
+    if ((rc = get_workspace(st, need, &w)) != FP8_OK) return rc;
+    args.counters = static_cast<uint32_t *>(w);
+    args.ws = reinterpret_cast<float *>(static_cast<char *>(w) + kCounterBytes);
+  }
   args.vec_store = vector_store_ok(args.c, args.ldc, args.out_dt);
   CUtensorMap tma, tmb;
   if ((rc = encode_operand(&tma, a, args.K, args.M, 128)) != FP8_OK) return rc;
@@ -314,6 +363,14 @@ int fp8_get_last_device_error(int *where_out, fp8_stream_t stream) {
   if (h[0] != 0) {
     const uint32_t z[2] = {0, 0};
     if (cudaMemcpy(d->err, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FP8_ERR_CUDA;
+    // an aborted kernel may have left split-K arrival counters non-zero
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto &kv : g_ws)
+      if (kv.first.first == dev && kv.second.ptr != nullptr &&
+          cudaMemset(kv.second.ptr, 0, kCounterBytes) != cudaSuccess)
+        return FP8_ERR_CUDA;
   }
   if (where_out != nullptr) *where_out = (int)h[1];
   return -(int)h[0];

@@ -112,6 +112,48 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Split-K workspace: 32 fp32 partial sums of one row for split `split`.
+__device__ __forceinline__ void store_partial32(const GemmArgs &a, int split, int64_t row,
+                                                int64_t col0, const float (&v)[32]) {
+  if (row >= a.M || col0 >= a.N) return;
+  float *dst = a.ws + ((int64_t)split * a.M + row) * a.N + col0;
+  if (col0 + 32 <= a.N && (a.N & 3) == 0) {
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) __stcg(d4 + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+  } else {
+    for (int i = 0; i < 32 && col0 + i < a.N; ++i) __stcg(dst + i, v[i]);
+  }
+}
+
+// Sum over the splits, in split order, of 32 partials of one row.
+__device__ __forceinline__ void sum_partials32(const GemmArgs &a, int64_t row, int64_t col0,
+                                               float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+  if (row >= a.M || col0 >= a.N) return;
+  const bool vec = col0 + 32 <= a.N && (a.N & 3) == 0;
+  for (int sp = 0; sp < a.ksplit; ++sp) {
+    const float *src = a.ws + ((int64_t)sp * a.M + row) * a.N + col0;
+    if (vec) {
+      const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 p = __ldcg(s4 + i);
+        v[4 * i] += p.x; v[4 * i + 1] += p.y; v[4 * i + 2] += p.z; v[4 * i + 3] += p.w;
+      }
+    } else {
+      for (int i = 0; i < 32 && col0 + i < a.N; ++i) v[i] += __ldcg(src + i);
+    }
+  }
+}
+
+// Barrier among the epilogue warps only (named barrier 1).
+template <int kThreadsEpi>
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kThreadsEpi) : "memory");
+}
+
 template <int MODE, int BN, int STAGES>
 __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
@@ -169,6 +211,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   const int64_t tiles_n = (args.N + BN - 1) / BN;
   const int64_t num_tiles = ((args.M + C::BM - 1) / C::BM) * tiles_n;
   const int KB = (int)((args.K + C::BK - 1) / C::BK);
+  // work unit u = (tile u % num_tiles, K split u / num_tiles); with ksplit 1
+  // units are tiles.  Split s covers k blocks [s*KB/ks, (s+1)*KB/ks).
+  const int ks = args.ksplit;
+  const int64_t num_units = num_tiles * ks;
+  auto unit_tile = [&](int64_t u) { return u % num_tiles; };
+  auto kb_begin = [&](int64_t u) { return (int)((u / num_tiles) * KB / ks); };
+  auto kb_end = [&](int64_t u) { return (int)((u / num_tiles + 1) * KB / ks); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -197,16 +246,20 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       }
     };
     if constexpr (MODE == kScaleGroupUe8m0) {
-      if ((int64_t)blockIdx.x < num_tiles) load_sf(blockIdx.x, 0, sfa_cur, sfb_cur);
+      if ((int64_t)blockIdx.x < num_units)
+        load_sf(unit_tile(blockIdx.x), kb_begin(blockIdx.x), sfa_cur, sfb_cur);
     }
-    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const int64_t t = unit_tile(u);
       const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
-      for (int kb = 0; kb < KB; ++kb) {
+      const int kb1 = kb_end(u);
+      for (int kb = kb_begin(u); kb < kb1; ++kb) {
         const int s = (int)(it % STAGES);
         const uint32_t round = it / STAGES;
         if constexpr (MODE == kScaleGroupUe8m0) {
-          const int64_t tn = kb + 1 < KB ? t : t + gridDim.x;
-          if (tn < num_tiles) load_sf(tn, kb + 1 < KB ? kb + 1 : 0, sfa_nxt, sfb_nxt);
+          const int64_t un = kb + 1 < kb1 ? u : u + gridDim.x;
+          if (un < num_units)
+            load_sf(unit_tile(un), kb + 1 < kb1 ? kb + 1 : kb_begin(un), sfa_nxt, sfb_nxt);
         }
         if (!mbar_wait(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) {
           ok = false;
@@ -264,8 +317,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     if (elect_one()) {
       uint32_t it = 0, j = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++j) {
+      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++j) {
         uint32_t d = tmem;
+        const int kb0 = kb_begin(u), kb1 = kb_end(u);
         uint32_t tile_buf = 0;
         if constexpr (!C::kPromote) {
           tile_buf = j % C::kAccBufs;
@@ -276,7 +330,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
           }
           d = tmem + tile_buf * BN;
         }
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = (int)(it % STAGES);
           const uint32_t round = it / STAGES;
           if (!mbar_wait(full_bar(s), round & 1u, abort_flag, err, 2)) {
@@ -307,13 +361,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
             for (int k = 0; k < 4; ++k) {
               const uint32_t idesc = idesc_mxf8f6f4(128, BN, args.fa, args.fb, k, k);
               mma_mxf8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + sfa_col,
-                           tmem + sfb_col, (kb | k) != 0 ? 1u : 0u);
+                           tmem + sfb_col, (kb != kb0 || k != 0) ? 1u : 0u);
             }
           } else {
             const uint32_t idesc = idesc_f8f6f4(128, BN, args.fa, args.fb);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const bool acc = C::kPromote ? (k != 0) : ((kb | k) != 0);
+              const bool acc = C::kPromote ? (k != 0) : (kb != kb0 || k != 0);
               mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc ? 1u : 0u);
             }
           }
@@ -331,6 +385,23 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // Split-K arrival: every epilogue thread has written (and fenced) its
+    // partials; one thread counts the split in; the last of the tile's splits
+    // reduces, then resets the counter for the next call.
+    __shared__ int split_last;
+    auto finish_split = [&](int64_t t) -> bool {
+      __threadfence();
+      epi_sync<C::kEpiWarps * 32>();
+      if (threadIdx.x == 64) {
+        const uint32_t old = atomicAdd(args.counters + t, 1u);
+        split_last = (old == (uint32_t)(ks - 1));
+        if (split_last) args.counters[t] = 0u;
+      }
+      epi_sync<C::kEpiWarps * 32>();
+      const bool last = split_last != 0;
+      if (last) __threadfence();
+      return last;
+    };
     const uint32_t q = warp & 3u;
     const uint32_t lane_base = tmem + ((32u * q) << 16);
     if constexpr (!C::kPromote) {
@@ -339,7 +410,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
         alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
       if constexpr (MODE == kScaleMx) alpha = *args.ga * *args.gb;
       uint32_t j = 0;
-      for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++j) {
+      for (int64_t u = blockIdx.x; u < num_units; u += gridDim.x, ++j) {
+        const int64_t t = unit_tile(u);
+        const int split = (int)(u / num_tiles);
         const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
         const int64_t row = m0 + 32 * q + lane;
         const uint32_t buf = j % C::kAccBufs, use = j / C::kAccBufs;
@@ -356,9 +429,25 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
             if (lane == 0) mbar_arrive(acce_bar(buf));
           }
           float v[32];
+          if (ks == 1) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
-          store_row32(args, row, n0 + c, v);
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
+            store_row32(args, row, n0 + c, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            store_partial32(args, split, row, n0 + c, v);
+          }
+        }
+        if (ks > 1 && finish_split(t)) {
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {
+            float v[32];
+            sum_partials32(args, row, n0 + c, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            store_row32(args, row, n0 + c, v);
+          }
         }
       }
     } else {
@@ -368,18 +457,21 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       const int64_t G = args.K / 128;
       uint32_t it = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const int64_t t = unit_tile(u);
+        const int split = (int)(u / num_tiles);
+        const int kb0 = kb_begin(u), kb1 = kb_end(u);
         const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
         const int64_t row = m0 + 32 * q + lane;
         const float *sb_row = sb + (n0 >> 7) * G;
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-        float sa_next = row < args.M ? __ldg(sa + row) : 0.0f;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        float sa_next = row < args.M ? __ldg(sa + (int64_t)kb0 * args.M + row) : 0.0f;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t buf = it & 3u, use = it >> 2;
           const float s_cur = sa_next * __ldg(sb_row + kb);
-          if (kb + 1 < KB)
+          if (kb + 1 < kb1)
             sa_next = row < args.M ? __ldg(sa + (int64_t)(kb + 1) * args.M + row) : 0.0f;
           if (!mbar_wait(accf_bar(buf), use & 1u, abort_flag, err, 3)) {
             ok = false;
@@ -404,10 +496,18 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = acc[i];
-        store_row32(args, row, n0 + h * 64, v);
+        if (ks == 1) store_row32(args, row, n0 + h * 64, v);
+        else store_partial32(args, split, row, n0 + h * 64, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = acc[32 + i];
-        store_row32(args, row, n0 + h * 64 + 32, v);
+        if (ks == 1) store_row32(args, row, n0 + h * 64 + 32, v);
+        else store_partial32(args, split, row, n0 + h * 64 + 32, v);
+        if (ks > 1 && finish_split(t)) {
+          sum_partials32(args, row, n0 + h * 64, v);
+          store_row32(args, row, n0 + h * 64, v);
+          sum_partials32(args, row, n0 + h * 64 + 32, v);
+          store_row32(args, row, n0 + h * 64 + 32, v);
+        }
       }
     }
   }
@@ -433,13 +533,25 @@ static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const Gem
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const int64_t tiles = ((args.M + C::BM - 1) / C::BM) * ((args.N + BN - 1) / BN);
-  const int grid = (int)(tiles < sms ? tiles : sms);
+  const int64_t units = ((args.M + C::BM - 1) / C::BM) * ((args.N + BN - 1) / BN) * args.ksplit;
+  const int grid = (int)(units < sms ? units : sms);
   kern<<<grid, C::kThreads, C::kSmem, st>>>(tma, tmb, args);
   return cudaGetLastError();
 }
 
 int gemm_tile_n(int mode) { return mode == kScaleGroupF32 ? 128 : 256; }
+
+// Split K when the tiles cannot fill half the SMs: as many splits as fit the
+// SMs, each covering at least four 128-wide K blocks.
+int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms) {
+  const int64_t bn = gemm_tile_n(mode);
+  const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+  const int64_t kb = (K + 127) / 128;
+  if (tiles * 2 > sms || kb < 8) return 1;
+  int64_t ks = sms / tiles;
+  if (ks > kb / 4) ks = kb / 4;
+  return ks < 2 ? 1 : (int)ks;
+}
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,
                         const GemmArgs &args, int sms, cudaStream_t st) {

@@ -43,7 +43,16 @@ struct GemmArgs {
   const void *sa, *sb;         // scale operands (meaning depends on the mode)
   const float *ga, *gb;        // global factors (kScaleMx)
   uint32_t *err;               // device error word
+  // split-K (small M): ksplit > 1 splits every tile's K range; fp32 partials
+  // go to ws [ksplit][M][N] and counters[tile] counts finished splits (the
+  // last one reduces in split order and resets the counter to 0)
+  int ksplit;
+  float *ws;
+  uint32_t *counters;
 };
+
+// Split count the launcher would use for this shape (1 = no split).
+int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms);
 
 // Output-tile width (N) of each mode; the B tensor map's box uses it.
 int gemm_tile_n(int mode);

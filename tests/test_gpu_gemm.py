@@ -197,3 +197,60 @@ def test_gemm_mx_distinct_local_factors():
     c, e = mx_reference(qa, la, ga, qb, lb, gb)
     ok, worst = OG.check(got, c, e, "f32")
     assert ok, worst
+
+
+# ------------------------------------------------------- split K (small M) --
+
+@pytest.mark.parametrize("m", [1, 7, 64, 128])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_gemm_group_small_m_split_k(m, sfmt):
+    """Config-3 shapes at decode-like M: the tiles cannot fill the GPU, so K is
+    split across CTAs and the last CTA of each tile reduces the fp32 partials.
+    Two calls in a row: the arrival counters must be back at zero."""
+    n, k = 2048, 7168
+    qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=2)
+    c, e = group_reference(qa, sa, qb, sb, sfmt)
+    for _ in range(2):
+        got = run_group(qa, sa, qb, sb, sfmt)
+        ok, worst = OG.check(got, c, e, "bf16")
+        assert ok, worst
+
+
+@pytest.mark.parametrize("mnk", [(1, 2048, 4096), (100, 256, 8192), (33, 1000, 2048)])
+def test_gemm_tensor_small_m_split_k(mnk):
+    m, n, k = mnk
+    qa, sa, qb, sb = per_tensor_operands(m, n, k, "e5m2", "e4m3", seed=m)
+    c, e = OG.gemm(OG.dequant_operand(qa, "e5m2", sa), OG.dequant_operand(qb, "e4m3", sb))
+    for out_dtype in ("f32", "bf16"):
+        got = run_tensor(qa, "e5m2", sa, qb, "e4m3", sb, out_dtype)
+        ok, worst = OG.check(got, c, e, out_dtype)
+        assert ok, (out_dtype, worst)
+
+
+def test_gemm_mx_small_m_split_k():
+    qa, la, ga, qb, lb, gb = mx_operands(1, 1024, 4096, seed=7)
+    c, e = mx_reference(qa, la, ga, qb, lb, gb)
+    got = run_mx(qa, la, ga, qb, lb, gb, "bf16")
+    ok, worst = OG.check(got, c, e, "bf16")
+    assert ok, worst
+
+
+def test_split_k_on_two_streams():
+    """Each stream has its own split-K scratch: interleaved calls on two
+    streams give the same results as calls on one."""
+    F = lib()
+    m, n, k = 16, 2048, 7168
+    qa, sa, qb, sb = group_operands(m, n, k, "f32", seed=4)
+    c, e = group_reference(qa, sa, qb, sb, "f32")
+    a_d, b_d = dev_u8(qa), dev_u8(qb)
+    sa_d = torch.from_numpy(np.ascontiguousarray(np.asarray(sa).T)).cuda()
+    sb_d = torch.from_numpy(np.ascontiguousarray(np.asarray(sb))).cuda()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = [torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        F.fp8_gemm_group(a_d, sa_d, b_d, sb_d, 0, o, stream=s1 if i % 2 == 0 else s2)
+    torch.cuda.synchronize()
+    for o in outs:
+        ok, worst = OG.check(o.float().cpu().numpy(), c, e, "bf16")
+        assert ok, worst
