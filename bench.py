@@ -341,15 +341,19 @@ def time_workload(wl, steps, warmup, world, flush, stream):
     return timer, len(launches)
 
 
+SPIN_CYCLES = 400_000  # ~0.2 ms at 2 GHz
+
+
 def time_isolated(wl, reps, flush, stream):
-    """Device time of each launch on its own: the 512 MiB flush queued before
-    every launch keeps the GPU busy while the host enqueues the launch, so the
-    events bracket the kernel alone, on a cold L2."""
+    """Device time of each launch on its own: the 512 MiB flush and a spin
+    kernel queued before every launch keep the GPU busy while the host
+    enqueues the launch, so the events bracket the kernel alone, on a cold L2."""
     per = {}
     launches = wl.launches()
     for _ in range(reps):
         for label, fn in launches:
             flush.zero_()
+            torch.cuda._sleep(SPIN_CYCLES)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             fn()
@@ -552,6 +556,7 @@ def time_launches(fns, iters, flush, stream, warmup=3):
     for _ in range(iters):
         for label, fn in fns:
             flush.zero_()
+            torch.cuda._sleep(SPIN_CYCLES)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             fn()
@@ -652,6 +657,43 @@ def run_extras(dev, flush, stream, peaks, iters=10):
                      "two_level": round(snr_db_dev(x, deq2.view(M, K)), 3)}
     out["two_level_8192"] = row
     del ad, bd, bufs, x, deq2, deqg
+    # FP8 SwiGLU MLP training with delayed scaling: d 4096, ffn 14336, 16384
+    # tokens, 16 steps (inputs drawn on the device from seeded generators)
+    from fp8_quantized_gemm_gb300.mlp import SwiGLUTrainer
+    x, w1, w3, w2 = workloads.swiglu(device=dev)
+    tr = SwiGLUTrainer(w1, w3, w2, tokens=x.shape[0])
+    del w1, w3, w2
+    dys = [workloads.swiglu_grad(t, device=dev) for t in range(17)]
+    tr.step(x, dys[0])  # warm-up step (kernel attributes, split-K scratch)
+    torch.cuda.synchronize()
+    steps16 = 16
+    fb_ms, opt_ms = [], []
+    s0 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for t in range(steps16):
+        e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e1.record(stream)
+        tr.forward_backward(x, dys[t + 1])
+        e2.record(stream)
+        tr.optimizer_and_state()
+        e3.record(stream)
+        fb_ms.append((e1, e2))
+        opt_ms.append((e2, e3))
+    s1 = torch.cuda.Event(enable_timing=True)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    total = s0.elapsed_time(s1)
+    fb = sum(a.elapsed_time(b) for a, b in fb_ms) / steps16
+    op = sum(a.elapsed_time(b) for a, b in opt_ms) / steps16
+    out["swiglu_training_delayed_16steps"] = {
+        "tflops_incl_quantize": round(tr.flops_per_step * steps16 / (total / 1e3) / 1e12, 2),
+        "frac_fp8_peak": round(tr.flops_per_step * steps16 / (total / 1e3) / 1e12 / fp8_peak, 4),
+        "ms_per_step": round(total / steps16, 3),
+        "ms_forward_backward": round(fb, 3), "ms_adamw_and_state": round(op, 3),
+        "tflop_per_step": round(tr.flops_per_step / 1e12, 3),
+        "launch": "eager, one API call per kernel (39 per step)"}
+    del tr, x, dys
+    torch.cuda.empty_cache()
     # delayed-state update (1024-entry history)
     hist = torch.zeros(1024, device=dev)
     sc = torch.ones(1, device=dev)

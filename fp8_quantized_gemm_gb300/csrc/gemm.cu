@@ -542,7 +542,9 @@ static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const Gem
 int gemm_tile_n(int mode) { return mode == kScaleGroupF32 ? 128 : 256; }
 
 // Split K when the tiles cannot fill half the SMs: as many splits as fit the
-// SMs, each covering at least four 128-wide K blocks.
+// SMs, each covering at least four 128-wide K blocks, and no more than the
+// last CTA of a tile can sum quickly (512 KB of fp32 partials per tile: the
+// reduction runs at one SM's L2 bandwidth).
 int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms) {
   const int64_t bn = gemm_tile_n(mode);
   const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
@@ -550,6 +552,9 @@ int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms) {
   if (tiles * 2 > sms || kb < 8) return 1;
   int64_t ks = sms / tiles;
   if (ks > kb / 4) ks = kb / 4;
+  const int64_t rows = M < 128 ? M : 128;
+  const int64_t by_partials = (512 * 1024) / (rows * bn * 4);
+  if (ks > by_partials) ks = by_partials;
   return ks < 2 ? 1 : (int)ks;
 }
 

@@ -1,0 +1,119 @@
+"""FP8 SwiGLU MLP training step with delayed scaling, as a sequence of C-ABI
+calls (every arithmetic step runs in the library's kernels).
+
+    h = x W1^T,  u = x W3^T,  a = silu(h) * u,  y = a W2^T
+    da = dy W2,  dW2 = dy^T a,  dh, du = swiglu_backward(da, h, u)
+    dx = dh W1 + du W3,  dW1 = dh^T x,  dW3 = du^T x
+    AdamW on fp32 master weights; bf16 copies feed the next step's quantizer.
+
+E4M3 for activations and weights, E5M2 for gradients (Flax guide 3.3).  Each
+linear keeps three (amax history, scale) pairs -- input, kernel, output
+gradient -- as the Flax guide's per-layer meta does (section 5.1); a tensor is
+quantized with the scale left by the previous step and its fused amax is
+pushed afterwards (section 2.3).  Both W1 and W3 take x as input: their two
+input states receive the same amax every step and so always hold the same
+scale; x is quantized once, with the first.
+
+Buffers are allocated once (device memory through torch); `step` issues the
+calls on the current stream and can be captured in a CUDA graph after one
+warm-up step.
+"""
+from __future__ import annotations
+
+import torch
+
+import fp8_quantized_gemm_gb300 as F
+
+# state slots: (input, kernel, output grad) for linear 1 (W1), 3 (W3), 2 (W2)
+X1, K1, G1, X3, K3, G3, A2, K2, G2 = range(9)
+STATE_NAMES = ("x@W1", "W1", "dh", "x@W3", "W3", "du", "a@W2", "W2", "dy")
+HISTORY = 1024
+
+
+class SwiGLUTrainer:
+    def __init__(self, w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, tokens: int,
+                 lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
+                 history: int = HISTORY):
+        dev = w1.device
+        ffn, d = w1.shape
+        assert w3.shape == (ffn, d) and w2.shape == (d, ffn)
+        self.T, self.d, self.ffn = tokens, d, ffn
+        self.hp = dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay)
+        self.t = 0
+        bf, f32 = dict(dtype=torch.bfloat16, device=dev), dict(dtype=torch.float32, device=dev)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        T = tokens
+        # weights: fp32 masters, moments, bf16 copies
+        self.w_bf = [w1.contiguous().clone(), w3.contiguous().clone(), w2.contiguous().clone()]
+        self.w_master = [w.float() for w in self.w_bf]
+        self.m = [torch.zeros_like(w) for w in self.w_master]
+        self.v = [torch.zeros_like(w) for w in self.w_master]
+        # delayed-scaling state
+        self.hist = torch.zeros((9, history), **f32)
+        self.scale = torch.ones(9, **f32)
+        self.amax = torch.zeros(9, **f32)
+        # quantized operands (row-major and transposed copies)
+        self.xq, self.xqt = torch.empty((T, d), **u8), torch.empty((d, T), **u8)
+        self.w1q, self.w1qt = torch.empty((ffn, d), **u8), torch.empty((d, ffn), **u8)
+        self.w3q, self.w3qt = torch.empty((ffn, d), **u8), torch.empty((d, ffn), **u8)
+        self.w2q, self.w2qt = torch.empty((d, ffn), **u8), torch.empty((ffn, d), **u8)
+        self.aq, self.aqt = torch.empty((T, ffn), **u8), torch.empty((ffn, T), **u8)
+        self.dyq, self.dyqt = torch.empty((T, d), **u8), torch.empty((d, T), **u8)
+        self.dhq, self.dhqt = torch.empty((T, ffn), **u8), torch.empty((ffn, T), **u8)
+        self.duq, self.duqt = torch.empty((T, ffn), **u8), torch.empty((ffn, T), **u8)
+        # activations and gradients
+        self.h, self.u, self.a = (torch.empty((T, ffn), **bf) for _ in range(3))
+        self.y = torch.empty((T, d), **bf)
+        self.da, self.dh, self.du = (torch.empty((T, ffn), **bf) for _ in range(3))
+        self.dx = torch.empty((T, d), **f32)
+        self.dw = [torch.empty((ffn, d), **f32), torch.empty((ffn, d), **f32),
+                   torch.empty((d, ffn), **f32)]
+        self.flops_per_step = 9 * 2.0 * T * d * ffn
+
+    def _sc(self, i):
+        return self.scale[i:i + 1]
+
+    def _am(self, i):
+        return self.amax[i:i + 1]
+
+    def forward_backward(self, x: torch.Tensor, dy: torch.Tensor):
+        """The nine GEMMs with their quantize and SwiGLU passes (no optimizer)."""
+        E4, E5 = F.E4M3, F.E5M2
+        q, g = F.fp8_quantize_tensor, F.fp8_gemm_tensor
+        w1, w3, w2 = self.w_bf
+        # forward
+        q(x, E4, self.xq, scale=self._sc(X1), q_t=self.xqt, amax_out=self._am(X1))
+        q(w1, E4, self.w1q, scale=self._sc(K1), q_t=self.w1qt, amax_out=self._am(K1))
+        q(w3, E4, self.w3q, scale=self._sc(K3), q_t=self.w3qt, amax_out=self._am(K3))
+        q(w2, E4, self.w2q, scale=self._sc(K2), q_t=self.w2qt, amax_out=self._am(K2))
+        g(self.xq, E4, self.w1q, E4, self._sc(X1), self._sc(K1), self.h)
+        g(self.xq, E4, self.w3q, E4, self._sc(X1), self._sc(K3), self.u)
+        F.fp8_swiglu_forward(self.h, self.u, self.a)
+        q(self.a, E4, self.aq, scale=self._sc(A2), q_t=self.aqt, amax_out=self._am(A2))
+        g(self.aq, E4, self.w2q, E4, self._sc(A2), self._sc(K2), self.y)
+        # backward
+        q(dy, E5, self.dyq, scale=self._sc(G2), q_t=self.dyqt, amax_out=self._am(G2))
+        g(self.dyq, E5, self.w2qt, E4, self._sc(G2), self._sc(K2), self.da)
+        g(self.dyqt, E5, self.aqt, E4, self._sc(G2), self._sc(A2), self.dw[2])
+        F.fp8_swiglu_backward(self.da, self.h, self.u, self.dh, self.du)
+        q(self.dh, E5, self.dhq, scale=self._sc(G1), q_t=self.dhqt, amax_out=self._am(G1))
+        q(self.du, E5, self.duq, scale=self._sc(G3), q_t=self.duqt, amax_out=self._am(G3))
+        g(self.dhq, E5, self.w1qt, E4, self._sc(G1), self._sc(K1), self.dx)
+        g(self.duq, E5, self.w3qt, E4, self._sc(G3), self._sc(K3), self.dx, accumulate=True)
+        g(self.dhqt, E5, self.xqt, E4, self._sc(G1), self._sc(X1), self.dw[0])
+        g(self.duqt, E5, self.xqt, E4, self._sc(G3), self._sc(X1), self.dw[1])
+
+    def optimizer_and_state(self):
+        """AdamW on the three weights, then the nine amax-history pushes."""
+        self.t += 1
+        for i in range(3):
+            F.fp8_adamw_step(self.w_master[i], self.dw[i], self.m[i], self.v[i], self.w_bf[i],
+                             self.t, **self.hp)
+        for i in range(9):
+            cur = X1 if i == X3 else i  # the x@W3 input state takes x's amax
+            fmt = F.E5M2 if i in (G1, G3, G2) else F.E4M3
+            F.fp8_delayed_state_update(self.hist[i], self.scale[i:i + 1], self._am(cur), fmt)
+
+    def step(self, x: torch.Tensor, dy: torch.Tensor):
+        self.forward_backward(x, dy)
+        self.optimizer_and_state()

@@ -32,14 +32,14 @@ from __future__ import annotations
 import torch
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
     return g
 
 
 def _normal(shape, std: float, gen: torch.Generator) -> torch.Tensor:
-    return torch.randn(*shape, generator=gen, dtype=torch.float32) * std
+    return torch.randn(*shape, generator=gen, dtype=torch.float32, device=gen.device) * std
 
 
 def _outlier_columns(x: torch.Tensor, frac: float, factor: float,
@@ -93,9 +93,14 @@ def two_level(seed: int = 3, m: int = 8192, n: int = 8192, k: int = 8192,
     return a.to(torch.bfloat16), b.to(torch.bfloat16)
 
 
-def swiglu(seed: int = 4, d: int = 4096, ffn: int = 14336, tokens: int = 16384):
-    """x[tokens,d], W1[ffn,d], W3[ffn,d], W2[d,ffn] in bf16."""
-    g = _gen(seed)
+def swiglu(seed: int = 4, d: int = 4096, ffn: int = 14336, tokens: int = 16384,
+           device="cpu"):
+    """x[tokens,d], W1[ffn,d], W3[ffn,d], W2[d,ffn] in bf16.
+
+    ``device`` selects the generator: the CPU stream (used by the parity
+    tests) or a seeded CUDA stream (different values, same distribution; used
+    to draw the full-size training workload quickly)."""
+    g = _gen(seed, device)
     x = _normal((tokens, d), 1.0, g).to(torch.bfloat16)
     w1 = _normal((ffn, d), 0.02, g).to(torch.bfloat16)
     w3 = _normal((ffn, d), 0.02, g).to(torch.bfloat16)
@@ -103,9 +108,9 @@ def swiglu(seed: int = 4, d: int = 4096, ffn: int = 14336, tokens: int = 16384):
     return x, w1, w3, w2
 
 
-def swiglu_grad(step: int, tokens: int = 16384, d: int = 4096):
+def swiglu_grad(step: int, tokens: int = 16384, d: int = 4096, device="cpu"):
     """Synthetic loss gradient dy[tokens,d] ~N(0,1e-3) for training step ``step``."""
-    g = _gen(1000 + step)
+    g = _gen(1000 + step, device)
     return _normal((tokens, d), 1e-3, g).to(torch.bfloat16)
 
 
