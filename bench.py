@@ -577,88 +577,132 @@ def snr_db_dev(x, xhat):
     return float(10.0 * torch.log10((x.double() ** 2).sum() / (d * d).sum()))
 
 
-def run_extras(dev, flush, stream, peaks, iters=10):
-    import fp8_quantized_gemm_gb300 as F
-    fp8_peak, hbm = 2.0 * peaks["bf16_tflops"], peaks["hbm_gbs"]
-    out = {}
-    # per-K-group GEMM (1x128 activations x 128x128 weight blocks), K 7168, N 2048
-    K, N = 7168, 2048
-    _, w = workloads.fine_grained(1, k=K, n=N)
-    wd = w.to(dev)
-    for sname, sfmt in (("f32", F.SCALE_F32), ("ue8m0", F.SCALE_UE8M0)):
+class GroupGemm:
+    """Fine-grained FP8 inference GEMM: activations quantized per token in
+    1x128 groups (timed), weights in 128x128 blocks (offline), K 7168, N 2048."""
+
+    _w_cache = {}
+
+    def __init__(self, dev, m, sfmt_name, k=7168, n=2048):
+        import fp8_quantized_gemm_gb300 as F
+        self.name = "group_%s_m%d" % (sfmt_name, m)
+        self.m, self.k, self.n = m, k, n
+        sfmt = F.SCALE_F32 if sfmt_name == "f32" else F.SCALE_UE8M0
         sdt = torch.float32 if sfmt == F.SCALE_F32 else torch.uint8
-        wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
-        ws = torch.empty((N // 128, K // 128), dtype=sdt, device=dev)
-        F.fp8_quantize_block(wd, F.E4M3, sfmt, wq, ws)  # offline weight quantization
-        for m in (1, 128, 4096):
-            act, _ = workloads.fine_grained(m, k=K, n=8)
-            ad = act.to(dev)
-            aq = torch.empty((m, K), dtype=torch.uint8, device=dev)
-            asc = torch.empty((K // 128, m), dtype=sdt, device=dev)
-            y = torch.empty((m, N), dtype=torch.bfloat16, device=dev)
-            fns = [("quantize", lambda: F.fp8_quantize_token_group(ad, F.E4M3, sfmt, aq, asc)),
-                   ("gemm", lambda: F.fp8_gemm_group(aq, asc, wq, ws, sfmt, y))]
-            per, step = time_launches(fns, iters, flush, stream)
-            flops = 2.0 * m * N * K
-            gemm_bytes = N * K + m * K + m * N * 2 + ws.numel() * ws.element_size() + \
-                asc.numel() * asc.element_size()
-            out["group_%s_m%d" % (sname, m)] = {
-                "tflops_incl_quantize": round(flops / (step / 1e3) / 1e12, 2),
+        key = (sfmt_name, k, n, str(dev))
+        if key not in GroupGemm._w_cache:
+            _, w = workloads.fine_grained(1, k=k, n=n)
+            wd = w.to(dev)
+            wq = torch.empty((n, k), dtype=torch.uint8, device=dev)
+            ws = torch.empty(((n + 127) // 128, k // 128), dtype=sdt, device=dev)
+            F.fp8_quantize_block(wd, F.E4M3, sfmt, wq, ws)  # offline weight quantization
+            GroupGemm._w_cache[key] = (wq, ws)
+        self.wq, self.ws = GroupGemm._w_cache[key]
+        act, _ = workloads.fine_grained(m, k=k, n=8)
+        self.ad = act.to(dev)
+        self.aq = torch.empty((m, k), dtype=torch.uint8, device=dev)
+        self.asc = torch.empty((k // 128, m), dtype=sdt, device=dev)
+        self.y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.sfmt, self.F = sfmt, F
+
+    def launches(self):
+        F = self.F
+        return [("quantize", lambda: F.fp8_quantize_token_group(self.ad, F.E4M3, self.sfmt, self.aq,
+                                                                self.asc)),
+                ("gemm", lambda: F.fp8_gemm_group(self.aq, self.asc, self.wq, self.ws, self.sfmt,
+                                                  self.y))]
+
+    def report(self, per, step, fp8_peak, hbm):
+        m, k, n = self.m, self.k, self.n
+        flops = 2.0 * m * n * k
+        gb = n * k + m * k + m * n * 2 + self.ws.numel() * self.ws.element_size() + \
+            self.asc.numel() * self.asc.element_size()
+        return {"tflops_incl_quantize": round(flops / (step / 1e3) / 1e12, 2),
                 "gemm_tflops": round(flops / (per["gemm"] / 1e3) / 1e12, 2),
                 "gemm_frac_fp8_peak": round(flops / (per["gemm"] / 1e3) / 1e12 / fp8_peak, 4),
-                "gemm_gbs": round(gemm_bytes / (per["gemm"] / 1e3) / 1e9, 1),
-                "gemm_frac_hbm": round(gemm_bytes / (per["gemm"] / 1e3) / 1e9 / hbm, 4),
-                "quantize_gbs": round((m * K * 3 + asc.numel() * asc.element_size())
+                "gemm_gbs": round(gb / (per["gemm"] / 1e3) / 1e9, 1),
+                "gemm_frac_hbm": round(gb / (per["gemm"] / 1e3) / 1e9 / hbm, 4),
+                "quantize_gbs": round((m * k * 3 + self.asc.numel() * self.asc.element_size())
                                       / (per["quantize"] / 1e3) / 1e9, 1),
-                "ms": {k: round(v, 4) for k, v in per.items()}}
-    del wd
-    # two-level microscaling GEMM, M = N = K = 8192
-    M = N = K = 8192
-    a, b = workloads.two_level(m=M, n=N, k=K)
-    ad, bd = a.to(dev), b.to(dev)
-    bufs = []
-    for t in (ad, bd):
-        bufs.append((t, torch.empty(1, device=dev), torch.empty(1, device=dev),
-                     torch.empty((M, K), dtype=torch.uint8, device=dev), F.mx_local_words(M, K, dev)))
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    fns = []
-    for t, am, gl, q, lw in bufs:
-        fns.append(("amax", lambda t=t, am=am: F.fp8_amax(t, am)))
-        fns.append(("quantize", lambda t=t, am=am, gl=gl, q=q, lw=lw:
-                    F.fp8_quantize_mx(t, F.E4M3, am, gl, q, lw)))
-    fns.append(("gemm", lambda: F.fp8_gemm_mx(bufs[0][3], bufs[0][4], bufs[0][2], bufs[1][3],
-                                              bufs[1][4], bufs[1][2], y)))
-    per, step = time_launches(fns, max(3, iters // 2), flush, stream)
-    flops = 2.0 * M * N * K
-    row = {"tflops_incl_quantize": round(flops / (step / 1e3) / 1e12, 2),
-           "gemm_tflops": round(flops / (per["gemm"] / 1e3) / 1e12, 2),
-           "gemm_frac_fp8_peak": round(flops / (per["gemm"] / 1e3) / 1e12 / fp8_peak, 4),
-           "quantize_gbs": round(M * K * (3 + 1 / 32) / (per["quantize"] / 1e3) / 1e9, 1),
-           "amax_gbs": round(M * K * 2 / (per["amax"] / 1e3) / 1e9, 1),
-           "ms": {k: round(v, 4) for k, v in per.items()}}
-    # SNR of A under the three granularities (dequantized from the kernels' codes)
-    e4 = torch.float8_e4m3fn
-    x = ad.float()
-    t, am, gl, q, lw = bufs[0]
-    loc = lw.view(torch.uint8).view(K // 128, -1, 4)  # [G, Rpad, 4] bytes in word order
-    rows_ = torch.arange(M, device=dev)
-    pos = (rows_ & ~127) + 4 * (rows_ % 32) + (rows_ % 128) // 32
-    r = loc[:, pos, :].permute(1, 0, 2).reshape(M, K // 32).float()
-    deq2 = q.view(e4).float().view(M, K // 32, 32) * (gl * torch.exp2(r - 127.0))[:, :, None]
-    qt = torch.empty((M, K), dtype=torch.uint8, device=dev)
-    st = torch.empty(1, device=dev)
-    F.fp8_quantize_tensor(ad, F.E4M3, qt, amax_in=am, scale_out=st)
-    qg = torch.empty((M, K), dtype=torch.uint8, device=dev)
-    sg = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
-    F.fp8_quantize_token_group(ad, F.E4M3, F.SCALE_F32, qg, sg)
-    deqg = qg.view(e4).float().view(M, K // 128, 128) * sg.t()[:, :, None]
-    row["snr_db"] = {"per_tensor": round(snr_db_dev(x, qt.view(e4).float() * st), 3),
-                     "per_group_1x128": round(snr_db_dev(x, deqg.view(M, K)), 3),
-                     "two_level": round(snr_db_dev(x, deq2.view(M, K)), 3)}
-    out["two_level_8192"] = row
-    del ad, bd, bufs, x, deq2, deqg
-    # FP8 SwiGLU MLP training with delayed scaling: d 4096, ffn 14336, 16384
-    # tokens, 16 steps (inputs drawn on the device from seeded generators)
+                "ms": {kk: round(v, 4) for kk, v in per.items()}}
+
+
+class TwoLevel:
+    """MOSS two-level microscaling GEMM, M = N = K = 8192: amax and two-level
+    quantization of both operands, then the block-scaled GEMM."""
+
+    name = "two_level_8192"
+
+    def __init__(self, dev, m=8192, n=8192, k=8192):
+        import fp8_quantized_gemm_gb300 as F
+        self.F, self.m, self.n, self.k = F, m, n, k
+        a, b = workloads.two_level(m=m, n=n, k=k)
+        self.ad, self.bd = a.to(dev), b.to(dev)
+        self.bufs = []
+        for t, r in ((self.ad, m), (self.bd, n)):
+            self.bufs.append((t, torch.empty(1, device=dev), torch.empty(1, device=dev),
+                              torch.empty((r, k), dtype=torch.uint8, device=dev),
+                              F.mx_local_words(r, k, dev)))
+        self.y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+
+    def launches(self):
+        F, out = self.F, []
+        for t, am, gl, q, lw in self.bufs:
+            out.append(("amax", lambda t=t, am=am: F.fp8_amax(t, am)))
+            out.append(("quantize", lambda t=t, am=am, gl=gl, q=q, lw=lw:
+                        F.fp8_quantize_mx(t, F.E4M3, am, gl, q, lw)))
+        A, B = self.bufs
+        out.append(("gemm", lambda: F.fp8_gemm_mx(A[3], A[4], A[2], B[3], B[4], B[2], self.y)))
+        return out
+
+    def report(self, per, step, fp8_peak, hbm):
+        M, N, K = self.m, self.n, self.k
+        flops = 2.0 * M * N * K
+        row = {"tflops_incl_quantize": round(flops / (step / 1e3) / 1e12, 2),
+               "gemm_tflops": round(flops / (per["gemm"] / 1e3) / 1e12, 2),
+               "gemm_frac_fp8_peak": round(flops / (per["gemm"] / 1e3) / 1e12 / fp8_peak, 4),
+               "quantize_gbs": round(M * K * (3 + 1 / 32) / (per["quantize"] / 1e3) / 1e9, 1),
+               "amax_gbs": round(M * K * 2 / (per["amax"] / 1e3) / 1e9, 1),
+               "ms": {kk: round(v, 4) for kk, v in per.items()}}
+        row["snr_db"] = self.snr()
+        return row
+
+    def snr(self):
+        """SNR of A under the three granularities, from the kernels' codes."""
+        F, M, K = self.F, self.m, self.k
+        dev = self.ad.device
+        e4 = torch.float8_e4m3fn
+        x = self.ad.float()
+        t, am, gl, q, lw = self.bufs[0]
+        F.fp8_amax(t, am)
+        F.fp8_quantize_mx(t, F.E4M3, am, gl, q, lw)
+        loc = lw.view(torch.uint8).view(K // 128, -1, 4)  # [G, Rpad, 4] bytes in word order
+        rows_ = torch.arange(M, device=dev)
+        pos = (rows_ & ~127) + 4 * (rows_ % 32) + (rows_ % 128) // 32
+        r = loc[:, pos, :].permute(1, 0, 2).reshape(M, K // 32).float()
+        deq2 = q.view(e4).float().view(M, K // 32, 32) * (gl * torch.exp2(r - 127.0))[:, :, None]
+        qt = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        st = torch.empty(1, device=dev)
+        F.fp8_quantize_tensor(self.ad, F.E4M3, qt, amax_in=am, scale_out=st)
+        qg = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sg = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        F.fp8_quantize_token_group(self.ad, F.E4M3, F.SCALE_F32, qg, sg)
+        deqg = qg.view(e4).float().view(M, K // 128, 128) * sg.t()[:, :, None]
+        return {"per_tensor": round(snr_db_dev(x, qt.view(e4).float() * st), 3),
+                "per_group_1x128": round(snr_db_dev(x, deqg.view(M, K)), 3),
+                "two_level": round(snr_db_dev(x, deq2.view(M, K)), 3)}
+
+
+def extra_workloads(dev):
+    for sname in ("f32", "ue8m0"):
+        for m in (1, 128, 4096):
+            yield GroupGemm(dev, m, sname)
+    yield TwoLevel(dev)
+
+
+def run_swiglu_row(dev, stream, fp8_peak):
+    """FP8 SwiGLU MLP training with delayed scaling: d 4096, ffn 14336, 16384
+    tokens, 16 steps (inputs drawn on the device from seeded generators)."""
     from fp8_quantized_gemm_gb300.mlp import SwiGLUTrainer
     x, w1, w3, w2 = workloads.swiglu(device=dev)
     tr = SwiGLUTrainer(w1, w3, w2, tokens=x.shape[0])
@@ -685,16 +729,26 @@ def run_extras(dev, flush, stream, peaks, iters=10):
     total = s0.elapsed_time(s1)
     fb = sum(a.elapsed_time(b) for a, b in fb_ms) / steps16
     op = sum(a.elapsed_time(b) for a, b in opt_ms) / steps16
-    out["swiglu_training_delayed_16steps"] = {
-        "tflops_incl_quantize": round(tr.flops_per_step * steps16 / (total / 1e3) / 1e12, 2),
-        "frac_fp8_peak": round(tr.flops_per_step * steps16 / (total / 1e3) / 1e12 / fp8_peak, 4),
-        "ms_per_step": round(total / steps16, 3),
-        "ms_forward_backward": round(fb, 3), "ms_adamw_and_state": round(op, 3),
-        "tflop_per_step": round(tr.flops_per_step / 1e12, 3),
-        "launch": "eager, one API call per kernel (39 per step)"}
+    row = {"tflops_incl_quantize": round(tr.flops_per_step * steps16 / (total / 1e3) / 1e12, 2),
+           "frac_fp8_peak": round(tr.flops_per_step * steps16 / (total / 1e3) / 1e12 / fp8_peak, 4),
+           "ms_per_step": round(total / steps16, 3),
+           "ms_forward_backward": round(fb, 3), "ms_adamw_and_state": round(op, 3),
+           "tflop_per_step": round(tr.flops_per_step / 1e12, 3),
+           "launch": "eager, one API call per kernel (39 per step)"}
     del tr, x, dys
     torch.cuda.empty_cache()
-    # delayed-state update (1024-entry history)
+    return row
+
+
+def run_extras(dev, flush, stream, peaks, iters=10):
+    import fp8_quantized_gemm_gb300 as F
+    fp8_peak, hbm = 2.0 * peaks["bf16_tflops"], peaks["hbm_gbs"]
+    out = {}
+    for wl in extra_workloads(dev):
+        per, step = time_launches(wl.launches(), iters, flush, stream)
+        out[wl.name] = wl.report(per, step, fp8_peak, hbm)
+        del wl
+    out["swiglu_training_delayed_16steps"] = run_swiglu_row(dev, stream, fp8_peak)
     hist = torch.zeros(1024, device=dev)
     sc = torch.ones(1, device=dev)
     cur = torch.full((1,), 3.0, device=dev)
@@ -704,12 +758,20 @@ def run_extras(dev, flush, stream, peaks, iters=10):
     return out
 
 
+PROFILE_WORKLOADS = {
+    "float8_linear": lambda dev: Float8Linear(dev),
+    "two_level_8192": lambda dev: TwoLevel(dev),
+    **{"group_%s_m%d" % (s_, m): (lambda dev, s_=s_, m=m: GroupGemm(dev, m, s_))
+       for s_ in ("f32", "ue8m0") for m in (1, 128, 4096)},
+}
+
+
 def run_profile(args):
-    """The workload's launch sequence only (warmup + steps passes, no flush
-    buffer, no extras, no baselines): the command ncu captures use."""
+    """A workload's launch sequence only (warmup + steps passes, no flush
+    buffer, no baselines): the command ncu captures use."""
     import fp8_quantized_gemm_gb300 as F
     dev, _, _ = setup_dist()
-    wl = Float8Linear(dev)
+    wl = PROFILE_WORKLOADS[args.profile](dev)
     for _ in range(args.warmup + args.steps):
         for _, fn in wl.launches():
             fn()
@@ -717,7 +779,8 @@ def run_profile(args):
     rc, where = F.fp8_get_last_device_error()
     if rc != 0:
         raise RuntimeError("device error %d (where %d)" % (rc, where))
-    print("profile run: %d passes of %d launches" % (args.warmup + args.steps, len(wl.launches())))
+    print("profile run %s: %d passes of %d launches" % (args.profile, args.warmup + args.steps,
+                                                        len(wl.launches())))
 
 
 def main():
@@ -730,10 +793,11 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time eager launches, not a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=8192)
-    ap.add_argument("--profile", action="store_true",
-                    help="run the launch sequence only (for ncu captures); prints no bench line")
+    ap.add_argument("--profile", default=None, choices=sorted(PROFILE_WORKLOADS),
+                    help="run one workload's launch sequence only (for ncu captures); "
+                         "prints no bench line")
     args = ap.parse_args()
-    if args.profile:
+    if args.profile is not None:
         run_profile(args)
         return
     if args.warmup < 3 and args.impl == "ours":

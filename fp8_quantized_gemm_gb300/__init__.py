@@ -32,7 +32,7 @@ E4M3, E5M2 = 0, 1
 SCALE_F32, SCALE_UE8M0 = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
 
-_vp, _i64, _int, _f = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+_vp, _i64, _int, _d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
 _SIGS = {
     "fp8_amax": [_vp, _int, _i64, _vp, _vp],
     "fp8_quantize_tensor": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
@@ -45,7 +45,7 @@ _SIGS = {
     "fp8_delayed_state_update": [_vp, _vp, _vp, _i64, _int, _vp],
     "fp8_swiglu_forward": [_vp, _vp, _vp, _i64, _vp],
     "fp8_swiglu_backward": [_vp, _vp, _vp, _vp, _vp, _i64, _vp],
-    "fp8_adamw_step": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f, _f, _f, _f, _f, _vp],
+    "fp8_adamw_step": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _d, _d, _d, _d, _d, _vp],
     "fp8_get_last_device_error": [ctypes.POINTER(ctypes.c_int), _vp],
 }
 for _name, _args in _SIGS.items():

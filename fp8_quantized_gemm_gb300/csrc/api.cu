@@ -325,8 +325,8 @@ int fp8_swiglu_backward(const void *da, const void *h, const void *u, void *dh, 
 }
 
 int fp8_adamw_step(float *p, const float *g, float *m, float *v, void *p_bf16, int64_t n,
-                   int64_t step, float lr, float beta1, float beta2, float eps,
-                   float weight_decay, fp8_stream_t stream) {
+                   int64_t step, double lr, double beta1, double beta2, double eps,
+                   double weight_decay, fp8_stream_t stream) {
   if (p == nullptr || g == nullptr || m == nullptr || v == nullptr || n < 0 || step < 1)
     return FP8_ERR_INVALID_ARG;
   if (n % 4 != 0 || !aligned16(p) || !aligned16(g) || !aligned16(m) || !aligned16(v) ||

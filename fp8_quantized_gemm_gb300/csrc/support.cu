@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(512)
 __global__ void __launch_bounds__(512)
     adamw_kernel(float4 *__restrict__ p, const float4 *__restrict__ g, float4 *__restrict__ m,
                  float4 *__restrict__ v, uint2 *__restrict__ pb, int64_t nvec, float lr,
-                 float b1, float b2, float eps, float decay, float bc1, float bc2) {
+                 float b1, float b2, float omb1, float omb2, float eps, float decay, float bc1,
+                 float bc2) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
     float4 pv = p[i], mv = m[i], vv = v[i];
@@ -77,8 +78,8 @@ __global__ void __launch_bounds__(512)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       pp[j] = pp[j] * decay;
-      mm[j] = b1 * mm[j] + (1.0f - b1) * gg[j];
-      vvp[j] = b2 * vvp[j] + (1.0f - b2) * gg[j] * gg[j];
+      mm[j] = b1 * mm[j] + omb1 * gg[j];
+      vvp[j] = b2 * vvp[j] + omb2 * gg[j] * gg[j];
       const float mhat = mm[j] / bc1;
       const float vhat = vvp[j] / bc2;
       pp[j] = pp[j] - lr * mhat / (sqrtf(vhat) + eps);
@@ -117,15 +118,18 @@ cudaError_t launch_swiglu_bwd(const void *da, const void *h, const void *u, void
 }
 
 cudaError_t launch_adamw(float *p, const float *g, float *m, float *v, void *pb, int64_t n,
-                         int64_t step, float lr, float b1, float b2, float eps, float wd, int sms,
+                         int64_t step, double lr, double b1, double b2, double eps, double wd, int sms,
                          cudaStream_t st) {
   const int64_t nvec = n / 4;
-  const float bc1 = (float)(1.0 - pow((double)b1, (double)step));
-  const float bc2 = (float)(1.0 - pow((double)b2, (double)step));
+  // 1 - beta and the bias corrections are formed in double on the host: in
+  // fp32, 1 - 0.999f is off by 1.3e-5 relative
+  const float bc1 = (float)(1.0 - pow(b1, (double)step));
+  const float bc2 = (float)(1.0 - pow(b2, (double)step));
+  const float omb1 = (float)(1.0 - b1), omb2 = (float)(1.0 - b2);
   adamw_kernel<<<blocks_for(nvec, 512, sms), 512, 0, st>>>(
       reinterpret_cast<float4 *>(p), reinterpret_cast<const float4 *>(g),
       reinterpret_cast<float4 *>(m), reinterpret_cast<float4 *>(v), static_cast<uint2 *>(pb), nvec,
-      lr, b1, b2, eps, 1.0f - lr * wd, bc1, bc2);
+      (float)lr, (float)b1, (float)b2, omb1, omb2, (float)eps, (float)(1.0 - lr * wd), bc1, bc2);
   return cudaGetLastError();
 }
 

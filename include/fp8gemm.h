@@ -221,14 +221,16 @@ FP8_API int fp8_delayed_state_update(float *hist, float *scale, const float *ama
  * fp8_swiglu_backward: dh = da * u * silu'(h), du = da * silu(h), bf16.
  * fp8_adamw_step: decoupled-weight-decay Adam on fp32 master weights p with
  *   moments m, v (fp32), gradient g (fp32); writes the bf16 copy p_bf16
- *   (nullable).  step counts from 1.  All buffers 16-byte aligned.
+ *   (nullable).  step counts from 1.  All buffers 16-byte aligned.  The
+ *   hyperparameters are doubles: 1 - beta and the bias corrections are formed
+ *   in double before the kernel sees them in fp32.
  */
 FP8_API int fp8_swiglu_forward(const void *h, const void *u, void *a, int64_t n, fp8_stream_t stream);
 FP8_API int fp8_swiglu_backward(const void *da, const void *h, const void *u, void *dh, void *du,
                         int64_t n, fp8_stream_t stream);
 FP8_API int fp8_adamw_step(float *p, const float *g, float *m, float *v, void *p_bf16, int64_t n,
-                   int64_t step, float lr, float beta1, float beta2, float eps,
-                   float weight_decay, fp8_stream_t stream);
+                   int64_t step, double lr, double beta1, double beta2, double eps,
+                   double weight_decay, fp8_stream_t stream);
 
 /* ---------------------------------------------------------------- status --
  * fp8_status_string: static text for a status code.
