@@ -345,14 +345,17 @@ SPIN_CYCLES = 400_000  # ~0.2 ms at 2 GHz
 
 
 def time_isolated(wl, reps, flush, stream):
-    """Device time of each launch on its own: the 512 MiB flush and a spin
-    kernel queued before every launch keep the GPU busy while the host
-    enqueues the launch, so the events bracket the kernel alone, on a cold L2."""
+    """Device time of each launch in step order: L2 is flushed once at the
+    start of every pass (as between timed steps), and a spin kernel that
+    touches no memory is queued before every launch so the host enqueues the
+    launch while the GPU spins; the events then bracket the kernel alone, with
+    the cache state the step itself leaves (e.g. a GEMM reads the codes its
+    quantize pass just wrote)."""
     per = {}
     launches = wl.launches()
     for _ in range(reps):
+        flush.zero_()
         for label, fn in launches:
-            flush.zero_()
             torch.cuda._sleep(SPIN_CYCLES)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
@@ -487,7 +490,8 @@ def run_ours(args):
                   "CUDA graph of the step's API calls, replayed",
         "eager": {"value": round(eager_value, 2), "ms_per_step": round(eager_total_ms / args.steps, 4)},
         "kernel_ms": {k: round(sum(v) / len(v), 4) for k, v in per.items()},
-        "kernel_timing": "each launch alone after a 512 MiB flush (cold L2), CUDA events",
+        "kernel_timing": "each launch bracketed by CUDA events in step order, L2 flushed per "
+                         "step, a memory-free spin kernel queued before each launch",
         "gpu_launches": n_launch * args.steps,
         "clocks": clk.summary(),
     }
@@ -545,17 +549,17 @@ def run_reference(args):
 # ------------------------------------------------------- other workloads --
 
 def time_launches(fns, iters, flush, stream, warmup=3):
-    """Mean device ms of each launch, each timed alone after a 512 MiB flush
-    (cold L2; the host enqueues the launch while the flush runs), and their
-    sum as the time of one pass."""
+    """Mean device ms of each launch in pass order (L2 flushed at the start of
+    every pass, a memory-free spin kernel before every launch so the host is
+    ahead of the GPU), and their sum as the time of one pass."""
     for _ in range(warmup):
         for _, fn in fns:
             fn()
     torch.cuda.synchronize()
     rec = {}
     for _ in range(iters):
+        flush.zero_()
         for label, fn in fns:
-            flush.zero_()
             torch.cuda._sleep(SPIN_CYCLES)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)

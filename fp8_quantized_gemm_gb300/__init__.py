@@ -47,6 +47,7 @@ _SIGS = {
     "fp8_swiglu_backward": [_vp, _vp, _vp, _vp, _vp, _i64, _vp],
     "fp8_adamw_step": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _d, _d, _d, _d, _d, _vp],
     "fp8_get_last_device_error": [ctypes.POINTER(ctypes.c_int), _vp],
+    "fp8_set_option": [_int, _int],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -185,6 +186,13 @@ def fp8_get_last_device_error(stream=None):
     where = ctypes.c_int(0)
     rc = _lib.fp8_get_last_device_error(ctypes.byref(where), _stream(stream))
     return rc, where.value
+
+
+OPT_GEMM_CTA_PAIRS = 1
+
+
+def fp8_set_option(option, value):
+    _call("fp8_set_option", int(option), int(value))
 
 
 # ------------------------------------------------------------ allocation --

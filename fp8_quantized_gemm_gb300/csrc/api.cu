@@ -43,6 +43,9 @@ struct Workspace {
   size_t bytes = 0;
 };
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+// CTA-pair GEMM path switch (on by default; fp8_set_option turns it off).
+bool g_use_pairs = true;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
@@ -156,6 +159,11 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
   args.vec_store = vector_store_ok(args.c, args.ldc, args.out_dt);
   CUtensorMap tma, tmb;
   if ((rc = encode_operand(&tma, a, args.K, args.M, 128)) != FP8_OK) return rc;
+  if (args.ksplit == 1 && g_use_pairs && fp8k::gemm_pair_eligible(mode, args.M, args.N, d->sms)) {
+    if ((rc = encode_operand(&tmb, b, args.K, args.N, fp8k::gemm_pair_b_rows())) != FP8_OK)
+      return rc;
+    return to_status(fp8k::launch_gemm_pair(tma, tmb, args, d->sms, st));
+  }
   if ((rc = encode_operand(&tmb, b, args.K, args.N, fp8k::gemm_tile_n(mode))) != FP8_OK) return rc;
   return to_status(fp8k::launch_gemm(mode, tma, tmb, args, d->sms, st));
 }
@@ -374,6 +382,14 @@ int fp8_get_last_device_error(int *where_out, fp8_stream_t stream) {
   }
   if (where_out != nullptr) *where_out = (int)h[1];
   return -(int)h[0];
+}
+
+int fp8_set_option(int option, int value) {
+  if (option == FP8_OPT_GEMM_CTA_PAIRS) {
+    g_use_pairs = value != 0;
+    return FP8_OK;
+  }
+  return FP8_ERR_INVALID_ARG;
 }
 
 const char *fp8_version(void) { return "fp8gemm 0.1 (sm_103a)"; }

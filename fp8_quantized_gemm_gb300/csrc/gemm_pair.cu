@@ -1,0 +1,243 @@
+// Per-tensor scaled-FP8 GEMM on CTA pairs (tcgen05 cta_group::2).
+//
+// A cluster of two CTAs on neighbouring SMs computes one 256 x BN output tile
+// with M = 256 MMAs issued by the even CTA (the leader):
+//
+//   - each CTA stages its own 128 rows of A and its own half (BN/2 rows) of B
+//     per 128-byte K slice, so a stage is 32 KB instead of 48 KB and six
+//     stages fit where four did (more bytes in flight per SM);
+//   - both CTAs' TMA loads complete on the LEADER's full barrier (the leader
+//     expects the bytes of both), the leader's MMA reads both CTAs' shared
+//     memory at the same offsets and writes each CTA's 128 rows of D into that
+//     CTA's TMEM;
+//   - tcgen05.commit multicasts each stage release and each "accumulator
+//     full" to both CTAs; both epilogues hand the accumulator back by arriving
+//     on the leader's barrier.
+//
+// Two TMEM accumulators per CTA: the epilogue of one tile overlaps the MMAs
+// of the next.  Scales are applied once in the epilogue (Flax guide 2.2).
+#include "common.cuh"
+#include "gemm_common.cuh"
+#include "kernels.h"
+
+namespace fp8k {
+
+template <int BN, int STAGES>
+struct PairCfg {
+  static constexpr int BM = 128, BK = 128;  // rows per CTA (256 per pair)
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr uint32_t kABytes = BM * BK;
+  static constexpr uint32_t kBBytes = (BN / 2) * BK;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTileBytes = STAGES * kStageBytes;
+  static constexpr int kAccBufs = 2;
+  static constexpr uint32_t kTmemCols = kAccBufs * BN;
+  static constexpr int kNumBars = 2 * STAGES + 2 * kAccBufs + 1;
+  static constexpr uint32_t kSmem = 1024 + kTileBytes + 8 * kNumBars + 16;
+  static_assert(kTmemCols <= 512, "TMEM budget");
+  static_assert(kSmem <= 227 * 1024, "shared-memory budget");
+};
+
+template <int BN, int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>::kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tma,
+                     const __grid_constant__ CUtensorMap tmb, const GemmArgs args) {
+  using C = PairCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kTileBytes);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  const DevErr err{args.err};
+
+  auto sA = [&](int s) { return smem_u32(smem + s * C::kStageBytes); };
+  auto sB = [&](int s) { return smem_u32(smem + s * C::kStageBytes + C::kABytes); };
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
+  auto accf_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + b]); };
+  auto acce_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + C::kAccBufs + b]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 2 * C::kAccBufs]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 2 * C::kEpiWarps);  // both CTAs' epilogue warps
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma);
+    tma_prefetch_desc(&tmb);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barrier inits visible to the peer before any remote use
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // pair p takes 256 x BN tiles p, p + npairs, ...; tile t covers rows
+  // (t / tiles_n) * 256 (this CTA: + rank * 128) and columns (t % tiles_n) * BN
+  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int64_t tiles_n = (args.N + BN - 1) / BN;
+  const int64_t num_tiles = ((args.M + 255) / 256) * tiles_n;
+  const int KB = (int)((args.K + C::BK - 1) / C::BK);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint32_t full_leader0 = mapa_shared(full_bar(0), 0);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
+      const int64_t m0 = (t / tiles_n) * 256 + rank * C::BM;
+      const int64_t nb0 = (t % tiles_n) * BN + rank * (BN / 2);
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = (int)(it % STAGES);
+        const uint32_t round = it / STAGES;
+        if (!mbar_wait(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
+          if (leader) {
+            mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
+            tma_load_2d(sA(s), &tma, full_bar(s), kb * C::BK, (int32_t)m0);
+            tma_load_2d(sB(s), &tmb, full_bar(s), kb * C::BK, (int32_t)nb0);
+          } else {
+            const uint32_t fb = full_leader0 + 8u * (uint32_t)s;
+            tma_load_2d_pair(sA(s), &tma, fb, kb * C::BK, (int32_t)m0);
+            tma_load_2d_pair(sB(s), &tmb, fb, kb * C::BK, (int32_t)nb0);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) {
+      if (leader) {
+        const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+        for (uint32_t i = first; i < it; ++i) drain_wait(full_bar(i % STAGES), (i / STAGES) & 1u);
+      } else {
+        drain_wait(drain_bar, 0);  // nothing arrives here: a fixed 20 ms grace period
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------- MMA (leader only)
+    if (leader && elect_one()) {
+      const uint32_t idesc = idesc_f8f6f4(256, BN, args.fa, args.fb);
+      uint32_t it = 0, j = 0;
+      bool ok = true;
+      for (int64_t t = pair; t < num_tiles && ok; t += npairs, ++j) {
+        const uint32_t buf = j & 1u, use = j >> 1;
+        if (!mbar_wait(acce_bar(buf), (use & 1u) ^ 1u, abort_flag, err, 2)) {
+          ok = false;
+          break;
+        }
+        const uint32_t d = tmem + buf * BN;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          const uint32_t round = it / STAGES;
+          if (!mbar_wait(full_bar(s), round & 1u, abort_flag, err, 2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_sw128(sA(s));
+          const uint64_t bdesc = sdesc_sw128(sB(s));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8f6f4_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair(empty_bar(s), (uint16_t)0x3);
+        }
+        if (!ok) break;
+        mma_commit_pair(accf_bar(buf), (uint16_t)0x3);
+      }
+      if (!ok) {
+        mma_commit_pair(drain_bar, (uint16_t)0x1);
+        drain_wait(drain_bar, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ epilogue (both)
+    const uint32_t q = warp & 3u;
+    const uint32_t lane_base = tmem + ((32u * q) << 16);
+    const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+    const float alpha =
+        *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
+    uint32_t j = 0;
+    for (int64_t t = pair; t < num_tiles; t += npairs, ++j) {
+      const int64_t m0 = (t / tiles_n) * 256 + rank * C::BM;
+      const int64_t n0 = (t % tiles_n) * BN;
+      const int64_t row = m0 + 32 * q + lane;
+      const uint32_t buf = j & 1u, use = j >> 1;
+      if (!mbar_wait(accf_bar(buf), use & 1u, abort_flag, err, 3)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        FP8K_TMEM_LD_X32(lane_base + buf * BN + (uint32_t)c, r);
+        tmem_ld_wait();
+        if (c + 32 == BN) {  // accumulator read out: hand it back to the leader
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acce_leader0 + 8u * buf);
+        }
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
+        store_row32(args, row, n0 + c, v);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal it
+  if (warp == 1) tmem_dealloc_pair(tmem, C::kTmemCols);
+}
+
+constexpr int kPairBN = 256, kPairStages = 6;
+
+int gemm_pair_b_rows() { return kPairBN / 2; }
+
+// CTA pairs pay off when the 256-row tiles still give every pair work.
+bool gemm_pair_eligible(int mode, int64_t M, int64_t N, int sms) {
+  if (mode != kScaleTensor) return false;
+  const int64_t tiles = ((M + 255) / 256) * ((N + kPairBN - 1) / kPairBN);
+  return tiles * 4 >= sms / 2;
+}
+
+cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
+                             int sms, cudaStream_t st) {
+  using C = PairCfg<kPairBN, kPairStages>;
+  auto kern = gemm_pair_kernel<kPairBN, kPairStages>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int64_t tiles = ((args.M + 255) / 256) * ((args.N + kPairBN - 1) / kPairBN);
+  const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
+  kern<<<(unsigned)(2 * pairs), C::kThreads, C::kSmem, st>>>(tma, tmb, args);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8k

@@ -60,4 +60,11 @@ int gemm_tile_n(int mode);
 cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,
                         const GemmArgs &args, int sms, cudaStream_t st);
 
+// CTA-pair (cta_group::2) variant of the per-tensor GEMM: 256 x 256 tiles, B
+// staged half per CTA (the B tensor map box has gemm_pair_b_rows() rows).
+bool gemm_pair_eligible(int mode, int64_t M, int64_t N, int sms);
+int gemm_pair_b_rows();
+cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
+                             int sms, cudaStream_t st);
+
 }  // namespace fp8k

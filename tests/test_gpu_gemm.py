@@ -254,3 +254,28 @@ def test_split_k_on_two_streams():
     for o in outs:
         ok, worst = OG.check(o.float().cpu().numpy(), c, e, "bf16")
         assert ok, worst
+
+
+# --------------------------------------------------- CTA pairs (2-SM MMA) --
+
+@pytest.mark.parametrize("mnk", [(2048, 2048, 1024), (1999, 1000, 512), (4096, 768, 2048)])
+@pytest.mark.parametrize("fmts", [("e4m3", "e4m3"), ("e5m2", "e4m3")])
+def test_gemm_tensor_cta_pairs(mnk, fmts):
+    """Shapes large enough for the 256 x 256 CTA-pair path (ragged M and N
+    included); the single-CTA path must agree within the same bound."""
+    F = lib()
+    m, n, k = mnk
+    fa, fb = fmts
+    qa, sa, qb, sb = per_tensor_operands(m, n, k, fa, fb, seed=k + 1)
+    c, e = OG.gemm(OG.dequant_operand(qa, fa, sa), OG.dequant_operand(qb, fb, sb))
+    try:
+        for pairs in (1, 0):
+            F.fp8_set_option(F.OPT_GEMM_CTA_PAIRS, pairs)
+            for out_dtype in ("bf16", "f32"):
+                got = run_tensor(qa, fa, sa, qb, fb, sb, out_dtype)
+                ok, worst = OG.check(got, c, e, out_dtype)
+                assert ok, (pairs, out_dtype, worst)
+    finally:
+        F.fp8_set_option(F.OPT_GEMM_CTA_PAIRS, 1)
+    rc, where = F.fp8_get_last_device_error()
+    assert rc == 0, (rc, where)

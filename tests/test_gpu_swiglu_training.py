@@ -106,8 +106,12 @@ def test_swiglu_training_teacher_forced():
             p_ref, m_ref, v_ref = OT.adamw_step(wm[i], dws[i], mm[i], vv[i], step=t + 1)
             p_gpu = tr.w_master[i].double().cpu().numpy()
             assert np.allclose(p_gpu, p_ref, rtol=2e-6, atol=1e-9), (t, i)
-            assert np.allclose(tr.m[i].double().cpu().numpy(), m_ref, rtol=1e-5, atol=1e-12)
-            assert np.allclose(tr.v[i].double().cpu().numpy(), v_ref, rtol=1e-5, atol=1e-18)
+            # fp32 moments: b*m + (1-b)*g can cancel, so the absolute error is
+            # a couple of fp32 ulps of the larger term, not of the result
+            assert np.allclose(tr.m[i].double().cpu().numpy(), m_ref, rtol=1e-5,
+                               atol=1e-6 * np.max(np.abs(m_ref)))
+            assert np.allclose(tr.v[i].double().cpu().numpy(), v_ref, rtol=1e-5,
+                               atol=1e-6 * np.max(np.abs(v_ref)))
             assert torch.equal(tr.w_bf[i], tr.w_master[i].to(torch.bfloat16))
         hist = tr.hist.cpu().numpy()
         for i in range(9):
