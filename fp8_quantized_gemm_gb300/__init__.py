@@ -27,6 +27,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 # enums (include/fp8gemm.h)
 FP8_OK, FP8_ERR_INVALID_ARG, FP8_ERR_MISALIGNED = 0, -1, -2
 FP8_ERR_UNSUPPORTED, FP8_ERR_CUDA, FP8_ERR_TIMEOUT, FP8_ERR_NO_DEVICE = -3, -4, -5, -6
+FP8_ERR_SCRATCH_LIMIT = -7
 IN_BF16, IN_F32 = 0, 1
 E4M3, E5M2 = 0, 1
 SCALE_F32, SCALE_UE8M0 = 0, 1
@@ -42,6 +43,7 @@ _SIGS = {
     "fp8_gemm_tensor": [_vp, _int, _vp, _int, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp],
     "fp8_gemm_group": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_gemm_mx": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp],
+    "fp8_gemm_group_noalloc": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_delayed_state_update": [_vp, _vp, _vp, _i64, _int, _vp],
     "fp8_swiglu_forward": [_vp, _vp, _vp, _i64, _vp],
     "fp8_swiglu_backward": [_vp, _vp, _vp, _vp, _vp, _i64, _vp],
@@ -151,6 +153,14 @@ def fp8_gemm_group(a, sa, b, sb, sfmt, out, stream=None):
     n = b.shape[0]
     _call("fp8_gemm_group", _p(a), _p(sa), _p(b), _p(sb), sfmt, m, n, k, _p(out), out.stride(0),
           _stream(stream))
+
+
+def fp8_gemm_group_noalloc(a, sa, b, sb, sfmt, out, stream=None):
+    """fp8_gemm_group without any device allocation (fixed in-library scratch)."""
+    m, k = a.shape
+    n = b.shape[0]
+    _call("fp8_gemm_group_noalloc", _p(a), _p(sa), _p(b), _p(sb), sfmt, m, n, k, _p(out),
+          out.stride(0), _stream(stream))
 
 
 def fp8_gemm_mx(a, la, ga, b, lb, gb, out, *, out_dt=None, stream=None):

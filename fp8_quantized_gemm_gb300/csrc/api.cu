@@ -179,6 +179,23 @@ int check_gemm_common(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, 
 
 }  // namespace
 
+namespace fp8k {
+// Internal hooks for entry points defined in other files (noalloc.cu): the
+// per-device setup (SM count, device error word) and the operand tensor map.
+int api_device(int *sms, uint32_t **err) {
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  *sms = d->sms;
+  *err = d->err;
+  return FP8_OK;
+}
+
+int api_encode_operand(CUtensorMap *map, const void *base, int64_t k, int64_t rows, int box_rows) {
+  return encode_operand(map, base, k, rows, box_rows);
+}
+}  // namespace fp8k
+
 extern "C" {
 
 int fp8_amax(const void *x, int in_dt, int64_t n, float *amax_out, fp8_stream_t stream) {
@@ -357,6 +374,7 @@ const char *fp8_status_string(int status) {
     case FP8_ERR_CUDA: return "CUDA runtime error";
     case FP8_ERR_TIMEOUT: return "device-side wait timed out";
     case FP8_ERR_NO_DEVICE: return "no sm_103 device is current";
+    case FP8_ERR_SCRATCH_LIMIT: return "shape exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }

@@ -63,7 +63,8 @@ typedef enum {
   FP8_ERR_UNSUPPORTED = -3, /* format combination or shape the kernels do not cover */
   FP8_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
   FP8_ERR_TIMEOUT = -5,     /* a device-side bounded wait expired (device error word) */
-  FP8_ERR_NO_DEVICE = -6    /* no sm_103 device is current */
+  FP8_ERR_NO_DEVICE = -6,   /* no sm_103 device is current */
+  FP8_ERR_SCRATCH_LIMIT = -7 /* shape needs more than fp8_gemm_group_noalloc's fixed scratch */
 } fp8_status_t;
 
 typedef enum { FP8_IN_BF16 = 0, FP8_IN_F32 = 1 } fp8_in_dtype_t;
@@ -184,6 +185,38 @@ FP8_API int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, 
 FP8_API int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
                    int sfmt, int64_t M, int64_t N, int64_t K, void *c, int64_t ldc,
                    fp8_stream_t stream);
+
+/* ------------------------------------- GEMM, per K group, no allocation --
+ * fp8_gemm_group_noalloc: the same computation, arguments and output as
+ * fp8_gemm_group, for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for this library's
+ * users.
+ *
+ * Why: for small M, fp8_gemm_group splits K across CTAs and keeps fp32
+ * partial sums and per-tile counters in a workspace that it cudaMalloc's the
+ * first time a (device, stream) pair needs it.  A caller that is capturing
+ * the stream into a CUDA graph cannot allocate at that point, and runtimes
+ * that own all device memory in their own pool, or that must never wait on
+ * the allocator, cannot let the library allocate at all.  This entry point
+ * calls no cudaMalloc or cudaFree: its scratch is one array compiled into the
+ * library (64 KiB of counters + 8 MiB of fp32 partials, 256-byte aligned),
+ * which every GPU that loads the library holds until the process exits.
+ *
+ * Limits and rules:
+ *   - A shape whose split-K partials need more than 8 MiB (or more than 16384
+ *     output tiles of counters) is rejected with FP8_ERR_SCRATCH_LIMIT; shapes
+ *     that need no split run without scratch.
+ *   - The first call on each device looks up the array's device address (and
+ *     does the library's per-device set-up); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents; each call clears the counters it uses on its stream.
+ *     Calls that overlap on the GPU (different streams, or concurrent graph
+ *     branches) race on the array and give wrong results: serialize them.
+ */
+FP8_API int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const uint8_t *b,
+                                   const void *sb, int sfmt, int64_t M, int64_t N, int64_t K,
+                                   void *c, int64_t ldc, fp8_stream_t stream);
 
 /* ----------------------------------------------------- GEMM, two level --
  * fp8_gemm_mx: C = S_a * S_b * sum_i r_a[m,i] r_b[n,i] sum_{k in i} a.b
