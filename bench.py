@@ -285,12 +285,22 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """Largest value over all ranks (the timing every rank reports is the
+    slowest rank's)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank: float, steps: int, rank_total_ms: float, world: int) -> float:
+    """Whole-job throughput: the units every rank processed in `steps` steps,
+    over the slowest rank's time (per second)."""
+    slowest_ms = max_over_ranks(rank_total_ms, world)
+    return units_per_rank * steps * world / (slowest_ms / 1e3)
 
 
 def source_digest(files) -> str:
@@ -450,14 +460,14 @@ def run_ours(args):
         raise RuntimeError("device error %d (where %d) during the timed region" % (rc, where))
     step_ms = timer.step_ms()
     eager_total_ms = max_over_ranks(sum(step_ms), world)
-    eager_value = wl.flops * args.steps * world / (eager_total_ms / 1e3) / 1e12
+    eager_value = job_throughput(wl.flops, args.steps, sum(step_ms), world) / 1e12
     if args.eager:
         total_ms, value = eager_total_ms, eager_value
     else:
         with ClockSampler(dev.index) as clk:
             graph_ms = time_graph(wl, args.steps, world, flush)
         total_ms = max_over_ranks(sum(graph_ms), world)
-        value = wl.flops * args.steps * world / (total_ms / 1e3) / 1e12
+        value = job_throughput(wl.flops, args.steps, sum(graph_ms), world) / 1e12
     per = time_isolated(wl, 10, flush, stream)
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # dense FP8 = 2 x bf16 (nominal ratio)
     gemm_ms = sum(per["gemm"]) / len(per["gemm"])

@@ -46,6 +46,8 @@ std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
 // CTA-pair GEMM path switch (on by default; fp8_set_option turns it off).
 bool g_use_pairs = true;
+// Bound of every device-side mbarrier wait (fp8_set_option).
+uint64_t g_wait_limit_ns = 2000000000ull;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
@@ -146,6 +148,7 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
   int rc = device_state(&d);
   if (rc != FP8_OK) return rc;
   args.err = d->err;
+  args.wait_limit_ns = g_wait_limit_ns;
   args.ksplit = fp8k::gemm_ksplit(mode, args.M, args.N, args.K, d->sms);
   args.ws = nullptr;
   args.counters = nullptr;
@@ -180,6 +183,8 @@ int check_gemm_common(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, 
 }  // namespace
 
 namespace fp8k {
+uint64_t wait_limit_ns() { return g_wait_limit_ns; }
+
 // Internal hooks for entry points defined in other files (noalloc.cu): the
 // per-device setup (SM count, device error word) and the operand tensor map.
 int api_device(int *sms, uint32_t **err) {
@@ -405,6 +410,11 @@ int fp8_get_last_device_error(int *where_out, fp8_stream_t stream) {
 int fp8_set_option(int option, int value) {
   if (option == FP8_OPT_GEMM_CTA_PAIRS) {
     g_use_pairs = value != 0;
+    return FP8_OK;
+  }
+  if (option == FP8_OPT_WAIT_LIMIT_US) {
+    if (value < 0) return FP8_ERR_INVALID_ARG;
+    g_wait_limit_ns = (uint64_t)value * 1000ull;
     return FP8_OK;
   }
   return FP8_ERR_INVALID_ARG;

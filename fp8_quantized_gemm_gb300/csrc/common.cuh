@@ -2,8 +2,9 @@
 // mbarriers, TMA (cp.async.bulk.tensor), tcgen05 (TMEM alloc, MMA, commit,
 // ld/st, cp) and FP8 conversion, plus the bounded-wait policy.
 //
-// Every spin on an mbarrier is bounded by %globaltimer: after kWaitLimitNs the
-// waiter records FP8_ERR_TIMEOUT in the library's device error word, raises a
+// Every spin on an mbarrier is bounded by %globaltimer: after the wait limit
+// (kWaitLimitNs by default; settable per call through the error-word struct,
+// which the failure tests use to make waits run out) the waiter records FP8_ERR_TIMEOUT in the library's device error word, raises a
 // CTA-wide abort flag in shared memory (so the other roles stop waiting too)
 // and returns false; the kernel then runs its normal teardown (TMEM dealloc)
 // and exits.  Nothing here traps.
@@ -25,7 +26,8 @@ __device__ __forceinline__ float fmt_max(int fmt) { return fmt == 0 ? kE4M3Max :
 
 // ------------------------------------------------------------ error word --
 struct DevErr {
-  uint32_t *word;  // [0] = first error code (positive), [1] = where
+  uint32_t *word;     // [0] = first error code (positive), [1] = where
+  uint64_t limit_ns;  // bound of every wait
 };
 
 __device__ __forceinline__ void record_error(DevErr e, uint32_t code, uint32_t where) {
@@ -92,17 +94,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           DevErr err, uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 0u) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        record_error(err, kErrTimeout, where);
-        return false;
-      }
+    if (*abort) return false;
+    if (globaltimer() - t0 > err.limit_ns) {
+      *abort = 1;
+      record_error(err, kErrTimeout, where);
+      return false;
     }
   }
+}
+
+// mbar_wait for a whole warp: every lane calls it; the result is the same on
+// all lanes (a lane that gave up makes the warp give up), so warp-collective
+// instructions after it (elect.sync, tcgen05.ld .sync.aligned) never run on a
+// partial warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort,
+                                               DevErr err, uint32_t where) {
+  const bool ok = mbar_wait(bar, parity, abort, err, where);
+  return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // -------------------------------------------------------------------- TMA --

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
-  const DevErr err{args.err};
+  const DevErr err{args.err, args.wait_limit_ns};
 
   auto sA = [&](int s) { return smem_u32(tiles + s * (C::kABytes + C::kBBytes)); };
   auto sB = [&](int s) { return smem_u32(tiles + s * (C::kABytes + C::kBBytes) + C::kABytes); };
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
           if (un < num_units)
             load_sf(unit_tile(un), kb + 1 < kb1 ? kb + 1 : kb_begin(un), sfa_nxt, sfb_nxt);
         }
-        if (!mbar_wait(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) {
+        if (!mbar_wait_warp(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) {
           ok = false;
           break;
         }
@@ -327,7 +327,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
         const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
         const int64_t row = m0 + 32 * q + lane;
         const uint32_t buf = j % C::kAccBufs, use = j / C::kAccBufs;
-        if (!mbar_wait(accf_bar(buf), use & 1u, abort_flag, err, 3)) break;
+        const bool got = mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3);
+        if (ks == 1 && !got) break;
+        // split K: every epilogue warp learns whether any gave up before the
+        // named barriers of the split arrival
+        if (ks > 1 && epi_any<C::kEpiWarps * 32>(!got)) break;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -384,7 +388,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
           const float s_cur = sa_next * __ldg(sb_row + kb);
           if (kb + 1 < kb1)
             sa_next = row < args.M ? __ldg(sa + (int64_t)(kb + 1) * args.M + row) : 0.0f;
-          if (!mbar_wait(accf_bar(buf), use & 1u, abort_flag, err, 3)) {
+          if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) {
             ok = false;
             break;
           }
@@ -403,7 +407,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
             acc[32 + i] = fmaf(s_cur, __uint_as_float(r1[i]), acc[32 + i]);
           }
         }
-        if (!ok) break;
+        if (ks == 1 && !ok) break;
+        if (ks > 1 && epi_any<C::kEpiWarps * 32>(!ok)) break;
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = acc[i];

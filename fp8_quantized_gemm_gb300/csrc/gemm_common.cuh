@@ -97,4 +97,21 @@ __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kThreadsEpi) : "memory");
 }
 
+// Barrier among the epilogue warps that returns the OR of every thread's
+// predicate: one decision ("some wait ran out") for all of them before any
+// further named barrier.
+template <int kThreadsEpi>
+__device__ __forceinline__ bool epi_any(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p), "r"(kThreadsEpi)
+      : "memory");
+  return r != 0;
+}
+
 }  // namespace fp8k

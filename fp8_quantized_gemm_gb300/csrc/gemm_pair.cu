@@ -55,7 +55,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
   const uint32_t lane = lane_id();
   const uint32_t rank = cluster_ctarank();
   const bool leader = (rank == 0);
-  const DevErr err{args.err};
+  const DevErr err{args.err, args.wait_limit_ns};
 
   auto sA = [&](int s) { return smem_u32(smem + s * C::kStageBytes); };
   auto sB = [&](int s) { return smem_u32(smem + s * C::kStageBytes + C::kABytes); };
@@ -107,7 +107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = (int)(it % STAGES);
         const uint32_t round = it / STAGES;
-        if (!mbar_wait(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) {
+        if (!mbar_wait_warp(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) {
           ok = false;
           break;
         }
@@ -183,7 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
       const int64_t n0 = (t % tiles_n) * BN;
       const int64_t row = m0 + 32 * q + lane;
       const uint32_t buf = j & 1u, use = j >> 1;
-      if (!mbar_wait(accf_bar(buf), use & 1u, abort_flag, err, 3)) break;
+      if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {

@@ -43,6 +43,7 @@ struct GemmArgs {
   const void *sa, *sb;         // scale operands (meaning depends on the mode)
   const float *ga, *gb;        // global factors (kScaleMx)
   uint32_t *err;               // device error word
+  uint64_t wait_limit_ns;      // bound of every mbarrier wait
   // split-K (small M): ksplit > 1 splits every tile's K range; fp32 partials
   // go to ws [ksplit][M][N] and counters[tile] counts finished splits (the
   // last one reduces in split order and resets the counter to 0)
@@ -50,6 +51,9 @@ struct GemmArgs {
   float *ws;
   uint32_t *counters;
 };
+
+// Wait bound the API passes to kernels (fp8_set_option FP8_OPT_WAIT_LIMIT_NS).
+uint64_t wait_limit_ns();
 
 // Split count the launcher would use for this shape (1 = no split).
 int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms);

@@ -78,6 +78,7 @@ extern "C" int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const ui
   args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
   args.out_dt = FP8_OUT_BF16; args.ldc = ldc; args.c = c; args.sa = sa; args.sb = sb;
   args.err = err;
+  args.wait_limit_ns = fp8k::wait_limit_ns();
   args.vec_store = (aligned16(c) && (ldc * 2) % 16 == 0) ? 1 : 0;
   args.ksplit = fp8k::gemm_ksplit(mode, M, N, K, sms);
   const cudaStream_t st = (cudaStream_t)stream;

@@ -278,11 +278,16 @@ FP8_API int fp8_get_last_device_error(int *where_out, fp8_stream_t stream);
 FP8_API const char *fp8_version(void);
 
 /* fp8_set_option: process-wide switches (not thread-safe against concurrent
- * GEMM calls).  FP8_OPT_GEMM_CTA_PAIRS: 1 (default) lets fp8_gemm_tensor run
- * large shapes on CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles); 0 keeps
- * every GEMM on single-CTA 128 x 256 tiles.  Results agree within the GEMM
- * bound either way. */
-typedef enum { FP8_OPT_GEMM_CTA_PAIRS = 1 } fp8_option_t;
+ * GEMM calls).
+ *   FP8_OPT_GEMM_CTA_PAIRS: 1 (default) lets fp8_gemm_tensor run large shapes
+ *     on CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles); 0 keeps every GEMM
+ *     on single-CTA 128 x 256 tiles.  Results agree within the GEMM bound.
+ *   FP8_OPT_WAIT_LIMIT_US: bound, in microseconds, of every device-side
+ *     mbarrier wait of later GEMM launches (default 2,000,000).  A wait that
+ *     runs out records FP8_ERR_TIMEOUT in the device error word and the
+ *     kernel exits cleanly (output undefined).  Small values exist to test
+ *     that path. */
+typedef enum { FP8_OPT_GEMM_CTA_PAIRS = 1, FP8_OPT_WAIT_LIMIT_US = 2 } fp8_option_t;
 FP8_API int fp8_set_option(int option, int value);
 
 #ifdef __cplusplus
