@@ -124,22 +124,25 @@ __global__ void __launch_bounds__(512) amax_kernel(const T *__restrict__ x, int6
   uint32_t key = 0;
   const int64_t nvec = n / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  // four independent 16-byte loads in flight per thread
-  for (; i + 3 * stride < nvec; i += 4 * stride) {
-    float v[4][8];
+  // batches of eight independent 16-byte loads per thread, all issued first
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec;
+       base += 8 * stride) {
+    // loads are unconditional (index clamped in range) so that all eight are
+    // in flight at once; out-of-range vectors are masked after the loads
+    Raw8<T> raw[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) Vec8<T>::load(x + (i + u * stride) * 8, v[u]);
+    for (int u = 0; u < 8; ++u) {
+      const int64_t i = base + u * stride;
+      raw[u].load_stream(x + (i < nvec ? i : nvec - 1) * 8);
+    }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < 8; ++u) {
+      if (base + u * stride >= nvec) continue;
+      float v[8];
+      raw[u].decode(v);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[u][j]));
-  }
-  for (; i < nvec; i += stride) {
-    float v[8];
-    Vec8<T>::load(x + i * 8, v);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
+      for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
+    }
   }
   for (int64_t i = nvec * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
     key = max(key, abs_key(load1(x + i)));
@@ -210,7 +213,7 @@ __device__ __forceinline__ uint64_t transpose8x8(const uint64_t (&r)[8], int j) 
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
     quant_tensor_t_kernel(const T *__restrict__ x, int64_t rows, int64_t cols, int fmt,
                           const float *amax_in, const float *scale_in, float *scale_out,
                           uint8_t *__restrict__ q, uint8_t *__restrict__ qt,
@@ -218,58 +221,77 @@ __global__ void __launch_bounds__(256)
   __shared__ __align__(16) uint8_t tile[kTT * kTPitch];
   const float mx = fmt_max(fmt);
   const float s = resolve_scale(amax_in, scale_in, mx);
-  if (scale_out != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-    *scale_out = s;
-  const int64_t r0 = (int64_t)blockIdx.y * kTT, c0 = (int64_t)blockIdx.x * kTT;
+  if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+  const int64_t tiles_c = (cols + kTT - 1) / kTT;
+  const int64_t ntiles = ((rows + kTT - 1) / kTT) * tiles_c;
   const int t = threadIdx.x;
-  uint32_t key = 0;
-  // phase 1: 16 vectors of 8 per tile row; 256 threads cover 16 rows per
-  // pass.  All eight loads of the thread are issued before any is used.
   const int lc = (t & 15) * 8;
-  const int64_t c = c0 + lc;
-  Raw8<T> raw[kTT / 16];
+  uint32_t key = 0;
+  // Persistent CTAs loop over 128 x 128 tiles; the eight 16-byte loads of the
+  // NEXT tile are issued before the current tile is processed.
+  auto load_tile = [&](int64_t tl, Raw8<T> (&raw)[kTT / 16]) {
+    const int64_t r0 = (tl / tiles_c) * kTT, c = (tl % tiles_c) * kTT + lc;
 #pragma unroll
-  for (int pass = 0; pass < kTT / 16; ++pass) {
-    const int64_t r = r0 + pass * 16 + (t >> 4);
-    if (r < rows && c < cols)
-      raw[pass].load_stream(x + r * cols + c);
-    else
-      raw[pass].zero();
-  }
+    for (int pass = 0; pass < kTT / 16; ++pass) {
+      const int64_t r = r0 + pass * 16 + (t >> 4);
+      if (r < rows && c < cols)
+        raw[pass].load_stream(x + r * cols + c);
+      else
+        raw[pass].zero();
+    }
+  };
+  constexpr bool kPrefetch = sizeof(T) == 2;  // fp32 inputs: registers too tight
+  Raw8<T> cur[kTT / 16], nxt[kTT / 16];
+  if (kPrefetch && (int64_t)blockIdx.x < ntiles) load_tile(blockIdx.x, cur);
+  for (int64_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x) {
+    if constexpr (kPrefetch) {
+      if (tl + gridDim.x < ntiles) load_tile(tl + gridDim.x, nxt);
+    } else {
+      load_tile(tl, cur);
+    }
+    const int64_t r0 = (tl / tiles_c) * kTT, c0 = (tl % tiles_c) * kTT;
+    const int64_t c = c0 + lc;
+    // phase 1: quantize, row-major store, stage the codes in shared memory
 #pragma unroll
-  for (int pass = 0; pass < kTT / 16; ++pass) {
-    const int lr = pass * 16 + (t >> 4);
-    const int64_t r = r0 + lr;
-    float v[8], y[8];
-    raw[pass].decode(v);
+    for (int pass = 0; pass < kTT / 16; ++pass) {
+      const int lr = pass * 16 + (t >> 4);
+      const int64_t r = r0 + lr;
+      float v[8], y[8];
+      cur[pass].decode(v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        key = max(key, abs_key(v[j]));
+        y[j] = q_prep(v[j], s, mx);
+      }
+      const uint2 packed = pack8(fmt, y);
+      if (r < rows && c < cols) *reinterpret_cast<uint2 *>(q + r * cols + c) = packed;
+      *reinterpret_cast<uint2 *>(&tile[lr * kTPitch + tchunk(lr, lc >> 3)]) = packed;
+    }
+    __syncthreads();
+    // phase 2: thread -> one 8x8 byte block; 16 threads per q_t row segment
+    const int rb = t & 15, cb = t >> 4;
+    uint64_t rr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      rr[i] = *reinterpret_cast<const uint64_t *>(&tile[(rb * 8 + i) * kTPitch + tchunk(rb * 8 + i, cb)]);
+    const int64_t orow0 = c0 + cb * 8;  // q_t row = input column
+    const int64_t ocol = r0 + rb * 8;   // q_t column = input row
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      key = max(key, abs_key(v[j]));
-      y[j] = q_prep(v[j], s, mx);
+      const int64_t orow = orow0 + j;
+      if (orow >= cols) break;
+      const uint64_t w = transpose8x8(rr, j);
+      uint8_t *dst = qt + orow * rows + ocol;
+      if (ocol + 8 <= rows && (rows & 7) == 0) {
+        *reinterpret_cast<uint64_t *>(dst) = w;
+      } else {
+        for (int i = 0; i < 8 && ocol + i < rows; ++i) dst[i] = (uint8_t)(w >> (8 * i));
+      }
     }
-    const uint2 packed = pack8(fmt, y);
-    if (r < rows && c < cols) *reinterpret_cast<uint2 *>(q + r * cols + c) = packed;
-    *reinterpret_cast<uint2 *>(&tile[lr * kTPitch + tchunk(lr, lc >> 3)]) = packed;
-  }
-  __syncthreads();
-  // phase 2: thread -> one 8x8 byte block; 16 threads per q_t row segment
-  const int rb = t & 15, cb = t >> 4;
-  uint64_t rr[8];
+    __syncthreads();  // the tile buffer is rewritten by the next iteration
+    if constexpr (kPrefetch) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    rr[i] = *reinterpret_cast<const uint64_t *>(&tile[(rb * 8 + i) * kTPitch + tchunk(rb * 8 + i, cb)]);
-  const int64_t orow0 = c0 + cb * 8;  // q_t row = input column
-  const int64_t ocol = r0 + rb * 8;   // q_t column = input row
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int64_t orow = orow0 + j;
-    if (orow >= cols) break;
-    const uint64_t w = transpose8x8(rr, j);
-    uint8_t *dst = qt + orow * rows + ocol;
-    if (ocol + 8 <= rows && (rows & 7) == 0) {
-      *reinterpret_cast<uint64_t *>(dst) = w;
-    } else {
-      for (int i = 0; i < 8 && ocol + i < rows; ++i) dst[i] = (uint8_t)(w >> (8 * i));
+      for (int pass = 0; pass < kTT / 16; ++pass) cur[pass] = nxt[pass];
     }
   }
   if (amax_out != nullptr) block_max_to(key, amax_out);
@@ -546,7 +568,9 @@ cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t 
       quant_tensor_kernel<float><<<blocks, threads, 0, st>>>(
           static_cast<const float *>(x), n, fmt, amax_in, scale, scale_out, q, ao);
   } else {
-    dim3 grid((unsigned)((cols + kTT - 1) / kTT), (unsigned)((rows + kTT - 1) / kTT));
+    const int64_t ntiles = ((cols + kTT - 1) / kTT) * ((rows + kTT - 1) / kTT);
+    const int64_t cap = (int64_t)sms * 2;
+    const unsigned grid = (unsigned)(ntiles < cap ? ntiles : cap);
     if (in_dt == 0)
       quant_tensor_t_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
           static_cast<const __nv_bfloat16 *>(x), rows, cols, fmt, amax_in, scale, scale_out,
