@@ -42,6 +42,7 @@ _SIGS = {
     "fp8_quantize_mx": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp],
     "fp8_gemm_tensor": [_vp, _int, _vp, _int, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp],
     "fp8_gemm_group": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
+    "fp8_gemm_tensor_grouped": [_vp, _int, _vp],
     "fp8_gemm_mx": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp],
     "fp8_gemm_group_noalloc": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_delayed_state_update": [_vp, _vp, _vp, _i64, _int, _vp],
@@ -146,6 +147,27 @@ def fp8_gemm_tensor(a, fa, b, fb, sa, sb, out, *, out_dt=None, accumulate=False,
         out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
     _call("fp8_gemm_tensor", _p(a), fa, _p(b), fb, _p(sa), _p(sb), m, n, k, out_dt, _p(out),
           out.stride(0), int(bool(accumulate)), _stream(stream))
+
+
+class GemmProblem(ctypes.Structure):
+    """fp8_gemm_problem_t (include/fp8gemm.h)."""
+    _fields_ = [("a", _vp), ("b", _vp), ("sa", _vp), ("sb", _vp), ("M", _i64), ("N", _i64),
+                ("K", _i64), ("fa", _int), ("fb", _int), ("out_dt", _int), ("accumulate", _int),
+                ("c", _vp), ("ldc", _i64)]
+
+
+def gemm_problem(a, fa, b, fb, sa, sb, out, *, accumulate=False):
+    """Descriptor of one per-tensor GEMM for fp8_gemm_tensor_grouped."""
+    m, k = a.shape
+    n = b.shape[0]
+    out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    return GemmProblem(_p(a), _p(b), _p(sa), _p(sb), m, n, k, fa, fb, out_dt,
+                       int(bool(accumulate)), _p(out), out.stride(0))
+
+
+def fp8_gemm_tensor_grouped(problems, stream=None):
+    arr = (GemmProblem * len(problems))(*problems)
+    _call("fp8_gemm_tensor_grouped", ctypes.cast(arr, _vp), len(problems), _stream(stream))
 
 
 def fp8_gemm_group(a, sa, b, sb, sfmt, out, stream=None):

@@ -290,6 +290,67 @@ int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, const fl
   return run_gemm(fp8k::kScaleTensor, a, b, args, (cudaStream_t)stream);
 }
 
+int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_stream_t stream) {
+  if (problems == nullptr || count < 1 || count > 64) return FP8_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    const fp8_gemm_problem_t &p = problems[i];
+    int rc = check_gemm_common(p.a, p.b, p.M, p.N, p.K, 16);
+    if (rc != FP8_OK) return rc;
+    if (p.sa == nullptr || p.sb == nullptr || !valid_fmt(p.fa) || !valid_fmt(p.fb))
+      return FP8_ERR_INVALID_ARG;
+    if ((rc = check_output(p.c, p.N, p.ldc, p.out_dt)) != FP8_OK) return rc;
+    if (p.accumulate != 0 && (p.accumulate != 1 || p.out_dt != FP8_OUT_F32))
+      return FP8_ERR_UNSUPPORTED;
+  }
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  const cudaStream_t st = (cudaStream_t)stream;
+  // one persistent CTA-pair launch when every problem takes that path
+  bool together = g_use_pairs && count <= fp8k::kMaxGroup;
+  int64_t tiles = 0;
+  for (int i = 0; i < count && together; ++i) {
+    const fp8_gemm_problem_t &p = problems[i];
+    together = fp8k::gemm_ksplit(fp8k::kScaleTensor, p.M, p.N, p.K, d->sms) == 1;
+    tiles += ((p.M + 255) / 256) * ((p.N + 255) / 256);
+  }
+  together = together && tiles * 4 >= d->sms / 2;
+  if (!together) {
+    for (int i = 0; i < count; ++i) {
+      const fp8_gemm_problem_t &p = problems[i];
+      if ((rc = fp8_gemm_tensor(p.a, p.fa, p.b, p.fb, p.sa, p.sb, p.M, p.N, p.K, p.out_dt, p.c,
+                                p.ldc, p.accumulate, stream)) != FP8_OK)
+        return rc;
+    }
+    return FP8_OK;
+  }
+  // longest K first: the strided tile assignment then balances the pairs
+  int order[fp8k::kMaxGroup];
+  for (int i = 0; i < count; ++i) order[i] = i;
+  for (int i = 1; i < count; ++i)
+    for (int j = i; j > 0 && problems[order[j]].K > problems[order[j - 1]].K; --j) {
+      const int tmp = order[j];
+      order[j] = order[j - 1];
+      order[j - 1] = tmp;
+    }
+  CUtensorMap tma[fp8k::kMaxGroup], tmb[fp8k::kMaxGroup];
+  GemmArgs args[fp8k::kMaxGroup];
+  for (int k = 0; k < count; ++k) {
+    const fp8_gemm_problem_t &p = problems[order[k]];
+    GemmArgs a{};
+    a.M = p.M; a.N = p.N; a.K = p.K; a.fa = p.fa; a.fb = p.fb; a.out_dt = p.out_dt;
+    a.accumulate = p.accumulate; a.ldc = p.ldc; a.c = p.c; a.sa = p.sa; a.sb = p.sb;
+    a.err = d->err;
+    a.wait_limit_ns = g_wait_limit_ns;
+    a.vec_store = vector_store_ok(p.c, p.ldc, p.out_dt);
+    a.ksplit = 1;
+    args[k] = a;
+    if ((rc = encode_operand(&tma[k], p.a, p.K, p.M, 128)) != FP8_OK) return rc;
+    if ((rc = encode_operand(&tmb[k], p.b, p.K, p.N, fp8k::gemm_pair_b_rows())) != FP8_OK) return rc;
+  }
+  return to_status(fp8k::launch_gemm_pair_group(tma, tmb, args, count, d->sms, st));
+}
+
 int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb, int sfmt,
                    int64_t M, int64_t N, int64_t K, void *c, int64_t ldc, fp8_stream_t stream) {
   int rc = check_gemm_common(a, b, M, N, K, 128);

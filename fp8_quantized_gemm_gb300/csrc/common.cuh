@@ -340,10 +340,13 @@ __device__ __forceinline__ uint16_t cvt_fp8x2(int fmt, float lo, float hi) {
   return fmt == 0 ? cvt_e4m3x2(lo, hi) : cvt_e5m2x2(lo, hi);
 }
 
-// Quantize one value: fl32(x / s), clipped to +-MAX (the cast then rounds).
+// Quantize one value: fl32(x / s); the clip to +-MAX is done by the
+// saturating conversion (cvt.rn.satfinite rounds to nearest even and clamps
+// finite values beyond the largest finite code to it, which for every finite
+// y equals rounding clip(y, -MAX, MAX)).
 __device__ __forceinline__ float q_prep(float x, float s, float mx) {
-  float y = __fdiv_rn(x, s);
-  return fminf(fmaxf(y, -mx), mx);
+  (void)mx;
+  return __fdiv_rn(x, s);
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }

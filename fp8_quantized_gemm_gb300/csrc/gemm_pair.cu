@@ -1,4 +1,5 @@
-// Per-tensor scaled-FP8 GEMM on CTA pairs (tcgen05 cta_group::2).
+// Per-tensor scaled-FP8 GEMM on CTA pairs (tcgen05 cta_group::2), for one
+// problem or a group of independent problems in one launch.
 //
 // A cluster of two CTAs on neighbouring SMs computes one 256 x BN output tile
 // with M = 256 MMAs issued by the even CTA (the leader):
@@ -16,6 +17,14 @@
 //
 // Two TMEM accumulators per CTA: the epilogue of one tile overlaps the MMAs
 // of the next.  Scales are applied once in the epilogue (Flax guide 2.2).
+//
+// Grouped launch: up to kMaxGroup independent problems (each with its own
+// operands, formats, scales and output) share one persistent tile space, the
+// problems' tiles laid end to end.  The host orders the problems longest-K
+// first so that the strided tile assignment stays balanced.  One launch pays
+// the prologue, pipeline fill and tail once for all of them (the Float8
+// linear's y, dx and dW GEMMs are independent once their operands are
+// quantized).
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "kernels.h"
@@ -39,10 +48,24 @@ struct PairCfg {
   static_assert(kSmem <= 227 * 1024, "shared-memory budget");
 };
 
+struct PairGroup {
+  CUtensorMap tma[kMaxGroup];
+  CUtensorMap tmb[kMaxGroup];
+  GemmArgs args[kMaxGroup];
+  int64_t tile_begin[kMaxGroup + 1];  // problem i owns tiles [tile_begin[i], tile_begin[i+1])
+  int count;
+};
+
+// Problem owning global tile t (the group is small: a linear scan).
+__device__ __forceinline__ int group_of(const PairGroup &g, int64_t t) {
+  int i = 0;
+  while (i + 1 < g.count && t >= g.tile_begin[i + 1]) ++i;
+  return i;
+}
+
 template <int BN, int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>::kThreads, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tma,
-                     const __grid_constant__ CUtensorMap tmb, const GemmArgs args) {
+    gemm_pair_kernel(const __grid_constant__ PairGroup grp) {
   using C = PairCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -55,7 +78,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
   const uint32_t lane = lane_id();
   const uint32_t rank = cluster_ctarank();
   const bool leader = (rank == 0);
-  const DevErr err{args.err, args.wait_limit_ns};
+  const DevErr err{grp.args[0].err, grp.args[0].wait_limit_ns};
 
   auto sA = [&](int s) { return smem_u32(smem + s * C::kStageBytes); };
   auto sB = [&](int s) { return smem_u32(smem + s * C::kStageBytes + C::kABytes); };
@@ -78,9 +101,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tma);
-    tma_prefetch_desc(&tmb);
+  if (warp == 0 && lane < (uint32_t)grp.count) {
+    tma_prefetch_desc(&grp.tma[lane]);
+    tma_prefetch_desc(&grp.tmb[lane]);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
@@ -89,22 +112,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // pair p takes 256 x BN tiles p, p + npairs, ...; tile t covers rows
-  // (t / tiles_n) * 256 (this CTA: + rank * 128) and columns (t % tiles_n) * BN
+  // pair p takes global tiles p, p + npairs, ...; within problem i, local
+  // tile t covers rows (t / tiles_n) * 256 (this CTA: + rank * 128) and
+  // columns (t % tiles_n) * BN
   const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int64_t tiles_n = (args.N + BN - 1) / BN;
-  const int64_t num_tiles = ((args.M + 255) / 256) * tiles_n;
-  const int KB = (int)((args.K + C::BK - 1) / C::BK);
+  const int64_t num_tiles = grp.tile_begin[grp.count];
+  struct TileRef {
+    int i;
+    int64_t m0, n0;
+    int kb_count;
+  };
+  auto tile_ref = [&](int64_t gt) {
+    TileRef r;
+    r.i = group_of(grp, gt);
+    const GemmArgs &a = grp.args[r.i];
+    const int64_t t = gt - grp.tile_begin[r.i];
+    const int64_t tiles_n = (a.N + BN - 1) / BN;
+    r.m0 = (t / tiles_n) * 256;
+    r.n0 = (t % tiles_n) * BN;
+    r.kb_count = (int)((a.K + C::BK - 1) / C::BK);
+    return r;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint32_t full_leader0 = mapa_shared(full_bar(0), 0);
     uint32_t it = 0;
     bool ok = true;
-    for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
-      const int64_t m0 = (t / tiles_n) * 256 + rank * C::BM;
-      const int64_t nb0 = (t % tiles_n) * BN + rank * (BN / 2);
-      for (int kb = 0; kb < KB; ++kb, ++it) {
+    for (int64_t gt = pair; gt < num_tiles && ok; gt += npairs) {
+      const TileRef tr = tile_ref(gt);
+      const CUtensorMap *ma = &grp.tma[tr.i];
+      const CUtensorMap *mb = &grp.tmb[tr.i];
+      const int64_t m0 = tr.m0 + rank * C::BM;
+      const int64_t nb0 = tr.n0 + rank * (BN / 2);
+      for (int kb = 0; kb < tr.kb_count; ++kb, ++it) {
         const int s = (int)(it % STAGES);
         const uint32_t round = it / STAGES;
         if (!mbar_wait_warp(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) {
@@ -114,12 +155,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
         if (elect_one()) {
           if (leader) {
             mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
-            tma_load_2d(sA(s), &tma, full_bar(s), kb * C::BK, (int32_t)m0);
-            tma_load_2d(sB(s), &tmb, full_bar(s), kb * C::BK, (int32_t)nb0);
+            tma_load_2d(sA(s), ma, full_bar(s), kb * C::BK, (int32_t)m0);
+            tma_load_2d(sB(s), mb, full_bar(s), kb * C::BK, (int32_t)nb0);
           } else {
             const uint32_t fb = full_leader0 + 8u * (uint32_t)s;
-            tma_load_2d_pair(sA(s), &tma, fb, kb * C::BK, (int32_t)m0);
-            tma_load_2d_pair(sB(s), &tmb, fb, kb * C::BK, (int32_t)nb0);
+            tma_load_2d_pair(sA(s), ma, fb, kb * C::BK, (int32_t)m0);
+            tma_load_2d_pair(sB(s), mb, fb, kb * C::BK, (int32_t)nb0);
           }
         }
         __syncwarp();
@@ -136,17 +177,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
   } else if (warp == 1) {
     // ----------------------------------------------------- MMA (leader only)
     if (leader && elect_one()) {
-      const uint32_t idesc = idesc_f8f6f4(256, BN, args.fa, args.fb);
       uint32_t it = 0, j = 0;
       bool ok = true;
-      for (int64_t t = pair; t < num_tiles && ok; t += npairs, ++j) {
+      for (int64_t gt = pair; gt < num_tiles && ok; gt += npairs, ++j) {
+        const TileRef tr = tile_ref(gt);
+        const uint32_t idesc = idesc_f8f6f4(256, BN, grp.args[tr.i].fa, grp.args[tr.i].fb);
         const uint32_t buf = j & 1u, use = j >> 1;
         if (!mbar_wait(acce_bar(buf), (use & 1u) ^ 1u, abort_flag, err, 2)) {
           ok = false;
           break;
         }
         const uint32_t d = tmem + buf * BN;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int kb = 0; kb < tr.kb_count; ++kb, ++it) {
           const int s = (int)(it % STAGES);
           const uint32_t round = it / STAGES;
           if (!mbar_wait(full_bar(s), round & 1u, abort_flag, err, 2)) {
@@ -175,13 +217,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
     const uint32_t q = warp & 3u;
     const uint32_t lane_base = tmem + ((32u * q) << 16);
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
-    const float alpha =
-        *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
     uint32_t j = 0;
-    for (int64_t t = pair; t < num_tiles; t += npairs, ++j) {
-      const int64_t m0 = (t / tiles_n) * 256 + rank * C::BM;
-      const int64_t n0 = (t % tiles_n) * BN;
-      const int64_t row = m0 + 32 * q + lane;
+    for (int64_t gt = pair; gt < num_tiles; gt += npairs, ++j) {
+      const TileRef tr = tile_ref(gt);
+      const GemmArgs &a = grp.args[tr.i];
+      const float alpha = *static_cast<const float *>(a.sa) * *static_cast<const float *>(a.sb);
+      const int64_t row = tr.m0 + rank * C::BM + 32 * q + lane;
       const uint32_t buf = j & 1u, use = j >> 1;
       if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) break;
       tc_fence_after();
@@ -198,7 +239,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
-        store_row32(args, row, n0 + c, v);
+        store_row32(a, row, tr.n0 + c, v);
       }
     }
   }
@@ -213,16 +254,20 @@ constexpr int kPairBN = 256, kPairStages = 6;
 
 int gemm_pair_b_rows() { return kPairBN / 2; }
 
+int64_t gemm_pair_tiles(int64_t M, int64_t N) {
+  return ((M + 255) / 256) * ((N + kPairBN - 1) / kPairBN);
+}
+
 // CTA pairs pay off when the 256-row tiles still give every pair work.
 bool gemm_pair_eligible(int mode, int64_t M, int64_t N, int sms) {
   if (mode != kScaleTensor) return false;
-  const int64_t tiles = ((M + 255) / 256) * ((N + kPairBN - 1) / kPairBN);
-  return tiles * 4 >= sms / 2;
+  return gemm_pair_tiles(M, N) * 4 >= sms / 2;
 }
 
-cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
-                             int sms, cudaStream_t st) {
+cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tmb,
+                                   const GemmArgs *args, int count, int sms, cudaStream_t st) {
   using C = PairCfg<kPairBN, kPairStages>;
+  if (count < 1 || count > kMaxGroup) return cudaErrorInvalidValue;
   auto kern = gemm_pair_kernel<kPairBN, kPairStages>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -234,10 +279,25 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb, con
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const int64_t tiles = ((args.M + 255) / 256) * ((args.N + kPairBN - 1) / kPairBN);
+  PairGroup g{};
+  g.count = count;
+  g.tile_begin[0] = 0;
+  for (int i = 0; i < count; ++i) {
+    g.tma[i] = tma[i];
+    g.tmb[i] = tmb[i];
+    g.args[i] = args[i];
+    g.tile_begin[i + 1] = g.tile_begin[i] + gemm_pair_tiles(args[i].M, args[i].N);
+  }
+  for (int i = count; i < kMaxGroup; ++i) g.tile_begin[i + 1] = g.tile_begin[count];
+  const int64_t tiles = g.tile_begin[count];
   const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
-  kern<<<(unsigned)(2 * pairs), C::kThreads, C::kSmem, st>>>(tma, tmb, args);
+  kern<<<(unsigned)(2 * pairs), C::kThreads, C::kSmem, st>>>(g);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
+                             int sms, cudaStream_t st) {
+  return launch_gemm_pair_group(&tma, &tmb, &args, 1, sms, st);
 }
 
 }  // namespace fp8k

@@ -67,6 +67,10 @@ cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb
 // CTA-pair (cta_group::2) variant of the per-tensor GEMM: 256 x 256 tiles, B
 // staged half per CTA (the B tensor map box has gemm_pair_b_rows() rows).
 bool gemm_pair_eligible(int mode, int64_t M, int64_t N, int sms);
+constexpr int kMaxGroup = 4;  // problems per grouped launch
+// One launch over `count` independent per-tensor problems (longest K first).
+cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tmb,
+                                   const GemmArgs *args, int count, int sms, cudaStream_t st);
 int gemm_pair_b_rows();
 cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
                              int sms, cudaStream_t st);

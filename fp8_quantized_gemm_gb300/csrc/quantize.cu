@@ -156,7 +156,7 @@ __device__ __forceinline__ float resolve_scale(const float *amax_in, const float
 }
 
 // Row-major output only: grid-stride over 8-element vectors.
-template <typename T>
+template <typename T, bool kAmax>
 __global__ void __launch_bounds__(512)
     quant_tensor_kernel(const T *__restrict__ x, int64_t n, int fmt, const float *amax_in,
                         const float *scale_in, float *scale_out, uint8_t *__restrict__ q,
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(512)
       float y[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        key = max(key, abs_key(v[u][j]));
+        if (kAmax) key = max(key, abs_key(v[u][j]));
         y[j] = q_prep(v[u][j], s, mx);
       }
       reinterpret_cast<uint2 *>(q)[i + u * stride] = pack8(fmt, y);
@@ -188,12 +188,12 @@ __global__ void __launch_bounds__(512)
     Vec8<T>::load_stream(x + i * 8, v);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      key = max(key, abs_key(v[j]));
+      if (kAmax) key = max(key, abs_key(v[j]));
       y[j] = q_prep(v[j], s, mx);
     }
     reinterpret_cast<uint2 *>(q)[i] = pack8(fmt, y);
   }
-  if (amax_out != nullptr) block_max_to(key, amax_out);
+  if (kAmax) block_max_to(key, amax_out);
 }
 
 // Row-major output plus the transposed copy q_t [cols, rows], in 128 x 128
@@ -212,7 +212,7 @@ __device__ __forceinline__ uint64_t transpose8x8(const uint64_t (&r)[8], int j) 
   return out;
 }
 
-template <typename T>
+template <typename T, bool kAmax>
 __global__ void __launch_bounds__(256, 2)
     quant_tensor_t_kernel(const T *__restrict__ x, int64_t rows, int64_t cols, int fmt,
                           const float *amax_in, const float *scale_in, float *scale_out,
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(256, 2)
       cur[pass].decode(v);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        key = max(key, abs_key(v[j]));
+        if (kAmax) key = max(key, abs_key(v[j]));
         y[j] = q_prep(v[j], s, mx);
       }
       const uint2 packed = pack8(fmt, y);
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(256, 2)
       for (int pass = 0; pass < kTT / 16; ++pass) cur[pass] = nxt[pass];
     }
   }
-  if (amax_out != nullptr) block_max_to(key, amax_out);
+  if (kAmax) block_max_to(key, amax_out);
 }
 
 // --------------------------------------------------- token group (1x128) --
@@ -558,27 +558,32 @@ cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t 
     if (e != cudaSuccess) return e;
   }
   uint32_t *ao = reinterpret_cast<uint32_t *>(amax_out);
+  const bool fused = amax_out != nullptr;
   if (qt == nullptr) {
     const int64_t n = rows * cols;
     const int threads = 512, blocks = grid_for(n / 8, threads, 4, sms);
-    if (in_dt == 0)
-      quant_tensor_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
-          static_cast<const __nv_bfloat16 *>(x), n, fmt, amax_in, scale, scale_out, q, ao);
-    else
-      quant_tensor_kernel<float><<<blocks, threads, 0, st>>>(
-          static_cast<const float *>(x), n, fmt, amax_in, scale, scale_out, q, ao);
+#define FP8K_QT(T, A)                                                                          \
+  quant_tensor_kernel<T, A><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), n, fmt, amax_in, \
+                                                        scale, scale_out, q, ao)
+    if (in_dt == 0) {
+      if (fused) FP8K_QT(__nv_bfloat16, true); else FP8K_QT(__nv_bfloat16, false);
+    } else {
+      if (fused) FP8K_QT(float, true); else FP8K_QT(float, false);
+    }
+#undef FP8K_QT
   } else {
     const int64_t ntiles = ((cols + kTT - 1) / kTT) * ((rows + kTT - 1) / kTT);
     const int64_t cap = (int64_t)sms * 2;
     const unsigned grid = (unsigned)(ntiles < cap ? ntiles : cap);
-    if (in_dt == 0)
-      quant_tensor_t_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-          static_cast<const __nv_bfloat16 *>(x), rows, cols, fmt, amax_in, scale, scale_out,
-          q, qt, ao);
-    else
-      quant_tensor_t_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(x), rows,
-                                                          cols, fmt, amax_in, scale, scale_out,
-                                                          q, qt, ao);
+#define FP8K_QTT(T, A)                                                                           \
+  quant_tensor_t_kernel<T, A><<<grid, 256, 0, st>>>(static_cast<const T *>(x), rows, cols, fmt,     \
+                                                    amax_in, scale, scale_out, q, qt, ao)
+    if (in_dt == 0) {
+      if (fused) FP8K_QTT(__nv_bfloat16, true); else FP8K_QTT(__nv_bfloat16, false);
+    } else {
+      if (fused) FP8K_QTT(float, true); else FP8K_QTT(float, false);
+    }
+#undef FP8K_QTT
   }
   return cudaGetLastError();
 }

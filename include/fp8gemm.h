@@ -171,6 +171,35 @@ FP8_API int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, 
                     const float *sb, int64_t M, int64_t N, int64_t K, int out_dt, void *c,
                     int64_t ldc, int accumulate, fp8_stream_t stream);
 
+/* ------------------------------------------- GEMM, per tensor, grouped --
+ * fp8_gemm_tensor_grouped: `count` independent per-tensor GEMMs in one call,
+ * each exactly as fp8_gemm_tensor would compute it (same arguments, same
+ * bound).  Up to 4 problems whose shapes suit the CTA-pair path run as ONE
+ * persistent launch over all their tiles (longest K first), which pays the
+ * kernel prologue, pipeline fill and tail once instead of per GEMM -- e.g.
+ * the forward and both backward GEMMs of a linear layer once their operands
+ * are quantized ([Nano] "实现": three GEMMs).  Otherwise the problems run one
+ * after another on `stream`.
+ *   problems  HOST array of `count` descriptors (read during the call only);
+ *             the pointers inside are device pointers as for fp8_gemm_tensor.
+ *   No output may overlap another problem's output or inputs.
+ */
+typedef struct {
+  const uint8_t *a; /* [M, K] codes, format fa */
+  const uint8_t *b; /* [N, K] codes, format fb */
+  const float *sa;  /* device fp32 dequant scale of a */
+  const float *sb;  /* device fp32 dequant scale of b */
+  int64_t M, N, K;
+  int fa, fb;
+  int out_dt;     /* FP8_OUT_F32 or FP8_OUT_BF16 */
+  int accumulate; /* 1: C += result (FP8_OUT_F32 only) */
+  void *c;        /* [M, ldc] row-major */
+  int64_t ldc;
+} fp8_gemm_problem_t;
+
+FP8_API int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count,
+                                    fp8_stream_t stream);
+
 /* ---------------------------------------------------- GEMM, per K group --
  * fp8_gemm_group: C[m,n] = sum_g sa[g,m] * sb[n/128, g] * sum_{k in g} a.b
  * ([HF] 一: 1x128 activation groups times 128x128 weight blocks), output

@@ -279,3 +279,67 @@ def test_gemm_tensor_cta_pairs(mnk, fmts):
         F.fp8_set_option(F.OPT_GEMM_CTA_PAIRS, 1)
     rc, where = F.fp8_get_last_device_error()
     assert rc == 0, (rc, where)
+
+
+# ------------------------------------------------------ grouped per tensor --
+
+def _linear_problems(t, d_in, d_out, seed):
+    """y = x W^T, dx = g W, dW = g^T x as three per-tensor problems."""
+    x = workloads.normal((t, d_in), 1.0, seed).to(torch.bfloat16).float().numpy()
+    w = workloads.normal((d_out, d_in), 0.02, seed + 1).to(torch.bfloat16).float().numpy()
+    g = workloads.normal((t, d_out), 1e-3, seed + 2).to(torch.bfloat16).float().numpy()
+    qx, sx = OQ.quantize_tensor(x, "e4m3")
+    qw, sw = OQ.quantize_tensor(w, "e4m3")
+    qg, sg = OQ.quantize_tensor(g, "e5m2")
+    return [  # (A codes, fa, sa, B codes, fb, sb)
+        (qx, "e4m3", sx, qw, "e4m3", sw),
+        (qg, "e5m2", sg, np.ascontiguousarray(qw.T), "e4m3", sw),
+        (np.ascontiguousarray(qg.T), "e5m2", sg, np.ascontiguousarray(qx.T), "e4m3", sx),
+    ]
+
+
+@pytest.mark.parametrize("shape", [(2048, 1024, 1024), (1999, 768, 1280), (256, 128, 256)])
+def test_gemm_tensor_grouped_linear(shape):
+    """The forward and both backward GEMMs of a linear layer in one call; the
+    (256, 128, 256) case is too small for the grouped CTA-pair launch and
+    exercises the one-after-another fallback."""
+    F = lib()
+    probs = _linear_problems(*shape, seed=shape[0])
+    outs, descs, keep = [], [], []
+    for i, (qa, fa, sa, qb, fb, sb) in enumerate(probs):
+        m, n = qa.shape[0], qb.shape[0]
+        dt = torch.float32 if i == 2 else torch.bfloat16
+        out = torch.empty((m, n), dtype=dt, device="cuda")
+        t = (dev_u8(qa), dev_u8(qb), dev_f32(sa), dev_f32(sb))
+        keep.append(t)
+        descs.append(F.gemm_problem(t[0], FMT[fa], t[1], FMT[fb], t[2], t[3], out))
+        outs.append(out)
+    F.fp8_gemm_tensor_grouped(descs)
+    torch.cuda.synchronize()
+    for i, (qa, fa, sa, qb, fb, sb) in enumerate(probs):
+        c, e = OG.gemm(OG.dequant_operand(qa, fa, sa), OG.dequant_operand(qb, fb, sb))
+        ok, worst = OG.check(outs[i].float().cpu().numpy(), c, e, "f32" if i == 2 else "bf16")
+        assert ok, (i, worst)
+    assert F.fp8_get_last_device_error()[0] == 0
+
+
+def test_gemm_tensor_grouped_accumulate_and_ragged():
+    F = lib()
+    shapes = [(1024, 520, 4096), (777, 1000, 512), (2048, 512, 128)]
+    probs, descs, outs, keep, prev = [], [], [], [], []
+    for i, (m, n, k) in enumerate(shapes):
+        qa, sa, qb, sb = per_tensor_operands(m, n, k, "e4m3", "e4m3", seed=40 + i)
+        probs.append((qa, sa, qb, sb))
+        init = workloads.normal((m, n), 1.0, 90 + i)
+        out = init.clone().cuda()
+        prev.append(init.numpy().astype(np.float64))
+        t = (dev_u8(qa), dev_u8(qb), dev_f32(sa), dev_f32(sb))
+        keep.append(t)
+        descs.append(F.gemm_problem(t[0], F.E4M3, t[1], F.E4M3, t[2], t[3], out, accumulate=True))
+        outs.append(out)
+    F.fp8_gemm_tensor_grouped(descs)
+    torch.cuda.synchronize()
+    for i, (qa, sa, qb, sb) in enumerate(probs):
+        c, e = OG.gemm(OG.dequant_operand(qa, "e4m3", sa), OG.dequant_operand(qb, "e4m3", sb))
+        ok, worst = OG.check(outs[i].cpu().numpy(), c + prev[i], e + np.abs(prev[i]) * 1e-3, "f32")
+        assert ok, (i, worst)
