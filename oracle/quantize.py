@@ -178,6 +178,41 @@ def quantize_two_level(x, fmt, block=32):
     return q, e8m0_encode(e), big_s
 
 
+def quantize_mxfp8(x, fmt, block=32):
+    """One-level microscaling (MOSS blog, section 1): every 32 consecutive
+    values along K share one power-of-two scale, the smallest power of two not
+    below amax_block / MAX, and the block is divided by it.
+
+    x: [R, K] fp32, K % block == 0.  Returns (codes [R,K], E8M0 bytes
+    [R, K/block]).  An all-zero block takes scale 1 (byte 127); exponents are
+    clamped to [-127, 127].
+    """
+    f = fmt_of(fmt)
+    x = np.asarray(x, dtype=F32)
+    r, k = x.shape
+    if k % block:
+        raise ValueError("mxfp8: K must be a multiple of the block")
+    xb = x.reshape(r, k // block, block)
+    am = np.max(np.abs(xb), axis=2).astype(F32) if x.size else np.zeros((r, 0), F32)
+    s_i = (am / F32(f.max)).astype(F32)
+    e = np.zeros(s_i.shape, dtype=np.int64)
+    pos = s_i > 0
+    if np.any(pos):
+        e[pos] = np.clip(ceil_log2_f32(s_i[pos]), -127, 127)
+    scale = np.ldexp(F32(1.0), e).astype(F32)
+    q = quantize_with_scale(x, np.repeat(scale, block, axis=1), f)
+    return q, e8m0_encode(e)
+
+
+def dequantize_block(q, fmt, scales, sfmt, block=128):
+    """Fold 128x128 block scales into the values (Transformers fine-grained
+    FP8, 五: dequantize=True turns the FP8 weights back into bf16): the
+    definition decode(q) * scale of the element's block, float64."""
+    q = np.asarray(q)
+    n, k = q.shape
+    return decode(q, fmt) * expand(group_scale_values(scales, sfmt), n, k, block, block)
+
+
 def two_level_scale_values(local_bytes, global_s) -> np.ndarray:
     """Effective per-block multipliers S * r_i (float64)."""
     b = np.asarray(local_bytes, dtype=np.int64)

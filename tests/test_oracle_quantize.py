@@ -174,3 +174,50 @@ def test_two_level_rescues_small_blocks():
     assert snr_db(x[small], d2[small]) > snr_db(x[small], dt[small]) + 20.0
     # on the large blocks both schemes agree exactly
     assert np.array_equal(d2[~small], dt[~small])
+
+
+def test_mxfp8_one_level_properties():
+    # MOSS blog, section 1: a power-of-two scale per 32 values from the block amax
+    x = workloads.normal((6, 256), 1.0, seed=51).numpy()
+    x[1, 32:64] = 0.0
+    x[2, :32] *= 1e4
+    q, b = Q.quantize_mxfp8(x, "e4m3")
+    assert b.shape == (6, 8)
+    for i in range(6):
+        for j in range(8):
+            xb = x[i, 32 * j:32 * j + 32]
+            e = int(b[i, j]) - 127
+            am = float(np.max(np.abs(xb)))
+            if am == 0:
+                assert e == 0 and not q[i, 32 * j:32 * j + 32].any()
+                continue
+            s_i = float(np.float32(np.float32(am) / np.float32(448.0)))
+            assert 2.0 ** (e - 1) < s_i <= 2.0 ** e
+            mag = np.max(np.abs(F.decode(q[i, 32 * j:32 * j + 32], "e4m3")))
+            assert 224.0 <= mag <= 448.0
+            ref = torch_cast(np.clip(xb * np.float32(2.0 ** -e), -448, 448), "e4m3")
+            assert np.array_equal(q[i, 32 * j:32 * j + 32], ref)
+
+
+def test_mxfp8_equals_two_level_with_unit_global():
+    # with every block amax a power of two times 448 the two schemes coincide
+    x = workloads.normal((4, 128), 1.0, seed=52).numpy()
+    xb = x.reshape(4, 4, 32)
+    xb[:] = np.clip(xb, -1, 1)
+    xb[:, :, 0] = 448.0 * 2.0 ** -np.arange(4)[None, :]
+    q1, b1 = Q.quantize_mxfp8(x, "e4m3")
+    q2, b2, s2 = Q.quantize_two_level(x, "e4m3")
+    assert s2 == 1.0
+    assert np.array_equal(q1, q2) and np.array_equal(b1, b2)
+
+
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_dequantize_block_roundtrip(sfmt):
+    w = workloads.normal((200, 260), 0.02, seed=53).numpy()
+    q, sc = Q.quantize_block(w, "e4m3", sfmt)
+    d = Q.dequantize_block(q, "e4m3", sc, sfmt)
+    vals = Q.group_scale_values(sc, sfmt)
+    lib = torch.tensor(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(d, lib * Q.expand(vals, 200, 260, 128, 128))
+    # within half an E4M3 step (1/16 relative) of the original, blockwise
+    assert np.all(np.abs(d - w) <= np.abs(w) / 16 + Q.expand(vals, 200, 260, 128, 128) * 2.0 ** -10)
