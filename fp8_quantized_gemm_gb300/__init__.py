@@ -40,6 +40,8 @@ _SIGS = {
     "fp8_quantize_token_group": [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp],
     "fp8_quantize_block": [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp],
     "fp8_quantize_mx": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp],
+    "fp8_quantize_mx1": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp],
+    "fp8_dequantize_block": [_vp, _int, _vp, _int, _i64, _i64, _vp, _vp],
     "fp8_gemm_tensor": [_vp, _int, _vp, _int, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp],
     "fp8_gemm_group": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_gemm_tensor_grouped": [_vp, _int, _vp],
@@ -138,6 +140,17 @@ def fp8_quantize_mx(x, fmt, amax, global_out, q, local, stream=None):
     r, k = x.shape
     _call("fp8_quantize_mx", _p(x), _in_dt(x), r, k, fmt, _p(amax), _p(global_out), _p(q),
           _p(local), _stream(stream))
+
+
+def fp8_quantize_mx1(x, fmt, global_out, q, local, stream=None):
+    r, k = x.shape
+    _call("fp8_quantize_mx1", _p(x), _in_dt(x), r, k, fmt, _p(global_out), _p(q), _p(local),
+          _stream(stream))
+
+
+def fp8_dequantize_block(q, fmt, scales, sfmt, out, stream=None):
+    n, k = q.shape
+    _call("fp8_dequantize_block", _p(q), fmt, _p(scales), sfmt, n, k, _p(out), _stream(stream))
 
 
 def fp8_gemm_tensor(a, fa, b, fb, sa, sb, out, *, out_dt=None, accumulate=False, stream=None):

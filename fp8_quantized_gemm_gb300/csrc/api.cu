@@ -275,6 +275,36 @@ int fp8_quantize_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt, con
                                          (cudaStream_t)stream));
 }
 
+int fp8_quantize_mx1(const void *x, int in_dt, int64_t R, int64_t K, int fmt, float *global_out,
+                     uint8_t *q, uint32_t *local, fp8_stream_t stream) {
+  if (x == nullptr || q == nullptr || local == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (R < 1 || K < 1 || R >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (K % 128 != 0 || !aligned16(x) || !aligned16(q) || !aligned16(local))
+    return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  // a null tensor amax selects the one-level variant of the two-level kernel
+  return to_status(fp8k::launch_quant_mx(x, in_dt, R, K, fmt, nullptr, global_out, q, local,
+                                         d->sms, (cudaStream_t)stream));
+}
+
+int fp8_dequantize_block(const uint8_t *q, int fmt, const void *scales, int sfmt, int64_t N,
+                         int64_t K, void *out, fp8_stream_t stream) {
+  if (q == nullptr || scales == nullptr || out == nullptr || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || N >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || (reinterpret_cast<uintptr_t>(q) & 7u) != 0 || !aligned16(out))
+    return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(
+      fp8k::launch_dequant_block(q, N, K, fmt, sfmt, scales, out, d->sms, (cudaStream_t)stream));
+}
+
 int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, const float *sa,
                     const float *sb, int64_t M, int64_t N, int64_t K, int out_dt, void *c,
                     int64_t ldc, int accumulate, fp8_stream_t stream) {

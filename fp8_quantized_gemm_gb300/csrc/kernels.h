@@ -21,6 +21,8 @@ cudaError_t launch_quant_block(const void *w, int in_dt, int64_t N, int64_t K, i
 cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
                             const float *amax, float *global_out, uint8_t *q, uint32_t *local,
                             int sms, cudaStream_t st);
+cudaError_t launch_dequant_block(const uint8_t *q, int64_t N, int64_t K, int fmt, int sfmt,
+                                 const void *scales, void *out, int sms, cudaStream_t st);
 cudaError_t launch_delayed_update(float *hist, float *scale, const float *amax_cur, int64_t L,
                                   int fmt, cudaStream_t st);
 

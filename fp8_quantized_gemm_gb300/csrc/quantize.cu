@@ -5,6 +5,8 @@
 // independent), and casts on store with cvt.rn.satfinite after the
 // fl32(x / s) division and the +-MAX clip of the Flax guide's `quantize`
 // (section 2.2).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -430,13 +432,16 @@ __device__ __forceinline__ int64_t mx_word_index(int64_t r, int64_t g, int64_t r
   return g * rpad + (r & ~(int64_t)127) + 4 * (r & 31) + ((r & 127) >> 5);
 }
 
-template <typename T>
+// kOneLevel: plain MXFP8 (MOSS blog, section 1): the global factor is 1 and
+// each block's power of two is the smallest not below amax_i / MAX.
+template <typename T, bool kOneLevel>
 __global__ void __launch_bounds__(256)
     quant_mx_kernel(const T *__restrict__ x, int64_t R, int64_t K, int fmt,
                     const float *amax_in, float *global_out, uint8_t *__restrict__ q,
                     uint32_t *__restrict__ local) {
   const float mx = fmt_max(fmt);
-  const float S = scale_from_amax(*amax_in, mx);  // == max_i fl32(amax_i / MAX)
+  // two level: S == max_i fl32(amax_i / MAX)
+  const float S = kOneLevel ? 1.0f : scale_from_amax(*amax_in, mx);
   if (global_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *global_out = S;
   const int64_t G = K / 128, pairs = (G + 1) / 2;
   const int64_t rpad = (R + 127) / 128 * 128;
@@ -467,7 +472,9 @@ __global__ void __launch_bounds__(256)
     const float amax_i = __uint_as_float(key);
     const float s_i = __fdiv_rn(amax_i, mx);     // step 1
     int e = 0;
-    if (s_i > 0.0f) {
+    if (kOneLevel) {
+      if (s_i > 0.0f) e = min(max(ceil_log2_pos(s_i), -127), 127);
+    } else if (s_i > 0.0f) {
       const float ratio = __fdiv_rn(s_i, S);     // step 3
       e = ratio > 0.0f ? max(ceil_log2_pos(ratio), -127) : -127;
     }
@@ -618,12 +625,65 @@ cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
                             int sms, cudaStream_t st) {
   const int64_t G = K / 128, pairs = (G + 1) / 2, rpad = (R + 127) / 128 * 128;
   const int threads = 256, blocks = grid_for(rpad * pairs * 32, threads, 8, sms);
-  if (in_dt == 0)
-    quant_mx_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(x), R, K, fmt, amax, global_out, q, local);
-  else
-    quant_mx_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float *>(x), R, K, fmt,
-                                                       amax, global_out, q, local);
+  if (in_dt == 0) {
+    if (amax != nullptr)
+      quant_mx_kernel<__nv_bfloat16, false><<<blocks, threads, 0, st>>>(
+          static_cast<const __nv_bfloat16 *>(x), R, K, fmt, amax, global_out, q, local);
+    else
+      quant_mx_kernel<__nv_bfloat16, true><<<blocks, threads, 0, st>>>(
+          static_cast<const __nv_bfloat16 *>(x), R, K, fmt, amax, global_out, q, local);
+  } else {
+    if (amax != nullptr)
+      quant_mx_kernel<float, false><<<blocks, threads, 0, st>>>(
+          static_cast<const float *>(x), R, K, fmt, amax, global_out, q, local);
+    else
+      quant_mx_kernel<float, true><<<blocks, threads, 0, st>>>(
+          static_cast<const float *>(x), R, K, fmt, amax, global_out, q, local);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------- block dequantization --
+// out[n, k] = decode(q[n, k]) * scale of block (n/128, k/128), rounded to bf16
+// (Transformers fine-grained FP8, 五).  Eight codes per thread: the FP8 -> f16
+// conversion is exact for both formats, the product is formed in fp32.
+__global__ void __launch_bounds__(256)
+    dequant_block_kernel(const uint8_t *__restrict__ q, int64_t N, int64_t K, int fmt,
+                         int sfmt, const void *scales, __nv_bfloat16 *__restrict__ out) {
+  const int64_t KB = (K + 127) / 128;
+  const int64_t nvec = N * K / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    const int64_t e0 = i * 8, n = e0 / K, k = e0 % K;
+    const int64_t bi = (n >> 7) * KB + (k >> 7);
+    const float sc = sfmt == 0 ? static_cast<const float *>(scales)[bi]
+                               : exp2_int((int)static_cast<const uint8_t *>(scales)[bi] - 127);
+    const uint2 c = __ldcs(reinterpret_cast<const uint2 *>(q) + i);
+    const uint32_t w[2] = {c.x, c.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint16_t pair = (uint16_t)(w[h >> 1] >> (16 * (h & 1)));
+      uint32_t f16x2;
+      if (fmt == 0)
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+      else
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+      const __half2 hv = *reinterpret_cast<const __half2 *>(&f16x2);
+      const float lo = __low2float(hv) * sc, hi = __high2float(hv) * sc;
+      __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+      o[h] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    __stcs(reinterpret_cast<uint4 *>(out) + i, make_uint4(o[0], o[1], o[2], o[3]));
+  }
+}
+
+cudaError_t launch_dequant_block(const uint8_t *q, int64_t N, int64_t K, int fmt, int sfmt,
+                                 const void *scales, void *out, int sms, cudaStream_t st) {
+  const int64_t nvec = N * K / 8;
+  const int threads = 256, blocks = grid_for(nvec, threads, 8, sms);
+  dequant_block_kernel<<<blocks, threads, 0, st>>>(q, N, K, fmt, sfmt, scales,
+                                                   static_cast<__nv_bfloat16 *>(out));
   return cudaGetLastError();
 }
 

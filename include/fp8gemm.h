@@ -152,6 +152,27 @@ FP8_API int fp8_quantize_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
                     const float *amax, float *global_out, uint8_t *q, uint32_t *local,
                     fp8_stream_t stream);
 
+/* ------------------------------------------------- quantize mx, one level --
+ * fp8_quantize_mx1: plain MXFP8 ([MOSS] 1): every 32 consecutive values of a
+ * row share one power-of-two scale, the smallest not below amax_i / MAX
+ * (byte e + 127, e clamped to [-127, 127]; byte 127 for an all-zero block),
+ * and the block is quantized with it.  The output layout is fp8_quantize_mx's
+ * (codes + packed E8M0 words), so fp8_gemm_mx contracts it with global
+ * factors of 1.0; global_out (nullable, device fp32) receives 1.0 for that.
+ */
+FP8_API int fp8_quantize_mx1(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
+                     float *global_out, uint8_t *q, uint32_t *local, fp8_stream_t stream);
+
+/* --------------------------------------------------- dequantize block --
+ * fp8_dequantize_block: out[n,k] = decode(q[n,k]) * scale of block
+ * (n/128, k/128), rounded to bf16 ([HF] 五: dequantize=True folds the block
+ * scales back into bf16 weights).  q [N, K] codes (8-byte aligned), scales as
+ * written by fp8_quantize_block (fp32 or UE8M0 bytes), out [N, K] bf16
+ * (16-byte aligned).  K % 16 == 0.  The product is formed in fp32.
+ */
+FP8_API int fp8_dequantize_block(const uint8_t *q, int fmt, const void *scales, int sfmt,
+                                 int64_t N, int64_t K, void *out, fp8_stream_t stream);
+
 /* ------------------------------------------------------ GEMM, per tensor --
  * fp8_gemm_tensor: C = (sa * sb) * (A_q . B_q^T) with FP32 accumulation in
  * TMEM and the scales applied in the epilogue ([Flax] 2.2: dot with

@@ -298,11 +298,12 @@ def _linear_problems(t, d_in, d_out, seed):
     ]
 
 
-@pytest.mark.parametrize("shape", [(2048, 1024, 1024), (1999, 768, 1280), (256, 128, 256)])
+@pytest.mark.parametrize("shape", [(2048, 1024, 1024), (2000, 784, 1296), (256, 128, 256)])
 def test_gemm_tensor_grouped_linear(shape):
-    """The forward and both backward GEMMs of a linear layer in one call; the
-    (256, 128, 256) case is too small for the grouped CTA-pair launch and
-    exercises the one-after-another fallback."""
+    """The forward and both backward GEMMs of a linear layer in one call.
+    Every size is some GEMM's K, so all are multiples of 16; (2000, 784, 1296)
+    is ragged against the 256-wide tiles; (256, 128, 256) is too small for the
+    grouped CTA-pair launch and exercises the one-after-another fallback."""
     F = lib()
     probs = _linear_problems(*shape, seed=shape[0])
     outs, descs, keep = [], [], []

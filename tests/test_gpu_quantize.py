@@ -206,3 +206,41 @@ def test_delayed_update_keeps_scale_on_nonfinite():
     assert scale.item() == 0.5
     F.fp8_delayed_state_update(hist, scale, torch.tensor([57344.0 * 4], device="cuda"), 1)
     assert scale.item() == 4.0
+
+
+@pytest.mark.parametrize("shape", [(1, 128), (130, 512), (333, 2048)])
+def test_mxfp8_one_level(shape):
+    F = lib()
+    r, k = shape
+    a, _ = workloads.two_level(m=r, n=8, k=k)
+    x = a.clone()
+    x[0, 32:64] = 0.0
+    xf = x.float().numpy()
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    words = F.mx_local_words(r, k)
+    glob = torch.zeros(1, device="cuda")
+    F.fp8_quantize_mx1(x.cuda(), 0, glob, q, words)
+    ref_q, ref_l = OQ.quantize_mxfp8(xf, "e4m3")
+    assert glob.item() == 1.0
+    assert np.array_equal(to_np_u8(q), ref_q)
+    assert np.array_equal(mx_unpack(words.cpu().numpy(), r, k), ref_l)
+
+
+@pytest.mark.parametrize("shape", [(200, 272), (2048, 7168)])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_dequantize_block(shape, sfmt, fmt):
+    """Bit-exact against the oracle's definition, rounded the way the kernel
+    forms it: the fp32 product of the code's value and the block scale, then
+    bf16 round-to-nearest-even."""
+    F = lib()
+    n, k = shape
+    _, w = workloads.fine_grained(1, k=k, n=n)
+    q, sc = OQ.quantize_block(w.float().numpy(), fmt, sfmt)
+    out = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    F.fp8_dequantize_block(torch.from_numpy(q).cuda(), FMT[fmt],
+                           torch.from_numpy(np.ascontiguousarray(sc)).cuda(),
+                           0 if sfmt == "f32" else 1, out)
+    ref = OQ.dequantize_block(q, fmt, sc, sfmt).astype(np.float32)  # fp32 product
+    ref_bf16 = torch.from_numpy(ref).to(torch.bfloat16)
+    assert torch.equal(out.cpu(), ref_bf16)
