@@ -17,10 +17,18 @@ blog (section 5) trains with Adam/AdamW.  Plain readings adopted:
   p <- p - lr*wd*p;  m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2;
   p <- p - lr * (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps).
 
-Float64 throughout.  Pins (``tests/test_oracle_training.py``): silu'(z)
+Automatic weight scaling (MOSS blog, section 5, eq. 10): within a re-scaling
+interval the weight scale is predicted, without reading the weights, as
+``(amax_0 + eta * t) / MAX``: amax_0 from the last max-reduction, t the steps
+since then, eta the learning rate (an Adam step moves a weight by about eta at
+most).  Evaluated in fp32 as fl32(fl32(amax_0 + fl32(eta * t)) / MAX).
+
+Float64 throughout (fp32 for the scale formula).  Pins
+(``tests/test_oracle_snr_training.py``): silu'(z)
 against a central finite difference, silu at 0 and large |z|, and AdamW's
 first step on a constant gradient (an update of lr * g / (|g| + eps') after
-the decay).
+the decay); the automatic scale bounds amax(W_t) on an AdamW trajectory
+with the Adam per-step bound (1 - beta1) / sqrt(1 - beta2) times eta.
 """
 from __future__ import annotations
 
@@ -70,3 +78,10 @@ def adamw_step(p, g, m, v, step: int, lr=ADAMW["lr"], beta1=ADAMW["beta1"],
     vhat = v / (1.0 - beta2 ** step)
     p = p - lr * mhat / (np.sqrt(vhat) + eps)
     return p, m, v
+
+
+def auto_weight_scale(amax0, lr, t, fmt_max) -> np.float32:
+    """MOSS eq. (10): predicted scale (amax_0 + eta * t) / MAX, in fp32."""
+    F32 = np.float32
+    grow = F32(np.float64(lr) * np.float64(t))
+    return F32(F32(F32(amax0) + grow) / F32(fmt_max))

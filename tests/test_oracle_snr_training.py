@@ -67,3 +67,27 @@ def test_adamw_update_is_bounded_by_lr():
         p_new, m, v = T.adamw_step(p, g, m, v, step=t, weight_decay=0.0)
         assert np.max(np.abs(p_new - p)) <= 1e-4 * 3.2
         p = p_new
+
+
+def test_auto_scale_bounds_adamw_trajectory():
+    """MOSS blog, section 5: Adam's step is bounded by eta times
+    (1 - beta1) / sqrt(1 - beta2) per coordinate, so amax(W_t) never exceeds
+    amax_0 + that bound times eta * t; the eq. (10) prediction with eta itself
+    is the blog's tighter (typical-case) version of it."""
+    rng = np.random.default_rng(3)
+    w = rng.standard_normal(4096) * 0.02
+    m = np.zeros_like(w)
+    v = np.zeros_like(w)
+    lr = 1e-4
+    c = (1 - 0.9) / math.sqrt(1 - 0.999)
+    amax0 = float(np.max(np.abs(w)))
+    for t in range(1, 40):
+        g = rng.standard_normal(4096) * 10.0 ** rng.integers(-5, 1)
+        w, m, v = T.adamw_step(w, g, m, v, step=t)
+        assert float(np.max(np.abs(w))) <= amax0 + c * lr * t + 1e-12
+        s_pred = float(T.auto_weight_scale(amax0, c * lr, t, 448.0))
+        assert np.max(np.abs(w)) / s_pred <= 448.0 * (1 + 1e-6)
+    # eq. (10) grows linearly: equal steps add equal increments (fp32)
+    s1 = T.auto_weight_scale(0.5, 1e-4, 100, 448.0)
+    s2 = T.auto_weight_scale(0.5, 1e-4, 200, 448.0)
+    assert abs((float(s2) - float(s1)) - 1e-4 * 100 / 448.0) < 1e-9
