@@ -711,12 +711,13 @@ def extra_workloads(dev):
     yield TwoLevel(dev)
 
 
-def run_swiglu_row(dev, stream, fp8_peak):
-    """FP8 SwiGLU MLP training with delayed scaling: d 4096, ffn 14336, 16384
-    tokens, 16 steps (inputs drawn on the device from seeded generators)."""
+def run_swiglu_row(dev, stream, fp8_peak, flush, weight_scaling="delayed"):
+    """FP8 SwiGLU MLP training, d 4096, ffn 14336, 16384 tokens, 16 steps
+    (inputs drawn on the device from seeded generators); activations and
+    gradients with delayed scaling, weights delayed or automatic (MOSS eq. 10)."""
     from fp8_quantized_gemm_gb300.mlp import SwiGLUTrainer
     x, w1, w3, w2 = workloads.swiglu(device=dev)
-    tr = SwiGLUTrainer(w1, w3, w2, tokens=x.shape[0])
+    tr = SwiGLUTrainer(w1, w3, w2, tokens=x.shape[0], weight_scaling=weight_scaling)
     del w1, w3, w2
     dys = [workloads.swiglu_grad(t, device=dev) for t in range(17)]
     tr.step(x, dys[0])  # warm-up step (kernel attributes, split-K scratch)
@@ -745,7 +746,24 @@ def run_swiglu_row(dev, stream, fp8_peak):
            "ms_per_step": round(total / steps16, 3),
            "ms_forward_backward": round(fb, 3), "ms_adamw_and_state": round(op, 3),
            "tflop_per_step": round(tr.flops_per_step / 1e12, 3),
-           "launch": "eager, one API call per kernel (39 per step)"}
+           "launch": "eager, one API call per kernel"}
+    if weight_scaling == "auto":
+        # per-tensor cost of the two ways of scaling a weight (MOSS Table 1:
+        # just-in-time 0.08-0.54 ms per tensor, automatic 0.02 ms)
+        import fp8_quantized_gemm_gb300 as F
+        jit, auto = [], []
+        for w in tr.w_bf:
+            per, _ = time_launches([("jit", lambda w=w: F.fp8_amax(w, tr.w_amax0[0:1]))], 10,
+                                   flush, stream)
+            jit.append(per["jit"])
+            per, _ = time_launches([("auto", lambda: F.fp8_auto_weight_scale(
+                tr.w_amax0[0:1], 7, 1e-4, F.E4M3, tr.scale[1:2]))], 10, flush, stream)
+            auto.append(per["auto"])
+        row["weight_scale_us_per_tensor"] = {
+            "jit_amax": round(1e3 * sum(jit) / 3, 2), "automatic": round(1e3 * sum(auto) / 3, 2),
+            "weight_bytes": int(tr.w_bf[0].numel() * 2),
+            "note": "jit = fp8_amax max-reduction of the bf16 weight after an L2 flush; "
+                    "automatic = fp8_auto_weight_scale"}
     del tr, x, dys
     torch.cuda.empty_cache()
     return row
@@ -759,7 +777,9 @@ def run_extras(dev, flush, stream, peaks, iters=10):
         per, step = time_launches(wl.launches(), iters, flush, stream)
         out[wl.name] = wl.report(per, step, fp8_peak, hbm)
         del wl
-    out["swiglu_training_delayed_16steps"] = run_swiglu_row(dev, stream, fp8_peak)
+    out["swiglu_training_delayed_16steps"] = run_swiglu_row(dev, stream, fp8_peak, flush)
+    out["swiglu_training_auto_weight_scaling_16steps"] = run_swiglu_row(dev, stream, fp8_peak,
+                                                                        flush, "auto")
     hist = torch.zeros(1024, device=dev)
     sc = torch.ones(1, device=dev)
     cur = torch.full((1,), 3.0, device=dev)

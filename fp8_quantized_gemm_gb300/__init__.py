@@ -48,6 +48,7 @@ _SIGS = {
     "fp8_gemm_mx": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp],
     "fp8_gemm_group_noalloc": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_delayed_state_update": [_vp, _vp, _vp, _i64, _int, _vp],
+    "fp8_auto_weight_scale": [_vp, _i64, _d, _int, _vp, _vp],
     "fp8_swiglu_forward": [_vp, _vp, _vp, _i64, _vp],
     "fp8_swiglu_backward": [_vp, _vp, _vp, _vp, _vp, _i64, _vp],
     "fp8_adamw_step": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _d, _d, _d, _d, _d, _vp],
@@ -209,6 +210,11 @@ def fp8_gemm_mx(a, la, ga, b, lb, gb, out, *, out_dt=None, stream=None):
 
 def fp8_delayed_state_update(hist, scale, amax_cur, fmt, stream=None):
     _call("fp8_delayed_state_update", _p(hist), _p(scale), _p(amax_cur), hist.numel(), fmt,
+          _stream(stream))
+
+
+def fp8_auto_weight_scale(amax0, t, lr, fmt, scale_out, stream=None):
+    _call("fp8_auto_weight_scale", _p(amax0), int(t), float(lr), fmt, _p(scale_out),
           _stream(stream))
 
 

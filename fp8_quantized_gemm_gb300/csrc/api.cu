@@ -421,6 +421,17 @@ int fp8_delayed_state_update(float *hist, float *scale, const float *amax_cur, i
   return to_status(fp8k::launch_delayed_update(hist, scale, amax_cur, L, fmt, (cudaStream_t)stream));
 }
 
+int fp8_auto_weight_scale(const float *amax0, int64_t t, double lr, int fmt, float *scale_out,
+                          fp8_stream_t stream) {
+  if (amax0 == nullptr || scale_out == nullptr || t < 0 || !valid_fmt(fmt) || !(lr >= 0.0))
+    return FP8_ERR_INVALID_ARG;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_auto_scale(amax0, lr * (double)t, fmt, scale_out,
+                                           (cudaStream_t)stream));
+}
+
 int fp8_swiglu_forward(const void *h, const void *u, void *a, int64_t n, fp8_stream_t stream) {
   if (h == nullptr || u == nullptr || a == nullptr || n < 0) return FP8_ERR_INVALID_ARG;
   if (n % 8 != 0 || !aligned16(h) || !aligned16(u) || !aligned16(a)) return FP8_ERR_MISALIGNED;

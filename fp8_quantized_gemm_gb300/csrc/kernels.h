@@ -23,6 +23,8 @@ cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
                             int sms, cudaStream_t st);
 cudaError_t launch_dequant_block(const uint8_t *q, int64_t N, int64_t K, int fmt, int sfmt,
                                  const void *scales, void *out, int sms, cudaStream_t st);
+cudaError_t launch_auto_scale(const float *amax0, double grow, int fmt, float *scale,
+                              cudaStream_t st);
 cudaError_t launch_delayed_update(float *hist, float *scale, const float *amax_cur, int64_t L,
                                   int fmt, cudaStream_t st);
 

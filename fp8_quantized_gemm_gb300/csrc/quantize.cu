@@ -687,6 +687,18 @@ cudaError_t launch_dequant_block(const uint8_t *q, int64_t N, int64_t K, int fmt
   return cudaGetLastError();
 }
 
+// MOSS automatic weight scaling (eq. 10): scale = (amax_0 + eta * t) / MAX,
+// with eta * t rounded to fp32 on the host; one thread, no reads of the weight.
+__global__ void auto_scale_kernel(const float *amax0, float grow, int fmt, float *scale) {
+  if (threadIdx.x == 0) *scale = __fdiv_rn(__fadd_rn(*amax0, grow), fmt_max(fmt));
+}
+
+cudaError_t launch_auto_scale(const float *amax0, double grow, int fmt, float *scale,
+                              cudaStream_t st) {
+  auto_scale_kernel<<<1, 32, 0, st>>>(amax0, (float)grow, fmt, scale);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_delayed_update(float *hist, float *scale, const float *amax_cur, int64_t L,
                                   int fmt, cudaStream_t st) {
   const size_t smem = (size_t)L * sizeof(float);

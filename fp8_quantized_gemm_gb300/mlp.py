@@ -14,9 +14,14 @@ pushed afterwards (section 2.3).  Both W1 and W3 take x as input: their two
 input states receive the same amax every step and so always hold the same
 scale; x is quantized once, with the first.
 
+Weight scaling: "delayed" (above) or "auto", the MOSS blog's automatic
+scaling (section 5, eq. 10): each weight's scale is predicted as
+(amax_0 + lr * t) / MAX from the amax_0 of its last max-reduction, t steps
+ago, without reading the weight; the max-reduction (fp8_amax) is redone every
+`rescale_interval` steps (500 in the blog).
+
 Buffers are allocated once (device memory through torch); `step` issues the
-calls on the current stream and can be captured in a CUDA graph after one
-warm-up step.
+calls on the current stream.
 """
 from __future__ import annotations
 
@@ -33,7 +38,12 @@ HISTORY = 1024
 class SwiGLUTrainer:
     def __init__(self, w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, tokens: int,
                  lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
-                 history: int = HISTORY):
+                 history: int = HISTORY, weight_scaling: str = "delayed",
+                 rescale_interval: int = 500):
+        if weight_scaling not in ("delayed", "auto"):
+            raise ValueError(weight_scaling)
+        self.weight_scaling = weight_scaling
+        self.rescale_interval = rescale_interval
         dev = w1.device
         ffn, d = w1.shape
         assert w3.shape == (ffn, d) and w2.shape == (d, ffn)
@@ -69,6 +79,17 @@ class SwiGLUTrainer:
         self.dw = [torch.empty((ffn, d), **f32), torch.empty((ffn, d), **f32),
                    torch.empty((d, ffn), **f32)]
         self.flops_per_step = 9 * 2.0 * T * d * ffn
+        # automatic weight scaling: amax at the last max-reduction, steps since
+        self.w_amax0 = torch.zeros(3, **f32)
+        self.t_since = 0
+        if weight_scaling == "auto":
+            self.refresh_weight_amax()
+
+    def refresh_weight_amax(self):
+        """The max-reduction of automatic scaling (fp8_amax of each weight)."""
+        for i in range(3):
+            F.fp8_amax(self.w_bf[i], self.w_amax0[i:i + 1])
+        self.t_since = 0
 
     def _sc(self, i):
         return self.scale[i:i + 1]
@@ -83,9 +104,16 @@ class SwiGLUTrainer:
         w1, w3, w2 = self.w_bf
         # forward
         q(x, E4, self.xq, scale=self._sc(X1), q_t=self.xqt, amax_out=self._am(X1))
-        q(w1, E4, self.w1q, scale=self._sc(K1), q_t=self.w1qt, amax_out=self._am(K1))
-        q(w3, E4, self.w3q, scale=self._sc(K3), q_t=self.w3qt, amax_out=self._am(K3))
-        q(w2, E4, self.w2q, scale=self._sc(K2), q_t=self.w2qt, amax_out=self._am(K2))
+        if self.weight_scaling == "auto":
+            for i, slot in ((0, K1), (1, K3), (2, K2)):
+                F.fp8_auto_weight_scale(self.w_amax0[i:i + 1], self.t_since, self.hp["lr"], E4,
+                                        self._sc(slot))
+            wam = (None, None, None)
+        else:
+            wam = (self._am(K1), self._am(K3), self._am(K2))
+        q(w1, E4, self.w1q, scale=self._sc(K1), q_t=self.w1qt, amax_out=wam[0])
+        q(w3, E4, self.w3q, scale=self._sc(K3), q_t=self.w3qt, amax_out=wam[1])
+        q(w2, E4, self.w2q, scale=self._sc(K2), q_t=self.w2qt, amax_out=wam[2])
         g(self.xq, E4, self.w1q, E4, self._sc(X1), self._sc(K1), self.h)
         g(self.xq, E4, self.w3q, E4, self._sc(X1), self._sc(K3), self.u)
         F.fp8_swiglu_forward(self.h, self.u, self.a)
@@ -109,7 +137,14 @@ class SwiGLUTrainer:
         for i in range(3):
             F.fp8_adamw_step(self.w_master[i], self.dw[i], self.m[i], self.v[i], self.w_bf[i],
                              self.t, **self.hp)
+        auto = self.weight_scaling == "auto"
+        if auto:
+            self.t_since += 1
+            if self.t_since >= self.rescale_interval:
+                self.refresh_weight_amax()
         for i in range(9):
+            if auto and i in (K1, K3, K2):
+                continue  # weights follow eq. (10), not a history
             cur = X1 if i == X3 else i  # the x@W3 input state takes x's amax
             fmt = F.E5M2 if i in (G1, G3, G2) else F.E4M3
             F.fp8_delayed_state_update(self.hist[i], self.scale[i:i + 1], self._am(cur), fmt)

@@ -297,6 +297,18 @@ FP8_API int fp8_gemm_mx(const uint8_t *a, const uint32_t *la, const float *ga, c
 FP8_API int fp8_delayed_state_update(float *hist, float *scale, const float *amax_cur, int64_t L,
                              int fmt, fp8_stream_t stream);
 
+/* ------------------------------------------- automatic weight scaling --
+ * fp8_auto_weight_scale: MOSS automatic scaling ([MOSS] 5, eq. 10): the scale
+ * of a weight t optimizer steps after its last max-reduction is predicted,
+ * without reading the weight, as
+ *     scale_out[0] = fl32(fl32(amax0[0] + fl32(lr * t)) / MAX)
+ * (an Adam step moves each weight by about lr at most).  amax0: device fp32,
+ * the weight's amax at the last max-reduction (fp8_amax, every ~500 steps);
+ * lr * t is formed in double on the host.  t >= 0.
+ */
+FP8_API int fp8_auto_weight_scale(const float *amax0, int64_t t, double lr, int fmt,
+                                  float *scale_out, fp8_stream_t stream);
+
 /* -------------------------------------------- SwiGLU / AdamW (support) --
  * Support kernels of the FP8 SwiGLU training step.  Not described on the
  * pages; plain definitions: silu(z) = z / (1 + exp(-z)) in fp32.

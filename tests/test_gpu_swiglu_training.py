@@ -116,3 +116,35 @@ def test_swiglu_training_teacher_forced():
         hist = tr.hist.cpu().numpy()
         for i in range(9):
             assert np.array_equal(hist[i].view(np.uint32), st[i].history.view(np.uint32)), (t, i)
+
+
+def test_swiglu_training_automatic_weight_scaling():
+    """MOSS automatic scaling (section 5, eq. 10) in the training step: each
+    weight's scale is (amax_0 + lr * t) / MAX from the amax at the last
+    max-reduction, t steps ago; the reduction is redone every 3 steps here."""
+    lib()
+    from fp8_quantized_gemm_gb300.mlp import K1, K2, K3, SwiGLUTrainer
+    x, w1, w3, w2 = workloads.swiglu(d=D, ffn=FFN, tokens=T)
+    tr = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T, weight_scaling="auto",
+                       rescale_interval=3)
+    xd = x.cuda()
+    slots = (K1, K3, K2)
+    qs = ((lambda: tr.w1q), (lambda: tr.w3q), (lambda: tr.w2q))
+    amax0 = [float(np.max(np.abs(f32(w)))) for w in tr.w_bf]
+    t_since = 0
+    for step in range(7):
+        wb = [f32(w) for w in tr.w_bf]
+        tr.forward_backward(xd, workloads.swiglu_grad(step, tokens=T, d=D).cuda())
+        torch.cuda.synchronize()
+        sc = tr.scale.cpu().numpy()
+        for i in range(3):
+            want = OT.auto_weight_scale(amax0[i], 1e-4, t_since, 448.0)
+            assert np.float32(sc[slots[i]]) == want, (step, i)
+            assert np.array_equal(to_np_u8(qs[i]()), OQ.quantize_with_scale(wb[i], want, "e4m3"))
+        tr.optimizer_and_state()
+        torch.cuda.synchronize()
+        t_since += 1
+        if t_since == 3:  # max-reduction on the updated bf16 weights
+            t_since = 0
+            amax0 = [float(np.max(np.abs(f32(w)))) for w in tr.w_bf]
+        assert np.allclose(tr.w_amax0.cpu().numpy(), amax0, rtol=0, atol=0)
