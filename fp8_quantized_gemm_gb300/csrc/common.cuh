@@ -174,6 +174,31 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
          ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile written by
+// TMA with 128-byte swizzling (box {128 rows of the operand, 128 K}): each
+// 128-byte line holds 128 consecutive M (or N) elements of one K index, 8
+// lines form a 1024-byte atom, atoms follow each other along K (stride byte
+// offset 1024), and further 128-element blocks of M or N sit `lbo` bytes
+// apart (leading byte offset).  One K = 32 step of the MMA covers four atoms,
+// so the start address advances by 4096 bytes per step.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t smem_addr, uint32_t lbo) {
+  return (uint64_t)((smem_addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Operand descriptor and its per-K=32-step increment (in 16-byte units) for
+// either layout: K-major steps 32 bytes along the swizzled line, MN-major
+// steps four 1024-byte atoms.
+struct OperandDesc {
+  uint64_t base;
+  uint32_t step;
+};
+__device__ __forceinline__ OperandDesc operand_desc(uint32_t smem_addr, int mn_major,
+                                                    uint32_t mn_lbo) {
+  if (mn_major) return {sdesc_sw128_mn(smem_addr, mn_lbo), 4096u >> 4};
+  return {sdesc_sw128(smem_addr), 32u >> 4};
+}
+
 // Descriptor of an unswizzled K-major source for tcgen05.cp: 8-row x 16-byte
 // core matrices stored contiguously (row stride 16 bytes, 128 bytes apart).
 __device__ __forceinline__ uint64_t sdesc_plain(uint32_t smem_addr) {
@@ -182,11 +207,14 @@ __device__ __forceinline__ uint64_t sdesc_plain(uint32_t smem_addr) {
 }
 
 // Instruction descriptor, kind::f8f6f4 (dense): D = f32 (bits 4-5 = 1),
-// A/B formats at bits 7-9 / 10-12 (E4M3 = 0, E5M2 = 1), both K-major,
-// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+// A/B formats at bits 7-9 / 10-12 (E4M3 = 0, E5M2 = 1), A / B major-ness at
+// bits 15 / 16 (0 = K-major, 1 = MN-major), N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t m, uint32_t n, uint32_t fa,
-                                                    uint32_t fb) {
-  return (1u << 4) | (fa << 7) | (fb << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+                                                    uint32_t fb, uint32_t a_mn = 0,
+                                                    uint32_t b_mn = 0) {
+  return (1u << 4) | (fa << 7) | (fb << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) |
+         ((m >> 4) << 24);
 }
 
 // Instruction descriptor, kind::mxf8f6f4 with block scaling: B scale-factor
@@ -344,10 +372,53 @@ __device__ __forceinline__ uint16_t cvt_fp8x2(int fmt, float lo, float hi) {
 // saturating conversion (cvt.rn.satfinite rounds to nearest even and clamps
 // finite values beyond the largest finite code to it, which for every finite
 // y equals rounding clip(y, -MAX, MAX)).
-__device__ __forceinline__ float q_prep(float x, float s, float mx) {
-  (void)mx;
-  return __fdiv_rn(x, s);
+//
+// Many values are divided by one scale, so the quotient is formed from the
+// correctly rounded reciprocal y = RN(1/s) by Markstein's FMA correction
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990; J.-M. Muller et al.,
+// Handbook of Floating-Point Arithmetic, division with an FMA):
+//   q0 = RN(x y)             within 2 ulp of z = x / s (|y s - 1| < 2^-24);
+//   q1 = RN(q0 + RN(x - s q0) y)   within 2^-22 ulp of z before rounding,
+//                                  hence a faithful rounding of z;
+//   q2 = RN(q1 + (x - s q1) y)     the remainder x - s q1 is exact because q1
+//                                  is faithful, and a quotient of two binary32
+//                                  numbers lies more than 2^-25 ulp from any
+//                                  midpoint, farther than the correction errs,
+//                                  so q2 = RN(z).
+// Preconditions, checked once per scale (ScaleDiv::fast): s in [2^-80, 2^80],
+// which keeps y normal and every remainder that matters (|z| >= 2^-23) free
+// of underflow.  Quotients below 2^-23 may differ from RN(z) in their last
+// bits but round to a signed zero in both FP8 formats either way, and the
+// sign is copied from x, as IEEE division gives it.  For |q0| >= 2^100 (x
+// infinite, or a quotient far beyond either format's MAX) and NaN x, q0 is
+// kept: the conversion saturates it, or keeps the NaN, as it would RN(z).
+__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r0 = __fmaf_rn(-s, q0, x);
+  const float q1 = __fmaf_rn(r0, y, q0);
+  const float r1 = __fmaf_rn(-s, q1, x);
+  const float q2 = copysignf(__fmaf_rn(r1, y, q1), x);
+  return fabsf(q0) < 0x1p100f ? q2 : q0;
 }
+
+struct ScaleDiv {
+  float s, y;
+  bool fast;
+  __device__ __forceinline__ explicit ScaleDiv(float s_) {
+    s = s_;
+    y = __frcp_rn(s_);
+    fast = s_ >= 0x1p-80f && s_ <= 0x1p80f;
+  }
+  // kFast: the caller has checked `fast` (uniformly, outside its loop)
+  template <bool kFast>
+  __device__ __forceinline__ float div(float x) const {
+    if constexpr (kFast)
+      return div_by_scale(x, s, y);
+    else
+      return __fdiv_rn(x, s);
+  }
+};
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
 

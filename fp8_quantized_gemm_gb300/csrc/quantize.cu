@@ -4,7 +4,8 @@
 // warp shuffles on order-preserving uint32 keys (exact: max is order
 // independent), and casts on store with cvt.rn.satfinite after the
 // fl32(x / s) division and the +-MAX clip of the Flax guide's `quantize`
-// (section 2.2).
+// (section 2.2).  The division is the correctly rounded quotient formed from
+// one reciprocal per scale (div_by_scale in common.cuh).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -105,6 +106,18 @@ __device__ __forceinline__ uint2 pack8(int fmt, const float (&y)[8]) {
   return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
 }
 
+// Eight quotients v[j] / s by one scale (ScaleDiv; the fast/slow choice is
+// per scale, so it diverges only between groups with extreme scales).
+__device__ __forceinline__ void div8(const ScaleDiv &d, const float *v, float (&y)[8]) {
+  if (d.fast) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] = d.div<true>(v[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] = d.div<false>(v[j]);
+  }
+}
+
 // Block-wide max of a uint32 key, then one atomicMax per block.
 __device__ __forceinline__ void block_max_to(uint32_t key, uint32_t *dst) {
   __shared__ uint32_t red[32];
@@ -157,16 +170,12 @@ __device__ __forceinline__ float resolve_scale(const float *amax_in, const float
   return amax_in != nullptr ? scale_from_amax(*amax_in, mx) : *scale_in;
 }
 
-// Row-major output only: grid-stride over 8-element vectors.
-template <typename T, bool kAmax>
-__global__ void __launch_bounds__(512)
-    quant_tensor_kernel(const T *__restrict__ x, int64_t n, int fmt, const float *amax_in,
-                        const float *scale_in, float *scale_out, uint8_t *__restrict__ q,
-                        uint32_t *amax_out) {
-  const float mx = fmt_max(fmt);
-  const float s = resolve_scale(amax_in, scale_in, mx);
-  if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
-  uint32_t key = 0;
+// Row-major output only: grid-stride over 8-element vectors.  kFast selects
+// the reciprocal-based quotient (ScaleDiv), checked once per launch.
+template <typename T, bool kAmax, bool kFast>
+__device__ __forceinline__ void quant_tensor_body(const T *__restrict__ x, int64_t n, int fmt,
+                                                  const ScaleDiv &d, uint8_t *__restrict__ q,
+                                                  uint32_t &key) {
   const int64_t nvec = n / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -180,7 +189,7 @@ __global__ void __launch_bounds__(512)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (kAmax) key = max(key, abs_key(v[u][j]));
-        y[j] = q_prep(v[u][j], s, mx);
+        y[j] = d.div<kFast>(v[u][j]);
       }
       reinterpret_cast<uint2 *>(q)[i + u * stride] = pack8(fmt, y);
     }
@@ -191,10 +200,26 @@ __global__ void __launch_bounds__(512)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (kAmax) key = max(key, abs_key(v[j]));
-      y[j] = q_prep(v[j], s, mx);
+      y[j] = d.div<kFast>(v[j]);
     }
     reinterpret_cast<uint2 *>(q)[i] = pack8(fmt, y);
   }
+}
+
+template <typename T, bool kAmax>
+__global__ void __launch_bounds__(512)
+    quant_tensor_kernel(const T *__restrict__ x, int64_t n, int fmt, const float *amax_in,
+                        const float *scale_in, float *scale_out, uint8_t *__restrict__ q,
+                        uint32_t *amax_out) {
+  const float mx = fmt_max(fmt);
+  const float s = resolve_scale(amax_in, scale_in, mx);
+  if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+  const ScaleDiv d(s);
+  uint32_t key = 0;
+  if (d.fast)
+    quant_tensor_body<T, kAmax, true>(x, n, fmt, d, q, key);
+  else
+    quant_tensor_body<T, kAmax, false>(x, n, fmt, d, q, key);
   if (kAmax) block_max_to(key, amax_out);
 }
 
@@ -206,29 +231,43 @@ constexpr int kTT = 128;
 constexpr int kTPitch = kTT;
 __device__ __forceinline__ int tchunk(int r, int c8) { return ((c8 ^ (r >> 3)) & 15) * 8; }
 
-__device__ __forceinline__ uint64_t transpose8x8(const uint64_t (&r)[8], int j) {
-  // byte j of every row r[i] -> byte i of the result
-  uint64_t out = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) out |= ((r[i] >> (8 * j)) & 0xFFull) << (8 * i);
-  return out;
+// 4x4 byte transpose: byte j of word i -> byte i of word j.
+__device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                             uint32_t (&o)[4]) {
+  const uint32_t ab01 = __byte_perm(a, b, 0x5140), cd01 = __byte_perm(c, d, 0x5140);
+  const uint32_t ab23 = __byte_perm(a, b, 0x7362), cd23 = __byte_perm(c, d, 0x7362);
+  o[0] = __byte_perm(ab01, cd01, 0x5410);
+  o[1] = __byte_perm(ab01, cd01, 0x7632);
+  o[2] = __byte_perm(ab23, cd23, 0x5410);
+  o[3] = __byte_perm(ab23, cd23, 0x7632);
 }
 
-template <typename T, bool kAmax>
-__global__ void __launch_bounds__(256, 2)
-    quant_tensor_t_kernel(const T *__restrict__ x, int64_t rows, int64_t cols, int fmt,
-                          const float *amax_in, const float *scale_in, float *scale_out,
-                          uint8_t *__restrict__ q, uint8_t *__restrict__ qt,
-                          uint32_t *amax_out) {
-  __shared__ __align__(16) uint8_t tile[kTT * kTPitch];
-  const float mx = fmt_max(fmt);
-  const float s = resolve_scale(amax_in, scale_in, mx);
-  if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+// 8x8 byte transpose from four 4x4 ones: byte j of r[i] -> byte i of c[j].
+__device__ __forceinline__ void transpose8x8(const uint64_t (&r)[8], uint64_t (&c)[8]) {
+  uint32_t lo_top[4], lo_bot[4], hi_top[4], hi_bot[4];
+  transpose4x4((uint32_t)r[0], (uint32_t)r[1], (uint32_t)r[2], (uint32_t)r[3], lo_top);
+  transpose4x4((uint32_t)r[4], (uint32_t)r[5], (uint32_t)r[6], (uint32_t)r[7], lo_bot);
+  transpose4x4((uint32_t)(r[0] >> 32), (uint32_t)(r[1] >> 32), (uint32_t)(r[2] >> 32),
+               (uint32_t)(r[3] >> 32), hi_top);
+  transpose4x4((uint32_t)(r[4] >> 32), (uint32_t)(r[5] >> 32), (uint32_t)(r[6] >> 32),
+               (uint32_t)(r[7] >> 32), hi_bot);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    c[j] = (uint64_t)lo_top[j] | ((uint64_t)lo_bot[j] << 32);
+    c[4 + j] = (uint64_t)hi_top[j] | ((uint64_t)hi_bot[j] << 32);
+  }
+}
+
+template <typename T, bool kAmax, bool kFast>
+__device__ __forceinline__ void quant_tensor_t_body(const T *__restrict__ x, int64_t rows,
+                                                    int64_t cols, int fmt, const ScaleDiv &d,
+                                                    uint8_t *__restrict__ q,
+                                                    uint8_t *__restrict__ qt, uint8_t *tile,
+                                                    uint32_t &key) {
   const int64_t tiles_c = (cols + kTT - 1) / kTT;
   const int64_t ntiles = ((rows + kTT - 1) / kTT) * tiles_c;
   const int t = threadIdx.x;
   const int lc = (t & 15) * 8;
-  uint32_t key = 0;
   // Persistent CTAs loop over 128 x 128 tiles; the eight 16-byte loads of the
   // NEXT tile are issued before the current tile is processed.
   auto load_tile = [&](int64_t tl, Raw8<T> (&raw)[kTT / 16]) {
@@ -263,7 +302,7 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (kAmax) key = max(key, abs_key(v[j]));
-        y[j] = q_prep(v[j], s, mx);
+        y[j] = d.div<kFast>(v[j]);
       }
       const uint2 packed = pack8(fmt, y);
       if (r < rows && c < cols) *reinterpret_cast<uint2 *>(q + r * cols + c) = packed;
@@ -272,22 +311,22 @@ __global__ void __launch_bounds__(256, 2)
     __syncthreads();
     // phase 2: thread -> one 8x8 byte block; 16 threads per q_t row segment
     const int rb = t & 15, cb = t >> 4;
-    uint64_t rr[8];
+    uint64_t rr[8], cc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       rr[i] = *reinterpret_cast<const uint64_t *>(&tile[(rb * 8 + i) * kTPitch + tchunk(rb * 8 + i, cb)]);
+    transpose8x8(rr, cc);
     const int64_t orow0 = c0 + cb * 8;  // q_t row = input column
     const int64_t ocol = r0 + rb * 8;   // q_t column = input row
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int64_t orow = orow0 + j;
       if (orow >= cols) break;
-      const uint64_t w = transpose8x8(rr, j);
       uint8_t *dst = qt + orow * rows + ocol;
       if (ocol + 8 <= rows && (rows & 7) == 0) {
-        *reinterpret_cast<uint64_t *>(dst) = w;
+        *reinterpret_cast<uint64_t *>(dst) = cc[j];
       } else {
-        for (int i = 0; i < 8 && ocol + i < rows; ++i) dst[i] = (uint8_t)(w >> (8 * i));
+        for (int i = 0; i < 8 && ocol + i < rows; ++i) dst[i] = (uint8_t)(cc[j] >> (8 * i));
       }
     }
     __syncthreads();  // the tile buffer is rewritten by the next iteration
@@ -296,6 +335,24 @@ __global__ void __launch_bounds__(256, 2)
       for (int pass = 0; pass < kTT / 16; ++pass) cur[pass] = nxt[pass];
     }
   }
+}
+
+template <typename T, bool kAmax>
+__global__ void __launch_bounds__(256, 2)
+    quant_tensor_t_kernel(const T *__restrict__ x, int64_t rows, int64_t cols, int fmt,
+                          const float *amax_in, const float *scale_in, float *scale_out,
+                          uint8_t *__restrict__ q, uint8_t *__restrict__ qt,
+                          uint32_t *amax_out) {
+  __shared__ __align__(16) uint8_t tile[kTT * kTPitch];
+  const float mx = fmt_max(fmt);
+  const float s = resolve_scale(amax_in, scale_in, mx);
+  if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+  const ScaleDiv d(s);
+  uint32_t key = 0;
+  if (d.fast)
+    quant_tensor_t_body<T, kAmax, true>(x, rows, cols, fmt, d, q, qt, tile, key);
+  else
+    quant_tensor_t_body<T, kAmax, false>(x, rows, cols, fmt, d, q, qt, tile, key);
   if (kAmax) block_max_to(key, amax_out);
 }
 
@@ -347,8 +404,7 @@ __global__ void __launch_bounds__(256)
     }
     if (valid) {
       float y[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) y[j] = q_prep(v[j], s, mx);
+      div8(ScaleDiv(s), v, y);
       *reinterpret_cast<uint2 *>(q + m * K + k) = pack8(fmt, y);
     }
   }
@@ -412,13 +468,13 @@ __global__ void __launch_bounds__(256)
     else
       reinterpret_cast<uint8_t *>(scales)[bn * KB + bk] = e8;
   }
+  const ScaleDiv d(s);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int64_t c = cbase + i * 8;
     if (r < N && c < K) {
       float y[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) y[j] = q_prep(v[i * 8 + j], s, mx);
+      div8(d, v + i * 8, y);
       *reinterpret_cast<uint2 *>(q + r * K + c) = pack8(fmt, y);
     }
   }
@@ -481,8 +537,7 @@ __global__ void __launch_bounds__(256)
     const float eff = S * exp2_int(e);           // step 4: S * r_i
     if (valid) {
       float y[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) y[j] = q_prep(v[j], eff, mx);
+      div8(ScaleDiv(eff), v, y);
       *reinterpret_cast<uint2 *>(q + r * K + k) = pack8(fmt, y);
     }
     // gather the four block bytes of each 128-wide slice into one word

@@ -69,7 +69,8 @@ def quantize_with_scale(x, scale, fmt) -> np.ndarray:
     f = fmt_of(fmt)
     x = np.asarray(x, dtype=F32)
     s = np.asarray(scale, dtype=F32)
-    y = (x / s).astype(F32)
+    with np.errstate(over="ignore"):  # x / s beyond fp32 range is inf, then clipped
+        y = (x / s).astype(F32)
     y = np.clip(y, F32(-f.max), F32(f.max)).astype(F32)
     return encode(y.astype(np.float64), f)
 

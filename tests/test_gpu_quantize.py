@@ -244,3 +244,100 @@ def test_dequantize_block(shape, sfmt, fmt):
     ref = OQ.dequantize_block(q, fmt, sc, sfmt).astype(np.float32)  # fp32 product
     ref_bf16 = torch.from_numpy(ref).to(torch.bfloat16)
     assert torch.equal(out.cpu(), ref_bf16)
+
+
+def all_finite_bf16():
+    """Every bf16 bit pattern except the NaNs (set to +0), as a 256 x 256
+    tensor: all normals, subnormals, both zeros and both infinities."""
+    bits = np.arange(65536, dtype=np.uint32)
+    nan = ((bits & 0x7F80) == 0x7F80) & ((bits & 0x007F) != 0)
+    bits[nan] = 0
+    x = (bits << 16).view(np.float32).reshape(256, 256)
+    return torch.from_numpy(x.copy()).to(torch.bfloat16)
+
+
+def scales_under_test(seed):
+    """Given scales spanning fp32: both ends of the range where the kernels
+    divide through the reciprocal (2^-80 .. 2^80) and their neighbours just
+    outside it, the usual 1 / MAX, and seeded draws with random mantissas and
+    exponents from -100 to 100."""
+    rng = np.random.default_rng(seed)
+    f = np.float32
+    fixed = [f(2.0 ** -80), f(2.0 ** 80), np.nextafter(f(2.0 ** -80), f(0)),
+             np.nextafter(f(2.0 ** 80), f(np.inf)), f(1.0) / f(448.0), f(1.0) / f(57344.0),
+             f(1.0), f(3.0), f(1e-30), f(1e30)]
+    mant = rng.integers(0, 1 << 23, 40, dtype=np.uint32)
+    expo = rng.integers(-100, 101, 40).astype(np.int64)
+    drawn = ((expo + 127).astype(np.uint32) << 23 | mant).view(np.float32)
+    return [f(v) for v in fixed] + [f(v) for v in drawn]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("transpose", [False, True])
+def test_given_scale_every_bf16_input(fmt, transpose):
+    """fl32(x / s) then the saturating cast, for every finite bf16 x and 50
+    scales: the kernels' reciprocal-based quotient must give the codes of the
+    IEEE quotient (numpy's fp32 division) bit for bit."""
+    F = lib()
+    x = all_finite_bf16()
+    xf = x.float().numpy()
+    xd = x.cuda()
+    q = torch.empty((256, 256), dtype=torch.uint8, device="cuda")
+    qt = torch.empty((256, 256), dtype=torch.uint8, device="cuda") if transpose else None
+    for s in scales_under_test(5):
+        F.fp8_quantize_tensor(xd, FMT[fmt], q, scale=torch.tensor([s], device="cuda"), q_t=qt)
+        ref = OQ.quantize_with_scale(xf, s, fmt)
+        assert np.array_equal(to_np_u8(q), ref), float(s)
+        if transpose:
+            assert np.array_equal(to_np_u8(qt), ref.T), float(s)
+
+
+def midpoint_neighbours(fmt, scales):
+    """fp32 inputs x whose quotient x / s lies on or within a few fp32 ulps of
+    a rounding midpoint between two FP8 codes (the cases a quotient that is
+    not correctly rounded would get wrong after the cast)."""
+    from oracle import formats as OF
+    f = OF.fmt_of(fmt)
+    vals = np.sort(np.unique(np.abs(OF.decode(np.arange(256, dtype=np.uint8), f))))
+    vals = vals[np.isfinite(vals)]
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    rows = []
+    for s in scales:
+        base = (mids * np.float32(s)).astype(np.float32)
+        for d in range(-3, 4):
+            v = base.view(np.int32) + np.int32(d)
+            rows.append(v.view(np.float32))
+    x = np.concatenate(rows)
+    x = np.concatenate([x, -x])
+    pad = (-len(x)) % 256
+    x = np.concatenate([x, np.zeros(pad, dtype=np.float32)]).reshape(-1, 256)
+    return x[np.isfinite(x).all(axis=1)]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_given_scale_fp32_near_fp8_midpoints(fmt):
+    F = lib()
+    scales = scales_under_test(6)[:30]
+    x = midpoint_neighbours(fmt, scales)
+    xd = torch.from_numpy(x).cuda()
+    q = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+    for s in scales:
+        F.fp8_quantize_tensor(xd, FMT[fmt], q, scale=torch.tensor([s], device="cuda"))
+        assert np.array_equal(to_np_u8(q), OQ.quantize_with_scale(x, s, fmt)), float(s)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_nan_input_gives_nan_code(fmt):
+    """The oracle takes finite inputs only; a NaN input must come out as a
+    NaN code (satfinite keeps NaN) whichever way the quotient is formed."""
+    F = lib()
+    x = torch.zeros((2, 128), device="cuda")
+    x[0, 5] = float("nan")
+    x[1, 7] = -float("nan")
+    q = torch.empty((2, 128), dtype=torch.uint8, device="cuda")
+    for s in (1.0 / 448.0, 2.0 ** 90):
+        F.fp8_quantize_tensor(x, FMT[fmt], q, scale=torch.tensor([s], device="cuda"))
+        c = to_np_u8(q)
+        nan_codes = {0x7F, 0xFF} if fmt == "e4m3" else {0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF}
+        assert int(c[0, 5]) in nan_codes and int(c[1, 7]) in nan_codes
+        assert int(c[0, 0]) == 0
