@@ -32,6 +32,7 @@ IN_BF16, IN_F32 = 0, 1
 E4M3, E5M2 = 0, 1
 SCALE_F32, SCALE_UE8M0 = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
+K_MAJOR, MN_MAJOR = 0, 1
 
 _vp, _i64, _int, _d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
 _SIGS = {
@@ -167,16 +168,18 @@ class GemmProblem(ctypes.Structure):
     """fp8_gemm_problem_t (include/fp8gemm.h)."""
     _fields_ = [("a", _vp), ("b", _vp), ("sa", _vp), ("sb", _vp), ("M", _i64), ("N", _i64),
                 ("K", _i64), ("fa", _int), ("fb", _int), ("out_dt", _int), ("accumulate", _int),
-                ("c", _vp), ("ldc", _i64)]
+                ("c", _vp), ("ldc", _i64), ("a_layout", _int), ("b_layout", _int)]
 
 
-def gemm_problem(a, fa, b, fb, sa, sb, out, *, accumulate=False):
-    """Descriptor of one per-tensor GEMM for fp8_gemm_tensor_grouped."""
-    m, k = a.shape
-    n = b.shape[0]
+def gemm_problem(a, fa, b, fb, sa, sb, out, *, accumulate=False, a_layout=K_MAJOR,
+                 b_layout=K_MAJOR):
+    """Descriptor of one per-tensor GEMM for fp8_gemm_tensor_grouped.  With
+    K_MAJOR a is [M, K] and b [N, K]; with MN_MAJOR a is [K, M] and b [K, N]."""
+    m, k = a.shape if a_layout == K_MAJOR else a.shape[::-1]
+    n = b.shape[0] if b_layout == K_MAJOR else b.shape[1]
     out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
     return GemmProblem(_p(a), _p(b), _p(sa), _p(sb), m, n, k, fa, fb, out_dt,
-                       int(bool(accumulate)), _p(out), out.stride(0))
+                       int(bool(accumulate)), _p(out), out.stride(0), a_layout, b_layout)
 
 
 def fp8_gemm_tensor_grouped(problems, stream=None):

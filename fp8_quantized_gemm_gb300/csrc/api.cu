@@ -103,6 +103,28 @@ int encode_operand(CUtensorMap *map, const void *base, int64_t k, int64_t rows, 
   return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
 }
 
+// 2-D uint8 operand stored MN-major, [k, rows] with row pitch `rows` bytes:
+// box {128 rows of the operand, 128 K}, 128-byte swizzle.
+int encode_operand_mn(CUtensorMap *map, const void *base, int64_t k, int64_t rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)rows, (cuuint64_t)k};
+  const cuuint64_t strides[1] = {(cuuint64_t)rows};
+  const cuuint32_t box[2] = {128u, 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
+// Tensor map of a per-tensor GEMM operand in either layout (box_rows: the
+// K-major box height the kernel stages).
+int encode_gemm_operand(CUtensorMap *map, const void *base, int mn_major, int64_t k,
+                        int64_t rows, int box_rows) {
+  return mn_major ? encode_operand_mn(map, base, k, rows)
+                  : encode_operand(map, base, k, rows, box_rows);
+}
+
 int check_output(const void *c, int64_t N, int64_t ldc, int out_dt) {
   if (c == nullptr) return FP8_ERR_INVALID_ARG;
   if (out_dt != FP8_OUT_F32 && out_dt != FP8_OUT_BF16) return FP8_ERR_INVALID_ARG;
@@ -161,13 +183,16 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
   }
   args.vec_store = vector_store_ok(args.c, args.ldc, args.out_dt);
   CUtensorMap tma, tmb;
-  if ((rc = encode_operand(&tma, a, args.K, args.M, 128)) != FP8_OK) return rc;
+  if ((rc = encode_gemm_operand(&tma, a, args.a_mn, args.K, args.M, 128)) != FP8_OK) return rc;
   if (args.ksplit == 1 && g_use_pairs && fp8k::gemm_pair_eligible(mode, args.M, args.N, d->sms)) {
-    if ((rc = encode_operand(&tmb, b, args.K, args.N, fp8k::gemm_pair_b_rows())) != FP8_OK)
+    if ((rc = encode_gemm_operand(&tmb, b, args.b_mn, args.K, args.N,
+                                  fp8k::gemm_pair_b_rows())) != FP8_OK)
       return rc;
     return to_status(fp8k::launch_gemm_pair(tma, tmb, args, d->sms, st));
   }
-  if ((rc = encode_operand(&tmb, b, args.K, args.N, fp8k::gemm_tile_n(mode))) != FP8_OK) return rc;
+  if ((rc = encode_gemm_operand(&tmb, b, args.b_mn, args.K, args.N, fp8k::gemm_tile_n(mode))) !=
+      FP8_OK)
+    return rc;
   return to_status(fp8k::launch_gemm(mode, tma, tmb, args, d->sms, st));
 }
 
@@ -178,6 +203,40 @@ int check_gemm_common(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, 
     return FP8_ERR_INVALID_ARG;
   if (K % kgran != 0 || !aligned16(a) || !aligned16(b)) return FP8_ERR_MISALIGNED;
   return FP8_OK;
+}
+
+// Validation of one per-tensor problem (fp8_gemm_tensor / _grouped).
+int check_tensor_problem(const fp8_gemm_problem_t &p) {
+  if (p.a == nullptr || p.b == nullptr) return FP8_ERR_INVALID_ARG;
+  if (p.M < 1 || p.N < 1 || p.K < 1 || p.M >= kMaxDim || p.N >= kMaxDim || p.K >= kMaxDim)
+    return FP8_ERR_INVALID_ARG;
+  const bool lay_ok = (p.a_layout == FP8_K_MAJOR || p.a_layout == FP8_MN_MAJOR) &&
+                      (p.b_layout == FP8_K_MAJOR || p.b_layout == FP8_MN_MAJOR);
+  if (!lay_ok) return FP8_ERR_INVALID_ARG;
+  if (p.sa == nullptr || p.sb == nullptr || !valid_fmt(p.fa) || !valid_fmt(p.fb))
+    return FP8_ERR_INVALID_ARG;
+  // the row pitch of each operand (K, or M / N when MN-major) must be a
+  // multiple of 16 bytes for its tensor map
+  const bool a_mn = p.a_layout == FP8_MN_MAJOR, b_mn = p.b_layout == FP8_MN_MAJOR;
+  if (!aligned16(p.a) || !aligned16(p.b)) return FP8_ERR_MISALIGNED;
+  if ((!a_mn || !b_mn) && p.K % 16 != 0) return FP8_ERR_MISALIGNED;
+  if ((a_mn && p.M % 16 != 0) || (b_mn && p.N % 16 != 0)) return FP8_ERR_MISALIGNED;
+  int rc = check_output(p.c, p.N, p.ldc, p.out_dt);
+  if (rc != FP8_OK) return rc;
+  if (p.accumulate != 0 && (p.accumulate != 1 || p.out_dt != FP8_OUT_F32))
+    return FP8_ERR_UNSUPPORTED;
+  return FP8_OK;
+}
+
+// One validated per-tensor problem through the regular launch path.
+int run_tensor_problem(const fp8_gemm_problem_t &p, cudaStream_t st) {
+  GemmArgs args{};
+  args.M = p.M; args.N = p.N; args.K = p.K; args.fa = p.fa; args.fb = p.fb;
+  args.out_dt = p.out_dt; args.accumulate = p.accumulate; args.ldc = p.ldc; args.c = p.c;
+  args.sa = p.sa; args.sb = p.sb;
+  args.a_mn = p.a_layout == FP8_MN_MAJOR;
+  args.b_mn = p.b_layout == FP8_MN_MAJOR;
+  return run_gemm(fp8k::kScaleTensor, p.a, p.b, args, st);
 }
 
 }  // namespace
@@ -308,29 +367,20 @@ int fp8_dequantize_block(const uint8_t *q, int fmt, const void *scales, int sfmt
 int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, const float *sa,
                     const float *sb, int64_t M, int64_t N, int64_t K, int out_dt, void *c,
                     int64_t ldc, int accumulate, fp8_stream_t stream) {
-  int rc = check_gemm_common(a, b, M, N, K, 16);
+  fp8_gemm_problem_t p{};
+  p.a = a; p.b = b; p.sa = sa; p.sb = sb; p.M = M; p.N = N; p.K = K; p.fa = fa; p.fb = fb;
+  p.out_dt = out_dt; p.accumulate = accumulate; p.c = c; p.ldc = ldc;
+  p.a_layout = FP8_K_MAJOR; p.b_layout = FP8_K_MAJOR;
+  int rc = check_tensor_problem(p);
   if (rc != FP8_OK) return rc;
-  if (sa == nullptr || sb == nullptr || !valid_fmt(fa) || !valid_fmt(fb)) return FP8_ERR_INVALID_ARG;
-  if ((rc = check_output(c, N, ldc, out_dt)) != FP8_OK) return rc;
-  if (accumulate != 0 && (accumulate != 1 || out_dt != FP8_OUT_F32)) return FP8_ERR_UNSUPPORTED;
-  GemmArgs args{};
-  args.M = M; args.N = N; args.K = K; args.fa = fa; args.fb = fb;
-  args.out_dt = out_dt; args.accumulate = accumulate; args.ldc = ldc; args.c = c;
-  args.sa = sa; args.sb = sb;
-  return run_gemm(fp8k::kScaleTensor, a, b, args, (cudaStream_t)stream);
+  return run_tensor_problem(p, (cudaStream_t)stream);
 }
 
 int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_stream_t stream) {
   if (problems == nullptr || count < 1 || count > 64) return FP8_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) {
-    const fp8_gemm_problem_t &p = problems[i];
-    int rc = check_gemm_common(p.a, p.b, p.M, p.N, p.K, 16);
+    const int rc = check_tensor_problem(problems[i]);
     if (rc != FP8_OK) return rc;
-    if (p.sa == nullptr || p.sb == nullptr || !valid_fmt(p.fa) || !valid_fmt(p.fb))
-      return FP8_ERR_INVALID_ARG;
-    if ((rc = check_output(p.c, p.N, p.ldc, p.out_dt)) != FP8_OK) return rc;
-    if (p.accumulate != 0 && (p.accumulate != 1 || p.out_dt != FP8_OUT_F32))
-      return FP8_ERR_UNSUPPORTED;
   }
   DeviceState *d = nullptr;
   int rc = device_state(&d);
@@ -346,12 +396,8 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
   }
   together = together && tiles * 4 >= d->sms / 2;
   if (!together) {
-    for (int i = 0; i < count; ++i) {
-      const fp8_gemm_problem_t &p = problems[i];
-      if ((rc = fp8_gemm_tensor(p.a, p.fa, p.b, p.fb, p.sa, p.sb, p.M, p.N, p.K, p.out_dt, p.c,
-                                p.ldc, p.accumulate, stream)) != FP8_OK)
-        return rc;
-    }
+    for (int i = 0; i < count; ++i)
+      if ((rc = run_tensor_problem(problems[i], st)) != FP8_OK) return rc;
     return FP8_OK;
   }
   // longest K first: the strided tile assignment then balances the pairs
@@ -373,10 +419,14 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
     a.err = d->err;
     a.wait_limit_ns = g_wait_limit_ns;
     a.vec_store = vector_store_ok(p.c, p.ldc, p.out_dt);
+    a.a_mn = p.a_layout == FP8_MN_MAJOR;
+    a.b_mn = p.b_layout == FP8_MN_MAJOR;
     a.ksplit = 1;
     args[k] = a;
-    if ((rc = encode_operand(&tma[k], p.a, p.K, p.M, 128)) != FP8_OK) return rc;
-    if ((rc = encode_operand(&tmb[k], p.b, p.K, p.N, fp8k::gemm_pair_b_rows())) != FP8_OK) return rc;
+    if ((rc = encode_gemm_operand(&tma[k], p.a, a.a_mn, p.K, p.M, 128)) != FP8_OK) return rc;
+    if ((rc = encode_gemm_operand(&tmb[k], p.b, a.b_mn, p.K, p.N, fp8k::gemm_pair_b_rows())) !=
+        FP8_OK)
+      return rc;
   }
   return to_status(fp8k::launch_gemm_pair_group(tma, tmb, args, count, d->sms, st));
 }

@@ -1,7 +1,10 @@
 // Scaled-FP8 GEMM kernels on the 5th-generation tensor cores (tcgen05).
 //
-// One CTA computes one 128 x BN output tile, K-major operands for both A
-// ([M, K]) and B ([N, K]), 128-byte K slices:
+// One CTA computes one 128 x BN output tile from 128-byte K slices of A
+// and B.  Operands are K-major (A [M, K], B [N, K]) in every mode; the
+// per-tensor mode also takes MN-major ones (A [K, M], B [K, N]: the codes of
+// a row-major tensor used transposed), loaded as 128-wide boxes along M or N
+// and described to the MMA as MN-major.
 //
 //   warp 0        TMA producer: A and B tiles (128-byte swizzle) into a ring
 //                 of shared-memory stages; for the block-scaled modes also
@@ -203,8 +206,20 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
             tx += C::kSfaBytes + sfb_bytes;
           }
           mbar_arrive_expect_tx(full_bar(s), tx);
-          tma_load_2d(sA(s), &tma, full_bar(s), kb * C::BK, (int32_t)m0);
-          tma_load_2d(sB(s), &tmb, full_bar(s), kb * C::BK, (int32_t)n0);
+          // tensor-map coordinates are (contiguous dim, row); an MN-major
+          // operand is loaded as 128-wide boxes along M or N, 16 KB apart
+          const int32_t k0 = kb * C::BK;
+          if (args.a_mn)
+            tma_load_2d(sA(s), &tma, full_bar(s), (int32_t)m0, k0);
+          else
+            tma_load_2d(sA(s), &tma, full_bar(s), k0, (int32_t)m0);
+          if (args.b_mn) {
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tma_load_2d(sB(s) + h * 128 * C::BK, &tmb, full_bar(s), (int32_t)n0 + 128 * h, k0);
+          } else {
+            tma_load_2d(sB(s), &tmb, full_bar(s), k0, (int32_t)n0);
+          }
           if constexpr (MODE == kScaleMx) {
             const int64_t mpad = (args.M + 127) / 128 * 128;
             const int64_t npad = (args.N + 127) / 128 * 128;
@@ -275,11 +290,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
                            tmem + sfb_col, (kb != kb0 || k != 0) ? 1u : 0u);
             }
           } else {
-            const uint32_t idesc = idesc_f8f6f4(128, BN, args.fa, args.fb);
+            const uint32_t idesc = idesc_f8f6f4(128, BN, args.fa, args.fb, args.a_mn, args.b_mn);
+            const OperandDesc ad = operand_desc(sA(s), args.a_mn, C::kABytes);
+            const OperandDesc bd = operand_desc(sB(s), args.b_mn, 128 * C::BK);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const bool acc = C::kPromote ? (k != 0) : (kb != kb0 || k != 0);
-              mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc ? 1u : 0u);
+              mma_f8f6f4(d, ad.base + k * ad.step, bd.base + k * bd.step, idesc, acc ? 1u : 0u);
             }
           }
           mma_commit(empty_bar(s));

@@ -15,6 +15,11 @@
 //     full" to both CTAs; both epilogues hand the accumulator back by arriving
 //     on the leader's barrier.
 //
+// Operands may be K-major ([rows, K]) or MN-major ([K, rows], the codes of a
+// row-major tensor used transposed); the tensor map, the TMA coordinates, the
+// shared-memory descriptors and the instruction descriptor's major bits
+// follow the layout, the data flow is the same.
+//
 // Two TMEM accumulators per CTA: the epilogue of one tile overlaps the MMAs
 // of the next.  Scales are applied once in the epilogue (Flax guide 2.2).
 //
@@ -46,6 +51,7 @@ struct PairCfg {
   static constexpr uint32_t kSmem = 1024 + kTileBytes + 8 * kNumBars + 16;
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kSmem <= 227 * 1024, "shared-memory budget");
+  static_assert(BM == 128 && BN / 2 == 128, "MN-major tiles: one 128-wide TMA box per operand");
 };
 
 struct PairGroup {
@@ -153,14 +159,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
           break;
         }
         if (elect_one()) {
+          // tensor-map coordinates are (contiguous dim, row): (k, m) for a
+          // K-major operand, (m, k) for an MN-major one; both boxes are 16 KB
+          const GemmArgs &ga = grp.args[tr.i];
+          const int32_t k0 = kb * C::BK;
+          const int32_t ax = ga.a_mn ? (int32_t)m0 : k0, ay = ga.a_mn ? k0 : (int32_t)m0;
+          const int32_t bx = ga.b_mn ? (int32_t)nb0 : k0, by = ga.b_mn ? k0 : (int32_t)nb0;
           if (leader) {
             mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
-            tma_load_2d(sA(s), ma, full_bar(s), kb * C::BK, (int32_t)m0);
-            tma_load_2d(sB(s), mb, full_bar(s), kb * C::BK, (int32_t)nb0);
+            tma_load_2d(sA(s), ma, full_bar(s), ax, ay);
+            tma_load_2d(sB(s), mb, full_bar(s), bx, by);
           } else {
             const uint32_t fb = full_leader0 + 8u * (uint32_t)s;
-            tma_load_2d_pair(sA(s), ma, fb, kb * C::BK, (int32_t)m0);
-            tma_load_2d_pair(sB(s), mb, fb, kb * C::BK, (int32_t)nb0);
+            tma_load_2d_pair(sA(s), ma, fb, ax, ay);
+            tma_load_2d_pair(sB(s), mb, fb, bx, by);
           }
         }
         __syncwarp();
@@ -181,7 +193,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
       bool ok = true;
       for (int64_t gt = pair; gt < num_tiles && ok; gt += npairs, ++j) {
         const TileRef tr = tile_ref(gt);
-        const uint32_t idesc = idesc_f8f6f4(256, BN, grp.args[tr.i].fa, grp.args[tr.i].fb);
+        const GemmArgs &ga = grp.args[tr.i];
+        const uint32_t idesc = idesc_f8f6f4(256, BN, ga.fa, ga.fb, ga.a_mn, ga.b_mn);
         const uint32_t buf = j & 1u, use = j >> 1;
         if (!mbar_wait(acce_bar(buf), (use & 1u) ^ 1u, abort_flag, err, 2)) {
           ok = false;
@@ -196,11 +209,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = sdesc_sw128(sA(s));
-          const uint64_t bdesc = sdesc_sw128(sB(s));
+          // per CTA each operand tile is 128 rows wide: one 128-element
+          // block along M or N, so the MN-major leading offset is not used
+          const OperandDesc ad = operand_desc(sA(s), ga.a_mn, C::kABytes);
+          const OperandDesc bd = operand_desc(sB(s), ga.b_mn, C::kBBytes);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f8f6f4_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            mma_f8f6f4_pair(d, ad.base + k * ad.step, bd.base + k * bd.step, idesc,
+                            (kb | k) != 0 ? 1u : 0u);
           mma_commit_pair(empty_bar(s), (uint16_t)0x3);
         }
         if (!ok) break;

@@ -42,6 +42,7 @@ struct GemmArgs {
   int out_dt;          // 0 = f32, 1 = bf16
   int accumulate;      // f32 output only
   int vec_store;       // 1: c and ldc allow 16-byte vector stores
+  int a_mn, b_mn;      // 1: operand stored MN-major ([K, M] / [K, N]); per-tensor mode only
   int64_t ldc;
   void *c;
   const void *sa, *sb;         // scale operands (meaning depends on the mode)

@@ -71,6 +71,10 @@ typedef enum { FP8_IN_BF16 = 0, FP8_IN_F32 = 1 } fp8_in_dtype_t;
 typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_fmt_t; /* E4M3fn max 448, E5M2 max 57344 */
 typedef enum { FP8_SCALE_F32 = 0, FP8_SCALE_UE8M0 = 1 } fp8_scale_fmt_t;
 typedef enum { FP8_OUT_F32 = 0, FP8_OUT_BF16 = 1 } fp8_out_dtype_t;
+/* Storage of a GEMM operand of logical shape [R, K] (R = M for A, N for B):
+ * K-major = [R, K] row-major (K contiguous); MN-major = [K, R] row-major (R
+ * contiguous), i.e. the row-major codes of the transposed operand. */
+typedef enum { FP8_K_MAJOR = 0, FP8_MN_MAJOR = 1 } fp8_layout_t;
 
 /* ------------------------------------------------------------------ amax --
  * fp8_amax: amax_out[0] = max |x[i]| over i < n ([Flax] 1: "amax is the max
@@ -194,20 +198,27 @@ FP8_API int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, 
 
 /* ------------------------------------------- GEMM, per tensor, grouped --
  * fp8_gemm_tensor_grouped: `count` independent per-tensor GEMMs in one call,
- * each exactly as fp8_gemm_tensor would compute it (same arguments, same
- * bound).  Up to 4 problems whose shapes suit the CTA-pair path run as ONE
- * persistent launch over all their tiles (longest K first), which pays the
- * kernel prologue, pipeline fill and tail once instead of per GEMM -- e.g.
- * the forward and both backward GEMMs of a linear layer once their operands
- * are quantized ([Nano] "实现": three GEMMs).  Otherwise the problems run one
- * after another on `stream`.
+ * each computed as fp8_gemm_tensor would (same bound), with a storage layout
+ * per operand.  Up to 4 problems whose shapes suit the CTA-pair path run as
+ * ONE persistent launch over all their tiles (longest K first), which pays
+ * the kernel prologue, pipeline fill and tail once instead of per GEMM --
+ * e.g. the forward and both backward GEMMs of a linear layer once their
+ * operands are quantized ([Nano] "实现": three GEMMs).  Otherwise the
+ * problems run one after another on `stream`.
  *   problems  HOST array of `count` descriptors (read during the call only);
  *             the pointers inside are device pointers as for fp8_gemm_tensor.
+ *   a_layout, b_layout  FP8_K_MAJOR (a [M, K], b [N, K], as fp8_gemm_tensor)
+ *             or FP8_MN_MAJOR (a [K, M], b [K, N]: the row-major codes of a
+ *             row-major tensor used transposed, so that dx = g W and
+ *             dW = g^T x read the codes of g, W and x without a transposed
+ *             copy).  An MN-major operand needs its row count (M or N) to be
+ *             a multiple of 16; K % 16 == 0 is needed only while an operand
+ *             is K-major.  FP8_ERR_MISALIGNED otherwise.
  *   No output may overlap another problem's output or inputs.
  */
 typedef struct {
-  const uint8_t *a; /* [M, K] codes, format fa */
-  const uint8_t *b; /* [N, K] codes, format fb */
+  const uint8_t *a; /* codes of format fa: [M, K] (K-major) or [K, M] (MN-major) */
+  const uint8_t *b; /* codes of format fb: [N, K] (K-major) or [K, N] (MN-major) */
   const float *sa;  /* device fp32 dequant scale of a */
   const float *sb;  /* device fp32 dequant scale of b */
   int64_t M, N, K;
@@ -216,6 +227,8 @@ typedef struct {
   int accumulate; /* 1: C += result (FP8_OUT_F32 only) */
   void *c;        /* [M, ldc] row-major */
   int64_t ldc;
+  int a_layout;   /* fp8_layout_t */
+  int b_layout;   /* fp8_layout_t */
 } fp8_gemm_problem_t;
 
 FP8_API int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count,

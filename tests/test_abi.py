@@ -97,3 +97,30 @@ def test_quantize_validation(lib):
     d.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
     assert d(16, 16, 16, 0, 0, None) == -1
     assert d(16, 16, 16, 1 << 20, 0, None) == -1
+
+
+def _grouped(lib, **kw):
+    import fp8_quantized_gemm_gb300 as F
+    p = dict(a=16, b=16, sa=16, sb=16, M=128, N=128, K=128, fa=0, fb=0, out_dt=1, accumulate=0,
+             c=256, ldc=128, a_layout=0, b_layout=0)
+    p.update(kw)
+    arr = (F.GemmProblem * 1)(F.GemmProblem(**p))
+    f = lib.fp8_gemm_tensor_grouped
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    return f(ctypes.cast(arr, ctypes.c_void_p), 1, None)
+
+
+def test_grouped_layout_validation(lib):
+    """MN-major operands: the pitch (M or N bytes) must be a multiple of 16;
+    K % 16 is required only while an operand is K-major."""
+    import torch
+    no_gpu = not torch.cuda.is_available()
+    assert _grouped(lib, a_layout=2) == -1                        # bad layout enum
+    assert _grouped(lib, a_layout=1, M=120) == -2                 # MN-major A, M % 16
+    assert _grouped(lib, b_layout=1, N=200) == -2                 # MN-major B, N % 16
+    assert _grouped(lib, a_layout=1, K=17) == -2                  # B still K-major
+    assert _grouped(lib, K=17) == -2
+    if no_gpu:
+        assert _grouped(lib, a_layout=1, b_layout=1, K=17) == -6  # valid: reaches the device
+        assert _grouped(lib, a_layout=1, b_layout=1, M=16, N=32, K=1) == -6
+        assert _grouped(lib) == -6

@@ -344,3 +344,105 @@ def test_gemm_tensor_grouped_accumulate_and_ragged():
         c, e = OG.gemm(OG.dequant_operand(qa, "e4m3", sa), OG.dequant_operand(qb, "e4m3", sb))
         ok, worst = OG.check(outs[i].cpu().numpy(), c + prev[i], e + np.abs(prev[i]) * 1e-3, "f32")
         assert ok, (i, worst)
+
+
+# ------------------------------------------------- MN-major operand layouts --
+
+def run_tensor_layout(qa, fa, sa, qb, fb, sb, a_mn, b_mn, out_dtype="bf16"):
+    """One per-tensor GEMM through fp8_gemm_tensor_grouped with the operands
+    uploaded in the requested layout: MN-major means the codes of the
+    transposed operand, row-major ([K, M] for A, [K, N] for B)."""
+    F = lib()
+    m, n = qa.shape[0], qb.shape[0]
+    a = dev_u8(qa.T if a_mn else qa)
+    b = dev_u8(qb.T if b_mn else qb)
+    out = torch.empty((m, n), dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float32,
+                      device="cuda")
+    lay = lambda mn: F.MN_MAJOR if mn else F.K_MAJOR
+    F.fp8_gemm_tensor_grouped([F.gemm_problem(a, FMT[fa], b, FMT[fb], dev_f32(sa), dev_f32(sb),
+                                              out, a_layout=lay(a_mn), b_layout=lay(b_mn))])
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+# (M, N, K): CTA-pair path, single-CTA path, ragged M / N, split-K (small M),
+# and K that is not a multiple of 16 (allowed when both operands are MN-major)
+MN_SHAPES = [(2048, 2048, 1024), (1296, 784, 2000), (256, 512, 384), (208, 400, 256),
+             (32, 2048, 4096)]
+
+
+@pytest.mark.parametrize("mnk", MN_SHAPES)
+@pytest.mark.parametrize("layout", [(False, True), (True, False), (True, True)])
+def test_gemm_tensor_mn_major(mnk, layout):
+    F = lib()
+    m, n, k = mnk
+    a_mn, b_mn = layout
+    qa, sa, qb, sb = per_tensor_operands(m, n, k, "e5m2", "e4m3", seed=m + 7 * k)
+    c, e = OG.gemm(OG.dequant_operand(qa, "e5m2", sa), OG.dequant_operand(qb, "e4m3", sb))
+    try:
+        for pairs in (1, 0):
+            F.fp8_set_option(F.OPT_GEMM_CTA_PAIRS, pairs)
+            got = run_tensor_layout(qa, "e5m2", sa, qb, "e4m3", sb, a_mn, b_mn)
+            ok, worst = OG.check(got, c, e, "bf16")
+            assert ok, (pairs, worst)
+    finally:
+        F.fp8_set_option(F.OPT_GEMM_CTA_PAIRS, 1)
+    assert F.fp8_get_last_device_error()[0] == 0
+
+
+@pytest.mark.parametrize("k", [1, 8, 200, 1000])
+def test_gemm_tensor_mn_major_ragged_k(k):
+    """Both operands MN-major: K is the outer dimension of both tensor maps,
+    so any K works (the last K slice is zero-filled by TMA)."""
+    m, n = 256, 512
+    qa, sa, qb, sb = per_tensor_operands(m, n, k, "e4m3", "e4m3", seed=k)
+    c, e = OG.gemm(OG.dequant_operand(qa, "e4m3", sa), OG.dequant_operand(qb, "e4m3", sb))
+    got = run_tensor_layout(qa, "e4m3", sa, qb, "e4m3", sb, True, True, "f32")
+    ok, worst = OG.check(got, c, e, "f32")
+    assert ok, worst
+
+
+@pytest.mark.parametrize("shape", [(2048, 1024, 1024), (2000, 784, 1296), (8192, 2048, 2048)])
+def test_gemm_tensor_grouped_linear_without_transposed_copies(shape):
+    """The linear layer's three GEMMs on the row-major codes of x, W and g
+    only: y = x W^T (K-major, K-major), dx = g W (K-major, W MN-major),
+    dW = g^T x (g MN-major, x MN-major); the last shape is the full-size
+    Float8 linear, checked on sampled outputs."""
+    F = lib()
+    t, d_in, d_out = shape
+    seed = t + 1
+    x = workloads.normal((t, d_in), 1.0, seed).to(torch.bfloat16).float().numpy()
+    w = workloads.normal((d_out, d_in), 0.02, seed + 1).to(torch.bfloat16).float().numpy()
+    g = workloads.normal((t, d_out), 1e-3, seed + 2).to(torch.bfloat16).float().numpy()
+    qx, sx = OQ.quantize_tensor(x, "e4m3")
+    qw, sw = OQ.quantize_tensor(w, "e4m3")
+    qg, sg = OQ.quantize_tensor(g, "e5m2")
+    dx_, dw_, dg_ = dev_u8(qx), dev_u8(qw), dev_u8(qg)
+    s = [dev_f32(sx), dev_f32(sw), dev_f32(sg)]
+    y = torch.empty((t, d_out), dtype=torch.bfloat16, device="cuda")
+    dxo = torch.empty((t, d_in), dtype=torch.bfloat16, device="cuda")
+    dwo = torch.empty((d_out, d_in), dtype=torch.float32, device="cuda")
+    K, MN = F.K_MAJOR, F.MN_MAJOR
+    F.fp8_gemm_tensor_grouped([
+        F.gemm_problem(dx_, F.E4M3, dw_, F.E4M3, s[0], s[1], y),
+        F.gemm_problem(dg_, F.E5M2, dw_, F.E4M3, s[2], s[1], dxo, b_layout=MN),
+        F.gemm_problem(dg_, F.E5M2, dx_, F.E4M3, s[2], s[0], dwo, a_layout=MN, b_layout=MN),
+    ])
+    torch.cuda.synchronize()
+    xd = OG.dequant_operand(qx, "e4m3", sx)
+    wd = OG.dequant_operand(qw, "e4m3", sw)
+    gd = OG.dequant_operand(qg, "e5m2", sg)
+    cases = [(y, xd, wd, "bf16"), (dxo, gd, np.ascontiguousarray(wd.T), "bf16"),
+             (dwo, np.ascontiguousarray(gd.T), np.ascontiguousarray(xd.T), "f32")]
+    full = t * d_in * d_out <= 2048 ** 3
+    for i, (out, a, b, odt) in enumerate(cases):
+        got = out.float().cpu().numpy()
+        if full:
+            c, e = OG.gemm(a, b)
+            ok, worst = OG.check(got, c, e, odt)
+        else:
+            rows, cols = sample_positions(a.shape[0], b.shape[0], 300, seed=i)
+            c, e = OG.gemm_sampled(a, b, rows, cols)
+            ok, worst = OG.check(got[rows, cols], c, e, odt)
+        assert ok, (i, worst)
+    assert F.fp8_get_last_device_error()[0] == 0
