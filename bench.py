@@ -2,9 +2,11 @@
 
 Default workload (one "step"): the Float8 linear forward + backward with
 per-tensor current scaling -- x[8192,2048] (E4M3), W[2048,2048] (E4M3),
-grad_out[8192,2048] (E5M2), bf16 in and out: three amax passes, three fused
-quantize passes (each also writing the transposed copy the backward GEMMs
-read), and the three GEMMs y = x W^T, dx = g W, dW = g^T x.
+grad_out[8192,2048] (E5M2), bf16 in and out: current scaling of x, g and W
+in one launch (amax, scale and row-major codes of each, the reduction of one
+tensor overlapped with the cast of the previous), then the three GEMMs
+y = x W^T, dx = g W, dW = g^T x in one grouped launch that reads the codes
+K-major or MN-major as each GEMM needs.
 
 Printed: one JSON line with the headline metric (FP8 scaled-GEMM TFLOP/s
 including quantization), the GEMM roofline against the dense FP8 peak, the
@@ -150,9 +152,10 @@ def pinned(t: torch.Tensor) -> torch.Tensor:
 class Float8Linear:
     """Float8 linear forward + backward, per-tensor current scaling.
 
-    GEMM operands are K-contiguous ([rows, K]): y = x W^T reads x_q and W_q;
-    dx = g W reads g_q and W_q^T; dW = g^T x reads g_q^T and x_q^T.  The
-    quantize passes write both layouts in one pass."""
+    Each tensor is quantized once, to row-major codes; the GEMMs read them in
+    the layout they need: y = x W^T takes x_q and W_q K-major; dx = g W takes
+    g_q K-major and W_q MN-major; dW = g^T x takes g_q and x_q MN-major (no
+    transposed copies are written)."""
 
     name = "float8_linear_fwd_bwd"
 
@@ -165,11 +168,12 @@ class Float8Linear:
         self.x, self.w, self.g = (t.to(dev) for t in self.host_in)
         u8 = dict(dtype=torch.uint8, device=dev)
         T, di, do = tokens, d_in, d_out
-        self.xq, self.xqt = torch.empty((T, di), **u8), torch.empty((di, T), **u8)
-        self.wq, self.wqt = torch.empty((do, di), **u8), torch.empty((di, do), **u8)
-        self.gq, self.gqt = torch.empty((T, do), **u8), torch.empty((do, T), **u8)
+        self.xq = torch.empty((T, di), **u8)
+        self.wq = torch.empty((do, di), **u8)
+        self.gq = torch.empty((T, do), **u8)
         self.amax = torch.empty(3, device=dev)
         self.scale = torch.empty(3, device=dev)
+        self.sync = torch.zeros(F.QUANT_SYNC_WORDS, dtype=torch.int32, device=dev)
         bf = dict(dtype=torch.bfloat16, device=dev)
         self.y, self.dx, self.dw = torch.empty((T, do), **bf), torch.empty((T, di), **bf), \
             torch.empty((do, di), **bf)
@@ -178,57 +182,33 @@ class Float8Linear:
         self.flops = 3 * 2.0 * T * di * do
         n_x, n_w, n_g = T * di, do * di, T * do
         self.n_elems = n_x + n_w + n_g
-        # algorithmic bytes per launch: amax reads 2 B/elem; quantize reads
-        # 2 B and writes 1 B + 1 B (transposed copy) per element
-        self.bytes = {"amax": 2.0 * self.n_elems / 3, "quantize": 4.0 * self.n_elems / 3}
-        # the three GEMMs (y = x W^T, dx = g W, dW = g^T x) as one grouped call
-        F = self.F
+        # algorithmic HBM bytes per step: current scaling of x, g and W reads
+        # each input once (2 B/elem) and writes its codes (1 B/elem)
+        self.bytes = {"quantize": 3.0 * self.n_elems}
+        # x, g and W in one launch, in that order (the small W last: while one
+        # tensor is cast the next is reduced, so the last one is the tail)
         s = self.scale
+        self.items = [F.quant_item(self.x, F.E4M3, self.xq, s[0:1], self.amax[0:1]),
+                      F.quant_item(self.g, F.E5M2, self.gq, s[2:3], self.amax[2:3]),
+                      F.quant_item(self.w, F.E4M3, self.wq, s[1:2], self.amax[1:2])]
+        # the three GEMMs (y = x W^T, dx = g W, dW = g^T x) as one grouped call
+        MN = F.MN_MAJOR
         self.problems = [
             F.gemm_problem(self.xq, F.E4M3, self.wq, F.E4M3, s[0:1], s[1:2], self.y),
-            F.gemm_problem(self.gq, F.E5M2, self.wqt, F.E4M3, s[2:3], s[1:2], self.dx),
-            F.gemm_problem(self.gqt, F.E5M2, self.xqt, F.E4M3, s[2:3], s[0:1], self.dw),
+            F.gemm_problem(self.gq, F.E5M2, self.wq, F.E4M3, s[2:3], s[1:2], self.dx,
+                           b_layout=MN),
+            F.gemm_problem(self.gq, F.E5M2, self.xq, F.E4M3, s[2:3], s[0:1], self.dw,
+                           a_layout=MN, b_layout=MN),
         ]
         self.h2d = sum(t.numel() * t.element_size() for t in self.host_in)
         self.d2h = sum(t.numel() * t.element_size() for t in self.outputs)
 
     def launches(self):
         F = self.F
-        a, s = self.amax, self.scale
-        T, di, do = self.T, self.din, self.dout
         return [
-            ("amax", lambda: F.fp8_amax(self.x, a[0:1])),
-            ("amax", lambda: F.fp8_amax(self.w, a[1:2])),
-            ("amax", lambda: F.fp8_amax(self.g, a[2:3])),
-            ("quantize", lambda: F.fp8_quantize_tensor(self.x, F.E4M3, self.xq, amax_in=a[0:1],
-                                                       scale_out=s[0:1], q_t=self.xqt)),
-            ("quantize", lambda: F.fp8_quantize_tensor(self.w, F.E4M3, self.wq, amax_in=a[1:2],
-                                                       scale_out=s[1:2], q_t=self.wqt)),
-            ("quantize", lambda: F.fp8_quantize_tensor(self.g, F.E5M2, self.gq, amax_in=a[2:3],
-                                                       scale_out=s[2:3], q_t=self.gqt)),
+            ("quantize", lambda: F.fp8_quantize_tensors(self.items, self.sync)),
             ("gemm", lambda: F.fp8_gemm_tensor_grouped(self.problems)),
         ]
-
-    def capture_branches(self):
-        """The step as a graph with independent branches on forked streams:
-        the three amax -> quantize chains run side by side, then the grouped
-        GEMM (y, dx and dW in one launch) runs once all three have finished."""
-        L = dict((i, fn) for i, (_, fn) in enumerate(self.launches()))
-        main = torch.cuda.current_stream()
-        side = [torch.cuda.Stream() for _ in range(2)]
-        for st in side:
-            st.wait_stream(main)
-        # quantize chains: x on main, W and g on the side streams
-        L[0](); L[3]()
-        with torch.cuda.stream(side[0]):
-            L[1](); L[4]()
-        with torch.cuda.stream(side[1]):
-            L[2](); L[5]()
-        for st in side:
-            main.wait_stream(st)
-            st.wait_stream(main)
-        # the three GEMMs: one grouped launch once all operands are quantized
-        L[6]()
 
     def upload(self, stream):
         for h, d in zip(self.host_in, (self.x, self.w, self.g)):
@@ -470,8 +450,7 @@ def run_ours(args):
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # dense FP8 = 2 x bf16 (nominal ratio)
     # algorithmic work of a step over the per-step device time of each kind
     gemm_tflops = wl.flops / (sum(per["gemm"]) / reps / 1e3) / 1e12
-    q_gbs = wl.bytes["quantize"] * 3 / (sum(per["quantize"]) / reps / 1e3) / 1e9
-    a_gbs = wl.bytes["amax"] * 3 / (sum(per["amax"]) / reps / 1e3) / 1e9
+    q_gbs = wl.bytes["quantize"] / (sum(per["quantize"]) / reps / 1e3) / 1e9
     src = "MEASURED_PEAKS.json (%s)" % peaks["source"]
     line = {
         "metric": "FP8 scaled-GEMM TFLOP/s incl. quantize, % of FP8 peak; quantize GB/s % HBM",
@@ -485,18 +464,17 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "fraction_of_fp8_peak": round(value / fp8_peak, 4),
         "roofline": roofline_entry("tensor", gemm_tflops, fp8_peak, "TFLOP/s",
-                                   recorded_traffic("gemm_tensor"),
+                                   recorded_traffic("gemm_pair_grouped"),
                                    "dense FP8 = 2 x measured bf16 burst (%s)" % src),
         "quantize_roofline": roofline_entry("hbm", q_gbs, peaks["hbm_gbs"], "GB/s",
-                                            recorded_traffic("quantize_tensor_t"),
+                                            recorded_traffic("quantize_multi"),
                                             "measured HBM copy (%s)" % src),
-        "amax_roofline": roofline_entry("hbm", a_gbs, peaks["hbm_gbs"], "GB/s",
-                                        recorded_traffic("amax"), "measured HBM copy (%s)" % src),
         "launch": "eager (one API call per kernel)" if args.eager else
                   "CUDA graph of the step's API calls, replayed",
         "eager": {"value": round(eager_value, 2), "ms_per_step": round(eager_total_ms / args.steps, 4)},
         "kernel_ms": {k: round(sum(v) / len(v), 4) for k, v in per.items()},
-        "kernel_ms_note": "mean per launch; gemm is one grouped launch of the three GEMMs",
+        "kernel_ms_note": "mean per launch: quantize is one launch for x, g and W (amax, "
+                          "scale and codes of each), gemm one grouped launch of the three GEMMs",
         "kernel_timing": "each launch bracketed by CUDA events in step order, L2 flushed per "
                          "step, a memory-free spin kernel queued before each launch",
         "gpu_launches": n_launch * args.steps,

@@ -46,6 +46,7 @@ _SIGS = {
     "fp8_gemm_tensor": [_vp, _int, _vp, _int, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp],
     "fp8_gemm_group": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_gemm_tensor_grouped": [_vp, _int, _vp],
+    "fp8_quantize_tensors": [_vp, _int, _vp, _vp],
     "fp8_gemm_mx": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp],
     "fp8_gemm_group_noalloc": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_delayed_state_update": [_vp, _vp, _vp, _i64, _int, _vp],
@@ -180,6 +181,30 @@ def gemm_problem(a, fa, b, fb, sa, sb, out, *, accumulate=False, a_layout=K_MAJO
     out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
     return GemmProblem(_p(a), _p(b), _p(sa), _p(sb), m, n, k, fa, fb, out_dt,
                        int(bool(accumulate)), _p(out), out.stride(0), a_layout, b_layout)
+
+
+class QuantItem(ctypes.Structure):
+    """fp8_quant_item_t (include/fp8gemm.h)."""
+    _fields_ = [("x", _vp), ("in_dt", _int), ("n", _i64), ("fmt", _int), ("q", _vp),
+                ("amax_out", _vp), ("scale_out", _vp)]
+
+
+def quant_item(x, fmt, q, scale_out, amax_out=None):
+    """Descriptor of one tensor for fp8_quantize_tensors (current scaling)."""
+    assert q.numel() == x.numel()
+    return QuantItem(_p(x), _in_dt(x), x.numel(), fmt, _p(q),
+                     _p(amax_out) if amax_out is not None else None, _p(scale_out))
+
+
+QUANT_SYNC_WORDS = 8
+
+
+def fp8_quantize_tensors(items, sync, stream=None):
+    """Current scaling of up to four tensors in one launch (pipelined in
+    order); `sync` is a device int32 tensor of QUANT_SYNC_WORDS words."""
+    assert sync.numel() * sync.element_size() >= 4 * QUANT_SYNC_WORDS
+    arr = (QuantItem * len(items))(*items)
+    _call("fp8_quantize_tensors", ctypes.cast(arr, _vp), len(items), _p(sync), _stream(stream))
 
 
 def fp8_gemm_tensor_grouped(problems, stream=None):

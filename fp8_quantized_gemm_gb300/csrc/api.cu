@@ -290,6 +290,44 @@ int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, in
                                              (cudaStream_t)stream));
 }
 
+int fp8_quantize_tensors(const fp8_quant_item_t *items, int count, uint32_t *sync,
+                         fp8_stream_t stream) {
+  static_assert(FP8_QUANT_SYNC_WORDS == 2 * fp8k::kMaxMulti, "sync scratch size");
+  if (items == nullptr || count < 1 || count > fp8k::kMaxMulti) return FP8_ERR_INVALID_ARG;
+  if (sync == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(sync)) return FP8_ERR_MISALIGNED;
+  const int in_dt = items[0].in_dt;
+  if (!valid_in(in_dt)) return FP8_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    const fp8_quant_item_t &it = items[i];
+    if (it.x == nullptr || it.q == nullptr || it.scale_out == nullptr || !valid_fmt(it.fmt))
+      return FP8_ERR_INVALID_ARG;
+    if (!valid_in(it.in_dt)) return FP8_ERR_INVALID_ARG;
+    if (it.in_dt != in_dt) return FP8_ERR_UNSUPPORTED;
+    if (it.amax_out == it.scale_out) return FP8_ERR_INVALID_ARG;
+    if (it.n < 0 || it.n >= ((int64_t)1 << 40)) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(it.x) || !aligned16(it.q)) return FP8_ERR_MISALIGNED;
+  }
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  const cudaStream_t st = (cudaStream_t)stream;
+  fp8k::MultiQuantArgs a{};
+  for (int i = 0; i < count; ++i) {
+    a.x[i] = items[i].x;
+    a.n[i] = items[i].n;
+    a.fmt[i] = items[i].fmt;
+    a.q[i] = items[i].q;
+    a.amax_out[i] = items[i].amax_out;
+    a.scale_out[i] = items[i].scale_out;
+  }
+  a.count = count;
+  a.sync = sync;
+  a.err = d->err;
+  a.wait_limit_ns = g_wait_limit_ns;
+  return to_status(fp8k::launch_quant_multi(a, in_dt, d->sms, st));
+}
+
 int fp8_quantize_token_group(const void *x, int in_dt, int64_t M, int64_t K, int fmt, int sfmt,
                              uint8_t *q, void *scales, fp8_stream_t stream) {
   if (x == nullptr || q == nullptr || scales == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))

@@ -115,6 +115,15 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// Short non-abortable wait used only on the abort path (drains async work
+// before the CTA exits).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > 20000000ull) break;  // 20 ms
+  }
+}
+
 // -------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -402,12 +411,70 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float y) {
   return fabsf(q0) < 0x1p100f ? q2 : q0;
 }
 
+// Packed fp32 pairs for the f32x2 FMA pipe of sm_100-class GPUs (one
+// instruction computes two independent single-precision mul / fma, each
+// rounded as the scalar instruction would be).
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// div_by_scale on two values at once: the same five rounded operations per
+// value, issued as packed pairs (y2 = {y, y}, ns2 = {-s, -s}).
+__device__ __forceinline__ void div_by_scale2(float x0, float x1, uint64_t ns2, uint64_t y2,
+                                              float &o0, float &o1) {
+  const uint64_t xv = f32x2_pack(x0, x1);
+  const uint64_t q0 = f32x2_mul(xv, y2);
+  const uint64_t r0 = f32x2_fma(ns2, q0, xv);
+  const uint64_t q1 = f32x2_fma(r0, y2, q0);
+  const uint64_t r1 = f32x2_fma(ns2, q1, xv);
+  const uint64_t q2 = f32x2_fma(r1, y2, q1);
+  float a0, a1, b0, b1;
+  f32x2_unpack(q0, a0, a1);
+  f32x2_unpack(q2, b0, b1);
+  o0 = fabsf(a0) < 0x1p100f ? copysignf(b0, x0) : a0;
+  o1 = fabsf(a1) < 0x1p100f ? copysignf(b1, x1) : a1;
+}
+
+// div_by_scale2 for quotients known to be finite and far from overflow (the
+// scale was formed from this very tensor's amax, so |x / s| <= MAX (1 +
+// 2^-23) and x is finite): no range guard, and the sign is not forced.  A
+// positive x still gives a non-negative result and a negative x a
+// non-positive one, but a zero or underflowed quotient may carry the wrong
+// sign of zero; the caller puts x's sign into each FP8 code instead.
+__device__ __forceinline__ void div_by_scale2_bounded(float x0, float x1, uint64_t ns2,
+                                                      uint64_t y2, float &o0, float &o1) {
+  const uint64_t xv = f32x2_pack(x0, x1);
+  const uint64_t q0 = f32x2_mul(xv, y2);
+  const uint64_t r0 = f32x2_fma(ns2, q0, xv);
+  const uint64_t q1 = f32x2_fma(r0, y2, q0);
+  const uint64_t r1 = f32x2_fma(ns2, q1, xv);
+  f32x2_unpack(f32x2_fma(r1, y2, q1), o0, o1);
+}
+
 struct ScaleDiv {
   float s, y;
+  uint64_t ns2, y2;  // {-s, -s}, {y, y} for div_by_scale2
   bool fast;
   __device__ __forceinline__ explicit ScaleDiv(float s_) {
     s = s_;
     y = __frcp_rn(s_);
+    ns2 = f32x2_pack(-s_, -s_);
+    y2 = f32x2_pack(y, y);
     fast = s_ >= 0x1p-80f && s_ <= 0x1p80f;
   }
   // kFast: the caller has checked `fast` (uniformly, outside its loop)
@@ -417,6 +484,19 @@ struct ScaleDiv {
       return div_by_scale(x, s, y);
     else
       return __fdiv_rn(x, s);
+  }
+  // eight quotients (four packed pairs on the fast path)
+  template <bool kFast>
+  __device__ __forceinline__ void div8(const float (&v)[8], float (&o)[8]) const {
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      if constexpr (kFast) {
+        div_by_scale2(v[j], v[j + 1], ns2, y2, o[j], o[j + 1]);
+      } else {
+        o[j] = __fdiv_rn(v[j], s);
+        o[j + 1] = __fdiv_rn(v[j + 1], s);
+      }
+    }
   }
 };
 

@@ -1,5 +1,5 @@
 // Epilogue helpers shared by the GEMM kernels: output stores, split-K
-// partials, the epilogue-only named barrier and the abort-path drain wait.
+// partials and the epilogue-only named barrier.
 #pragma once
 
 #include "common.cuh"
@@ -43,15 +43,6 @@ __device__ __forceinline__ void store_row32(const GemmArgs &a, int64_t row, int6
     } else {
       for (int i = 0; i < 32 && col0 + i < a.N; ++i) dst[i] = a.accumulate ? dst[i] + v[i] : v[i];
     }
-  }
-}
-
-// Short non-abortable wait used only on the abort path (drains async work
-// before the CTA exits).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > 20000000ull) break;  // 20 ms
   }
 }
 

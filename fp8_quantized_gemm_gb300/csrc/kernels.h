@@ -28,6 +28,24 @@ cudaError_t launch_auto_scale(const float *amax0, double grow, int fmt, float *s
 cudaError_t launch_delayed_update(float *hist, float *scale, const float *amax_cur, int64_t L,
                                   int fmt, cudaStream_t st);
 
+// Current scaling of up to kMaxMulti tensors in one cooperative launch
+// (quantize_multi.cu).  `sync` is device scratch of 2 * kMaxMulti uint32
+// words (keys, then arrival counters), cleared by the launcher.
+constexpr int kMaxMulti = 4;
+struct MultiQuantArgs {
+  const void *x[kMaxMulti];
+  int64_t n[kMaxMulti];
+  int fmt[kMaxMulti];
+  uint8_t *q[kMaxMulti];
+  float *amax_out[kMaxMulti];   // nullable
+  float *scale_out[kMaxMulti];
+  int count;
+  uint32_t *sync;
+  uint32_t *err;               // device error word
+  uint64_t wait_limit_ns;      // bound of every wait
+};
+cudaError_t launch_quant_multi(const MultiQuantArgs &args, int in_dt, int sms, cudaStream_t st);
+
 // GEMM family.  Scale modes of the epilogue / main loop:
 enum GemmScaleMode : int {
   kScaleTensor = 0,      // per-tensor: alpha = sa[0] * sb[0] in the epilogue

@@ -10,140 +10,24 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "quant_common.cuh"
 
 namespace fp8k {
 
-// ---------------------------------------------------------------- loads --
-// Eight consecutive input elements as fp32 (bf16: one 16-byte load; f32: two).
-template <typename T>
-struct Vec8;
-
-template <>
-struct Vec8<__nv_bfloat16> {
-  static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[8]) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
-  static __device__ __forceinline__ void load_stream(const __nv_bfloat16 *p, float (&v)[8]) {
-    const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
-};
-
-template <>
-struct Vec8<float> {
-  static __device__ __forceinline__ void load(const float *p, float (&v)[8]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  }
-  static __device__ __forceinline__ void load_stream(const float *p, float (&v)[8]) {
-    const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  }
-};
-
-// Raw 16-byte vectors holding 8 elements (bf16: one uint4; f32: two), kept
-// undecoded in registers until used.
-template <typename T>
-struct Raw8 {
-  static constexpr int kWords = sizeof(T) * 8 / 16;
-  uint4 w[kWords];
-  __device__ __forceinline__ void load_stream(const T *p) {
-#pragma unroll
-    for (int i = 0; i < kWords; ++i) w[i] = __ldcs(reinterpret_cast<const uint4 *>(p) + i);
-  }
-  __device__ __forceinline__ void zero() {
-#pragma unroll
-    for (int i = 0; i < kWords; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  __device__ __forceinline__ void decode(float (&v)[8]) const {
-    if constexpr (sizeof(T) == 2) {
-      const uint32_t u[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(u[i] << 16);
-        v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        v[4 * i] = __uint_as_float(w[i].x);
-        v[4 * i + 1] = __uint_as_float(w[i].y);
-        v[4 * i + 2] = __uint_as_float(w[i].z);
-        v[4 * i + 3] = __uint_as_float(w[i].w);
-      }
-    }
-  }
-};
-
-template <typename T>
-__device__ __forceinline__ float load1(const T *p);
-template <>
-__device__ __forceinline__ float load1<__nv_bfloat16>(const __nv_bfloat16 *p) {
-  return __bfloat162float(*p);
-}
-template <>
-__device__ __forceinline__ float load1<float>(const float *p) { return *p; }
-
-// 8 values -> 8 codes packed little-endian into a uint2.
-__device__ __forceinline__ uint2 pack8(int fmt, const float (&y)[8]) {
-  const uint32_t c0 = cvt_fp8x2(fmt, y[0], y[1]), c1 = cvt_fp8x2(fmt, y[2], y[3]);
-  const uint32_t c2 = cvt_fp8x2(fmt, y[4], y[5]), c3 = cvt_fp8x2(fmt, y[6], y[7]);
-  return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
-}
-
-// Eight quotients v[j] / s by one scale (ScaleDiv; the fast/slow choice is
-// per scale, so it diverges only between groups with extreme scales).
-__device__ __forceinline__ void div8(const ScaleDiv &d, const float *v, float (&y)[8]) {
-  if (d.fast) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) y[j] = d.div<true>(v[j]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) y[j] = d.div<false>(v[j]);
-  }
-}
-
-// Block-wide max of a uint32 key, then one atomicMax per block.
-__device__ __forceinline__ void block_max_to(uint32_t key, uint32_t *dst) {
-  __shared__ uint32_t red[32];
-  key = warp_max_u32(key);
-  const int w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  if (lane_id() == 0) red[w] = key;
-  __syncthreads();
-  if (w == 0) {
-    uint32_t k = lane_id() < (uint32_t)nw ? red[lane_id()] : 0u;
-    k = warp_max_u32(k);
-    if (lane_id() == 0 && k != 0u) atomicMax(dst, k);
-  }
-}
-
 // ------------------------------------------------------------------ amax --
+// One wave of persistent CTAs (2 x 512 threads per SM) streams the tensor
+// with batches of eight independent 16-byte loads per thread.
 template <typename T>
-__global__ void __launch_bounds__(512) amax_kernel(const T *__restrict__ x, int64_t n,
-                                                   uint32_t *__restrict__ out) {
-  uint32_t key = 0;
+__global__ void __launch_bounds__(512, 2) amax_kernel(const T *__restrict__ x, int64_t n,
+                                                      uint32_t *__restrict__ out) {
+  uint32_t key_a = 0, key_b = 0;
   const int64_t nvec = n / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  // batches of eight independent 16-byte loads per thread, all issued first
   for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec;
        base += 8 * stride) {
     // loads are unconditional (index clamped in range) so that all eight are
-    // in flight at once; out-of-range vectors are masked after the loads
+    // in flight at once; a clamped load repeats the last vector, which leaves
+    // the max unchanged
     Raw8<T> raw[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -151,14 +35,9 @@ __global__ void __launch_bounds__(512) amax_kernel(const T *__restrict__ x, int6
       raw[u].load_stream(x + (i < nvec ? i : nvec - 1) * 8);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (base + u * stride >= nvec) continue;
-      float v[8];
-      raw[u].decode(v);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
-    }
+    for (int u = 0; u < 8; ++u) raw[u].max_abs(key_a, key_b);
   }
+  uint32_t key = Raw8<T>::merge_keys(key_a, key_b);
   for (int64_t i = nvec * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
     key = max(key, abs_key(load1(x + i)));
   block_max_to(key, out);
@@ -179,35 +58,39 @@ __device__ __forceinline__ void quant_tensor_body(const T *__restrict__ x, int64
   const int64_t nvec = n / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < nvec; i += 4 * stride) {
-    float v[4][8];
+  // four 16-byte loads in flight per thread (bf16: four vectors, f32: two),
+  // kept as raw words until used
+  constexpr int kU = sizeof(T) == 2 ? 4 : 2;
+  for (; i + (kU - 1) * stride < nvec; i += kU * stride) {
+    Raw8<T> raw[kU];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) Vec8<T>::load_stream(x + (i + u * stride) * 8, v[u]);
+    for (int u = 0; u < kU; ++u) raw[u].load_stream(x + (i + u * stride) * 8);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float y[8];
+    for (int u = 0; u < kU; ++u) {
+      float v[8], y[8];
+      raw[u].decode(v);
+      if (kAmax) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (kAmax) key = max(key, abs_key(v[u][j]));
-        y[j] = d.div<kFast>(v[u][j]);
+        for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
       }
+      d.div8<kFast>(v, y);
       reinterpret_cast<uint2 *>(q)[i + u * stride] = pack8(fmt, y);
     }
   }
   for (; i < nvec; i += stride) {
     float v[8], y[8];
     Vec8<T>::load_stream(x + i * 8, v);
+    if (kAmax) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (kAmax) key = max(key, abs_key(v[j]));
-      y[j] = d.div<kFast>(v[j]);
+      for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
     }
+    d.div8<kFast>(v, y);
     reinterpret_cast<uint2 *>(q)[i] = pack8(fmt, y);
   }
 }
 
 template <typename T, bool kAmax>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(256, kAmax ? 3 : 4)
     quant_tensor_kernel(const T *__restrict__ x, int64_t n, int fmt, const float *amax_in,
                         const float *scale_in, float *scale_out, uint8_t *__restrict__ q,
                         uint32_t *amax_out) {
@@ -264,14 +147,21 @@ __device__ __forceinline__ void quant_tensor_t_body(const T *__restrict__ x, int
                                                     uint8_t *__restrict__ q,
                                                     uint8_t *__restrict__ qt, uint8_t *tile,
                                                     uint32_t &key) {
-  const int64_t tiles_c = (cols + kTT - 1) / kTT;
-  const int64_t ntiles = ((rows + kTT - 1) / kTT) * tiles_c;
+  // tile counts fit 32 bits (rows, cols < 2^31 and 128-wide tiles), so the
+  // tile -> (row, column) split is a 32-bit division, once per tile
+  const uint32_t tiles_c = (uint32_t)((cols + kTT - 1) / kTT);
+  const uint32_t ntiles = (uint32_t)((rows + kTT - 1) / kTT) * tiles_c;
   const int t = threadIdx.x;
   const int lc = (t & 15) * 8;
+  auto tile_origin = [&](uint32_t tl, int64_t &r0, int64_t &c0) {
+    const uint32_t tr = tl / tiles_c;
+    r0 = (int64_t)tr * kTT;
+    c0 = (int64_t)(tl - tr * tiles_c) * kTT;
+  };
   // Persistent CTAs loop over 128 x 128 tiles; the eight 16-byte loads of the
   // NEXT tile are issued before the current tile is processed.
-  auto load_tile = [&](int64_t tl, Raw8<T> (&raw)[kTT / 16]) {
-    const int64_t r0 = (tl / tiles_c) * kTT, c = (tl % tiles_c) * kTT + lc;
+  auto load_tile = [&](int64_t r0, int64_t c0, Raw8<T> (&raw)[kTT / 16]) {
+    const int64_t c = c0 + lc;
 #pragma unroll
     for (int pass = 0; pass < kTT / 16; ++pass) {
       const int64_t r = r0 + pass * 16 + (t >> 4);
@@ -283,14 +173,19 @@ __device__ __forceinline__ void quant_tensor_t_body(const T *__restrict__ x, int
   };
   constexpr bool kPrefetch = sizeof(T) == 2;  // fp32 inputs: registers too tight
   Raw8<T> cur[kTT / 16], nxt[kTT / 16];
-  if (kPrefetch && (int64_t)blockIdx.x < ntiles) load_tile(blockIdx.x, cur);
-  for (int64_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x) {
+  int64_t r0 = 0, c0 = 0, nr0 = 0, nc0 = 0;
+  if (blockIdx.x < ntiles) {
+    tile_origin(blockIdx.x, r0, c0);
+    if (kPrefetch) load_tile(r0, c0, cur);
+  }
+  for (uint32_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x) {
+    const bool has_next = tl + gridDim.x < ntiles;
+    if (has_next) tile_origin(tl + gridDim.x, nr0, nc0);
     if constexpr (kPrefetch) {
-      if (tl + gridDim.x < ntiles) load_tile(tl + gridDim.x, nxt);
+      if (has_next) load_tile(nr0, nc0, nxt);
     } else {
-      load_tile(tl, cur);
+      load_tile(r0, c0, cur);
     }
-    const int64_t r0 = (tl / tiles_c) * kTT, c0 = (tl % tiles_c) * kTT;
     const int64_t c = c0 + lc;
     // phase 1: quantize, row-major store, stage the codes in shared memory
 #pragma unroll
@@ -299,11 +194,11 @@ __device__ __forceinline__ void quant_tensor_t_body(const T *__restrict__ x, int
       const int64_t r = r0 + lr;
       float v[8], y[8];
       cur[pass].decode(v);
+      if (kAmax) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (kAmax) key = max(key, abs_key(v[j]));
-        y[j] = d.div<kFast>(v[j]);
+        for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
       }
+      d.div8<kFast>(v, y);
       const uint2 packed = pack8(fmt, y);
       if (r < rows && c < cols) *reinterpret_cast<uint2 *>(q + r * cols + c) = packed;
       *reinterpret_cast<uint2 *>(&tile[lr * kTPitch + tchunk(lr, lc >> 3)]) = packed;
@@ -334,6 +229,8 @@ __device__ __forceinline__ void quant_tensor_t_body(const T *__restrict__ x, int
 #pragma unroll
       for (int pass = 0; pass < kTT / 16; ++pass) cur[pass] = nxt[pass];
     }
+    r0 = nr0;
+    c0 = nc0;
   }
 }
 
@@ -601,7 +498,7 @@ cudaError_t launch_amax(const void *x, int in_dt, int64_t n, float *out, int sms
                         cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), st);
   if (e != cudaSuccess || n == 0) return e;
-  const int threads = 512, blocks = grid_for((n + 7) / 8, threads, 4, sms);
+  const int threads = 512, blocks = grid_for((n + 7) / 8, threads, 2, sms);
   if (in_dt == 0)
     amax_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(x), n, reinterpret_cast<uint32_t *>(out));
@@ -623,7 +520,8 @@ cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t 
   const bool fused = amax_out != nullptr;
   if (qt == nullptr) {
     const int64_t n = rows * cols;
-    const int threads = 512, blocks = grid_for(n / 8, threads, 4, sms);
+    // one wave of resident CTAs (launch bounds: 4 per SM, 3 with the fused amax)
+    const int threads = 256, blocks = grid_for(n / 8, threads, fused ? 3 : 4, sms);
 #define FP8K_QT(T, A)                                                                          \
   quant_tensor_kernel<T, A><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), n, fmt, amax_in, \
                                                         scale, scale_out, q, ao)

@@ -20,6 +20,12 @@ scaling (section 5, eq. 10): each weight's scale is predicted as
 ago, without reading the weight; the max-reduction (fp8_amax) is redone every
 `rescale_interval` steps (500 in the blog).
 
+Every tensor is quantized once, to row-major codes; the GEMMs read them
+K-major or MN-major as they need (dx = dh W1 reads W1's codes MN-major,
+dW1 = dh^T x reads dh's and x's codes MN-major), so no transposed copies are
+written.  GEMMs with independent outputs share one grouped launch (h and u;
+da and dW2; dx's first term, dW1 and dW3).
+
 Buffers are allocated once (device memory through torch); `step` issues the
 calls on the current stream.
 """
@@ -62,15 +68,13 @@ class SwiGLUTrainer:
         self.hist = torch.zeros((9, history), **f32)
         self.scale = torch.ones(9, **f32)
         self.amax = torch.zeros(9, **f32)
-        # quantized operands (row-major and transposed copies)
-        self.xq, self.xqt = torch.empty((T, d), **u8), torch.empty((d, T), **u8)
-        self.w1q, self.w1qt = torch.empty((ffn, d), **u8), torch.empty((d, ffn), **u8)
-        self.w3q, self.w3qt = torch.empty((ffn, d), **u8), torch.empty((d, ffn), **u8)
-        self.w2q, self.w2qt = torch.empty((d, ffn), **u8), torch.empty((ffn, d), **u8)
-        self.aq, self.aqt = torch.empty((T, ffn), **u8), torch.empty((ffn, T), **u8)
-        self.dyq, self.dyqt = torch.empty((T, d), **u8), torch.empty((d, T), **u8)
-        self.dhq, self.dhqt = torch.empty((T, ffn), **u8), torch.empty((ffn, T), **u8)
-        self.duq, self.duqt = torch.empty((T, ffn), **u8), torch.empty((ffn, T), **u8)
+        # quantized operands (row-major codes)
+        self.xq = torch.empty((T, d), **u8)
+        self.w1q, self.w3q = torch.empty((ffn, d), **u8), torch.empty((ffn, d), **u8)
+        self.w2q = torch.empty((d, ffn), **u8)
+        self.aq = torch.empty((T, ffn), **u8)
+        self.dyq = torch.empty((T, d), **u8)
+        self.dhq, self.duq = torch.empty((T, ffn), **u8), torch.empty((T, ffn), **u8)
         # activations and gradients
         self.h, self.u, self.a = (torch.empty((T, ffn), **bf) for _ in range(3))
         self.y = torch.empty((T, d), **bf)
@@ -99,37 +103,42 @@ class SwiGLUTrainer:
 
     def forward_backward(self, x: torch.Tensor, dy: torch.Tensor):
         """The nine GEMMs with their quantize and SwiGLU passes (no optimizer)."""
-        E4, E5 = F.E4M3, F.E5M2
-        q, g = F.fp8_quantize_tensor, F.fp8_gemm_tensor
+        E4, E5, MN = F.E4M3, F.E5M2, F.MN_MAJOR
+        q, P, run = F.fp8_quantize_tensor, F.gemm_problem, F.fp8_gemm_tensor_grouped
         w1, w3, w2 = self.w_bf
+        sc = self._sc
         # forward
-        q(x, E4, self.xq, scale=self._sc(X1), q_t=self.xqt, amax_out=self._am(X1))
+        q(x, E4, self.xq, scale=sc(X1), amax_out=self._am(X1))
         if self.weight_scaling == "auto":
             for i, slot in ((0, K1), (1, K3), (2, K2)):
                 F.fp8_auto_weight_scale(self.w_amax0[i:i + 1], self.t_since, self.hp["lr"], E4,
-                                        self._sc(slot))
+                                        sc(slot))
             wam = (None, None, None)
         else:
             wam = (self._am(K1), self._am(K3), self._am(K2))
-        q(w1, E4, self.w1q, scale=self._sc(K1), q_t=self.w1qt, amax_out=wam[0])
-        q(w3, E4, self.w3q, scale=self._sc(K3), q_t=self.w3qt, amax_out=wam[1])
-        q(w2, E4, self.w2q, scale=self._sc(K2), q_t=self.w2qt, amax_out=wam[2])
-        g(self.xq, E4, self.w1q, E4, self._sc(X1), self._sc(K1), self.h)
-        g(self.xq, E4, self.w3q, E4, self._sc(X1), self._sc(K3), self.u)
+        q(w1, E4, self.w1q, scale=sc(K1), amax_out=wam[0])
+        q(w3, E4, self.w3q, scale=sc(K3), amax_out=wam[1])
+        q(w2, E4, self.w2q, scale=sc(K2), amax_out=wam[2])
+        run([P(self.xq, E4, self.w1q, E4, sc(X1), sc(K1), self.h),          # h = x W1^T
+             P(self.xq, E4, self.w3q, E4, sc(X1), sc(K3), self.u)])         # u = x W3^T
         F.fp8_swiglu_forward(self.h, self.u, self.a)
-        q(self.a, E4, self.aq, scale=self._sc(A2), q_t=self.aqt, amax_out=self._am(A2))
-        g(self.aq, E4, self.w2q, E4, self._sc(A2), self._sc(K2), self.y)
+        q(self.a, E4, self.aq, scale=sc(A2), amax_out=self._am(A2))
+        run([P(self.aq, E4, self.w2q, E4, sc(A2), sc(K2), self.y)])         # y = a W2^T
         # backward
-        q(dy, E5, self.dyq, scale=self._sc(G2), q_t=self.dyqt, amax_out=self._am(G2))
-        g(self.dyq, E5, self.w2qt, E4, self._sc(G2), self._sc(K2), self.da)
-        g(self.dyqt, E5, self.aqt, E4, self._sc(G2), self._sc(A2), self.dw[2])
+        q(dy, E5, self.dyq, scale=sc(G2), amax_out=self._am(G2))
+        run([P(self.dyq, E5, self.w2q, E4, sc(G2), sc(K2), self.da, b_layout=MN),   # da = dy W2
+             P(self.dyq, E5, self.aq, E4, sc(G2), sc(A2), self.dw[2],               # dW2 = dy^T a
+               a_layout=MN, b_layout=MN)])
         F.fp8_swiglu_backward(self.da, self.h, self.u, self.dh, self.du)
-        q(self.dh, E5, self.dhq, scale=self._sc(G1), q_t=self.dhqt, amax_out=self._am(G1))
-        q(self.du, E5, self.duq, scale=self._sc(G3), q_t=self.duqt, amax_out=self._am(G3))
-        g(self.dhq, E5, self.w1qt, E4, self._sc(G1), self._sc(K1), self.dx)
-        g(self.duq, E5, self.w3qt, E4, self._sc(G3), self._sc(K3), self.dx, accumulate=True)
-        g(self.dhqt, E5, self.xqt, E4, self._sc(G1), self._sc(X1), self.dw[0])
-        g(self.duqt, E5, self.xqt, E4, self._sc(G3), self._sc(X1), self.dw[1])
+        q(self.dh, E5, self.dhq, scale=sc(G1), amax_out=self._am(G1))
+        q(self.du, E5, self.duq, scale=sc(G3), amax_out=self._am(G3))
+        run([P(self.dhq, E5, self.w1q, E4, sc(G1), sc(K1), self.dx, b_layout=MN),   # dx = dh W1
+             P(self.dhq, E5, self.xq, E4, sc(G1), sc(X1), self.dw[0],               # dW1 = dh^T x
+               a_layout=MN, b_layout=MN),
+             P(self.duq, E5, self.xq, E4, sc(G3), sc(X1), self.dw[1],               # dW3 = du^T x
+               a_layout=MN, b_layout=MN)])
+        run([P(self.duq, E5, self.w3q, E4, sc(G3), sc(K3), self.dx, b_layout=MN,    # dx += du W3
+               accumulate=True)])
 
     def optimizer_and_state(self):
         """AdamW on the three weights, then the nine amax-history pushes."""

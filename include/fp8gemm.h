@@ -106,6 +106,43 @@ FP8_API int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t 
                         const float *amax_in, const float *scale, float *scale_out,
                         uint8_t *q, uint8_t *q_t, float *amax_out, fp8_stream_t stream);
 
+/* ------------------------------------------ quantize, several tensors --
+ * fp8_quantize_tensors: current scaling ([Flax] 2.2) of `count` (1..4)
+ * tensors in ONE launch.  For each item: amax = max |x|, scale =
+ * fl32(amax / MAX) (1.0 for amax 0), q = RNE_fp8(clip(x / scale)) -- the same
+ * amax, scale and bytes as fp8_amax followed by fp8_quantize_tensor with
+ * amax_in.  Row-major codes only (the per-tensor GEMMs read them K- or
+ * MN-major).  The items are pipelined in the order given: while tensor t is
+ * divided and cast, tensor t+1 is being reduced.
+ *   items  HOST array of `count` descriptors (read during the call only).
+ *     x         device, 16-byte aligned, n >= 0 elements of in_dt (every item
+ *               the same in_dt, else FP8_ERR_UNSUPPORTED)
+ *     q         device, 16-byte aligned, n bytes; must not overlap any x
+ *     amax_out  nullable device fp32;  scale_out  device fp32 (required,
+ *               distinct from amax_out)
+ *   sync   device scratch of FP8_QUANT_SYNC_WORDS uint32 words, 16-byte
+ *          aligned, owned by the caller: the call clears it (a memset on
+ *          `stream`) and the kernel's CTAs count themselves in there.  Calls
+ *          that can run at the same time need distinct scratch.  Nothing is
+ *          allocated, so the call can be captured into a CUDA graph.
+ * Runs as a cooperative launch (one CTA per SM, all resident at once: its
+ * quantize warps wait for every CTA's share of the amax, bounded by the wait
+ * limit; FP8_ERR_TIMEOUT is then reported by fp8_get_last_device_error).
+ */
+#define FP8_QUANT_SYNC_WORDS 8
+typedef struct {
+  const void *x;
+  int in_dt;
+  int64_t n;
+  int fmt;
+  uint8_t *q;
+  float *amax_out;
+  float *scale_out;
+} fp8_quant_item_t;
+
+FP8_API int fp8_quantize_tensors(const fp8_quant_item_t *items, int count, uint32_t *sync,
+                                 fp8_stream_t stream);
+
 /* -------------------------------------------------- quantize token group --
  * fp8_quantize_token_group: dynamic per-token activation quantization in
  * 1 x 128 K groups ([HF] 一; scale formats [HF] 四/七).

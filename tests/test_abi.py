@@ -124,3 +124,35 @@ def test_grouped_layout_validation(lib):
         assert _grouped(lib, a_layout=1, b_layout=1, K=17) == -6  # valid: reaches the device
         assert _grouped(lib, a_layout=1, b_layout=1, M=16, N=32, K=1) == -6
         assert _grouped(lib) == -6
+
+
+def _qtensors(lib, count=1, sync=16, **kw):
+    import fp8_quantized_gemm_gb300 as F
+    p = dict(x=16, in_dt=0, n=1024, fmt=0, q=32, amax_out=None, scale_out=48)
+    p.update(kw)
+    items = [F.QuantItem(**p) for _ in range(max(count, 1))]
+    arr = (F.QuantItem * len(items))(*items)
+    f = lib.fp8_quantize_tensors
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    return f(ctypes.cast(arr, ctypes.c_void_p), count, sync, None)
+
+
+def test_quantize_tensors_validation(lib):
+    import fp8_quantized_gemm_gb300 as F
+    import torch
+    assert _qtensors(lib, count=0) == -1                 # empty list
+    assert _qtensors(lib, count=5) == -1                 # more than four tensors
+    assert _qtensors(lib, sync=None) == -1               # no scratch
+    assert _qtensors(lib, sync=20) == -2                 # misaligned scratch
+    assert _qtensors(lib, scale_out=None) == -1          # scale is an output
+    assert _qtensors(lib, amax_out=48) == -1             # amax and scale alias
+    assert _qtensors(lib, x=24) == -2                    # misaligned input
+    assert _qtensors(lib, fmt=3) == -1
+    items = [F.QuantItem(x=16, in_dt=0, n=64, fmt=0, q=32, amax_out=None, scale_out=48),
+             F.QuantItem(x=64, in_dt=1, n=64, fmt=0, q=96, amax_out=None, scale_out=52)]
+    arr = (F.QuantItem * 2)(*items)
+    f = lib.fp8_quantize_tensors
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(ctypes.cast(arr, ctypes.c_void_p), 2, 16, None) == -3   # mixed input dtypes
+    if not torch.cuda.is_available():
+        assert _qtensors(lib) == -6

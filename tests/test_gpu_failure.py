@@ -55,3 +55,26 @@ def test_timeout_in_group_gemm_resets_split_k_counters():
     for _ in range(2):
         ok, worst = OG.check(run_group(qa, sa, qb, sb, "f32"), c, e, "bf16")
         assert ok, worst
+
+
+def test_timeout_in_multi_tensor_quantize():
+    """The cooperative quantize waits on its copies and on the other CTAs'
+    amax shares; with the bound at zero one of them runs out, the kernel
+    reports it and exits, and the next call is exact."""
+    F = lib()
+    import workloads
+    from gpu_util import FMT, f32_bits, to_np_u8
+    from oracle import quantize as OQ
+    x = workloads.normal((2048, 2048), 1.0, 7).to(torch.bfloat16).cuda()
+    q = torch.empty((2048, 2048), dtype=torch.uint8, device="cuda")
+    scale = torch.zeros(1, device="cuda")
+    sync = torch.zeros(F.QUANT_SYNC_WORDS, dtype=torch.int32, device="cuda")
+    items = [F.quant_item(x, FMT["e4m3"], q, scale)]
+    rc, where = forced_timeout(lambda: F.fp8_quantize_tensors(items, sync))
+    assert rc == F.FP8_ERR_TIMEOUT and 11 <= where <= 15, (rc, where)
+    F.fp8_quantize_tensors(items, sync)
+    torch.cuda.synchronize()
+    ref_q, ref_s = OQ.quantize_tensor(x.float().cpu().numpy(), "e4m3")
+    assert f32_bits(scale.item()) == f32_bits(ref_s)
+    assert np.array_equal(to_np_u8(q), ref_q)
+    assert F.fp8_get_last_device_error()[0] == 0

@@ -341,3 +341,108 @@ def test_nan_input_gives_nan_code(fmt):
         nan_codes = {0x7F, 0xFF} if fmt == "e4m3" else {0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF}
         assert int(c[0, 5]) in nan_codes and int(c[1, 7]) in nan_codes
         assert int(c[0, 0]) == 0
+
+
+# ------------------------------------------ several tensors in one launch --
+
+def run_quantize_tensors(xs, fmts):
+    F = lib()
+    dev = [x.cuda() for x in xs]
+    qs = [torch.empty(x.numel(), dtype=torch.uint8, device="cuda") for x in xs]
+    amax = torch.zeros(len(xs), device="cuda")
+    scale = torch.zeros(len(xs), device="cuda")
+    sync = torch.zeros(F.QUANT_SYNC_WORDS, dtype=torch.int32, device="cuda")
+    items = [F.quant_item(d, FMT[f], q, scale[i:i + 1], amax[i:i + 1])
+             for i, (d, f, q) in enumerate(zip(dev, fmts, qs))]
+    F.fp8_quantize_tensors(items, sync)
+    torch.cuda.synchronize()
+    return [to_np_u8(q) for q in qs], amax.cpu().numpy(), scale.cpu().numpy()
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_quantize_tensors_matches_oracle(dt):
+    """Four tensors: ragged sizes (n % 8 == 1 included), both formats, and an
+    all-zero tensor (amax 0 -> scale 1); amax, scale and codes bit-exact."""
+    xs = [special_input((300, 520), 1.0, 21, dt, "e4m3"),
+          special_input((8, 16), 1e-3, 22, dt, "e5m2"),
+          workloads.normal((1001,), 1.0, 23).to(dt),
+          torch.zeros((64, 64), dtype=dt)]
+    fmts = ["e4m3", "e5m2", "e4m3", "e5m2"]
+    codes, amax, scale = run_quantize_tensors(xs, fmts)
+    for i, (x, f) in enumerate(zip(xs, fmts)):
+        xf = x.float().numpy().reshape(-1)
+        ref_q, ref_s = OQ.quantize_tensor(xf, f)
+        assert f32_bits(amax[i]) == f32_bits(OQ.amax(xf)), i
+        assert f32_bits(scale[i]) == f32_bits(ref_s), i
+        assert np.array_equal(codes[i], ref_q), i
+
+
+def test_quantize_tensors_float8_linear_full_size():
+    """The Float8 linear step's x, g and W (8192 x 2048, 8192 x 2048,
+    2048 x 2048) in the order the step quantizes them."""
+    x, w, g = workloads.float8_linear()
+    xs, fmts = [x, g, w], ["e4m3", "e5m2", "e4m3"]
+    codes, amax, scale = run_quantize_tensors(xs, fmts)
+    for i, (t, f) in enumerate(zip(xs, fmts)):
+        tf = t.float().numpy().reshape(-1)
+        ref_q, ref_s = OQ.quantize_tensor(tf, f)
+        assert f32_bits(scale[i]) == f32_bits(ref_s), i
+        assert np.array_equal(codes[i], ref_q), i
+
+
+def test_quantize_tensors_in_a_cuda_graph():
+    """Captured once, replayed on new data: the scratch is cleared by the
+    captured memset, so every replay starts from zero."""
+    F = lib()
+    shapes = [(512, 1024), (256, 256)]
+    xs = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in shapes]
+    qs = [torch.empty(s, dtype=torch.uint8, device="cuda") for s in shapes]
+    scale = torch.zeros(2, device="cuda")
+    sync = torch.zeros(F.QUANT_SYNC_WORDS, dtype=torch.int32, device="cuda")
+    items = [F.quant_item(xs[i], F.E4M3, qs[i], scale[i:i + 1]) for i in range(2)]
+    for i, s in enumerate(shapes):
+        xs[i].copy_(workloads.normal(s, 1.0, 30 + i))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        F.fp8_quantize_tensors(items, sync)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        F.fp8_quantize_tensors(items, sync)
+    for rep in range(3):
+        host = [workloads.normal(s, 0.5 + rep, 40 + 2 * rep + i).to(torch.bfloat16)
+                for i, s in enumerate(shapes)]
+        for i in range(2):
+            xs[i].copy_(host[i])
+        graph.replay()
+        torch.cuda.synchronize()
+        for i in range(2):
+            ref_q, ref_s = OQ.quantize_tensor(host[i].float().numpy(), "e4m3")
+            assert f32_bits(scale[i].item()) == f32_bits(ref_s), (rep, i)
+            assert np.array_equal(to_np_u8(qs[i]), ref_q), (rep, i)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_quantize_tensors_every_bf16_below_amax(fmt):
+    """The scale of current scaling comes from the tensor itself, so every
+    quotient is bounded; the kernel then divides without the range guard and
+    puts each input's sign into its code.  Checked on tensors that hold every
+    finite bf16 value up to 2^k (both zeros, all subnormals, both signs), for
+    k from -100 to 100: amax, scale and every code bit-exact."""
+    bits = np.arange(65536, dtype=np.uint32)
+    allv = (bits << 16).view(np.float32)
+    allv = allv[np.isfinite(allv)]
+    xs = []
+    for k in (-100, -20, -3, 0, 5, 17, 60, 100):
+        v = allv[np.abs(allv) <= np.float32(2.0 ** k)]
+        xs.append(torch.from_numpy(v.copy()).to(torch.bfloat16))
+    for i in range(0, len(xs), 4):
+        chunk = xs[i:i + 4]
+        codes, amax, scale = run_quantize_tensors(chunk, [fmt] * len(chunk))
+        for j, x in enumerate(chunk):
+            xf = x.float().numpy()
+            ref_q, ref_s = OQ.quantize_tensor(xf, fmt)
+            assert f32_bits(scale[j]) == f32_bits(ref_s), (i + j)
+            assert np.array_equal(codes[j], ref_q), (i + j)
