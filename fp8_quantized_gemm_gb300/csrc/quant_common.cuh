@@ -69,20 +69,19 @@ struct Raw8 {
 #pragma unroll
     for (int i = 0; i < kWords; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
   }
-  // Running max of |x| over the 8 elements as order-preserving uint32 keys
-  // (the fp32 bit pattern of |x|).  bf16: the high halves of the words are
-  // compared in place (key_a) and the low halves unshifted (key_b, shifted
-  // once at the end), two instructions per element pair each way.
+  // Running max of |x| over the 8 elements as order-preserving keys.  bf16:
+  // key_a holds two 16-bit keys (|x| bits of the even and odd elements, max
+  // taken per halfword), so one mask and one paired max per element pair;
+  // merge_keys folds them into the fp32 bit pattern of |x|.  fp32: two
+  // running uint32 keys.
   __device__ __forceinline__ void max_abs(uint32_t &key_a, uint32_t &key_b) const {
     if constexpr (sizeof(T) == 2) {
+      (void)key_b;
 #pragma unroll
       for (int i = 0; i < kWords; ++i) {
         const uint32_t u[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          key_a = max(key_a, u[j] & 0x7FFF0000u);
-          key_b = max(key_b, u[j] & 0x00007FFFu);
-        }
+        for (int j = 0; j < 4; ++j) key_a = __vmaxu2(key_a, u[j] & 0x7FFF7FFFu);
       }
     } else {
 #pragma unroll
@@ -112,7 +111,8 @@ struct Raw8 {
   }
   // Combine the two running keys of max_abs into one fp32 |x| key.
   static __device__ __forceinline__ uint32_t merge_keys(uint32_t key_a, uint32_t key_b) {
-    return sizeof(T) == 2 ? max(key_a, key_b << 16) : max(key_a, key_b);
+    if constexpr (sizeof(T) == 2) return max(key_a & 0xFFFF0000u, key_a << 16);
+    return max(key_a, key_b);
   }
   __device__ __forceinline__ void decode(float (&v)[8]) const {
     if constexpr (sizeof(T) == 2) {

@@ -30,7 +30,9 @@
 namespace fp8k {
 
 constexpr uint32_t kMQChunk = 24576;
-constexpr int kMQStagesA = 4, kMQStagesB = 4;
+// ring A streams from HBM (deep: ~144 KB in flight per SM); ring B mostly
+// hits L2 (the amax pass read the same bytes just before)
+constexpr int kMQStagesA = 6, kMQStagesB = 3;
 constexpr int kMQWarpsA = 4, kMQWarpsB = 24;
 constexpr int kMQThreadsA = 32 * kMQWarpsA, kMQThreadsB = 32 * kMQWarpsB;
 constexpr int kMQThreads = 64 + kMQThreadsA + kMQThreadsB;
@@ -153,7 +155,16 @@ __global__ void __launch_bounds__(kMQThreads, 1)
         if (!mbar_wait_warp(full_a(s), (it / kMQStagesA) & 1u, abort_flag, err, 13)) continue;
         const uint32_t nvec = chunk_bytes(t, c) / (8 * sizeof(T));
         const uint8_t *base = ring_a + s * kMQChunk;
-        for (uint32_t v = tid; v < nvec; v += kMQThreadsA) {
+        // four vectors per step: four shared loads in flight per thread
+        uint32_t v = tid;
+        for (; v + 3 * kMQThreadsA < nvec; v += 4 * kMQThreadsA) {
+          Raw8<T> r[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) r[u].load_shared(base + (v + u * kMQThreadsA) * 8 * sizeof(T));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) r[u].max_abs(key_a, key_b);
+        }
+        for (; v < nvec; v += kMQThreadsA) {
           Raw8<T> r;
           r.load_shared(base + v * 8 * sizeof(T));
           r.max_abs(key_a, key_b);
