@@ -171,10 +171,12 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
   if (rc != FP8_OK) return rc;
   args.err = d->err;
   args.wait_limit_ns = g_wait_limit_ns;
-  args.ksplit = fp8k::gemm_ksplit(mode, args.M, args.N, args.K, d->sms);
+  args.ksplit = fp8k::gemm_ksplit(mode, args.M, args.N, args.K, d->sms, true);
   args.ws = nullptr;
   args.counters = nullptr;
-  if (args.ksplit > 1) {
+  // split K reduces inside a thread-block cluster (no workspace)
+  args.cluster_split = args.ksplit > 1 ? 1 : 0;
+  if (args.ksplit > 1 && !args.cluster_split) {
     const size_t need = kCounterBytes + (size_t)args.ksplit * args.M * args.N * sizeof(float);
     void *w = nullptr;
     if ((rc = get_workspace(st, need, &w)) != FP8_OK) return rc;
@@ -190,7 +192,8 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
       return rc;
     return to_status(fp8k::launch_gemm_pair(tma, tmb, args, d->sms, st));
   }
-  if ((rc = encode_gemm_operand(&tmb, b, args.b_mn, args.K, args.N, fp8k::gemm_tile_n(mode))) !=
+  if ((rc = encode_gemm_operand(&tmb, b, args.b_mn, args.K, args.N,
+                                fp8k::gemm_tile_n(mode, args.M))) !=
       FP8_OK)
     return rc;
   return to_status(fp8k::launch_gemm(mode, tma, tmb, args, d->sms, st));
@@ -429,7 +432,7 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
   int64_t tiles = 0;
   for (int i = 0; i < count && together; ++i) {
     const fp8_gemm_problem_t &p = problems[i];
-    together = fp8k::gemm_ksplit(fp8k::kScaleTensor, p.M, p.N, p.K, d->sms) == 1;
+    together = fp8k::gemm_ksplit(fp8k::kScaleTensor, p.M, p.N, p.K, d->sms, true) == 1;
     tiles += ((p.M + 255) / 256) * ((p.N + 255) / 256);
   }
   together = together && tiles * 4 >= d->sms / 2;

@@ -85,6 +85,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const DevErr err{args.err, args.wait_limit_ns};
+  // split cluster: after the main loop the stage buffers hold this split's
+  // fp32 partial tile, [128][kPartStride] (see cluster_reduce)
+  float *part = reinterpret_cast<float *>(tiles);
+  static_assert((uint32_t)C::BM * kPartStride<BN> * 4 <= C::kTileBytes, "partial tile fits the stages");
 
   auto sA = [&](int s) { return smem_u32(tiles + s * (C::kABytes + C::kBBytes)); };
   auto sB = [&](int s) { return smem_u32(tiles + s * (C::kABytes + C::kBBytes) + C::kABytes); };
@@ -129,6 +133,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   // units are tiles.  Split s covers k blocks [s*KB/ks, (s+1)*KB/ks).
   const int ks = args.ksplit;
   const int64_t num_units = num_tiles * ks;
+  // the CTA's units: u_first, u_first + u_step, ...  In a split cluster the
+  // CTA owns exactly one unit: tile = cluster index, split = cluster rank.
+  const bool csplit = args.cluster_split != 0;
+  const int64_t u_first =
+      csplit ? (int64_t)cluster_ctarank() * num_tiles + blockIdx.x / ks : (int64_t)blockIdx.x;
+  const int64_t u_step = csplit ? num_units : (int64_t)gridDim.x;
   auto unit_tile = [&](int64_t u) { return u % num_tiles; };
   auto kb_begin = [&](int64_t u) { return (int)((u / num_tiles) * KB / ks); };
   auto kb_end = [&](int64_t u) { return (int)((u / num_tiles + 1) * KB / ks); };
@@ -137,16 +147,42 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     // ------------------------------------------------------------ producer
     uint32_t it = 0;  // stage iterations issued, across tiles
     bool ok = true;
-    // group-UE8M0 mode: the per-128 scale bytes of the NEXT stage are loaded
-    // into registers before waiting on the current stage, so their latency
-    // hides behind the wait instead of stalling every stage.
-    uint32_t sfa_cur[4] = {}, sfb_cur[BN / 32] = {}, sfa_nxt[4] = {}, sfb_nxt[BN / 32] = {};
-    auto load_sf = [&](int64_t t, int kb, uint32_t (&fa)[4], uint32_t (&fb)[BN / 32]) {
+    // group-UE8M0 mode: the per-128 scale bytes of a k block are loaded into
+    // registers kSfAhead k blocks before their stage is filled, so the
+    // producer never waits on a scale load (with a one-deep prefetch every
+    // stage paid a load latency, which dominated small-M GEMMs).  The queue
+    // is kSfAhead register slots used round-robin with compile-time indices
+    // (the stage loop below is unrolled over the slots), so no register ever
+    // moves while its load is still in flight.
+    constexpr int kSfAhead = MODE == kScaleGroupUe8m0 ? STAGES : 1;
+    uint32_t sfa_q[kSfAhead][4] = {}, sfb_q[kSfAhead][BN / 32] = {};
+    // A position in the CTA's flat k-block sequence, with the unit's tile
+    // origin and k range cached (64-bit divisions once per unit, not per k
+    // block: the producer issues every stage and must stay cheap).
+    struct Cursor {
+      int64_t u, m0, n0;
+      int kb, kb_end;
+    };
+    auto enter = [&](Cursor &c, int64_t u) {
+      c.u = u;
+      if (u < num_units) {
+        const int64_t t = unit_tile(u);
+        c.m0 = (t / tiles_n) * C::BM;
+        c.n0 = (t % tiles_n) * BN;
+        c.kb = kb_begin(u);
+        c.kb_end = kb_end(u);
+      }
+    };
+    auto next_kb = [&](Cursor &c) {
+      if (++c.kb >= c.kb_end) enter(c, c.u + u_step);
+    };
+    auto load_sf = [&](const Cursor &cs, uint32_t (&fa)[4], uint32_t (&fb)[BN / 32]) {
       if constexpr (MODE == kScaleGroupUe8m0) {
         const uint8_t *sa8 = static_cast<const uint8_t *>(args.sa);
         const uint8_t *sb8 = static_cast<const uint8_t *>(args.sb);
         const int64_t G = args.K / 128;
-        const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
+        const int64_t m0 = cs.m0, n0 = cs.n0;
+        const int kb = cs.kb;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int64_t m = m0 + 32 * c + lane;
@@ -159,78 +195,85 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
         }
       }
     };
+    // the CTA's k blocks as one flat sequence: `cur` is the one the next
+    // stage takes, `look` the one whose scales are loaded next
+    Cursor cur, look;
+    enter(cur, u_first);
+    enter(look, u_first);
+    auto push_sf = [&](uint32_t (&fa)[4], uint32_t (&fb)[BN / 32]) {
+      if (look.u < num_units) {
+        load_sf(look, fa, fb);
+        next_kb(look);
+      }
+    };
     if constexpr (MODE == kScaleGroupUe8m0) {
-      if ((int64_t)blockIdx.x < num_units)
-        load_sf(unit_tile(blockIdx.x), kb_begin(blockIdx.x), sfa_cur, sfb_cur);
+#pragma unroll
+      for (int d = 0; d < kSfAhead; ++d) push_sf(sfa_q[d], sfb_q[d]);
     }
-    for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const int64_t t = unit_tile(u);
-      const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
-      const int kb1 = kb_end(u);
-      for (int kb = kb_begin(u); kb < kb1; ++kb) {
-        const int s = (int)(it % STAGES);
-        const uint32_t round = it / STAGES;
-        if constexpr (MODE == kScaleGroupUe8m0) {
-          const int64_t un = kb + 1 < kb1 ? u : u + gridDim.x;
-          if (un < num_units)
-            load_sf(unit_tile(un), kb + 1 < kb1 ? kb + 1 : kb_begin(un), sfa_nxt, sfb_nxt);
-        }
-        if (!mbar_wait_warp(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) {
-          ok = false;
-          break;
-        }
-        uint32_t tx = C::kABytes + C::kBBytes;
-        if constexpr (MODE == kScaleGroupUe8m0) {
-          // byte -> word with the byte in all four 1x32 slots; the word for
-          // row 32c + l of a 128-row chunk sits at index 4l + c
-          uint32_t *wa = reinterpret_cast<uint32_t *>(sSfa(s));
-          uint32_t *wb = reinterpret_cast<uint32_t *>(sSfb(s));
+    // one k block (cu, ckb) into stage it % STAGES; false when a wait gave up
+    auto stage = [&](uint32_t (&fa)[4], uint32_t (&fb)[BN / 32]) -> bool {
+      const int64_t m0 = cur.m0, n0 = cur.n0;
+      const int kb = cur.kb;
+      const int s = (int)(it % STAGES);
+      const uint32_t round = it / STAGES;
+      if (!mbar_wait_warp(empty_bar(s), (round & 1u) ^ 1u, abort_flag, err, 1)) return false;
+      uint32_t tx = C::kABytes + C::kBBytes;
+      if constexpr (MODE == kScaleGroupUe8m0) {
+        // byte -> word with the byte in all four 1x32 slots; the word for
+        // row 32c + l of a 128-row chunk sits at index 4l + c
+        uint32_t *wa = reinterpret_cast<uint32_t *>(sSfa(s));
+        uint32_t *wb = reinterpret_cast<uint32_t *>(sSfb(s));
 #pragma unroll
-          for (int c = 0; c < 4; ++c) wa[4 * lane + c] = sfa_cur[c] * 0x01010101u;
+        for (int c = 0; c < 4; ++c) wa[4 * lane + c] = fa[c] * 0x01010101u;
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c)
-            wb[(c >> 2) * 128 + 4 * lane + (c & 3)] = sfb_cur[c] * 0x01010101u;
-          fence_proxy_async_smem();
-          __syncwarp();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) sfa_cur[c] = sfa_nxt[c];
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c) sfb_cur[c] = sfb_nxt[c];
-        }
-        if (elect_one()) {
-          uint32_t sfb_bytes = 0;
-          if constexpr (MODE == kScaleMx) {
-            const int64_t npad = (args.N + 127) / 128 * 128;
-            const int64_t rows = (npad - n0) < BN ? (npad - n0) : BN;
-            sfb_bytes = (uint32_t)rows * 4u;
-            tx += C::kSfaBytes + sfb_bytes;
-          }
-          mbar_arrive_expect_tx(full_bar(s), tx);
-          // tensor-map coordinates are (contiguous dim, row); an MN-major
-          // operand is loaded as 128-wide boxes along M or N, 16 KB apart
-          const int32_t k0 = kb * C::BK;
-          if (args.a_mn)
-            tma_load_2d(sA(s), &tma, full_bar(s), (int32_t)m0, k0);
-          else
-            tma_load_2d(sA(s), &tma, full_bar(s), k0, (int32_t)m0);
-          if (args.b_mn) {
-#pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
-              tma_load_2d(sB(s) + h * 128 * C::BK, &tmb, full_bar(s), (int32_t)n0 + 128 * h, k0);
-          } else {
-            tma_load_2d(sB(s), &tmb, full_bar(s), k0, (int32_t)n0);
-          }
-          if constexpr (MODE == kScaleMx) {
-            const int64_t mpad = (args.M + 127) / 128 * 128;
-            const int64_t npad = (args.N + 127) / 128 * 128;
-            const uint32_t *la = static_cast<const uint32_t *>(args.sa) + (int64_t)kb * mpad + m0;
-            const uint32_t *lb = static_cast<const uint32_t *>(args.sb) + (int64_t)kb * npad + n0;
-            bulk_load(smem_u32(sSfa(s)), la, C::kSfaBytes, full_bar(s));
-            bulk_load(smem_u32(sSfb(s)), lb, sfb_bytes, full_bar(s));
-          }
-        }
+        for (int c = 0; c < BN / 32; ++c)
+          wb[(c >> 2) * 128 + 4 * lane + (c & 3)] = fb[c] * 0x01010101u;
+        fence_proxy_async_smem();
         __syncwarp();
-        ++it;
+        push_sf(fa, fb);  // this slot now waits for the k block kSfAhead ahead
+      }
+      if (elect_one()) {
+        uint32_t sfb_bytes = 0;
+        if constexpr (MODE == kScaleMx) {
+          const int64_t npad = (args.N + 127) / 128 * 128;
+          const int64_t rows = (npad - n0) < BN ? (npad - n0) : BN;
+          sfb_bytes = (uint32_t)rows * 4u;
+          tx += C::kSfaBytes + sfb_bytes;
+        }
+        mbar_arrive_expect_tx(full_bar(s), tx);
+        // tensor-map coordinates are (contiguous dim, row); an MN-major
+        // operand is loaded as 128-wide boxes along M or N, 16 KB apart
+        const int32_t k0 = kb * C::BK;
+        if (args.a_mn)
+          tma_load_2d(sA(s), &tma, full_bar(s), (int32_t)m0, k0);
+        else
+          tma_load_2d(sA(s), &tma, full_bar(s), k0, (int32_t)m0);
+        if (args.b_mn) {
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            tma_load_2d(sB(s) + h * 128 * C::BK, &tmb, full_bar(s), (int32_t)n0 + 128 * h, k0);
+        } else {
+          tma_load_2d(sB(s), &tmb, full_bar(s), k0, (int32_t)n0);
+        }
+        if constexpr (MODE == kScaleMx) {
+          const int64_t mpad = (args.M + 127) / 128 * 128;
+          const int64_t npad = (args.N + 127) / 128 * 128;
+          const uint32_t *la = static_cast<const uint32_t *>(args.sa) + (int64_t)kb * mpad + m0;
+          const uint32_t *lb = static_cast<const uint32_t *>(args.sb) + (int64_t)kb * npad + n0;
+          bulk_load(smem_u32(sSfa(s)), la, C::kSfaBytes, full_bar(s));
+          bulk_load(smem_u32(sSfb(s)), lb, sfb_bytes, full_bar(s));
+        }
+      }
+      __syncwarp();
+      ++it;
+      next_kb(cur);
+      return true;
+    };
+    while (cur.u < num_units && ok) {
+#pragma unroll
+      for (int j = 0; j < kSfAhead; ++j) {
+        if (cur.u >= num_units || !ok) break;
+        ok = stage(sfa_q[j], sfb_q[j]);
       }
     }
     if (!ok && lane == 0) {
@@ -243,7 +286,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     if (elect_one()) {
       uint32_t it = 0, j = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++j) {
+      for (int64_t u = u_first; u < num_units && ok; u += u_step, ++j) {
         uint32_t d = tmem;
         const int kb0 = kb_begin(u), kb1 = kb_end(u);
         uint32_t tile_buf = 0;
@@ -338,7 +381,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
         alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
       if constexpr (MODE == kScaleMx) alpha = *args.ga * *args.gb;
       uint32_t j = 0;
-      for (int64_t u = blockIdx.x; u < num_units; u += gridDim.x, ++j) {
+      for (int64_t u = u_first; u < num_units; u += u_step, ++j) {
         const int64_t t = unit_tile(u);
         const int split = (int)(u / num_tiles);
         const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
@@ -368,19 +411,15 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-            store_partial32(args, split, row, n0 + c, v);
+            if (csplit)
+              stash_partial32_bn<BN>(part, 32 * q + lane, c, v);
+            else
+              store_partial32(args, split, row, n0 + c, v);
           }
         }
-        if (ks > 1 && finish_split(t)) {
-#pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
-            float v[32];
-            sum_partials32(args, row, n0 + c, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            store_row32(args, row, n0 + c, v);
-          }
-        }
+        if (ks > 1 && !csplit && finish_split(t))
+          reduce_split_tile(args, m0, n0, C::BM, BN, alpha, (int)threadIdx.x - 64,
+                            C::kEpiWarps * 32);
       }
     } else {
       const int h = (int)(warp - 2) >> 2;  // column half of the 128-wide tile
@@ -389,7 +428,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       const int64_t G = args.K / 128;
       uint32_t it = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      for (int64_t u = u_first; u < num_units && ok; u += u_step) {
         const int64_t t = unit_tile(u);
         const int split = (int)(u / num_tiles);
         const int kb0 = kb_begin(u), kb1 = kb_end(u);
@@ -430,21 +469,36 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = acc[i];
         if (ks == 1) store_row32(args, row, n0 + h * 64, v);
+        else if (csplit) stash_partial32_bn<BN>(part, 32 * q + lane, h * 64, v);
         else store_partial32(args, split, row, n0 + h * 64, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = acc[32 + i];
         if (ks == 1) store_row32(args, row, n0 + h * 64 + 32, v);
+        else if (csplit) stash_partial32_bn<BN>(part, 32 * q + lane, h * 64 + 32, v);
         else store_partial32(args, split, row, n0 + h * 64 + 32, v);
-        if (ks > 1 && finish_split(t)) {
-          sum_partials32(args, row, n0 + h * 64, v);
-          store_row32(args, row, n0 + h * 64, v);
-          sum_partials32(args, row, n0 + h * 64 + 32, v);
-          store_row32(args, row, n0 + h * 64 + 32, v);
-        }
+        if (ks > 1 && !csplit && finish_split(t))
+          reduce_split_tile(args, m0, n0, C::BM, BN, 1.0f, (int)threadIdx.x - 64,
+                            C::kEpiWarps * 32);
       }
     }
   }
 
+  if (csplit) {
+    // every split's partial tile is in its CTA's shared memory: each CTA sums
+    // a slice of the tile's rows over the cluster, in split order
+    cluster_sync();
+    if (warp >= 2) {
+      const int64_t t = unit_tile(u_first);
+      const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
+      float alpha = 1.0f;
+      if constexpr (MODE == kScaleTensor)
+        alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
+      if constexpr (MODE == kScaleMx) alpha = *args.ga * *args.gb;
+      cluster_reduce<BN>(args, part, m0, n0, C::BM, alpha, cluster_ctarank(), ks,
+                         (int)threadIdx.x - 64, C::kEpiWarps * 32);
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its partial
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
@@ -467,27 +521,105 @@ static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const Gem
     attr_done[dev] = true;
   }
   const int64_t units = ((args.M + C::BM - 1) / C::BM) * ((args.N + BN - 1) / BN) * args.ksplit;
+  if (args.cluster_split) {
+    // one CTA per unit; the splits of a tile are one cluster
+    if (args.ksplit < 2 || args.ksplit > kMaxClusterSplit) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)units);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)args.ksplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tma, tmb, args);
+  }
   const int grid = (int)(units < sms ? units : sms);
   kern<<<grid, C::kThreads, C::kSmem, st>>>(tma, tmb, args);
   return cudaGetLastError();
 }
 
-int gemm_tile_n(int mode) { return mode == kScaleGroupF32 ? 128 : 256; }
+// Tile width: 128 for the FP32-promotion mode, and for the UE8M0 mode at
+// small M (twice the tiles, so the split GEMM fills the SMs); 256 otherwise.
+int gemm_tile_n(int mode, int64_t M) {
+  if (mode == kScaleGroupF32) return 128;
+  if (mode == kScaleGroupUe8m0 && M <= 256) return 128;
+  return 256;
+}
 
 // Split K when the tiles cannot fill half the SMs: as many splits as fit the
-// SMs, each covering at least four 128-wide K blocks, and no more than the
-// last CTA of a tile can sum quickly (512 KB of fp32 partials per tile: the
-// reduction runs at one SM's L2 bandwidth).
-int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms) {
-  const int64_t bn = gemm_tile_n(mode);
+// SMs, each covering at least four 128-wide K blocks.  Cluster splits reduce
+// through distributed shared memory (at most kMaxClusterSplit per tile);
+// workspace splits are capped at 512 KB of fp32 partials per tile, which the
+// last CTA of the tile sums.
+// Clusters of `size` CTAs of the kernel that `mode` runs at M rows that can
+// be resident at once (cached per device, mode, tile width and size).
+template <int MODE, int BN, int STAGES>
+static int active_clusters(int size) {
+  using C = Cfg<MODE, BN, STAGES>;
+  auto kern = gemm_kernel<MODE, BN, STAGES>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)size;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)size);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  int n = 0;
+  return cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess ? n : 0;
+}
+
+static int max_active_clusters(int mode, int64_t M, int size) {
+  static int cache[64][4][2][kMaxClusterSplit + 1];
+  static bool have[64][4][2][kMaxClusterSplit + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int w = gemm_tile_n(mode, M) == 128 ? 0 : 1;
+  if (!have[dev][mode][w][size]) {
+    int n = 0;
+    switch (mode) {
+      case kScaleTensor: n = active_clusters<kScaleTensor, 256, 4>(size); break;
+      case kScaleMx: n = active_clusters<kScaleMx, 256, 4>(size); break;
+      case kScaleGroupUe8m0:
+        n = w == 0 ? active_clusters<kScaleGroupUe8m0, 128, 6>(size)
+                   : active_clusters<kScaleGroupUe8m0, 256, 4>(size);
+        break;
+      default: n = active_clusters<kScaleGroupF32, 128, 6>(size); break;
+    }
+    cache[dev][mode][w][size] = n;
+    have[dev][mode][w][size] = true;
+  }
+  return cache[dev][mode][w][size];
+}
+
+int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster) {
+  const int64_t bn = gemm_tile_n(mode, M);
   const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
   const int64_t kb = (K + 127) / 128;
   if (tiles * 2 > sms || kb < 8) return 1;
   int64_t ks = sms / tiles;
   if (ks > kb / 4) ks = kb / 4;
-  const int64_t rows = M < 128 ? M : 128;
-  const int64_t by_partials = (512 * 1024) / (rows * bn * 4);
-  if (ks > by_partials) ks = by_partials;
+  if (cluster) {
+    // the largest split whose clusters (one per tile) are all resident at
+    // once: a second wave of clusters would double the time
+    if (ks > kMaxClusterSplit) ks = kMaxClusterSplit;
+    while (ks > 1 && max_active_clusters(mode, M, (int)ks) < tiles) --ks;
+  } else {
+    const int64_t rows = M < 128 ? M : 128;
+    const int64_t by_partials = (512 * 1024) / (rows * bn * 4);
+    if (ks > by_partials) ks = by_partials;
+  }
   return ks < 2 ? 1 : (int)ks;
 }
 
@@ -496,7 +628,10 @@ cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb
   switch (mode) {
     case kScaleTensor: return run<kScaleTensor, 256, 4>(tma, tmb, args, sms, st);
     case kScaleMx: return run<kScaleMx, 256, 4>(tma, tmb, args, sms, st);
-    case kScaleGroupUe8m0: return run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, sms, st);
+    case kScaleGroupUe8m0:
+      if (gemm_tile_n(mode, args.M) == 128)
+        return run<kScaleGroupUe8m0, 128, 6>(tma, tmb, args, sms, st);
+      return run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, sms, st);
     case kScaleGroupF32: return run<kScaleGroupF32, 128, 6>(tma, tmb, args, sms, st);
     default: return cudaErrorInvalidValue;
   }

@@ -60,24 +60,147 @@ __device__ __forceinline__ void store_partial32(const GemmArgs &a, int split, in
   }
 }
 
-// Sum over the splits, in split order, of 32 partials of one row.
-__device__ __forceinline__ void sum_partials32(const GemmArgs &a, int64_t row, int64_t col0,
-                                               float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-  if (row >= a.M || col0 >= a.N) return;
-  const bool vec = col0 + 32 <= a.N && (a.N & 3) == 0;
-  for (int sp = 0; sp < a.ksplit; ++sp) {
-    const float *src = a.ws + ((int64_t)sp * a.M + row) * a.N + col0;
+// Store up to four consecutive results of one output row (already scaled).
+__device__ __forceinline__ void store4(const GemmArgs &a, int64_t row, int64_t col, int n,
+                                       const float (&v)[4]) {
+  if (a.out_dt == 1) {
+    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.c) + row * a.ldc + col;
+    if (n == 4 && a.vec_store) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]), hi = __floats2bfloat162_rn(v[2], v[3]);
+      *reinterpret_cast<uint2 *>(dst) =
+          make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+    } else {
+      for (int i = 0; i < n; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+    }
+  } else {
+    float *dst = static_cast<float *>(a.c) + row * a.ldc + col;
+    if (n == 4 && a.vec_store) {
+      float4 o = make_float4(v[0], v[1], v[2], v[3]);
+      if (a.accumulate) {
+        const float4 p = *reinterpret_cast<const float4 *>(dst);
+        o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
+      }
+      *reinterpret_cast<float4 *>(dst) = o;
+    } else {
+      for (int i = 0; i < n; ++i) dst[i] = a.accumulate ? dst[i] + v[i] : v[i];
+    }
+  }
+}
+
+// Split K, in the CTA that arrived last for a tile: out = alpha * (sum over
+// the splits, in split order, of the fp32 partials), for the whole
+// tile_rows x tile_cols tile at (m0, n0).  The work is spread over all `nthr`
+// epilogue threads in groups of four columns, and the partial loads of eight
+// splits at a time are issued before they are added, so the reduction is
+// bandwidth-bound rather than a chain of load latencies.
+__device__ __forceinline__ void reduce_split_tile(const GemmArgs &a, int64_t m0, int64_t n0,
+                                                  int64_t tile_rows, int64_t tile_cols,
+                                                  float alpha, int tid, int nthr) {
+  const int64_t rows = a.M - m0 < tile_rows ? a.M - m0 : tile_rows;
+  const int64_t cols = a.N - n0 < tile_cols ? a.N - n0 : tile_cols;
+  if (rows <= 0 || cols <= 0) return;
+  const int64_t cg = (cols + 3) / 4;
+  const bool vec = (a.N & 3) == 0;
+  const int64_t plane = a.M * a.N;  // elements of one split's partials
+  for (int64_t gi = tid; gi < rows * cg; gi += nthr) {
+    const int64_t row = m0 + gi / cg, col = n0 + (gi % cg) * 4;
+    const int n = a.N - col < 4 ? (int)(a.N - col) : 4;
+    const float *src = a.ws + row * a.N + col;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (vec) {
-      const float4 *s4 = reinterpret_cast<const float4 *>(src);
+      int sp = 0;
+      for (; sp + 8 <= a.ksplit; sp += 8) {
+        float4 p[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 p = __ldcg(s4 + i);
-        v[4 * i] += p.x; v[4 * i + 1] += p.y; v[4 * i + 2] += p.z; v[4 * i + 3] += p.w;
+        for (int u = 0; u < 8; ++u) p[u] = __ldcg(reinterpret_cast<const float4 *>(src + (sp + u) * plane));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          acc[0] += p[u].x; acc[1] += p[u].y; acc[2] += p[u].z; acc[3] += p[u].w;
+        }
+      }
+      for (; sp < a.ksplit; ++sp) {
+        const float4 p = __ldcg(reinterpret_cast<const float4 *>(src + sp * plane));
+        acc[0] += p.x; acc[1] += p.y; acc[2] += p.z; acc[3] += p.w;
       }
     } else {
-      for (int i = 0; i < 32 && col0 + i < a.N; ++i) v[i] += __ldcg(src + i);
+      for (int sp = 0; sp < a.ksplit; ++sp)
+        for (int i = 0; i < n; ++i) acc[i] += __ldcg(src + sp * plane + i);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] *= alpha;
+    store4(a, row, col, n, acc);
+  }
+}
+
+// ----------------------------------------------------- split clusters --
+// Row pitch (floats) of the fp32 partial tile kept in shared memory: four
+// words of padding spread a warp's 32 rows over the banks.
+template <int BN>
+constexpr uint32_t kPartStride = BN + 4;
+
+// 32 partials of local row `r`, columns [c, c + 32), into the partial tile.
+template <int BN>
+__device__ __forceinline__ void stash_partial32_bn(float *part, int r, int c, const float (&v)[32]) {
+  float4 *dst = reinterpret_cast<float4 *>(part + (uint32_t)r * kPartStride<BN> + c);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// The reduction of a split cluster: CTA `rank` of the `ks` CTAs sums rows
+// [rank * R / ks, (rank + 1) * R / ks) of the tile (R its valid rows) over
+// every CTA's partial tile, in split order (the same order, hence the same
+// sums, as the global-workspace reduction), scales by alpha and stores.
+template <int BN>
+__device__ __forceinline__ void cluster_reduce(const GemmArgs &a, const float *part, int64_t m0,
+                                               int64_t n0, int64_t tile_rows, float alpha,
+                                               uint32_t rank, int ks, int tid, int nthr) {
+  const int64_t rows = a.M - m0 < tile_rows ? a.M - m0 : tile_rows;
+  const int64_t cols = a.N - n0 < BN ? a.N - n0 : BN;
+  if (rows <= 0 || cols <= 0) return;
+  const int64_t r0 = (int64_t)rank * rows / ks, r1 = ((int64_t)rank + 1) * rows / ks;
+  const int64_t cg = (cols + 3) / 4;
+  const uint32_t base = smem_u32(part);
+  const int64_t groups = (r1 - r0) * cg;
+  // two groups per step: up to 2 * ks remote loads in flight per thread
+  for (int64_t g0 = tid; g0 < groups; g0 += 2 * (int64_t)nthr) {
+    float4 p[2][kMaxClusterSplit];
+    uint32_t off[2];
+    bool live[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t gi = g0 + h * (int64_t)nthr;
+      live[h] = gi < groups;
+      const int64_t r = r0 + (live[h] ? gi / cg : 0), c = live[h] ? (gi % cg) * 4 : 0;
+      off[h] = base + (uint32_t)((r * kPartStride<BN> + c) * 4);
+#pragma unroll
+      for (int sp = 0; sp < kMaxClusterSplit; ++sp)
+        if (live[h] && sp < ks) p[h][sp] = ld_shared_cluster_f4(mapa_shared(off[h], (uint32_t)sp));
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (!live[h]) continue;
+      const int64_t gi = g0 + h * (int64_t)nthr;
+      const int64_t r = r0 + gi / cg, c = (gi % cg) * 4;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int sp = 0; sp < kMaxClusterSplit; ++sp) {
+        if (sp < ks) {
+          acc[0] += p[h][sp].x; acc[1] += p[h][sp].y; acc[2] += p[h][sp].z; acc[3] += p[h][sp].w;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] *= alpha;
+      const int n = a.N - (n0 + c) < 4 ? (int)(a.N - (n0 + c)) : 4;
+      store4(a, m0 + r, n0 + c, n, acc);
     }
   }
 }

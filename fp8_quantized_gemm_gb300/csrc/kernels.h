@@ -73,16 +73,23 @@ struct GemmArgs {
   int ksplit;
   float *ws;
   uint32_t *counters;
+  // cluster_split: the ksplit CTAs of a tile form one thread-block cluster
+  // (cluster rank = split) and reduce their partials through distributed
+  // shared memory; ws and counters are then unused
+  int cluster_split;
 };
 
 // Wait bound the API passes to kernels (fp8_set_option FP8_OPT_WAIT_LIMIT_NS).
 uint64_t wait_limit_ns();
 
-// Split count the launcher would use for this shape (1 = no split).
-int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms);
+// Split count the launcher would use for this shape (1 = no split);
+// `cluster`: the splits reduce through a cluster (at most kMaxClusterSplit,
+// no partials in global memory) rather than through a global workspace.
+constexpr int kMaxClusterSplit = 8;
+int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster);
 
-// Output-tile width (N) of each mode; the B tensor map's box uses it.
-int gemm_tile_n(int mode);
+// Output-tile width (N) of a mode at M rows; the B tensor map's box uses it.
+int gemm_tile_n(int mode, int64_t M);
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,
                         const GemmArgs &args, int sms, cudaStream_t st);

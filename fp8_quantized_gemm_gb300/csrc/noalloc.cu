@@ -73,14 +73,17 @@ extern "C" int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const ui
   if ((rc = scratch_for_current_device(&scratch)) != FP8_OK) return rc;
 
   const int mode = sfmt == FP8_SCALE_F32 ? fp8k::kScaleGroupF32 : fp8k::kScaleGroupUe8m0;
-  const int bn = fp8k::gemm_tile_n(mode);
+  const int bn = fp8k::gemm_tile_n(mode, M);
   fp8k::GemmArgs args{};
   args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
   args.out_dt = FP8_OUT_BF16; args.ldc = ldc; args.c = c; args.sa = sa; args.sb = sb;
   args.err = err;
   args.wait_limit_ns = fp8k::wait_limit_ns();
   args.vec_store = (aligned16(c) && (ldc * 2) % 16 == 0) ? 1 : 0;
-  args.ksplit = fp8k::gemm_ksplit(mode, M, N, K, sms);
+  // split K through the fixed scratch (partials in global memory), not a
+  // cluster: this entry point keeps the workspace form of the reduction
+  args.ksplit = fp8k::gemm_ksplit(mode, M, N, K, sms, false);
+  args.cluster_split = 0;
   const cudaStream_t st = (cudaStream_t)stream;
   if (args.ksplit > 1) {
     const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);

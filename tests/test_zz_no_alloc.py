@@ -53,8 +53,9 @@ def test_noalloc_matches_regular_entry_point(m, n, k, sfmt):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    """M 128, N 6144, K 7168 with UE8M0 scales splits K four ways: 12.6 MB of
-    partials, more than the 8 MiB the fixed scratch holds."""
+    """M 128, N 6144, K 7168 with UE8M0 scales (128-wide tiles at this M)
+    splits K three ways: 9.4 MB of partials, more than the 8 MiB the fixed
+    scratch holds."""
     F = lib()
     m, n, k = 128, 6144, 7168
     qa = torch.zeros((m, k), dtype=torch.uint8, device="cuda")
