@@ -26,10 +26,18 @@ Alongside C the oracle returns the error budget of each element,
 is accepted when ``|gpu - C| <= 1e-3 * E`` (plus one output ulp of |C| for a
 bf16 output).
 
+Mixture-of-experts grouping (Transformers fine-grained FP8, 六 6.4:
+FP8Experts): token rows [offsets[e], offsets[e+1]) use expert e's weights,
+so the product is the plain one per expert, ``C[rows_e] = A[rows_e] B_e^T``
+(``gemm_experts``).
+
 Pins (``tests/test_oracle_gemm.py``): exact rational brute force on tiny
 shapes (products of two 8-bit floats and their short sums are exact), the
 scale = 1 case against an integer matmul on the code grid, and a transposed
-operand / dropped scale / sign flip each failing the check.
+operand / dropped scale / sign flip each failing the check.  Expert
+grouping: exact rational brute force on two tiny experts, one expert equal
+to the plain product, invariance under reordering the experts with their
+rows, empty experts, and swapped expert weights failing the check.
 """
 from __future__ import annotations
 
@@ -48,6 +56,20 @@ def gemm(a_deq, b_deq):
     a = np.asarray(a_deq, dtype=np.float64)
     b = np.asarray(b_deq, dtype=np.float64)
     return a @ b.T, np.abs(a) @ np.abs(b).T
+
+
+def gemm_experts(a_deq, b_deq_list, offsets):
+    """C and E for expert-grouped rows: rows [offsets[e], offsets[e+1]) of
+    A [M, K] times expert e's B_e [N, K] (``b_deq_list[e]``), float64."""
+    a = np.asarray(a_deq, dtype=np.float64)
+    n = np.asarray(b_deq_list[0]).shape[0]
+    c = np.zeros((a.shape[0], n))
+    e_ = np.zeros((a.shape[0], n))
+    for e, b in enumerate(b_deq_list):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            c[r0:r1], e_[r0:r1] = gemm(a[r0:r1], b)
+    return c, e_
 
 
 def gemm_sampled(a_deq, b_deq, rows, cols):

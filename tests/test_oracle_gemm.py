@@ -127,3 +127,64 @@ def test_bf16_ulp():
     v = torch.tensor([1.0, 3.0, 1000.0], dtype=torch.bfloat16)
     nxt = torch.nextafter(v, torch.tensor(float("inf"), dtype=torch.bfloat16))
     assert np.array_equal((nxt - v).double().numpy(), G.bf16_ulp(v.double().numpy()))
+
+
+# ------------------------------------------------------- expert grouping --
+
+def _expert_case(rng, offsets, n=6, k=5):
+    m = offsets[-1]
+    qa = finite_codes(rng, (m, k), "e4m3")
+    qbs = [finite_codes(rng, (n, k), "e4m3") for _ in range(len(offsets) - 1)]
+    a = torch_decode(qa, "e4m3") * 0.5
+    bs = [torch_decode(q, "e4m3") * (2.0 ** -e) for e, q in enumerate(qbs)]
+    return a, bs
+
+
+def test_experts_exact_rational_brute_force():
+    """Two tiny experts (3 and 2 rows) against a sum of exact rationals,
+    written out row by row with each row's own expert."""
+    rng = np.random.default_rng(21)
+    offsets = [0, 3, 5]
+    a, bs = _expert_case(rng, offsets)
+    c, e = G.gemm_experts(a, bs, offsets)
+    for ex in range(2):
+        for m in range(offsets[ex], offsets[ex + 1]):
+            for n in range(bs[ex].shape[0]):
+                ref = sum(Fraction(float(a[m, kk])) * Fraction(float(bs[ex][n, kk]))
+                          for kk in range(a.shape[1]))
+                assert Fraction(float(c[m, n])) == ref
+                assert e[m, n] == sum(abs(float(a[m, kk]) * float(bs[ex][n, kk]))
+                                      for kk in range(a.shape[1]))
+
+
+def test_one_expert_is_the_plain_product_and_empty_experts_add_nothing():
+    rng = np.random.default_rng(22)
+    a, bs = _expert_case(rng, [0, 7])
+    c1, e1 = G.gemm_experts(a, bs, [0, 7])
+    c0, e0 = G.gemm(a, bs[0])
+    assert np.array_equal(c1, c0) and np.array_equal(e1, e0)
+    # the same rows with empty experts before, between and after
+    filler = [np.full_like(bs[0], 3.0)] * 3
+    c2, _ = G.gemm_experts(a, [filler[0], bs[0], filler[1], filler[2]], [0, 0, 7, 7, 7])
+    assert np.array_equal(c2, c0)
+
+
+def test_experts_reordered_with_their_rows_permute_the_output():
+    rng = np.random.default_rng(23)
+    offsets = [0, 2, 6, 9]
+    a, bs = _expert_case(rng, offsets)
+    c, _ = G.gemm_experts(a, bs, offsets)
+    order = [2, 0, 1]
+    rows = np.concatenate([np.arange(offsets[i], offsets[i + 1]) for i in order])
+    new_off = np.concatenate([[0], np.cumsum([offsets[i + 1] - offsets[i] for i in order])])
+    c2, _ = G.gemm_experts(a[rows], [bs[i] for i in order], new_off)
+    assert np.array_equal(c2, c[rows])
+
+
+def test_swapped_expert_weights_fail_the_check():
+    rng = np.random.default_rng(24)
+    offsets = [0, 4, 8]
+    a, bs = _expert_case(rng, offsets, n=16, k=32)
+    c, e = G.gemm_experts(a, bs, offsets)
+    wrong, _ = G.gemm_experts(a, bs[::-1], offsets)
+    assert not G.check(wrong, c, e, "f32")[0]
