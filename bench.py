@@ -698,6 +698,54 @@ class GroupGemm:
                 "ms": {kk: round(v, 4) for kk, v in per.items()}}
 
 
+class MoeExperts:
+    """Mixture-of-experts layer, 8 experts, 4096 routed tokens (uneven
+    counts), N 2048, K 7168: token-group quantization of the activations
+    (timed), expert weights in 128x128 blocks (offline), one expert-grouped
+    GEMM launch over all experts."""
+
+    def __init__(self, dev, sfmt_name, experts=8, tokens=4096, k=7168, n=2048):
+        import fp8_quantized_gemm_gb300 as F
+        self.name = "moe_experts_%s_e%d_t%d" % (sfmt_name, experts, tokens)
+        self.e, self.t, self.k, self.n = experts, tokens, k, n
+        sfmt = F.SCALE_F32 if sfmt_name == "f32" else F.SCALE_UE8M0
+        sdt = torch.float32 if sfmt == F.SCALE_F32 else torch.uint8
+        act, w, counts = workloads.moe_experts(experts, tokens, n, k)
+        self.counts = counts.tolist()
+        offsets = torch.cat([torch.zeros(1, dtype=torch.int64), counts.cumsum(0)]).to(torch.int32)
+        self.offsets = offsets.to(dev)
+        wd = w.to(dev)
+        self.wq = torch.empty((experts, n, k), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty((experts, (n + 127) // 128, k // 128), dtype=sdt, device=dev)
+        for e in range(experts):  # offline weight quantization
+            F.fp8_quantize_block(wd[e], F.E4M3, sfmt, self.wq[e], self.ws[e])
+        del wd
+        self.ad = act.to(dev)
+        self.aq = torch.empty((tokens, k), dtype=torch.uint8, device=dev)
+        self.asc = torch.empty((k // 128, tokens), dtype=sdt, device=dev)
+        self.y = torch.empty((tokens, n), dtype=torch.bfloat16, device=dev)
+        self.sfmt, self.F = sfmt, F
+
+    def launches(self):
+        F = self.F
+        return [("quantize", lambda: F.fp8_quantize_token_group(self.ad, F.E4M3, self.sfmt, self.aq,
+                                                                self.asc)),
+                ("gemm", lambda: F.fp8_gemm_group_experts(self.aq, self.asc, self.wq, self.ws,
+                                                          self.sfmt, self.offsets, self.y))]
+
+    def report(self, per, step, fp8_peak, hbm):
+        t, k, n, e = self.t, self.k, self.n, self.e
+        flops = 2.0 * t * n * k
+        gb = e * n * k + t * k + t * n * 2 + self.ws.numel() * self.ws.element_size() + \
+            self.asc.numel() * self.asc.element_size()
+        return {"tflops_incl_quantize": round(flops / (step / 1e3) / 1e12, 2),
+                "gemm_tflops": round(flops / (per["gemm"] / 1e3) / 1e12, 2),
+                "gemm_frac_fp8_peak": round(flops / (per["gemm"] / 1e3) / 1e12 / fp8_peak, 4),
+                "gemm_gbs": round(gb / (per["gemm"] / 1e3) / 1e9, 1),
+                "tokens_per_expert": self.counts,
+                "ms": {kk: round(v, 4) for kk, v in per.items()}}
+
+
 class TwoLevel:
     """MOSS two-level microscaling GEMM, M = N = K = 8192: amax and two-level
     quantization of both operands, then the block-scaled GEMM."""
@@ -769,6 +817,8 @@ def extra_workloads(dev):
         for m in (1, 128, 4096):
             yield GroupGemm(dev, m, sname)
     yield TwoLevel(dev)
+    for sname in ("ue8m0", "f32"):
+        yield MoeExperts(dev, sname)
 
 
 def run_swiglu_row(dev, stream, fp8_peak, flush, weight_scaling="delayed"):
@@ -854,6 +904,7 @@ PROFILE_WORKLOADS = {
     "two_level_8192": lambda dev: TwoLevel(dev),
     **{"group_%s_m%d" % (s_, m): (lambda dev, s_=s_, m=m: GroupGemm(dev, m, s_))
        for s_ in ("f32", "ue8m0") for m in (1, 128, 4096)},
+    **{"moe_%s" % s_: (lambda dev, s_=s_: MoeExperts(dev, s_)) for s_ in ("f32", "ue8m0")},
 }
 
 

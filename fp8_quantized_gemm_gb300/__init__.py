@@ -47,6 +47,7 @@ _SIGS = {
     "fp8_gemm_group": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_gemm_tensor_grouped": [_vp, _int, _vp],
     "fp8_quantize_tensors": [_vp, _int, _vp, _vp],
+    "fp8_gemm_group_experts": [_vp, _vp, _vp, _vp, _int, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_gemm_mx": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp],
     "fp8_gemm_group_noalloc": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_delayed_state_update": [_vp, _vp, _vp, _i64, _int, _vp],
@@ -217,6 +218,16 @@ def fp8_gemm_group(a, sa, b, sb, sfmt, out, stream=None):
     n = b.shape[0]
     _call("fp8_gemm_group", _p(a), _p(sa), _p(b), _p(sb), sfmt, m, n, k, _p(out), out.stride(0),
           _stream(stream))
+
+
+def fp8_gemm_group_experts(a, sa, b, sb, sfmt, offsets, out, stream=None):
+    """Per-K-group GEMM of a MoE layer: a [M, K] rows grouped by expert
+    (offsets: device int32 [E + 1]), b [E, N, K], sb [E, ceil(N/128), K/128]."""
+    m, k = a.shape
+    e, n, kb = b.shape
+    assert kb == k and offsets.dtype == torch.int32 and offsets.numel() == e + 1
+    _call("fp8_gemm_group_experts", _p(a), _p(sa), _p(b), _p(sb), sfmt, _p(offsets), e, m, n, k,
+          _p(out), out.stride(0), _stream(stream))
 
 
 def fp8_gemm_group_noalloc(a, sa, b, sb, sfmt, out, stream=None):

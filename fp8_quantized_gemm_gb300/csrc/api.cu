@@ -486,6 +486,37 @@ int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const voi
   return run_gemm(mode, a, b, args, (cudaStream_t)stream);
 }
 
+int fp8_gemm_group_experts(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
+                           int sfmt, const int32_t *offsets, int experts, int64_t M, int64_t N,
+                           int64_t K, void *c, int64_t ldc, fp8_stream_t stream) {
+  int rc = check_gemm_common(a, b, M, N, K, 128);
+  if (rc != FP8_OK) return rc;
+  if (sa == nullptr || sb == nullptr || offsets == nullptr) return FP8_ERR_INVALID_ARG;
+  if (experts < 1 || experts > fp8k::kMaxExperts) return FP8_ERR_INVALID_ARG;
+  if (experts * N >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
+  if ((rc = check_output(c, N, ldc, FP8_OUT_BF16)) != FP8_OK) return rc;
+  DeviceState *d = nullptr;
+  if ((rc = device_state(&d)) != FP8_OK) return rc;
+  const int mode = sfmt == FP8_SCALE_F32 ? fp8k::kScaleGroupF32 : fp8k::kScaleGroupUe8m0;
+  fp8k::GemmArgs args{};
+  args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
+  args.out_dt = FP8_OUT_BF16; args.ldc = ldc; args.c = c; args.sa = sa; args.sb = sb;
+  args.err = d->err;
+  args.wait_limit_ns = g_wait_limit_ns;
+  args.vec_store = vector_store_ok(c, ldc, FP8_OUT_BF16);
+  args.ksplit = 1;
+  args.experts = experts;
+  args.offsets = offsets;
+  args.sb_expert_stride = ((N + 127) / 128) * (K / 128);
+  // tile width chosen for the average rows per expert
+  const int bn = fp8k::gemm_tile_n(mode, M / experts);
+  CUtensorMap tma, tmb;
+  if ((rc = encode_operand(&tma, a, K, M, 128)) != FP8_OK) return rc;
+  if ((rc = encode_operand(&tmb, b, K, (int64_t)experts * N, bn)) != FP8_OK) return rc;
+  return to_status(fp8k::launch_gemm_experts(mode, bn, tma, tmb, args, d->sms, (cudaStream_t)stream));
+}
+
 int fp8_gemm_mx(const uint8_t *a, const uint32_t *la, const float *ga, const uint8_t *b,
                 const uint32_t *lb, const float *gb, int64_t M, int64_t N, int64_t K, int out_dt,
                 void *c, int64_t ldc, fp8_stream_t stream) {

@@ -127,12 +127,81 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   // (t % tiles_n) * BN; CTA b takes tiles b, b + gridDim.x, ...  Consecutive
   // CTAs share an A row block (L2 reuse of A; B is read by every row block).
   const int64_t tiles_n = (args.N + BN - 1) / BN;
-  const int64_t num_tiles = ((args.M + C::BM - 1) / C::BM) * tiles_n;
+  // Expert-grouped rows: a tile never spans two experts; expert e owns
+  // ceil(rows_e / 128) * tiles_n consecutive tile indices.  One warp turns
+  // the device offsets into that prefix (kept in shared memory) per CTA.
+  __shared__ int64_t ex_tile0[kMaxExperts + 1];
+  __shared__ int32_t ex_row0[kMaxExperts + 1];
+  const int E = args.experts;
+  if (E > 0) {
+    if (warp == 0) {
+      // lane l takes experts [8l, 8l + 8)
+      int64_t cnt[8];
+      int64_t sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = 8 * (int)lane + i;
+        cnt[i] = 0;
+        if (e < E) {
+          const int32_t r0 = args.offsets[e], r1 = args.offsets[e + 1];
+          ex_row0[e] = r0;
+          cnt[i] = r1 > r0 ? (int64_t)((r1 - r0 + C::BM - 1) / C::BM) * tiles_n : 0;
+          if (e == E - 1) ex_row0[E] = r1;
+        }
+        sum += cnt[i];
+      }
+      int64_t incl = sum;  // inclusive scan of the lane sums
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if ((int)lane >= o) incl += v;
+      }
+      int64_t run = incl - sum;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = 8 * (int)lane + i;
+        if (e < E) ex_tile0[e] = run;
+        run += cnt[i];
+        if (e == E - 1) ex_tile0[E] = run;
+      }
+    }
+    __syncthreads();
+  }
+  const int64_t num_tiles = E > 0 ? ex_tile0[E] : ((args.M + C::BM - 1) / C::BM) * tiles_n;
   const int KB = (int)((args.K + C::BK - 1) / C::BK);
   // work unit u = (tile u % num_tiles, K split u / num_tiles); with ksplit 1
   // units are tiles.  Split s covers k blocks [s*KB/ks, (s+1)*KB/ks).
   const int ks = args.ksplit;
   const int64_t num_units = num_tiles * ks;
+  // Tile origin: rows [m0, row_end) of A and C (row_end ends the expert's
+  // rows), columns [n0, n0 + BN), B tensor-map row brow, scale offset sbo.
+  struct TileInfo {
+    int64_t m0, n0, row_end, brow, sbo;
+  };
+  auto tile_info = [&](int64_t t) {
+    TileInfo ti;
+    if (E > 0) {
+      int lo = 0, hi = E;  // the expert e with ex_tile0[e] <= t < ex_tile0[e + 1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ex_tile0[mid] <= t) lo = mid; else hi = mid;
+      }
+      while (lo + 1 < E && ex_tile0[lo + 1] <= t) ++lo;  // skip empty experts
+      const int64_t local = t - ex_tile0[lo];
+      ti.m0 = ex_row0[lo] + (local / tiles_n) * C::BM;
+      ti.n0 = (local % tiles_n) * BN;
+      ti.row_end = ex_row0[lo + 1];
+      ti.brow = (int64_t)lo * args.N + ti.n0;
+      ti.sbo = (int64_t)lo * args.sb_expert_stride;
+    } else {
+      ti.m0 = (t / tiles_n) * C::BM;
+      ti.n0 = (t % tiles_n) * BN;
+      ti.row_end = args.M;
+      ti.brow = ti.n0;
+      ti.sbo = 0;
+    }
+    return ti;
+  };
   // the CTA's units: u_first, u_first + u_step, ...  In a split cluster the
   // CTA owns exactly one unit: tile = cluster index, split = cluster rank.
   const bool csplit = args.cluster_split != 0;
@@ -160,15 +229,17 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     // origin and k range cached (64-bit divisions once per unit, not per k
     // block: the producer issues every stage and must stay cheap).
     struct Cursor {
-      int64_t u, m0, n0;
+      int64_t u, m0, n0, brow, sbo;
       int kb, kb_end;
     };
     auto enter = [&](Cursor &c, int64_t u) {
       c.u = u;
       if (u < num_units) {
-        const int64_t t = unit_tile(u);
-        c.m0 = (t / tiles_n) * C::BM;
-        c.n0 = (t % tiles_n) * BN;
+        const TileInfo ti = tile_info(unit_tile(u));
+        c.m0 = ti.m0;
+        c.n0 = ti.n0;
+        c.brow = ti.brow;
+        c.sbo = ti.sbo;
         c.kb = kb_begin(u);
         c.kb_end = kb_end(u);
       }
@@ -183,6 +254,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
         const int64_t G = args.K / 128;
         const int64_t m0 = cs.m0, n0 = cs.n0;
         const int kb = cs.kb;
+        sb8 += cs.sbo;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int64_t m = m0 + 32 * c + lane;
@@ -212,7 +284,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     }
     // one k block (cu, ckb) into stage it % STAGES; false when a wait gave up
     auto stage = [&](uint32_t (&fa)[4], uint32_t (&fb)[BN / 32]) -> bool {
-      const int64_t m0 = cur.m0, n0 = cur.n0;
+      const int64_t m0 = cur.m0, n0 = cur.n0, brow = cur.brow;
       const int kb = cur.kb;
       const int s = (int)(it % STAGES);
       const uint32_t round = it / STAGES;
@@ -253,7 +325,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
           for (int h = 0; h < BN / 128; ++h)
             tma_load_2d(sB(s) + h * 128 * C::BK, &tmb, full_bar(s), (int32_t)n0 + 128 * h, k0);
         } else {
-          tma_load_2d(sB(s), &tmb, full_bar(s), k0, (int32_t)n0);
+          tma_load_2d(sB(s), &tmb, full_bar(s), k0, (int32_t)brow);
         }
         if constexpr (MODE == kScaleMx) {
           const int64_t mpad = (args.M + 127) / 128 * 128;
@@ -384,8 +456,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       for (int64_t u = u_first; u < num_units; u += u_step, ++j) {
         const int64_t t = unit_tile(u);
         const int split = (int)(u / num_tiles);
-        const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
-        const int64_t row = m0 + 32 * q + lane;
+        const TileInfo ti = tile_info(t);
+        const int64_t m0 = ti.m0, n0 = ti.n0;
+        // rows past the tile's expert belong to the next expert: not stored
+        const int64_t row = m0 + 32 * q + lane < ti.row_end ? m0 + 32 * q + lane : args.M;
         const uint32_t buf = j % C::kAccBufs, use = j / C::kAccBufs;
         const bool got = mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3);
         if (ks == 1 && !got) break;
@@ -432,35 +506,54 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
         const int64_t t = unit_tile(u);
         const int split = (int)(u / num_tiles);
         const int kb0 = kb_begin(u), kb1 = kb_end(u);
-        const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
-        const int64_t row = m0 + 32 * q + lane;
-        const float *sb_row = sb + (n0 >> 7) * G;
+        const TileInfo ti = tile_info(t);
+        const int64_t m0 = ti.m0, n0 = ti.n0;
+        // rows past the tile's expert belong to the next expert: not stored
+        const int64_t row = m0 + 32 * q + lane < ti.row_end ? m0 + 32 * q + lane : args.M;
+        const float *sb_row = sb + ti.sbo + (n0 >> 7) * G;
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-        float sa_next = row < args.M ? __ldg(sa + (int64_t)kb0 * args.M + row) : 0.0f;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const uint32_t buf = it & 3u, use = it >> 2;
-          const float s_cur = sa_next * __ldg(sb_row + kb);
-          if (kb + 1 < kb1)
-            sa_next = row < args.M ? __ldg(sa + (int64_t)(kb + 1) * args.M + row) : 0.0f;
-          if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          uint32_t r0[32], r1[32];
-          const uint32_t col = buf * BN + (uint32_t)(h * 64);
-          FP8K_TMEM_LD_X32(lane_base + col, r0);
-          FP8K_TMEM_LD_X32(lane_base + col + 32, r1);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acce_bar(buf));
+        // the two scales of a k block are loaded kQ k blocks before it is
+        // promoted, into register slots used round-robin (constant indices:
+        // the loop is unrolled over the slots), so no promotion step waits on
+        // a scale load
+        constexpr int kQ = 4;
+        float sa_q[kQ], sb_q[kQ];
+        auto load_s = [&](int k, float &fa, float &fb) {
+          fa = row < args.M ? __ldg(sa + (int64_t)k * args.M + row) : 0.0f;
+          fb = __ldg(sb_row + k);
+        };
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            acc[i] = fmaf(s_cur, __uint_as_float(r0[i]), acc[i]);
-            acc[32 + i] = fmaf(s_cur, __uint_as_float(r1[i]), acc[32 + i]);
+        for (int d = 0; d < kQ; ++d)
+          if (kb0 + d < kb1) load_s(kb0 + d, sa_q[d], sb_q[d]);
+        for (int kb = kb0; kb < kb1 && ok; kb += kQ) {
+#pragma unroll
+          for (int j = 0; j < kQ; ++j) {
+            const int k = kb + j;
+            if (k >= kb1) break;
+            const uint32_t buf = it & 3u, use = it >> 2;
+            const float s_cur = sa_q[j] * sb_q[j];
+            if (k + kQ < kb1) load_s(k + kQ, sa_q[j], sb_q[j]);
+            if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            const uint32_t col = buf * BN + (uint32_t)(h * 64);
+            FP8K_TMEM_LD_X32(lane_base + col, r0);
+            FP8K_TMEM_LD_X32(lane_base + col + 32, r1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(buf));
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              acc[i] = fmaf(s_cur, __uint_as_float(r0[i]), acc[i]);
+              acc[32 + i] = fmaf(s_cur, __uint_as_float(r1[i]), acc[32 + i]);
+            }
+            ++it;
           }
         }
         if (ks == 1 && !ok) break;
@@ -488,8 +581,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     // a slice of the tile's rows over the cluster, in split order
     cluster_sync();
     if (warp >= 2) {
-      const int64_t t = unit_tile(u_first);
-      const int64_t m0 = (t / tiles_n) * C::BM, n0 = (t % tiles_n) * BN;
+      const TileInfo ti = tile_info(unit_tile(u_first));
+      const int64_t m0 = ti.m0, n0 = ti.n0;
       float alpha = 1.0f;
       if constexpr (MODE == kScaleTensor)
         alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
@@ -520,7 +613,9 @@ static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const Gem
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const int64_t units = ((args.M + C::BM - 1) / C::BM) * ((args.N + BN - 1) / BN) * args.ksplit;
+  // (expert-grouped rows: at most one partial row tile per expert more)
+  const int64_t row_tiles = (args.M + C::BM - 1) / C::BM + (args.experts > 0 ? args.experts : 0);
+  const int64_t units = row_tiles * ((args.N + BN - 1) / BN) * args.ksplit;
   if (args.cluster_split) {
     // one CTA per unit; the splits of a tile are one cluster
     if (args.ksplit < 2 || args.ksplit > kMaxClusterSplit) return cudaErrorInvalidValue;
@@ -621,6 +716,14 @@ int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster
     if (ks > by_partials) ks = by_partials;
   }
   return ks < 2 ? 1 : (int)ks;
+}
+
+cudaError_t launch_gemm_experts(int mode, int bn, const CUtensorMap &tma, const CUtensorMap &tmb,
+                                const GemmArgs &args, int sms, cudaStream_t st) {
+  if (mode == kScaleGroupF32) return run<kScaleGroupF32, 128, 6>(tma, tmb, args, sms, st);
+  if (mode != kScaleGroupUe8m0) return cudaErrorInvalidValue;
+  if (bn == 128) return run<kScaleGroupUe8m0, 128, 6>(tma, tmb, args, sms, st);
+  return run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, sms, st);
 }
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,

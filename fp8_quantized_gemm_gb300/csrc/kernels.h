@@ -77,7 +77,14 @@ struct GemmArgs {
   // (cluster rank = split) and reduce their partials through distributed
   // shared memory; ws and counters are then unused
   int cluster_split;
+  // experts > 0 (group modes, ksplit 1): rows [offsets[e], offsets[e+1]) of A
+  // use expert e's weights: B rows e*N .. e*N+N-1 of the [E*N, K] tensor map
+  // and scales sb + e * sb_expert_stride
+  int experts;
+  const int32_t *offsets;       // device, experts + 1 entries
+  int64_t sb_expert_stride;     // elements of sb per expert
 };
+constexpr int kMaxExperts = 256;
 
 // Wait bound the API passes to kernels (fp8_set_option FP8_OPT_WAIT_LIMIT_NS).
 uint64_t wait_limit_ns();
@@ -93,6 +100,9 @@ int gemm_tile_n(int mode, int64_t M);
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,
                         const GemmArgs &args, int sms, cudaStream_t st);
+// Expert-grouped per-K-group GEMM (args.experts > 0) with B tiles `bn` wide.
+cudaError_t launch_gemm_experts(int mode, int bn, const CUtensorMap &tma, const CUtensorMap &tmb,
+                                const GemmArgs &args, int sms, cudaStream_t st);
 
 // CTA-pair (cta_group::2) variant of the per-tensor GEMM: 256 x 256 tiles, B
 // staged half per CTA (the B tensor map box has gemm_pair_b_rows() rows).

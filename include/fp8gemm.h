@@ -318,6 +318,30 @@ FP8_API int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const uint8
                                    const void *sb, int sfmt, int64_t M, int64_t N, int64_t K,
                                    void *c, int64_t ldc, fp8_stream_t stream);
 
+/* ------------------------------------- GEMM, per K group, MoE experts --
+ * fp8_gemm_group_experts: the per-K-group GEMM of a mixture-of-experts layer
+ * whose token rows are grouped by expert ([HF] 一 and 六 6.4: FP8Experts,
+ * 128x128 weight blocks per expert; 七: UE8M0 scales).  Rows
+ * [offsets[e], offsets[e+1]) of A are the tokens routed to expert e, and for
+ * such a row m
+ *   C[m,n] = sum_g sa[g,m] * sb[e][n/128, g] * sum_{k in g} a[m,k] b[e][n,k].
+ *   a        [M, K] E4M3 codes, sa [K/128, M] (fp8_quantize_token_group)
+ *   b        [E, N, K] E4M3 codes, expert-major: expert e's [N, K] block
+ *            quantized as by fp8_quantize_block
+ *   sb       [E, ceil(N/128), K/128] scales (fp32 or UE8M0 bytes per sfmt)
+ *   offsets  DEVICE int32 [E + 1]: 0 = offsets[0] <= ... <= offsets[E] = M;
+ *            segments of any size, empty experts allowed.  Read by the
+ *            kernel: the host does not check them (a tile never spans two
+ *            experts; rows outside [0, M) are never loaded or stored).
+ *   experts  E, 1 <= E <= 256.  c [M, ldc] bf16.  K % 128 == 0.
+ * One persistent launch over all experts' tiles (each expert's row range
+ * split into 128-row tiles); no split K.
+ */
+FP8_API int fp8_gemm_group_experts(const uint8_t *a, const void *sa, const uint8_t *b,
+                                   const void *sb, int sfmt, const int32_t *offsets, int experts,
+                                   int64_t M, int64_t N, int64_t K, void *c, int64_t ldc,
+                                   fp8_stream_t stream);
+
 /* ----------------------------------------------------- GEMM, two level --
  * fp8_gemm_mx: C = S_a * S_b * sum_i r_a[m,i] r_b[n,i] sum_{k in i} a.b
  * ([MOSS] 4, step 4): the E8M0 local factors are block scale factors of the

@@ -156,3 +156,25 @@ def test_quantize_tensors_validation(lib):
     assert f(ctypes.cast(arr, ctypes.c_void_p), 2, 16, None) == -3   # mixed input dtypes
     if not torch.cuda.is_available():
         assert _qtensors(lib) == -6
+
+
+def test_gemm_group_experts_validation(lib):
+    import torch
+    f = lib.fp8_gemm_group_experts
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_int] + \
+        [ctypes.c_int64] * 3 + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    ok = dict(a=16, sa=16, b=16, sb=16, sfmt=1, off=16, e=8, m=1024, n=256, k=1024, c=256, ldc=256)
+
+    def call(**kw):
+        p = dict(ok)
+        p.update(kw)
+        return f(p["a"], p["sa"], p["b"], p["sb"], p["sfmt"], p["off"], p["e"], p["m"], p["n"],
+                 p["k"], p["c"], p["ldc"], None)
+    assert call(e=0) == -1                  # no experts
+    assert call(e=257) == -1                # more than 256 experts
+    assert call(off=None) == -1             # offsets are required
+    assert call(k=1000) == -2               # K % 128
+    assert call(sfmt=2) == -1
+    assert call(ldc=100) == -1
+    if not torch.cuda.is_available():
+        assert call() == -6

@@ -446,3 +446,50 @@ def test_gemm_tensor_grouped_linear_without_transposed_copies(shape):
             ok, worst = OG.check(got[rows, cols], c, e, odt)
         assert ok, (i, worst)
     assert F.fp8_get_last_device_error()[0] == 0
+
+
+# ------------------------------------------------- MoE expert-grouped GEMM --
+
+def expert_operands(experts, tokens, n, k, sfmt, seed, counts=None):
+    act, w, drawn = workloads.moe_experts(experts, tokens, n, k, seed=seed)
+    counts = drawn if counts is None else torch.tensor(counts, dtype=torch.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts.numpy())]).astype(np.int32)
+    m = int(offsets[-1])
+    act = act[:m]
+    qa, sa = OQ.quantize_token_group(act.float().numpy(), "e4m3", sfmt)
+    a_deq = OG.dequant_operand(qa, "e4m3", OQ.expand(OQ.group_scale_values(sa, sfmt), m, k, 1, 128))
+    qbs, sbs, b_deq = [], [], []
+    for e in range(experts):
+        qb, sb = OQ.quantize_block(w[e].float().numpy(), "e4m3", sfmt)
+        qbs.append(qb)
+        sbs.append(np.asarray(sb))
+        b_deq.append(OG.dequant_operand(qb, "e4m3",
+                                        OQ.expand(OQ.group_scale_values(sb, sfmt), n, k, 128, 128)))
+    c, e_ = OG.gemm_experts(a_deq, b_deq, offsets)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    return (dev(qa), dev(np.asarray(sa).T), dev(np.stack(qbs)), dev(np.stack(sbs)),
+            dev(offsets), c, e_, m)
+
+
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+@pytest.mark.parametrize("case", [
+    # experts, tokens, N, K, fixed counts (None: drawn)
+    (8, 1000, 256, 1024, None),
+    (5, 0, 384, 512, [0, 300, 1, 0, 129]),       # empty experts, a 1-row expert
+    (3, 0, 200, 256, [130, 0, 257]),             # N not a multiple of 128
+    (16, 4096, 512, 2048, None),
+])
+def test_gemm_group_experts(sfmt, case):
+    F = lib()
+    experts, tokens, n, k, counts = case
+    if counts is not None:
+        tokens = sum(counts)
+    qa, sa, qb, sb, offs, c, e, m = expert_operands(experts, tokens, n, k, sfmt, seed=experts + n,
+                                                    counts=counts)
+    out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    code = F.SCALE_F32 if sfmt == "f32" else F.SCALE_UE8M0
+    F.fp8_gemm_group_experts(qa, sa, qb, sb, code, offs, out)
+    torch.cuda.synchronize()
+    ok, worst = OG.check(out.float().cpu().numpy(), c, e, "bf16")
+    assert ok, worst
+    assert F.fp8_get_last_device_error()[0] == 0

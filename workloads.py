@@ -22,6 +22,11 @@ Workloads (shapes and distributions follow the five scaled-FP8 configurations):
   B[8192,8192] ~N(0,0.02), bf16, seed 3 (MOSS two-level microscaling).
 * ``swiglu``            SwiGLU MLP: x[T,d] ~N(0,1), W1/W3[ffn,d], W2[d,ffn]
   ~N(0,0.02), bf16, seed 4; step-t output gradient dy ~N(0,1e-3), seed 1000+t.
+* ``moe_experts``       mixture-of-experts layer (Transformers fine-grained
+  FP8, FP8Experts): token counts per expert from a seeded multinomial over
+  expert weights ~ U[0.2, 1) (uneven, some experts may get no tokens),
+  activations [T, K] ~N(0,1) with 0.5 % outlier columns x50 ordered by
+  expert, expert weights [E, N, K] ~N(0,0.02), bf16, seed 5.
 
 Outlier columns: count = round(frac * K); the indices are the first ``count``
 entries of a seeded permutation of range(K); the multiply is done in fp32
@@ -112,6 +117,20 @@ def swiglu_grad(step: int, tokens: int = 16384, d: int = 4096, device="cpu"):
     """Synthetic loss gradient dy[tokens,d] ~N(0,1e-3) for training step ``step``."""
     g = _gen(1000 + step, device)
     return _normal((tokens, d), 1e-3, g).to(torch.bfloat16)
+
+
+def moe_experts(experts: int, tokens: int, n: int, k: int, seed: int = 5,
+                outlier_frac: float = 0.005, outlier_factor: float = 50.0):
+    """(act[tokens,k] bf16, w[experts,n,k] bf16, counts[experts] int64): the
+    rows of act are already grouped by expert, counts[e] rows for expert e."""
+    g = _gen(seed)
+    probs = torch.rand(experts, generator=g) * 0.8 + 0.2
+    idx = torch.multinomial(probs, tokens, replacement=True, generator=g)
+    counts = torch.bincount(idx, minlength=experts).to(torch.int64)
+    w = _normal((experts, n, k), 0.02, g).to(torch.bfloat16)
+    act = _normal((tokens, k), 1.0, g)
+    act = _outlier_columns(act, outlier_frac, outlier_factor, g)
+    return act.to(torch.bfloat16), w, counts
 
 
 def uniform(shape, lo: float, hi: float, seed: int) -> torch.Tensor:
