@@ -37,7 +37,9 @@ scale = 1 case against an integer matmul on the code grid, and a transposed
 operand / dropped scale / sign flip each failing the check.  Expert
 grouping: exact rational brute force on two tiny experts, one expert equal
 to the plain product, invariance under reordering the experts with their
-rows, empty experts, and swapped expert weights failing the check.
+rows, empty experts, and swapped expert weights failing the check.  Bias:
+zero operands give the bias in every row, and a bias applied along the rows
+instead of the columns fails the check.
 """
 from __future__ import annotations
 
@@ -72,6 +74,16 @@ def gemm_experts(a_deq, b_deq_list, offsets):
     return c, e_
 
 
+def gemm_bias(c, e, bias):
+    """Epilogue bias (the nanochat module, "实现": Float8Linear adds the
+    linear's bias to the FP8 matmul's output, y = x W^T + b): C + bias[n],
+    float64, and the extra absolute allowance of one fp32 rounding of the
+    biased value (2^-23 |C + b|), because the kernels add the fp32 bias to
+    the fp32 result before the output cast."""
+    cb = np.asarray(c, dtype=np.float64) + np.asarray(bias, dtype=np.float64)[None, :]
+    return cb, np.asarray(e, dtype=np.float64), np.abs(cb) * 2.0 ** -23
+
+
 def gemm_sampled(a_deq, b_deq, rows, cols):
     """C and E at the (rows[i], cols[i]) output positions only."""
     a = np.asarray(a_deq, dtype=np.float64)[np.asarray(rows)]
@@ -87,17 +99,18 @@ def bf16_ulp(v) -> np.ndarray:
     return np.where(a > 0, ulp, np.ldexp(1.0, -133))
 
 
-def tolerance(c_ref, e_ref, out_dtype: str, rel: float = 1e-3) -> np.ndarray:
-    tol = rel * np.asarray(e_ref, dtype=np.float64)
+def tolerance(c_ref, e_ref, out_dtype: str, rel: float = 1e-3, extra=0.0) -> np.ndarray:
+    tol = rel * np.asarray(e_ref, dtype=np.float64) + extra
     if out_dtype == "bf16":
         tol = tol + bf16_ulp(c_ref)
     return tol
 
 
-def check(c_gpu, c_ref, e_ref, out_dtype: str, rel: float = 1e-3):
-    """Returns (ok, worst ratio |err| / tol)."""
+def check(c_gpu, c_ref, e_ref, out_dtype: str, rel: float = 1e-3, extra=0.0):
+    """Returns (ok, worst ratio |err| / tol); ``extra`` is an additional
+    absolute allowance per element (``gemm_bias``)."""
     err = np.abs(np.asarray(c_gpu, dtype=np.float64) - np.asarray(c_ref, dtype=np.float64))
-    tol = tolerance(c_ref, e_ref, out_dtype, rel)
+    tol = tolerance(c_ref, e_ref, out_dtype, rel, extra)
     ratio = err / tol
     worst = float(np.max(ratio)) if ratio.size else 0.0
     return bool(np.all(err <= tol)), worst

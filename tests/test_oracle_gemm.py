@@ -188,3 +188,29 @@ def test_swapped_expert_weights_fail_the_check():
     c, e = G.gemm_experts(a, bs, offsets)
     wrong, _ = G.gemm_experts(a, bs[::-1], offsets)
     assert not G.check(wrong, c, e, "f32")[0]
+
+
+# ------------------------------------------------------------ epilogue bias --
+
+def test_bias_with_zero_operands_is_the_bias_in_every_row():
+    a = np.zeros((5, 64))
+    b = np.zeros((8, 64))
+    bias = np.arange(8, dtype=np.float32) * np.float32(0.375) - np.float32(1.0)
+    c, e = G.gemm(a, b)
+    cb, eb, extra = G.gemm_bias(c, e, bias)
+    assert np.array_equal(cb, np.tile(bias.astype(np.float64), (5, 1)))
+    assert np.array_equal(eb, e)
+    assert np.all(extra == np.abs(cb) * 2.0 ** -23)
+
+
+def test_bias_along_the_wrong_axis_fails_the_check():
+    rng = np.random.default_rng(25)
+    a = torch_decode(finite_codes(rng, (16, 32), "e4m3"), "e4m3") * 0.25
+    b = torch_decode(finite_codes(rng, (16, 32), "e4m3"), "e4m3") * 0.25
+    bias = rng.standard_normal(16).astype(np.float32) * 4.0
+    c, e = G.gemm(a, b)
+    cb, eb, extra = G.gemm_bias(c, e, bias)
+    wrong = c + bias.astype(np.float64)[:, None]
+    assert not G.check(wrong, cb, eb, "f32", extra=extra)[0]
+    # the fp32 rounding of the biased result is within the allowance
+    assert G.check((c.astype(np.float32) + bias).astype(np.float64), cb, eb, "f32", extra=extra)[0]
