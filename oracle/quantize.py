@@ -37,7 +37,9 @@ Pins (``tests/test_oracle_quantize.py``): the amax element maps to exactly
 +-MAX; hand inputs; round-trip error within half a code step times the scale;
 UE8M0 bounds 2**(e-1) < s <= 2**e; the two-level invariants (S is the max of
 the s_i and equals fl32(amax/MAX); every r_i is a power of two in (0, 1];
-S*r_i >= s_i; no NaN codes).
+S*r_i >= s_i; no NaN codes); for the per-row global factor the same per row,
+equality with the per-tensor scheme when every row holds the tensor amax,
+and invariance under power-of-two row scaling.
 """
 from __future__ import annotations
 
@@ -149,11 +151,14 @@ def group_scale_values(stored, sfmt) -> np.ndarray:
 
 # ---------------------------------------------------------- two level ----
 
-def quantize_two_level(x, fmt, block=32):
+def quantize_two_level(x, fmt, block=32, global_per_row=False):
     """MOSS two-level microscaling (MOSS blog, section 4, steps 1-4).
 
     x: [R, K] fp32 with K % block == 0.  Returns (codes [R,K], local E8M0 bytes
-    [R, K/block], global fp32 S).
+    [R, K/block], global fp32 S).  ``global_per_row``: the global factor of
+    step 2 is taken over each row's blocks instead of the whole tensor (the
+    garbled extent of the page's "整个 _ 范围" read per row); S is then an
+    fp32 array [R] and each row's local factors are relative to its own S.
     """
     f = fmt_of(fmt)
     x = np.asarray(x, dtype=F32)
@@ -163,6 +168,18 @@ def quantize_two_level(x, fmt, block=32):
     xb = x.reshape(r, k // block, block)
     am = np.max(np.abs(xb), axis=2).astype(F32) if x.size else np.zeros((r, 0), F32)
     s_i = (am / F32(f.max)).astype(F32)                     # step 1
+    if global_per_row:                                      # step 2, per row
+        big_s = (np.max(s_i, axis=1) if s_i.size else np.zeros(r)).astype(F32)
+        big_s = np.where(big_s > 0, big_s, F32(1.0)).astype(F32)
+        ratio = (s_i / big_s[:, None]).astype(F32)          # step 3
+        e = np.where(s_i > 0, -127, 0).astype(np.int64)
+        pos = ratio > 0
+        if np.any(pos):
+            e[pos] = np.maximum(ceil_log2_f32(ratio[pos]), -127)
+        r_i = np.ldexp(F32(1.0), e).astype(F32)
+        eff = (big_s[:, None] * r_i).astype(F32)            # step 4
+        q = quantize_with_scale(x, np.repeat(eff, block, axis=1), f)
+        return q, e8m0_encode(e), big_s
     big_s = F32(np.max(s_i)) if s_i.size else F32(0.0)      # step 2
     if not big_s > 0:
         big_s = F32(1.0)
@@ -215,9 +232,13 @@ def dequantize_block(q, fmt, scales, sfmt, block=128):
 
 
 def two_level_scale_values(local_bytes, global_s) -> np.ndarray:
-    """Effective per-block multipliers S * r_i (float64)."""
+    """Effective per-block multipliers S * r_i (float64); ``global_s`` is a
+    scalar or, for the per-row variant, one factor per row."""
     b = np.asarray(local_bytes, dtype=np.int64)
-    return float(global_s) * np.ldexp(1.0, b - 127)
+    g = np.asarray(global_s, dtype=np.float64)
+    if g.ndim == 1:
+        g = g[:, None]
+    return g * np.ldexp(1.0, b - 127)
 
 
 def expand(scales, rows, cols, row_block, col_block) -> np.ndarray:

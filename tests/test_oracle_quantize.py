@@ -221,3 +221,44 @@ def test_dequantize_block_roundtrip(sfmt):
     assert np.array_equal(d, lib * Q.expand(vals, 200, 260, 128, 128))
     # within half an E4M3 step (1/16 relative) of the original, blockwise
     assert np.all(np.abs(d - w) <= np.abs(w) / 16 + Q.expand(vals, 200, 260, 128, 128) * 2.0 ** -10)
+
+
+def test_two_level_per_row_global_invariants():
+    """Per-row global factors: S_r is the max of row r's 1x32 scales (which
+    is fl32(row amax / MAX)); every r_i is a power of two in (0, 1] and the
+    smallest with S_r * r_i >= s_i."""
+    a, _ = workloads.two_level(m=48, n=8, k=512)
+    x = a.float().numpy()
+    x[5] *= np.float32(2.0 ** -20)          # one row far smaller than the rest
+    q, local, big_s = Q.quantize_two_level(x, "e4m3", global_per_row=True)
+    assert big_s.shape == (48,)
+    s_i = (np.max(np.abs(x.reshape(48, 16, 32)), axis=2) / F32(448)).astype(F32)
+    assert np.array_equal(big_s, np.max(s_i, axis=1))
+    row_amax = np.max(np.abs(x), axis=1).astype(F32)
+    assert np.array_equal(big_s, (row_amax / F32(448)).astype(F32))
+    r = F.e8m0_decode(local)
+    assert np.all((r > 0) & (r <= 1)) and np.all(np.log2(r) == np.round(np.log2(r)))
+    s = big_s.astype(np.float64)[:, None]
+    assert np.all(s * r >= s_i) and np.all(s * r / 2 < s_i)
+    # each row's block holding the row amax has r = 1 and codes reaching MAX
+    assert np.all(np.max(local, axis=1) == 127)
+    assert np.all(np.max(np.abs(F.decode(q, "e4m3")), axis=1) == 448.0)
+
+
+def test_two_level_per_row_equals_per_tensor_when_rows_share_the_max():
+    x = workloads.normal((6, 256), 1.0, seed=33).numpy()
+    x[:, 17] = 9.0                          # every row holds the tensor amax
+    q1, l1, s1 = Q.quantize_two_level(x, "e4m3")
+    q2, l2, s2 = Q.quantize_two_level(x, "e4m3", global_per_row=True)
+    assert np.all(s2 == s1) and np.array_equal(l1, l2) and np.array_equal(q1, q2)
+
+
+def test_two_level_per_row_is_row_scale_invariant():
+    """Rows that are power-of-two multiples of one row get the same codes and
+    local factors, and global factors in the same ratio."""
+    base = workloads.normal((1, 256), 1.0, seed=35).numpy()
+    x = np.concatenate([base * np.float32(2.0 ** e) for e in (-12, -3, 0, 7)])
+    q, local, big_s = Q.quantize_two_level(x, "e4m3", global_per_row=True)
+    for i in range(1, 4):
+        assert np.array_equal(q[i], q[0]) and np.array_equal(local[i], local[0])
+    assert np.array_equal(big_s / big_s[2], np.float32([2.0 ** -12, 2.0 ** -3, 1.0, 2.0 ** 7]))
