@@ -48,6 +48,10 @@ _SIGS = {
     "fp8_gemm_tensor_grouped": [_vp, _int, _vp],
     "fp8_quantize_tensors": [_vp, _int, _vp, _vp],
     "fp8_gemm_group_experts": [_vp, _vp, _vp, _vp, _int, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
+    "fp8_gemm_group_bias": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _vp, _i64, _vp],
+    "fp8_amax_rows": [_vp, _int, _i64, _i64, _vp, _vp],
+    "fp8_quantize_mx_rows": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp],
+    "fp8_gemm_mx_rows": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp],
     "fp8_gemm_mx": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp],
     "fp8_gemm_group_noalloc": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_delayed_state_update": [_vp, _vp, _vp, _i64, _int, _vp],
@@ -170,18 +174,21 @@ class GemmProblem(ctypes.Structure):
     """fp8_gemm_problem_t (include/fp8gemm.h)."""
     _fields_ = [("a", _vp), ("b", _vp), ("sa", _vp), ("sb", _vp), ("M", _i64), ("N", _i64),
                 ("K", _i64), ("fa", _int), ("fb", _int), ("out_dt", _int), ("accumulate", _int),
-                ("c", _vp), ("ldc", _i64), ("a_layout", _int), ("b_layout", _int)]
+                ("c", _vp), ("ldc", _i64), ("a_layout", _int), ("b_layout", _int),
+                ("bias", _vp)]
 
 
 def gemm_problem(a, fa, b, fb, sa, sb, out, *, accumulate=False, a_layout=K_MAJOR,
-                 b_layout=K_MAJOR):
+                 b_layout=K_MAJOR, bias=None):
     """Descriptor of one per-tensor GEMM for fp8_gemm_tensor_grouped.  With
-    K_MAJOR a is [M, K] and b [N, K]; with MN_MAJOR a is [K, M] and b [K, N]."""
+    K_MAJOR a is [M, K] and b [N, K]; with MN_MAJOR a is [K, M] and b [K, N];
+    bias: optional device fp32 [N] added to every row."""
     m, k = a.shape if a_layout == K_MAJOR else a.shape[::-1]
     n = b.shape[0] if b_layout == K_MAJOR else b.shape[1]
     out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
     return GemmProblem(_p(a), _p(b), _p(sa), _p(sb), m, n, k, fa, fb, out_dt,
-                       int(bool(accumulate)), _p(out), out.stride(0), a_layout, b_layout)
+                       int(bool(accumulate)), _p(out), out.stride(0), a_layout, b_layout,
+                       _p(bias) if bias is not None else None)
 
 
 class QuantItem(ctypes.Structure):
@@ -213,9 +220,13 @@ def fp8_gemm_tensor_grouped(problems, stream=None):
     _call("fp8_gemm_tensor_grouped", ctypes.cast(arr, _vp), len(problems), _stream(stream))
 
 
-def fp8_gemm_group(a, sa, b, sb, sfmt, out, stream=None):
+def fp8_gemm_group(a, sa, b, sb, sfmt, out, stream=None, *, bias=None):
     m, k = a.shape
     n = b.shape[0]
+    if bias is not None:
+        _call("fp8_gemm_group_bias", _p(a), _p(sa), _p(b), _p(sb), sfmt, m, n, k, _p(bias),
+              _p(out), out.stride(0), _stream(stream))
+        return
     _call("fp8_gemm_group", _p(a), _p(sa), _p(b), _p(sb), sfmt, m, n, k, _p(out), out.stride(0),
           _stream(stream))
 
@@ -245,6 +256,26 @@ def fp8_gemm_mx(a, la, ga, b, lb, gb, out, *, out_dt=None, stream=None):
         out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
     _call("fp8_gemm_mx", _p(a), _p(la), _p(ga), _p(b), _p(lb), _p(gb), m, n, k, out_dt, _p(out),
           out.stride(0), _stream(stream))
+
+
+def fp8_amax_rows(x, amax_out, stream=None):
+    r, k = x.shape
+    _call("fp8_amax_rows", _p(x), _in_dt(x), r, k, _p(amax_out), _stream(stream))
+
+
+def fp8_quantize_mx_rows(x, fmt, amax_rows, global_out, q, local, stream=None):
+    r, k = x.shape
+    _call("fp8_quantize_mx_rows", _p(x), _in_dt(x), r, k, fmt, _p(amax_rows), _p(global_out),
+          _p(q), _p(local), _stream(stream))
+
+
+def fp8_gemm_mx_rows(a, la, ga, b, lb, gb, out, *, out_dt=None, stream=None):
+    m, k = a.shape
+    n = b.shape[0]
+    if out_dt is None:
+        out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    _call("fp8_gemm_mx_rows", _p(a), _p(la), _p(ga), _p(b), _p(lb), _p(gb), m, n, k, out_dt,
+          _p(out), out.stride(0), _stream(stream))
 
 
 def fp8_delayed_state_update(hist, scale, amax_cur, fmt, stream=None):

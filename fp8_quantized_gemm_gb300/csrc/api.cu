@@ -239,6 +239,7 @@ int run_tensor_problem(const fp8_gemm_problem_t &p, cudaStream_t st) {
   args.sa = p.sa; args.sb = p.sb;
   args.a_mn = p.a_layout == FP8_MN_MAJOR;
   args.b_mn = p.b_layout == FP8_MN_MAJOR;
+  args.bias = p.bias;
   return run_gemm(fp8k::kScaleTensor, p.a, p.b, args, st);
 }
 
@@ -375,6 +376,33 @@ int fp8_quantize_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt, con
                                          (cudaStream_t)stream));
 }
 
+int fp8_amax_rows(const void *x, int in_dt, int64_t R, int64_t K, float *amax_out,
+                  fp8_stream_t stream) {
+  if (x == nullptr || amax_out == nullptr || !valid_in(in_dt)) return FP8_ERR_INVALID_ARG;
+  if (R < 1 || K < 1 || R >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (K % 8 != 0 || !aligned16(x)) return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_row_amax(x, in_dt, R, K, amax_out, d->sms, (cudaStream_t)stream));
+}
+
+int fp8_quantize_mx_rows(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
+                         const float *amax_rows, float *global_out, uint8_t *q, uint32_t *local,
+                         fp8_stream_t stream) {
+  if (x == nullptr || amax_rows == nullptr || global_out == nullptr || q == nullptr ||
+      local == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (R < 1 || K < 1 || R >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (K % 128 != 0 || !aligned16(x) || !aligned16(q) || !aligned16(local))
+    return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_quant_mx(x, in_dt, R, K, fmt, amax_rows, global_out, q, local,
+                                         d->sms, (cudaStream_t)stream, true));
+}
+
 int fp8_quantize_mx1(const void *x, int in_dt, int64_t R, int64_t K, int fmt, float *global_out,
                      uint8_t *q, uint32_t *local, fp8_stream_t stream) {
   if (x == nullptr || q == nullptr || local == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
@@ -462,6 +490,7 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
     a.vec_store = vector_store_ok(p.c, p.ldc, p.out_dt);
     a.a_mn = p.a_layout == FP8_MN_MAJOR;
     a.b_mn = p.b_layout == FP8_MN_MAJOR;
+    a.bias = p.bias;
     a.ksplit = 1;
     args[k] = a;
     if ((rc = encode_gemm_operand(&tma[k], p.a, a.a_mn, p.K, p.M, 128)) != FP8_OK) return rc;
@@ -474,6 +503,12 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
 
 int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb, int sfmt,
                    int64_t M, int64_t N, int64_t K, void *c, int64_t ldc, fp8_stream_t stream) {
+  return fp8_gemm_group_bias(a, sa, b, sb, sfmt, M, N, K, nullptr, c, ldc, stream);
+}
+
+int fp8_gemm_group_bias(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
+                        int sfmt, int64_t M, int64_t N, int64_t K, const float *bias, void *c,
+                        int64_t ldc, fp8_stream_t stream) {
   int rc = check_gemm_common(a, b, M, N, K, 128);
   if (rc != FP8_OK) return rc;
   if (sa == nullptr || sb == nullptr) return FP8_ERR_INVALID_ARG;
@@ -482,6 +517,7 @@ int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const voi
   GemmArgs args{};
   args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
   args.out_dt = FP8_OUT_BF16; args.ldc = ldc; args.c = c; args.sa = sa; args.sb = sb;
+  args.bias = bias;
   const int mode = sfmt == FP8_SCALE_F32 ? fp8k::kScaleGroupF32 : fp8k::kScaleGroupUe8m0;
   return run_gemm(mode, a, b, args, (cudaStream_t)stream);
 }
@@ -529,6 +565,23 @@ int fp8_gemm_mx(const uint8_t *a, const uint32_t *la, const float *ga, const uin
   args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
   args.out_dt = out_dt; args.ldc = ldc; args.c = c; args.sa = la; args.sb = lb;
   args.ga = ga; args.gb = gb;
+  return run_gemm(fp8k::kScaleMx, a, b, args, (cudaStream_t)stream);
+}
+
+int fp8_gemm_mx_rows(const uint8_t *a, const uint32_t *la, const float *ga, const uint8_t *b,
+                     const uint32_t *lb, const float *gb, int64_t M, int64_t N, int64_t K,
+                     int out_dt, void *c, int64_t ldc, fp8_stream_t stream) {
+  int rc = check_gemm_common(a, b, M, N, K, 128);
+  if (rc != FP8_OK) return rc;
+  if (la == nullptr || lb == nullptr || ga == nullptr || gb == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(la) || !aligned16(lb)) return FP8_ERR_MISALIGNED;
+  if ((rc = check_output(c, N, ldc, out_dt)) != FP8_OK) return rc;
+  GemmArgs args{};
+  args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
+  args.out_dt = out_dt; args.ldc = ldc; args.c = c; args.sa = la; args.sb = lb;
+  args.ga = ga; args.gb = gb;
+  args.row_scale = ga;  // S_a[m] * S_b[n] per output element, in the epilogue
+  args.col_scale = gb;
   return run_gemm(fp8k::kScaleMx, a, b, args, (cudaStream_t)stream);
 }
 

@@ -217,9 +217,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     uint32_t it = 0;  // stage iterations issued, across tiles
     bool ok = true;
     // group-UE8M0 mode: the per-128 scale bytes of a k block are loaded into
-    // registers kSfAhead k blocks before their stage is filled, so the
-    // producer never waits on a scale load (with a one-deep prefetch every
-    // stage paid a load latency, which dominated small-M GEMMs).  The queue
+    // registers kSfAhead (= STAGES) k blocks before their stage is filled,
+    // so the producer does not wait on scale loads (with a one-deep prefetch
+    // every stage paid a load latency, which dominated small-M GEMMs; a
+    // queue much deeper than the ring measured slower: the unrolled stage
+    // loop below grows with it).  The queue
     // is kSfAhead register slots used round-robin with compile-time indices
     // (the stage loop below is unrolled over the slots), so no register ever
     // moves while its load is still in flight.
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       float alpha = 1.0f;
       if constexpr (MODE == kScaleTensor)
         alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
-      if constexpr (MODE == kScaleMx) alpha = *args.ga * *args.gb;
+      if constexpr (MODE == kScaleMx) alpha = args.row_scale != nullptr ? 1.0f : *args.ga * *args.gb;
       uint32_t j = 0;
       for (int64_t u = u_first; u < num_units; u += u_step, ++j) {
         const int64_t t = unit_tile(u);
@@ -586,7 +588,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       float alpha = 1.0f;
       if constexpr (MODE == kScaleTensor)
         alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
-      if constexpr (MODE == kScaleMx) alpha = *args.ga * *args.gb;
+      if constexpr (MODE == kScaleMx) alpha = args.row_scale != nullptr ? 1.0f : *args.ga * *args.gb;
       cluster_reduce<BN>(args, part, m0, n0, C::BM, alpha, cluster_ctarank(), ks,
                          (int)threadIdx.x - 64, C::kEpiWarps * 32);
     }

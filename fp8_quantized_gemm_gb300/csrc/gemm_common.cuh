@@ -7,11 +7,35 @@
 
 namespace fp8k {
 
-// Store 32 consecutive results of one output row (already scaled).
+// Store 32 consecutive results of one output row (already scaled), plus the
+// bias of their columns when there is one.
 __device__ __forceinline__ void store_row32(const GemmArgs &a, int64_t row, int64_t col0,
-                                            const float (&v)[32]) {
+                                            const float (&vin)[32]) {
   if (row >= a.M || col0 >= a.N) return;
   const bool full = (col0 + 32 <= a.N) && a.vec_store;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = vin[i];
+  if (a.row_scale != nullptr) {
+    const float rs = __ldg(a.row_scale + row);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < a.N) v[i] *= rs * __ldg(a.col_scale + col0 + i);
+  }
+  if (a.bias != nullptr) {
+    if (col0 + 32 <= a.N && (reinterpret_cast<uintptr_t>(a.bias + col0) & 15u) == 0) {
+      const float4 *b4 = reinterpret_cast<const float4 *>(a.bias + col0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 b = __ldg(b4 + i);
+        v[4 * i] += b.x; v[4 * i + 1] += b.y; v[4 * i + 2] += b.z; v[4 * i + 3] += b.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < a.N) v[i] += __ldg(a.bias + col0 + i);
+    }
+  }
   if (a.out_dt == 1) {
     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.c) + row * a.ldc + col0;
     if (full) {
@@ -60,9 +84,22 @@ __device__ __forceinline__ void store_partial32(const GemmArgs &a, int split, in
   }
 }
 
-// Store up to four consecutive results of one output row (already scaled).
+// Store up to four consecutive results of one output row (already scaled),
+// plus the bias of their columns when there is one.
 __device__ __forceinline__ void store4(const GemmArgs &a, int64_t row, int64_t col, int n,
-                                       const float (&v)[4]) {
+                                       const float (&vin)[4]) {
+  float v[4] = {vin[0], vin[1], vin[2], vin[3]};
+  if (a.row_scale != nullptr) {
+    const float rs = __ldg(a.row_scale + row);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i < n) v[i] *= rs * __ldg(a.col_scale + col + i);
+  }
+  if (a.bias != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i < n) v[i] += __ldg(a.bias + col + i);
+  }
   if (a.out_dt == 1) {
     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.c) + row * a.ldc + col;
     if (n == 4 && a.vec_store) {

@@ -18,9 +18,12 @@ cudaError_t launch_quant_group(const void *x, int in_dt, int64_t M, int64_t K, i
                                int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st);
 cudaError_t launch_quant_block(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
                                int sfmt, uint8_t *q, void *scales, cudaStream_t st);
+// amax == nullptr: one-level MXFP8; per_row: amax and global_out are [R]
 cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
                             const float *amax, float *global_out, uint8_t *q, uint32_t *local,
-                            int sms, cudaStream_t st);
+                            int sms, cudaStream_t st, bool per_row = false);
+cudaError_t launch_row_amax(const void *x, int in_dt, int64_t R, int64_t K, float *out, int sms,
+                            cudaStream_t st);
 cudaError_t launch_dequant_block(const uint8_t *q, int64_t N, int64_t K, int fmt, int sfmt,
                                  const void *scales, void *out, int sms, cudaStream_t st);
 cudaError_t launch_auto_scale(const float *amax0, double grow, int fmt, float *scale,
@@ -83,6 +86,12 @@ struct GemmArgs {
   int experts;
   const int32_t *offsets;       // device, experts + 1 entries
   int64_t sb_expert_stride;     // elements of sb per expert
+  // nullable fp32 [N]: added to every row of the result (after the scales,
+  // before the output cast)
+  const float *bias;
+  // nullable fp32 [M] and [N] (together): the result is multiplied by
+  // row_scale[m] * col_scale[n] (per-row global factors of two-level scaling)
+  const float *row_scale, *col_scale;
 };
 constexpr int kMaxExperts = 256;
 

@@ -385,17 +385,25 @@ __device__ __forceinline__ int64_t mx_word_index(int64_t r, int64_t g, int64_t r
   return g * rpad + (r & ~(int64_t)127) + 4 * (r & 31) + ((r & 127) >> 5);
 }
 
-// kOneLevel: plain MXFP8 (MOSS blog, section 1): the global factor is 1 and
-// each block's power of two is the smallest not below amax_i / MAX.
-template <typename T, bool kOneLevel>
+// kGlobal selects the global factor:
+//   kMxTensor   two level (MOSS blog, section 4): S = fl32(tensor amax / MAX)
+//               (= max_i fl32(amax_i / MAX)), one for the tensor;
+//   kMxOneLevel plain MXFP8 (section 1): S = 1, each block's power of two the
+//               smallest not below amax_i / MAX;
+//   kMxRow      two level with a global factor per row: S_r = fl32(row amax /
+//               MAX) from amax_in[r], written to global_out[r].
+constexpr int kMxTensor = 0, kMxOneLevel = 1, kMxRow = 2;
+template <typename T, int kGlobal>
 __global__ void __launch_bounds__(256)
     quant_mx_kernel(const T *__restrict__ x, int64_t R, int64_t K, int fmt,
                     const float *amax_in, float *global_out, uint8_t *__restrict__ q,
                     uint32_t *__restrict__ local) {
+  constexpr bool kOneLevel = kGlobal == kMxOneLevel;
   const float mx = fmt_max(fmt);
   // two level: S == max_i fl32(amax_i / MAX)
-  const float S = kOneLevel ? 1.0f : scale_from_amax(*amax_in, mx);
-  if (global_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *global_out = S;
+  const float S_tensor = kGlobal == kMxTensor ? scale_from_amax(*amax_in, mx) : 1.0f;
+  if (kGlobal != kMxRow && global_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+    *global_out = S_tensor;
   const int64_t G = K / 128, pairs = (G + 1) / 2;
   const int64_t rpad = (R + 127) / 128 * 128;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -408,6 +416,11 @@ __global__ void __launch_bounds__(256)
     if (r >= R) {  // padding rows: factor 1 (byte 127)
       if ((l & 15) == 0 && g < G) local[mx_word_index(r, g, rpad)] = 0x7F7F7F7Fu;
       continue;
+    }
+    float S = S_tensor;
+    if constexpr (kGlobal == kMxRow) {
+      S = scale_from_amax(amax_in[r], mx);
+      if (p == 0 && l == 0 && global_out != nullptr) global_out[r] = S;
     }
     const bool valid = k < K;
     float v[8];
@@ -575,24 +588,58 @@ cudaError_t launch_quant_block(const void *w, int in_dt, int64_t N, int64_t K, i
 
 cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
                             const float *amax, float *global_out, uint8_t *q, uint32_t *local,
-                            int sms, cudaStream_t st) {
+                            int sms, cudaStream_t st, bool per_row) {
   const int64_t G = K / 128, pairs = (G + 1) / 2, rpad = (R + 127) / 128 * 128;
   const int threads = 256, blocks = grid_for(rpad * pairs * 32, threads, 8, sms);
+  const int kind = amax == nullptr ? kMxOneLevel : (per_row ? kMxRow : kMxTensor);
+#define FP8K_QMX(T, G)                                                                           \
+  quant_mx_kernel<T, G><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), R, K, fmt, amax, \
+                                                    global_out, q, local)
   if (in_dt == 0) {
-    if (amax != nullptr)
-      quant_mx_kernel<__nv_bfloat16, false><<<blocks, threads, 0, st>>>(
-          static_cast<const __nv_bfloat16 *>(x), R, K, fmt, amax, global_out, q, local);
-    else
-      quant_mx_kernel<__nv_bfloat16, true><<<blocks, threads, 0, st>>>(
-          static_cast<const __nv_bfloat16 *>(x), R, K, fmt, amax, global_out, q, local);
+    if (kind == kMxTensor) FP8K_QMX(__nv_bfloat16, kMxTensor);
+    else if (kind == kMxOneLevel) FP8K_QMX(__nv_bfloat16, kMxOneLevel);
+    else FP8K_QMX(__nv_bfloat16, kMxRow);
   } else {
-    if (amax != nullptr)
-      quant_mx_kernel<float, false><<<blocks, threads, 0, st>>>(
-          static_cast<const float *>(x), R, K, fmt, amax, global_out, q, local);
-    else
-      quant_mx_kernel<float, true><<<blocks, threads, 0, st>>>(
-          static_cast<const float *>(x), R, K, fmt, amax, global_out, q, local);
+    if (kind == kMxTensor) FP8K_QMX(float, kMxTensor);
+    else if (kind == kMxOneLevel) FP8K_QMX(float, kMxOneLevel);
+    else FP8K_QMX(float, kMxRow);
   }
+#undef FP8K_QMX
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- row amax --
+// amax_out[r] = max |x[r, :]|: one warp per row, 16-byte loads, the same
+// order-preserving keys as the tensor amax (exact).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    row_amax_kernel(const T *__restrict__ x, int64_t R, int64_t K, float *__restrict__ out) {
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t l = lane_id();
+  for (int64_t r = warp; r < R; r += nwarps) {
+    uint32_t key_a = 0, key_b = 0;
+    const T *row = x + r * K;
+    for (int64_t v = l; v < K / 8; v += 32) {
+      Raw8<T> raw;
+      raw.load_stream(row + v * 8);
+      raw.max_abs(key_a, key_b);
+    }
+    uint32_t key = Raw8<T>::merge_keys(key_a, key_b);
+    for (int64_t i = K / 8 * 8 + l; i < K; i += 32) key = max(key, abs_key(load1(row + i)));
+    key = warp_max_u32(key);
+    if (l == 0) out[r] = __uint_as_float(key);
+  }
+}
+
+cudaError_t launch_row_amax(const void *x, int in_dt, int64_t R, int64_t K, float *out, int sms,
+                            cudaStream_t st) {
+  const int threads = 256, blocks = grid_for(R * 32, threads, 8, sms);
+  if (in_dt == 0)
+    row_amax_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(x), R, K, out);
+  else
+    row_amax_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float *>(x), R, K, out);
   return cudaGetLastError();
 }
 

@@ -193,6 +193,22 @@ FP8_API int fp8_quantize_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
                     const float *amax, float *global_out, uint8_t *q, uint32_t *local,
                     fp8_stream_t stream);
 
+/* ---------------------------------- quantize mx, per-row global factor --
+ * The two-level scheme with the global factor of step 2 taken per row (the
+ * page's garbled extent "整个 _ 范围" read per row; [MOSS] 4): row r's
+ * S_r = fl32(max |x[r,:]| / MAX) (= max over its 1x32 blocks of s_i) and its
+ * local factors r_i = 2^ceil(log2(s_i / S_r)).  fp8_amax_rows gives the row
+ * amaxes; fp8_quantize_mx_rows quantizes with them and writes S_r to
+ * global_out[r]; the codes and local words have fp8_quantize_mx's layout.
+ *   amax_out / amax_rows / global_out  device fp32 [R].  K % 8 == 0 for
+ *   fp8_amax_rows, K % 128 == 0 for fp8_quantize_mx_rows.
+ */
+FP8_API int fp8_amax_rows(const void *x, int in_dt, int64_t R, int64_t K, float *amax_out,
+                          fp8_stream_t stream);
+FP8_API int fp8_quantize_mx_rows(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
+                                 const float *amax_rows, float *global_out, uint8_t *q,
+                                 uint32_t *local, fp8_stream_t stream);
+
 /* ------------------------------------------------- quantize mx, one level --
  * fp8_quantize_mx1: plain MXFP8 ([MOSS] 1): every 32 consecutive values of a
  * row share one power-of-two scale, the smallest not below amax_i / MAX
@@ -266,6 +282,9 @@ typedef struct {
   int64_t ldc;
   int a_layout;   /* fp8_layout_t */
   int b_layout;   /* fp8_layout_t */
+  const float *bias; /* nullable device fp32 [N]: C = result + bias[n] ([Nano]
+                        "实现": the linear's bias; added in fp32 before the
+                        output cast; with accumulate, C += result + bias) */
 } fp8_gemm_problem_t;
 
 FP8_API int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count,
@@ -317,6 +336,22 @@ FP8_API int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, c
 FP8_API int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const uint8_t *b,
                                    const void *sb, int sfmt, int64_t M, int64_t N, int64_t K,
                                    void *c, int64_t ldc, fp8_stream_t stream);
+
+/* fp8_gemm_group_bias: fp8_gemm_group plus an epilogue bias, C[m,n] =
+ * result + bias[n] (bias: device fp32 [N], added in fp32 before the bf16
+ * cast, in every path: promotion, block-scaled, split K).  bias == NULL is
+ * fp8_gemm_group. */
+FP8_API int fp8_gemm_group_bias(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
+                                int sfmt, int64_t M, int64_t N, int64_t K, const float *bias,
+                                void *c, int64_t ldc, fp8_stream_t stream);
+
+/* fp8_gemm_mx_rows: fp8_gemm_mx with per-row global factors (operands from
+ * fp8_quantize_mx_rows): C[m,n] = (ga[m] * gb[n]) * sum_i r_a r_b sum a.b;
+ * ga device fp32 [M], gb device fp32 [N]. */
+FP8_API int fp8_gemm_mx_rows(const uint8_t *a, const uint32_t *la, const float *ga,
+                             const uint8_t *b, const uint32_t *lb, const float *gb, int64_t M,
+                             int64_t N, int64_t K, int out_dt, void *c, int64_t ldc,
+                             fp8_stream_t stream);
 
 /* ------------------------------------- GEMM, per K group, MoE experts --
  * fp8_gemm_group_experts: the per-K-group GEMM of a mixture-of-experts layer

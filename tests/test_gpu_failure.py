@@ -28,10 +28,13 @@ def forced_timeout(fn):
     return F.fp8_get_last_device_error()
 
 
-@pytest.mark.parametrize("mnk", [(2048, 2048, 16384), (128, 256, 16384)])
+@pytest.mark.parametrize("mnk", [(2048, 2048, 16384), (128, 256, 65536)])
 def test_timeout_reported_then_context_usable(mnk):
-    """(2048, 2048) runs on CTA pairs, (128, 256) on one CTA per tile with
-    split K."""
+    """(2048, 2048) runs on CTA pairs, (128, 256) on one CTA per tile with K
+    split over a cluster.  A wait only runs out once it outlasts the
+    barrier's own suspend window (mbarrier.try_wait blocks for a while before
+    it reports "not yet"), so K is long enough that the epilogue waits for
+    many k blocks."""
     F = lib()
     m, n, k = mnk
     qa, sa, qb, sb = per_tensor_operands(m, n, k, "e4m3", "e4m3", seed=5)

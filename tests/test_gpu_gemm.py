@@ -493,3 +493,72 @@ def test_gemm_group_experts(sfmt, case):
     ok, worst = OG.check(out.float().cpu().numpy(), c, e, "bf16")
     assert ok, worst
     assert F.fp8_get_last_device_error()[0] == 0
+
+
+# ------------------------------------------------------------ epilogue bias --
+
+def _bias(n, seed):
+    return (workloads.normal((n,), 0.5, seed)).numpy().astype(np.float32)
+
+
+@pytest.mark.parametrize("mnk", [(2048, 2048, 1024), (200, 384, 1024), (16, 2048, 8192)])
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_gemm_tensor_bias(mnk, out_dtype):
+    """CTA-pair path, single-CTA path and the split-K cluster path, each with
+    a bias added in the epilogue."""
+    F = lib()
+    m, n, k = mnk
+    qa, sa, qb, sb = per_tensor_operands(m, n, k, "e4m3", "e4m3", seed=k + 11)
+    bias = _bias(n, m + 1)
+    out = torch.empty((m, n), dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float32,
+                      device="cuda")
+    a, b = dev_u8(qa), dev_u8(qb)
+    F.fp8_gemm_tensor_grouped([F.gemm_problem(a, F.E4M3, b, F.E4M3, dev_f32(sa), dev_f32(sb), out,
+                                              bias=torch.from_numpy(bias).cuda())])
+    torch.cuda.synchronize()
+    c, e = OG.gemm(OG.dequant_operand(qa, "e4m3", sa), OG.dequant_operand(qb, "e4m3", sb))
+    cb, eb, extra = OG.gemm_bias(c, e, bias)
+    ok, worst = OG.check(out.float().cpu().numpy(), cb, eb, out_dtype, extra=extra)
+    assert ok, worst
+
+
+@pytest.mark.parametrize("m", [1, 200, 2048])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_gemm_group_bias(m, sfmt):
+    F = lib()
+    n, k = 2048, 7168 if m == 1 else 2048
+    qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=m + 3)
+    c, e = group_reference(qa, sa, qb, sb, sfmt)
+    bias = _bias(n, m + 7)
+    out = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    code = F.SCALE_F32 if sfmt == "f32" else F.SCALE_UE8M0
+    F.fp8_gemm_group(dev_u8(qa), torch.from_numpy(np.ascontiguousarray(np.asarray(sa).T)).cuda(),
+                     dev_u8(qb), torch.from_numpy(np.ascontiguousarray(sb)).cuda(), code, out,
+                     bias=torch.from_numpy(bias).cuda())
+    torch.cuda.synchronize()
+    cb, eb, extra = OG.gemm_bias(c, e, bias)
+    ok, worst = OG.check(out.float().cpu().numpy(), cb, eb, "bf16", extra=extra)
+    assert ok, worst
+
+
+@pytest.mark.parametrize("mnk", [(256, 384, 512), (200, 1000, 1024), (16, 2048, 8192)])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_gemm_mx_per_row_global(mnk, out_dtype):
+    """Two-level operands with a global factor per row of A and per row of B
+    (per output column): the epilogue multiplies by S_a[m] * S_b[n].  The last
+    shape runs the split-K cluster path."""
+    F = lib()
+    m, n, k = mnk
+    a, b = workloads.two_level(seed=7, m=m, n=n, k=k)
+    af, bf = a.float().numpy(), b.float().numpy()
+    af[1] *= np.float32(2.0 ** -12)
+    qa, la, ga = OQ.quantize_two_level(af, "e4m3", global_per_row=True)
+    qb, lb, gb = OQ.quantize_two_level(bf, "e4m3", global_per_row=True)
+    out = torch.empty((m, n), dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float32,
+                      device="cuda")
+    F.fp8_gemm_mx_rows(dev_u8(qa), torch.from_numpy(mx_pack(la)).cuda(), dev_f32(ga), dev_u8(qb),
+                       torch.from_numpy(mx_pack(lb)).cuda(), dev_f32(gb), out)
+    torch.cuda.synchronize()
+    c, e = mx_reference(qa, la, ga, qb, lb, gb)
+    ok, worst = OG.check(out.float().cpu().numpy(), c, e, out_dtype)
+    assert ok, worst

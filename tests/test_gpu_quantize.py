@@ -446,3 +446,37 @@ def test_quantize_tensors_every_bf16_below_amax(fmt):
             ref_q, ref_s = OQ.quantize_tensor(xf, fmt)
             assert f32_bits(scale[j]) == f32_bits(ref_s), (i + j)
             assert np.array_equal(codes[j], ref_q), (i + j)
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_amax_rows(dt):
+    F = lib()
+    x = special_input((300, 520), 1.0, 17, dt, "e4m3")
+    x[7] = 0.0
+    out = torch.empty(300, device="cuda")
+    F.fp8_amax_rows(x.cuda(), out)
+    ref = np.max(np.abs(x.float().numpy()), axis=1).astype(np.float32)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("shape", [(1, 128), (130, 512), (333, 2048)])
+def test_two_level_per_row_global(shape):
+    F = lib()
+    r, k = shape
+    a, _ = workloads.two_level(m=r, n=8, k=k)
+    x = a.clone()
+    x[0, 32:64] = 0.0
+    if r > 3:
+        x[3] *= 2.0 ** -20     # a row far smaller than the others
+    xf = x.float().numpy()
+    xd = x.cuda()
+    am = torch.empty(r, device="cuda")
+    F.fp8_amax_rows(xd, am)
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    words = F.mx_local_words(r, k)
+    glob = torch.empty(r, device="cuda")
+    F.fp8_quantize_mx_rows(xd, 0, am, glob, q, words)
+    ref_q, ref_l, ref_s = OQ.quantize_two_level(xf, "e4m3", global_per_row=True)
+    assert np.array_equal(glob.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(to_np_u8(q), ref_q)
+    assert np.array_equal(mx_unpack(words.cpu().numpy(), r, k), ref_l)
