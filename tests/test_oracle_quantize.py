@@ -262,3 +262,29 @@ def test_two_level_per_row_is_row_scale_invariant():
     for i in range(1, 4):
         assert np.array_equal(q[i], q[0]) and np.array_equal(local[i], local[0])
     assert np.array_equal(big_s / big_s[2], np.float32([2.0 ** -12, 2.0 ** -3, 1.0, 2.0 ** 7]))
+
+
+def test_block_32x32_ue8m0_brute_force():
+    """(32, 32) weight blocks (Transformers fine-grained FP8, 八: a non-default
+    weight_block_size) with UE8M0 scales, against a loop over the blocks: each
+    block's byte is 127 + ceil(log2(fl32(block amax / 448))) (127 for an
+    all-zero block) and its codes are the block divided by that power of
+    two, with ragged edge blocks."""
+    w = workloads.normal((70, 96), 0.02, seed=37).numpy()
+    w[32:64, 32:64] = 0.0
+    w[5, 70] = 3.0
+    q, sc = Q.quantize_block(w, "e4m3", "ue8m0", block=32)
+    assert np.asarray(sc).shape == (3, 3)
+    for bi in range(3):
+        for bj in range(3):
+            blk = w[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32]
+            am = np.float32(np.max(np.abs(blk)))
+            if am == 0:
+                e = 0
+            else:
+                s = np.float32(am / np.float32(448.0))
+                e = int(np.ceil(np.log2(np.float64(s))))
+                assert 2.0 ** (e - 1) < s <= 2.0 ** e
+            assert int(np.asarray(sc)[bi, bj]) == 127 + e
+            ref = Q.quantize_with_scale(blk, np.float32(2.0 ** e), "e4m3")
+            assert np.array_equal(q[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32], ref)
