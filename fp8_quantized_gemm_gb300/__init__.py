@@ -42,6 +42,7 @@ _SIGS = {
     "fp8_quantize_block": [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp],
     "fp8_quantize_mx": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp],
     "fp8_quantize_mx1": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp],
+    "fp8_quantize_block32": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp, _vp],
     "fp8_dequantize_block": [_vp, _int, _vp, _int, _i64, _i64, _vp, _vp],
     "fp8_gemm_tensor": [_vp, _int, _vp, _int, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp],
     "fp8_gemm_group": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
@@ -153,6 +154,12 @@ def fp8_quantize_mx(x, fmt, amax, global_out, q, local, stream=None):
 def fp8_quantize_mx1(x, fmt, global_out, q, local, stream=None):
     r, k = x.shape
     _call("fp8_quantize_mx1", _p(x), _in_dt(x), r, k, fmt, _p(global_out), _p(q), _p(local),
+          _stream(stream))
+
+
+def fp8_quantize_block32(w, fmt, q, scales, local, stream=None):
+    n, k = w.shape
+    _call("fp8_quantize_block32", _p(w), _in_dt(w), n, k, fmt, _p(q), _p(scales), _p(local),
           _stream(stream))
 
 

@@ -418,6 +418,20 @@ int fp8_quantize_mx1(const void *x, int in_dt, int64_t R, int64_t K, int fmt, fl
                                          d->sms, (cudaStream_t)stream));
 }
 
+int fp8_quantize_block32(const void *w, int in_dt, int64_t N, int64_t K, int fmt, uint8_t *q,
+                         uint8_t *scales, uint32_t *local, fp8_stream_t stream) {
+  if (w == nullptr || q == nullptr || local == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || N >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (K % 128 != 0 || !aligned16(w) || !aligned16(q) || !aligned16(local))
+    return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_quant_block32(w, in_dt, N, K, fmt, q, scales, local, d->sms,
+                                              (cudaStream_t)stream));
+}
+
 int fp8_dequantize_block(const uint8_t *q, int fmt, const void *scales, int sfmt, int64_t N,
                          int64_t K, void *out, fp8_stream_t stream) {
   if (q == nullptr || scales == nullptr || out == nullptr || !valid_fmt(fmt))

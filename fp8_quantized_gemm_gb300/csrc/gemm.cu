@@ -68,7 +68,7 @@ struct Cfg {
   static_assert(BN % 32 == 0 && BN <= 256, "tile N");
 };
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int STAGES, bool EXPERTS>
 __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                 const GemmArgs args) {
@@ -130,10 +130,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   // Expert-grouped rows: a tile never spans two experts; expert e owns
   // ceil(rows_e / 128) * tiles_n consecutive tile indices.  One warp turns
   // the device offsets into that prefix (kept in shared memory) per CTA.
-  __shared__ int64_t ex_tile0[kMaxExperts + 1];
-  __shared__ int32_t ex_row0[kMaxExperts + 1];
-  const int E = args.experts;
-  if (E > 0) {
+  // The plain kernels compile this out (EXPERTS false).
+  __shared__ int64_t ex_tile0[EXPERTS ? kMaxExperts + 1 : 1];
+  __shared__ int32_t ex_row0[EXPERTS ? kMaxExperts + 1 : 1];
+  const int E = EXPERTS ? args.experts : 0;
+  if constexpr (EXPERTS) {
     if (warp == 0) {
       // lane l takes experts [8l, 8l + 8)
       int64_t cnt[8];
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     }
     __syncthreads();
   }
-  const int64_t num_tiles = E > 0 ? ex_tile0[E] : ((args.M + C::BM - 1) / C::BM) * tiles_n;
+  const int64_t num_tiles = EXPERTS ? ex_tile0[E] : ((args.M + C::BM - 1) / C::BM) * tiles_n;
   const int KB = (int)((args.K + C::BK - 1) / C::BK);
   // work unit u = (tile u % num_tiles, K split u / num_tiles); with ksplit 1
   // units are tiles.  Split s covers k blocks [s*KB/ks, (s+1)*KB/ks).
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   };
   auto tile_info = [&](int64_t t) {
     TileInfo ti;
-    if (E > 0) {
+    if constexpr (EXPERTS) {
       int lo = 0, hi = E;  // the expert e with ex_tile0[e] <= t < ex_tile0[e + 1]
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -599,11 +600,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int STAGES, bool EXPERTS = false>
 static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
                        int sms, cudaStream_t st) {
   using C = Cfg<MODE, BN, STAGES>;
-  auto kern = gemm_kernel<MODE, BN, STAGES>;
+  auto kern = gemm_kernel<MODE, BN, STAGES, EXPERTS>;
+  if (EXPERTS != (args.experts > 0)) return cudaErrorInvalidValue;
   // the shared-memory opt-in is set once per device (not inside a capture)
   static bool attr_done[64] = {};
   int dev = 0;
@@ -658,7 +660,7 @@ int gemm_tile_n(int mode, int64_t M) {
 template <int MODE, int BN, int STAGES>
 static int active_clusters(int size) {
   using C = Cfg<MODE, BN, STAGES>;
-  auto kern = gemm_kernel<MODE, BN, STAGES>;
+  auto kern = gemm_kernel<MODE, BN, STAGES, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) !=
       cudaSuccess)
     return 0;
@@ -722,10 +724,10 @@ int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster
 
 cudaError_t launch_gemm_experts(int mode, int bn, const CUtensorMap &tma, const CUtensorMap &tmb,
                                 const GemmArgs &args, int sms, cudaStream_t st) {
-  if (mode == kScaleGroupF32) return run<kScaleGroupF32, 128, 6>(tma, tmb, args, sms, st);
+  if (mode == kScaleGroupF32) return run<kScaleGroupF32, 128, 6, true>(tma, tmb, args, sms, st);
   if (mode != kScaleGroupUe8m0) return cudaErrorInvalidValue;
-  if (bn == 128) return run<kScaleGroupUe8m0, 128, 6>(tma, tmb, args, sms, st);
-  return run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, sms, st);
+  if (bn == 128) return run<kScaleGroupUe8m0, 128, 6, true>(tma, tmb, args, sms, st);
+  return run<kScaleGroupUe8m0, 256, 4, true>(tma, tmb, args, sms, st);
 }
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,

@@ -24,6 +24,9 @@ cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
                             int sms, cudaStream_t st, bool per_row = false);
 cudaError_t launch_row_amax(const void *x, int in_dt, int64_t R, int64_t K, float *out, int sms,
                             cudaStream_t st);
+cudaError_t launch_quant_block32(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
+                                 uint8_t *q, uint8_t *scales, uint32_t *local, int sms,
+                                 cudaStream_t st);
 cudaError_t launch_dequant_block(const uint8_t *q, int64_t N, int64_t K, int fmt, int sfmt,
                                  const void *scales, void *out, int sms, cudaStream_t st);
 cudaError_t launch_auto_scale(const float *amax0, double grow, int fmt, float *scale,

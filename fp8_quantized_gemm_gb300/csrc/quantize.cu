@@ -608,6 +608,80 @@ cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
   return cudaGetLastError();
 }
 
+// ------------------------------------------------- weight block 32 x 32 --
+// (32, 32) weight blocks with UE8M0 scales (Transformers fine-grained FP8,
+// 八: a non-default weight_block_size; 七: UE8M0 rounded up, quantize with
+// it).  One warp per block: lane l holds row n0 + l of the block.  Writes the
+// codes, the block bytes [ceil(N/32), K/32] (nullable) and, for every row,
+// the block byte of each 1x32 piece into the packed E8M0 word layout of the
+// two-level GEMM (rows past N up to R_pad get byte 127), so fp8_gemm_mx
+// contracts these weights with one-level MXFP8 activations directly.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    quant_block32_kernel(const T *__restrict__ w, int64_t N, int64_t K, int fmt,
+                         uint8_t *__restrict__ q, uint8_t *__restrict__ scales,
+                         uint32_t *__restrict__ local) {
+  const float mx = fmt_max(fmt);
+  const int64_t KB = K / 32, rpad = (N + 127) / 128 * 128;
+  const int64_t nblk = (rpad / 32) * KB;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t l = lane_id();
+  uint8_t *local8 = reinterpret_cast<uint8_t *>(local);
+  for (int64_t b = warp; b < nblk; b += nwarps) {
+    const int64_t bn = b / KB, bk = b % KB;
+    const int64_t n = bn * 32 + l, k0 = bk * 32;
+    const bool valid = n < N;
+    Raw8<T> raw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (valid)
+        raw[i].load_stream(w + n * K + k0 + 8 * i);
+      else
+        raw[i].zero();
+    }
+    uint32_t key_a = 0, key_b = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) raw[i].max_abs(key_a, key_b);
+    const uint32_t key = warp_max_u32(Raw8<T>::merge_keys(key_a, key_b));
+    const float amax = __uint_as_float(key);
+    int e = 0;
+    if (amax > 0.0f) e = min(max(ceil_log2_pos(__fdiv_rn(amax, mx)), -127), 127);
+    const uint8_t byte = (uint8_t)(e + 127);
+    if (l == 0 && scales != nullptr && bn * 32 < N) scales[bn * KB + bk] = byte;
+    // this row's byte in the packed word of (row n, 128-wide slice k0 / 128)
+    local8[4 * mx_word_index(n, k0 / 128, rpad) + (k0 % 128) / 32] = valid ? byte : (uint8_t)127;
+    if (valid) {
+      const ScaleDiv d(exp2_int(e));
+      uint2 c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float x8[8], y8[8];
+        raw[i].decode(x8);
+        div8(d, x8, y8);
+        c[i] = pack8(fmt, y8);
+      }
+      uint4 *dst = reinterpret_cast<uint4 *>(q + n * K + k0);
+      dst[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+      dst[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+    }
+  }
+}
+
+cudaError_t launch_quant_block32(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
+                                 uint8_t *q, uint8_t *scales, uint32_t *local, int sms,
+                                 cudaStream_t st) {
+  const int64_t rpad = (N + 127) / 128 * 128;
+  const int threads = 256, blocks = grid_for((rpad / 32) * (K / 32) * 32, threads, 8, sms);
+  if (in_dt == 0)
+    quant_block32_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(w), N, K, fmt, q, scales, local);
+  else
+    quant_block32_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float *>(w), N, K,
+                                                            fmt, q, scales, local);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------- row amax --
 // amax_out[r] = max |x[r, :]|: one warp per row, 16-byte loads, the same
 // order-preserving keys as the tensor amax (exact).

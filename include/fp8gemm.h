@@ -220,6 +220,26 @@ FP8_API int fp8_quantize_mx_rows(const void *x, int in_dt, int64_t R, int64_t K,
 FP8_API int fp8_quantize_mx1(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
                      float *global_out, uint8_t *q, uint32_t *local, fp8_stream_t stream);
 
+/* ------------------------------------------- quantize 32x32 blocks --
+ * fp8_quantize_block32: weight blocks of 32 x 32 with UE8M0 scales ([HF] 八:
+ * weight_block_size is configurable; 七: the scale amax / MAX is rounded UP
+ * to a power of two and the block is quantized with the rounded scale).
+ * Block (i, j) covers rows [32i, 32i + 32) and columns [32j, 32j + 32) of
+ * w [N, K]; its exponent e = ceil(log2(fl32(amax / MAX))) clamped to
+ * [-127, 127] (byte 127 for an all-zero block).
+ *   w       [N, K] bf16 or fp32, 16-byte aligned; K % 128 == 0.
+ *   q       [N, K] uint8 codes, 16-byte aligned.
+ *   scales  nullable; uint8 [ceil(N/32), K/32] block bytes.
+ *   local   every row's block byte for each 1x32 piece, in fp8_quantize_mx's
+ *           packed E8M0 word layout (R = N; padding rows hold 127 bytes), so
+ *           that fp8_gemm_mx contracts these weights with fp8_quantize_mx1
+ *           activations (both global factors 1.0).  16-byte aligned,
+ *           4 * (K/128) * R_pad bytes.
+ */
+FP8_API int fp8_quantize_block32(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
+                                 uint8_t *q, uint8_t *scales, uint32_t *local,
+                                 fp8_stream_t stream);
+
 /* --------------------------------------------------- dequantize block --
  * fp8_dequantize_block: out[n,k] = decode(q[n,k]) * scale of block
  * (n/128, k/128), rounded to bf16 ([HF] 五: dequantize=True folds the block

@@ -99,6 +99,20 @@ def test_quantize_validation(lib):
     assert d(16, 16, 16, 1 << 20, 0, None) == -1
 
 
+def test_quantize_block32_validation(lib):
+    f = lib.fp8_quantize_block32
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int] + \
+        [ctypes.c_void_p] * 4
+    assert f(None, 0, 64, 128, 0, 16, None, 16, None) == -1   # no input
+    assert f(16, 0, 64, 128, 0, 16, None, None, None) == -1   # no MX words
+    assert f(16, 2, 64, 128, 0, 16, None, 16, None) == -1     # bad input dtype
+    assert f(16, 0, 64, 128, 3, 16, None, 16, None) == -1     # bad format
+    assert f(16, 0, 0, 128, 0, 16, None, 16, None) == -1      # empty
+    assert f(16, 0, 64, 96, 0, 16, None, 16, None) == -2      # K % 128
+    assert f(24, 0, 64, 128, 0, 16, None, 16, None) == -2     # misaligned weights
+    assert f(16, 0, 64, 128, 0, 16, None, 20, None) == -2     # misaligned words
+
+
 def _grouped(lib, **kw):
     import fp8_quantized_gemm_gb300 as F
     p = dict(a=16, b=16, sa=16, sb=16, M=128, N=128, K=128, fa=0, fb=0, out_dt=1, accumulate=0,

@@ -185,6 +185,43 @@ def test_gemm_mx(mnk, out_dtype):
     assert ok, worst
 
 
+@pytest.mark.parametrize("mnk", [(128, 256, 256), (200, 300, 512), (1, 128, 128), (4096, 2048, 7168)])
+def test_gemm_mxfp8_by_block32_weights(mnk):
+    """One-level MXFP8 activations (1x32 power-of-two scales) times (32, 32)
+    UE8M0 weight blocks, both quantized on the GPU and contracted by the
+    block-scaled GEMM with unit global factors; the oracle dequantizes with
+    its own quantizers' scales.  The large case is checked on sampled
+    outputs."""
+    F = lib()
+    m, n, k = mnk
+    a, w = workloads.fine_grained(m, k=k, n=n)
+    af, wf = a.float().numpy(), w.float().numpy()
+    qa = torch.empty((m, k), dtype=torch.uint8, device="cuda")
+    la = F.mx_local_words(m, k)
+    ga = torch.zeros(1, device="cuda")
+    F.fp8_quantize_mx1(a.cuda(), 0, ga, qa, la)
+    qb = torch.empty((n, k), dtype=torch.uint8, device="cuda")
+    lb = F.mx_local_words(n, k)
+    F.fp8_quantize_block32(w.cuda(), 0, qb, None, lb)
+    gb = torch.ones(1, device="cuda")
+    out = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    F.fp8_gemm_mx(qa, la, ga, qb, lb, gb, out)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy()
+    rq_a, rl_a = OQ.quantize_mxfp8(af, "e4m3")
+    rq_b, rs_b = OQ.quantize_block(wf, "e4m3", "ue8m0", block=32)
+    a_deq = OG.dequant_operand(rq_a, "e4m3", OQ.expand(OQ.group_scale_values(rl_a, "ue8m0"), m, k, 1, 32))
+    b_deq = OG.dequant_operand(rq_b, "e4m3", OQ.expand(OQ.group_scale_values(rs_b, "ue8m0"), n, k, 32, 32))
+    if m * n * k > 1 << 30:
+        rows, cols = sample_positions(m, n, 256, seed=9)
+        c, e = OG.gemm_sampled(a_deq, b_deq, rows, cols)
+        ok, worst = OG.check(got[rows, cols], c, e, "bf16")
+    else:
+        c, e = OG.gemm(a_deq, b_deq)
+        ok, worst = OG.check(got, c, e, "bf16")
+    assert ok, worst
+
+
 def test_gemm_mx_distinct_local_factors():
     """Every 1x32 block of both operands gets its own power-of-two factor, so a
     factor applied to the wrong block or row shows up."""

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import workloads
-from gpu_util import FMT, f32_bits, lib, mx_unpack, to_np_u8
+from gpu_util import FMT, f32_bits, lib, mx_pack, mx_unpack, to_np_u8
 from oracle import delayed as OD
 from oracle import quantize as OQ
 
@@ -224,6 +224,44 @@ def test_mxfp8_one_level(shape):
     assert glob.item() == 1.0
     assert np.array_equal(to_np_u8(q), ref_q)
     assert np.array_equal(mx_unpack(words.cpu().numpy(), r, k), ref_l)
+
+
+@pytest.mark.parametrize("shape", [(32, 128), (200, 384), (2048, 7168)])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float32])
+def test_quantize_block32(shape, fmt, in_dtype):
+    """(32, 32) UE8M0 weight blocks: codes and block bytes bit-exact against
+    the oracle; the MX words hold each row's block bytes (127 for padding
+    rows).  An all-zero block and a tiny block exercise byte 127 and a
+    negative exponent."""
+    F = lib()
+    n, k = shape
+    _, w = workloads.fine_grained(1, k=k, n=n)
+    w = w.to(in_dtype)
+    w[:32, 32:64] = 0.0
+    w[(n - 1) // 32 * 32:, -32:] *= 1e-28  # the last block: exponent near -100
+    wf = w.float().numpy()
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(((n + 31) // 32, k // 32), dtype=torch.uint8, device="cuda")
+    words = F.mx_local_words(n, k)
+    F.fp8_quantize_block32(w.cuda(), FMT[fmt], q, sc, words)
+    ref_q, ref_s = OQ.quantize_block(wf, fmt, "ue8m0", block=32)
+    assert np.array_equal(to_np_u8(q), ref_q)
+    assert np.array_equal(to_np_u8(sc), ref_s)
+    per_row = np.repeat(ref_s, 32, axis=0)[:n]
+    assert np.array_equal(words.cpu().numpy().view(np.uint32), mx_pack(per_row).view(np.uint32))
+
+
+def test_quantize_block32_without_block_bytes():
+    F = lib()
+    _, w = workloads.fine_grained(1, k=256, n=96)
+    q = torch.empty((96, 256), dtype=torch.uint8, device="cuda")
+    words = F.mx_local_words(96, 256)
+    F.fp8_quantize_block32(w.cuda(), 0, q, None, words)
+    ref_q, ref_s = OQ.quantize_block(w.float().numpy(), "e4m3", "ue8m0", block=32)
+    assert np.array_equal(to_np_u8(q), ref_q)
+    assert np.array_equal(mx_unpack(words.cpu().numpy(), 96, 256),
+                          np.repeat(ref_s, 32, axis=0)[:96])
 
 
 @pytest.mark.parametrize("shape", [(200, 272), (2048, 7168)])
