@@ -143,11 +143,26 @@ __device__ __forceinline__ float load1<__nv_bfloat16>(const __nv_bfloat16 *p) {
 template <>
 __device__ __forceinline__ float load1<float>(const float *p) { return *p; }
 
+// Two values -> two codes of the format F (0 E4M3, 1 E5M2), fixed at compile
+// time so that the hot loops issue one conversion per pair.
+template <int F>
+__device__ __forceinline__ uint32_t cvt8x2(float lo, float hi) {
+  if constexpr (F == 0)
+    return cvt_e4m3x2(lo, hi);
+  else
+    return cvt_e5m2x2(lo, hi);
+}
+
 // 8 values -> 8 codes packed little-endian into a uint2.
+template <int F>
+__device__ __forceinline__ uint2 pack8(const float (&y)[8]) {
+  const uint32_t c0 = cvt8x2<F>(y[0], y[1]), c1 = cvt8x2<F>(y[2], y[3]);
+  const uint32_t c2 = cvt8x2<F>(y[4], y[5]), c3 = cvt8x2<F>(y[6], y[7]);
+  return make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
+}
+// the same with the format chosen at run time (cold paths)
 __device__ __forceinline__ uint2 pack8(int fmt, const float (&y)[8]) {
-  const uint32_t c0 = cvt_fp8x2(fmt, y[0], y[1]), c1 = cvt_fp8x2(fmt, y[2], y[3]);
-  const uint32_t c2 = cvt_fp8x2(fmt, y[4], y[5]), c3 = cvt_fp8x2(fmt, y[6], y[7]);
-  return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+  return fmt == 0 ? pack8<0>(y) : pack8<1>(y);
 }
 
 // Eight quotients v[j] / s by one scale (ScaleDiv; the fast/slow choice is
@@ -179,24 +194,119 @@ __device__ __forceinline__ void block_max_to(uint32_t key, uint32_t *dst) {
 // quotient, the saturating cast, then each element's sign put into its code
 // (a zero or underflowed quotient becomes +-0 with the sign of x, as the
 // IEEE quotient would).
-template <typename T>
-__device__ __forceinline__ uint2 quant8_own_scale(const Raw8<T> &r, int fmt, const ScaleDiv &d) {
+template <int F, typename T>
+__device__ __forceinline__ uint2 quant8_own_scale(const Raw8<T> &r, const ScaleDiv &d) {
   float x[8], y[8];
   r.decode(x);
 #pragma unroll
   for (int j = 0; j < 8; j += 2) div_by_scale2_bounded(x[j], x[j + 1], d.ns2, d.y2, y[j], y[j + 1]);
-  const uint2 c = pack8(fmt, y);
+  const uint2 c = pack8<F>(y);
   const uint2 sg = r.code_signs();
   return make_uint2(c.x | sg.x, c.y | sg.y);
 }
 
 // The same codes through IEEE division (scales outside the fast range).
-template <typename T>
-__device__ __forceinline__ uint2 quant8_ieee(const Raw8<T> &r, int fmt, const ScaleDiv &d) {
+template <int F, typename T>
+__device__ __forceinline__ uint2 quant8_ieee(const Raw8<T> &r, const ScaleDiv &d) {
   float x[8], y[8];
   r.decode(x);
   d.div8<false>(x, y);
-  return pack8(fmt, y);
+  return pack8<F>(y);
+}
+
+// Codes of eight elements divided by a power-of-two scale s = 2^e, given as
+// the packed pair {2^-e, 2^-e}: the reciprocal of a power of two is exact,
+// so x * 2^-e rounds the same real number as x / s, once.
+template <int F, typename T>
+__device__ __forceinline__ uint2 quant8_pow2(const Raw8<T> &r, uint64_t inv2) {
+  float x[8], y[8];
+  r.decode(x);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) f32x2_unpack(f32x2_mul(f32x2_pack(x[j], x[j + 1]), inv2), y[j], y[j + 1]);
+  return pack8<F>(y);
+}
+
+// A lane's run of 32 consecutive elements of one row (four Raw8 vectors),
+// for the kernels where each lane owns whole scale blocks (1x32) or a
+// quarter of one (1x128).  Vectors at or past the row's end K read as zero
+// and are not stored (K % 16 == 0, so each 16-element half is whole).
+template <typename T>
+struct Run32 {
+  Raw8<T> v[4];
+  __device__ __forceinline__ void load(const T *row, int64_t k, int64_t K) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (k + 8 * i < K)
+        v[i].load_stream(row + k + 8 * i);
+      else
+        v[i].zero();
+    }
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i].zero();
+  }
+  // max |x| of the 32 elements as an fp32 bit pattern
+  __device__ __forceinline__ uint32_t max_key() const {
+    uint32_t key_a = 0, key_b = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i].max_abs(key_a, key_b);
+    return Raw8<T>::merge_keys(key_a, key_b);
+  }
+  // codes of the 32 elements divided by the power-of-two scale 1 / inv
+  // (inv = 2^-e exactly, so the product is the correctly rounded quotient),
+  // stored at row_q + k
+  template <int F>
+  __device__ __forceinline__ void quant_store_pow2(uint8_t *row_q, int64_t k, int64_t K,
+                                                   float inv) const {
+    const uint64_t inv2 = f32x2_pack(inv, inv);
+    uint2 c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = quant8_pow2<F>(v[i], inv2);
+    if (k < K) *reinterpret_cast<uint4 *>(row_q + k) = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+    if (k + 16 < K)
+      *reinterpret_cast<uint4 *>(row_q + k + 16) = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+  }
+  // codes of the 32 elements divided by d.s (a scale formed from an amax
+  // that covers them), stored at row_q + k
+  template <int F>
+  __device__ __forceinline__ void quant_store(uint8_t *row_q, int64_t k, int64_t K,
+                                              const ScaleDiv &d) const {
+    uint2 c[4];
+    if (d.fast) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = quant8_own_scale<F>(v[i], d);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = quant8_ieee<F>(v[i], d);
+    }
+    if (k < K) *reinterpret_cast<uint4 *>(row_q + k) = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+    if (k + 16 < K)
+      *reinterpret_cast<uint4 *>(row_q + k + 16) = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+  }
+};
+
+// Codes of eight elements divided by a scale formed from the amax of a block
+// that contains them (so |x / s| stays within the format's range): the packed
+// bounded quotient when the scale is in the fast range, IEEE division
+// otherwise (tiny or huge scales; a NaN amax).
+template <int F, typename T>
+__device__ __forceinline__ uint2 quant8_block(const Raw8<T> &r, const ScaleDiv &d) {
+  return d.fast ? quant8_own_scale<F>(r, d) : quant8_ieee<F>(r, d);
+}
+
+// task -> (row, column task) of a row-major task space with `per_row` tasks
+// per row; `narrow` (the whole space below 2^32) takes the 32-bit division.
+__device__ __forceinline__ void split_task(int64_t task, int64_t per_row, bool narrow,
+                                           int64_t &row, int64_t &col) {
+  if (narrow) {
+    const uint32_t t = (uint32_t)task, d = (uint32_t)per_row, r = t / d;
+    row = r;
+    col = t - r * d;
+  } else {
+    row = task / per_row;
+    col = task - row * per_row;
+  }
 }
 
 }  // namespace fp8k

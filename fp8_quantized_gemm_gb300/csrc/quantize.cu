@@ -51,8 +51,8 @@ __device__ __forceinline__ float resolve_scale(const float *amax_in, const float
 
 // Row-major output only: grid-stride over 8-element vectors.  kFast selects
 // the reciprocal-based quotient (ScaleDiv), checked once per launch.
-template <typename T, bool kAmax, bool kFast>
-__device__ __forceinline__ void quant_tensor_body(const T *__restrict__ x, int64_t n, int fmt,
+template <typename T, int F, bool kAmax, bool kFast>
+__device__ __forceinline__ void quant_tensor_body(const T *__restrict__ x, int64_t n,
                                                   const ScaleDiv &d, uint8_t *__restrict__ q,
                                                   uint32_t &key) {
   const int64_t nvec = n / 8;
@@ -74,7 +74,7 @@ __device__ __forceinline__ void quant_tensor_body(const T *__restrict__ x, int64
         for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
       }
       d.div8<kFast>(v, y);
-      reinterpret_cast<uint2 *>(q)[i + u * stride] = pack8(fmt, y);
+      reinterpret_cast<uint2 *>(q)[i + u * stride] = pack8<F>(y);
     }
   }
   for (; i < nvec; i += stride) {
@@ -85,24 +85,24 @@ __device__ __forceinline__ void quant_tensor_body(const T *__restrict__ x, int64
       for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
     }
     d.div8<kFast>(v, y);
-    reinterpret_cast<uint2 *>(q)[i] = pack8(fmt, y);
+    reinterpret_cast<uint2 *>(q)[i] = pack8<F>(y);
   }
 }
 
-template <typename T, bool kAmax>
+template <typename T, int F, bool kAmax>
 __global__ void __launch_bounds__(256, kAmax ? 3 : 4)
-    quant_tensor_kernel(const T *__restrict__ x, int64_t n, int fmt, const float *amax_in,
+    quant_tensor_kernel(const T *__restrict__ x, int64_t n, const float *amax_in,
                         const float *scale_in, float *scale_out, uint8_t *__restrict__ q,
                         uint32_t *amax_out) {
-  const float mx = fmt_max(fmt);
+  const float mx = fmt_max(F);
   const float s = resolve_scale(amax_in, scale_in, mx);
   if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
   const ScaleDiv d(s);
   uint32_t key = 0;
   if (d.fast)
-    quant_tensor_body<T, kAmax, true>(x, n, fmt, d, q, key);
+    quant_tensor_body<T, F, kAmax, true>(x, n, d, q, key);
   else
-    quant_tensor_body<T, kAmax, false>(x, n, fmt, d, q, key);
+    quant_tensor_body<T, F, kAmax, false>(x, n, d, q, key);
   if (kAmax) block_max_to(key, amax_out);
 }
 
@@ -141,9 +141,9 @@ __device__ __forceinline__ void transpose8x8(const uint64_t (&r)[8], uint64_t (&
   }
 }
 
-template <typename T, bool kAmax, bool kFast>
+template <typename T, int F, bool kAmax, bool kFast>
 __device__ __forceinline__ void quant_tensor_t_body(const T *__restrict__ x, int64_t rows,
-                                                    int64_t cols, int fmt, const ScaleDiv &d,
+                                                    int64_t cols, const ScaleDiv &d,
                                                     uint8_t *__restrict__ q,
                                                     uint8_t *__restrict__ qt, uint8_t *tile,
                                                     uint32_t &key) {
@@ -199,7 +199,7 @@ __device__ __forceinline__ void quant_tensor_t_body(const T *__restrict__ x, int
         for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
       }
       d.div8<kFast>(v, y);
-      const uint2 packed = pack8(fmt, y);
+      const uint2 packed = pack8<F>(y);
       if (r < rows && c < cols) *reinterpret_cast<uint2 *>(q + r * cols + c) = packed;
       *reinterpret_cast<uint2 *>(&tile[lr * kTPitch + tchunk(lr, lc >> 3)]) = packed;
     }
@@ -234,75 +234,76 @@ __device__ __forceinline__ void quant_tensor_t_body(const T *__restrict__ x, int
   }
 }
 
-template <typename T, bool kAmax>
+template <typename T, int F, bool kAmax>
 __global__ void __launch_bounds__(256, 2)
-    quant_tensor_t_kernel(const T *__restrict__ x, int64_t rows, int64_t cols, int fmt,
+    quant_tensor_t_kernel(const T *__restrict__ x, int64_t rows, int64_t cols,
                           const float *amax_in, const float *scale_in, float *scale_out,
                           uint8_t *__restrict__ q, uint8_t *__restrict__ qt,
                           uint32_t *amax_out) {
   __shared__ __align__(16) uint8_t tile[kTT * kTPitch];
-  const float mx = fmt_max(fmt);
+  const float mx = fmt_max(F);
   const float s = resolve_scale(amax_in, scale_in, mx);
   if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
   const ScaleDiv d(s);
   uint32_t key = 0;
   if (d.fast)
-    quant_tensor_t_body<T, kAmax, true>(x, rows, cols, fmt, d, q, qt, tile, key);
+    quant_tensor_t_body<T, F, kAmax, true>(x, rows, cols, d, q, qt, tile, key);
   else
-    quant_tensor_t_body<T, kAmax, false>(x, rows, cols, fmt, d, q, qt, tile, key);
+    quant_tensor_t_body<T, F, kAmax, false>(x, rows, cols, d, q, qt, tile, key);
   if (kAmax) block_max_to(key, amax_out);
 }
 
 // --------------------------------------------------- token group (1x128) --
-// One warp per (row, pair of 128-wide K groups); lane l holds elements
-// [8l, 8l+8) of the 256-wide window, so lanes 0-15 form group 2p and lanes
-// 16-31 group 2p+1.
-template <typename T>
-__global__ void __launch_bounds__(256)
-    quant_group_kernel(const T *__restrict__ x, int64_t M, int64_t K, int fmt, int sfmt,
+// One warp per (row, 1024-wide window of K): lane l owns the 32 elements
+// [32l, 32l + 32) of the window, so four lanes form a 1x128 group (lanes
+// 4c..4c+3: group 8w + c of window w) and each lane forms its group's scale
+// once for 32 elements.  Each warp takes kU windows at once (w, w + W, ...,
+// W warps in the grid) and issues all their loads first.
+template <typename T, int F>
+__global__ void __launch_bounds__(256, 3)
+    quant_group_kernel(const T *__restrict__ x, int64_t M, int64_t K, int sfmt,
                        uint8_t *__restrict__ q, void *scales) {
-  const float mx = fmt_max(fmt);
-  const int64_t G = (K + 127) / 128, pairs = (G + 1) / 2;
+  constexpr int kU = sizeof(T) == 2 ? 2 : 1;
+  const float mx = fmt_max(F);
+  const int64_t G = (K + 127) / 128, wins = (K + 1023) / 1024, ntasks = M * wins;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const bool narrow = ntasks + kU * nwarps <= (int64_t)0xFFFFFFFFu;
   const uint32_t l = lane_id();
-  for (int64_t task = warp; task < M * pairs; task += nwarps) {
-    const int64_t m = task / pairs, p = task % pairs;
-    const int64_t k = p * 256 + l * 8;
-    float v[8];
-    const bool valid = k < K;
-    if (valid) {
-      Vec8<T>::load_stream(x + m * K + k, v);
-    } else {
+  for (int64_t base = warp; base < ntasks; base += kU * nwarps) {
+    Run32<T> run[kU];
+    int64_t row[kU], col[kU];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-    }
-    uint32_t key = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
-    const float amax = __uint_as_float(key);
-    float s = scale_from_amax(amax, mx);
-    uint8_t e8 = 127;
-    if (sfmt == 1 && amax > 0.0f) {
-      const int e = min(max(ceil_log2_pos(s), -127), 127);
-      s = exp2_int(e);
-      e8 = (uint8_t)(e + 127);
-    } else if (sfmt == 1) {
-      s = 1.0f;
-    }
-    const int64_t g = p * 2 + (l >> 4);
-    if ((l & 15) == 0 && g < G) {
-      if (sfmt == 0)
-        reinterpret_cast<float *>(scales)[g * M + m] = s;
+    for (int u = 0; u < kU; ++u) {
+      const int64_t task = base + u * nwarps;
+      int64_t w;
+      split_task(task, wins, narrow, row[u], w);
+      col[u] = w * 1024 + l * 32;
+      if (task < ntasks)
+        run[u].load(x + row[u] * K, col[u], K);
       else
-        reinterpret_cast<uint8_t *>(scales)[g * M + m] = e8;
+        run[u].zero();
     }
-    if (valid) {
-      float y[8];
-      div8(ScaleDiv(s), v, y);
-      *reinterpret_cast<uint2 *>(q + m * K + k) = pack8(fmt, y);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (base + u * nwarps >= ntasks) break;  // warp-uniform
+      const int64_t m = row[u], k = col[u];
+      uint32_t key = run[u].max_key();
+      key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
+      key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
+      const float amax = __uint_as_float(key);
+      const int64_t g = k >> 7;
+      const bool scale_lane = (l & 3) == 0 && g < G;
+      if (sfmt == 0) {
+        const float s = scale_from_amax(amax, mx);
+        if (scale_lane) reinterpret_cast<float *>(scales)[g * M + m] = s;
+        run[u].template quant_store<F>(q + m * K, k, K, ScaleDiv(s));
+      } else {
+        // UE8M0: 2^e, e = ceil(log2(fl32(amax / MAX))); 1.0 for a zero group
+        const int e = amax > 0.0f ? min(max(ceil_log2_pos(__fdiv_rn(amax, mx)), -127), 127) : 0;
+        if (scale_lane) reinterpret_cast<uint8_t *>(scales)[g * M + m] = (uint8_t)(e + 127);
+        run[u].template quant_store_pow2<F>(q + m * K, k, K, exp2_int(-e));
+      }
     }
   }
 }
@@ -393,69 +394,77 @@ __device__ __forceinline__ int64_t mx_word_index(int64_t r, int64_t g, int64_t r
 //   kMxRow      two level with a global factor per row: S_r = fl32(row amax /
 //               MAX) from amax_in[r], written to global_out[r].
 constexpr int kMxTensor = 0, kMxOneLevel = 1, kMxRow = 2;
-template <typename T, int kGlobal>
-__global__ void __launch_bounds__(256)
-    quant_mx_kernel(const T *__restrict__ x, int64_t R, int64_t K, int fmt,
+// One warp per (row, 1024-wide window of K): lane l owns the 1x32 block
+// 32w + l of the row (elements [32l, 32l + 32) of window w), so each lane
+// forms one block's factor for its 32 elements; lanes 4c..4c+3 hold the four
+// bytes of one packed word.  Rows are padded to a multiple of 128 (padding
+// rows only write their words).  kU windows per warp at once, loads first.
+template <typename T, int kGlobal, int F>
+__global__ void __launch_bounds__(256, 3)
+    quant_mx_kernel(const T *__restrict__ x, int64_t R, int64_t K,
                     const float *amax_in, float *global_out, uint8_t *__restrict__ q,
                     uint32_t *__restrict__ local) {
   constexpr bool kOneLevel = kGlobal == kMxOneLevel;
-  const float mx = fmt_max(fmt);
+  constexpr int kU = sizeof(T) == 2 ? 2 : 1;
+  const float mx = fmt_max(F);
   // two level: S == max_i fl32(amax_i / MAX)
   const float S_tensor = kGlobal == kMxTensor ? scale_from_amax(*amax_in, mx) : 1.0f;
   if (kGlobal != kMxRow && global_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
     *global_out = S_tensor;
-  const int64_t G = K / 128, pairs = (G + 1) / 2;
-  const int64_t rpad = (R + 127) / 128 * 128;
+  const int64_t G = K / 128, wins = (K + 1023) / 1024;
+  const int64_t rpad = (R + 127) / 128 * 128, ntasks = rpad * wins;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const bool narrow = ntasks + kU * nwarps <= (int64_t)0xFFFFFFFFu;
   const uint32_t l = lane_id();
-  for (int64_t task = warp; task < rpad * pairs; task += nwarps) {
-    const int64_t r = task / pairs, p = task % pairs;
-    const int64_t g = p * 2 + (l >> 4);
-    const int64_t k = p * 256 + l * 8;
-    if (r >= R) {  // padding rows: factor 1 (byte 127)
-      if ((l & 15) == 0 && g < G) local[mx_word_index(r, g, rpad)] = 0x7F7F7F7Fu;
-      continue;
-    }
-    float S = S_tensor;
-    if constexpr (kGlobal == kMxRow) {
-      S = scale_from_amax(amax_in[r], mx);
-      if (p == 0 && l == 0 && global_out != nullptr) global_out[r] = S;
-    }
-    const bool valid = k < K;
-    float v[8];
-    if (valid) {
-      Vec8<T>::load_stream(x + r * K + k, v);
-    } else {
+  for (int64_t base = warp; base < ntasks; base += kU * nwarps) {
+    Run32<T> run[kU];
+    int64_t row[kU], col[kU];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+    for (int u = 0; u < kU; ++u) {
+      const int64_t task = base + u * nwarps;
+      int64_t w;
+      split_task(task, wins, narrow, row[u], w);
+      col[u] = w * 1024 + l * 32;
+      if (task < ntasks && row[u] < R)
+        run[u].load(x + row[u] * K, col[u], K);
+      else
+        run[u].zero();
     }
-    uint32_t key = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) key = max(key, abs_key(v[j]));
-    key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
-    key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
-    const float amax_i = __uint_as_float(key);
-    const float s_i = __fdiv_rn(amax_i, mx);     // step 1
-    int e = 0;
-    if (kOneLevel) {
-      if (s_i > 0.0f) e = min(max(ceil_log2_pos(s_i), -127), 127);
-    } else if (s_i > 0.0f) {
-      const float ratio = __fdiv_rn(s_i, S);     // step 3
-      e = ratio > 0.0f ? max(ceil_log2_pos(ratio), -127) : -127;
+    for (int u = 0; u < kU; ++u) {
+      if (base + u * nwarps >= ntasks) break;  // warp-uniform
+      const int64_t r = row[u], k = col[u], g = k >> 7;
+      const bool word_lane = (l & 3) == 0 && g < G;
+      if (r >= R) {  // padding rows: factor 1 (byte 127)
+        if (word_lane) local[mx_word_index(r, g, rpad)] = 0x7F7F7F7Fu;
+        continue;
+      }
+      float S = S_tensor;
+      if constexpr (kGlobal == kMxRow) {
+        S = scale_from_amax(amax_in[r], mx);
+        if (k == 0 && global_out != nullptr) global_out[r] = S;
+      }
+      const float amax_i = __uint_as_float(run[u].max_key());
+      const float s_i = __fdiv_rn(amax_i, mx);     // step 1
+      int e = 0;
+      if (kOneLevel) {
+        if (s_i > 0.0f) e = min(max(ceil_log2_pos(s_i), -127), 127);
+      } else if (s_i > 0.0f) {
+        const float ratio = __fdiv_rn(s_i, S);     // step 3
+        e = ratio > 0.0f ? max(ceil_log2_pos(ratio), -127) : -127;
+      }
+      if (kOneLevel)
+        run[u].template quant_store_pow2<F>(q + r * K, k, K, exp2_int(-e));
+      else
+        run[u].template quant_store<F>(q + r * K, k, K, ScaleDiv(S * exp2_int(e)));  // step 4: S * r_i
+      // the four block bytes of a 128-wide slice into one word
+      const uint32_t b = (uint32_t)(e + 127) & 0xFFu;
+      const uint32_t b1 = __shfl_down_sync(0xffffffffu, b, 1);
+      const uint32_t b2 = __shfl_down_sync(0xffffffffu, b, 2);
+      const uint32_t b3 = __shfl_down_sync(0xffffffffu, b, 3);
+      if (word_lane) local[mx_word_index(r, g, rpad)] = b | (b1 << 8) | (b2 << 16) | (b3 << 24);
     }
-    const float eff = S * exp2_int(e);           // step 4: S * r_i
-    if (valid) {
-      float y[8];
-      div8(ScaleDiv(eff), v, y);
-      *reinterpret_cast<uint2 *>(q + r * K + k) = pack8(fmt, y);
-    }
-    // gather the four block bytes of each 128-wide slice into one word
-    uint32_t b = (uint32_t)(e + 127) & 0xFFu;
-    const uint32_t b1 = __shfl_down_sync(0xffffffffu, b, 4);
-    const uint32_t b2 = __shfl_down_sync(0xffffffffu, b, 8);
-    const uint32_t b3 = __shfl_down_sync(0xffffffffu, b, 12);
-    if ((l & 15) == 0 && g < G) local[mx_word_index(r, g, rpad)] = b | (b1 << 8) | (b2 << 16) | (b3 << 24);
   }
 }
 
@@ -535,9 +544,11 @@ cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t 
     const int64_t n = rows * cols;
     // one wave of resident CTAs (launch bounds: 4 per SM, 3 with the fused amax)
     const int threads = 256, blocks = grid_for(n / 8, threads, fused ? 3 : 4, sms);
-#define FP8K_QT(T, A)                                                                          \
-  quant_tensor_kernel<T, A><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), n, fmt, amax_in, \
-                                                        scale, scale_out, q, ao)
+#define FP8K_QT(T, A)                                                                         \
+  (fmt == 0 ? quant_tensor_kernel<T, 0, A><<<blocks, threads, 0, st>>>(                        \
+                  static_cast<const T *>(x), n, amax_in, scale, scale_out, q, ao)              \
+            : quant_tensor_kernel<T, 1, A><<<blocks, threads, 0, st>>>(                        \
+                  static_cast<const T *>(x), n, amax_in, scale, scale_out, q, ao))
     if (in_dt == 0) {
       if (fused) FP8K_QT(__nv_bfloat16, true); else FP8K_QT(__nv_bfloat16, false);
     } else {
@@ -548,9 +559,11 @@ cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t 
     const int64_t ntiles = ((cols + kTT - 1) / kTT) * ((rows + kTT - 1) / kTT);
     const int64_t cap = (int64_t)sms * 2;
     const unsigned grid = (unsigned)(ntiles < cap ? ntiles : cap);
-#define FP8K_QTT(T, A)                                                                           \
-  quant_tensor_t_kernel<T, A><<<grid, 256, 0, st>>>(static_cast<const T *>(x), rows, cols, fmt,     \
-                                                    amax_in, scale, scale_out, q, qt, ao)
+#define FP8K_QTT(T, A)                                                                        \
+  (fmt == 0 ? quant_tensor_t_kernel<T, 0, A><<<grid, 256, 0, st>>>(                            \
+                  static_cast<const T *>(x), rows, cols, amax_in, scale, scale_out, q, qt, ao) \
+            : quant_tensor_t_kernel<T, 1, A><<<grid, 256, 0, st>>>(                            \
+                  static_cast<const T *>(x), rows, cols, amax_in, scale, scale_out, q, qt, ao))
     if (in_dt == 0) {
       if (fused) FP8K_QTT(__nv_bfloat16, true); else FP8K_QTT(__nv_bfloat16, false);
     } else {
@@ -563,14 +576,17 @@ cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t 
 
 cudaError_t launch_quant_group(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
                                int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st) {
-  const int64_t G = (K + 127) / 128, pairs = (G + 1) / 2;
-  const int threads = 256, blocks = grid_for(M * pairs * 32, threads, 8, sms);
-  if (in_dt == 0)
-    quant_group_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(x), M, K, fmt, sfmt, q, scales);
-  else
-    quant_group_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float *>(x), M, K,
-                                                          fmt, sfmt, q, scales);
+  // one resident wave (launch bounds: 3 CTAs per SM)
+  const int threads = 256, blocks = grid_for(M * ((K + 1023) / 1024) * 32, threads, 3, sms);
+#define FP8K_QG(T, F)                                                                           \
+  quant_group_kernel<T, F><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), M, K, sfmt, q, \
+                                                       scales)
+  if (in_dt == 0) {
+    if (fmt == 0) FP8K_QG(__nv_bfloat16, 0); else FP8K_QG(__nv_bfloat16, 1);
+  } else {
+    if (fmt == 0) FP8K_QG(float, 0); else FP8K_QG(float, 1);
+  }
+#undef FP8K_QG
   return cudaGetLastError();
 }
 
@@ -589,12 +605,14 @@ cudaError_t launch_quant_block(const void *w, int in_dt, int64_t N, int64_t K, i
 cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
                             const float *amax, float *global_out, uint8_t *q, uint32_t *local,
                             int sms, cudaStream_t st, bool per_row) {
-  const int64_t G = K / 128, pairs = (G + 1) / 2, rpad = (R + 127) / 128 * 128;
-  const int threads = 256, blocks = grid_for(rpad * pairs * 32, threads, 8, sms);
+  const int64_t rpad = (R + 127) / 128 * 128;
+  const int threads = 256, blocks = grid_for(rpad * ((K + 1023) / 1024) * 32, threads, 3, sms);
   const int kind = amax == nullptr ? kMxOneLevel : (per_row ? kMxRow : kMxTensor);
-#define FP8K_QMX(T, G)                                                                           \
-  quant_mx_kernel<T, G><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), R, K, fmt, amax, \
-                                                    global_out, q, local)
+#define FP8K_QMX(T, G)                                                                         \
+  (fmt == 0 ? quant_mx_kernel<T, G, 0><<<blocks, threads, 0, st>>>(                            \
+                  static_cast<const T *>(x), R, K, amax, global_out, q, local)                 \
+            : quant_mx_kernel<T, G, 1><<<blocks, threads, 0, st>>>(                            \
+                  static_cast<const T *>(x), R, K, amax, global_out, q, local))
   if (in_dt == 0) {
     if (kind == kMxTensor) FP8K_QMX(__nv_bfloat16, kMxTensor);
     else if (kind == kMxOneLevel) FP8K_QMX(__nv_bfloat16, kMxOneLevel);
@@ -616,12 +634,12 @@ cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
 // the block byte of each 1x32 piece into the packed E8M0 word layout of the
 // two-level GEMM (rows past N up to R_pad get byte 127), so fp8_gemm_mx
 // contracts these weights with one-level MXFP8 activations directly.
-template <typename T>
+template <typename T, int F>
 __global__ void __launch_bounds__(256)
-    quant_block32_kernel(const T *__restrict__ w, int64_t N, int64_t K, int fmt,
+    quant_block32_kernel(const T *__restrict__ w, int64_t N, int64_t K,
                          uint8_t *__restrict__ q, uint8_t *__restrict__ scales,
                          uint32_t *__restrict__ local) {
-  const float mx = fmt_max(fmt);
+  const float mx = fmt_max(F);
   const int64_t KB = K / 32, rpad = (N + 127) / 128 * 128;
   const int64_t nblk = (rpad / 32) * KB;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -652,15 +670,10 @@ __global__ void __launch_bounds__(256)
     // this row's byte in the packed word of (row n, 128-wide slice k0 / 128)
     local8[4 * mx_word_index(n, k0 / 128, rpad) + (k0 % 128) / 32] = valid ? byte : (uint8_t)127;
     if (valid) {
-      const ScaleDiv d(exp2_int(e));
+      const uint64_t inv2 = f32x2_pack(exp2_int(-e), exp2_int(-e));
       uint2 c[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float x8[8], y8[8];
-        raw[i].decode(x8);
-        div8(d, x8, y8);
-        c[i] = pack8(fmt, y8);
-      }
+      for (int i = 0; i < 4; ++i) c[i] = quant8_pow2<F>(raw[i], inv2);
       uint4 *dst = reinterpret_cast<uint4 *>(q + n * K + k0);
       dst[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
       dst[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
@@ -673,12 +686,15 @@ cudaError_t launch_quant_block32(const void *w, int in_dt, int64_t N, int64_t K,
                                  cudaStream_t st) {
   const int64_t rpad = (N + 127) / 128 * 128;
   const int threads = 256, blocks = grid_for((rpad / 32) * (K / 32) * 32, threads, 8, sms);
-  if (in_dt == 0)
-    quant_block32_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(w), N, K, fmt, q, scales, local);
-  else
-    quant_block32_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float *>(w), N, K,
-                                                            fmt, q, scales, local);
+#define FP8K_QB32(T, F)                                                                        \
+  quant_block32_kernel<T, F><<<blocks, threads, 0, st>>>(static_cast<const T *>(w), N, K, q,    \
+                                                         scales, local)
+  if (in_dt == 0) {
+    if (fmt == 0) FP8K_QB32(__nv_bfloat16, 0); else FP8K_QB32(__nv_bfloat16, 1);
+  } else {
+    if (fmt == 0) FP8K_QB32(float, 0); else FP8K_QB32(float, 1);
+  }
+#undef FP8K_QB32
   return cudaGetLastError();
 }
 

@@ -66,6 +66,29 @@ __device__ __forceinline__ bool wait_count(const uint32_t *ctr, uint32_t target,
   }
 }
 
+// The quantize warps' pass over one staged chunk of nvec 8-element vectors.
+template <int F, typename T>
+__device__ __forceinline__ void cast_chunk(const uint8_t *base, uint32_t nvec, uint2 *dst,
+                                           const ScaleDiv &d, int tid) {
+  if (d.fast) {
+    // two vectors per step: independent FMA chains to interleave
+    for (uint32_t v = tid; v < nvec; v += 2 * kMQThreadsB) {
+      const uint32_t v2 = v + kMQThreadsB;
+      Raw8<T> r0, r1;
+      r0.load_shared(base + v * 8 * sizeof(T));
+      if (v2 < nvec) r1.load_shared(base + v2 * 8 * sizeof(T));
+      dst[v] = quant8_own_scale<F>(r0, d);
+      if (v2 < nvec) dst[v2] = quant8_own_scale<F>(r1, d);
+    }
+  } else {
+    for (uint32_t v = tid; v < nvec; v += kMQThreadsB) {
+      Raw8<T> r;
+      r.load_shared(base + v * 8 * sizeof(T));
+      dst[v] = quant8_ieee<F>(r, d);
+    }
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kMQThreads, 1)
     quant_multi_kernel(const __grid_constant__ MultiQuantArgs args) {
@@ -216,23 +239,10 @@ __global__ void __launch_bounds__(kMQThreads, 1)
         const uint32_t nvec = chunk_bytes(t, c) / (8 * sizeof(T));
         const uint8_t *base = ring_b + s * kMQChunk;
         uint2 *dst = reinterpret_cast<uint2 *>(q + (uint64_t)c * (kMQChunk / sizeof(T)));
-        if (d.fast) {
-          // two vectors per step: independent FMA chains to interleave
-          for (uint32_t v = tid; v < nvec; v += 2 * kMQThreadsB) {
-            const uint32_t v2 = v + kMQThreadsB;
-            Raw8<T> r0, r1;
-            r0.load_shared(base + v * 8 * sizeof(T));
-            if (v2 < nvec) r1.load_shared(base + v2 * 8 * sizeof(T));
-            dst[v] = quant8_own_scale(r0, fmt, d);
-            if (v2 < nvec) dst[v2] = quant8_own_scale(r1, fmt, d);
-          }
-        } else {
-          for (uint32_t v = tid; v < nvec; v += kMQThreadsB) {
-            Raw8<T> r;
-            r.load_shared(base + v * 8 * sizeof(T));
-            dst[v] = quant8_ieee(r, fmt, d);
-          }
-        }
+        if (fmt == 0)
+          cast_chunk<0, T>(base, nvec, dst, d, tid);
+        else
+          cast_chunk<1, T>(base, nvec, dst, d, tid);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_b(s));
       }
