@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <utility>
 
@@ -42,7 +43,10 @@ struct Workspace {
   void *ptr = nullptr;
   size_t bytes = 0;
 };
-std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+// Slots: kWsSplit (the split-K scratch above), kWsWords (E8M0 words of UE8M0
+// group scales, see fp8_gemm_group_bias).
+constexpr int kWsSplit = 0, kWsWords = 1;
+std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_ws;
 
 // CTA-pair GEMM path switch (on by default; fp8_set_option turns it off).
 bool g_use_pairs = true;
@@ -140,11 +144,11 @@ int vector_store_ok(const void *c, int64_t ldc, int out_dt) {
   return aligned16(c) && (ldc * es) % 16 == 0 ? 1 : 0;
 }
 
-int get_workspace(cudaStream_t st, size_t need, void **out) {
+int get_workspace(cudaStream_t st, size_t need, void **out, int slot = kWsSplit) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FP8_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  Workspace &w = g_ws[std::make_pair(dev, st)];
+  Workspace &w = g_ws[std::make_tuple(dev, st, slot)];
   if (w.bytes < need) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return FP8_ERR_CUDA;
@@ -193,7 +197,7 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
     return to_status(fp8k::launch_gemm_pair(tma, tmb, args, d->sms, st));
   }
   if ((rc = encode_gemm_operand(&tmb, b, args.b_mn, args.K, args.N,
-                                fp8k::gemm_tile_n(mode, args.M))) !=
+                                fp8k::gemm_tile_n(mode, args.M, args.N, d->sms))) !=
       FP8_OK)
     return rc;
   return to_status(fp8k::launch_gemm(mode, tma, tmb, args, d->sms, st));
@@ -533,6 +537,29 @@ int fp8_gemm_group_bias(const uint8_t *a, const void *sa, const uint8_t *b, cons
   args.out_dt = FP8_OUT_BF16; args.ldc = ldc; args.c = c; args.sa = sa; args.sb = sb;
   args.bias = bias;
   const int mode = sfmt == FP8_SCALE_F32 ? fp8k::kScaleGroupF32 : fp8k::kScaleGroupUe8m0;
+  if (mode == fp8k::kScaleGroupUe8m0 && M > 256) {
+    // Beyond small M: the UE8M0 scales become E8M0 words (four equal bytes per
+    // 128-wide K slice) that the block-scaled GEMM bulk-copies per stage, in
+    // place of the per-stage byte loads of the group mode.  Same products,
+    // same FP32 accumulation: the tensor core applies 2^e to each 1x32
+    // sub-block of the group instead of the group as a whole.
+    DeviceState *d = nullptr;
+    if ((rc = device_state(&d)) != FP8_OK) return rc;
+    const size_t G = (size_t)(K / 128);
+    const size_t mpad = (size_t)(M + 127) / 128 * 128, npad = (size_t)(N + 127) / 128 * 128;
+    void *w = nullptr;
+    if ((rc = get_workspace((cudaStream_t)stream, G * (mpad + npad) * 4, &w, kWsWords)) != FP8_OK)
+      return rc;
+    uint32_t *la = static_cast<uint32_t *>(w), *lb = la + G * mpad;
+    if ((rc = to_status(fp8k::launch_ue8m0_words(static_cast<const uint8_t *>(sa),
+                                                 static_cast<const uint8_t *>(sb), M, N, K, la, lb,
+                                                 d->sms, (cudaStream_t)stream))) != FP8_OK)
+      return rc;
+    args.sa = la;
+    args.sb = lb;
+    args.ga = args.gb = nullptr;
+    return run_gemm(fp8k::kScaleMx, a, b, args, (cudaStream_t)stream);
+  }
   return run_gemm(mode, a, b, args, (cudaStream_t)stream);
 }
 
@@ -559,8 +586,9 @@ int fp8_gemm_group_experts(const uint8_t *a, const void *sa, const uint8_t *b, c
   args.experts = experts;
   args.offsets = offsets;
   args.sb_expert_stride = ((N + 127) / 128) * (K / 128);
-  // tile width chosen for the average rows per expert
-  const int bn = fp8k::gemm_tile_n(mode, M / experts);
+  // tile width for the expected tile count (about half a row tile of
+  // padding per expert)
+  const int bn = fp8k::gemm_tile_n(mode, M + 64 * (int64_t)experts, N, d->sms);
   CUtensorMap tma, tmb;
   if ((rc = encode_operand(&tma, a, K, M, 128)) != FP8_OK) return rc;
   if ((rc = encode_operand(&tmb, b, K, (int64_t)experts * N, bn)) != FP8_OK) return rc;
@@ -690,8 +718,8 @@ int fp8_get_last_device_error(int *where_out, fp8_stream_t stream) {
     if (cudaGetDevice(&dev) != cudaSuccess) return FP8_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto &kv : g_ws)
-      if (kv.first.first == dev && kv.second.ptr != nullptr &&
-          cudaMemset(kv.second.ptr, 0, kCounterBytes) != cudaSuccess)
+      if (std::get<0>(kv.first) == dev && std::get<2>(kv.first) == kWsSplit &&
+          kv.second.ptr != nullptr && cudaMemset(kv.second.ptr, 0, kCounterBytes) != cudaSuccess)
         return FP8_ERR_CUDA;
   }
   if (where_out != nullptr) *where_out = (int)h[1];

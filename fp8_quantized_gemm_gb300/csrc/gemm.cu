@@ -68,6 +68,13 @@ struct Cfg {
   static_assert(BN % 32 == 0 && BN <= 256, "tile N");
 };
 
+// Epilogue factor of the block-scaled mode: the two global factors, or 1
+// when there are none (per-row factors, or UE8M0 group scales run as E8M0
+// words).
+__device__ __forceinline__ float mx_alpha(const GemmArgs &a) {
+  return a.row_scale != nullptr || a.ga == nullptr ? 1.0f : *a.ga * *a.gb;
+}
+
 template <int MODE, int BN, int STAGES, bool EXPERTS>
 __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
@@ -454,7 +461,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       float alpha = 1.0f;
       if constexpr (MODE == kScaleTensor)
         alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
-      if constexpr (MODE == kScaleMx) alpha = args.row_scale != nullptr ? 1.0f : *args.ga * *args.gb;
+      if constexpr (MODE == kScaleMx) alpha = mx_alpha(args);
       uint32_t j = 0;
       for (int64_t u = u_first; u < num_units; u += u_step, ++j) {
         const int64_t t = unit_tile(u);
@@ -583,15 +590,15 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     // every split's partial tile is in its CTA's shared memory: each CTA sums
     // a slice of the tile's rows over the cluster, in split order
     cluster_sync();
-    if (warp >= 2) {
+    {  // every warp takes part (the producer and MMA warps are done)
       const TileInfo ti = tile_info(unit_tile(u_first));
       const int64_t m0 = ti.m0, n0 = ti.n0;
       float alpha = 1.0f;
       if constexpr (MODE == kScaleTensor)
         alpha = *static_cast<const float *>(args.sa) * *static_cast<const float *>(args.sb);
-      if constexpr (MODE == kScaleMx) alpha = args.row_scale != nullptr ? 1.0f : *args.ga * *args.gb;
+      if constexpr (MODE == kScaleMx) alpha = mx_alpha(args);
       cluster_reduce<BN>(args, part, m0, n0, C::BM, alpha, cluster_ctarank(), ks,
-                         (int)threadIdx.x - 64, C::kEpiWarps * 32);
+                         (int)threadIdx.x, C::kThreads);
     }
     cluster_sync();  // no CTA leaves while a peer may still read its partial
   }
@@ -642,12 +649,15 @@ static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const Gem
   return cudaGetLastError();
 }
 
-// Tile width: 128 for the FP32-promotion mode, and for the UE8M0 mode at
-// small M (twice the tiles, so the split GEMM fills the SMs); 256 otherwise.
-int gemm_tile_n(int mode, int64_t M) {
+// Tile width: 128 for the FP32-promotion mode; 256 for the per-tensor mode
+// (whose large shapes run on CTA pairs); for the block-scaled modes 256 when
+// the 128 x 256 tiles fill the SMs and 128 otherwise (twice the tiles: mid-
+// size M then needs no split K, small M splits K over fewer k blocks).
+int gemm_tile_n(int mode, int64_t M, int64_t N, int sms) {
   if (mode == kScaleGroupF32) return 128;
-  if (mode == kScaleGroupUe8m0 && M <= 256) return 128;
-  return 256;
+  if (mode == kScaleTensor) return 256;
+  const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+  return tiles256 < sms ? 128 : 256;
 }
 
 // Split K when the tiles cannot fill half the SMs: as many splits as fit the
@@ -679,17 +689,20 @@ static int active_clusters(int size) {
   return cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess ? n : 0;
 }
 
-static int max_active_clusters(int mode, int64_t M, int size) {
+static int max_active_clusters(int mode, int bn, int size) {
   static int cache[64][4][2][kMaxClusterSplit + 1];
   static bool have[64][4][2][kMaxClusterSplit + 1];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int w = gemm_tile_n(mode, M) == 128 ? 0 : 1;
+  const int w = bn == 128 ? 0 : 1;
   if (!have[dev][mode][w][size]) {
     int n = 0;
     switch (mode) {
       case kScaleTensor: n = active_clusters<kScaleTensor, 256, 4>(size); break;
-      case kScaleMx: n = active_clusters<kScaleMx, 256, 4>(size); break;
+      case kScaleMx:
+        n = w == 0 ? active_clusters<kScaleMx, 128, 6>(size)
+                   : active_clusters<kScaleMx, 256, 4>(size);
+        break;
       case kScaleGroupUe8m0:
         n = w == 0 ? active_clusters<kScaleGroupUe8m0, 128, 6>(size)
                    : active_clusters<kScaleGroupUe8m0, 256, 4>(size);
@@ -703,7 +716,7 @@ static int max_active_clusters(int mode, int64_t M, int size) {
 }
 
 int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster) {
-  const int64_t bn = gemm_tile_n(mode, M);
+  const int64_t bn = gemm_tile_n(mode, M, N, sms);
   const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
   const int64_t kb = (K + 127) / 128;
   if (tiles * 2 > sms || kb < 8) return 1;
@@ -713,7 +726,7 @@ int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster
     // the largest split whose clusters (one per tile) are all resident at
     // once: a second wave of clusters would double the time
     if (ks > kMaxClusterSplit) ks = kMaxClusterSplit;
-    while (ks > 1 && max_active_clusters(mode, M, (int)ks) < tiles) --ks;
+    while (ks > 1 && max_active_clusters(mode, (int)bn, (int)ks) < tiles) --ks;
   } else {
     const int64_t rows = M < 128 ? M : 128;
     const int64_t by_partials = (512 * 1024) / (rows * bn * 4);
@@ -734,9 +747,12 @@ cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb
                         const GemmArgs &args, int sms, cudaStream_t st) {
   switch (mode) {
     case kScaleTensor: return run<kScaleTensor, 256, 4>(tma, tmb, args, sms, st);
-    case kScaleMx: return run<kScaleMx, 256, 4>(tma, tmb, args, sms, st);
+    case kScaleMx:
+      if (gemm_tile_n(mode, args.M, args.N, sms) == 128)
+        return run<kScaleMx, 128, 6>(tma, tmb, args, sms, st);
+      return run<kScaleMx, 256, 4>(tma, tmb, args, sms, st);
     case kScaleGroupUe8m0:
-      if (gemm_tile_n(mode, args.M) == 128)
+      if (gemm_tile_n(mode, args.M, args.N, sms) == 128)
         return run<kScaleGroupUe8m0, 128, 6>(tma, tmb, args, sms, st);
       return run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, sms, st);
     case kScaleGroupF32: return run<kScaleGroupF32, 128, 6>(tma, tmb, args, sms, st);

@@ -183,6 +183,15 @@ __device__ __forceinline__ void stash_partial32_bn(float *part, int r, int c, co
   for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -196,6 +205,53 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
 // [rank * R / ks, (rank + 1) * R / ks) of the tile (R its valid rows) over
 // every CTA's partial tile, in split order (the same order, hence the same
 // sums, as the global-workspace reduction), scales by alpha and stores.
+// Every thread of the CTA takes part: thread t owns float4 column t % (BN/4)
+// and rows t / (BN/4), + nthr / (BN/4), ...; each step issues the remote
+// loads of kStep rows of all KS splits (about 16 in flight per thread)
+// before summing any, since a distributed-shared-memory load has a long
+// latency.
+template <int BN, int KS>
+__device__ __forceinline__ void cluster_reduce_ks(const GemmArgs &a, uint32_t base, int64_t m0,
+                                                  int64_t n0, int64_t r0, int64_t r1,
+                                                  int64_t cols, float alpha, uint32_t rank,
+                                                  int tid, int nthr) {
+  constexpr int kCg = BN / 4;
+  constexpr int kStep = KS >= 16 ? 1 : 16 / KS;
+  const int rstride = nthr / kCg;
+  if (tid >= rstride * kCg) return;
+  const int64_t c = (int64_t)(tid % kCg) * 4;
+  if (c >= cols) return;
+  const int n = cols - c < 4 ? (int)(cols - c) : 4;
+  for (int64_t rb = r0 + tid / kCg; rb < r1; rb += (int64_t)kStep * rstride) {
+    float4 p[kStep][KS];
+#pragma unroll
+    for (int j = 0; j < kStep; ++j) {
+      const int64_t r = rb + (int64_t)j * rstride;
+      if (r < r1) {
+        const uint32_t off = base + (uint32_t)((r * kPartStride<BN> + c) * 4);
+#pragma unroll
+        for (int sp = 0; sp < KS; ++sp)  // this CTA's own partial: a local load
+          p[j][sp] = (uint32_t)sp == rank ? ld_shared_f4(off)
+                                          : ld_shared_cluster_f4(mapa_shared(off, (uint32_t)sp));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kStep; ++j) {
+      const int64_t r = rb + (int64_t)j * rstride;
+      if (r < r1) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int sp = 0; sp < KS; ++sp) {
+          acc[0] += p[j][sp].x; acc[1] += p[j][sp].y; acc[2] += p[j][sp].z; acc[3] += p[j][sp].w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] *= alpha;
+        store4(a, m0 + r, n0 + c, n, acc);
+      }
+    }
+  }
+}
+
 template <int BN>
 __device__ __forceinline__ void cluster_reduce(const GemmArgs &a, const float *part, int64_t m0,
                                                int64_t n0, int64_t tile_rows, float alpha,
@@ -204,41 +260,16 @@ __device__ __forceinline__ void cluster_reduce(const GemmArgs &a, const float *p
   const int64_t cols = a.N - n0 < BN ? a.N - n0 : BN;
   if (rows <= 0 || cols <= 0) return;
   const int64_t r0 = (int64_t)rank * rows / ks, r1 = ((int64_t)rank + 1) * rows / ks;
-  const int64_t cg = (cols + 3) / 4;
   const uint32_t base = smem_u32(part);
-  const int64_t groups = (r1 - r0) * cg;
-  // two groups per step: up to 2 * ks remote loads in flight per thread
-  for (int64_t g0 = tid; g0 < groups; g0 += 2 * (int64_t)nthr) {
-    float4 p[2][kMaxClusterSplit];
-    uint32_t off[2];
-    bool live[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t gi = g0 + h * (int64_t)nthr;
-      live[h] = gi < groups;
-      const int64_t r = r0 + (live[h] ? gi / cg : 0), c = live[h] ? (gi % cg) * 4 : 0;
-      off[h] = base + (uint32_t)((r * kPartStride<BN> + c) * 4);
-#pragma unroll
-      for (int sp = 0; sp < kMaxClusterSplit; ++sp)
-        if (live[h] && sp < ks) p[h][sp] = ld_shared_cluster_f4(mapa_shared(off[h], (uint32_t)sp));
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (!live[h]) continue;
-      const int64_t gi = g0 + h * (int64_t)nthr;
-      const int64_t r = r0 + gi / cg, c = (gi % cg) * 4;
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int sp = 0; sp < kMaxClusterSplit; ++sp) {
-        if (sp < ks) {
-          acc[0] += p[h][sp].x; acc[1] += p[h][sp].y; acc[2] += p[h][sp].z; acc[3] += p[h][sp].w;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] *= alpha;
-      const int n = a.N - (n0 + c) < 4 ? (int)(a.N - (n0 + c)) : 4;
-      store4(a, m0 + r, n0 + c, n, acc);
-    }
+  static_assert(kMaxClusterSplit == 8, "split counts below");
+  switch (ks) {
+    case 2: cluster_reduce_ks<BN, 2>(a, base, m0, n0, r0, r1, cols, alpha, rank, tid, nthr); break;
+    case 3: cluster_reduce_ks<BN, 3>(a, base, m0, n0, r0, r1, cols, alpha, rank, tid, nthr); break;
+    case 4: cluster_reduce_ks<BN, 4>(a, base, m0, n0, r0, r1, cols, alpha, rank, tid, nthr); break;
+    case 5: cluster_reduce_ks<BN, 5>(a, base, m0, n0, r0, r1, cols, alpha, rank, tid, nthr); break;
+    case 6: cluster_reduce_ks<BN, 6>(a, base, m0, n0, r0, r1, cols, alpha, rank, tid, nthr); break;
+    case 7: cluster_reduce_ks<BN, 7>(a, base, m0, n0, r0, r1, cols, alpha, rank, tid, nthr); break;
+    default: cluster_reduce_ks<BN, 8>(a, base, m0, n0, r0, r1, cols, alpha, rank, tid, nthr); break;
   }
 }
 

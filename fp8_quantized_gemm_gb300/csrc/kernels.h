@@ -24,6 +24,8 @@ cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
                             int sms, cudaStream_t st, bool per_row = false);
 cudaError_t launch_row_amax(const void *x, int in_dt, int64_t R, int64_t K, float *out, int sms,
                             cudaStream_t st);
+cudaError_t launch_ue8m0_words(const uint8_t *sa, const uint8_t *sb, int64_t M, int64_t N,
+                               int64_t K, uint32_t *la, uint32_t *lb, int sms, cudaStream_t st);
 cudaError_t launch_quant_block32(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
                                  uint8_t *q, uint8_t *scales, uint32_t *local, int sms,
                                  cudaStream_t st);
@@ -55,7 +57,7 @@ cudaError_t launch_quant_multi(const MultiQuantArgs &args, int in_dt, int sms, c
 // GEMM family.  Scale modes of the epilogue / main loop:
 enum GemmScaleMode : int {
   kScaleTensor = 0,      // per-tensor: alpha = sa[0] * sb[0] in the epilogue
-  kScaleMx = 1,          // block-scaled MMA, packed E8M0 words; alpha = ga[0] * gb[0]
+  kScaleMx = 1,          // block-scaled MMA, packed E8M0 words; alpha = ga[0] * gb[0] (1 if ga null)
   kScaleGroupUe8m0 = 2,  // block-scaled MMA, per-128 UE8M0 bytes replicated in-kernel
   kScaleGroupF32 = 3     // per-128 fp32 scales promoted on the CUDA cores
 };
@@ -108,7 +110,7 @@ constexpr int kMaxClusterSplit = 8;
 int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster);
 
 // Output-tile width (N) of a mode at M rows; the B tensor map's box uses it.
-int gemm_tile_n(int mode, int64_t M);
+int gemm_tile_n(int mode, int64_t M, int64_t N, int sms);
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,
                         const GemmArgs &args, int sms, cudaStream_t st);

@@ -73,7 +73,7 @@ extern "C" int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const ui
   if ((rc = scratch_for_current_device(&scratch)) != FP8_OK) return rc;
 
   const int mode = sfmt == FP8_SCALE_F32 ? fp8k::kScaleGroupF32 : fp8k::kScaleGroupUe8m0;
-  const int bn = fp8k::gemm_tile_n(mode, M);
+  const int bn = fp8k::gemm_tile_n(mode, M, N, sms);
   fp8k::GemmArgs args{};
   args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
   args.out_dt = FP8_OUT_BF16; args.ldc = ldc; args.c = c; args.sa = sa; args.sb = sb;

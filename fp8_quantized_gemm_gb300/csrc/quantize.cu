@@ -698,6 +698,42 @@ cudaError_t launch_quant_block32(const void *w, int in_dt, int64_t N, int64_t K,
   return cudaGetLastError();
 }
 
+// ------------------------------------------ UE8M0 group scales -> MX words --
+// The per-K-group GEMM with UE8M0 scales runs as the block-scaled GEMM: each
+// 1x128 activation scale and 128x128 weight-block scale becomes the four
+// equal E8M0 bytes of its row's packed word for that 128-wide K slice (the
+// tensor core then applies the same factor to each 1x32 sub-block, which is
+// the group's factor).  Word i of slice g (i < R_pad) belongs to row
+// (i & ~127) + 32 (i & 3) + ((i & 127) >> 2), the inverse of mx_word_index;
+// padding rows get byte 127 (factor 1).
+__global__ void __launch_bounds__(256)
+    ue8m0_words_kernel(const uint8_t *__restrict__ sa, const uint8_t *__restrict__ sb,
+                       int64_t M, int64_t N, int64_t G, uint32_t *__restrict__ la,
+                       uint32_t *__restrict__ lb) {
+  const int64_t mpad = (M + 127) / 128 * 128, npad = (N + 127) / 128 * 128;
+  const int64_t na = G * mpad, total = na + G * npad;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool is_a = i < na;
+    const int64_t j = is_a ? i : i - na, pad = is_a ? mpad : npad;
+    const int64_t g = j / pad, w = j - g * pad;
+    const int64_t r = (w & ~(int64_t)127) + 32 * (w & 3) + ((w & 127) >> 2);
+    uint32_t b = 127u;
+    if (is_a && r < M) b = sa[g * M + r];
+    if (!is_a && r < N) b = sb[(r >> 7) * G + g];
+    (is_a ? la : lb)[j] = b * 0x01010101u;
+  }
+}
+
+cudaError_t launch_ue8m0_words(const uint8_t *sa, const uint8_t *sb, int64_t M, int64_t N,
+                               int64_t K, uint32_t *la, uint32_t *lb, int sms, cudaStream_t st) {
+  const int64_t G = K / 128;
+  const int64_t words = G * ((M + 127) / 128 * 128 + (N + 127) / 128 * 128);
+  const int threads = 256, blocks = grid_for(words, threads, 8, sms);
+  ue8m0_words_kernel<<<blocks, threads, 0, st>>>(sa, sb, M, N, G, la, lb);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------- row amax --
 // amax_out[r] = max |x[r, :]|: one warp per row, 16-byte loads, the same
 // order-preserving keys as the tensor amax (exact).

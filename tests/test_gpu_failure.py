@@ -47,17 +47,34 @@ def test_timeout_reported_then_context_usable(mnk):
     assert F.fp8_get_last_device_error()[0] == 0
 
 
-def test_timeout_in_group_gemm_resets_split_k_counters():
-    """A timed-out split-K call can leave arrival counters behind; reading the
-    error resets them, so the next call on the same stream is correct."""
+def run_group_noalloc(qa, sa, qb, sb):
     F = lib()
-    qa, sa, qb, sb = group_operands(16, 2048, 7168, "f32", seed=2)
-    rc, where = forced_timeout(lambda: run_group(qa, sa, qb, sb, "f32"))
+    m, n = qa.shape[0], qb.shape[0]
+    sa_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sa).T)).cuda()   # [G, M]
+    sb_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sb))).cuda()     # [N/128, G]
+    out = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    F.fp8_gemm_group_noalloc(torch.from_numpy(qa).cuda(), sa_dev, torch.from_numpy(qb).cuda(),
+                             sb_dev, 0, out)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+def test_timeout_in_group_gemm_resets_split_k_counters():
+    """The no-allocation entry point splits K over CTAs that meet through
+    arrival counters in its fixed scratch; a timed-out call can leave counters
+    behind, reading the error resets them, and the next calls (that entry
+    point and the regular one) are correct.  K is long enough for a wait to
+    outlast the barrier's suspend window."""
+    F = lib()
+    qa, sa, qb, sb = group_operands(16, 256, 65536, "f32", seed=2)
+    rc, where = forced_timeout(lambda: run_group_noalloc(qa, sa, qb, sb))
     assert rc == F.FP8_ERR_TIMEOUT, (rc, where)
     c, e = group_reference(qa, sa, qb, sb, "f32")
     for _ in range(2):
-        ok, worst = OG.check(run_group(qa, sa, qb, sb, "f32"), c, e, "bf16")
+        ok, worst = OG.check(run_group_noalloc(qa, sa, qb, sb), c, e, "bf16")
         assert ok, worst
+    ok, worst = OG.check(run_group(qa, sa, qb, sb, "f32"), c, e, "bf16")
+    assert ok, worst
 
 
 def test_timeout_in_multi_tensor_quantize():
