@@ -50,6 +50,8 @@ std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_ws;
 
 // CTA-pair GEMM path switch (on by default; fp8_set_option turns it off).
 bool g_use_pairs = true;
+// B-multicast clusters in the single-CTA GEMM (on by default).
+bool g_use_multicast = true;
 // Bound of every device-side mbarrier wait (fp8_set_option).
 uint64_t g_wait_limit_ns = 2000000000ull;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -196,9 +198,16 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
       return rc;
     return to_status(fp8k::launch_gemm_pair(tma, tmb, args, d->sms, st));
   }
+  // multicast pairs of vertically adjacent tiles share each B box: measured
+  // faster for 128-wide tiles (the FP32-promotion mode, and the block-scaled
+  // modes at mid-size M), not for the 128 x 256 block-scaled tiles
+  const int bn = fp8k::gemm_tile_n(mode, args.M, args.N, d->sms);
+  args.multicast = g_use_multicast && mode != fp8k::kScaleTensor && bn == 128 &&
+                           args.ksplit == 1 && !args.b_mn && args.experts == 0 && args.M > 128
+                       ? 1
+                       : 0;
   if ((rc = encode_gemm_operand(&tmb, b, args.b_mn, args.K, args.N,
-                                fp8k::gemm_tile_n(mode, args.M, args.N, d->sms))) !=
-      FP8_OK)
+                                args.multicast ? bn / 2 : bn)) != FP8_OK)
     return rc;
   return to_status(fp8k::launch_gemm(mode, tma, tmb, args, d->sms, st));
 }
@@ -729,6 +738,10 @@ int fp8_get_last_device_error(int *where_out, fp8_stream_t stream) {
 int fp8_set_option(int option, int value) {
   if (option == FP8_OPT_GEMM_CTA_PAIRS) {
     g_use_pairs = value != 0;
+    return FP8_OK;
+  }
+  if (option == FP8_OPT_GEMM_MULTICAST) {
+    g_use_multicast = value != 0;
     return FP8_OK;
   }
   if (option == FP8_OPT_WAIT_LIMIT_US) {

@@ -75,7 +75,12 @@ __device__ __forceinline__ float mx_alpha(const GemmArgs &a) {
   return a.row_scale != nullptr || a.ga == nullptr ? 1.0f : *a.ga * *a.gb;
 }
 
-template <int MODE, int BN, int STAGES, bool EXPERTS>
+// MC == 2: the two CTAs of a cluster take vertically adjacent tiles (row
+// tiles 2p and 2p + 1, the same columns) and share the B box of every stage:
+// each CTA loads one half of it and multicasts that half to both, so the L2
+// traffic of B halves; a stage is refilled once both CTAs' MMAs have
+// released it (the commit arrives on both CTAs' empty barriers).
+template <int MODE, int BN, int STAGES, bool EXPERTS, int MC>
 __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                 const GemmArgs args) {
@@ -110,7 +115,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), MC);
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -175,7 +180,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     }
     __syncthreads();
   }
-  const int64_t num_tiles = EXPERTS ? ex_tile0[E] : ((args.M + C::BM - 1) / C::BM) * tiles_n;
+  static_assert(MC == 1 || (MC == 2 && !EXPERTS), "multicast pairs plain row tiles");
+  const int64_t row_tiles = (args.M + C::BM - 1) / C::BM;
+  const int64_t num_tiles =
+      EXPERTS ? ex_tile0[E] : (MC == 2 ? (row_tiles + 1) / 2 : row_tiles) * tiles_n;
+  const uint32_t mc_rank = MC == 2 ? cluster_ctarank() : 0u;
   const int KB = (int)((args.K + C::BK - 1) / C::BK);
   // work unit u = (tile u % num_tiles, K split u / num_tiles); with ksplit 1
   // units are tiles.  Split s covers k blocks [s*KB/ks, (s+1)*KB/ks).
@@ -202,7 +211,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       ti.brow = (int64_t)lo * args.N + ti.n0;
       ti.sbo = (int64_t)lo * args.sb_expert_stride;
     } else {
-      ti.m0 = (t / tiles_n) * C::BM;
+      // (MC == 2: t indexes row-tile pairs; this CTA takes row tile 2p + rank)
+      ti.m0 = ((t / tiles_n) * MC + mc_rank) * C::BM;
       ti.n0 = (t % tiles_n) * BN;
       ti.row_end = args.M;
       ti.brow = ti.n0;
@@ -213,9 +223,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   // the CTA's units: u_first, u_first + u_step, ...  In a split cluster the
   // CTA owns exactly one unit: tile = cluster index, split = cluster rank.
   const bool csplit = args.cluster_split != 0;
-  const int64_t u_first =
-      csplit ? (int64_t)cluster_ctarank() * num_tiles + blockIdx.x / ks : (int64_t)blockIdx.x;
-  const int64_t u_step = csplit ? num_units : (int64_t)gridDim.x;
+  const int64_t u_first = csplit ? (int64_t)cluster_ctarank() * num_tiles + blockIdx.x / ks
+                                 : (int64_t)(blockIdx.x / MC);
+  const int64_t u_step = csplit ? num_units : (int64_t)(gridDim.x / MC);
   auto unit_tile = [&](int64_t u) { return u % num_tiles; };
   auto kb_begin = [&](int64_t u) { return (int)((u / num_tiles) * KB / ks); };
   auto kb_end = [&](int64_t u) { return (int)((u / num_tiles + 1) * KB / ks); };
@@ -316,11 +326,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       }
       if (elect_one()) {
         uint32_t sfb_bytes = 0;
+        // (a multicast CTA whose row tile lies past M loads no A factors)
+        const int64_t a_mpad = (args.M + 127) / 128 * 128;
         if constexpr (MODE == kScaleMx) {
           const int64_t npad = (args.N + 127) / 128 * 128;
           const int64_t rows = (npad - n0) < BN ? (npad - n0) : BN;
           sfb_bytes = (uint32_t)rows * 4u;
-          tx += C::kSfaBytes + sfb_bytes;
+          tx += (m0 < a_mpad ? C::kSfaBytes : 0u) + sfb_bytes;
         }
         mbar_arrive_expect_tx(full_bar(s), tx);
         // tensor-map coordinates are (contiguous dim, row); an MN-major
@@ -330,7 +342,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
           tma_load_2d(sA(s), &tma, full_bar(s), (int32_t)m0, k0);
         else
           tma_load_2d(sA(s), &tma, full_bar(s), k0, (int32_t)m0);
-        if (args.b_mn) {
+        if constexpr (MC == 2) {
+          // this CTA's half of the B box (tensor-map box BN / 2 rows), to both
+          tma_load_2d_mc(sB(s) + mc_rank * (BN / 2) * C::BK, &tmb, full_bar(s), k0,
+                         (int32_t)brow + (int32_t)mc_rank * (BN / 2), (uint16_t)0x3);
+        } else if (args.b_mn) {
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h)
             tma_load_2d(sB(s) + h * 128 * C::BK, &tmb, full_bar(s), (int32_t)n0 + 128 * h, k0);
@@ -338,11 +354,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
           tma_load_2d(sB(s), &tmb, full_bar(s), k0, (int32_t)brow);
         }
         if constexpr (MODE == kScaleMx) {
-          const int64_t mpad = (args.M + 127) / 128 * 128;
           const int64_t npad = (args.N + 127) / 128 * 128;
-          const uint32_t *la = static_cast<const uint32_t *>(args.sa) + (int64_t)kb * mpad + m0;
+          const uint32_t *la = static_cast<const uint32_t *>(args.sa) + (int64_t)kb * a_mpad + m0;
           const uint32_t *lb = static_cast<const uint32_t *>(args.sb) + (int64_t)kb * npad + n0;
-          bulk_load(smem_u32(sSfa(s)), la, C::kSfaBytes, full_bar(s));
+          if (m0 < a_mpad) bulk_load(smem_u32(sSfa(s)), la, C::kSfaBytes, full_bar(s));
           bulk_load(smem_u32(sSfb(s)), lb, sfb_bytes, full_bar(s));
         }
       }
@@ -362,6 +377,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       // let the copies already in flight land before the CTA can exit
       const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
       for (uint32_t i = first; i < it; ++i) drain_wait(full_bar(i % STAGES), (i / STAGES) & 1u);
+      // the peer's multicast halves for stages this CTA never armed
+      if (MC == 2) grace_wait(20000000ull);  // 20 ms
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -424,7 +441,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
               mma_f8f6f4(d, ad.base + k * ad.step, bd.base + k * bd.step, idesc, acc ? 1u : 0u);
             }
           }
-          mma_commit(empty_bar(s));
+          if constexpr (MC == 2)
+            mma_commit_mc(empty_bar(s), (uint16_t)0x3);
+          else
+            mma_commit(empty_bar(s));
           if constexpr (C::kPromote) mma_commit(accf_bar(it & 3u));
         }
         if (!ok) break;
@@ -604,17 +624,46 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // a multicast pair leaves together: no CTA exits while the other may still
+  // write into its shared memory
+  if constexpr (MC == 2) cluster_sync();
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int MODE, int BN, int STAGES, bool EXPERTS = false>
+// Clusters of `size` CTAs of a GEMM kernel variant that can be resident at
+// once.
+template <int MODE, int BN, int STAGES, int MC = 1>
+static int active_clusters(int size) {
+  using C = Cfg<MODE, BN, STAGES>;
+  auto kern = gemm_kernel<MODE, BN, STAGES, false, MC>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)size;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)size);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  int n = 0;
+  return cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess ? n : 0;
+}
+
+template <int MODE, int BN, int STAGES, bool EXPERTS = false, int MC = 1>
 static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
                        int sms, cudaStream_t st) {
   using C = Cfg<MODE, BN, STAGES>;
-  auto kern = gemm_kernel<MODE, BN, STAGES, EXPERTS>;
+  auto kern = gemm_kernel<MODE, BN, STAGES, EXPERTS, MC>;
   if (EXPERTS != (args.experts > 0)) return cudaErrorInvalidValue;
+  if (MC == 2 && (args.ksplit != 1 || args.cluster_split || args.b_mn)) return cudaErrorInvalidValue;
   // the shared-memory opt-in is set once per device (not inside a capture)
   static bool attr_done[64] = {};
+  static int mc_clusters[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -622,22 +671,33 @@ static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const Gem
   if (!attr_done[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
+    if (MC == 2) mc_clusters[dev] = active_clusters<MODE, BN, STAGES, MC>(2);
     attr_done[dev] = true;
   }
   // (expert-grouped rows: at most one partial row tile per expert more)
   const int64_t row_tiles = (args.M + C::BM - 1) / C::BM + (args.experts > 0 ? args.experts : 0);
   const int64_t units = row_tiles * ((args.N + BN - 1) / BN) * args.ksplit;
-  if (args.cluster_split) {
-    // one CTA per unit; the splits of a tile are one cluster
-    if (args.ksplit < 2 || args.ksplit > kMaxClusterSplit) return cudaErrorInvalidValue;
+  if (args.cluster_split || MC == 2) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)units);
+    unsigned csize = 0;
+    if (args.cluster_split) {
+      // one CTA per unit; the splits of a tile are one cluster
+      if (args.ksplit < 2 || args.ksplit > kMaxClusterSplit) return cudaErrorInvalidValue;
+      cfg.gridDim = dim3((unsigned)units);
+      csize = (unsigned)args.ksplit;
+    } else {
+      // persistent multicast pairs: one cluster per pair of row tiles
+      const int64_t pair_tiles = (row_tiles + 1) / 2 * ((args.N + BN - 1) / BN);
+      const int64_t cap = mc_clusters[dev] > 0 ? mc_clusters[dev] : sms / 2;
+      cfg.gridDim = dim3((unsigned)(2 * (pair_tiles < cap ? pair_tiles : cap)));
+      csize = 2;
+    }
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)args.ksplit;
+    attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -665,30 +725,6 @@ int gemm_tile_n(int mode, int64_t M, int64_t N, int sms) {
 // through distributed shared memory (at most kMaxClusterSplit per tile);
 // workspace splits are capped at 512 KB of fp32 partials per tile, which the
 // last CTA of the tile sums.
-// Clusters of `size` CTAs of the kernel that `mode` runs at M rows that can
-// be resident at once (cached per device, mode, tile width and size).
-template <int MODE, int BN, int STAGES>
-static int active_clusters(int size) {
-  using C = Cfg<MODE, BN, STAGES>;
-  auto kern = gemm_kernel<MODE, BN, STAGES, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) !=
-      cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)size;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.gridDim = dim3((unsigned)size);
-  cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
-  int n = 0;
-  return cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess ? n : 0;
-}
-
 static int max_active_clusters(int mode, int bn, int size) {
   static int cache[64][4][2][kMaxClusterSplit + 1];
   static bool have[64][4][2][kMaxClusterSplit + 1];
@@ -745,17 +781,25 @@ cudaError_t launch_gemm_experts(int mode, int bn, const CUtensorMap &tma, const 
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb,
                         const GemmArgs &args, int sms, cudaStream_t st) {
+  const bool mc = args.multicast != 0;
+  if (mc && mode == kScaleTensor) return cudaErrorInvalidValue;
   switch (mode) {
     case kScaleTensor: return run<kScaleTensor, 256, 4>(tma, tmb, args, sms, st);
     case kScaleMx:
       if (gemm_tile_n(mode, args.M, args.N, sms) == 128)
-        return run<kScaleMx, 128, 6>(tma, tmb, args, sms, st);
-      return run<kScaleMx, 256, 4>(tma, tmb, args, sms, st);
+        return mc ? run<kScaleMx, 128, 6, false, 2>(tma, tmb, args, sms, st)
+                  : run<kScaleMx, 128, 6>(tma, tmb, args, sms, st);
+      return mc ? run<kScaleMx, 256, 4, false, 2>(tma, tmb, args, sms, st)
+                : run<kScaleMx, 256, 4>(tma, tmb, args, sms, st);
     case kScaleGroupUe8m0:
       if (gemm_tile_n(mode, args.M, args.N, sms) == 128)
-        return run<kScaleGroupUe8m0, 128, 6>(tma, tmb, args, sms, st);
-      return run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, sms, st);
-    case kScaleGroupF32: return run<kScaleGroupF32, 128, 6>(tma, tmb, args, sms, st);
+        return mc ? run<kScaleGroupUe8m0, 128, 6, false, 2>(tma, tmb, args, sms, st)
+                  : run<kScaleGroupUe8m0, 128, 6>(tma, tmb, args, sms, st);
+      return mc ? run<kScaleGroupUe8m0, 256, 4, false, 2>(tma, tmb, args, sms, st)
+                : run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, sms, st);
+    case kScaleGroupF32:
+      return mc ? run<kScaleGroupF32, 128, 6, false, 2>(tma, tmb, args, sms, st)
+                : run<kScaleGroupF32, 128, 6>(tma, tmb, args, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -97,6 +97,10 @@ struct GemmArgs {
   // nullable fp32 [M] and [N] (together): the result is multiplied by
   // row_scale[m] * col_scale[n] (per-row global factors of two-level scaling)
   const float *row_scale, *col_scale;
+  // 1 (block-scaled and FP32-promotion modes, ksplit 1, K-major B, no
+  // experts): clusters of two CTAs on vertically adjacent tiles multicast
+  // the B boxes (the B tensor map's box is then BN / 2 rows)
+  int multicast;
 };
 constexpr int kMaxExperts = 256;
 

@@ -477,8 +477,17 @@ FP8_API const char *fp8_version(void);
  *     mbarrier wait of later GEMM launches (default 2,000,000).  A wait that
  *     runs out records FP8_ERR_TIMEOUT in the device error word and the
  *     kernel exits cleanly (output undefined).  Small values exist to test
- *     that path. */
-typedef enum { FP8_OPT_GEMM_CTA_PAIRS = 1, FP8_OPT_WAIT_LIMIT_US = 2 } fp8_option_t;
+ *     that path.
+ *   FP8_OPT_GEMM_MULTICAST: 1 (default) runs the per-group and block-scaled
+ *     GEMMs that use 128-wide tiles (K-major weights, no split K) as
+ *     clusters of two CTAs on vertically adjacent tiles that share each
+ *     weight box through TMA multicast; 0 gives every CTA its own copy.
+ *     Same results. */
+typedef enum {
+  FP8_OPT_GEMM_CTA_PAIRS = 1,
+  FP8_OPT_WAIT_LIMIT_US = 2,
+  FP8_OPT_GEMM_MULTICAST = 3
+} fp8_option_t;
 FP8_API int fp8_set_option(int option, int value);
 
 #ifdef __cplusplus

@@ -38,6 +38,16 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(F.EXPORTED) == set(declared_symbols())
 
 
+def test_options(lib):
+    f = lib.fp8_set_option
+    f.argtypes = [ctypes.c_int, ctypes.c_int]
+    for opt in (1, 3):  # CTA pairs, multicast: switches
+        assert f(opt, 0) == 0 and f(opt, 1) == 0
+    assert f(2, -1) == -1                           # negative wait bound
+    assert f(2, 2_000_000) == 0
+    assert f(99, 1) == -1                           # unknown option
+
+
 def test_status_strings(lib):
     lib.fp8_status_string.restype = ctypes.c_char_p
     assert lib.fp8_status_string(0) == b"ok"

@@ -144,6 +144,27 @@ def test_gemm_group(mnk, sfmt):
     assert ok, worst
 
 
+@pytest.mark.parametrize("multicast", [0, 1])
+@pytest.mark.parametrize("mnk", [(300, 384, 1024), (1000, 2048, 512)])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_gemm_group_multicast_switch(mnk, sfmt, multicast):
+    """The B-multicast clusters (two CTAs on vertically adjacent row tiles,
+    including a last pair whose second tile lies past M) and the plain
+    launch give results within the bound, for both scale formats (UE8M0
+    beyond M = 256 runs through the E8M0-word block-scaled kernel)."""
+    F = lib()
+    m, n, k = mnk
+    qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=4)
+    F.fp8_set_option(F.OPT_GEMM_MULTICAST, multicast)
+    try:
+        got = run_group(qa, sa, qb, sb, sfmt)
+    finally:
+        F.fp8_set_option(F.OPT_GEMM_MULTICAST, 1)
+    c, e = group_reference(qa, sa, qb, sb, sfmt)
+    ok, worst = OG.check(got, c, e, "bf16")
+    assert ok, worst
+
+
 # -------------------------------------------------------------- two level --
 
 def mx_operands(m, n, k, seed):
