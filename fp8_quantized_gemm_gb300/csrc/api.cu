@@ -601,6 +601,25 @@ int fp8_gemm_group_experts(const uint8_t *a, const void *sa, const uint8_t *b, c
   CUtensorMap tma, tmb;
   if ((rc = encode_operand(&tma, a, K, M, 128)) != FP8_OK) return rc;
   if ((rc = encode_operand(&tmb, b, K, (int64_t)experts * N, bn)) != FP8_OK) return rc;
+  if (mode == fp8k::kScaleGroupUe8m0 && M > 256 && N % 128 == 0) {
+    // as in fp8_gemm_group: the UE8M0 scales become E8M0 words for the
+    // block-scaled kernel; the A words are stored per expert row tile
+    const int64_t G = K / 128, tmax = (M + 127) / 128 + experts;
+    const size_t a_words = (size_t)tmax * (size_t)G * 128, b_words = (size_t)G * experts * N;
+    void *w = nullptr;
+    if ((rc = get_workspace((cudaStream_t)stream, (a_words + b_words) * 4, &w, kWsWords)) != FP8_OK)
+      return rc;
+    uint32_t *la = static_cast<uint32_t *>(w), *lb = la + a_words;
+    if ((rc = to_status(fp8k::launch_ue8m0_words_experts(
+             static_cast<const uint8_t *>(sa), static_cast<const uint8_t *>(sb), offsets, experts,
+             M, N, K, tmax, la, lb, d->sms, (cudaStream_t)stream))) != FP8_OK)
+      return rc;
+    args.sa = la;
+    args.sb = lb;
+    args.ga = args.gb = nullptr;
+    return to_status(
+        fp8k::launch_gemm_experts(fp8k::kScaleMx, bn, tma, tmb, args, d->sms, (cudaStream_t)stream));
+  }
   return to_status(fp8k::launch_gemm_experts(mode, bn, tma, tmb, args, d->sms, (cudaStream_t)stream));
 }
 

@@ -191,9 +191,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   const int ks = args.ksplit;
   const int64_t num_units = num_tiles * ks;
   // Tile origin: rows [m0, row_end) of A and C (row_end ends the expert's
-  // rows), columns [n0, n0 + BN), B tensor-map row brow, scale offset sbo.
+  // rows), columns [n0, n0 + BN), B tensor-map row brow, scale offset sbo,
+  // and (expert-grouped rows) the row tile's index in the list of all
+  // experts' row tiles (atile: the block-scaled mode's per-tile A words).
   struct TileInfo {
-    int64_t m0, n0, row_end, brow, sbo;
+    int64_t m0, n0, row_end, brow, sbo, atile;
   };
   auto tile_info = [&](int64_t t) {
     TileInfo ti;
@@ -210,6 +212,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       ti.row_end = ex_row0[lo + 1];
       ti.brow = (int64_t)lo * args.N + ti.n0;
       ti.sbo = (int64_t)lo * args.sb_expert_stride;
+      ti.atile = ex_tile0[lo] / tiles_n + local / tiles_n;
     } else {
       // (MC == 2: t indexes row-tile pairs; this CTA takes row tile 2p + rank)
       ti.m0 = ((t / tiles_n) * MC + mc_rank) * C::BM;
@@ -217,6 +220,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       ti.row_end = args.M;
       ti.brow = ti.n0;
       ti.sbo = 0;
+      ti.atile = 0;
     }
     return ti;
   };
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
     // origin and k range cached (64-bit divisions once per unit, not per k
     // block: the producer issues every stage and must stay cheap).
     struct Cursor {
-      int64_t u, m0, n0, brow, sbo;
+      int64_t u, m0, n0, brow, sbo, atile;
       int kb, kb_end;
     };
     auto enter = [&](Cursor &c, int64_t u) {
@@ -260,6 +264,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
         c.n0 = ti.n0;
         c.brow = ti.brow;
         c.sbo = ti.sbo;
+        c.atile = ti.atile;
         c.kb = kb_begin(u);
         c.kb_end = kb_end(u);
       }
@@ -328,11 +333,15 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
         uint32_t sfb_bytes = 0;
         // (a multicast CTA whose row tile lies past M loads no A factors)
         const int64_t a_mpad = (args.M + 127) / 128 * 128;
+        // block-scaled words: B rows n (or e * N + n with experts) of the
+        // [K/128][rows padded to 128] word array
+        const int64_t b_rows = EXPERTS ? (int64_t)args.experts * args.N : args.N;
+        const int64_t b_npad = (b_rows + 127) / 128 * 128;
+        const bool a_words = EXPERTS || m0 < a_mpad;
         if constexpr (MODE == kScaleMx) {
-          const int64_t npad = (args.N + 127) / 128 * 128;
-          const int64_t rows = (npad - n0) < BN ? (npad - n0) : BN;
+          const int64_t rows = (b_npad - brow) < BN ? (b_npad - brow) : BN;
           sfb_bytes = (uint32_t)rows * 4u;
-          tx += (m0 < a_mpad ? C::kSfaBytes : 0u) + sfb_bytes;
+          tx += (a_words ? C::kSfaBytes : 0u) + sfb_bytes;
         }
         mbar_arrive_expect_tx(full_bar(s), tx);
         // tensor-map coordinates are (contiguous dim, row); an MN-major
@@ -354,10 +363,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
           tma_load_2d(sB(s), &tmb, full_bar(s), k0, (int32_t)brow);
         }
         if constexpr (MODE == kScaleMx) {
-          const int64_t npad = (args.N + 127) / 128 * 128;
-          const uint32_t *la = static_cast<const uint32_t *>(args.sa) + (int64_t)kb * a_mpad + m0;
-          const uint32_t *lb = static_cast<const uint32_t *>(args.sb) + (int64_t)kb * npad + n0;
-          if (m0 < a_mpad) bulk_load(smem_u32(sSfa(s)), la, C::kSfaBytes, full_bar(s));
+          // A words: [K/128][M padded] by row, or with experts per row tile,
+          // [tile][K/128][128]
+          const uint32_t *la = static_cast<const uint32_t *>(args.sa) +
+                               (EXPERTS ? (cur.atile * KB + kb) * 128 : (int64_t)kb * a_mpad + m0);
+          const uint32_t *lb = static_cast<const uint32_t *>(args.sb) + (int64_t)kb * b_npad + brow;
+          if (a_words) bulk_load(smem_u32(sSfa(s)), la, C::kSfaBytes, full_bar(s));
           bulk_load(smem_u32(sSfb(s)), lb, sfb_bytes, full_bar(s));
         }
       }
@@ -774,6 +785,10 @@ int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster
 cudaError_t launch_gemm_experts(int mode, int bn, const CUtensorMap &tma, const CUtensorMap &tmb,
                                 const GemmArgs &args, int sms, cudaStream_t st) {
   if (mode == kScaleGroupF32) return run<kScaleGroupF32, 128, 6, true>(tma, tmb, args, sms, st);
+  if (mode == kScaleMx) {
+    if (bn == 128) return run<kScaleMx, 128, 6, true>(tma, tmb, args, sms, st);
+    return run<kScaleMx, 256, 4, true>(tma, tmb, args, sms, st);
+  }
   if (mode != kScaleGroupUe8m0) return cudaErrorInvalidValue;
   if (bn == 128) return run<kScaleGroupUe8m0, 128, 6, true>(tma, tmb, args, sms, st);
   return run<kScaleGroupUe8m0, 256, 4, true>(tma, tmb, args, sms, st);

@@ -26,6 +26,10 @@ cudaError_t launch_row_amax(const void *x, int in_dt, int64_t R, int64_t K, floa
                             cudaStream_t st);
 cudaError_t launch_ue8m0_words(const uint8_t *sa, const uint8_t *sb, int64_t M, int64_t N,
                                int64_t K, uint32_t *la, uint32_t *lb, int sms, cudaStream_t st);
+cudaError_t launch_ue8m0_words_experts(const uint8_t *sa, const uint8_t *sb,
+                                       const int32_t *offsets, int E, int64_t M, int64_t N,
+                                       int64_t K, int64_t tmax, uint32_t *la, uint32_t *lb,
+                                       int sms, cudaStream_t st);
 cudaError_t launch_quant_block32(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
                                  uint8_t *q, uint8_t *scales, uint32_t *local, int sms,
                                  cudaStream_t st);

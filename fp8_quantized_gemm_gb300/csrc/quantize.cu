@@ -734,6 +734,93 @@ cudaError_t launch_ue8m0_words(const uint8_t *sa, const uint8_t *sb, int64_t M, 
   return cudaGetLastError();
 }
 
+// Expert-grouped rows (expert e owns rows [o_e, o_{e+1}), cut into
+// ceil(rows_e / 128) row tiles, the tiles of all experts in order): the A
+// words are stored per row tile, [tile][K/128][128] in the MMA's order, so a
+// tile that starts at any row reads one contiguous 512-byte slice per k
+// block.  The B words use the plain layout over the E * N weight rows
+// (N % 128 == 0, so no expert's rows share a 128-row block).
+__global__ void __launch_bounds__(256)
+    ue8m0_words_experts_kernel(const uint8_t *__restrict__ sa, const uint8_t *__restrict__ sb,
+                               const int32_t *__restrict__ offsets, int E, int64_t M, int64_t N,
+                               int64_t G, int64_t tmax, uint32_t *__restrict__ la,
+                               uint32_t *__restrict__ lb) {
+  __shared__ int32_t rt0[kMaxExperts + 1];   // first row tile of each expert
+  __shared__ int32_t row0[kMaxExperts + 1];  // first row of each expert
+  if (threadIdx.x < 32) {
+    const int l = (int)threadIdx.x;
+    int cnt[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 8 * l + i;
+      cnt[i] = 0;
+      if (e < E) {
+        const int32_t r0 = offsets[e], r1 = offsets[e + 1];
+        row0[e] = r0;
+        cnt[i] = r1 > r0 ? (r1 - r0 + 127) / 128 : 0;
+        if (e == E - 1) row0[E] = r1;
+      }
+      sum += cnt[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (l >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 8 * l + i;
+      if (e < E) rt0[e] = run;
+      run += cnt[i];
+      if (e == E - 1) rt0[E] = run;
+    }
+  }
+  __syncthreads();
+  const int T = rt0[E];
+  const int64_t R = (int64_t)E * N;
+  const int64_t na = tmax * G * 128, total = na + G * R;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t b = 127u;
+    if (i < na) {
+      const int64_t j = i / (G * 128), rem = i - j * (G * 128);
+      const int64_t g = rem >> 7, p = rem & 127;
+      const int64_t ir = 32 * (p & 3) + (p >> 2);  // tile row of word p
+      if (j < T) {
+        int lo = 0, hi = E;  // the expert with rt0[lo] <= j < rt0[lo + 1]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (rt0[mid] <= j) lo = mid; else hi = mid;
+        }
+        while (lo + 1 < E && rt0[lo + 1] <= j) ++lo;
+        const int64_t r = row0[lo] + (j - rt0[lo]) * 128 + ir;
+        if (r < row0[lo + 1]) b = sa[g * M + r];
+      }
+      la[i] = b * 0x01010101u;
+    } else {
+      const int64_t k = i - na, g = k / R, w = k - g * R;
+      const int64_t r = (w & ~(int64_t)127) + 32 * (w & 3) + ((w & 127) >> 2);
+      const int64_t e = r / N, n = r - e * N;
+      b = sb[e * ((N / 128) * G) + (n >> 7) * G + g];
+      lb[k] = b * 0x01010101u;
+    }
+  }
+}
+
+cudaError_t launch_ue8m0_words_experts(const uint8_t *sa, const uint8_t *sb,
+                                       const int32_t *offsets, int E, int64_t M, int64_t N,
+                                       int64_t K, int64_t tmax, uint32_t *la, uint32_t *lb,
+                                       int sms, cudaStream_t st) {
+  const int64_t G = K / 128;
+  const int64_t words = tmax * G * 128 + G * (int64_t)E * N;
+  const int threads = 256, blocks = grid_for(words, threads, 8, sms);
+  ue8m0_words_experts_kernel<<<blocks, threads, 0, st>>>(sa, sb, offsets, E, M, N, G, tmax, la,
+                                                         lb);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------- row amax --
 // amax_out[r] = max |x[r, :]|: one warp per row, 16-byte loads, the same
 // order-preserving keys as the tensor amax (exact).

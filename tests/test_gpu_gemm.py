@@ -536,8 +536,11 @@ def expert_operands(experts, tokens, n, k, sfmt, seed, counts=None):
     (5, 0, 384, 512, [0, 300, 1, 0, 129]),       # empty experts, a 1-row expert
     (3, 0, 200, 256, [130, 0, 257]),             # N not a multiple of 128
     (16, 4096, 512, 2048, None),
+    (8, 4096, 2048, 1024, None),                 # 128 x 256 tiles
 ])
 def test_gemm_group_experts(sfmt, case):
+    """Beyond M = 256 with N % 128 == 0 the UE8M0 case runs as the
+    block-scaled kernel on per-expert-row-tile E8M0 words."""
     F = lib()
     experts, tokens, n, k, counts = case
     if counts is not None:
