@@ -41,6 +41,9 @@ constexpr uint32_t pow2_cols(uint32_t c) {
   return p;
 }
 
+// Row tiles per band of the grouped tile order (see tile_info).
+constexpr int64_t kBandRows = 16;
+
 template <int MODE, int BN, int STAGES>
 struct Cfg {
   static constexpr int BM = 128, BK = 128;
@@ -214,9 +217,19 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       ti.sbo = (int64_t)lo * args.sb_expert_stride;
       ti.atile = ex_tile0[lo] / tiles_n + local / tiles_n;
     } else {
-      // (MC == 2: t indexes row-tile pairs; this CTA takes row tile 2p + rank)
-      ti.m0 = ((t / tiles_n) * MC + mc_rank) * C::BM;
-      ti.n0 = (t % tiles_n) * BN;
+      // Grouped order: bands of kBandRows row tiles (row-tile pairs when
+      // MC == 2), each walked column by column, so the CTAs in flight share
+      // a few A row blocks and B column blocks and both stay in L2 (a plain
+      // row-major order streams all of B once per wave of row blocks).
+      const int64_t rows = MC == 2 ? (row_tiles + 1) / 2 : row_tiles;
+      const int64_t band = t / (kBandRows * tiles_n);
+      const int64_t band_rows =
+          rows - band * kBandRows < kBandRows ? rows - band * kBandRows : kBandRows;
+      const int64_t local = t - band * kBandRows * tiles_n;
+      const int64_t mt = band * kBandRows + local % band_rows;
+      // (MC == 2: mt indexes row-tile pairs; this CTA takes row tile 2 mt + rank)
+      ti.m0 = (mt * MC + mc_rank) * C::BM;
+      ti.n0 = (local / band_rows) * BN;
       ti.row_end = args.M;
       ti.brow = ti.n0;
       ti.sbo = 0;

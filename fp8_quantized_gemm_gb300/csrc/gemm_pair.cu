@@ -36,6 +36,9 @@
 
 namespace fp8k {
 
+// 256-row tiles per band of the grouped tile order (see tile_ref).
+constexpr int64_t kPairBandRows = 8;
+
 template <int BN, int STAGES>
 struct PairCfg {
   static constexpr int BM = 128, BK = 128;  // rows per CTA (256 per pair)
@@ -134,8 +137,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
     const GemmArgs &a = grp.args[r.i];
     const int64_t t = gt - grp.tile_begin[r.i];
     const int64_t tiles_n = (a.N + BN - 1) / BN;
-    r.m0 = (t / tiles_n) * 256;
-    r.n0 = (t % tiles_n) * BN;
+    // grouped order: bands of kPairBandRows 256-row tiles walked column by
+    // column, so the pairs in flight share A and B blocks in L2
+    const int64_t rows = (a.M + 255) / 256;
+    const int64_t band = t / (kPairBandRows * tiles_n);
+    const int64_t band_rows =
+        rows - band * kPairBandRows < kPairBandRows ? rows - band * kPairBandRows : kPairBandRows;
+    const int64_t local = t - band * kPairBandRows * tiles_n;
+    r.m0 = (band * kPairBandRows + local % band_rows) * 256;
+    r.n0 = (local / band_rows) * BN;
     r.kb_count = (int)((a.K + C::BK - 1) / C::BK);
     return r;
   };

@@ -706,31 +706,34 @@ cudaError_t launch_quant_block32(const void *w, int in_dt, int64_t N, int64_t K,
 // the group's factor).  Word i of slice g (i < R_pad) belongs to row
 // (i & ~127) + 32 (i & 3) + ((i & 127) >> 2), the inverse of mx_word_index;
 // padding rows get byte 127 (factor 1).
+// Grid: x over the words of one K slice (4 per thread), y over the K slices
+// g, z = operand (0 A, 1 B); no divisions.
 __global__ void __launch_bounds__(256)
     ue8m0_words_kernel(const uint8_t *__restrict__ sa, const uint8_t *__restrict__ sb,
                        int64_t M, int64_t N, int64_t G, uint32_t *__restrict__ la,
                        uint32_t *__restrict__ lb) {
-  const int64_t mpad = (M + 127) / 128 * 128, npad = (N + 127) / 128 * 128;
-  const int64_t na = G * mpad, total = na + G * npad;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const bool is_a = i < na;
-    const int64_t j = is_a ? i : i - na, pad = is_a ? mpad : npad;
-    const int64_t g = j / pad, w = j - g * pad;
-    const int64_t r = (w & ~(int64_t)127) + 32 * (w & 3) + ((w & 127) >> 2);
-    uint32_t b = 127u;
-    if (is_a && r < M) b = sa[g * M + r];
-    if (!is_a && r < N) b = sb[(r >> 7) * G + g];
-    (is_a ? la : lb)[j] = b * 0x01010101u;
+  const bool is_a = blockIdx.z == 0;
+  const int64_t R = is_a ? M : N, pad = (R + 127) / 128 * 128;
+  for (int64_t g = blockIdx.y; g < G; g += gridDim.y) {
+    uint32_t *dst = (is_a ? la : lb) + g * pad;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t w = ((int64_t)blockIdx.x * 4 + u) * blockDim.x + threadIdx.x;
+      if (w >= pad) break;
+      const int64_t r = (w & ~(int64_t)127) + 32 * (w & 3) + ((w & 127) >> 2);
+      uint32_t b = 127u;
+      if (r < R) b = is_a ? sa[g * M + r] : sb[(r >> 7) * G + g];
+      dst[w] = b * 0x01010101u;
+    }
   }
 }
 
 cudaError_t launch_ue8m0_words(const uint8_t *sa, const uint8_t *sb, int64_t M, int64_t N,
                                int64_t K, uint32_t *la, uint32_t *lb, int sms, cudaStream_t st) {
-  const int64_t G = K / 128;
-  const int64_t words = G * ((M + 127) / 128 * 128 + (N + 127) / 128 * 128);
-  const int threads = 256, blocks = grid_for(words, threads, 8, sms);
-  ue8m0_words_kernel<<<blocks, threads, 0, st>>>(sa, sb, M, N, G, la, lb);
+  (void)sms;
+  const int64_t G = K / 128, pad = ((M > N ? M : N) + 127) / 128 * 128;
+  const dim3 grid((unsigned)((pad + 1023) / 1024), (unsigned)(G < 65535 ? G : 65535), 2);
+  ue8m0_words_kernel<<<grid, 256, 0, st>>>(sa, sb, M, N, G, la, lb);
   return cudaGetLastError();
 }
 
@@ -778,33 +781,38 @@ __global__ void __launch_bounds__(256)
     }
   }
   __syncthreads();
+  // grid: y over the K slices g, z = operand (0 A, 1 B), x over a slice's words
   const int T = rt0[E];
-  const int64_t R = (int64_t)E * N;
-  const int64_t na = tmax * G * 128, total = na + G * R;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    uint32_t b = 127u;
-    if (i < na) {
-      const int64_t j = i / (G * 128), rem = i - j * (G * 128);
-      const int64_t g = rem >> 7, p = rem & 127;
-      const int64_t ir = 32 * (p & 3) + (p >> 2);  // tile row of word p
-      if (j < T) {
-        int lo = 0, hi = E;  // the expert with rt0[lo] <= j < rt0[lo + 1]
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (rt0[mid] <= j) lo = mid; else hi = mid;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t g = blockIdx.y; g < G; g += gridDim.y) {
+    if (blockIdx.z == 0) {
+      // A: word p of row tile j at la[(j * G + g) * 128 + p]
+      for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < tmax * 128; w += stride) {
+        const int64_t j = w >> 7, p = w & 127;
+        const int64_t ir = 32 * (p & 3) + (p >> 2);  // tile row of word p
+        uint32_t b = 127u;
+        if (j < T) {
+          int lo = 0, hi = E;  // the expert with rt0[lo] <= j < rt0[lo + 1]
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (rt0[mid] <= j) lo = mid; else hi = mid;
+          }
+          while (lo + 1 < E && rt0[lo + 1] <= j) ++lo;
+          const int64_t r = row0[lo] + (j - rt0[lo]) * 128 + ir;
+          if (r < row0[lo + 1]) b = sa[g * M + r];
         }
-        while (lo + 1 < E && rt0[lo + 1] <= j) ++lo;
-        const int64_t r = row0[lo] + (j - rt0[lo]) * 128 + ir;
-        if (r < row0[lo + 1]) b = sa[g * M + r];
+        la[(j * G + g) * 128 + p] = b * 0x01010101u;
       }
-      la[i] = b * 0x01010101u;
     } else {
-      const int64_t k = i - na, g = k / R, w = k - g * R;
-      const int64_t r = (w & ~(int64_t)127) + 32 * (w & 3) + ((w & 127) >> 2);
-      const int64_t e = r / N, n = r - e * N;
-      b = sb[e * ((N / 128) * G) + (n >> 7) * G + g];
-      lb[k] = b * 0x01010101u;
+      // B: the plain layout over the E * N weight rows (e = r / N, 32-bit)
+      const int64_t R = (int64_t)E * N;
+      const uint32_t n32 = (uint32_t)N;
+      for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < R; w += stride) {
+        const int64_t r = (w & ~(int64_t)127) + 32 * (w & 3) + ((w & 127) >> 2);
+        const uint32_t e = (uint32_t)r / n32, n = (uint32_t)r - e * n32;
+        const uint32_t b = sb[(int64_t)e * ((N / 128) * G) + (int64_t)(n >> 7) * G + g];
+        lb[g * R + w] = b * 0x01010101u;
+      }
     }
   }
 }
@@ -813,11 +821,12 @@ cudaError_t launch_ue8m0_words_experts(const uint8_t *sa, const uint8_t *sb,
                                        const int32_t *offsets, int E, int64_t M, int64_t N,
                                        int64_t K, int64_t tmax, uint32_t *la, uint32_t *lb,
                                        int sms, cudaStream_t st) {
+  (void)sms;
   const int64_t G = K / 128;
-  const int64_t words = tmax * G * 128 + G * (int64_t)E * N;
-  const int threads = 256, blocks = grid_for(words, threads, 8, sms);
-  ue8m0_words_experts_kernel<<<blocks, threads, 0, st>>>(sa, sb, offsets, E, M, N, G, tmax, la,
-                                                         lb);
+  const int64_t per_slice = tmax * 128 > (int64_t)E * N ? tmax * 128 : (int64_t)E * N;
+  const int64_t bx = (per_slice + 4 * 256 - 1) / (4 * 256);
+  const dim3 grid((unsigned)bx, (unsigned)(G < 65535 ? G : 65535), 2);
+  ue8m0_words_experts_kernel<<<grid, 256, 0, st>>>(sa, sb, offsets, E, M, N, G, tmax, la, lb);
   return cudaGetLastError();
 }
 
