@@ -43,6 +43,9 @@ constexpr uint32_t pow2_cols(uint32_t c) {
 
 // Row tiles per band of the grouped tile order (see tile_info).
 constexpr int64_t kBandRows = 16;
+// Pipeline depth of the FP32-promotion mode (32 KB stages, no scale-factor
+// staging; seven fit beside no expert tables but measured no faster).
+constexpr int kF32Stages = 6;
 
 template <int MODE, int BN, int STAGES>
 struct Cfg {
@@ -767,7 +770,7 @@ static int max_active_clusters(int mode, int bn, int size) {
         n = w == 0 ? active_clusters<kScaleGroupUe8m0, 128, 6>(size)
                    : active_clusters<kScaleGroupUe8m0, 256, 4>(size);
         break;
-      default: n = active_clusters<kScaleGroupF32, 128, 6>(size); break;
+      default: n = active_clusters<kScaleGroupF32, 128, kF32Stages>(size); break;
     }
     cache[dev][mode][w][size] = n;
     have[dev][mode][w][size] = true;
@@ -797,6 +800,7 @@ int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster
 
 cudaError_t launch_gemm_experts(int mode, int bn, const CUtensorMap &tma, const CUtensorMap &tmb,
                                 const GemmArgs &args, int sms, cudaStream_t st) {
+  // (six stages: the expert tables take 3 KB of static shared memory)
   if (mode == kScaleGroupF32) return run<kScaleGroupF32, 128, 6, true>(tma, tmb, args, sms, st);
   if (mode == kScaleMx) {
     if (bn == 128) return run<kScaleMx, 128, 6, true>(tma, tmb, args, sms, st);
@@ -826,8 +830,8 @@ cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb
       return mc ? run<kScaleGroupUe8m0, 256, 4, false, 2>(tma, tmb, args, sms, st)
                 : run<kScaleGroupUe8m0, 256, 4>(tma, tmb, args, sms, st);
     case kScaleGroupF32:
-      return mc ? run<kScaleGroupF32, 128, 6, false, 2>(tma, tmb, args, sms, st)
-                : run<kScaleGroupF32, 128, 6>(tma, tmb, args, sms, st);
+      return mc ? run<kScaleGroupF32, 128, kF32Stages, false, 2>(tma, tmb, args, sms, st)
+                : run<kScaleGroupF32, 128, kF32Stages>(tma, tmb, args, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }
