@@ -316,7 +316,7 @@ def fp8_get_last_device_error(stream=None):
     return rc, where.value
 
 
-OPT_GEMM_CTA_PAIRS, OPT_WAIT_LIMIT_US, OPT_GEMM_MULTICAST = 1, 2, 3
+OPT_GEMM_CTA_PAIRS, OPT_WAIT_LIMIT_US, OPT_GEMM_MULTICAST, OPT_GEMM_TMA_STORE = 1, 2, 3, 4
 
 
 def fp8_set_option(option, value):

@@ -52,6 +52,8 @@ std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_ws;
 bool g_use_pairs = true;
 // B-multicast clusters in the single-CTA GEMM (on by default).
 bool g_use_multicast = true;
+// TMA-store epilogue of the CTA-pair GEMM (on by default).
+bool g_use_tma_store = true;
 // Bound of every device-side mbarrier wait (fp8_set_option).
 uint64_t g_wait_limit_ns = 2000000000ull;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -131,6 +133,24 @@ int encode_gemm_operand(CUtensorMap *map, const void *base, int mn_major, int64_
                   : encode_operand(map, base, k, rows, box_rows);
 }
 
+// Output C [M, N] (pitch ldc elements) for the CTA-pair kernel's TMA-store
+// epilogue: boxes of 32 rows x 128 bytes (64 bf16 or 32 fp32), 128-byte
+// swizzle.  Needs a 16-byte aligned base and pitch.
+int encode_output(CUtensorMap *map, void *c, int out_dt, int64_t M, int64_t N, int64_t ldc) {
+  const cuuint64_t es = out_dt == FP8_OUT_F32 ? 4 : 2;
+  const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)ldc * es};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / es), 32u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(map,
+                        out_dt == FP8_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, c, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
 int check_output(const void *c, int64_t N, int64_t ldc, int out_dt) {
   if (c == nullptr) return FP8_ERR_INVALID_ARG;
   if (out_dt != FP8_OUT_F32 && out_dt != FP8_OUT_BF16) return FP8_ERR_INVALID_ARG;
@@ -144,6 +164,12 @@ int check_output(const void *c, int64_t N, int64_t ldc, int out_dt) {
 int vector_store_ok(const void *c, int64_t ldc, int out_dt) {
   const int64_t es = out_dt == FP8_OUT_F32 ? 4 : 2;
   return aligned16(c) && (ldc * es) % 16 == 0 ? 1 : 0;
+}
+
+// Whether the CTA-pair epilogue may write C with TMA stores (plain stores
+// otherwise: accumulation, or an unaligned base or pitch).
+bool use_tma_store(const void *c, int64_t ldc, int out_dt, int accumulate) {
+  return g_use_tma_store && accumulate == 0 && vector_store_ok(c, ldc, out_dt);
 }
 
 int get_workspace(cudaStream_t st, size_t need, void **out, int slot = kWsSplit) {
@@ -196,7 +222,12 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
     if ((rc = encode_gemm_operand(&tmb, b, args.b_mn, args.K, args.N,
                                   fp8k::gemm_pair_b_rows())) != FP8_OK)
       return rc;
-    return to_status(fp8k::launch_gemm_pair(tma, tmb, args, d->sms, st));
+    CUtensorMap tmc{};
+    args.tma_store = use_tma_store(args.c, args.ldc, args.out_dt, args.accumulate) ? 1 : 0;
+    if (args.tma_store &&
+        (rc = encode_output(&tmc, args.c, args.out_dt, args.M, args.N, args.ldc)) != FP8_OK)
+      return rc;
+    return to_status(fp8k::launch_gemm_pair(tma, tmb, tmc, args, d->sms, st));
   }
   // multicast pairs of vertically adjacent tiles share each B box: measured
   // faster for 128-wide tiles (the FP32-promotion mode, and the block-scaled
@@ -505,7 +536,7 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
       order[j] = order[j - 1];
       order[j - 1] = tmp;
     }
-  CUtensorMap tma[fp8k::kMaxGroup], tmb[fp8k::kMaxGroup];
+  CUtensorMap tma[fp8k::kMaxGroup], tmb[fp8k::kMaxGroup], tmc[fp8k::kMaxGroup] = {};
   GemmArgs args[fp8k::kMaxGroup];
   for (int k = 0; k < count; ++k) {
     const fp8_gemm_problem_t &p = problems[order[k]];
@@ -519,13 +550,16 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
     a.b_mn = p.b_layout == FP8_MN_MAJOR;
     a.bias = p.bias;
     a.ksplit = 1;
+    a.tma_store = use_tma_store(p.c, p.ldc, p.out_dt, p.accumulate) ? 1 : 0;
+    if (a.tma_store && (rc = encode_output(&tmc[k], p.c, p.out_dt, p.M, p.N, p.ldc)) != FP8_OK)
+      return rc;
     args[k] = a;
     if ((rc = encode_gemm_operand(&tma[k], p.a, a.a_mn, p.K, p.M, 128)) != FP8_OK) return rc;
     if ((rc = encode_gemm_operand(&tmb[k], p.b, a.b_mn, p.K, p.N, fp8k::gemm_pair_b_rows())) !=
         FP8_OK)
       return rc;
   }
-  return to_status(fp8k::launch_gemm_pair_group(tma, tmb, args, count, d->sms, st));
+  return to_status(fp8k::launch_gemm_pair_group(tma, tmb, tmc, args, count, d->sms, st));
 }
 
 int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb, int sfmt,
@@ -757,6 +791,10 @@ int fp8_get_last_device_error(int *where_out, fp8_stream_t stream) {
 int fp8_set_option(int option, int value) {
   if (option == FP8_OPT_GEMM_CTA_PAIRS) {
     g_use_pairs = value != 0;
+    return FP8_OK;
+  }
+  if (option == FP8_OPT_GEMM_TMA_STORE) {
+    g_use_tma_store = value != 0;
     return FP8_OK;
   }
   if (option == FP8_OPT_GEMM_MULTICAST) {

@@ -51,7 +51,10 @@ struct PairCfg {
   static constexpr int kAccBufs = 2;
   static constexpr uint32_t kTmemCols = kAccBufs * BN;
   static constexpr int kNumBars = 2 * STAGES + 2 * kAccBufs + 1;
-  static constexpr uint32_t kSmem = 1024 + kTileBytes + 8 * kNumBars + 16;
+  // TMA-store staging: per epilogue warp two 32-row x 128-byte boxes
+  static constexpr uint32_t kOutBox = 32 * 128;
+  static constexpr uint32_t kOutBytes = kEpiWarps * 2 * kOutBox;
+  static constexpr uint32_t kSmem = 1024 + kTileBytes + kOutBytes + 8 * kNumBars + 16;
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kSmem <= 227 * 1024, "shared-memory budget");
   static_assert(BM == 128 && BN / 2 == 128, "MN-major tiles: one 128-wide TMA box per operand");
@@ -60,6 +63,7 @@ struct PairCfg {
 struct PairGroup {
   CUtensorMap tma[kMaxGroup];
   CUtensorMap tmb[kMaxGroup];
+  CUtensorMap tmc[kMaxGroup];  // outputs (problems with args.tma_store)
   GemmArgs args[kMaxGroup];
   int64_t tile_begin[kMaxGroup + 1];  // problem i owns tiles [tile_begin[i], tile_begin[i+1])
   int count;
@@ -79,7 +83,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kTileBytes);
+  uint8_t *out_stage = smem + C::kTileBytes;  // 1024-aligned (kTileBytes is)
+  uint64_t *bars = reinterpret_cast<uint64_t *>(out_stage + C::kOutBytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -243,7 +248,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
     const uint32_t q = warp & 3u;
     const uint32_t lane_base = tmem + ((32u * q) << 16);
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
-    uint32_t j = 0;
+    const uint64_t out_policy = policy_evict_first();
+    uint32_t j = 0, out_n = 0;
     for (int64_t gt = pair; gt < num_tiles; gt += npairs, ++j) {
       const TileRef tr = tile_ref(gt);
       const GemmArgs &a = grp.args[tr.i];
@@ -252,6 +258,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
       const uint32_t buf = j & 1u, use = j >> 1;
       if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) break;
       tc_fence_after();
+      if (a.tma_store) {
+        // 128-byte column chunks (64 bf16 or 32 fp32 values per row) staged
+        // as a 32-row box in this warp's two alternating buffers (128-byte
+        // swizzle: 16-byte unit u of row l at l * 128 + (u ^ (l & 7)) * 16)
+        // and written by one TMA store each
+        const bool f32 = a.out_dt == 0;
+        const int cw = f32 ? 32 : 64;
+        const int32_t row0 = (int32_t)(tr.m0 + rank * C::BM + 32 * q);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += cw) {
+          uint32_t r[64];
+          FP8K_TMEM_LD_X32(lane_base + buf * BN + (uint32_t)c, r);
+          if (!f32) FP8K_TMEM_LD_X32(lane_base + buf * BN + (uint32_t)c + 32, (r + 32));
+          tmem_ld_wait();
+          if (c + cw == BN) {  // accumulator read out: hand it back to the leader
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acce_leader0 + 8u * buf);
+          }
+          const int64_t col0 = tr.n0 + c;
+          uint32_t packed[32];
+          if (f32) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float v = __uint_as_float(r[i]) * alpha;
+              if (a.bias != nullptr && col0 + i < a.N) v += __ldg(a.bias + col0 + i);
+              packed[i] = __float_as_uint(v);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float v0 = __uint_as_float(r[2 * i]) * alpha, v1 = __uint_as_float(r[2 * i + 1]) * alpha;
+              if (a.bias != nullptr) {
+                if (col0 + 2 * i < a.N) v0 += __ldg(a.bias + col0 + 2 * i);
+                if (col0 + 2 * i + 1 < a.N) v1 += __ldg(a.bias + col0 + 2 * i + 1);
+              }
+              const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+              packed[i] = *reinterpret_cast<const uint32_t *>(&h);
+            }
+          }
+          // boxes wholly past M or N are not stored (a partial box is
+          // clipped by TMA); the buffers alternate per store issued, so the
+          // store two back, the last reader of this buffer, has read it
+          if (row0 < a.M && col0 < a.N) {
+            uint8_t *box = out_stage + ((warp - 2) * 2 + (out_n & 1u)) * C::kOutBox;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4 *>(box + lane * 128 + ((u ^ (lane & 7)) << 4)) = make_uint4(
+                  packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d_hint(&grp.tmc[tr.i], smem_u32(box), (int32_t)col0, row0, out_policy);
+              bulk_commit();
+            }
+            ++out_n;
+          }
+        }
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
@@ -268,6 +336,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
         store_row32(a, row, tr.n0 + c, v);
       }
     }
+    // every TMA store has finished reading its box and writing C
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -291,7 +362,8 @@ bool gemm_pair_eligible(int mode, int64_t M, int64_t N, int sms) {
 }
 
 cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tmb,
-                                   const GemmArgs *args, int count, int sms, cudaStream_t st) {
+                                   const CUtensorMap *tmc, const GemmArgs *args, int count,
+                                   int sms, cudaStream_t st) {
   using C = PairCfg<kPairBN, kPairStages>;
   if (count < 1 || count > kMaxGroup) return cudaErrorInvalidValue;
   auto kern = gemm_pair_kernel<kPairBN, kPairStages>;
@@ -311,7 +383,9 @@ cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tm
   for (int i = 0; i < count; ++i) {
     g.tma[i] = tma[i];
     g.tmb[i] = tmb[i];
+    if (tmc != nullptr) g.tmc[i] = tmc[i];
     g.args[i] = args[i];
+    if (tmc == nullptr) g.args[i].tma_store = 0;
     g.tile_begin[i + 1] = g.tile_begin[i] + gemm_pair_tiles(args[i].M, args[i].N);
   }
   for (int i = count; i < kMaxGroup; ++i) g.tile_begin[i + 1] = g.tile_begin[count];
@@ -321,9 +395,10 @@ cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tm
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
-                             int sms, cudaStream_t st) {
-  return launch_gemm_pair_group(&tma, &tmb, &args, 1, sms, st);
+cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb,
+                             const CUtensorMap &tmc, const GemmArgs &args, int sms,
+                             cudaStream_t st) {
+  return launch_gemm_pair_group(&tma, &tmb, &tmc, &args, 1, sms, st);
 }
 
 }  // namespace fp8k

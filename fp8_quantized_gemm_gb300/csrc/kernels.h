@@ -105,6 +105,10 @@ struct GemmArgs {
   // experts): clusters of two CTAs on vertically adjacent tiles multicast
   // the B boxes (the B tensor map's box is then BN / 2 rows)
   int multicast;
+  // 1 (CTA-pair kernel; no accumulate, 16-byte aligned c and pitch): the
+  // epilogue writes C through shared memory with TMA stores of 32-row x
+  // 128-byte boxes (the kernel gets the output tensor map separately)
+  int tma_store;
 };
 constexpr int kMaxExperts = 256;
 
@@ -131,10 +135,13 @@ cudaError_t launch_gemm_experts(int mode, int bn, const CUtensorMap &tma, const 
 bool gemm_pair_eligible(int mode, int64_t M, int64_t N, int sms);
 constexpr int kMaxGroup = 4;  // problems per grouped launch
 // One launch over `count` independent per-tensor problems (longest K first).
+// tmc[i]: the output tensor map of problem i (read when args[i].tma_store).
 cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tmb,
-                                   const GemmArgs *args, int count, int sms, cudaStream_t st);
+                                   const CUtensorMap *tmc, const GemmArgs *args, int count,
+                                   int sms, cudaStream_t st);
 int gemm_pair_b_rows();
-cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb, const GemmArgs &args,
-                             int sms, cudaStream_t st);
+cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb,
+                             const CUtensorMap &tmc, const GemmArgs &args, int sms,
+                             cudaStream_t st);
 
 }  // namespace fp8k

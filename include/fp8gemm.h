@@ -482,11 +482,16 @@ FP8_API const char *fp8_version(void);
  *     GEMMs that use 128-wide tiles (K-major weights, no split K) as
  *     clusters of two CTAs on vertically adjacent tiles that share each
  *     weight box through TMA multicast; 0 gives every CTA its own copy.
- *     Same results. */
+ *     Same results.
+ *   FP8_OPT_GEMM_TMA_STORE: 1 (default) lets the CTA-pair per-tensor GEMM
+ *     write C through shared memory with TMA stores (when c and ldc allow
+ *     16-byte vectors and accumulate is 0); 0 keeps plain per-thread row
+ *     stores.  Same bytes. */
 typedef enum {
   FP8_OPT_GEMM_CTA_PAIRS = 1,
   FP8_OPT_WAIT_LIMIT_US = 2,
-  FP8_OPT_GEMM_MULTICAST = 3
+  FP8_OPT_GEMM_MULTICAST = 3,
+  FP8_OPT_GEMM_TMA_STORE = 4
 } fp8_option_t;
 FP8_API int fp8_set_option(int option, int value);
 

@@ -339,6 +339,39 @@ def test_gemm_tensor_cta_pairs(mnk, fmts):
     assert rc == 0, (rc, where)
 
 
+@pytest.mark.parametrize("pad", [24, 3])
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_gemm_tensor_tma_store_epilogue(out_dtype, pad):
+    """The CTA-pair epilogue writes C with TMA stores when c and its pitch
+    allow 16-byte vectors (pad 24: a pitched output, ldc = N + 24) and with
+    per-thread stores otherwise (pad 3); both, with a bias, ragged M and N,
+    and the switch off, leave the padding columns untouched and agree with
+    the oracle."""
+    F = lib()
+    m, n, k = 1999, 1000, 512
+    qa, sa, qb, sb = per_tensor_operands(m, n, k, "e4m3", "e4m3", seed=31)
+    bias = _bias(n, 5)
+    c, e = OG.gemm(OG.dequant_operand(qa, "e4m3", sa), OG.dequant_operand(qb, "e4m3", sb))
+    cb, eb, extra = OG.gemm_bias(c, e, bias)
+    dt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+    a, b = dev_u8(qa), dev_u8(qb)
+    try:
+        for tma in (1, 0):
+            F.fp8_set_option(F.OPT_GEMM_TMA_STORE, tma)
+            full = torch.full((m, n + pad), 7.0, dtype=dt, device="cuda")
+            F.fp8_gemm_tensor_grouped([F.gemm_problem(a, F.E4M3, b, F.E4M3, dev_f32(sa),
+                                                      dev_f32(sb), full,
+                                                      bias=torch.from_numpy(bias).cuda())])
+            torch.cuda.synchronize()
+            got = full.float().cpu().numpy()
+            assert np.all(got[:, n:] == 7.0), tma
+            ok, worst = OG.check(got[:, :n], cb, eb, out_dtype, extra=extra)
+            assert ok, (tma, worst)
+    finally:
+        F.fp8_set_option(F.OPT_GEMM_TMA_STORE, 1)
+    assert F.fp8_get_last_device_error()[0] == 0
+
+
 # ------------------------------------------------------ grouped per tensor --
 
 def _linear_problems(t, d_in, d_out, seed):
