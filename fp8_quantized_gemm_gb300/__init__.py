@@ -316,7 +316,8 @@ def fp8_get_last_device_error(stream=None):
     return rc, where.value
 
 
-OPT_GEMM_CTA_PAIRS, OPT_WAIT_LIMIT_US, OPT_GEMM_MULTICAST, OPT_GEMM_TMA_STORE = 1, 2, 3, 4
+(OPT_GEMM_CTA_PAIRS, OPT_WAIT_LIMIT_US, OPT_GEMM_MULTICAST, OPT_GEMM_TMA_STORE,
+ OPT_GEMM_FEW_ROWS) = 1, 2, 3, 4, 5
 
 
 def fp8_set_option(option, value):

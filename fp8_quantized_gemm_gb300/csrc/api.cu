@@ -54,6 +54,8 @@ bool g_use_pairs = true;
 bool g_use_multicast = true;
 // TMA-store epilogue of the CTA-pair GEMM (on by default).
 bool g_use_tma_store = true;
+// CUDA-core path of the per-group GEMM for one to four rows (on by default).
+bool g_use_gemv = true;
 // Bound of every device-side mbarrier wait (fp8_set_option).
 uint64_t g_wait_limit_ns = 2000000000ull;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -580,6 +582,13 @@ int fp8_gemm_group_bias(const uint8_t *a, const void *sa, const uint8_t *b, cons
   args.out_dt = FP8_OUT_BF16; args.ldc = ldc; args.c = c; args.sa = sa; args.sb = sb;
   args.bias = bias;
   const int mode = sfmt == FP8_SCALE_F32 ? fp8k::kScaleGroupF32 : fp8k::kScaleGroupUe8m0;
+  if (g_use_gemv && fp8k::gemv_group_eligible(M, K)) {
+    // one row: a stream over the weights on the CUDA cores
+    DeviceState *d = nullptr;
+    if ((rc = device_state(&d)) != FP8_OK) return rc;
+    return to_status(
+        fp8k::launch_gemv_group(a, sa, b, sb, sfmt, M, N, K, bias, c, (cudaStream_t)stream));
+  }
   if (mode == fp8k::kScaleGroupUe8m0 && M > 256) {
     // Beyond small M: the UE8M0 scales become E8M0 words (four equal bytes per
     // 128-wide K slice) that the block-scaled GEMM bulk-copies per stage, in
@@ -791,6 +800,10 @@ int fp8_get_last_device_error(int *where_out, fp8_stream_t stream) {
 int fp8_set_option(int option, int value) {
   if (option == FP8_OPT_GEMM_CTA_PAIRS) {
     g_use_pairs = value != 0;
+    return FP8_OK;
+  }
+  if (option == FP8_OPT_GEMM_FEW_ROWS) {
+    g_use_gemv = value != 0;
     return FP8_OK;
   }
   if (option == FP8_OPT_GEMM_TMA_STORE) {

@@ -24,6 +24,12 @@ cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
                             int sms, cudaStream_t st, bool per_row = false);
 cudaError_t launch_row_amax(const void *x, int in_dt, int64_t R, int64_t K, float *out, int sms,
                             cudaStream_t st);
+// Per-K-group GEMM of one activation row on the CUDA cores (gemv.cu): bf16
+// output [1, N], optional fp32 bias; K % 128 == 0.
+bool gemv_group_eligible(int64_t M, int64_t K);
+cudaError_t launch_gemv_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
+                              int sfmt, int64_t M, int64_t N, int64_t K, const float *bias,
+                              void *c, cudaStream_t st);
 cudaError_t launch_ue8m0_words(const uint8_t *sa, const uint8_t *sb, int64_t M, int64_t N,
                                int64_t K, uint32_t *la, uint32_t *lb, int sms, cudaStream_t st);
 cudaError_t launch_ue8m0_words_experts(const uint8_t *sa, const uint8_t *sb,

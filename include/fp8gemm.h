@@ -486,12 +486,17 @@ FP8_API const char *fp8_version(void);
  *   FP8_OPT_GEMM_TMA_STORE: 1 (default) lets the CTA-pair per-tensor GEMM
  *     write C through shared memory with TMA stores (when c and ldc allow
  *     16-byte vectors and accumulate is 0); 0 keeps plain per-thread row
- *     stores.  Same bytes. */
+ *     stores.  Same bytes.
+ *   FP8_OPT_GEMM_FEW_ROWS: 1 (default) runs fp8_gemm_group / _group_bias
+ *     with a single activation row on the CUDA cores as a stream over the
+ *     weights; 0 keeps it on the tensor cores.  Results agree within the
+ *     GEMM bound. */
 typedef enum {
   FP8_OPT_GEMM_CTA_PAIRS = 1,
   FP8_OPT_WAIT_LIMIT_US = 2,
   FP8_OPT_GEMM_MULTICAST = 3,
-  FP8_OPT_GEMM_TMA_STORE = 4
+  FP8_OPT_GEMM_TMA_STORE = 4,
+  FP8_OPT_GEMM_FEW_ROWS = 5
 } fp8_option_t;
 FP8_API int fp8_set_option(int option, int value);
 

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_options(lib):
     f = lib.fp8_set_option
     f.argtypes = [ctypes.c_int, ctypes.c_int]
-    for opt in (1, 3, 4):  # CTA pairs, multicast, TMA-store epilogue: switches
+    for opt in (1, 3, 4, 5):  # CTA pairs, multicast, TMA-store epilogue, few rows
         assert f(opt, 0) == 0 and f(opt, 1) == 0
     assert f(2, -1) == -1                           # negative wait bound
     assert f(2, 2_000_000) == 0

@@ -144,6 +144,34 @@ def test_gemm_group(mnk, sfmt):
     assert ok, worst
 
 
+@pytest.mark.parametrize("m", [1, 3])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_gemm_group_few_rows(m, sfmt):
+    """A single row runs on the CUDA cores (a stream over the weights), more
+    rows and the switch off on the tensor cores.  Ragged N (an odd column
+    count leaves a warp with one column), a bias, both scale formats."""
+    F = lib()
+    n, k = 301, 7168
+    qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=m + 40)
+    bias = _bias(n, m)
+    c, e = group_reference(qa, sa, qb, sb, sfmt)
+    cb, eb, extra = OG.gemm_bias(c, e, bias)
+    sa_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sa).T)).cuda()
+    sb_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sb))).cuda()
+    code = F.SCALE_F32 if sfmt == "f32" else F.SCALE_UE8M0
+    try:
+        for few in (1, 0):
+            F.fp8_set_option(F.OPT_GEMM_FEW_ROWS, few)
+            out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+            F.fp8_gemm_group(dev_u8(qa), sa_dev, dev_u8(qb), sb_dev, code, out,
+                             bias=torch.from_numpy(bias).cuda())
+            torch.cuda.synchronize()
+            ok, worst = OG.check(out.float().cpu().numpy(), cb, eb, "bf16", extra=extra)
+            assert ok, (few, worst)
+    finally:
+        F.fp8_set_option(F.OPT_GEMM_FEW_ROWS, 1)
+
+
 @pytest.mark.parametrize("multicast", [0, 1])
 @pytest.mark.parametrize("mnk", [(300, 384, 1024), (1000, 2048, 512)])
 @pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
