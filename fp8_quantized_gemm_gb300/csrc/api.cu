@@ -362,14 +362,26 @@ int fp8_quantize_tensors(const fp8_quant_item_t *items, int count, uint32_t *syn
   int rc = device_state(&d);
   if (rc != FP8_OK) return rc;
   const cudaStream_t st = (cudaStream_t)stream;
+  // The launch pipelines the tensors in order: the amax pass of the first
+  // runs alone and so does the cast of the last.  The smallest tensor goes
+  // first (the others keep their order): its short amax pass starts the
+  // pipeline sooner.  Every tensor's outputs are its own, so the order does
+  // not change any result.
+  int order[fp8k::kMaxMulti], smallest = 0;
+  for (int i = 1; i < count; ++i)
+    if (items[i].n < items[smallest].n) smallest = i;
+  order[0] = smallest;
+  for (int i = 0, k = 1; i < count; ++i)
+    if (i != smallest) order[k++] = i;
   fp8k::MultiQuantArgs a{};
-  for (int i = 0; i < count; ++i) {
-    a.x[i] = items[i].x;
-    a.n[i] = items[i].n;
-    a.fmt[i] = items[i].fmt;
-    a.q[i] = items[i].q;
-    a.amax_out[i] = items[i].amax_out;
-    a.scale_out[i] = items[i].scale_out;
+  for (int j = 0; j < count; ++j) {
+    const fp8_quant_item_t &it = items[order[j]];
+    a.x[j] = it.x;
+    a.n[j] = it.n;
+    a.fmt[j] = it.fmt;
+    a.q[j] = it.q;
+    a.amax_out[j] = it.amax_out;
+    a.scale_out[j] = it.scale_out;
   }
   a.count = count;
   a.sync = sync;

@@ -112,8 +112,10 @@ FP8_API int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t 
  * fl32(amax / MAX) (1.0 for amax 0), q = RNE_fp8(clip(x / scale)) -- the same
  * amax, scale and bytes as fp8_amax followed by fp8_quantize_tensor with
  * amax_in.  Row-major codes only (the per-tensor GEMMs read them K- or
- * MN-major).  The items are pipelined in the order given: while tensor t is
- * divided and cast, tensor t+1 is being reduced.
+ * MN-major).  The items are pipelined: while one tensor is divided and
+ * cast, the next is being reduced; the smallest item goes first (its amax
+ * pass runs alone), the others follow in the order given.  The order changes
+ * no result.
  *   items  HOST array of `count` descriptors (read during the call only).
  *     x         device, 16-byte aligned, n >= 0 elements of in_dt (every item
  *               the same in_dt, else FP8_ERR_UNSUPPORTED)
