@@ -489,6 +489,17 @@ def cpu_baseline(wl, rows, min_seconds=10.0, max_reps=8):
             "sample": sample, "seconds": round(dt, 3)}
 
 
+def same_flush_copy_gbs(nbytes, flush, stream, reps=10):
+    """A plain device copy moving `nbytes` (half read, half written) after the
+    same L2 flush as the timed launches: what a pure stream of that much
+    traffic reaches under the flush protocol (the flush leaves L2 full of
+    dirty lines, which the next kernel's traffic has to evict)."""
+    src = torch.empty(nbytes // 2, dtype=torch.uint8, device=flush.device)
+    dst = torch.empty_like(src)
+    per, _ = time_launches([("copy", lambda: dst.copy_(src))], reps, flush, stream)
+    return nbytes / (per["copy"] / 1e3) / 1e9
+
+
 def roofline_entry(bound, achieved, peak, unit, traffic, note):
     return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": note}
@@ -522,6 +533,7 @@ def run_ours(args):
     # algorithmic work of a step over the per-step device time of each kind
     gemm_tflops = wl.flops / (sum(per["gemm"]) / reps / 1e3) / 1e12
     q_gbs = wl.bytes["quantize"] / (sum(per["quantize"]) / reps / 1e3) / 1e9
+    copy_gbs = same_flush_copy_gbs(int(wl.bytes["quantize"]), flush, stream)
     src = "MEASURED_PEAKS.json (%s)" % peaks["source"]
     line = {
         "metric": "FP8 scaled-GEMM TFLOP/s incl. quantize, % of FP8 peak; quantize GB/s % HBM",
@@ -537,9 +549,10 @@ def run_ours(args):
         "roofline": roofline_entry("tensor", gemm_tflops, fp8_peak, "TFLOP/s",
                                    recorded_traffic("gemm_pair_grouped"),
                                    "dense FP8 = 2 x measured bf16 burst (%s)" % src),
-        "quantize_roofline": roofline_entry("hbm", q_gbs, peaks["hbm_gbs"], "GB/s",
-                                            recorded_traffic("quantize_multi"),
-                                            "measured HBM copy (%s)" % src),
+        "quantize_roofline": dict(
+            roofline_entry("hbm", q_gbs, peaks["hbm_gbs"], "GB/s",
+                           recorded_traffic("quantize_multi"), "measured HBM copy (%s)" % src),
+            same_flush_copy_gbs=round(copy_gbs, 1), frac_of_same_flush_copy=round(q_gbs / copy_gbs, 4)),
         "launch": "eager (one API call per kernel)" if args.eager else
                   "CUDA graph of the step's API calls, replayed",
         "eager": {"value": round(eager_value, 2), "ms_per_step": round(eager_total_ms / args.steps, 4)},
