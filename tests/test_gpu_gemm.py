@@ -285,6 +285,21 @@ def test_gemm_mx_distinct_local_factors():
     assert ok, worst
 
 
+@pytest.mark.parametrize("mnk", [(4096, 2048, 7168), (2048, 4096, 1024)])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_gemm_group_large(mnk, sfmt):
+    """The configured M = 4096 shape and a wider one (FP32 promotion on
+    multicast 128-wide tiles; UE8M0 on E8M0 words and 128 x 256 tiles),
+    checked on sampled outputs including every edge tile's corners."""
+    m, n, k = mnk
+    qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=6)
+    got = run_group(qa, sa, qb, sb, sfmt)
+    rows, cols = sample_positions(m, n, 512, seed=m + k)
+    c, e = group_reference(qa, sa, qb, sb, sfmt, rows, cols)
+    ok, worst = OG.check(got[rows, cols], c, e, "bf16")
+    assert ok, worst
+
+
 # ------------------------------------------------------- split K (small M) --
 
 @pytest.mark.parametrize("m", [1, 7, 64, 128])
