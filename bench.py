@@ -66,9 +66,9 @@ class ClockSampler:
         self.path = None
 
     def __enter__(self):
-        out_dir = os.path.join(ROOT, "gpurun_out")
-        os.makedirs(out_dir, exist_ok=True)
-        self.path = os.path.join(out_dir, "clocks_%d.csv" % os.getpid())
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_%d_" % os.getpid(), suffix=".csv")
+        os.close(fd)
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
