@@ -350,13 +350,14 @@ int fp8_quantize_tensors(const fp8_quant_item_t *items, int count, uint32_t *syn
   if (!valid_in(in_dt)) return FP8_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) {
     const fp8_quant_item_t &it = items[i];
-    if (it.x == nullptr || it.q == nullptr || it.scale_out == nullptr || !valid_fmt(it.fmt))
-      return FP8_ERR_INVALID_ARG;
+    if (it.scale_out == nullptr || !valid_fmt(it.fmt)) return FP8_ERR_INVALID_ARG;
     if (!valid_in(it.in_dt)) return FP8_ERR_INVALID_ARG;
     if (it.in_dt != in_dt) return FP8_ERR_UNSUPPORTED;
     if (it.amax_out == it.scale_out) return FP8_ERR_INVALID_ARG;
     if (it.n < 0 || it.n >= ((int64_t)1 << 40)) return FP8_ERR_INVALID_ARG;
-    if (!aligned16(it.x) || !aligned16(it.q)) return FP8_ERR_MISALIGNED;
+    // an empty tensor is read and written nowhere: its pointers may be null
+    if (it.n > 0 && (it.x == nullptr || it.q == nullptr)) return FP8_ERR_INVALID_ARG;
+    if (it.n > 0 && (!aligned16(it.x) || !aligned16(it.q))) return FP8_ERR_MISALIGNED;
   }
   DeviceState *d = nullptr;
   int rc = device_state(&d);

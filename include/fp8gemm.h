@@ -120,6 +120,8 @@ FP8_API int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t 
  *     x         device, 16-byte aligned, n >= 0 elements of in_dt (every item
  *               the same in_dt, else FP8_ERR_UNSUPPORTED)
  *     q         device, 16-byte aligned, n bytes; must not overlap any x
+ *               (x and q may be null when n == 0: the item then reports
+ *               amax 0 and scale 1.0)
  *     amax_out  nullable device fp32;  scale_out  device fp32 (required,
  *               distinct from amax_out)
  *   sync   device scratch of FP8_QUANT_SYNC_WORDS uint32 words, 16-byte

@@ -172,6 +172,9 @@ def test_quantize_tensors_validation(lib):
     assert _qtensors(lib, amax_out=48) == -1             # amax and scale alias
     assert _qtensors(lib, x=24) == -2                    # misaligned input
     assert _qtensors(lib, fmt=3) == -1
+    assert _qtensors(lib, x=None) == -1                  # a non-empty item needs data
+    assert _qtensors(lib, q=None) == -1
+    assert _qtensors(lib, n=-1) == -1
     items = [F.QuantItem(x=16, in_dt=0, n=64, fmt=0, q=32, amax_out=None, scale_out=48),
              F.QuantItem(x=64, in_dt=1, n=64, fmt=0, q=96, amax_out=None, scale_out=52)]
     arr = (F.QuantItem * 2)(*items)
@@ -180,6 +183,8 @@ def test_quantize_tensors_validation(lib):
     assert f(ctypes.cast(arr, ctypes.c_void_p), 2, 16, None) == -3   # mixed input dtypes
     if not torch.cuda.is_available():
         assert _qtensors(lib) == -6
+        assert _qtensors(lib, x=None, q=None, n=0) == -6   # empty item: valid
+        assert _qtensors(lib, x=24, q=40, n=0) == -6       # ... read nowhere
 
 
 def test_gemm_group_experts_validation(lib):

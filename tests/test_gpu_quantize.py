@@ -415,6 +415,32 @@ def test_quantize_tensors_matches_oracle(dt):
         assert np.array_equal(codes[i], ref_q), i
 
 
+def test_quantize_tensors_empty_item():
+    """An empty tensor among the items (null pointers, n == 0): amax 0 and
+    scale 1 for it, the other items as the oracle gives them."""
+    dt = torch.bfloat16
+    xs = [workloads.normal((2, 4104), 1.0, 31).to(dt), torch.empty(0, dtype=dt),
+          workloads.normal((777,), 3.0, 32).to(dt)]
+    fmts = ["e4m3", "e5m2", "e5m2"]
+    codes, amax, scale = run_quantize_tensors(xs, fmts)
+    assert amax[1] == 0.0 and scale[1] == 1.0 and codes[1].size == 0
+    for i in (0, 2):
+        xf = xs[i].float().numpy().reshape(-1)
+        ref_q, ref_s = OQ.quantize_tensor(xf, fmts[i])
+        assert f32_bits(amax[i]) == f32_bits(OQ.amax(xf)), i
+        assert f32_bits(scale[i]) == f32_bits(ref_s), i
+        assert np.array_equal(codes[i], ref_q), i
+
+
+def test_amax_empty():
+    """n == 0: the call clears the output to 0 (the amax of nothing, as the
+    oracle's amax of an empty array) and reads no input."""
+    F = lib()
+    out = torch.full((1,), 7.0, device="cuda")
+    F.fp8_amax(torch.empty(0, device="cuda"), out)
+    assert out.item() == 0.0 == float(OQ.amax(np.zeros(0, np.float32)))
+
+
 def test_quantize_tensors_float8_linear_full_size():
     """The Float8 linear step's x, g and W (8192 x 2048, 8192 x 2048,
     2048 x 2048) in the order the step quantizes them."""
