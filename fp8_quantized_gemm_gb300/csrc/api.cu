@@ -231,6 +231,13 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
       return rc;
     return to_status(fp8k::launch_gemm_pair(tma, tmb, tmc, args, d->sms, st));
   }
+  if (mode == fp8k::kScaleGroupF32 && args.ksplit == 1 && g_use_pairs && args.experts == 0 &&
+      !args.a_mn && !args.b_mn &&
+      fp8k::gemm_pair_promote_eligible(args.M, args.N, args.K, d->sms)) {
+    if ((rc = encode_operand(&tmb, b, args.K, args.N, fp8k::gemm_pair_promote_b_rows())) != FP8_OK)
+      return rc;
+    return to_status(fp8k::launch_gemm_pair_promote(tma, tmb, args, d->sms, st));
+  }
   // multicast pairs of vertically adjacent tiles share each B box: measured
   // faster for 128-wide tiles (the FP32-promotion mode, and the block-scaled
   // modes at mid-size M), not for the 128 x 256 block-scaled tiles

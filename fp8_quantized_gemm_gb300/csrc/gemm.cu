@@ -532,7 +532,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
           if (c + 32 == BN) {  // accumulator fully read: hand it back to the MMA
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(buf));
+            // (relaxed: the reads are complete; the stores of the earlier
+            // chunks need not be)
+            if (lane == 0) mbar_arrive_relaxed(acce_bar(buf));
           }
           float v[32];
           if (ks == 1) {
@@ -604,7 +606,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(buf));
+            // the reads are complete (wait::ld): a relaxed arrival hands the
+            // buffer back without waiting for the scale prefetches in flight
+            if (lane == 0) mbar_arrive_relaxed(acce_bar(buf));
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               acc[i] = fmaf(s_cur, __uint_as_float(r0[i]), acc[i]);

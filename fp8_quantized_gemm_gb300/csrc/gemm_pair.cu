@@ -272,10 +272,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
           FP8K_TMEM_LD_X32(lane_base + buf * BN + (uint32_t)c, r);
           if (!f32) FP8K_TMEM_LD_X32(lane_base + buf * BN + (uint32_t)c + 32, (r + 32));
           tmem_ld_wait();
+          // (relaxed arrivals: the TMEM reads are complete after wait::ld,
+          // and nothing else has to be ordered before the hand-back)
           if (c + cw == BN) {  // accumulator read out: hand it back to the leader
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acce_leader0 + 8u * buf);
+            if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader0 + 8u * buf);
           }
           const int64_t col0 = tr.n0 + c;
           uint32_t packed[32];
@@ -328,7 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
         if (c + 32 == BN) {  // accumulator read out: hand it back to the leader
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acce_leader0 + 8u * buf);
+          if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader0 + 8u * buf);
         }
         float v[32];
 #pragma unroll

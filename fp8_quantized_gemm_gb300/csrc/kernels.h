@@ -150,4 +150,13 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb,
                              const CUtensorMap &tmc, const GemmArgs &args, int sms,
                              cudaStream_t st);
 
+// CTA-pair variant of the FP32-scale per-group GEMM (kScaleGroupF32):
+// 256 x 128 tiles, the per-slice promotion in both CTAs' epilogues; K-major
+// operands, K % 128 == 0, no split K, no experts.  The B tensor map box has
+// gemm_pair_promote_b_rows() rows.
+bool gemm_pair_promote_eligible(int64_t M, int64_t N, int64_t K, int sms);
+int gemm_pair_promote_b_rows();
+cudaError_t launch_gemm_pair_promote(const CUtensorMap &tma, const CUtensorMap &tmb,
+                                     const GemmArgs &args, int sms, cudaStream_t st);
+
 }  // namespace fp8k

@@ -475,8 +475,9 @@ FP8_API const char *fp8_version(void);
 /* fp8_set_option: process-wide switches (not thread-safe against concurrent
  * GEMM calls).
  *   FP8_OPT_GEMM_CTA_PAIRS: 1 (default) lets fp8_gemm_tensor run large shapes
- *     on CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles); 0 keeps every GEMM
- *     on single-CTA 128 x 256 tiles.  Results agree within the GEMM bound.
+ *     on CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles) and fp8_gemm_group
+ *     with FP32 scales run them on pairs of 256 x 128 tiles; 0 keeps every
+ *     GEMM on single-CTA tiles.  Results agree within the GEMM bound.
  *   FP8_OPT_WAIT_LIMIT_US: bound, in microseconds, of every device-side
  *     mbarrier wait of later GEMM launches (default 2,000,000).  A wait that
  *     runs out records FP8_ERR_TIMEOUT in the device error word and the

@@ -47,14 +47,14 @@ def test_timeout_reported_then_context_usable(mnk):
     assert F.fp8_get_last_device_error()[0] == 0
 
 
-def run_group_noalloc(qa, sa, qb, sb):
+def run_group_noalloc(qa, sa, qb, sb, sfmt="f32"):
     F = lib()
     m, n = qa.shape[0], qb.shape[0]
     sa_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sa).T)).cuda()   # [G, M]
     sb_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sb))).cuda()     # [N/128, G]
     out = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
     F.fp8_gemm_group_noalloc(torch.from_numpy(qa).cuda(), sa_dev, torch.from_numpy(qb).cuda(),
-                             sb_dev, 0, out)
+                             sb_dev, 0 if sfmt == "f32" else 1, out)
     torch.cuda.synchronize()
     return out.float().cpu().numpy()
 
@@ -63,17 +63,20 @@ def test_timeout_in_group_gemm_resets_split_k_counters():
     """The no-allocation entry point splits K over CTAs that meet through
     arrival counters in its fixed scratch; a timed-out call can leave counters
     behind, reading the error resets them, and the next calls (that entry
-    point and the regular one) are correct.  K is long enough for a wait to
-    outlast the barrier's suspend window."""
+    point and the regular one) are correct.  UE8M0 scales keep one
+    accumulator per tile, so the epilogue's first wait spans the CTA's whole
+    share of K (M = 128 limits the split to eight 64-block shares), long
+    enough to outlast the barrier's suspend window; the FP32 mode's waits
+    are one 128-deep slice each and may all end within it."""
     F = lib()
-    qa, sa, qb, sb = group_operands(16, 256, 65536, "f32", seed=2)
-    rc, where = forced_timeout(lambda: run_group_noalloc(qa, sa, qb, sb))
+    qa, sa, qb, sb = group_operands(128, 256, 65536, "ue8m0", seed=2)
+    rc, where = forced_timeout(lambda: run_group_noalloc(qa, sa, qb, sb, "ue8m0"))
     assert rc == F.FP8_ERR_TIMEOUT, (rc, where)
-    c, e = group_reference(qa, sa, qb, sb, "f32")
+    c, e = group_reference(qa, sa, qb, sb, "ue8m0")
     for _ in range(2):
-        ok, worst = OG.check(run_group_noalloc(qa, sa, qb, sb), c, e, "bf16")
+        ok, worst = OG.check(run_group_noalloc(qa, sa, qb, sb, "ue8m0"), c, e, "bf16")
         assert ok, worst
-    ok, worst = OG.check(run_group(qa, sa, qb, sb, "f32"), c, e, "bf16")
+    ok, worst = OG.check(run_group(qa, sa, qb, sb, "ue8m0"), c, e, "bf16")
     assert ok, worst
 
 

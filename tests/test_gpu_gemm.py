@@ -193,6 +193,35 @@ def test_gemm_group_multicast_switch(mnk, sfmt, multicast):
     assert ok, worst
 
 
+@pytest.mark.parametrize("mnk", [(1800, 2000, 512), (1024, 9728, 256)])
+def test_gemm_group_f32_cta_pairs(mnk):
+    """FP32 group scales on CTA pairs (256 x 128 tiles, the promotion in both
+    CTAs): ragged M and N (1800 = 7 * 256 + 8: the last pair's second CTA
+    lies wholly past M; 2000 = 15 * 128 + 80) and a bias, against the oracle
+    with pairs on and off; the switch off runs the one-CTA kernel."""
+    F = lib()
+    m, n, k = mnk
+    qa, sa, qb, sb = group_operands(m, n, k, "f32", seed=9)
+    bias = np.asarray(workloads.normal((n,), 0.5, 91).numpy(), np.float32)
+    c, e = group_reference(qa, sa, qb, sb, "f32")
+    cb, eb, extra = OG.gemm_bias(c, e, bias)
+    sa_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sa).T)).cuda()
+    sb_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sb))).cuda()
+    try:
+        for pairs in (1, 0):
+            F.fp8_set_option(F.OPT_GEMM_CTA_PAIRS, pairs)
+            out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+            F.fp8_gemm_group(dev_u8(qa), sa_dev, dev_u8(qb), sb_dev, 0, out,
+                             bias=torch.from_numpy(bias).cuda())
+            torch.cuda.synchronize()
+            ok, worst = OG.check(out.float().cpu().numpy(), cb, eb, "bf16", extra=extra)
+            assert ok, (pairs, worst)
+    finally:
+        F.fp8_set_option(F.OPT_GEMM_CTA_PAIRS, 1)
+    rc, where = F.fp8_get_last_device_error()
+    assert rc == 0, (rc, where)
+
+
 # -------------------------------------------------------------- two level --
 
 def mx_operands(m, n, k, seed):
