@@ -222,6 +222,26 @@ def test_gemm_group_f32_cta_pairs(mnk):
     assert rc == 0, (rc, where)
 
 
+def test_gemm_group_f32_cta_pairs_one_slice_pitched():
+    """The CTA-pair FP32 kernel with a single 128-deep K slice (fewer slices
+    than the scale prefetch distance) writing a pitched output (ldc = N + 24):
+    the padding columns stay untouched and the result agrees with the oracle."""
+    F = lib()
+    m, n, k, pad = 2048, 1280, 128, 24
+    qa, sa, qb, sb = group_operands(m, n, k, "f32", seed=12)
+    c, e = group_reference(qa, sa, qb, sb, "f32")
+    sa_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sa).T)).cuda()
+    sb_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sb))).cuda()
+    full = torch.full((m, n + pad), 7.0, dtype=torch.bfloat16, device="cuda")
+    F.fp8_gemm_group(dev_u8(qa), sa_dev, dev_u8(qb), sb_dev, 0, full)
+    torch.cuda.synchronize()
+    got = full.float().cpu().numpy()
+    assert np.all(got[:, n:] == 7.0)
+    ok, worst = OG.check(got[:, :n], c, e, "bf16")
+    assert ok, worst
+    assert F.fp8_get_last_device_error()[0] == 0
+
+
 # -------------------------------------------------------------- two level --
 
 def mx_operands(m, n, k, seed):
