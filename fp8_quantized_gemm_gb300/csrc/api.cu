@@ -609,12 +609,14 @@ int fp8_gemm_group_bias(const uint8_t *a, const void *sa, const uint8_t *b, cons
     return to_status(
         fp8k::launch_gemv_group(a, sa, b, sb, sfmt, M, N, K, bias, c, (cudaStream_t)stream));
   }
-  if (mode == fp8k::kScaleGroupUe8m0 && M > 256) {
-    // Beyond small M: the UE8M0 scales become E8M0 words (four equal bytes per
-    // 128-wide K slice) that the block-scaled GEMM bulk-copies per stage, in
-    // place of the per-stage byte loads of the group mode.  Same products,
-    // same FP32 accumulation: the tensor core applies 2^e to each 1x32
-    // sub-block of the group instead of the group as a whole.
+  if (mode == fp8k::kScaleGroupUe8m0 && M > 128) {
+    // Beyond one row tile: the UE8M0 scales become E8M0 words (four equal
+    // bytes per 128-wide K slice) that the block-scaled GEMM bulk-copies per
+    // stage, in place of the per-stage byte loads of the group mode.  Same
+    // products, same FP32 accumulation: the tensor core applies 2^e to each
+    // 1x32 sub-block of the group instead of the group as a whole.  (At
+    // K 7168, N 2048 the words measured equal at M = 64-128, slower at
+    // M = 16 (the conversion's launch) and faster from M = 256 on.)
     DeviceState *d = nullptr;
     if ((rc = device_state(&d)) != FP8_OK) return rc;
     const size_t G = (size_t)(K / 128);

@@ -179,7 +179,7 @@ def test_gemm_group_multicast_switch(mnk, sfmt, multicast):
     """The B-multicast clusters (two CTAs on vertically adjacent row tiles,
     including a last pair whose second tile lies past M) and the plain
     launch give results within the bound, for both scale formats (UE8M0
-    beyond M = 256 runs through the E8M0-word block-scaled kernel)."""
+    beyond M = 128 runs through the E8M0-word block-scaled kernel)."""
     F = lib()
     m, n, k = mnk
     qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=4)
