@@ -144,14 +144,16 @@ def test_gemm_group(mnk, sfmt):
     assert ok, worst
 
 
-@pytest.mark.parametrize("m", [1, 3])
+@pytest.mark.parametrize("m,k", [(1, 7168), (3, 7168), (1, 20480)])
 @pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
-def test_gemm_group_few_rows(m, sfmt):
+def test_gemm_group_few_rows(m, k, sfmt):
     """A single row runs on the CUDA cores (a stream over the weights), more
-    rows and the switch off on the tensor cores.  Ragged N (an odd column
-    count leaves a warp with one column), a bias, both scale formats."""
+    rows and the switch off on the tensor cores.  Ragged N (301: the last
+    block of the one-row kernel holds one valid column), a K with several
+    load steps per lane and a partial last one (20480), a bias, both scale
+    formats."""
     F = lib()
-    n, k = 301, 7168
+    n = 301
     qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=m + 40)
     bias = _bias(n, m)
     c, e = group_reference(qa, sa, qb, sb, sfmt)
