@@ -488,10 +488,10 @@ FP8_API const char *fp8_version(void);
  *     clusters of two CTAs on vertically adjacent tiles that share each
  *     weight box through TMA multicast; 0 gives every CTA its own copy.
  *     Same results.
- *   FP8_OPT_GEMM_TMA_STORE: 1 (default) lets the CTA-pair per-tensor GEMM
- *     write C through shared memory with TMA stores (when c and ldc allow
- *     16-byte vectors and accumulate is 0); 0 keeps plain per-thread row
- *     stores.  Same bytes.
+ *   FP8_OPT_GEMM_TMA_STORE: 1 lets the CTA-pair per-tensor GEMM write C
+ *     through shared memory with TMA stores (when c and ldc allow 16-byte
+ *     vectors and accumulate is 0); 0 (default) keeps plain per-thread row
+ *     stores, which measured faster.  Same bytes.
  *   FP8_OPT_GEMM_FEW_ROWS: 1 (default) runs fp8_gemm_group / _group_bias
  *     with a single activation row on the CUDA cores as a stream over the
  *     weights; 0 keeps it on the tensor cores.  Results agree within the

@@ -436,11 +436,11 @@ def test_gemm_tensor_cta_pairs(mnk, fmts):
 @pytest.mark.parametrize("pad", [24, 3])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
 def test_gemm_tensor_tma_store_epilogue(out_dtype, pad):
-    """The CTA-pair epilogue writes C with TMA stores when c and its pitch
-    allow 16-byte vectors (pad 24: a pitched output, ldc = N + 24) and with
-    per-thread stores otherwise (pad 3); both, with a bias, ragged M and N,
-    and the switch off, leave the padding columns untouched and agree with
-    the oracle."""
+    """With the switch on, the CTA-pair epilogue writes C with TMA stores
+    when c and its pitch allow 16-byte vectors (pad 24: a pitched output,
+    ldc = N + 24) and with per-thread stores otherwise (pad 3); both, with a
+    bias, ragged M and N, and the switch off (the default) leave the
+    padding columns untouched and agree with the oracle."""
     F = lib()
     m, n, k = 1999, 1000, 512
     qa, sa, qb, sb = per_tensor_operands(m, n, k, "e4m3", "e4m3", seed=31)
@@ -462,7 +462,7 @@ def test_gemm_tensor_tma_store_epilogue(out_dtype, pad):
             ok, worst = OG.check(got[:, :n], cb, eb, out_dtype, extra=extra)
             assert ok, (tma, worst)
     finally:
-        F.fp8_set_option(F.OPT_GEMM_TMA_STORE, 1)
+        F.fp8_set_option(F.OPT_GEMM_TMA_STORE, 0)  # the default
     assert F.fp8_get_last_device_error()[0] == 0
 
 
