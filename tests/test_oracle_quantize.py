@@ -63,6 +63,18 @@ def test_zero_and_signed_zero():
     assert q[0] == 0x80
 
 
+def test_empty_tensor_reading():
+    """Reading R4 extended to zero elements: the amax of nothing is 0 (the
+    identity of max over magnitudes), so the scale is 1.0 and there are no
+    codes; a planted mistake (amax of nothing taken as 1) would give a scale
+    of 1/448 and fails here."""
+    x = np.zeros((0,), F32)
+    assert Q.amax(x) == 0.0
+    q, s = Q.quantize_tensor(x, "e5m2")
+    assert s == F32(1.0) and q.size == 0
+    assert Q.scale_from_amax(F32(1.0), "e4m3") != F32(1.0)  # the planted mistake differs
+
+
 def test_pow2_scale_matches_library_cast():
     # with a power-of-two scale the division is exact, so quantization is
     # torch's cast of x * 2^-e (clipped): independent of the oracle's division
