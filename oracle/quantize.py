@@ -33,7 +33,10 @@ Readings where the pages are silent (each listed in the design notes):
 * Ragged tails (K or N not a multiple of the group) use the valid elements
   only.
 
-Pins (``tests/test_oracle_quantize.py``): the amax element maps to exactly
+Pins (``tests/test_oracle_quantize.py``, ``tests/test_oracle_division.py``):
+the quotient is a true division (inputs whose exact quotient is an FP8
+rounding midpoint, where a reciprocal multiply lands on the other code,
+decided by exact rational arithmetic); the amax element maps to exactly
 +-MAX; hand inputs; round-trip error within half a code step times the scale;
 UE8M0 bounds 2**(e-1) < s <= 2**e; the two-level invariants (S is the max of
 the s_i and equals fl32(amax/MAX); every r_i is a power of two in (0, 1];

@@ -25,10 +25,13 @@ most).  Evaluated in fp32 as fl32(fl32(amax_0 + fl32(eta * t)) / MAX).
 
 Float64 throughout (fp32 for the scale formula).  Pins
 (``tests/test_oracle_snr_training.py``): silu'(z)
-against a central finite difference, silu at 0 and large |z|, and AdamW's
+against a central finite difference, silu at 0 and large |z|; every element
+of dh and du against its own central difference of the forward; AdamW's
 first step on a constant gradient (an update of lr * g / (|g| + eps') after
 the decay); the automatic scale bounds amax(W_t) on an AdamW trajectory
-with the Adam per-step bound (1 - beta1) / sqrt(1 - beta2) times eta.
+with the Adam per-step bound (1 - beta1) / sqrt(1 - beta2) times eta, equals
+the current-scaling scale at t = 0 bit for bit, and stays within two fp32
+ulps of the exact rational (amax_0 + eta t) / MAX for t >= 1.
 """
 from __future__ import annotations
 

@@ -46,6 +46,28 @@ def test_swiglu_backward_matches_finite_difference():
     assert math.isclose(np.sum(du), fd_u, rel_tol=1e-6, abs_tol=1e-8)
 
 
+def test_swiglu_backward_elementwise_central_difference():
+    """Each element of dh and du against its own central difference of the
+    forward (a swapped pair, a permuted index or a missing factor of da or u
+    fails here even where a sum would cancel)."""
+    rng = np.random.default_rng(7)
+    n = 400
+    h = rng.standard_normal(n) * 3.0
+    u = rng.standard_normal(n)
+    da = rng.standard_normal(n)
+    dh, du = T.swiglu_backward(da, h, u)
+    eps = 1e-5
+    fd_h = da * (T.swiglu_forward(h + eps, u) - T.swiglu_forward(h - eps, u)) / (2 * eps)
+    fd_u = da * (T.swiglu_forward(h, u + eps) - T.swiglu_forward(h, u - eps)) / (2 * eps)
+    assert np.allclose(dh, fd_h, rtol=1e-7, atol=1e-9)
+    assert np.allclose(du, fd_u, rtol=1e-7, atol=1e-9)
+    # a is linear in u, so du is exact: da * silu(h)
+    assert np.array_equal(du, da * T.silu(h))
+    # one element: z = 0 gives silu'(0) = 1/2, so dh = da * u / 2
+    dh0, du0 = T.swiglu_backward(np.array([2.0]), np.array([0.0]), np.array([3.0]))
+    assert dh0[0] == 3.0 and du0[0] == 0.0
+
+
 def test_adamw_first_step_closed_form():
     # on the first step m_hat = g and v_hat = g^2, so the step is lr * g / (|g| + eps)
     p0, g = np.array([1.0, -2.0, 0.5]), np.array([0.3, -1e-3, 0.0])
@@ -91,3 +113,29 @@ def test_auto_scale_bounds_adamw_trajectory():
     s1 = T.auto_weight_scale(0.5, 1e-4, 100, 448.0)
     s2 = T.auto_weight_scale(0.5, 1e-4, 200, 448.0)
     assert abs((float(s2) - float(s1)) - 1e-4 * 100 / 448.0) < 1e-9
+
+
+def test_auto_scale_start_and_step_count():
+    """MOSS blog, section 5, eq. (10) at its start and first steps: t = 0 is
+    the current-scaling scale of the weight, bit for bit (the per-tensor
+    ``scale_from_amax``, pinned on its own); every later t lies within two
+    fp32 ulps of the exact rational (amax_0 + eta * t) / MAX, which moves by
+    eta / MAX per step -- far more than two ulps at these magnitudes, so an
+    off-by-one in t fails."""
+    from fractions import Fraction
+
+    from oracle import quantize as OQ
+    rng = np.random.default_rng(11)
+    w = (rng.standard_normal(4096) * 0.02).astype(np.float32)
+    amax0 = OQ.amax(w)
+    lr = 1e-4
+    assert T.auto_weight_scale(amax0, lr, 0, 448.0) == OQ.scale_from_amax(amax0, "e4m3")
+    for fmt_max, fmt in ((448.0, "e4m3"), (57344.0, "e5m2")):
+        assert T.auto_weight_scale(amax0, lr, 0, fmt_max) == OQ.scale_from_amax(amax0, fmt)
+    ulp = np.spacing(np.float32(amax0 / 448.0))
+    for t in range(1, 6):
+        exact = (Fraction(float(amax0)) + Fraction(lr) * t) / 448
+        got = T.auto_weight_scale(amax0, lr, t, 448.0)
+        assert abs(Fraction(float(got)) - exact) <= 2 * Fraction(float(ulp))
+        # neighbouring step counts are distinguishable at this resolution
+        assert abs(Fraction(float(got)) - (exact - Fraction(lr) / 448)) > 4 * Fraction(float(ulp))
