@@ -60,6 +60,10 @@ _SIGS = {
     "fp8_swiglu_forward": [_vp, _vp, _vp, _i64, _vp],
     "fp8_swiglu_backward": [_vp, _vp, _vp, _vp, _vp, _i64, _vp],
     "fp8_adamw_step": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _d, _d, _d, _d, _d, _vp],
+    "fp8_swiglu_forward_quantize": [_vp, _vp, _i64, _int, _vp, _vp, _vp, _vp],
+    "fp8_swiglu_backward_quantize": [_vp, _vp, _vp, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     _vp],
+    "fp8_adamw_multi": [_vp, _int, _vp, _d, _d, _d, _d, _d, _vp],
     "fp8_get_last_device_error": [ctypes.POINTER(ctypes.c_int), _vp],
     "fp8_set_option": [_int, _int],
 }
@@ -307,6 +311,42 @@ def fp8_adamw_step(p, g, m, v, p_bf16, step, lr=1e-4, beta1=0.9, beta2=0.999, ep
                    weight_decay=0.01, stream=None):
     _call("fp8_adamw_step", _p(p), _p(g), _p(m), _p(v), _p(p_bf16), p.numel(), int(step), lr,
           beta1, beta2, eps, weight_decay, _stream(stream))
+
+
+def fp8_swiglu_forward_quantize(h, u, fmt, scale, q, amax_out=None, stream=None):
+    """a = bf16(silu(h) * u) quantized with the given (delayed) scale into q;
+    amax_out receives max |a|.  The bf16 a is not written."""
+    assert q.numel() == h.numel() == u.numel()
+    _call("fp8_swiglu_forward_quantize", _p(h), _p(u), h.numel(), fmt, _p(scale), _p(q),
+          _p(amax_out), _stream(stream))
+
+
+def fp8_swiglu_backward_quantize(da, h, u, fmt, scale_dh, scale_du, q_dh, q_du, amax_dh=None,
+                                 amax_du=None, stream=None):
+    """dh, du of a = silu(h) * u, each quantized with its own scale."""
+    assert q_dh.numel() == q_du.numel() == h.numel() == u.numel() == da.numel()
+    _call("fp8_swiglu_backward_quantize", _p(da), _p(h), _p(u), h.numel(), fmt, _p(scale_dh),
+          _p(scale_du), _p(q_dh), _p(q_du), _p(amax_dh), _p(amax_du), _stream(stream))
+
+
+class AdamwItem(ctypes.Structure):
+    """fp8_adamw_item_t (include/fp8gemm.h)."""
+    _fields_ = [("p", _vp), ("g", _vp), ("m", _vp), ("v", _vp), ("p_bf16", _vp), ("n", _i64)]
+
+
+def adamw_item(p, g, m, v, p_bf16=None):
+    assert p.numel() == g.numel() == m.numel() == v.numel()
+    return AdamwItem(_p(p), _p(g), _p(m), _p(v), _p(p_bf16), p.numel())
+
+
+def fp8_adamw_multi(items, step, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
+                    stream=None):
+    """One AdamW step over several tensors; `step` is a device int64 tensor of
+    one element, incremented by the call (the update uses the new value)."""
+    assert step.dtype == torch.int64 and step.numel() == 1
+    arr = (AdamwItem * len(items))(*items)
+    _call("fp8_adamw_multi", ctypes.cast(arr, _vp), len(items), _p(step), lr, beta1, beta2, eps,
+          weight_decay, _stream(stream))
 
 
 def fp8_get_last_device_error(stream=None):

@@ -33,19 +33,17 @@ constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 
-// Split-K scratch of the small-M GEMM path, one per (device, stream) so that
-// calls on different streams never share it.  Layout: uint32 arrival
-// counters (one per output tile, zero between calls) in the first
-// kCounterBytes, then the fp32 partials [ksplit][M][N].  Allocated (zeroed) on
-// first need and grown by doubling; never inside a stream capture.
-constexpr size_t kCounterBytes = 64 * 1024;
+// Device workspace of the UE8M0 per-group GEMM beyond one row tile: the
+// E8M0 words the byte scales are expanded into (see fp8_gemm_group_bias),
+// one buffer per (device, stream, slot) so that calls on different streams
+// never share it.  Allocated on first need and grown by doubling; never
+// inside a stream capture.  (Split K needs no workspace: the splits of a
+// tile reduce inside a thread-block cluster.)
 struct Workspace {
   void *ptr = nullptr;
   size_t bytes = 0;
 };
-// Slots: kWsSplit (the split-K scratch above), kWsWords (E8M0 words of UE8M0
-// group scales, see fp8_gemm_group_bias).
-constexpr int kWsSplit = 0, kWsWords = 1;
+constexpr int kWsWords = 1;
 std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_ws;
 
 // CTA-pair GEMM path switch (on by default; fp8_set_option turns it off).
@@ -177,7 +175,7 @@ bool use_tma_store(const void *c, int64_t ldc, int out_dt, int accumulate) {
   return g_use_tma_store && accumulate == 0 && vector_store_ok(c, ldc, out_dt);
 }
 
-int get_workspace(cudaStream_t st, size_t need, void **out, int slot = kWsSplit) {
+int get_workspace(cudaStream_t st, size_t need, void **out, int slot) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FP8_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -213,13 +211,6 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
   args.counters = nullptr;
   // split K reduces inside a thread-block cluster (no workspace)
   args.cluster_split = args.ksplit > 1 ? 1 : 0;
-  if (args.ksplit > 1 && !args.cluster_split) {
-    const size_t need = kCounterBytes + (size_t)args.ksplit * args.M * args.N * sizeof(float);
-    void *w = nullptr;
-    if ((rc = get_workspace(st, need, &w)) != FP8_OK) return rc;
-    args.counters = static_cast<uint32_t *>(w);
-    args.ws = reinterpret_cast<float *>(static_cast<char *>(w) + kCounterBytes);
-  }
   args.vec_store = vector_store_ok(args.c, args.ldc, args.out_dt);
   CUtensorMap tma, tmb;
   if ((rc = encode_gemm_operand(&tma, a, args.a_mn, args.K, args.M, 128)) != FP8_OK) return rc;
@@ -746,7 +737,8 @@ int fp8_auto_weight_scale(const float *amax0, int64_t t, double lr, int fmt, flo
 }
 
 int fp8_swiglu_forward(const void *h, const void *u, void *a, int64_t n, fp8_stream_t stream) {
-  if (h == nullptr || u == nullptr || a == nullptr || n < 0) return FP8_ERR_INVALID_ARG;
+  if (n < 0 || (n > 0 && (h == nullptr || u == nullptr || a == nullptr)))
+    return FP8_ERR_INVALID_ARG;
   if (n % 8 != 0 || !aligned16(h) || !aligned16(u) || !aligned16(a)) return FP8_ERR_MISALIGNED;
   DeviceState *d = nullptr;
   int rc = device_state(&d);
@@ -757,7 +749,8 @@ int fp8_swiglu_forward(const void *h, const void *u, void *a, int64_t n, fp8_str
 
 int fp8_swiglu_backward(const void *da, const void *h, const void *u, void *dh, void *du,
                         int64_t n, fp8_stream_t stream) {
-  if (da == nullptr || h == nullptr || u == nullptr || dh == nullptr || du == nullptr || n < 0)
+  if (n < 0 || (n > 0 && (da == nullptr || h == nullptr || u == nullptr || dh == nullptr ||
+                          du == nullptr)))
     return FP8_ERR_INVALID_ARG;
   if (n % 8 != 0 || !aligned16(da) || !aligned16(h) || !aligned16(u) || !aligned16(dh) ||
       !aligned16(du))
@@ -767,6 +760,78 @@ int fp8_swiglu_backward(const void *da, const void *h, const void *u, void *dh, 
   if (rc != FP8_OK) return rc;
   if (n == 0) return FP8_OK;
   return to_status(fp8k::launch_swiglu_bwd(da, h, u, dh, du, n, d->sms, (cudaStream_t)stream));
+}
+
+int fp8_swiglu_forward_quantize(const void *h, const void *u, int64_t n, int fmt,
+                                const float *scale, uint8_t *q, float *amax_out,
+                                fp8_stream_t stream) {
+  if (n < 0 || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
+  // an empty tensor is read and written nowhere: its pointers may be null
+  if (n > 0 && (h == nullptr || u == nullptr || scale == nullptr || q == nullptr))
+    return FP8_ERR_INVALID_ARG;
+  if (amax_out != nullptr && amax_out == scale) return FP8_ERR_INVALID_ARG;
+  if (n % 8 != 0 || !aligned16(h) || !aligned16(u) || !aligned16(q)) return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_swiglu_fwd_quant(h, u, n, fmt, scale, q, amax_out, d->sms,
+                                                 (cudaStream_t)stream));
+}
+
+int fp8_swiglu_backward_quantize(const void *da, const void *h, const void *u, int64_t n, int fmt,
+                                 const float *scale_dh, const float *scale_du, uint8_t *q_dh,
+                                 uint8_t *q_du, float *amax_dh, float *amax_du,
+                                 fp8_stream_t stream) {
+  if (n < 0 || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
+  if (n > 0 && (da == nullptr || h == nullptr || u == nullptr || scale_dh == nullptr ||
+                scale_du == nullptr || q_dh == nullptr || q_du == nullptr))
+    return FP8_ERR_INVALID_ARG;
+  if ((amax_dh == nullptr) != (amax_du == nullptr)) return FP8_ERR_INVALID_ARG;
+  if (amax_dh != nullptr &&
+      (amax_dh == amax_du || amax_dh == scale_dh || amax_dh == scale_du ||
+       amax_du == scale_dh || amax_du == scale_du))
+    return FP8_ERR_INVALID_ARG;
+  if (n % 8 != 0 || !aligned16(da) || !aligned16(h) || !aligned16(u) || !aligned16(q_dh) ||
+      !aligned16(q_du))
+    return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_swiglu_bwd_quant(da, h, u, n, fmt, scale_dh, scale_du, q_dh, q_du,
+                                                 amax_dh, amax_du, d->sms, (cudaStream_t)stream));
+}
+
+int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, double lr,
+                    double beta1, double beta2, double eps, double weight_decay,
+                    fp8_stream_t stream) {
+  if (items == nullptr || step == nullptr || count < 1 || count > fp8k::kMaxAdamw)
+    return FP8_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(step) & 7u) != 0) return FP8_ERR_MISALIGNED;
+  fp8k::AdamwMulti a{};
+  for (int k = 0; k < count; ++k) {
+    const fp8_adamw_item_t &it = items[k];
+    if (it.n < 0 || (it.n > 0 && (it.p == nullptr || it.g == nullptr || it.m == nullptr ||
+                                  it.v == nullptr)))
+      return FP8_ERR_INVALID_ARG;
+    if (it.n % 4 != 0) return FP8_ERR_MISALIGNED;
+    if (it.n > 0 && (!aligned16(it.p) || !aligned16(it.g) || !aligned16(it.m) ||
+                     !aligned16(it.v) ||
+                     (it.p_bf16 != nullptr && (reinterpret_cast<uintptr_t>(it.p_bf16) & 7u) != 0)))
+      return FP8_ERR_MISALIGNED;
+    a.p[k] = it.p;
+    a.g[k] = it.g;
+    a.m[k] = it.m;
+    a.v[k] = it.v;
+    a.pb[k] = it.p_bf16;
+    a.n[k] = it.n;
+  }
+  a.count = count;
+  a.step = step;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_adamw_multi(a, lr, beta1, beta2, eps, weight_decay, d->sms,
+                                            (cudaStream_t)stream));
 }
 
 int fp8_adamw_step(float *p, const float *g, float *m, float *v, void *p_bf16, int64_t n,
@@ -809,14 +874,6 @@ int fp8_get_last_device_error(int *where_out, fp8_stream_t stream) {
   if (h[0] != 0) {
     const uint32_t z[2] = {0, 0};
     if (cudaMemcpy(d->err, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FP8_ERR_CUDA;
-    // an aborted kernel may have left split-K arrival counters non-zero
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FP8_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_mu);
-    for (auto &kv : g_ws)
-      if (std::get<0>(kv.first) == dev && std::get<2>(kv.first) == kWsSplit &&
-          kv.second.ptr != nullptr && cudaMemset(kv.second.ptr, 0, kCounterBytes) != cudaSuccess)
-        return FP8_ERR_CUDA;
   }
   if (where_out != nullptr) *where_out = (int)h[1];
   return -(int)h[0];

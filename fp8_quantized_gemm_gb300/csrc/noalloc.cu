@@ -1,16 +1,17 @@
 // fp8_gemm_group_noalloc: the per-K-group GEMM for callers that cannot
 // allocate device memory.
 //
-// The regular fp8_gemm_group splits K across CTAs for small M and keeps the
-// fp32 partial sums and per-tile arrival counters in a workspace it
-// cudaMalloc's on first use for each (device, stream).  Some callers cannot
-// allow that: code running while a stream is being captured into a CUDA
-// graph (allocation is not permitted during capture, and a fresh stream has
-// no workspace yet), and runtimes that reserve all device memory up front in
-// their own pool or must never stall on the allocator (cudaFree synchronizes
-// the device).  This entry point instead uses a fixed scratch array compiled
-// into the library: 64 KiB of counters plus 8 MiB of partials, held on every
-// GPU that loads the library until the process exits.  It allocates nothing.
+// The regular fp8_gemm_group allocates device memory on first use for some
+// shapes (the E8M0-word buffer of UE8M0 scales beyond one row tile).  Some
+// callers cannot allow that: runtimes that reserve all device memory up
+// front in their own pool, and code that must never stall on the allocator
+// (cudaMalloc and cudaFree may synchronize the device).  This entry point
+// always runs the tensor-core per-group kernel; where that kernel splits K
+// for small M it keeps the fp32 partial sums and per-tile arrival counters in
+// a fixed scratch array compiled into the library -- 64 KiB of counters plus
+// 8 MiB of partials, held on every GPU that loads the library until the
+// process exits -- and reduces them in global memory (the workspace form of
+// the split).  It allocates nothing.
 #include <mutex>
 
 #include "fp8gemm.h"

@@ -1,8 +1,16 @@
 // Elementwise support kernels of the FP8 SwiGLU training step (HBM-bound):
-// SwiGLU forward / backward and the AdamW update.  16-byte vector loads,
+// SwiGLU forward / backward, the same fused with the delayed-scaling
+// quantization of their outputs, and the AdamW update.  16-byte vector loads,
 // grid-stride loops sized to the SM count, fp32 arithmetic.
+//
+// The SwiGLU values are formed by one function per direction with every
+// operation an explicitly rounded intrinsic (no contraction left to the
+// compiler), so the plain kernels and the fused ones produce the same bf16
+// value for the same inputs: the fused kernels quantize exactly the bf16
+// tensor the plain kernel would have written.
 #include "common.cuh"
 #include "kernels.h"
+#include "quant_common.cuh"
 #include "support.h"
 
 namespace fp8k {
@@ -26,7 +34,29 @@ __device__ __forceinline__ uint4 f32x8_to_bf16(const float (&v)[8]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+// The eight bf16 values of a packed vector, widened back to fp32 (exact).
+__device__ __forceinline__ void bf16_roundtrip(const float (&v)[8], float (&o)[8]) {
+  bf16x8_to_f32(f32x8_to_bf16(v), o);
+}
+
+// logistic function 1 / (1 + e^-z), IEEE division
+__device__ __forceinline__ float sigmoidf_(float z) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
+}
+
+// a = silu(h) * u = (h * s(h)) * u
+__device__ __forceinline__ float swiglu_value(float h, float u) {
+  return __fmul_rn(__fmul_rn(h, sigmoidf_(h)), u);
+}
+
+// dh = (da * u) * s(h) (1 + h (1 - s(h)));  du = da * (h * s(h))
+__device__ __forceinline__ void swiglu_grad_values(float da, float h, float u, float &dh,
+                                                   float &du) {
+  const float s = sigmoidf_(h);
+  const float dsilu = __fmul_rn(s, __fmaf_rn(h, __fsub_rn(1.0f, s), 1.0f));
+  dh = __fmul_rn(__fmul_rn(da, u), dsilu);
+  du = __fmul_rn(da, __fmul_rn(h, s));
+}
 
 __global__ void __launch_bounds__(512)
     swiglu_fwd_kernel(const uint4 *__restrict__ h, const uint4 *__restrict__ u,
@@ -37,7 +67,7 @@ __global__ void __launch_bounds__(512)
     bf16x8_to_f32(__ldcs(h + i), hv);
     bf16x8_to_f32(__ldcs(u + i), uv);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) av[j] = hv[j] * sigmoidf_(hv[j]) * uv[j];
+    for (int j = 0; j < 8; ++j) av[j] = swiglu_value(hv[j], uv[j]);
     __stcs(a + i, f32x8_to_bf16(av));
   }
 }
@@ -53,15 +83,148 @@ __global__ void __launch_bounds__(512)
     bf16x8_to_f32(__ldcs(h + i), hv);
     bf16x8_to_f32(__ldcs(u + i), uv);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float s = sigmoidf_(hv[j]);
-      const float silu = hv[j] * s;
-      dhv[j] = dav[j] * uv[j] * (s * (1.0f + hv[j] * (1.0f - s)));
-      duv[j] = dav[j] * silu;
-    }
+    for (int j = 0; j < 8; ++j) swiglu_grad_values(dav[j], hv[j], uv[j], dhv[j], duv[j]);
     __stcs(dh + i, f32x8_to_bf16(dhv));
     __stcs(du + i, f32x8_to_bf16(duv));
   }
+}
+
+// ---------------------------------------- SwiGLU fused with quantization --
+// Delayed scaling knows the scale before the pass (the one the previous
+// step's history left), so the SwiGLU output is quantized as it is formed:
+// the bf16 value is rounded as the plain kernel would store it, divided by
+// the scale (the same correctly rounded quotient as fp8_quantize_tensor),
+// cast with the saturating RNE conversion, and its |value| enters the fused
+// amax.  The bf16 tensor itself is never written.  kFast: the scale is in
+// the reciprocal-quotient range (checked once per launch).
+template <int F, bool kAmax, bool kFast>
+__device__ __forceinline__ void swiglu_fwd_quant_body(const uint4 *__restrict__ h,
+                                                      const uint4 *__restrict__ u, int64_t nvec,
+                                                      const ScaleDiv &d, uint2 *__restrict__ q,
+                                                      uint32_t &key) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // two vectors of each input in flight per thread
+  for (; i + stride < nvec; i += 2 * stride) {
+    const uint4 hw0 = __ldcs(h + i), uw0 = __ldcs(u + i);
+    const uint4 hw1 = __ldcs(h + i + stride), uw1 = __ldcs(u + i + stride);
+    const uint4 hw[2] = {hw0, hw1}, uw[2] = {uw0, uw1};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float hv[8], uv[8], av[8], ab[8], y[8];
+      bf16x8_to_f32(hw[r], hv);
+      bf16x8_to_f32(uw[r], uv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) av[j] = swiglu_value(hv[j], uv[j]);
+      bf16_roundtrip(av, ab);
+      if (kAmax) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) key = max(key, abs_key(ab[j]));
+      }
+      d.div8<kFast>(ab, y);
+      __stcs(q + i + r * stride, pack8<F>(y));
+    }
+  }
+  for (; i < nvec; i += stride) {
+    float hv[8], uv[8], av[8], ab[8], y[8];
+    bf16x8_to_f32(__ldcs(h + i), hv);
+    bf16x8_to_f32(__ldcs(u + i), uv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) av[j] = swiglu_value(hv[j], uv[j]);
+    bf16_roundtrip(av, ab);
+    if (kAmax) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) key = max(key, abs_key(ab[j]));
+    }
+    d.div8<kFast>(ab, y);
+    __stcs(q + i, pack8<F>(y));
+  }
+}
+
+template <int F, bool kAmax>
+__global__ void __launch_bounds__(256)
+    swiglu_fwd_quant_kernel(const uint4 *__restrict__ h, const uint4 *__restrict__ u,
+                            int64_t nvec, const float *scale, uint2 *__restrict__ q,
+                            uint32_t *amax_out) {
+  const ScaleDiv d(*scale);
+  uint32_t key = 0;
+  if (d.fast)
+    swiglu_fwd_quant_body<F, kAmax, true>(h, u, nvec, d, q, key);
+  else
+    swiglu_fwd_quant_body<F, kAmax, false>(h, u, nvec, d, q, key);
+  if (kAmax) block_max_to(key, amax_out);
+}
+
+// dh and du quantized with their own scales; one amax each.  Both scales'
+// fast checks are folded into one launch-uniform branch.
+template <int F, bool kAmax, bool kFast>
+__device__ __forceinline__ void swiglu_bwd_quant_body(
+    const uint4 *__restrict__ da, const uint4 *__restrict__ h, const uint4 *__restrict__ u,
+    int64_t nvec, const ScaleDiv &dsh, const ScaleDiv &dsu, uint2 *__restrict__ qh,
+    uint2 *__restrict__ qu, uint32_t &key_h, uint32_t &key_u) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    float dav[8], hv[8], uv[8], dhv[8], duv[8], dhb[8], dub[8], y[8];
+    bf16x8_to_f32(__ldcs(da + i), dav);
+    bf16x8_to_f32(__ldcs(h + i), hv);
+    bf16x8_to_f32(__ldcs(u + i), uv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) swiglu_grad_values(dav[j], hv[j], uv[j], dhv[j], duv[j]);
+    bf16_roundtrip(dhv, dhb);
+    bf16_roundtrip(duv, dub);
+    if (kAmax) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        key_h = max(key_h, abs_key(dhb[j]));
+        key_u = max(key_u, abs_key(dub[j]));
+      }
+    }
+    dsh.div8<kFast>(dhb, y);
+    __stcs(qh + i, pack8<F>(y));
+    dsu.div8<kFast>(dub, y);
+    __stcs(qu + i, pack8<F>(y));
+  }
+}
+
+template <int F, bool kAmax>
+__global__ void __launch_bounds__(256)
+    swiglu_bwd_quant_kernel(const uint4 *__restrict__ da, const uint4 *__restrict__ h,
+                            const uint4 *__restrict__ u, int64_t nvec, const float *scale_h,
+                            const float *scale_u, uint2 *__restrict__ qh, uint2 *__restrict__ qu,
+                            uint32_t *amax_h, uint32_t *amax_u) {
+  const ScaleDiv dsh(*scale_h), dsu(*scale_u);
+  uint32_t key_h = 0, key_u = 0;
+  if (dsh.fast && dsu.fast)
+    swiglu_bwd_quant_body<F, kAmax, true>(da, h, u, nvec, dsh, dsu, qh, qu, key_h, key_u);
+  else
+    swiglu_bwd_quant_body<F, kAmax, false>(da, h, u, nvec, dsh, dsu, qh, qu, key_h, key_u);
+  if (kAmax) {
+    block_max_to(key_h, amax_h);
+    __syncthreads();  // block_max_to's shared scratch is reused
+    block_max_to(key_u, amax_u);
+  }
+}
+
+// ------------------------------------------------------------------ AdamW --
+__device__ __forceinline__ void adamw4(float4 &pv, float4 &mv, float4 &vv, const float4 gv,
+                                       float lr, float b1, float b2, float omb1, float omb2,
+                                       float eps, float decay, float bc1, float bc2) {
+  float *pp = &pv.x, *mm = &mv.x, *vvp = &vv.x;
+  const float *gg = &gv.x;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    pp[j] = pp[j] * decay;
+    mm[j] = b1 * mm[j] + omb1 * gg[j];
+    vvp[j] = b2 * vvp[j] + omb2 * gg[j] * gg[j];
+    const float mhat = mm[j] / bc1;
+    const float vhat = vvp[j] / bc2;
+    pp[j] = pp[j] - lr * mhat / (sqrtf(vhat) + eps);
+  }
+}
+
+__device__ __forceinline__ uint2 f32x4_to_bf16(const float4 pv) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(pv.x, pv.y), hi = __floats2bfloat162_rn(pv.z, pv.w);
+  return make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
 }
 
 __global__ void __launch_bounds__(512)
@@ -73,37 +236,59 @@ __global__ void __launch_bounds__(512)
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
     float4 pv = p[i], mv = m[i], vv = v[i];
     const float4 gv = __ldcs(g + i);
-    float *pp = &pv.x, *mm = &mv.x, *vvp = &vv.x;
-    const float *gg = &gv.x;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      pp[j] = pp[j] * decay;
-      mm[j] = b1 * mm[j] + omb1 * gg[j];
-      vvp[j] = b2 * vvp[j] + omb2 * gg[j] * gg[j];
-      const float mhat = mm[j] / bc1;
-      const float vhat = vvp[j] / bc2;
-      pp[j] = pp[j] - lr * mhat / (sqrtf(vhat) + eps);
-    }
+    adamw4(pv, mv, vv, gv, lr, b1, b2, omb1, omb2, eps, decay, bc1, bc2);
     p[i] = pv;
     m[i] = mv;
     v[i] = vv;
-    if (pb != nullptr) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(pv.x, pv.y), hi = __floats2bfloat162_rn(pv.z, pv.w);
-      pb[i] = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+    if (pb != nullptr) pb[i] = f32x4_to_bf16(pv);
+  }
+}
+
+// The step counter of the multi-tensor update lives on the device, so a
+// captured training step advances it on every replay.
+__global__ void adamw_advance_step_kernel(int64_t *step) { *step += 1; }
+
+// One launch over every parameter tensor; the bias corrections 1 - beta^t
+// are formed in double from the device step counter, once per block.
+__global__ void __launch_bounds__(512) adamw_multi_kernel(const __grid_constant__ AdamwMulti a) {
+  __shared__ float bc[2];
+  if (threadIdx.x == 0) {
+    const double t = (double)*a.step;
+    bc[0] = (float)(1.0 - pow(a.b1d, t));
+    bc[1] = (float)(1.0 - pow(a.b2d, t));
+  }
+  __syncthreads();
+  const float bc1 = bc[0], bc2 = bc[1];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int k = 0; k < a.count; ++k) {
+    float4 *__restrict__ p = reinterpret_cast<float4 *>(a.p[k]);
+    const float4 *__restrict__ g = reinterpret_cast<const float4 *>(a.g[k]);
+    float4 *__restrict__ m = reinterpret_cast<float4 *>(a.m[k]);
+    float4 *__restrict__ v = reinterpret_cast<float4 *>(a.v[k]);
+    uint2 *__restrict__ pb = reinterpret_cast<uint2 *>(a.pb[k]);
+    const int64_t nvec = a.n[k] / 4;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+      float4 pv = p[i], mv = m[i], vv = v[i];
+      const float4 gv = __ldcs(g + i);
+      adamw4(pv, mv, vv, gv, a.lr, a.b1, a.b2, a.omb1, a.omb2, a.eps, a.decay, bc1, bc2);
+      p[i] = pv;
+      m[i] = mv;
+      v[i] = vv;
+      if (pb != nullptr) pb[i] = f32x4_to_bf16(pv);
     }
   }
 }
 
-static int blocks_for(int64_t nvec, int threads, int sms) {
+static int blocks_for(int64_t nvec, int threads, int per_sm, int sms) {
   const int64_t need = (nvec + threads - 1) / threads;
-  const int64_t cap = (int64_t)sms * 4;
+  const int64_t cap = (int64_t)sms * per_sm;
   return (int)(need < 1 ? 1 : (need < cap ? need : cap));
 }
 
 cudaError_t launch_swiglu_fwd(const void *h, const void *u, void *a, int64_t n, int sms,
                               cudaStream_t st) {
   const int64_t nvec = n / 8;
-  swiglu_fwd_kernel<<<blocks_for(nvec, 512, sms), 512, 0, st>>>(
+  swiglu_fwd_kernel<<<blocks_for(nvec, 512, 4, sms), 512, 0, st>>>(
       static_cast<const uint4 *>(h), static_cast<const uint4 *>(u), static_cast<uint4 *>(a), nvec);
   return cudaGetLastError();
 }
@@ -111,9 +296,62 @@ cudaError_t launch_swiglu_fwd(const void *h, const void *u, void *a, int64_t n, 
 cudaError_t launch_swiglu_bwd(const void *da, const void *h, const void *u, void *dh, void *du,
                               int64_t n, int sms, cudaStream_t st) {
   const int64_t nvec = n / 8;
-  swiglu_bwd_kernel<<<blocks_for(nvec, 512, sms), 512, 0, st>>>(
+  swiglu_bwd_kernel<<<blocks_for(nvec, 512, 4, sms), 512, 0, st>>>(
       static_cast<const uint4 *>(da), static_cast<const uint4 *>(h), static_cast<const uint4 *>(u),
       static_cast<uint4 *>(dh), static_cast<uint4 *>(du), nvec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_fwd_quant(const void *h, const void *u, int64_t n, int fmt,
+                                    const float *scale, uint8_t *q, float *amax_out, int sms,
+                                    cudaStream_t st) {
+  const bool fused = amax_out != nullptr;
+  if (fused) {
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  if (n == 0) return cudaSuccess;
+  const int64_t nvec = n / 8;
+  const int blocks = blocks_for(nvec, 256, 8, sms);
+  const uint4 *hp = static_cast<const uint4 *>(h), *up = static_cast<const uint4 *>(u);
+  uint2 *qp = reinterpret_cast<uint2 *>(q);
+  uint32_t *ao = reinterpret_cast<uint32_t *>(amax_out);
+#define FP8K_SFQ(F, A) swiglu_fwd_quant_kernel<F, A><<<blocks, 256, 0, st>>>(hp, up, nvec, scale, qp, ao)
+  if (fmt == 0) {
+    if (fused) FP8K_SFQ(0, true); else FP8K_SFQ(0, false);
+  } else {
+    if (fused) FP8K_SFQ(1, true); else FP8K_SFQ(1, false);
+  }
+#undef FP8K_SFQ
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_bwd_quant(const void *da, const void *h, const void *u, int64_t n,
+                                    int fmt, const float *scale_h, const float *scale_u,
+                                    uint8_t *qh, uint8_t *qu, float *amax_h, float *amax_u,
+                                    int sms, cudaStream_t st) {
+  const bool fused = amax_h != nullptr;  // both or neither (checked by the API)
+  if (fused) {
+    cudaError_t e = cudaMemsetAsync(amax_h, 0, sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(amax_u, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  if (n == 0) return cudaSuccess;
+  const int64_t nvec = n / 8;
+  const int blocks = blocks_for(nvec, 256, 8, sms);
+  const uint4 *dap = static_cast<const uint4 *>(da), *hp = static_cast<const uint4 *>(h),
+              *up = static_cast<const uint4 *>(u);
+  uint2 *qhp = reinterpret_cast<uint2 *>(qh), *qup = reinterpret_cast<uint2 *>(qu);
+  uint32_t *ah = reinterpret_cast<uint32_t *>(amax_h), *au = reinterpret_cast<uint32_t *>(amax_u);
+#define FP8K_SBQ(F, A)                                                                      \
+  swiglu_bwd_quant_kernel<F, A><<<blocks, 256, 0, st>>>(dap, hp, up, nvec, scale_h, scale_u, \
+                                                        qhp, qup, ah, au)
+  if (fmt == 0) {
+    if (fused) FP8K_SBQ(0, true); else FP8K_SBQ(0, false);
+  } else {
+    if (fused) FP8K_SBQ(1, true); else FP8K_SBQ(1, false);
+  }
+#undef FP8K_SBQ
   return cudaGetLastError();
 }
 
@@ -126,10 +364,30 @@ cudaError_t launch_adamw(float *p, const float *g, float *m, float *v, void *pb,
   const float bc1 = (float)(1.0 - pow(b1, (double)step));
   const float bc2 = (float)(1.0 - pow(b2, (double)step));
   const float omb1 = (float)(1.0 - b1), omb2 = (float)(1.0 - b2);
-  adamw_kernel<<<blocks_for(nvec, 512, sms), 512, 0, st>>>(
+  adamw_kernel<<<blocks_for(nvec, 512, 4, sms), 512, 0, st>>>(
       reinterpret_cast<float4 *>(p), reinterpret_cast<const float4 *>(g),
       reinterpret_cast<float4 *>(m), reinterpret_cast<float4 *>(v), static_cast<uint2 *>(pb), nvec,
       (float)lr, (float)b1, (float)b2, omb1, omb2, (float)eps, (float)(1.0 - lr * wd), bc1, bc2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adamw_multi(AdamwMulti a, double lr, double b1, double b2, double eps,
+                               double wd, int sms, cudaStream_t st) {
+  a.lr = (float)lr;
+  a.b1 = (float)b1;
+  a.b2 = (float)b2;
+  a.omb1 = (float)(1.0 - b1);
+  a.omb2 = (float)(1.0 - b2);
+  a.eps = (float)eps;
+  a.decay = (float)(1.0 - lr * wd);
+  a.b1d = b1;
+  a.b2d = b2;
+  int64_t most = 0;
+  for (int k = 0; k < a.count; ++k) most = a.n[k] > most ? a.n[k] : most;
+  adamw_advance_step_kernel<<<1, 1, 0, st>>>(a.step);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || most == 0) return e;
+  adamw_multi_kernel<<<blocks_for(most / 4, 512, 4, sms), 512, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,13 @@ dW1 = dh^T x reads dh's and x's codes MN-major), so no transposed copies are
 written.  GEMMs with independent outputs share one grouped launch (h and u;
 da and dW2; dx's first term, dW1 and dW3).
 
+Delayed scaling fixes every scale before its tensor exists, so the SwiGLU
+passes quantize what they produce: a, dh and du reach memory only as FP8
+codes (fp8_swiglu_forward_quantize / _backward_quantize give the same codes
+and amaxes as the bf16 tensors quantized afterwards would).  The optimizer
+keeps its step count on the device (fp8_adamw_multi), so `step` issues the
+same calls every time and can be captured as a CUDA graph and replayed.
+
 Buffers are allocated once (device memory through torch); `step` issues the
 calls on the current stream.
 """
@@ -75,14 +82,18 @@ class SwiGLUTrainer:
         self.aq = torch.empty((T, ffn), **u8)
         self.dyq = torch.empty((T, d), **u8)
         self.dhq, self.duq = torch.empty((T, ffn), **u8), torch.empty((T, ffn), **u8)
-        # activations and gradients
-        self.h, self.u, self.a = (torch.empty((T, ffn), **bf) for _ in range(3))
+        # activations and gradients (a, dh and du exist only as codes)
+        self.h, self.u = (torch.empty((T, ffn), **bf) for _ in range(2))
         self.y = torch.empty((T, d), **bf)
-        self.da, self.dh, self.du = (torch.empty((T, ffn), **bf) for _ in range(3))
+        self.da = torch.empty((T, ffn), **bf)
         self.dx = torch.empty((T, d), **f32)
         self.dw = [torch.empty((ffn, d), **f32), torch.empty((ffn, d), **f32),
                    torch.empty((d, ffn), **f32)]
         self.flops_per_step = 9 * 2.0 * T * d * ffn
+        # optimizer step count on the device (advanced by fp8_adamw_multi)
+        self.step_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.adamw_items = [F.adamw_item(self.w_master[i], self.dw[i], self.m[i], self.v[i],
+                                         self.w_bf[i]) for i in range(3)]
         # automatic weight scaling: amax at the last max-reduction, steps since
         self.w_amax0 = torch.zeros(3, **f32)
         self.t_since = 0
@@ -121,17 +132,16 @@ class SwiGLUTrainer:
         q(w2, E4, self.w2q, scale=sc(K2), amax_out=wam[2])
         run([P(self.xq, E4, self.w1q, E4, sc(X1), sc(K1), self.h),          # h = x W1^T
              P(self.xq, E4, self.w3q, E4, sc(X1), sc(K3), self.u)])         # u = x W3^T
-        F.fp8_swiglu_forward(self.h, self.u, self.a)
-        q(self.a, E4, self.aq, scale=sc(A2), amax_out=self._am(A2))
+        F.fp8_swiglu_forward_quantize(self.h, self.u, E4, sc(A2), self.aq,   # a = silu(h) u
+                                      self._am(A2))
         run([P(self.aq, E4, self.w2q, E4, sc(A2), sc(K2), self.y)])         # y = a W2^T
         # backward
         q(dy, E5, self.dyq, scale=sc(G2), amax_out=self._am(G2))
         run([P(self.dyq, E5, self.w2q, E4, sc(G2), sc(K2), self.da, b_layout=MN),   # da = dy W2
              P(self.dyq, E5, self.aq, E4, sc(G2), sc(A2), self.dw[2],               # dW2 = dy^T a
                a_layout=MN, b_layout=MN)])
-        F.fp8_swiglu_backward(self.da, self.h, self.u, self.dh, self.du)
-        q(self.dh, E5, self.dhq, scale=sc(G1), amax_out=self._am(G1))
-        q(self.du, E5, self.duq, scale=sc(G3), amax_out=self._am(G3))
+        F.fp8_swiglu_backward_quantize(self.da, self.h, self.u, E5, sc(G1), sc(G3),  # dh, du
+                                       self.dhq, self.duq, self._am(G1), self._am(G3))
         run([P(self.dhq, E5, self.w1q, E4, sc(G1), sc(K1), self.dx, b_layout=MN),   # dx = dh W1
              P(self.dhq, E5, self.xq, E4, sc(G1), sc(X1), self.dw[0],               # dW1 = dh^T x
                a_layout=MN, b_layout=MN),
@@ -143,9 +153,7 @@ class SwiGLUTrainer:
     def optimizer_and_state(self):
         """AdamW on the three weights, then the nine amax-history pushes."""
         self.t += 1
-        for i in range(3):
-            F.fp8_adamw_step(self.w_master[i], self.dw[i], self.m[i], self.v[i], self.w_bf[i],
-                             self.t, **self.hp)
+        F.fp8_adamw_multi(self.adamw_items, self.step_dev, **self.hp)
         auto = self.weight_scaling == "auto"
         if auto:
             self.t_since += 1

@@ -330,32 +330,38 @@ FP8_API int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, c
                    fp8_stream_t stream);
 
 /* ------------------------------------- GEMM, per K group, no allocation --
- * fp8_gemm_group_noalloc: the same computation, arguments and output as
- * fp8_gemm_group, for callers that cannot allocate device memory.  The pages
- * have no counterpart to this entry point; it exists for this library's
- * users.
+ * fp8_gemm_group_noalloc: the per-K-group GEMM of fp8_gemm_group (same
+ * arguments, same definition, same bound) for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this entry point; it
+ * exists for this library's users.  Its result agrees with fp8_gemm_group's
+ * within the GEMM bound, not bit for bit: it always runs the tensor-core
+ * per-group kernel, while fp8_gemm_group takes the CUDA-core path for one
+ * row and converts UE8M0 scales to block-scale words for M > 128.
  *
- * Why: for small M, fp8_gemm_group splits K across CTAs and keeps fp32
- * partial sums and per-tile counters in a workspace that it cudaMalloc's the
- * first time a (device, stream) pair needs it.  A caller that is capturing
- * the stream into a CUDA graph cannot allocate at that point, and runtimes
- * that own all device memory in their own pool, or that must never wait on
- * the allocator, cannot let the library allocate at all.  This entry point
- * calls no cudaMalloc or cudaFree: its scratch is one array compiled into the
- * library (64 KiB of counters + 8 MiB of fp32 partials, 256-byte aligned),
- * which every GPU that loads the library holds until the process exits.
+ * Why: fp8_gemm_group allocates device memory on first use for some shapes
+ * (the E8M0-word buffer of UE8M0 scales at M > 128).  Some callers cannot
+ * let a library do that: runtimes that reserve all device memory up front in
+ * their own pool (an inference server with a fixed memory budget), and code
+ * that must never stall on the allocator (cudaMalloc and cudaFree may
+ * synchronize the device).  This entry point calls no cudaMalloc, cudaFree
+ * or other allocating routine: where it splits K over CTAs for small M, its
+ * fp32 partial sums and per-tile counters live in one array compiled into
+ * the library (64 KiB of counters + 8 MiB of fp32 partials, 256-byte
+ * aligned), which every GPU that loads the library holds until the process
+ * exits.  The caller still passes the inputs and the output.
  *
  * Limits and rules:
  *   - A shape whose split-K partials need more than 8 MiB (or more than 16384
  *     output tiles of counters) is rejected with FP8_ERR_SCRATCH_LIMIT; shapes
- *     that need no split run without scratch.
+ *     that need no split run without the array.
  *   - The first call on each device looks up the array's device address (and
  *     does the library's per-device set-up); make that first call before any
  *     stream capture.
- *   - Every call on a device shares the one array and it keeps the last
- *     call's contents; each call clears the counters it uses on its stream.
- *     Calls that overlap on the GPU (different streams, or concurrent graph
- *     branches) race on the array and give wrong results: serialize them.
+ *   - Every call on a device shares the one array, and it keeps the last
+ *     call's contents; each call clears the counters it uses on its stream
+ *     before the kernel runs.  Calls that overlap on the GPU (different
+ *     streams, or concurrent graph branches) race on the array and give wrong
+ *     results: serialize them.
  */
 FP8_API int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const uint8_t *b,
                                    const void *sb, int sfmt, int64_t M, int64_t N, int64_t K,
@@ -459,6 +465,55 @@ FP8_API int fp8_swiglu_backward(const void *da, const void *h, const void *u, vo
 FP8_API int fp8_adamw_step(float *p, const float *g, float *m, float *v, void *p_bf16, int64_t n,
                    int64_t step, double lr, double beta1, double beta2, double eps,
                    double weight_decay, fp8_stream_t stream);
+
+/* ------------------------------- SwiGLU fused with delayed scaling --
+ * With delayed scaling the quantization scale of a tensor is known before
+ * the tensor is formed ([Flax] 2.3: in_q quantizes with the scale the
+ * previous step's amax history left and records the current amax), so the
+ * SwiGLU passes can quantize their outputs as they produce them.  The values
+ * are exactly those of fp8_swiglu_forward / _backward (the same bf16
+ * rounding), and the codes and amax exactly those fp8_quantize_tensor would
+ * give for that bf16 tensor with `scale` and `amax_out`: the bf16 tensor is
+ * simply never written to memory.
+ *
+ * fp8_swiglu_forward_quantize: a = bf16(silu(h) * u); q = codes of a / scale
+ *   (fmt), amax_out = max |a| (nullable; cleared first; must not alias scale).
+ * fp8_swiglu_backward_quantize: dh, du as fp8_swiglu_backward; q_dh, q_du =
+ *   their codes under scale_dh, scale_du (both in format fmt, E5M2 for
+ *   gradients, [Flax] 3.3); amax_dh, amax_du = max |dh|, max |du| (both null
+ *   or both set, distinct from each other and from the scales).
+ * n elements, n % 8 == 0; h, u, da bf16, 16-byte aligned; q's 16-byte aligned.
+ * n == 0 writes only the amaxes (0); the other pointers may then be null.
+ */
+FP8_API int fp8_swiglu_forward_quantize(const void *h, const void *u, int64_t n, int fmt,
+                                        const float *scale, uint8_t *q, float *amax_out,
+                                        fp8_stream_t stream);
+FP8_API int fp8_swiglu_backward_quantize(const void *da, const void *h, const void *u, int64_t n,
+                                         int fmt, const float *scale_dh, const float *scale_du,
+                                         uint8_t *q_dh, uint8_t *q_du, float *amax_dh,
+                                         float *amax_du, fp8_stream_t stream);
+
+/* fp8_adamw_multi: one AdamW step (as fp8_adamw_step) over `count` (1..8)
+ * parameter tensors in one launch, with the step number kept on the device:
+ * the call first increments *step (device int64, 8-byte aligned) and the
+ * update uses the incremented value as t (bias corrections 1 - beta^t formed
+ * in double on the device).  A captured training step therefore advances t
+ * on every replay.  Start *step at 0 for a fresh optimizer.
+ *   items  HOST array of `count` descriptors (read during the call only);
+ *          per item p, g, m, v fp32 [n] and p_bf16 (nullable) bf16 [n], all
+ *          device, 16-byte aligned (p_bf16 8-byte), n % 4 == 0; empty items
+ *          (n == 0) may have null pointers. */
+typedef struct {
+  float *p;
+  const float *g;
+  float *m;
+  float *v;
+  void *p_bf16;
+  int64_t n;
+} fp8_adamw_item_t;
+FP8_API int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, double lr,
+                            double beta1, double beta2, double eps, double weight_decay,
+                            fp8_stream_t stream);
 
 /* ---------------------------------------------------------------- status --
  * fp8_status_string: static text for a status code.
