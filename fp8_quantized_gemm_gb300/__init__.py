@@ -181,25 +181,65 @@ def fp8_gemm_tensor(a, fa, b, fb, sa, sb, out, *, out_dt=None, accumulate=False,
           out.stride(0), int(bool(accumulate)), _stream(stream))
 
 
+class AdamwEpilogue(ctypes.Structure):
+    """fp8_adamw_epilogue_t (include/fp8gemm.h)."""
+    _fields_ = [("p", _vp), ("m", _vp), ("v", _vp), ("p_bf16", _vp), ("step", _vp),
+                ("lr", _d), ("beta1", _d), ("beta2", _d), ("eps", _d), ("weight_decay", _d)]
+
+
+class SwigluEpilogue(ctypes.Structure):
+    """fp8_swiglu_epilogue_t (include/fp8gemm.h)."""
+    _fields_ = [("b_up", _vp), ("sb_up", _vp), ("u", _vp), ("q", _vp), ("fmt", _int),
+                ("scale", _vp), ("amax", _vp)]
+
+
 class GemmProblem(ctypes.Structure):
     """fp8_gemm_problem_t (include/fp8gemm.h)."""
     _fields_ = [("a", _vp), ("b", _vp), ("sa", _vp), ("sb", _vp), ("M", _i64), ("N", _i64),
                 ("K", _i64), ("fa", _int), ("fb", _int), ("out_dt", _int), ("accumulate", _int),
                 ("c", _vp), ("ldc", _i64), ("a_layout", _int), ("b_layout", _int),
-                ("bias", _vp)]
+                ("bias", _vp), ("adamw", ctypes.POINTER(AdamwEpilogue)),
+                ("swiglu", ctypes.POINTER(SwigluEpilogue))]
+
+
+def adamw_epilogue(p, m, v, p_bf16, step, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8,
+                   weight_decay=0.01):
+    """AdamW epilogue of a weight-gradient GEMM: the GEMM result (shape of p)
+    updates p, m, v and the bf16 copy in place at t = step[0] (device int64,
+    read only)."""
+    assert step.dtype == torch.int64 and step.numel() == 1
+    return AdamwEpilogue(_p(p), _p(m), _p(v), _p(p_bf16), _p(step), lr, beta1, beta2, eps,
+                         weight_decay)
+
+
+def swiglu_epilogue(b_up, sb_up, u, q, fmt, scale, amax):
+    """Gated SwiGLU epilogue: the problem's b (W1) and b_up (W3) give h (the
+    problem's output) and u; q receives the codes of silu(h) u under `scale`."""
+    return SwigluEpilogue(_p(b_up), _p(sb_up), _p(u), _p(q), fmt, _p(scale), _p(amax))
 
 
 def gemm_problem(a, fa, b, fb, sa, sb, out, *, accumulate=False, a_layout=K_MAJOR,
-                 b_layout=K_MAJOR, bias=None):
+                 b_layout=K_MAJOR, bias=None, adamw=None, swiglu=None, n=None, ldc=None):
     """Descriptor of one per-tensor GEMM for fp8_gemm_tensor_grouped.  With
     K_MAJOR a is [M, K] and b [N, K]; with MN_MAJOR a is [K, M] and b [K, N];
-    bias: optional device fp32 [N] added to every row."""
+    bias: optional device fp32 [N] added to every row.  adamw / swiglu:
+    epilogue descriptors (adamw_epilogue / swiglu_epilogue); with adamw, `out`
+    may be None (the result updates the parameters instead)."""
     m, k = a.shape if a_layout == K_MAJOR else a.shape[::-1]
-    n = b.shape[0] if b_layout == K_MAJOR else b.shape[1]
-    out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
-    return GemmProblem(_p(a), _p(b), _p(sa), _p(sb), m, n, k, fa, fb, out_dt,
-                       int(bool(accumulate)), _p(out), out.stride(0), a_layout, b_layout,
-                       _p(bias) if bias is not None else None)
+    if n is None:
+        n = b.shape[0] if b_layout == K_MAJOR else b.shape[1]
+    if out is None:
+        out_dt, c, pitch = OUT_F32, None, ldc if ldc is not None else n
+    else:
+        out_dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+        c, pitch = _p(out), out.stride(0)
+    prob = GemmProblem(_p(a), _p(b), _p(sa), _p(sb), m, n, k, fa, fb, out_dt,
+                       int(bool(accumulate)), c, pitch, a_layout, b_layout,
+                       _p(bias) if bias is not None else None,
+                       ctypes.pointer(adamw) if adamw is not None else None,
+                       ctypes.pointer(swiglu) if swiglu is not None else None)
+    prob._keep = (adamw, swiglu)  # the descriptors live as long as the problem
+    return prob
 
 
 class QuantItem(ctypes.Structure):
@@ -342,11 +382,12 @@ def adamw_item(p, g, m, v, p_bf16=None):
 def fp8_adamw_multi(items, step, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
                     stream=None):
     """One AdamW step over several tensors; `step` is a device int64 tensor of
-    one element, incremented by the call (the update uses the new value)."""
+    one element, incremented by the call (the update uses the new value).  No
+    items: only the increment."""
     assert step.dtype == torch.int64 and step.numel() == 1
-    arr = (AdamwItem * len(items))(*items)
-    _call("fp8_adamw_multi", ctypes.cast(arr, _vp), len(items), _p(step), lr, beta1, beta2, eps,
-          weight_decay, _stream(stream))
+    arr = (AdamwItem * len(items))(*items) if items else None
+    _call("fp8_adamw_multi", ctypes.cast(arr, _vp) if arr is not None else None, len(items),
+          _p(step), lr, beta1, beta2, eps, weight_decay, _stream(stream))
 
 
 def fp8_get_last_device_error(stream=None):

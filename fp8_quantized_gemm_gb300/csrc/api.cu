@@ -271,10 +271,35 @@ int check_tensor_problem(const fp8_gemm_problem_t &p) {
   if (!aligned16(p.a) || !aligned16(p.b)) return FP8_ERR_MISALIGNED;
   if ((!a_mn || !b_mn) && p.K % 16 != 0) return FP8_ERR_MISALIGNED;
   if ((a_mn && p.M % 16 != 0) || (b_mn && p.N % 16 != 0)) return FP8_ERR_MISALIGNED;
+  if (p.adamw != nullptr && p.swiglu != nullptr) return FP8_ERR_INVALID_ARG;
+  if (p.adamw != nullptr) {
+    const fp8_adamw_epilogue_t &e = *p.adamw;
+    if (e.p == nullptr || e.m == nullptr || e.v == nullptr || e.step == nullptr)
+      return FP8_ERR_INVALID_ARG;
+    if (p.out_dt != FP8_OUT_F32 || p.accumulate != 0 || p.bias != nullptr || p.ldc < p.N)
+      return FP8_ERR_UNSUPPORTED;
+    if (!aligned16(e.p) || !aligned16(e.m) || !aligned16(e.v) || p.ldc % 4 != 0 ||
+        (reinterpret_cast<uintptr_t>(e.p_bf16) & 7u) != 0 ||
+        (reinterpret_cast<uintptr_t>(e.step) & 7u) != 0)
+      return FP8_ERR_MISALIGNED;
+    return FP8_OK;
+  }
   int rc = check_output(p.c, p.N, p.ldc, p.out_dt);
   if (rc != FP8_OK) return rc;
   if (p.accumulate != 0 && (p.accumulate != 1 || p.out_dt != FP8_OUT_F32))
     return FP8_ERR_UNSUPPORTED;
+  if (p.swiglu != nullptr) {
+    const fp8_swiglu_epilogue_t &e = *p.swiglu;
+    if (e.b_up == nullptr || e.sb_up == nullptr || e.u == nullptr || e.q == nullptr ||
+        e.scale == nullptr || e.amax == nullptr || !valid_fmt(e.fmt))
+      return FP8_ERR_INVALID_ARG;
+    if (e.amax == e.scale) return FP8_ERR_INVALID_ARG;
+    if (p.out_dt != FP8_OUT_BF16 || p.accumulate != 0 || p.bias != nullptr)
+      return FP8_ERR_UNSUPPORTED;
+    if (!aligned16(e.b_up) || !aligned16(e.u) || !aligned16(e.q) || !aligned16(p.c) ||
+        p.N % 32 != 0 || p.ldc % 16 != 0)
+      return FP8_ERR_MISALIGNED;
+  }
   return FP8_OK;
 }
 
@@ -531,13 +556,22 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
   const cudaStream_t st = (cudaStream_t)stream;
   // one persistent CTA-pair launch when every problem takes that path
   bool together = g_use_pairs && count <= fp8k::kMaxGroup;
+  bool epilogue = false;
   int64_t tiles = 0;
-  for (int i = 0; i < count && together; ++i) {
+  for (int i = 0; i < count; ++i) {
     const fp8_gemm_problem_t &p = problems[i];
-    together = fp8k::gemm_ksplit(fp8k::kScaleTensor, p.M, p.N, p.K, d->sms, true) == 1;
+    epilogue = epilogue || p.adamw != nullptr || p.swiglu != nullptr;
+    together = together &&
+               fp8k::gemm_ksplit(fp8k::kScaleTensor, p.M, p.N, p.K, d->sms, true) == 1;
     tiles += ((p.M + 255) / 256) * ((p.N + 255) / 256);
   }
   together = together && tiles * 4 >= d->sms / 2;
+  // the epilogue variants live in the pair kernel, which takes any shape
+  // (ragged tiles are masked): a group with one always runs there
+  if (epilogue) {
+    if (count > fp8k::kMaxGroup) return FP8_ERR_UNSUPPORTED;
+    together = true;
+  }
   if (!together) {
     for (int i = 0; i < count; ++i)
       if ((rc = run_tensor_problem(problems[i], st)) != FP8_OK) return rc;
@@ -553,6 +587,8 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
       order[j - 1] = tmp;
     }
   CUtensorMap tma[fp8k::kMaxGroup], tmb[fp8k::kMaxGroup], tmc[fp8k::kMaxGroup] = {};
+  CUtensorMap tmb2[fp8k::kMaxGroup] = {};
+  bool any_gated = false;
   GemmArgs args[fp8k::kMaxGroup];
   for (int k = 0; k < count; ++k) {
     const fp8_gemm_problem_t &p = problems[order[k]];
@@ -567,6 +603,34 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
     a.bias = p.bias;
     a.ksplit = 1;
     a.tma_store = use_tma_store(p.c, p.ldc, p.out_dt, p.accumulate) ? 1 : 0;
+    if (p.adamw != nullptr) {
+      const fp8_adamw_epilogue_t &e = *p.adamw;
+      a.tma_store = 0;
+      a.vec_store = 1;  // 16-byte aligned parameters and pitch (validated)
+      a.adam_p = e.p;
+      a.adam_m = e.m;
+      a.adam_v = e.v;
+      a.adam_pb = e.p_bf16;
+      a.adam_step = e.step;
+      a.adam_hp = fp8k::adamw_hp(e.lr, e.beta1, e.beta2, e.eps, e.weight_decay);
+      a.adam_b1d = e.beta1;
+      a.adam_b2d = e.beta2;
+    }
+    if (p.swiglu != nullptr) {
+      const fp8_swiglu_epilogue_t &e = *p.swiglu;
+      a.tma_store = 0;
+      a.gated = 1;
+      a.swi_sb2 = e.sb_up;
+      a.swi_u = e.u;
+      a.swi_q = e.q;
+      a.swi_scale = e.scale;
+      a.swi_amax = reinterpret_cast<uint32_t *>(e.amax);
+      a.swi_fmt = e.fmt;
+      any_gated = true;
+      if ((rc = encode_gemm_operand(&tmb2[k], e.b_up, a.b_mn, p.K, p.N,
+                                    fp8k::gemm_pair_b_rows())) != FP8_OK)
+        return rc;
+    }
     if (a.tma_store && (rc = encode_output(&tmc[k], p.c, p.out_dt, p.M, p.N, p.ldc)) != FP8_OK)
       return rc;
     args[k] = a;
@@ -575,7 +639,8 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
         FP8_OK)
       return rc;
   }
-  return to_status(fp8k::launch_gemm_pair_group(tma, tmb, tmc, args, count, d->sms, st));
+  return to_status(fp8k::launch_gemm_pair_group(tma, tmb, tmc, any_gated ? tmb2 : nullptr, args,
+                                                count, d->sms, st));
 }
 
 int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb, int sfmt,
@@ -804,7 +869,7 @@ int fp8_swiglu_backward_quantize(const void *da, const void *h, const void *u, i
 int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, double lr,
                     double beta1, double beta2, double eps, double weight_decay,
                     fp8_stream_t stream) {
-  if (items == nullptr || step == nullptr || count < 1 || count > fp8k::kMaxAdamw)
+  if (step == nullptr || count < 0 || count > fp8k::kMaxAdamw || (count > 0 && items == nullptr))
     return FP8_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(step) & 7u) != 0) return FP8_ERR_MISALIGNED;
   fp8k::AdamwMulti a{};

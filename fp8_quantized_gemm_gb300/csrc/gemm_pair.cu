@@ -30,9 +30,23 @@
 // the prologue, pipeline fill and tail once for all of them (the Float8
 // linear's y, dx and dW GEMMs are independent once their operands are
 // quantized).
+//
+// Two epilogue variants fold the training step's element-wise work into the
+// GEMM, so that its inputs are read from TMEM instead of HBM (the epilogue of
+// one tile runs while the MMAs of the next fill the other accumulator):
+//   - gated SwiGLU (h = x W1^T, u = x W3^T): rank 0 of the pair stages rows
+//     of W1 and rank 1 the same rows of W3, so each 256 x 256 accumulator is
+//     [h | u] for 128 output columns; the epilogue writes h and u (bf16) and
+//     the codes of a = silu(h) u under the delayed scale, and its amax;
+//   - AdamW on a weight-gradient GEMM: the fp32 gradient tile updates the
+//     parameters, moments and bf16 copy in place and is never stored.
+// Both use exactly the arithmetic of the standalone kernels (elementwise.cuh),
+// so the results are the same bits.
 #include "common.cuh"
+#include "elementwise.cuh"
 #include "gemm_common.cuh"
 #include "kernels.h"
+#include "quant_common.cuh"
 
 namespace fp8k {
 
@@ -63,7 +77,8 @@ struct PairCfg {
 struct PairGroup {
   CUtensorMap tma[kMaxGroup];
   CUtensorMap tmb[kMaxGroup];
-  CUtensorMap tmc[kMaxGroup];  // outputs (problems with args.tma_store)
+  CUtensorMap tmc[kMaxGroup];   // outputs (problems with args.tma_store)
+  CUtensorMap tmb2[kMaxGroup];  // second weight of gated problems
   GemmArgs args[kMaxGroup];
   int64_t tile_begin[kMaxGroup + 1];  // problem i owns tiles [tile_begin[i], tile_begin[i+1])
   int count;
@@ -74,6 +89,98 @@ __device__ __forceinline__ int group_of(const PairGroup &g, int64_t t) {
   int i = 0;
   while (i + 1 < g.count && t >= g.tile_begin[i + 1]) ++i;
   return i;
+}
+
+// AdamW on 32 consecutive parameters of row `row` (columns col0 ..), with
+// the fp32 gradient g of those columns (the GEMM result).  All 24 loads of a
+// full chunk are issued before any update; p, m and v stream (each is read
+// and written once per step).
+__device__ __forceinline__ void adamw_row32(const GemmArgs &a, int64_t row, int64_t col0,
+                                            const float (&g)[32], const AdamwHp &hp) {
+  if (row >= a.M || col0 >= a.N) return;
+  const int64_t off = row * a.ldc + col0;
+  float *p = a.adam_p + off, *m = a.adam_m + off, *v = a.adam_v + off;
+  __nv_bfloat16 *pb =
+      a.adam_pb != nullptr ? static_cast<__nv_bfloat16 *>(a.adam_pb) + off : nullptr;
+  if (col0 + 32 <= a.N && a.vec_store) {
+    float4 pv[8], mv[8], vv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      pv[i] = __ldcs(reinterpret_cast<const float4 *>(p) + i);
+      mv[i] = __ldcs(reinterpret_cast<const float4 *>(m) + i);
+      vv[i] = __ldcs(reinterpret_cast<const float4 *>(v) + i);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      adamw4(pv[i], mv[i], vv[i], make_float4(g[4 * i], g[4 * i + 1], g[4 * i + 2], g[4 * i + 3]),
+             hp);
+      __stcs(reinterpret_cast<float4 *>(p) + i, pv[i]);
+      __stcs(reinterpret_cast<float4 *>(m) + i, mv[i]);
+      __stcs(reinterpret_cast<float4 *>(v) + i, vv[i]);
+      if (pb != nullptr) __stcs(reinterpret_cast<uint2 *>(pb) + i, f32x4_to_bf16(pv[i]));
+    }
+  } else {
+    for (int i = 0; i < 32 && col0 + i < a.N; ++i) {
+      float pp = p[i], mm = m[i], vvv = v[i];
+      adamw1(pp, mm, vvv, g[i], hp);
+      p[i] = pp;
+      m[i] = mm;
+      v[i] = vvv;
+      if (pb != nullptr) pb[i] = __float2bfloat16_rn(pp);
+    }
+  }
+}
+
+// The gated SwiGLU epilogue for 32 columns of one row: h and u (fp32 scaled
+// results) are rounded to bf16 and stored, a = bf16(silu(h) u) is divided by
+// the delayed scale and cast (the codes fp8_swiglu_forward_quantize would
+// give for the stored h and u), and |a| enters the running key.  Full
+// chunks only (N % 32 == 0 and 16-byte rows, checked by the host).
+template <bool kFast>
+__device__ __forceinline__ void gated_row32(const GemmArgs &a, int64_t row, int64_t col0,
+                                            const float (&hv)[32], const float (&uv)[32],
+                                            const ScaleDiv &d, uint32_t &key) {
+  if (row >= a.M || col0 >= a.N) return;
+  const int64_t off = row * a.ldc + col0;
+  float hb[32], ub[32], ab[32];
+  uint32_t hw[16], uw[16], aw[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(hv[2 * i], hv[2 * i + 1]);
+    const __nv_bfloat162 u2 = __floats2bfloat162_rn(uv[2 * i], uv[2 * i + 1]);
+    hw[i] = *reinterpret_cast<const uint32_t *>(&h2);
+    uw[i] = *reinterpret_cast<const uint32_t *>(&u2);
+    hb[2 * i] = __uint_as_float(hw[i] << 16);
+    hb[2 * i + 1] = __uint_as_float(hw[i] & 0xFFFF0000u);
+    ub[2 * i] = __uint_as_float(uw[i] << 16);
+    ub[2 * i + 1] = __uint_as_float(uw[i] & 0xFFFF0000u);
+  }
+  uint4 *hd = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.c) + off);
+  uint4 *ud = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.swi_u) + off);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    hd[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
+    ud[i] = make_uint4(uw[4 * i], uw[4 * i + 1], uw[4 * i + 2], uw[4 * i + 3]);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __nv_bfloat162 a2 = __floats2bfloat162_rn(swiglu_value(hb[2 * i], ub[2 * i]),
+                                                    swiglu_value(hb[2 * i + 1], ub[2 * i + 1]));
+    aw[i] = *reinterpret_cast<const uint32_t *>(&a2);
+    ab[2 * i] = __uint_as_float(aw[i] << 16);
+    ab[2 * i + 1] = __uint_as_float(aw[i] & 0xFFFF0000u);
+    key = max(key, max(abs_key(ab[2 * i]), abs_key(ab[2 * i + 1])));
+  }
+  uint2 c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float y[8];
+    d.div8<kFast>(*reinterpret_cast<const float(*)[8]>(ab + 8 * j), y);
+    c[j] = pack8(a.swi_fmt, y);
+  }
+  uint4 *qd = reinterpret_cast<uint4 *>(a.swi_q + off);
+  qd[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+  qd[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
 }
 
 template <int BN, int STAGES>
@@ -141,7 +248,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
     r.i = group_of(grp, gt);
     const GemmArgs &a = grp.args[r.i];
     const int64_t t = gt - grp.tile_begin[r.i];
-    const int64_t tiles_n = (a.N + BN - 1) / BN;
+    // a gated tile covers BN / 2 output columns (h and u of each)
+    const int64_t tn = a.gated ? BN / 2 : BN;
+    const int64_t tiles_n = (a.N + tn - 1) / tn;
     // grouped order: bands of kPairBandRows 256-row tiles walked column by
     // column, so the pairs in flight share A and B blocks in L2
     const int64_t rows = (a.M + 255) / 256;
@@ -150,7 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
         rows - band * kPairBandRows < kPairBandRows ? rows - band * kPairBandRows : kPairBandRows;
     const int64_t local = t - band * kPairBandRows * tiles_n;
     r.m0 = (band * kPairBandRows + local % band_rows) * 256;
-    r.n0 = (local / band_rows) * BN;
+    r.n0 = (local / band_rows) * tn;
     r.kb_count = (int)((a.K + C::BK - 1) / C::BK);
     return r;
   };
@@ -163,9 +272,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
     for (int64_t gt = pair; gt < num_tiles && ok; gt += npairs) {
       const TileRef tr = tile_ref(gt);
       const CUtensorMap *ma = &grp.tma[tr.i];
-      const CUtensorMap *mb = &grp.tmb[tr.i];
+      // gated: both CTAs stage the same B rows, rank 1 from the second weight
+      const bool gated = grp.args[tr.i].gated != 0;
+      const CUtensorMap *mb = gated && rank != 0 ? &grp.tmb2[tr.i] : &grp.tmb[tr.i];
       const int64_t m0 = tr.m0 + rank * C::BM;
-      const int64_t nb0 = tr.n0 + rank * (BN / 2);
+      const int64_t nb0 = gated ? tr.n0 : tr.n0 + rank * (BN / 2);
       for (int kb = 0; kb < tr.kb_count; ++kb, ++it) {
         const int s = (int)(it % STAGES);
         const uint32_t round = it / STAGES;
@@ -249,6 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
     const uint32_t lane_base = tmem + ((32u * q) << 16);
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
     const uint64_t out_policy = policy_evict_first();
+    uint32_t gkey[kMaxGroup] = {};  // running max |a| of each gated problem
     uint32_t j = 0, out_n = 0;
     for (int64_t gt = pair; gt < num_tiles; gt += npairs, ++j) {
       const TileRef tr = tile_ref(gt);
@@ -258,6 +370,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
       const uint32_t buf = j & 1u, use = j >> 1;
       if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) break;
       tc_fence_after();
+      if (a.gated) {
+        // columns [0, BN/2) of the accumulator are h, [BN/2, BN) are u
+        const float alpha_u = *static_cast<const float *>(a.sa) * *a.swi_sb2;
+        const ScaleDiv d(*a.swi_scale);
+        uint32_t key = 0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t rh[32], ru[32];
+          FP8K_TMEM_LD_X32(lane_base + buf * BN + (uint32_t)c, rh);
+          FP8K_TMEM_LD_X32(lane_base + buf * BN + (uint32_t)(BN / 2 + c), ru);
+          tmem_ld_wait();
+          if (c + 32 == BN / 2) {  // accumulator read out: hand it back to the leader
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader0 + 8u * buf);
+          }
+          float hv[32], uv[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            hv[i] = __uint_as_float(rh[i]) * alpha;
+            uv[i] = __uint_as_float(ru[i]) * alpha_u;
+          }
+          if (d.fast)
+            gated_row32<true>(a, row, tr.n0 + c, hv, uv, d, key);
+          else
+            gated_row32<false>(a, row, tr.n0 + c, hv, uv, d, key);
+        }
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g)
+          if (g == tr.i) gkey[g] = max(gkey[g], key);
+        continue;
+      }
+      if (a.adam_p != nullptr) {
+        // AdamW on the gradient tile; bias corrections from the step counter
+        AdamwHp hp = a.adam_hp;
+        float bc1 = 0.0f, bc2 = 0.0f;
+        if (lane == 0) {
+          const int64_t t = *a.adam_step;
+          bc1 = bias_correction(a.adam_b1d, t);
+          bc2 = bias_correction(a.adam_b2d, t);
+        }
+        hp.bc1 = __shfl_sync(0xffffffffu, bc1, 0);
+        hp.bc2 = __shfl_sync(0xffffffffu, bc2, 0);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          FP8K_TMEM_LD_X32(lane_base + buf * BN + (uint32_t)c, r);
+          tmem_ld_wait();
+          if (c + 32 == BN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader0 + 8u * buf);
+          }
+          float gv[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) gv[i] = __uint_as_float(r[i]) * alpha;
+          adamw_row32(a, row, tr.n0 + c, gv, hp);
+        }
+        continue;
+      }
       if (a.tma_store) {
         // 128-byte column chunks (64 bf16 or 32 fp32 values per row) staged
         // as a 32-row box in this warp's two alternating buffers (128-byte
@@ -341,6 +513,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
     // every TMA store has finished reading its box and writing C
     if (lane == 0) bulk_wait_all();
     __syncwarp();
+#pragma unroll
+    for (int g = 0; g < kMaxGroup; ++g) {
+      if (g < grp.count && grp.args[g].gated) {
+        const uint32_t k = warp_max_u32(gkey[g]);
+        if (lane == 0 && k != 0u) atomicMax(grp.args[g].swi_amax, k);
+      }
+    }
   }
 
   tc_fence_before();
@@ -363,9 +542,15 @@ bool gemm_pair_eligible(int mode, int64_t M, int64_t N, int sms) {
   return gemm_pair_tiles(M, N) * 4 >= sms / 2;
 }
 
+// Tiles of one problem: gated problems cover BN / 2 output columns per tile.
+int64_t gemm_pair_tiles_of(const GemmArgs &a) {
+  const int64_t tn = a.gated ? kPairBN / 2 : kPairBN;
+  return ((a.M + 255) / 256) * ((a.N + tn - 1) / tn);
+}
+
 cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tmb,
-                                   const CUtensorMap *tmc, const GemmArgs *args, int count,
-                                   int sms, cudaStream_t st) {
+                                   const CUtensorMap *tmc, const CUtensorMap *tmb2,
+                                   const GemmArgs *args, int count, int sms, cudaStream_t st) {
   using C = PairCfg<kPairBN, kPairStages>;
   if (count < 1 || count > kMaxGroup) return cudaErrorInvalidValue;
   auto kern = gemm_pair_kernel<kPairBN, kPairStages>;
@@ -386,9 +571,15 @@ cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tm
     g.tma[i] = tma[i];
     g.tmb[i] = tmb[i];
     if (tmc != nullptr) g.tmc[i] = tmc[i];
+    if (tmb2 != nullptr) g.tmb2[i] = tmb2[i];
     g.args[i] = args[i];
     if (tmc == nullptr) g.args[i].tma_store = 0;
-    g.tile_begin[i + 1] = g.tile_begin[i] + gemm_pair_tiles(args[i].M, args[i].N);
+    if (tmb2 == nullptr) g.args[i].gated = 0;
+    if (g.args[i].gated) {  // the fused amax starts from zero
+      e = cudaMemsetAsync(g.args[i].swi_amax, 0, sizeof(uint32_t), st);
+      if (e != cudaSuccess) return e;
+    }
+    g.tile_begin[i + 1] = g.tile_begin[i] + gemm_pair_tiles_of(g.args[i]);
   }
   for (int i = count; i < kMaxGroup; ++i) g.tile_begin[i + 1] = g.tile_begin[count];
   const int64_t tiles = g.tile_begin[count];
@@ -400,7 +591,7 @@ cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tm
 cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb,
                              const CUtensorMap &tmc, const GemmArgs &args, int sms,
                              cudaStream_t st) {
-  return launch_gemm_pair_group(&tma, &tmb, &tmc, &args, 1, sms, st);
+  return launch_gemm_pair_group(&tma, &tmb, &tmc, nullptr, &args, 1, sms, st);
 }
 
 }  // namespace fp8k

@@ -8,6 +8,13 @@
 
 namespace fp8k {
 
+// fp32 hyperparameters of one AdamW update: 1 - beta and the decay factor
+// 1 - lr * wd formed in double on the host; the bias corrections 1 - beta^t
+// (bc1, bc2) in double on the device from the step counter.
+struct AdamwHp {
+  float lr, b1, b2, omb1, omb2, eps, decay, bc1, bc2;
+};
+
 cudaError_t launch_amax(const void *x, int in_dt, int64_t n, float *out, int sms,
                         cudaStream_t st);
 cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, int fmt,
@@ -115,6 +122,29 @@ struct GemmArgs {
   // epilogue writes C through shared memory with TMA stores of 32-row x
   // 128-byte boxes (the kernel gets the output tensor map separately)
   int tma_store;
+  // AdamW epilogue (CTA-pair kernel): the fp32 result sa*sb*A*B^T is the
+  // gradient of the parameters adam_p [M, ldc] (moments adam_m, adam_v, bf16
+  // copy adam_pb, nullable), which it updates in place at step t =
+  // *adam_step; c is not written
+  float *adam_p, *adam_m, *adam_v;
+  void *adam_pb;
+  const int64_t *adam_step;
+  AdamwHp adam_hp;  // bc1, bc2 formed in the kernel
+  double adam_b1d, adam_b2d;
+  // Gated SwiGLU epilogue (CTA-pair kernel): in each pair, rank 0 stages
+  // rows of B and rank 1 the same rows of a second weight (its own tensor
+  // map; dequant scale swi_sb2), so one 256 x 256 accumulator holds h
+  // (columns 0-127) and u (128-255) of the same 128 output columns.  The
+  // epilogue writes c <- bf16(h), swi_u <- bf16(u) and swi_q <- the codes of
+  // a = bf16(silu(h) u) divided by *swi_scale (format swi_fmt), all [M, ldc],
+  // and folds max |a| into *swi_amax (cleared by the launcher)
+  int gated;
+  const float *swi_sb2;
+  void *swi_u;
+  uint8_t *swi_q;
+  const float *swi_scale;
+  uint32_t *swi_amax;
+  int swi_fmt;
 };
 constexpr int kMaxExperts = 256;
 
@@ -142,9 +172,11 @@ bool gemm_pair_eligible(int mode, int64_t M, int64_t N, int sms);
 constexpr int kMaxGroup = 4;  // problems per grouped launch
 // One launch over `count` independent per-tensor problems (longest K first).
 // tmc[i]: the output tensor map of problem i (read when args[i].tma_store).
+// tmb2[i]: the second weight of a gated problem (read when args[i].gated;
+// tmb2 may be null when no problem is gated).
 cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tmb,
-                                   const CUtensorMap *tmc, const GemmArgs *args, int count,
-                                   int sms, cudaStream_t st);
+                                   const CUtensorMap *tmc, const CUtensorMap *tmb2,
+                                   const GemmArgs *args, int count, int sms, cudaStream_t st);
 int gemm_pair_b_rows();
 cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb,
                              const CUtensorMap &tmc, const GemmArgs &args, int sms,

@@ -9,6 +9,7 @@
 // value for the same inputs: the fused kernels quantize exactly the bf16
 // tensor the plain kernel would have written.
 #include "common.cuh"
+#include "elementwise.cuh"
 #include "kernels.h"
 #include "quant_common.cuh"
 #include "support.h"
@@ -37,25 +38,6 @@ __device__ __forceinline__ uint4 f32x8_to_bf16(const float (&v)[8]) {
 // The eight bf16 values of a packed vector, widened back to fp32 (exact).
 __device__ __forceinline__ void bf16_roundtrip(const float (&v)[8], float (&o)[8]) {
   bf16x8_to_f32(f32x8_to_bf16(v), o);
-}
-
-// logistic function 1 / (1 + e^-z), IEEE division
-__device__ __forceinline__ float sigmoidf_(float z) {
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
-}
-
-// a = silu(h) * u = (h * s(h)) * u
-__device__ __forceinline__ float swiglu_value(float h, float u) {
-  return __fmul_rn(__fmul_rn(h, sigmoidf_(h)), u);
-}
-
-// dh = (da * u) * s(h) (1 + h (1 - s(h)));  du = da * (h * s(h))
-__device__ __forceinline__ void swiglu_grad_values(float da, float h, float u, float &dh,
-                                                   float &du) {
-  const float s = sigmoidf_(h);
-  const float dsilu = __fmul_rn(s, __fmaf_rn(h, __fsub_rn(1.0f, s), 1.0f));
-  dh = __fmul_rn(__fmul_rn(da, u), dsilu);
-  du = __fmul_rn(da, __fmul_rn(h, s));
 }
 
 __global__ void __launch_bounds__(512)
@@ -206,37 +188,14 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ AdamW --
-__device__ __forceinline__ void adamw4(float4 &pv, float4 &mv, float4 &vv, const float4 gv,
-                                       float lr, float b1, float b2, float omb1, float omb2,
-                                       float eps, float decay, float bc1, float bc2) {
-  float *pp = &pv.x, *mm = &mv.x, *vvp = &vv.x;
-  const float *gg = &gv.x;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    pp[j] = pp[j] * decay;
-    mm[j] = b1 * mm[j] + omb1 * gg[j];
-    vvp[j] = b2 * vvp[j] + omb2 * gg[j] * gg[j];
-    const float mhat = mm[j] / bc1;
-    const float vhat = vvp[j] / bc2;
-    pp[j] = pp[j] - lr * mhat / (sqrtf(vhat) + eps);
-  }
-}
-
-__device__ __forceinline__ uint2 f32x4_to_bf16(const float4 pv) {
-  __nv_bfloat162 lo = __floats2bfloat162_rn(pv.x, pv.y), hi = __floats2bfloat162_rn(pv.z, pv.w);
-  return make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
-}
-
 __global__ void __launch_bounds__(512)
     adamw_kernel(float4 *__restrict__ p, const float4 *__restrict__ g, float4 *__restrict__ m,
-                 float4 *__restrict__ v, uint2 *__restrict__ pb, int64_t nvec, float lr,
-                 float b1, float b2, float omb1, float omb2, float eps, float decay, float bc1,
-                 float bc2) {
+                 float4 *__restrict__ v, uint2 *__restrict__ pb, int64_t nvec, AdamwHp hp) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
     float4 pv = p[i], mv = m[i], vv = v[i];
     const float4 gv = __ldcs(g + i);
-    adamw4(pv, mv, vv, gv, lr, b1, b2, omb1, omb2, eps, decay, bc1, bc2);
+    adamw4(pv, mv, vv, gv, hp);
     p[i] = pv;
     m[i] = mv;
     v[i] = vv;
@@ -253,12 +212,14 @@ __global__ void adamw_advance_step_kernel(int64_t *step) { *step += 1; }
 __global__ void __launch_bounds__(512) adamw_multi_kernel(const __grid_constant__ AdamwMulti a) {
   __shared__ float bc[2];
   if (threadIdx.x == 0) {
-    const double t = (double)*a.step;
-    bc[0] = (float)(1.0 - pow(a.b1d, t));
-    bc[1] = (float)(1.0 - pow(a.b2d, t));
+    const int64_t t = *a.step;
+    bc[0] = bias_correction(a.b1d, t);
+    bc[1] = bias_correction(a.b2d, t);
   }
   __syncthreads();
-  const float bc1 = bc[0], bc2 = bc[1];
+  AdamwHp hp = a.hp;
+  hp.bc1 = bc[0];
+  hp.bc2 = bc[1];
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int k = 0; k < a.count; ++k) {
     float4 *__restrict__ p = reinterpret_cast<float4 *>(a.p[k]);
@@ -270,7 +231,7 @@ __global__ void __launch_bounds__(512) adamw_multi_kernel(const __grid_constant_
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
       float4 pv = p[i], mv = m[i], vv = v[i];
       const float4 gv = __ldcs(g + i);
-      adamw4(pv, mv, vv, gv, a.lr, a.b1, a.b2, a.omb1, a.omb2, a.eps, a.decay, bc1, bc2);
+      adamw4(pv, mv, vv, gv, hp);
       p[i] = pv;
       m[i] = mv;
       v[i] = vv;
@@ -355,31 +316,37 @@ cudaError_t launch_swiglu_bwd_quant(const void *da, const void *h, const void *u
   return cudaGetLastError();
 }
 
+AdamwHp adamw_hp(double lr, double b1, double b2, double eps, double wd) {
+  // 1 - beta and the decay factor are formed in double: in fp32, 1 - 0.999f
+  // is off by 1.3e-5 relative
+  AdamwHp h{};
+  h.lr = (float)lr;
+  h.b1 = (float)b1;
+  h.b2 = (float)b2;
+  h.omb1 = (float)(1.0 - b1);
+  h.omb2 = (float)(1.0 - b2);
+  h.eps = (float)eps;
+  h.decay = (float)(1.0 - lr * wd);
+  return h;
+}
+
 cudaError_t launch_adamw(float *p, const float *g, float *m, float *v, void *pb, int64_t n,
                          int64_t step, double lr, double b1, double b2, double eps, double wd, int sms,
                          cudaStream_t st) {
   const int64_t nvec = n / 4;
-  // 1 - beta and the bias corrections are formed in double on the host: in
-  // fp32, 1 - 0.999f is off by 1.3e-5 relative
-  const float bc1 = (float)(1.0 - pow(b1, (double)step));
-  const float bc2 = (float)(1.0 - pow(b2, (double)step));
-  const float omb1 = (float)(1.0 - b1), omb2 = (float)(1.0 - b2);
+  AdamwHp hp = adamw_hp(lr, b1, b2, eps, wd);
+  hp.bc1 = (float)(1.0 - pow(b1, (double)step));
+  hp.bc2 = (float)(1.0 - pow(b2, (double)step));
   adamw_kernel<<<blocks_for(nvec, 512, 4, sms), 512, 0, st>>>(
       reinterpret_cast<float4 *>(p), reinterpret_cast<const float4 *>(g),
       reinterpret_cast<float4 *>(m), reinterpret_cast<float4 *>(v), static_cast<uint2 *>(pb), nvec,
-      (float)lr, (float)b1, (float)b2, omb1, omb2, (float)eps, (float)(1.0 - lr * wd), bc1, bc2);
+      hp);
   return cudaGetLastError();
 }
 
 cudaError_t launch_adamw_multi(AdamwMulti a, double lr, double b1, double b2, double eps,
                                double wd, int sms, cudaStream_t st) {
-  a.lr = (float)lr;
-  a.b1 = (float)b1;
-  a.b2 = (float)b2;
-  a.omb1 = (float)(1.0 - b1);
-  a.omb2 = (float)(1.0 - b2);
-  a.eps = (float)eps;
-  a.decay = (float)(1.0 - lr * wd);
+  a.hp = adamw_hp(lr, b1, b2, eps, wd);
   a.b1d = b1;
   a.b2d = b2;
   int64_t most = 0;

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "elementwise.cuh"
+
 namespace fp8k {
 
 cudaError_t launch_swiglu_fwd(const void *h, const void *u, void *a, int64_t n, int sms,
@@ -35,9 +37,11 @@ struct AdamwMulti {
   int64_t n[kMaxAdamw];
   int count;
   int64_t *step;        // device: incremented, then read as t
-  float lr, b1, b2, omb1, omb2, eps, decay;  // set by the launcher
+  AdamwHp hp;           // set by the launcher (bias corrections: in the kernel)
   double b1d, b2d;
 };
+// The fp32 hyperparameters of an AdamW update (1 - beta, decay in double).
+AdamwHp adamw_hp(double lr, double b1, double b2, double eps, double wd);
 cudaError_t launch_adamw_multi(AdamwMulti a, double lr, double b1, double b2, double eps,
                                double wd, int sms, cudaStream_t st);
 

@@ -28,10 +28,15 @@ da and dW2; dx's first term, dW1 and dW3).
 
 Delayed scaling fixes every scale before its tensor exists, so the SwiGLU
 passes quantize what they produce: a, dh and du reach memory only as FP8
-codes (fp8_swiglu_forward_quantize / _backward_quantize give the same codes
-and amaxes as the bf16 tensors quantized afterwards would).  The optimizer
-keeps its step count on the device (fp8_adamw_multi), so `step` issues the
-same calls every time and can be captured as a CUDA graph and replayed.
+codes (the same codes and amaxes as the bf16 tensors quantized afterwards
+would give).  By default the element-wise work also moves into the GEMM
+epilogues (fp8_gemm_tensor_grouped's epilogue variants): h and u come out of
+one gated launch whose epilogue also writes a's codes, and the three
+weight-gradient GEMMs apply AdamW to their tiles instead of storing dW.  The
+optimizer keeps its step count on the device, so `step` issues the same
+calls every time and can be captured as a CUDA graph and replayed.
+``fuse_forward=False`` / ``fuse_optimizer=False`` select the standalone passes
+(the latter stores dW in ``self.dw`` and runs fp8_adamw_multi).
 
 Buffers are allocated once (device memory through torch); `step` issues the
 calls on the current stream.
@@ -52,10 +57,12 @@ class SwiGLUTrainer:
     def __init__(self, w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, tokens: int,
                  lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
                  history: int = HISTORY, weight_scaling: str = "delayed",
-                 rescale_interval: int = 500):
+                 rescale_interval: int = 500, fuse_forward: bool = True,
+                 fuse_optimizer: bool = True):
         if weight_scaling not in ("delayed", "auto"):
             raise ValueError(weight_scaling)
         self.weight_scaling = weight_scaling
+        self.fuse_forward, self.fuse_optimizer = fuse_forward, fuse_optimizer
         self.rescale_interval = rescale_interval
         dev = w1.device
         ffn, d = w1.shape
@@ -87,13 +94,25 @@ class SwiGLUTrainer:
         self.y = torch.empty((T, d), **bf)
         self.da = torch.empty((T, ffn), **bf)
         self.dx = torch.empty((T, d), **f32)
-        self.dw = [torch.empty((ffn, d), **f32), torch.empty((ffn, d), **f32),
-                   torch.empty((d, ffn), **f32)]
         self.flops_per_step = 9 * 2.0 * T * d * ffn
         # optimizer step count on the device (advanced by fp8_adamw_multi)
         self.step_dev = torch.zeros(1, dtype=torch.int64, device=dev)
-        self.adamw_items = [F.adamw_item(self.w_master[i], self.dw[i], self.m[i], self.v[i],
-                                         self.w_bf[i]) for i in range(3)]
+        if fuse_optimizer:
+            # the weight-gradient GEMMs update the weights in their epilogues
+            self.dw = [None, None, None]
+            self.adamw_ep = [F.adamw_epilogue(self.w_master[i], self.m[i], self.v[i],
+                                              self.w_bf[i], self.step_dev, **self.hp)
+                             for i in range(3)]
+        else:
+            self.dw = [torch.empty((ffn, d), **f32), torch.empty((ffn, d), **f32),
+                       torch.empty((d, ffn), **f32)]
+            self.adamw_ep = [None, None, None]
+            self.adamw_items = [F.adamw_item(self.w_master[i], self.dw[i], self.m[i], self.v[i],
+                                             self.w_bf[i]) for i in range(3)]
+        # gated forward: h | u in one launch whose epilogue also quantizes a
+        self.swiglu_ep = (F.swiglu_epilogue(self.w3q, self.scale[K3:K3 + 1], self.u, self.aq,
+                                            F.E4M3, self.scale[A2:A2 + 1],
+                                            self.amax[A2:A2 + 1]) if fuse_forward else None)
         # automatic weight scaling: amax at the last max-reduction, steps since
         self.w_amax0 = torch.zeros(3, **f32)
         self.t_since = 0
@@ -113,7 +132,8 @@ class SwiGLUTrainer:
         return self.amax[i:i + 1]
 
     def forward_backward(self, x: torch.Tensor, dy: torch.Tensor):
-        """The nine GEMMs with their quantize and SwiGLU passes (no optimizer)."""
+        """The nine GEMMs with their quantize and SwiGLU passes; with the fused
+        optimizer also the AdamW updates (in the weight-gradient GEMMs)."""
         E4, E5, MN = F.E4M3, F.E5M2, F.MN_MAJOR
         q, P, run = F.fp8_quantize_tensor, F.gemm_problem, F.fp8_gemm_tensor_grouped
         w1, w3, w2 = self.w_bf
@@ -130,30 +150,39 @@ class SwiGLUTrainer:
         q(w1, E4, self.w1q, scale=sc(K1), amax_out=wam[0])
         q(w3, E4, self.w3q, scale=sc(K3), amax_out=wam[1])
         q(w2, E4, self.w2q, scale=sc(K2), amax_out=wam[2])
-        run([P(self.xq, E4, self.w1q, E4, sc(X1), sc(K1), self.h),          # h = x W1^T
-             P(self.xq, E4, self.w3q, E4, sc(X1), sc(K3), self.u)])         # u = x W3^T
-        F.fp8_swiglu_forward_quantize(self.h, self.u, E4, sc(A2), self.aq,   # a = silu(h) u
-                                      self._am(A2))
+        if self.fuse_forward:
+            run([P(self.xq, E4, self.w1q, E4, sc(X1), sc(K1), self.h,       # h, u = x W1^T, x W3^T
+                   swiglu=self.swiglu_ep)])                                 # a = silu(h) u
+        else:
+            run([P(self.xq, E4, self.w1q, E4, sc(X1), sc(K1), self.h),      # h = x W1^T
+                 P(self.xq, E4, self.w3q, E4, sc(X1), sc(K3), self.u)])     # u = x W3^T
+            F.fp8_swiglu_forward_quantize(self.h, self.u, E4, sc(A2), self.aq,  # a = silu(h) u
+                                          self._am(A2))
         run([P(self.aq, E4, self.w2q, E4, sc(A2), sc(K2), self.y)])         # y = a W2^T
         # backward
+        if self.fuse_optimizer:
+            F.fp8_adamw_multi([], self.step_dev, **self.hp)  # t of this step's updates
+        ep = self.adamw_ep
         q(dy, E5, self.dyq, scale=sc(G2), amax_out=self._am(G2))
         run([P(self.dyq, E5, self.w2q, E4, sc(G2), sc(K2), self.da, b_layout=MN),   # da = dy W2
              P(self.dyq, E5, self.aq, E4, sc(G2), sc(A2), self.dw[2],               # dW2 = dy^T a
-               a_layout=MN, b_layout=MN)])
+               a_layout=MN, b_layout=MN, adamw=ep[2])])
         F.fp8_swiglu_backward_quantize(self.da, self.h, self.u, E5, sc(G1), sc(G3),  # dh, du
                                        self.dhq, self.duq, self._am(G1), self._am(G3))
         run([P(self.dhq, E5, self.w1q, E4, sc(G1), sc(K1), self.dx, b_layout=MN),   # dx = dh W1
              P(self.dhq, E5, self.xq, E4, sc(G1), sc(X1), self.dw[0],               # dW1 = dh^T x
-               a_layout=MN, b_layout=MN),
+               a_layout=MN, b_layout=MN, adamw=ep[0]),
              P(self.duq, E5, self.xq, E4, sc(G3), sc(X1), self.dw[1],               # dW3 = du^T x
-               a_layout=MN, b_layout=MN)])
+               a_layout=MN, b_layout=MN, adamw=ep[1])])
         run([P(self.duq, E5, self.w3q, E4, sc(G3), sc(K3), self.dx, b_layout=MN,    # dx += du W3
                accumulate=True)])
 
     def optimizer_and_state(self):
-        """AdamW on the three weights, then the nine amax-history pushes."""
+        """AdamW on the three weights (unless the weight-gradient GEMMs did it),
+        then the nine amax-history pushes."""
         self.t += 1
-        F.fp8_adamw_multi(self.adamw_items, self.step_dev, **self.hp)
+        if not self.fuse_optimizer:
+            F.fp8_adamw_multi(self.adamw_items, self.step_dev, **self.hp)
         auto = self.weight_scaling == "auto"
         if auto:
             self.t_since += 1

@@ -292,7 +292,49 @@ FP8_API int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, 
  *             a multiple of 16; K % 16 == 0 is needed only while an operand
  *             is K-major.  FP8_ERR_MISALIGNED otherwise.
  *   No output may overlap another problem's output or inputs.
+ *   A group with an epilogue variant (adamw or swiglu) runs as one CTA-pair
+ *   launch whatever the shapes (ragged tiles are masked; no split K, even for
+ *   small M) and holds at most 4 problems (FP8_ERR_UNSUPPORTED otherwise).
  */
+/* Epilogue variants of a grouped per-tensor problem (fp8_gemm_tensor_grouped;
+ * CTA-pair path only).  Both fold element-wise work of the FP8 training step
+ * into the GEMM's epilogue, which reads the accumulator from tensor memory
+ * instead of a stored result from HBM.  Not described on the pages (the
+ * SwiGLU MLP and AdamW around the FP8 GEMMs are support arithmetic); the
+ * values are exactly those of the standalone calls named below. */
+
+/* AdamW epilogue: the problem's fp32 result G = sa*sb*A*B^T is the gradient of
+ * the parameters p [M, N] (row pitch ldc) and is NOT stored (c may be null);
+ * instead each element is updated as fp8_adamw_multi would update it with
+ * gradient G at step t = step[0] (device int64, read only; advance it first,
+ * e.g. fp8_adamw_multi with count 0).  p, m, v fp32 16-byte aligned, p_bf16
+ * (nullable) bf16 8-byte aligned, ldc % 4 == 0.  The problem must have
+ * out_dt FP8_OUT_F32, accumulate 0 and no bias. */
+typedef struct {
+  float *p, *m, *v;
+  void *p_bf16;
+  const int64_t *step;
+  double lr, beta1, beta2, eps, weight_decay;
+} fp8_adamw_epilogue_t;
+
+/* Gated SwiGLU epilogue (h = A B^T, u = A B_up^T, a = silu(h) * u): the pair
+ * computes h and u for the same output columns (B = W1 codes, b_up = W3 codes
+ * in the same layout and format, scale sb_up) and writes c <- bf16(h) (the
+ * problem's output, FP8_OUT_BF16), u <- bf16(u), q <- codes of
+ * a = bf16(silu(h) u) divided by scale[0] (format fmt), amax[0] <- max |a|
+ * (cleared by the call) -- what fp8_swiglu_forward_quantize gives for the
+ * stored h and u.  c, u, q [M, N] with row pitch ldc (elements; q in bytes),
+ * 16-byte aligned, ldc % 16 == 0, N % 32 == 0; no bias, no accumulate. */
+typedef struct {
+  const uint8_t *b_up;
+  const float *sb_up;
+  void *u;
+  uint8_t *q;
+  int fmt;
+  const float *scale;
+  float *amax;
+} fp8_swiglu_epilogue_t;
+
 typedef struct {
   const uint8_t *a; /* codes of format fa: [M, K] (K-major) or [K, M] (MN-major) */
   const uint8_t *b; /* codes of format fb: [N, K] (K-major) or [K, N] (MN-major) */
@@ -309,6 +351,8 @@ typedef struct {
   const float *bias; /* nullable device fp32 [N]: C = result + bias[n] ([Nano]
                         "实现": the linear's bias; added in fp32 before the
                         output cast; with accumulate, C += result + bias) */
+  const fp8_adamw_epilogue_t *adamw;   /* nullable HOST pointer (read during the call) */
+  const fp8_swiglu_epilogue_t *swiglu; /* nullable HOST pointer (read during the call) */
 } fp8_gemm_problem_t;
 
 FP8_API int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count,
@@ -493,12 +537,14 @@ FP8_API int fp8_swiglu_backward_quantize(const void *da, const void *h, const vo
                                          uint8_t *q_dh, uint8_t *q_du, float *amax_dh,
                                          float *amax_du, fp8_stream_t stream);
 
-/* fp8_adamw_multi: one AdamW step (as fp8_adamw_step) over `count` (1..8)
+/* fp8_adamw_multi: one AdamW step (as fp8_adamw_step) over `count` (0..8)
  * parameter tensors in one launch, with the step number kept on the device:
  * the call first increments *step (device int64, 8-byte aligned) and the
  * update uses the incremented value as t (bias corrections 1 - beta^t formed
  * in double on the device).  A captured training step therefore advances t
- * on every replay.  Start *step at 0 for a fresh optimizer.
+ * on every replay.  Start *step at 0 for a fresh optimizer.  count == 0 only
+ * advances the counter (items may be null): for updates done by GEMM
+ * epilogues (fp8_adamw_epilogue_t), which read t without advancing it.
  *   items  HOST array of `count` descriptors (read during the call only);
  *          per item p, g, m, v fp32 [n] and p_bf16 (nullable) bf16 [n], all
  *          device, 16-byte aligned (p_bf16 8-byte), n % 4 == 0; empty items

@@ -3,12 +3,14 @@ benchmark times.
 
 * FP8 SwiGLU training step with delayed scaling, d 4096, ffn 14336, 16384
   tokens (Flax guide 2.3 delayed scaling, 3.3 E4M3 forward / E5M2
-  gradients): two steps of the trainer, the second checked teacher-forced --
+  gradients): two steps of the trainer (weight gradients stored, standalone
+  AdamW), the second checked teacher-forced --
   every scale used and every amax-history entry exactly, the codes of every
   quantized tensor bit-exact on sampled rows (the amaxes over the whole
   tensors), the nine GEMMs within the GEMM bound on 4096 sampled outputs each
   plus tile corners, SwiGLU within one bf16 ulp on sampled rows, AdamW on
-  sampled weights.
+  sampled weights.  Then the default trainer (gated SwiGLU epilogue, AdamW
+  in the weight-gradient GEMMs) against that path, bit for bit.
 * MOSS two-level microscaling GEMM, M = N = K = 8192 (MOSS blog, section 4,
   steps 1-4) on the two-level workload's own inputs (8 outlier K columns x100
   in A): amax and global factor bit-exact, codes and local factors bit-exact
@@ -61,7 +63,9 @@ def test_swiglu_training_step_full_size():
     x, w1, w3, w2 = workloads.swiglu(device=dev)
     T, d = x.shape
     ffn = w1.shape[0]
-    tr = SwiGLUTrainer(w1, w3, w2, tokens=T)
+    # dW stored, so that the weight-gradient GEMMs are checked on their own
+    # (the AdamW epilogue is checked against this path bit for bit below)
+    tr = SwiGLUTrainer(w1, w3, w2, tokens=T, fuse_optimizer=False)
     del w1, w3, w2
     fmt = {i: ("e5m2" if i in (G1, G3, G2) else "e4m3") for i in range(9)}
     states = [OD.DelayedState.initial(1024) for _ in range(9)]
@@ -186,6 +190,32 @@ def test_swiglu_training_step_full_size():
             new_scale = OD.compute_scale(np.max(states[i].history), states[i].scale, fmt[i])
             assert np.float32(tr.scale[i].item()) == new_scale, i
     rc, where = F.fp8_get_last_device_error()
+    assert rc == 0, (rc, where)
+
+
+def test_fused_training_step_full_size_matches_standalone_passes():
+    """At full size, two steps of the default trainer (gated SwiGLU epilogue,
+    AdamW in the weight-gradient GEMMs) give the bits of the standalone
+    passes (checked against the oracle in the test above)."""
+    lib()
+    from fp8_quantized_gemm_gb300.mlp import SwiGLUTrainer
+    dev = torch.device("cuda")
+    x, w1, w3, w2 = workloads.swiglu(device=dev)
+    T = x.shape[0]
+    fused = SwiGLUTrainer(w1, w3, w2, tokens=T)
+    plain = SwiGLUTrainer(w1, w3, w2, tokens=T, fuse_forward=False, fuse_optimizer=False)
+    del w1, w3, w2
+    for t in range(2):
+        dy = workloads.swiglu_grad(t, device=dev)
+        for tr in (fused, plain):
+            tr.step(x, dy)
+        torch.cuda.synchronize()
+        for name in ("h", "u", "aq", "dhq", "duq", "amax", "scale", "hist"):
+            assert torch.equal(getattr(fused, name), getattr(plain, name)), (t, name)
+        for name in ("w_master", "m", "v", "w_bf"):
+            for i in range(3):
+                assert torch.equal(getattr(fused, name)[i], getattr(plain, name)[i]), (t, name, i)
+    rc, where = lib().fp8_get_last_device_error()
     assert rc == 0, (rc, where)
 
 

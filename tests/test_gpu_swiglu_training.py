@@ -50,12 +50,17 @@ def swiglu_bf16(tr):
     return a, dh, du
 
 
-def test_swiglu_training_teacher_forced():
+@pytest.mark.parametrize("fuse_forward", [True, False])
+def test_swiglu_training_teacher_forced(fuse_forward):
+    """The weight gradients are stored (fuse_optimizer=False) so that the
+    three dW GEMMs and the standalone AdamW are checked on their own; the
+    forward runs as the gated epilogue or as the standalone fused pass."""
     lib()
     from fp8_quantized_gemm_gb300.mlp import (A2, G1, G2, G3, K1, K2, K3, X1, X3,
                                               SwiGLUTrainer)
     x, w1, w3, w2 = workloads.swiglu(d=D, ffn=FFN, tokens=T)
-    tr = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T)
+    tr = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T, fuse_forward=fuse_forward,
+                       fuse_optimizer=False)
     xd = x.cuda()
     xf = f32(x)
     st = [OD.DelayedState.initial(1024) for _ in range(9)]
@@ -256,3 +261,30 @@ def test_swiglu_training_16_steps_free_running():
         assert rel(upd_gpu, upd_ref) <= 1e-2, i
     assert rel(f32(tr.y), ref_y) <= 1e-2
     assert rel(f32(tr.dx), ref_dx) <= 1e-2
+
+
+def test_fused_epilogues_match_standalone_passes():
+    """The gated SwiGLU epilogue and the AdamW epilogues (the default trainer)
+    give the same bits as the standalone passes (fp8_swiglu_forward_quantize,
+    stored dW + fp8_adamw_multi) over several steps: h, u, a's codes, every
+    amax and scale, the weights, moments and bf16 copies."""
+    lib()
+    from fp8_quantized_gemm_gb300.mlp import SwiGLUTrainer
+    x, w1, w3, w2 = workloads.swiglu(d=D, ffn=FFN, tokens=T)
+    fused = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T)
+    plain = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T, fuse_forward=False,
+                          fuse_optimizer=False)
+    xd = x.cuda()
+    for t in range(4):
+        dy = workloads.swiglu_grad(t, tokens=T, d=D).cuda()
+        for tr in (fused, plain):
+            tr.step(xd, dy)
+        torch.cuda.synchronize()
+        for name in ("h", "u", "aq", "y", "da", "dhq", "duq", "dx", "amax", "scale", "hist"):
+            assert torch.equal(getattr(fused, name), getattr(plain, name)), (t, name)
+        for name in ("w_master", "m", "v", "w_bf"):
+            for i in range(3):
+                assert torch.equal(getattr(fused, name)[i], getattr(plain, name)[i]), (t, name, i)
+        assert int(fused.step_dev.item()) == int(plain.step_dev.item()) == t + 1
+    rc, where = lib().fp8_get_last_device_error()
+    assert rc == 0, (rc, where)
