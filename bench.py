@@ -287,12 +287,11 @@ class SwiGLUStep:
 
     name = "swiglu_training_delayed_d4096_ffn14336_t16384"
     # kernels each step launches: quantize x, W1, W3, W2, dy (5); GEMMs: the
-    # gated h|u launch (its epilogue writes a's codes), y, da|dW2 and
-    # dx|dW1|dW3 (the dW tiles update the weights with AdamW in the epilogue)
+    # gated h|u launch (its epilogue writes a's codes), y, da|dW2, dx|dW1|dW3
     # and the accumulating dx += du W3 (5); the fused SwiGLU-backward +
-    # quantize pass (1); the optimizer's step advance (1); nine amax-history
+    # quantize pass (1); AdamW (step advance + update: 2); nine amax-history
     # updates (9).  The amax clears are memsets, not kernels.
-    kernels_per_step = 21
+    kernels_per_step = 22
     CALL_LABELS = {"fp8_gemm_tensor_grouped": "gemm", "fp8_quantize_tensor": "quantize",
                    "fp8_swiglu_forward_quantize": "swiglu_quantize",
                    "fp8_swiglu_backward_quantize": "swiglu_quantize",
@@ -486,7 +485,8 @@ def run_headline(args, dev, peaks):
         "roofline": dict(roofline_entry(
             "tensor", gemm_tflops, fp8_peak, "TFLOP/s", recorded_traffic("gemm_pair_swiglu_step"),
             "dense FP8 = 2 x measured bf16 burst (%s): each GEMM call timed alone" % src),
-            kernel="fp8k::gemm_pair_kernel (the 5 GEMM launches of a step, epilogues included)",
+            kernel="fp8k::gemm_pair_kernel (the 5 GEMM launches of a step; the gated "
+                   "h|u launch includes the SwiGLU forward in its epilogue)",
             units="17.32 TFLOP of GEMMs per step over the GEMM launches' summed device time",
             frac_of_sustained_peak=round(gemm_tflops / fp8_peak_sus, 4),
             sustained_peak=round(fp8_peak_sus, 1)),
@@ -499,11 +499,13 @@ def run_headline(args, dev, peaks):
         "passes_gbs": {
             "quantize": round(qbytes / (per["quantize"] / 1e3) / 1e9, 1),
             "swiglu_quantize": round(sbytes / (per["swiglu_quantize"] / 1e3) / 1e9, 1),
+            "adamw": round(30.0 * 3 * ffn * d / (per["adamw"] / 1e3) / 1e9, 1),
             "hbm_peak": peaks["hbm_gbs"],
             "note": "algorithmic bytes of the standalone passes: quantize x, dy, W1, W3, W2 "
                     "(2 B read, 1 B codes); the SwiGLU backward reads da, h, u and writes the "
-                    "codes of dh and du.  The SwiGLU forward (gated h|u launch) and AdamW (the "
-                    "dW GEMMs) run in GEMM epilogues and are inside 'gemm'"},
+                    "codes of dh and du; AdamW 30 B per weight (p, m, v read and written, dW "
+                    "read, bf16 copy written).  The SwiGLU forward runs in the gated h|u "
+                    "GEMM's epilogue and is inside 'gemm'"},
         "clocks": clk.summary(),
         "gpu_launches": wl.kernels_per_step * args.steps,
     }
@@ -814,6 +816,50 @@ class GroupGemm:
                 "ms": {kk: round(v, 4) for kk, v in per.items()}}
 
 
+class GroupGemm32(GroupGemm):
+    """The fine-grained GEMM with (32, 32) weight blocks and 1 x 32 activation
+    groups, FP32 scales (Transformers fine-grained FP8, 八 and 四): activation
+    quantization timed, weights offline, K 7168, N 2048."""
+
+    def __init__(self, dev, m, k=7168, n=2048):
+        import fp8_quantized_gemm_gb300 as F
+        self.name = "group32_f32_m%d" % m
+        self.sfmt_name = "f32"
+        self.m, self.k, self.n, self.F = m, k, n, F
+        act, w = workloads.fine_grained(m, k=k, n=n)
+        self.act_host, self.w_host = act, w
+        self.wq = torch.empty((n, k), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(((n + 31) // 32, k // 32), dtype=torch.float32, device=dev)
+        F.fp8_quantize_block32_f32(w.to(dev), F.E4M3, self.wq, self.ws)  # offline
+        self.ad = act.to(dev)
+        self.aq = torch.empty((m, k), dtype=torch.uint8, device=dev)
+        self.asc = torch.empty((k // 32, m), dtype=torch.float32, device=dev)
+        self.y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+
+    def launches(self):
+        F = self.F
+        return [("quantize", lambda: F.fp8_quantize_token_group32(self.ad, F.E4M3, F.SCALE_F32,
+                                                                  self.aq, self.asc)),
+                ("gemm", lambda: F.fp8_gemm_group32(self.aq, self.asc, self.wq, self.ws, self.y))]
+
+    def oracle_sample(self, rows=256):
+        from oracle import gemm as OG
+        from oracle import quantize as OQ
+        r = min(self.m, rows)
+        if "b32" not in GroupGemm._w_oracle:
+            qb, sb = OQ.quantize_block(self.w_host.float().numpy(), "e4m3", "f32", block=32)
+            GroupGemm._w_oracle["b32"] = OG.dequant_operand(
+                qb, "e4m3", OQ.expand(np.asarray(sb, np.float64), self.n, self.k, 32, 32))
+        wdq = GroupGemm._w_oracle["b32"]
+        act = self.act_host[:r].float().numpy()
+        t0 = time.perf_counter()
+        qa, sa = OQ.quantize_token_group(act, "e4m3", "f32", group=32)
+        a = OG.dequant_operand(qa, "e4m3", OQ.expand(np.asarray(sa, np.float64), r, self.k, 1, 32))
+        OG.gemm(a, wdq)
+        dt = time.perf_counter() - t0
+        return 2.0 * r * self.n * self.k, dt, "%d of %d activation rows" % (r, self.m)
+
+
 class MoeExperts:
     """Mixture-of-experts layer, 8 experts, 4096 routed tokens (uneven
     counts), N 2048, K 7168: token-group quantization of the activations
@@ -1005,6 +1051,14 @@ def run_extras(dev, flush, stream, peaks, args):
                 row["cpu_baseline"] = cpu_baseline(wl.oracle_sample, args.cpu_seconds / 2)
             out[wl.name] = row
             del wl
+    for m in (128, 4096):
+        wl = GroupGemm32(dev, m)
+        per, step = time_launches(wl.launches(), 10, flush, stream)
+        row = wl.report(per, step, fp8_peak, hbm)
+        if not args.no_cpu_baseline:
+            row["cpu_baseline"] = cpu_baseline(wl.oracle_sample, args.cpu_seconds / 2)
+        out[wl.name] = row
+        del wl
     wl = TwoLevel(dev)
     per, step = time_launches(wl.launches(), 10, flush, stream)
     row = wl.report(per, step, fp8_peak, hbm)
@@ -1095,6 +1149,7 @@ PROFILE_WORKLOADS = {
     **{"group_%s_m%d" % (s_, m): (lambda dev, s_=s_, m=m: GroupGemm(dev, m, s_))
        for s_ in ("f32", "ue8m0") for m in (1, 128, 4096)},
     **{"moe_%s" % s_: (lambda dev, s_=s_: MoeExperts(dev, s_)) for s_ in ("f32", "ue8m0")},
+    **{"group32_f32_m%d" % m: (lambda dev, m=m: GroupGemm32(dev, m)) for m in (128, 4096)},
 }
 
 

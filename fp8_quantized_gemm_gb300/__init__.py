@@ -64,6 +64,9 @@ _SIGS = {
     "fp8_swiglu_backward_quantize": [_vp, _vp, _vp, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp,
                                      _vp],
     "fp8_adamw_multi": [_vp, _int, _vp, _d, _d, _d, _d, _d, _vp],
+    "fp8_quantize_token_group32": [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp],
+    "fp8_quantize_block32_f32": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp],
+    "fp8_gemm_group32": [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_get_last_device_error": [ctypes.POINTER(ctypes.c_int), _vp],
     "fp8_set_option": [_int, _int],
 }
@@ -164,6 +167,28 @@ def fp8_quantize_mx1(x, fmt, global_out, q, local, stream=None):
 def fp8_quantize_block32(w, fmt, q, scales, local, stream=None):
     n, k = w.shape
     _call("fp8_quantize_block32", _p(w), _in_dt(w), n, k, fmt, _p(q), _p(scales), _p(local),
+          _stream(stream))
+
+
+def fp8_quantize_token_group32(x, fmt, sfmt, q, scales, stream=None):
+    """1x32 token groups; scales group-major [ceil(K/32), M]."""
+    m, k = x.shape
+    _call("fp8_quantize_token_group32", _p(x), _in_dt(x), m, k, fmt, sfmt, _p(q), _p(scales),
+          _stream(stream))
+
+
+def fp8_quantize_block32_f32(w, fmt, q, scales, stream=None):
+    """32x32 weight blocks with fp32 scales [ceil(N/32), K/32]."""
+    n, k = w.shape
+    _call("fp8_quantize_block32_f32", _p(w), _in_dt(w), n, k, fmt, _p(q), _p(scales),
+          _stream(stream))
+
+
+def fp8_gemm_group32(a, sa, b, sb, out, stream=None):
+    """Per-K-group GEMM with fp32 scales of 1x32 groups and 32x32 blocks."""
+    m, k = a.shape
+    n = b.shape[0]
+    _call("fp8_gemm_group32", _p(a), _p(sa), _p(b), _p(sb), m, n, k, _p(out), out.stride(0),
           _stream(stream))
 
 

@@ -6,6 +6,7 @@
 // shared object loads on a machine without a GPU driver (only the calls need
 // a device).
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <map>
 #include <tuple>
@@ -19,6 +20,16 @@
 namespace {
 
 using fp8k::GemmArgs;
+
+// An NVTX range named after the entry point around each call, so that a
+// timeline shows which library call enqueued which kernels (NVTX v3 is
+// header-only: without a profiler attached the range is a no-op).
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Device error word: [0] first error code (positive), [1] where.
 __device__ uint32_t g_device_error[2];
@@ -236,7 +247,8 @@ int run_gemm(int mode, const uint8_t *a, const uint8_t *b, GemmArgs &args, cudaS
   // faster for 128-wide tiles (the FP32-promotion mode, and the block-scaled
   // modes at mid-size M), not for the 128 x 256 block-scaled tiles
   const int bn = fp8k::gemm_tile_n(mode, args.M, args.N, d->sms);
-  args.multicast = g_use_multicast && mode != fp8k::kScaleTensor && bn == 128 &&
+  args.multicast = g_use_multicast && mode != fp8k::kScaleTensor &&
+                           mode != fp8k::kScaleGroupF32x32 && bn == 128 &&
                            args.ksplit == 1 && !args.b_mn && args.experts == 0 && args.M > 128
                        ? 1
                        : 0;
@@ -339,6 +351,7 @@ int api_encode_operand(CUtensorMap *map, const void *base, int64_t k, int64_t ro
 extern "C" {
 
 int fp8_amax(const void *x, int in_dt, int64_t n, float *amax_out, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (amax_out == nullptr || n < 0 || !valid_in(in_dt) || (n > 0 && x == nullptr))
     return FP8_ERR_INVALID_ARG;
   if (n > 0 && !aligned16(x)) return FP8_ERR_MISALIGNED;
@@ -351,6 +364,7 @@ int fp8_amax(const void *x, int in_dt, int64_t n, float *amax_out, fp8_stream_t 
 int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, int fmt,
                         const float *amax_in, const float *scale, float *scale_out, uint8_t *q,
                         uint8_t *q_t, float *amax_out, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (x == nullptr || q == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
   if (amax_in == nullptr && scale == nullptr) return FP8_ERR_INVALID_ARG;
@@ -368,6 +382,7 @@ int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, in
 
 int fp8_quantize_tensors(const fp8_quant_item_t *items, int count, uint32_t *sync,
                          fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   static_assert(FP8_QUANT_SYNC_WORDS == 2 * fp8k::kMaxMulti, "sync scratch size");
   if (items == nullptr || count < 1 || count > fp8k::kMaxMulti) return FP8_ERR_INVALID_ARG;
   if (sync == nullptr) return FP8_ERR_INVALID_ARG;
@@ -419,6 +434,7 @@ int fp8_quantize_tensors(const fp8_quant_item_t *items, int count, uint32_t *syn
 
 int fp8_quantize_token_group(const void *x, int in_dt, int64_t M, int64_t K, int fmt, int sfmt,
                              uint8_t *q, void *scales, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (x == nullptr || q == nullptr || scales == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
   if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
@@ -433,6 +449,7 @@ int fp8_quantize_token_group(const void *x, int in_dt, int64_t M, int64_t K, int
 
 int fp8_quantize_block(const void *w, int in_dt, int64_t N, int64_t K, int fmt, int sfmt,
                        uint8_t *q, void *scales, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (w == nullptr || q == nullptr || scales == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
   if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
@@ -448,6 +465,7 @@ int fp8_quantize_block(const void *w, int in_dt, int64_t N, int64_t K, int fmt, 
 
 int fp8_quantize_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt, const float *amax,
                     float *global_out, uint8_t *q, uint32_t *local, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (x == nullptr || amax == nullptr || q == nullptr || local == nullptr || !valid_in(in_dt) ||
       !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
@@ -463,6 +481,7 @@ int fp8_quantize_mx(const void *x, int in_dt, int64_t R, int64_t K, int fmt, con
 
 int fp8_amax_rows(const void *x, int in_dt, int64_t R, int64_t K, float *amax_out,
                   fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (x == nullptr || amax_out == nullptr || !valid_in(in_dt)) return FP8_ERR_INVALID_ARG;
   if (R < 1 || K < 1 || R >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
   if (K % 8 != 0 || !aligned16(x)) return FP8_ERR_MISALIGNED;
@@ -475,6 +494,7 @@ int fp8_amax_rows(const void *x, int in_dt, int64_t R, int64_t K, float *amax_ou
 int fp8_quantize_mx_rows(const void *x, int in_dt, int64_t R, int64_t K, int fmt,
                          const float *amax_rows, float *global_out, uint8_t *q, uint32_t *local,
                          fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (x == nullptr || amax_rows == nullptr || global_out == nullptr || q == nullptr ||
       local == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
@@ -490,6 +510,7 @@ int fp8_quantize_mx_rows(const void *x, int in_dt, int64_t R, int64_t K, int fmt
 
 int fp8_quantize_mx1(const void *x, int in_dt, int64_t R, int64_t K, int fmt, float *global_out,
                      uint8_t *q, uint32_t *local, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (x == nullptr || q == nullptr || local == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
   if (R < 1 || K < 1 || R >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
@@ -505,6 +526,7 @@ int fp8_quantize_mx1(const void *x, int in_dt, int64_t R, int64_t K, int fmt, fl
 
 int fp8_quantize_block32(const void *w, int in_dt, int64_t N, int64_t K, int fmt, uint8_t *q,
                          uint8_t *scales, uint32_t *local, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (w == nullptr || q == nullptr || local == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
   if (N < 1 || K < 1 || N >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
@@ -517,8 +539,51 @@ int fp8_quantize_block32(const void *w, int in_dt, int64_t N, int64_t K, int fmt
                                               (cudaStream_t)stream));
 }
 
+int fp8_quantize_token_group32(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
+                               int sfmt, uint8_t *q, void *scales, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
+  if (x == nullptr || q == nullptr || scales == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
+  if (M < 1 || K < 1 || M >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || !aligned16(x) || !aligned16(q)) return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_quant_group32(x, in_dt, M, K, fmt, sfmt, q, scales, d->sms,
+                                              (cudaStream_t)stream));
+}
+
+int fp8_quantize_block32_f32(const void *w, int in_dt, int64_t N, int64_t K, int fmt, uint8_t *q,
+                             float *scales, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
+  if (w == nullptr || q == nullptr || scales == nullptr || !valid_in(in_dt) || !valid_fmt(fmt))
+    return FP8_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || N >= kMaxDim || K >= kMaxDim) return FP8_ERR_INVALID_ARG;
+  if (K % 32 != 0 || !aligned16(w) || !aligned16(q)) return FP8_ERR_MISALIGNED;
+  DeviceState *d = nullptr;
+  int rc = device_state(&d);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_quant_block32_f32(w, in_dt, N, K, fmt, q, scales, d->sms,
+                                                  (cudaStream_t)stream));
+}
+
+int fp8_gemm_group32(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb,
+                     int64_t M, int64_t N, int64_t K, void *c, int64_t ldc, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
+  int rc = check_gemm_common(a, b, M, N, K, 128);
+  if (rc != FP8_OK) return rc;
+  if (sa == nullptr || sb == nullptr) return FP8_ERR_INVALID_ARG;
+  if ((rc = check_output(c, N, ldc, FP8_OUT_BF16)) != FP8_OK) return rc;
+  GemmArgs args{};
+  args.M = M; args.N = N; args.K = K; args.fa = FP8_E4M3; args.fb = FP8_E4M3;
+  args.out_dt = FP8_OUT_BF16; args.ldc = ldc; args.c = c; args.sa = sa; args.sb = sb;
+  return run_gemm(fp8k::kScaleGroupF32x32, a, b, args, (cudaStream_t)stream);
+}
+
 int fp8_dequantize_block(const uint8_t *q, int fmt, const void *scales, int sfmt, int64_t N,
                          int64_t K, void *out, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (q == nullptr || scales == nullptr || out == nullptr || !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
   if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
@@ -535,6 +600,7 @@ int fp8_dequantize_block(const uint8_t *q, int fmt, const void *scales, int sfmt
 int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, const float *sa,
                     const float *sb, int64_t M, int64_t N, int64_t K, int out_dt, void *c,
                     int64_t ldc, int accumulate, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   fp8_gemm_problem_t p{};
   p.a = a; p.b = b; p.sa = sa; p.sb = sb; p.M = M; p.N = N; p.K = K; p.fa = fa; p.fb = fb;
   p.out_dt = out_dt; p.accumulate = accumulate; p.c = c; p.ldc = ldc;
@@ -545,6 +611,7 @@ int fp8_gemm_tensor(const uint8_t *a, int fa, const uint8_t *b, int fb, const fl
 }
 
 int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (problems == nullptr || count < 1 || count > 64) return FP8_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) {
     const int rc = check_tensor_problem(problems[i]);
@@ -645,12 +712,14 @@ int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int count, fp8_s
 
 int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb, int sfmt,
                    int64_t M, int64_t N, int64_t K, void *c, int64_t ldc, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   return fp8_gemm_group_bias(a, sa, b, sb, sfmt, M, N, K, nullptr, c, ldc, stream);
 }
 
 int fp8_gemm_group_bias(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
                         int sfmt, int64_t M, int64_t N, int64_t K, const float *bias, void *c,
                         int64_t ldc, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   int rc = check_gemm_common(a, b, M, N, K, 128);
   if (rc != FP8_OK) return rc;
   if (sa == nullptr || sb == nullptr) return FP8_ERR_INVALID_ARG;
@@ -699,6 +768,7 @@ int fp8_gemm_group_bias(const uint8_t *a, const void *sa, const uint8_t *b, cons
 int fp8_gemm_group_experts(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
                            int sfmt, const int32_t *offsets, int experts, int64_t M, int64_t N,
                            int64_t K, void *c, int64_t ldc, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   int rc = check_gemm_common(a, b, M, N, K, 128);
   if (rc != FP8_OK) return rc;
   if (sa == nullptr || sb == nullptr || offsets == nullptr) return FP8_ERR_INVALID_ARG;
@@ -750,6 +820,7 @@ int fp8_gemm_group_experts(const uint8_t *a, const void *sa, const uint8_t *b, c
 int fp8_gemm_mx(const uint8_t *a, const uint32_t *la, const float *ga, const uint8_t *b,
                 const uint32_t *lb, const float *gb, int64_t M, int64_t N, int64_t K, int out_dt,
                 void *c, int64_t ldc, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   int rc = check_gemm_common(a, b, M, N, K, 128);
   if (rc != FP8_OK) return rc;
   if (la == nullptr || lb == nullptr || ga == nullptr || gb == nullptr) return FP8_ERR_INVALID_ARG;
@@ -765,6 +836,7 @@ int fp8_gemm_mx(const uint8_t *a, const uint32_t *la, const float *ga, const uin
 int fp8_gemm_mx_rows(const uint8_t *a, const uint32_t *la, const float *ga, const uint8_t *b,
                      const uint32_t *lb, const float *gb, int64_t M, int64_t N, int64_t K,
                      int out_dt, void *c, int64_t ldc, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   int rc = check_gemm_common(a, b, M, N, K, 128);
   if (rc != FP8_OK) return rc;
   if (la == nullptr || lb == nullptr || ga == nullptr || gb == nullptr) return FP8_ERR_INVALID_ARG;
@@ -781,6 +853,7 @@ int fp8_gemm_mx_rows(const uint8_t *a, const uint32_t *la, const float *ga, cons
 
 int fp8_delayed_state_update(float *hist, float *scale, const float *amax_cur, int64_t L,
                              int fmt, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (hist == nullptr || scale == nullptr || amax_cur == nullptr || !valid_fmt(fmt))
     return FP8_ERR_INVALID_ARG;
   if (L < 1 || L > 32768) return FP8_ERR_INVALID_ARG;
@@ -792,6 +865,7 @@ int fp8_delayed_state_update(float *hist, float *scale, const float *amax_cur, i
 
 int fp8_auto_weight_scale(const float *amax0, int64_t t, double lr, int fmt, float *scale_out,
                           fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (amax0 == nullptr || scale_out == nullptr || t < 0 || !valid_fmt(fmt) || !(lr >= 0.0))
     return FP8_ERR_INVALID_ARG;
   DeviceState *d = nullptr;
@@ -802,6 +876,7 @@ int fp8_auto_weight_scale(const float *amax0, int64_t t, double lr, int fmt, flo
 }
 
 int fp8_swiglu_forward(const void *h, const void *u, void *a, int64_t n, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (n < 0 || (n > 0 && (h == nullptr || u == nullptr || a == nullptr)))
     return FP8_ERR_INVALID_ARG;
   if (n % 8 != 0 || !aligned16(h) || !aligned16(u) || !aligned16(a)) return FP8_ERR_MISALIGNED;
@@ -814,6 +889,7 @@ int fp8_swiglu_forward(const void *h, const void *u, void *a, int64_t n, fp8_str
 
 int fp8_swiglu_backward(const void *da, const void *h, const void *u, void *dh, void *du,
                         int64_t n, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (n < 0 || (n > 0 && (da == nullptr || h == nullptr || u == nullptr || dh == nullptr ||
                           du == nullptr)))
     return FP8_ERR_INVALID_ARG;
@@ -830,6 +906,7 @@ int fp8_swiglu_backward(const void *da, const void *h, const void *u, void *dh, 
 int fp8_swiglu_forward_quantize(const void *h, const void *u, int64_t n, int fmt,
                                 const float *scale, uint8_t *q, float *amax_out,
                                 fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (n < 0 || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
   // an empty tensor is read and written nowhere: its pointers may be null
   if (n > 0 && (h == nullptr || u == nullptr || scale == nullptr || q == nullptr))
@@ -847,6 +924,7 @@ int fp8_swiglu_backward_quantize(const void *da, const void *h, const void *u, i
                                  const float *scale_dh, const float *scale_du, uint8_t *q_dh,
                                  uint8_t *q_du, float *amax_dh, float *amax_du,
                                  fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (n < 0 || !valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
   if (n > 0 && (da == nullptr || h == nullptr || u == nullptr || scale_dh == nullptr ||
                 scale_du == nullptr || q_dh == nullptr || q_du == nullptr))
@@ -869,6 +947,7 @@ int fp8_swiglu_backward_quantize(const void *da, const void *h, const void *u, i
 int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, double lr,
                     double beta1, double beta2, double eps, double weight_decay,
                     fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (step == nullptr || count < 0 || count > fp8k::kMaxAdamw || (count > 0 && items == nullptr))
     return FP8_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(step) & 7u) != 0) return FP8_ERR_MISALIGNED;
@@ -902,6 +981,7 @@ int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, dou
 int fp8_adamw_step(float *p, const float *g, float *m, float *v, void *p_bf16, int64_t n,
                    int64_t step, double lr, double beta1, double beta2, double eps,
                    double weight_decay, fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (p == nullptr || g == nullptr || m == nullptr || v == nullptr || n < 0 || step < 1)
     return FP8_ERR_INVALID_ARG;
   if (n % 4 != 0 || !aligned16(p) || !aligned16(g) || !aligned16(m) || !aligned16(v) ||

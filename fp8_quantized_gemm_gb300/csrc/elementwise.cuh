@@ -10,9 +10,10 @@
 
 namespace fp8k {
 
-// logistic function 1 / (1 + e^-z), IEEE division
+// logistic function 1 / (1 + e^-z): the correctly rounded reciprocal (the
+// same value as the IEEE quotient 1 / x, with fewer instructions)
 __device__ __forceinline__ float sigmoidf_(float z) {
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
+  return __frcp_rn(__fadd_rn(1.0f, expf(-z)));
 }
 
 // a = silu(h) * u = (h * s(h)) * u

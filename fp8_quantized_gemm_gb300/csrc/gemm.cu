@@ -29,6 +29,11 @@
 //                                  the epilogue warps promote
 //                                  acc += sa[m,g] * sb[n/128,g] * partial
 //                                  while the tensor cores run the next slice.
+//   group FP32, (32, 32) blocks (Transformers 八: weight_block_size (32, 32),
+//                                  四: float scales) the same with every K=32
+//                                  MMA in its own buffer: a promotion per
+//                                  32-deep K step, with the scales of each
+//                                  32-column weight block.
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "kernels.h"
@@ -51,7 +56,9 @@ template <int MODE, int BN, int STAGES>
 struct Cfg {
   static constexpr int BM = 128, BK = 128;
   static constexpr bool kBlockScaled = (MODE == kScaleMx || MODE == kScaleGroupUe8m0);
-  static constexpr bool kPromote = (MODE == kScaleGroupF32);
+  static constexpr bool kPromote = (MODE == kScaleGroupF32 || MODE == kScaleGroupF32x32);
+  // promotion slices per 128-wide K block (one per K=32 MMA with 32-wide groups)
+  static constexpr int kSub = MODE == kScaleGroupF32x32 ? 4 : 1;
   static constexpr int kEpiWarps = kPromote ? 8 : 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kABytes = BM * BK, kBBytes = BN * BK;
@@ -432,6 +439,28 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
             ok = false;
             break;
           }
+          if constexpr (MODE == kScaleGroupF32x32) {
+            // every K=32 MMA into its own TMEM buffer (four in a ring), each
+            // committed to the epilogue as soon as it is issued
+            tc_fence_after();
+            const uint32_t idesc = idesc_f8f6f4(128, BN, args.fa, args.fb, 0, 0);
+            const OperandDesc ad = operand_desc(sA(s), 0, C::kABytes);
+            const OperandDesc bd = operand_desc(sB(s), 0, 128 * C::BK);
+#pragma unroll 1
+            for (int k = 0; k < 4 && ok; ++k) {
+              const uint32_t sub = it * 4u + (uint32_t)k, buf = sub & 3u, use = sub >> 2;
+              if (!mbar_wait(acce_bar(buf), (use & 1u) ^ 1u, abort_flag, err, 2)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              mma_f8f6f4(tmem + buf * BN, ad.base + k * ad.step, bd.base + k * bd.step, idesc, 0u);
+              mma_commit(accf_bar(buf));
+            }
+            if (!ok) break;
+            mma_commit(empty_bar(s));
+            continue;
+          }
           if constexpr (C::kPromote) {
             // one TMEM buffer per 128-wide K slice, four in a ring
             const uint32_t buf = it & 3u, use = it >> 2;
@@ -558,34 +587,42 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
       const int h = (int)(warp - 2) >> 2;  // column half of the 128-wide tile
       const float *sa = static_cast<const float *>(args.sa);
       const float *sb = static_cast<const float *>(args.sb);
-      const int64_t G = args.K / 128;
+      // scale groups along K: 128-wide (one per k block), or 32-wide
+      constexpr int kGS = 128 / C::kSub;
+      const int64_t G = (args.K + kGS - 1) / kGS;
+      const int64_t nb32 = (args.N + 31) / 32;  // 32-row weight blocks
       uint32_t it = 0;
       bool ok = true;
       for (int64_t u = u_first; u < num_units && ok; u += u_step) {
         const int64_t t = unit_tile(u);
         const int split = (int)(u / num_tiles);
-        const int kb0 = kb_begin(u), kb1 = kb_end(u);
+        // promotion slices [kb0, kb1): k blocks, or K=32 steps (kSub per block)
+        const int kb0 = kb_begin(u) * C::kSub, kb1 = kb_end(u) * C::kSub;
         const TileInfo ti = tile_info(t);
         const int64_t m0 = ti.m0, n0 = ti.n0;
         // rows past the tile's expert belong to the next expert: not stored
         const int64_t row = m0 + 32 * q + lane < ti.row_end ? m0 + 32 * q + lane : args.M;
-        const float *sb_row = sb + ti.sbo + (n0 >> 7) * G;
+        // the weight scales of this thread's two 32-column halves: one
+        // 128 x 128 block for both, or two 32 x 32 block rows
+        const int64_t wb0 = C::kSub == 1 ? (n0 >> 7) : ((n0 + h * 64) >> 5);
+        const float *sb_row0 = sb + ti.sbo + (C::kSub == 1 ? wb0 : (wb0 < nb32 ? wb0 : 0)) * G;
+        const float *sb_row1 = C::kSub == 1 ? sb_row0 : sb + (wb0 + 1 < nb32 ? wb0 + 1 : 0) * G;
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-        // the two scales of a k block are loaded kQ k blocks before it is
-        // promoted, into register slots used round-robin (constant indices:
-        // the loop is unrolled over the slots), so no promotion step waits on
-        // a scale load
+        // the scales of a slice are loaded kQ slices before it is promoted,
+        // into register slots used round-robin (constant indices: the loop is
+        // unrolled over the slots), so no promotion step waits on a scale load
         constexpr int kQ = 4;
-        float sa_q[kQ], sb_q[kQ];
-        auto load_s = [&](int k, float &fa, float &fb) {
+        float sa_q[kQ], sb_q[kQ], sb2_q[kQ];
+        auto load_s = [&](int k, float &fa, float &fb, float &fb2) {
           fa = row < args.M ? __ldg(sa + (int64_t)k * args.M + row) : 0.0f;
-          fb = __ldg(sb_row + k);
+          fb = __ldg(sb_row0 + k);
+          fb2 = C::kSub == 1 ? fb : __ldg(sb_row1 + k);
         };
 #pragma unroll
         for (int d = 0; d < kQ; ++d)
-          if (kb0 + d < kb1) load_s(kb0 + d, sa_q[d], sb_q[d]);
+          if (kb0 + d < kb1) load_s(kb0 + d, sa_q[d], sb_q[d], sb2_q[d]);
         for (int kb = kb0; kb < kb1 && ok; kb += kQ) {
 #pragma unroll
           for (int j = 0; j < kQ; ++j) {
@@ -593,7 +630,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
             if (k >= kb1) break;
             const uint32_t buf = it & 3u, use = it >> 2;
             const float s_cur = sa_q[j] * sb_q[j];
-            if (k + kQ < kb1) load_s(k + kQ, sa_q[j], sb_q[j]);
+            const float s_cur2 = sa_q[j] * sb2_q[j];
+            if (k + kQ < kb1) load_s(k + kQ, sa_q[j], sb_q[j], sb2_q[j]);
             if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) {
               ok = false;
               break;
@@ -612,7 +650,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               acc[i] = fmaf(s_cur, __uint_as_float(r0[i]), acc[i]);
-              acc[32 + i] = fmaf(s_cur, __uint_as_float(r1[i]), acc[32 + i]);
+              acc[32 + i] = fmaf(s_cur2, __uint_as_float(r1[i]), acc[32 + i]);
             }
             ++it;
           }
@@ -745,7 +783,7 @@ static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const Gem
 // the 128 x 256 tiles fill the SMs and 128 otherwise (twice the tiles: mid-
 // size M then needs no split K, small M splits K over fewer k blocks).
 int gemm_tile_n(int mode, int64_t M, int64_t N, int sms) {
-  if (mode == kScaleGroupF32) return 128;
+  if (mode == kScaleGroupF32 || mode == kScaleGroupF32x32) return 128;
   if (mode == kScaleTensor) return 256;
   const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
   return tiles256 < sms ? 128 : 256;
@@ -757,8 +795,8 @@ int gemm_tile_n(int mode, int64_t M, int64_t N, int sms) {
 // workspace splits are capped at 512 KB of fp32 partials per tile, which the
 // last CTA of the tile sums.
 static int max_active_clusters(int mode, int bn, int size) {
-  static int cache[64][4][2][kMaxClusterSplit + 1];
-  static bool have[64][4][2][kMaxClusterSplit + 1];
+  static int cache[64][5][2][kMaxClusterSplit + 1];
+  static bool have[64][5][2][kMaxClusterSplit + 1];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int w = bn == 128 ? 0 : 1;
@@ -774,6 +812,7 @@ static int max_active_clusters(int mode, int bn, int size) {
         n = w == 0 ? active_clusters<kScaleGroupUe8m0, 128, 6>(size)
                    : active_clusters<kScaleGroupUe8m0, 256, 4>(size);
         break;
+      case kScaleGroupF32x32: n = active_clusters<kScaleGroupF32x32, 128, kF32Stages>(size); break;
       default: n = active_clusters<kScaleGroupF32, 128, kF32Stages>(size); break;
     }
     cache[dev][mode][w][size] = n;
@@ -836,6 +875,9 @@ cudaError_t launch_gemm(int mode, const CUtensorMap &tma, const CUtensorMap &tmb
     case kScaleGroupF32:
       return mc ? run<kScaleGroupF32, 128, kF32Stages, false, 2>(tma, tmb, args, sms, st)
                 : run<kScaleGroupF32, 128, kF32Stages>(tma, tmb, args, sms, st);
+    case kScaleGroupF32x32:
+      if (mc) return cudaErrorInvalidValue;
+      return run<kScaleGroupF32x32, 128, kF32Stages>(tma, tmb, args, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

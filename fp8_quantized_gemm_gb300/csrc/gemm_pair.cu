@@ -72,6 +72,7 @@ struct PairCfg {
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kSmem <= 227 * 1024, "shared-memory budget");
   static_assert(BM == 128 && BN / 2 == 128, "MN-major tiles: one 128-wide TMA box per operand");
+  static_assert(2 * kOutBox >= 32 * 36 * 4, "a warp's AdamW staging buffer fits its two boxes");
 };
 
 struct PairGroup {
@@ -91,42 +92,57 @@ __device__ __forceinline__ int group_of(const PairGroup &g, int64_t t) {
   return i;
 }
 
-// AdamW on 32 consecutive parameters of row `row` (columns col0 ..), with
-// the fp32 gradient g of those columns (the GEMM result).  All 24 loads of a
-// full chunk are issued before any update; p, m and v stream (each is read
-// and written once per step).
-__device__ __forceinline__ void adamw_row32(const GemmArgs &a, int64_t row, int64_t col0,
-                                            const float (&g)[32], const AdamwHp &hp) {
-  if (row >= a.M || col0 >= a.N) return;
-  const int64_t off = row * a.ldc + col0;
-  float *p = a.adam_p + off, *m = a.adam_m + off, *v = a.adam_v + off;
-  __nv_bfloat16 *pb =
-      a.adam_pb != nullptr ? static_cast<__nv_bfloat16 *>(a.adam_pb) + off : nullptr;
-  if (col0 + 32 <= a.N && a.vec_store) {
-    float4 pv[8], mv[8], vv[8];
+// AdamW on a warp's 32 x 32 gradient chunk (rows row0 .. row0 + 31, columns
+// col0 ..), restaged through shared memory so that the parameter traffic is
+// coalesced: lane l handles rows 4i + l / 8 and the four columns 4 (l % 8) ..
+// of each, so eight lanes cover one 128-byte row segment.  `stage` is the
+// warp's 32 x kStageLd fp32 buffer (each lane has already written its own
+// row's 32 gradients there).  All 24 loads are issued before any update; p,
+// m and v stream (each is read and written once per step).
+constexpr int kStageLd = 36;  // row pitch in floats: conflict-free float4 rows
+__device__ __forceinline__ void adamw_chunk32(const GemmArgs &a, int64_t row0, int64_t col0,
+                                              const float *stage, const AdamwHp &hp,
+                                              uint32_t lane) {
+  const int rs = (int)(lane >> 3), c4 = (int)(lane & 7) * 4;
+  const int64_t col = col0 + c4;
+  const bool vec = col + 4 <= a.N;
+  float4 pv[8], mv[8], vv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      pv[i] = __ldcs(reinterpret_cast<const float4 *>(p) + i);
-      mv[i] = __ldcs(reinterpret_cast<const float4 *>(m) + i);
-      vv[i] = __ldcs(reinterpret_cast<const float4 *>(v) + i);
+  for (int i = 0; i < 8; ++i) {
+    const int64_t row = row0 + 4 * i + rs;
+    if (vec && row < a.M) {
+      const int64_t off = row * a.ldc + col;
+      pv[i] = __ldcs(reinterpret_cast<const float4 *>(a.adam_p + off));
+      mv[i] = __ldcs(reinterpret_cast<const float4 *>(a.adam_m + off));
+      vv[i] = __ldcs(reinterpret_cast<const float4 *>(a.adam_v + off));
     }
+  }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      adamw4(pv[i], mv[i], vv[i], make_float4(g[4 * i], g[4 * i + 1], g[4 * i + 2], g[4 * i + 3]),
-             hp);
-      __stcs(reinterpret_cast<float4 *>(p) + i, pv[i]);
-      __stcs(reinterpret_cast<float4 *>(m) + i, mv[i]);
-      __stcs(reinterpret_cast<float4 *>(v) + i, vv[i]);
-      if (pb != nullptr) __stcs(reinterpret_cast<uint2 *>(pb) + i, f32x4_to_bf16(pv[i]));
-    }
-  } else {
-    for (int i = 0; i < 32 && col0 + i < a.N; ++i) {
-      float pp = p[i], mm = m[i], vvv = v[i];
-      adamw1(pp, mm, vvv, g[i], hp);
-      p[i] = pp;
-      m[i] = mm;
-      v[i] = vvv;
-      if (pb != nullptr) pb[i] = __float2bfloat16_rn(pp);
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + rs;
+    const int64_t row = row0 + r;
+    if (row >= a.M || col >= a.N) continue;
+    const float4 g = *reinterpret_cast<const float4 *>(stage + r * kStageLd + c4);
+    const int64_t off = row * a.ldc + col;
+    if (vec) {
+      adamw4(pv[i], mv[i], vv[i], g, hp);
+      __stcs(reinterpret_cast<float4 *>(a.adam_p + off), pv[i]);
+      __stcs(reinterpret_cast<float4 *>(a.adam_m + off), mv[i]);
+      __stcs(reinterpret_cast<float4 *>(a.adam_v + off), vv[i]);
+      if (a.adam_pb != nullptr)
+        __stcs(reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.adam_pb) + off),
+               f32x4_to_bf16(pv[i]));
+    } else {  // the ragged last columns
+      const float gg[4] = {g.x, g.y, g.z, g.w};
+      for (int e = 0; e < 4 && col + e < a.N; ++e) {
+        float pp = a.adam_p[off + e], mm = a.adam_m[off + e], vvv = a.adam_v[off + e];
+        adamw1(pp, mm, vvv, gg[e], hp);
+        a.adam_p[off + e] = pp;
+        a.adam_m[off + e] = mm;
+        a.adam_v[off + e] = vvv;
+        if (a.adam_pb != nullptr)
+          static_cast<__nv_bfloat16 *>(a.adam_pb)[off + e] = __float2bfloat16_rn(pp);
+      }
     }
   }
 }
@@ -413,6 +429,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
         }
         hp.bc1 = __shfl_sync(0xffffffffu, bc1, 0);
         hp.bc2 = __shfl_sync(0xffffffffu, bc2, 0);
+        // this warp's 32 x 32 staging buffer (the TMA-store boxes' space;
+        // any bulk store still reading it finishes first)
+        float *stage = reinterpret_cast<float *>(out_stage + (warp - 2) * 2 * C::kOutBox);
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        const int64_t row0 = tr.m0 + rank * C::BM + 32 * q;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
@@ -423,10 +445,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader0 + 8u * buf);
           }
-          float gv[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) gv[i] = __uint_as_float(r[i]) * alpha;
-          adamw_row32(a, row, tr.n0 + c, gv, hp);
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4 *>(stage + lane * kStageLd + 4 * i) = make_float4(
+                __uint_as_float(r[4 * i]) * alpha, __uint_as_float(r[4 * i + 1]) * alpha,
+                __uint_as_float(r[4 * i + 2]) * alpha, __uint_as_float(r[4 * i + 3]) * alpha);
+          __syncwarp();
+          adamw_chunk32(a, row0, tr.n0 + c, stage, hp, lane);
+          __syncwarp();  // the buffer is rewritten by the next chunk
         }
         continue;
       }

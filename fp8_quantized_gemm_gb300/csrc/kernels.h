@@ -46,6 +46,12 @@ cudaError_t launch_ue8m0_words_experts(const uint8_t *sa, const uint8_t *sb,
 cudaError_t launch_quant_block32(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
                                  uint8_t *q, uint8_t *scales, uint32_t *local, int sms,
                                  cudaStream_t st);
+// (32, 32) weight blocks with fp32 scales [ceil(N/32), K/32] (no MX words).
+cudaError_t launch_quant_block32_f32(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
+                                     uint8_t *q, float *scales, int sms, cudaStream_t st);
+// 1 x 32 token groups (scales group-major [ceil(K/32), M], fp32 or UE8M0).
+cudaError_t launch_quant_group32(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
+                                 int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st);
 cudaError_t launch_dequant_block(const uint8_t *q, int64_t N, int64_t K, int fmt, int sfmt,
                                  const void *scales, void *out, int sms, cudaStream_t st);
 cudaError_t launch_auto_scale(const float *amax0, double grow, int fmt, float *scale,
@@ -76,7 +82,9 @@ enum GemmScaleMode : int {
   kScaleTensor = 0,      // per-tensor: alpha = sa[0] * sb[0] in the epilogue
   kScaleMx = 1,          // block-scaled MMA, packed E8M0 words; alpha = ga[0] * gb[0] (1 if ga null)
   kScaleGroupUe8m0 = 2,  // block-scaled MMA, per-128 UE8M0 bytes replicated in-kernel
-  kScaleGroupF32 = 3     // per-128 fp32 scales promoted on the CUDA cores
+  kScaleGroupF32 = 3,    // per-128 fp32 scales promoted on the CUDA cores
+  kScaleGroupF32x32 = 4  // fp32 scales per 1x32 activation group and 32x32 weight
+                         // block: every K=32 MMA into its own TMEM buffer, promoted
 };
 
 struct GemmArgs {

@@ -12,6 +12,8 @@
 // 8 MiB of partials, held on every GPU that loads the library until the
 // process exits -- and reduces them in global memory (the workspace form of
 // the split).  It allocates nothing.
+#include <nvtx3/nvToolsExt.h>
+
 #include <mutex>
 
 #include "fp8gemm.h"
@@ -54,9 +56,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-extern "C" int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const uint8_t *b,
-                                      const void *sb, int sfmt, int64_t M, int64_t N, int64_t K,
-                                      void *c, int64_t ldc, fp8_stream_t stream) {
+namespace {
+
+int gemm_group_noalloc(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
+                       int sfmt, int64_t M, int64_t N, int64_t K, void *c, int64_t ldc,
+                       fp8_stream_t stream) {
   if (a == nullptr || b == nullptr || sa == nullptr || sb == nullptr || c == nullptr)
     return FP8_ERR_INVALID_ARG;
   if (sfmt != FP8_SCALE_F32 && sfmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
@@ -100,4 +104,15 @@ extern "C" int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const ui
   if ((rc = fp8k::api_encode_operand(&tma, a, K, M, 128)) != FP8_OK) return rc;
   if ((rc = fp8k::api_encode_operand(&tmb, b, K, N, bn)) != FP8_OK) return rc;
   return fp8k::launch_gemm(mode, tma, tmb, args, sms, st) == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int fp8_gemm_group_noalloc(const uint8_t *a, const void *sa, const uint8_t *b,
+                                      const void *sb, int sfmt, int64_t M, int64_t N, int64_t K,
+                                      void *c, int64_t ldc, fp8_stream_t stream) {
+  nvtxRangePushA("fp8_gemm_group_noalloc");
+  const int rc = gemm_group_noalloc(a, sa, b, sb, sfmt, M, N, K, c, ldc, stream);
+  nvtxRangePop();
+  return rc;
 }

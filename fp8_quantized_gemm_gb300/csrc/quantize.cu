@@ -259,13 +259,14 @@ __global__ void __launch_bounds__(256, 2)
 // 4c..4c+3: group 8w + c of window w) and each lane forms its group's scale
 // once for 32 elements.  Each warp takes kU windows at once (w, w + W, ...,
 // W warps in the grid) and issues all their loads first.
-template <typename T, int F>
+template <typename T, int F, int GS>
 __global__ void __launch_bounds__(256, 3)
     quant_group_kernel(const T *__restrict__ x, int64_t M, int64_t K, int sfmt,
                        uint8_t *__restrict__ q, void *scales) {
   constexpr int kU = sizeof(T) == 2 ? 2 : 1;
+  constexpr int kShift = GS == 128 ? 7 : 5;  // log2 of the group size
   const float mx = fmt_max(F);
-  const int64_t G = (K + 127) / 128, wins = (K + 1023) / 1024, ntasks = M * wins;
+  const int64_t G = (K + GS - 1) / GS, wins = (K + 1023) / 1024, ntasks = M * wins;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const bool narrow = ntasks + kU * nwarps <= (int64_t)0xFFFFFFFFu;
@@ -289,11 +290,13 @@ __global__ void __launch_bounds__(256, 3)
       if (base + u * nwarps >= ntasks) break;  // warp-uniform
       const int64_t m = row[u], k = col[u];
       uint32_t key = run[u].max_key();
-      key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
-      key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
+      if constexpr (GS == 128) {  // a group is four lanes' runs
+        key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
+        key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
+      }
       const float amax = __uint_as_float(key);
-      const int64_t g = k >> 7;
-      const bool scale_lane = (l & 3) == 0 && g < G;
+      const int64_t g = k >> kShift;
+      const bool scale_lane = (GS == 32 || (l & 3) == 0) && g < G;
       if (sfmt == 0) {
         const float s = scale_from_amax(amax, mx);
         if (scale_lane) reinterpret_cast<float *>(scales)[g * M + m] = s;
@@ -578,9 +581,9 @@ cudaError_t launch_quant_group(const void *x, int in_dt, int64_t M, int64_t K, i
                                int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st) {
   // one resident wave (launch bounds: 3 CTAs per SM)
   const int threads = 256, blocks = grid_for(M * ((K + 1023) / 1024) * 32, threads, 3, sms);
-#define FP8K_QG(T, F)                                                                           \
-  quant_group_kernel<T, F><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), M, K, sfmt, q, \
-                                                       scales)
+#define FP8K_QG(T, F)                                                                          \
+  quant_group_kernel<T, F, 128><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), M, K, sfmt, \
+                                                            q, scales)
   if (in_dt == 0) {
     if (fmt == 0) FP8K_QG(__nv_bfloat16, 0); else FP8K_QG(__nv_bfloat16, 1);
   } else {
@@ -634,13 +637,16 @@ cudaError_t launch_quant_mx(const void *x, int in_dt, int64_t R, int64_t K, int 
 // the block byte of each 1x32 piece into the packed E8M0 word layout of the
 // two-level GEMM (rows past N up to R_pad get byte 127), so fp8_gemm_mx
 // contracts these weights with one-level MXFP8 activations directly.
-template <typename T, int F>
+// kF32: fp32 scales fl32(amax / MAX) (1.0 for an all-zero block) written to
+// scales_f32 [ceil(N/32), K/32], each block divided by its own scale; no MX
+// words (the per-32 FP32 GEMM promotes them on the CUDA cores).
+template <typename T, int F, bool kF32>
 __global__ void __launch_bounds__(256)
     quant_block32_kernel(const T *__restrict__ w, int64_t N, int64_t K,
                          uint8_t *__restrict__ q, uint8_t *__restrict__ scales,
-                         uint32_t *__restrict__ local) {
+                         uint32_t *__restrict__ local, float *__restrict__ scales_f32) {
   const float mx = fmt_max(F);
-  const int64_t KB = K / 32, rpad = (N + 127) / 128 * 128;
+  const int64_t KB = K / 32, rpad = kF32 ? (N + 31) / 32 * 32 : (N + 127) / 128 * 128;
   const int64_t nblk = (rpad / 32) * KB;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -663,6 +669,20 @@ __global__ void __launch_bounds__(256)
     for (int i = 0; i < 4; ++i) raw[i].max_abs(key_a, key_b);
     const uint32_t key = warp_max_u32(Raw8<T>::merge_keys(key_a, key_b));
     const float amax = __uint_as_float(key);
+    if constexpr (kF32) {
+      const float sc = scale_from_amax(amax, mx);
+      if (l == 0) scales_f32[bn * KB + bk] = sc;
+      if (valid) {
+        const ScaleDiv d(sc);
+        uint2 c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = quant8_block<F>(raw[i], d);
+        uint4 *dst = reinterpret_cast<uint4 *>(q + n * K + k0);
+        dst[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+        dst[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+      }
+      continue;
+    }
     int e = 0;
     if (amax > 0.0f) e = min(max(ceil_log2_pos(__fdiv_rn(amax, mx)), -127), 127);
     const uint8_t byte = (uint8_t)(e + 127);
@@ -686,15 +706,46 @@ cudaError_t launch_quant_block32(const void *w, int in_dt, int64_t N, int64_t K,
                                  cudaStream_t st) {
   const int64_t rpad = (N + 127) / 128 * 128;
   const int threads = 256, blocks = grid_for((rpad / 32) * (K / 32) * 32, threads, 8, sms);
-#define FP8K_QB32(T, F)                                                                        \
-  quant_block32_kernel<T, F><<<blocks, threads, 0, st>>>(static_cast<const T *>(w), N, K, q,    \
-                                                         scales, local)
+#define FP8K_QB32(T, F)                                                                       \
+  quant_block32_kernel<T, F, false><<<blocks, threads, 0, st>>>(static_cast<const T *>(w), N, K, \
+                                                                q, scales, local, nullptr)
   if (in_dt == 0) {
     if (fmt == 0) FP8K_QB32(__nv_bfloat16, 0); else FP8K_QB32(__nv_bfloat16, 1);
   } else {
     if (fmt == 0) FP8K_QB32(float, 0); else FP8K_QB32(float, 1);
   }
 #undef FP8K_QB32
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_block32_f32(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
+                                     uint8_t *q, float *scales, int sms, cudaStream_t st) {
+  const int64_t npad = (N + 31) / 32 * 32;
+  const int threads = 256, blocks = grid_for((npad / 32) * (K / 32) * 32, threads, 8, sms);
+#define FP8K_QB32F(T, F)                                                                     \
+  quant_block32_kernel<T, F, true><<<blocks, threads, 0, st>>>(static_cast<const T *>(w), N, K, \
+                                                               q, nullptr, nullptr, scales)
+  if (in_dt == 0) {
+    if (fmt == 0) FP8K_QB32F(__nv_bfloat16, 0); else FP8K_QB32F(__nv_bfloat16, 1);
+  } else {
+    if (fmt == 0) FP8K_QB32F(float, 0); else FP8K_QB32F(float, 1);
+  }
+#undef FP8K_QB32F
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_group32(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
+                                 int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st) {
+  const int threads = 256, blocks = grid_for(M * ((K + 1023) / 1024) * 32, threads, 3, sms);
+#define FP8K_QG32(T, F)                                                                        \
+  quant_group_kernel<T, F, 32><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), M, K, sfmt, \
+                                                           q, scales)
+  if (in_dt == 0) {
+    if (fmt == 0) FP8K_QG32(__nv_bfloat16, 0); else FP8K_QG32(__nv_bfloat16, 1);
+  } else {
+    if (fmt == 0) FP8K_QG32(float, 0); else FP8K_QG32(float, 1);
+  }
+#undef FP8K_QG32
   return cudaGetLastError();
 }
 

@@ -29,14 +29,16 @@ da and dW2; dx's first term, dW1 and dW3).
 Delayed scaling fixes every scale before its tensor exists, so the SwiGLU
 passes quantize what they produce: a, dh and du reach memory only as FP8
 codes (the same codes and amaxes as the bf16 tensors quantized afterwards
-would give).  By default the element-wise work also moves into the GEMM
-epilogues (fp8_gemm_tensor_grouped's epilogue variants): h and u come out of
-one gated launch whose epilogue also writes a's codes, and the three
-weight-gradient GEMMs apply AdamW to their tiles instead of storing dW.  The
-optimizer keeps its step count on the device, so `step` issues the same
-calls every time and can be captured as a CUDA graph and replayed.
-``fuse_forward=False`` / ``fuse_optimizer=False`` select the standalone passes
-(the latter stores dW in ``self.dw`` and runs fp8_adamw_multi).
+would give).  The forward's element-wise work also moves into a GEMM
+epilogue (fp8_gemm_tensor_grouped's gated variant): h and u come out of one
+launch whose epilogue also writes a's codes (``fuse_forward``, default on).
+``fuse_optimizer=True`` has the three weight-gradient GEMMs apply AdamW to
+their tiles instead of storing dW (the AdamW epilogue: the same bits, no dW
+buffers, measured no faster than the standalone update at these shapes, so
+off by default: dW is stored in ``self.dw`` and fp8_adamw_multi updates the
+weights).  The optimizer keeps its step count on the device, so `step`
+issues the same calls every time and can be captured as a CUDA graph and
+replayed.
 
 Buffers are allocated once (device memory through torch); `step` issues the
 calls on the current stream.
@@ -58,7 +60,7 @@ class SwiGLUTrainer:
                  lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
                  history: int = HISTORY, weight_scaling: str = "delayed",
                  rescale_interval: int = 500, fuse_forward: bool = True,
-                 fuse_optimizer: bool = True):
+                 fuse_optimizer: bool = False):
         if weight_scaling not in ("delayed", "auto"):
             raise ValueError(weight_scaling)
         self.weight_scaling = weight_scaling

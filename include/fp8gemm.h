@@ -244,6 +244,31 @@ FP8_API int fp8_quantize_block32(const void *w, int in_dt, int64_t N, int64_t K,
                                  uint8_t *q, uint8_t *scales, uint32_t *local,
                                  fp8_stream_t stream);
 
+/* ------------------------------ (32, 32) weight blocks, FP32 scales --
+ * The configurable weight_block_size of [HF] 八 at (32, 32) with the default
+ * float scales ([HF] 四 scale_fmt): the activations go in 1 x 32 groups.
+ *
+ * fp8_quantize_token_group32: fp8_quantize_token_group with 1 x 32 groups:
+ *   scales GROUP-MAJOR [ceil(K/32), M] (fp32 amax/MAX, 1.0 for an all-zero
+ *   group; or UE8M0 bytes as there).  x [M, K], K % 16 == 0.
+ * fp8_quantize_block32_f32: 32 x 32 weight blocks with fp32 scales:
+ *   scales [ceil(N/32), K/32] = fl32(block amax / MAX) (1.0 for an all-zero
+ *   block); each block divided by its own scale.  w [N, K], K % 32 == 0.
+ * fp8_gemm_group32: C[m,n] = sum_g sa[g,m] * sb[n/32, g] * sum_{k in g} a.b
+ *   over 32-wide K groups g; E4M3 codes a [M, K], b [N, K] with the scales
+ *   above; bf16 output c [M, ldc].  K % 128 == 0.  Every K=32 MMA is
+ *   contracted into its own tensor-memory buffer and promoted on the CUDA
+ *   cores with its two scales (a promotion per 32-deep K step, four times as
+ *   many as the 128-wide groups of fp8_gemm_group).
+ */
+FP8_API int fp8_quantize_token_group32(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
+                                       int sfmt, uint8_t *q, void *scales, fp8_stream_t stream);
+FP8_API int fp8_quantize_block32_f32(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
+                                     uint8_t *q, float *scales, fp8_stream_t stream);
+FP8_API int fp8_gemm_group32(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb,
+                             int64_t M, int64_t N, int64_t K, void *c, int64_t ldc,
+                             fp8_stream_t stream);
+
 /* --------------------------------------------------- dequantize block --
  * fp8_dequantize_block: out[n,k] = decode(q[n,k]) * scale of block
  * (n/128, k/128), rounded to bf16 ([HF] 五: dequantize=True folds the block

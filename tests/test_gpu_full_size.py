@@ -9,8 +9,8 @@ benchmark times.
   quantized tensor bit-exact on sampled rows (the amaxes over the whole
   tensors), the nine GEMMs within the GEMM bound on 4096 sampled outputs each
   plus tile corners, SwiGLU within one bf16 ulp on sampled rows, AdamW on
-  sampled weights.  Then the default trainer (gated SwiGLU epilogue, AdamW
-  in the weight-gradient GEMMs) against that path, bit for bit.
+  sampled weights.  Then the trainer with both epilogue variants (gated
+  SwiGLU, AdamW in the weight-gradient GEMMs) against that path, bit for bit.
 * MOSS two-level microscaling GEMM, M = N = K = 8192 (MOSS blog, section 4,
   steps 1-4) on the two-level workload's own inputs (8 outlier K columns x100
   in A): amax and global factor bit-exact, codes and local factors bit-exact
@@ -194,15 +194,15 @@ def test_swiglu_training_step_full_size():
 
 
 def test_fused_training_step_full_size_matches_standalone_passes():
-    """At full size, two steps of the default trainer (gated SwiGLU epilogue,
-    AdamW in the weight-gradient GEMMs) give the bits of the standalone
-    passes (checked against the oracle in the test above)."""
+    """At full size, two steps of the trainer with both epilogue variants
+    (gated SwiGLU, AdamW in the weight-gradient GEMMs) give the bits of the
+    standalone passes (checked against the oracle in the test above)."""
     lib()
     from fp8_quantized_gemm_gb300.mlp import SwiGLUTrainer
     dev = torch.device("cuda")
     x, w1, w3, w2 = workloads.swiglu(device=dev)
     T = x.shape[0]
-    fused = SwiGLUTrainer(w1, w3, w2, tokens=T)
+    fused = SwiGLUTrainer(w1, w3, w2, tokens=T, fuse_forward=True, fuse_optimizer=True)
     plain = SwiGLUTrainer(w1, w3, w2, tokens=T, fuse_forward=False, fuse_optimizer=False)
     del w1, w3, w2
     for t in range(2):

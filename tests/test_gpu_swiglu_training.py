@@ -225,7 +225,8 @@ def oracle_trajectory(x, w_init, dys, steps):
     return scales, master, y, dx
 
 
-def test_swiglu_training_16_steps_free_running():
+@pytest.mark.parametrize("fuse_optimizer", [False, True])
+def test_swiglu_training_16_steps_free_running(fuse_optimizer):
     """16 steps of the GPU trainer against the oracle's own trajectory from the
     same initial weights and gradients (not teacher-forced: the two runs only
     share their inputs).  Rounding-boundary flips of single codes are expected
@@ -237,7 +238,7 @@ def test_swiglu_training_16_steps_free_running():
     x, w1, w3, w2 = workloads.swiglu(d=D, ffn=FFN, tokens=T)
     dys = [workloads.swiglu_grad(t, tokens=T, d=D) for t in range(STEPS)]
     w_init = [f32(w).astype(np.float64) for w in (w1, w3, w2)]
-    tr = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T)
+    tr = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T, fuse_optimizer=fuse_optimizer)
     xd = x.cuda()
     gpu_scales = []
     for t in range(STEPS):
@@ -264,14 +265,15 @@ def test_swiglu_training_16_steps_free_running():
 
 
 def test_fused_epilogues_match_standalone_passes():
-    """The gated SwiGLU epilogue and the AdamW epilogues (the default trainer)
-    give the same bits as the standalone passes (fp8_swiglu_forward_quantize,
-    stored dW + fp8_adamw_multi) over several steps: h, u, a's codes, every
-    amax and scale, the weights, moments and bf16 copies."""
+    """The gated SwiGLU epilogue and the AdamW epilogues give the same bits as
+    the standalone passes (fp8_swiglu_forward_quantize, stored dW +
+    fp8_adamw_multi) over several steps: h, u, a's codes, every amax and
+    scale, the weights, moments and bf16 copies."""
     lib()
     from fp8_quantized_gemm_gb300.mlp import SwiGLUTrainer
     x, w1, w3, w2 = workloads.swiglu(d=D, ffn=FFN, tokens=T)
-    fused = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T)
+    fused = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T, fuse_forward=True,
+                          fuse_optimizer=True)
     plain = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T, fuse_forward=False,
                           fuse_optimizer=False)
     xd = x.cuda()

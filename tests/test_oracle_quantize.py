@@ -300,3 +300,54 @@ def test_block_32x32_ue8m0_brute_force():
             assert int(np.asarray(sc)[bi, bj]) == 127 + e
             ref = Q.quantize_with_scale(blk, np.float32(2.0 ** e), "e4m3")
             assert np.array_equal(q[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32], ref)
+
+
+def test_block_32x32_f32_brute_force():
+    """(32, 32) weight blocks with FP32 scales (Transformers fine-grained FP8,
+    八: weight_block_size (32, 32); 四: scale_fmt float, the default), against
+    a loop over the blocks: each scale is fl32(block amax / 448) (1.0 for an
+    all-zero block), each block's largest element lands exactly on +-448, and
+    its codes are the block divided by its own scale; ragged edge blocks."""
+    w = workloads.normal((70, 96), 0.02, seed=41).numpy()
+    w[32:64, 32:64] = 0.0
+    w[5, 70] = -3.0
+    q, sc = Q.quantize_block(w, "e4m3", "f32", block=32)
+    sc = np.asarray(sc)
+    assert sc.shape == (3, 3) and sc.dtype == np.float32
+    for bi in range(3):
+        for bj in range(3):
+            blk = w[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32]
+            qb = q[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32]
+            am = np.float32(np.max(np.abs(blk)))
+            if am == 0:
+                assert sc[bi, bj] == 1.0 and not qb.any()
+                continue
+            assert sc[bi, bj] == np.float32(am / np.float32(448.0))
+            assert np.array_equal(qb, Q.quantize_with_scale(blk, sc[bi, bj], "e4m3"))
+            assert np.max(np.abs(F.decode(qb, "e4m3"))) == 448.0
+    # a block's outlier moves only that block's scale
+    w2 = w.copy()
+    w2[5, 70] = 0.01
+    _, sc2 = Q.quantize_block(w2, "e4m3", "f32", block=32)
+    assert [tuple(d) for d in np.argwhere(np.asarray(sc2) != sc)] == [(0, 2)]
+
+
+def test_token_group_1x32_f32_brute_force():
+    """1 x 32 activation groups with FP32 scales, the activation side of
+    (32, 32) weight blocks (Transformers fine-grained FP8, 八: the activation
+    group follows the block's K size): per row and 32-wide group, scale
+    fl32(amax / 448) (1.0 for a zero group), codes of the group divided by it."""
+    x = workloads.normal((6, 96), 1.0, seed=42).numpy()
+    x[1, 32:64] = 0.0
+    x[4, 3] = 200.0
+    q, sc = Q.quantize_token_group(x, "e4m3", "f32", group=32)
+    sc = np.asarray(sc)
+    assert sc.shape == (6, 3)
+    for r in range(6):
+        for g in range(3):
+            xg = x[r, 32 * g:32 * g + 32]
+            am = np.float32(np.max(np.abs(xg)))
+            want_s = np.float32(am / np.float32(448.0)) if am > 0 else np.float32(1.0)
+            assert sc[r, g] == want_s
+            assert np.array_equal(q[r, 32 * g:32 * g + 32],
+                                  Q.quantize_with_scale(xg, want_s, "e4m3"))
