@@ -1160,8 +1160,8 @@ def run_profile(args):
     import fp8_quantized_gemm_gb300 as F
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    if args.profile == "swiglu":
-        wl = SwiGLUStep(dev, n_dy=2)
+    if args.profile in ("swiglu", "swiglu_t4096"):
+        wl = SwiGLUStep(dev, n_dy=2, tokens=16384 if args.profile == "swiglu" else 4096)
         for i in range(args.warmup + args.steps):
             wl.eager_step(i)
         n = SwiGLUStep.kernels_per_step
@@ -1189,7 +1189,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=5.0,
                     help="CPU seconds of oracle work per row baseline (headline: twice this)")
     ap.add_argument("--profile", default=None,
-                    choices=sorted(PROFILE_WORKLOADS) + ["swiglu"],
+                    choices=sorted(PROFILE_WORKLOADS) + ["swiglu", "swiglu_t4096"],
                     help="run one workload's launch sequence only (for ncu captures); "
                          "prints no bench line")
     args = ap.parse_args()
