@@ -62,8 +62,8 @@ def run_group_noalloc(qa, sa, qb, sb, sfmt="f32"):
 def test_timeout_in_group_gemm_resets_split_k_counters():
     """The no-allocation entry point splits K over CTAs that meet through
     arrival counters in its fixed scratch; a timed-out call can leave counters
-    behind, reading the error resets them, and the next calls (that entry
-    point and the regular one) are correct.  UE8M0 scales keep one
+    behind, every call clears the counters it uses before its kernel runs, and
+    the next calls (that entry point and the regular one) are correct.  UE8M0 scales keep one
     accumulator per tile, so the epilogue's first wait spans the CTA's whole
     share of K (M = 128 limits the split to eight 64-block shares), long
     enough to outlast the barrier's suspend window; the FP32 mode's waits

@@ -388,8 +388,9 @@ def test_gemm_mx_small_m_split_k():
 
 
 def test_split_k_on_two_streams():
-    """Each stream has its own split-K scratch: interleaved calls on two
-    streams give the same results as calls on one."""
+    """Split-K calls on two streams at once (each tile's splits reduce inside
+    their own thread-block cluster, so concurrent calls share nothing) give
+    the results of calls on one stream."""
     F = lib()
     m, n, k = 16, 2048, 7168
     qa, sa, qb, sb = group_operands(m, n, k, "f32", seed=4)
