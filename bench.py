@@ -1113,10 +1113,10 @@ def run_reference(args):
     class _Weights:  # the weights the sample slices, as the trainer holds them
         w_bf = [w1, w3, w2]
     wl.tr = _Weights()
-    _, dt_cal, _ = wl.oracle_sample(tokens=128, hidden=128)
-    budget = 120.0 / max(args.steps + args.warmup, 1)
+    _, dt_cal, _ = wl.oracle_sample(tokens=128, hidden=512)
+    budget = 100.0 / max(args.steps + args.warmup, 1)
     # the sample's cost grows about linearly with hidden (weights) at fixed tokens
-    hidden = int(max(128, min(4096, 128 * budget / max(dt_cal, 1e-3))) // 128 * 128)
+    hidden = int(max(128, min(1024, 512 * budget / max(dt_cal, 1e-3))) // 128 * 128)
     tokens = 128
     for _ in range(args.warmup):
         wl.oracle_sample(tokens=tokens, hidden=hidden)
