@@ -10,10 +10,12 @@
 
 namespace fp8k {
 
-// logistic function 1 / (1 + e^-z): the correctly rounded reciprocal (the
-// same value as the IEEE quotient 1 / x, with fewer instructions)
+// logistic function 1 / (1 + e^-z): the hardware exponential (__expf, a
+// few fp32 ulps from e^-z) and the correctly rounded reciprocal.  The
+// SwiGLU values it feeds are rounded to bf16 (8 significant bits), far
+// coarser than that error.
 __device__ __forceinline__ float sigmoidf_(float z) {
-  return __frcp_rn(__fadd_rn(1.0f, expf(-z)));
+  return __frcp_rn(__fadd_rn(1.0f, __expf(-z)));
 }
 
 // a = silu(h) * u = (h * s(h)) * u

@@ -145,11 +145,11 @@ __device__ __forceinline__ void swiglu_bwd_quant_body(
     int64_t nvec, const ScaleDiv &dsh, const ScaleDiv &dsu, uint2 *__restrict__ qh,
     uint2 *__restrict__ qu, uint32_t &key_h, uint32_t &key_u) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+  auto one = [&](int64_t i, const uint4 daw, const uint4 hw, const uint4 uw) {
     float dav[8], hv[8], uv[8], dhv[8], duv[8], dhb[8], dub[8], y[8];
-    bf16x8_to_f32(__ldcs(da + i), dav);
-    bf16x8_to_f32(__ldcs(h + i), hv);
-    bf16x8_to_f32(__ldcs(u + i), uv);
+    bf16x8_to_f32(daw, dav);
+    bf16x8_to_f32(hw, hv);
+    bf16x8_to_f32(uw, uv);
 #pragma unroll
     for (int j = 0; j < 8; ++j) swiglu_grad_values(dav[j], hv[j], uv[j], dhv[j], duv[j]);
     bf16_roundtrip(dhv, dhb);
@@ -165,7 +165,17 @@ __device__ __forceinline__ void swiglu_bwd_quant_body(
     __stcs(qh + i, pack8<F>(y));
     dsu.div8<kFast>(dub, y);
     __stcs(qu + i, pack8<F>(y));
+  };
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // two vectors of each input in flight per thread
+  for (; i + stride < nvec; i += 2 * stride) {
+    const uint4 da0 = __ldcs(da + i), h0 = __ldcs(h + i), u0 = __ldcs(u + i);
+    const uint4 da1 = __ldcs(da + i + stride), h1 = __ldcs(h + i + stride),
+                u1 = __ldcs(u + i + stride);
+    one(i, da0, h0, u0);
+    one(i + stride, da1, h1, u1);
   }
+  for (; i < nvec; i += stride) one(i, __ldcs(da + i), __ldcs(h + i), __ldcs(u + i));
 }
 
 template <int F, bool kAmax>
