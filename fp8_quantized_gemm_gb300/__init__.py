@@ -63,7 +63,7 @@ _SIGS = {
     "fp8_swiglu_forward_quantize": [_vp, _vp, _i64, _int, _vp, _vp, _vp, _vp],
     "fp8_swiglu_backward_quantize": [_vp, _vp, _vp, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp,
                                      _vp],
-    "fp8_adamw_multi": [_vp, _int, _vp, _d, _d, _d, _d, _d, _vp],
+    "fp8_adamw_multi": [_vp, _int, _vp, _int, _d, _d, _d, _d, _d, _vp],
     "fp8_quantize_token_group32": [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp],
     "fp8_quantize_block32_f32": [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp],
     "fp8_gemm_group32": [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp],
@@ -405,14 +405,15 @@ def adamw_item(p, g, m, v, p_bf16=None):
 
 
 def fp8_adamw_multi(items, step, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
-                    stream=None):
+                    stream=None, advance=True):
     """One AdamW step over several tensors; `step` is a device int64 tensor of
-    one element, incremented by the call (the update uses the new value).  No
-    items: only the increment."""
+    one element, incremented by the call first (the update uses the new
+    value) unless advance=False (the update uses it as it stands).  No items:
+    only the increment."""
     assert step.dtype == torch.int64 and step.numel() == 1
     arr = (AdamwItem * len(items))(*items) if items else None
     _call("fp8_adamw_multi", ctypes.cast(arr, _vp) if arr is not None else None, len(items),
-          _p(step), lr, beta1, beta2, eps, weight_decay, _stream(stream))
+          _p(step), int(bool(advance)), lr, beta1, beta2, eps, weight_decay, _stream(stream))
 
 
 def fp8_get_last_device_error(stream=None):
@@ -423,7 +424,7 @@ def fp8_get_last_device_error(stream=None):
 
 
 (OPT_GEMM_CTA_PAIRS, OPT_WAIT_LIMIT_US, OPT_GEMM_MULTICAST, OPT_GEMM_TMA_STORE,
- OPT_GEMM_FEW_ROWS) = 1, 2, 3, 4, 5
+ OPT_GEMM_FEW_ROWS, OPT_GEMM_BAND_ROWS) = 1, 2, 3, 4, 5, 6
 
 
 def fp8_set_option(option, value):

@@ -68,6 +68,8 @@ bool g_use_multicast = true;
 bool g_use_tma_store = false;
 // CUDA-core path of the per-group GEMM for one to four rows (on by default).
 bool g_use_gemv = true;
+// 256-row tiles per band of the CTA-pair kernel's tile order.
+int64_t g_pair_band_rows = 8;
 // Bound of every device-side mbarrier wait (fp8_set_option).
 uint64_t g_wait_limit_ns = 2000000000ull;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -331,6 +333,7 @@ int run_tensor_problem(const fp8_gemm_problem_t &p, cudaStream_t st) {
 
 namespace fp8k {
 uint64_t wait_limit_ns() { return g_wait_limit_ns; }
+int64_t gemm_pair_band_rows() { return g_pair_band_rows; }
 
 // Internal hooks for entry points defined in other files (noalloc.cu): the
 // per-device setup (SM count, device error word) and the operand tensor map.
@@ -944,12 +947,13 @@ int fp8_swiglu_backward_quantize(const void *da, const void *h, const void *u, i
                                                  amax_dh, amax_du, d->sms, (cudaStream_t)stream));
 }
 
-int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, double lr,
-                    double beta1, double beta2, double eps, double weight_decay,
+int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, int advance,
+                    double lr, double beta1, double beta2, double eps, double weight_decay,
                     fp8_stream_t stream) {
   const NvtxRange nvtx_range(__func__);
   if (step == nullptr || count < 0 || count > fp8k::kMaxAdamw || (count > 0 && items == nullptr))
     return FP8_ERR_INVALID_ARG;
+  if (advance != 0 && advance != 1) return FP8_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(step) & 7u) != 0) return FP8_ERR_MISALIGNED;
   fp8k::AdamwMulti a{};
   for (int k = 0; k < count; ++k) {
@@ -974,8 +978,8 @@ int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, dou
   DeviceState *d = nullptr;
   int rc = device_state(&d);
   if (rc != FP8_OK) return rc;
-  return to_status(fp8k::launch_adamw_multi(a, lr, beta1, beta2, eps, weight_decay, d->sms,
-                                            (cudaStream_t)stream));
+  return to_status(fp8k::launch_adamw_multi(a, advance != 0, lr, beta1, beta2, eps, weight_decay,
+                                            d->sms, (cudaStream_t)stream));
 }
 
 int fp8_adamw_step(float *p, const float *g, float *m, float *v, void *p_bf16, int64_t n,
@@ -1039,6 +1043,11 @@ int fp8_set_option(int option, int value) {
   }
   if (option == FP8_OPT_GEMM_MULTICAST) {
     g_use_multicast = value != 0;
+    return FP8_OK;
+  }
+  if (option == FP8_OPT_GEMM_BAND_ROWS) {
+    if (value < 1 || value > 4096) return FP8_ERR_INVALID_ARG;
+    g_pair_band_rows = value;
     return FP8_OK;
   }
   if (option == FP8_OPT_WAIT_LIMIT_US) {

@@ -50,7 +50,9 @@
 
 namespace fp8k {
 
-// 256-row tiles per band of the grouped tile order (see tile_ref).
+// 256-row tiles per band of the grouped tile order (see tile_ref); the
+// launcher's value (fp8_set_option FP8_OPT_GEMM_BAND_ROWS) is passed in
+// PairGroup::band_rows.
 constexpr int64_t kPairBandRows = 8;
 
 template <int BN, int STAGES>
@@ -83,6 +85,7 @@ struct PairGroup {
   GemmArgs args[kMaxGroup];
   int64_t tile_begin[kMaxGroup + 1];  // problem i owns tiles [tile_begin[i], tile_begin[i+1])
   int count;
+  int64_t band_rows;  // 256-row tiles per band of the tile order
 };
 
 // Problem owning global tile t (the group is small: a linear scan).
@@ -270,11 +273,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN, STAGES>:
     // grouped order: bands of kPairBandRows 256-row tiles walked column by
     // column, so the pairs in flight share A and B blocks in L2
     const int64_t rows = (a.M + 255) / 256;
-    const int64_t band = t / (kPairBandRows * tiles_n);
-    const int64_t band_rows =
-        rows - band * kPairBandRows < kPairBandRows ? rows - band * kPairBandRows : kPairBandRows;
-    const int64_t local = t - band * kPairBandRows * tiles_n;
-    r.m0 = (band * kPairBandRows + local % band_rows) * 256;
+    const int64_t bandh = grp.band_rows;
+    const int64_t band = t / (bandh * tiles_n);
+    const int64_t band_rows = rows - band * bandh < bandh ? rows - band * bandh : bandh;
+    const int64_t local = t - band * bandh * tiles_n;
+    r.m0 = (band * bandh + local % band_rows) * 256;
     r.n0 = (local / band_rows) * tn;
     r.kb_count = (int)((a.K + C::BK - 1) / C::BK);
     return r;
@@ -592,6 +595,7 @@ cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tm
   }
   PairGroup g{};
   g.count = count;
+  g.band_rows = gemm_pair_band_rows();
   g.tile_begin[0] = 0;
   for (int i = 0; i < count; ++i) {
     g.tma[i] = tma[i];

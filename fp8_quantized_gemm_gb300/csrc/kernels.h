@@ -186,6 +186,8 @@ cudaError_t launch_gemm_pair_group(const CUtensorMap *tma, const CUtensorMap *tm
                                    const CUtensorMap *tmc, const CUtensorMap *tmb2,
                                    const GemmArgs *args, int count, int sms, cudaStream_t st);
 int gemm_pair_b_rows();
+// 256-row tiles per band of the CTA-pair tile order (fp8_set_option).
+int64_t gemm_pair_band_rows();
 cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb,
                              const CUtensorMap &tmc, const GemmArgs &args, int sms,
                              cudaStream_t st);

@@ -354,15 +354,18 @@ cudaError_t launch_adamw(float *p, const float *g, float *m, float *v, void *pb,
   return cudaGetLastError();
 }
 
-cudaError_t launch_adamw_multi(AdamwMulti a, double lr, double b1, double b2, double eps,
-                               double wd, int sms, cudaStream_t st) {
+cudaError_t launch_adamw_multi(AdamwMulti a, bool advance, double lr, double b1, double b2,
+                               double eps, double wd, int sms, cudaStream_t st) {
   a.hp = adamw_hp(lr, b1, b2, eps, wd);
   a.b1d = b1;
   a.b2d = b2;
   int64_t most = 0;
   for (int k = 0; k < a.count; ++k) most = a.n[k] > most ? a.n[k] : most;
-  adamw_advance_step_kernel<<<1, 1, 0, st>>>(a.step);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (advance) {
+    adamw_advance_step_kernel<<<1, 1, 0, st>>>(a.step);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess || most == 0) return e;
   adamw_multi_kernel<<<blocks_for(most / 4, 512, 4, sms), 512, 0, st>>>(a);
   return cudaGetLastError();

@@ -36,13 +36,13 @@ struct AdamwMulti {
   void *pb[kMaxAdamw];  // nullable bf16 copies
   int64_t n[kMaxAdamw];
   int count;
-  int64_t *step;        // device: incremented, then read as t
+  int64_t *step;        // device: read as t (incremented first when advancing)
   AdamwHp hp;           // set by the launcher (bias corrections: in the kernel)
   double b1d, b2d;
 };
 // The fp32 hyperparameters of an AdamW update (1 - beta, decay in double).
 AdamwHp adamw_hp(double lr, double b1, double b2, double eps, double wd);
-cudaError_t launch_adamw_multi(AdamwMulti a, double lr, double b1, double b2, double eps,
-                               double wd, int sms, cudaStream_t st);
+cudaError_t launch_adamw_multi(AdamwMulti a, bool advance, double lr, double b1, double b2,
+                               double eps, double wd, int sms, cudaStream_t st);
 
 }  // namespace fp8k

@@ -36,9 +36,13 @@ launch whose epilogue also writes a's codes (``fuse_forward``, default on).
 their tiles instead of storing dW (the AdamW epilogue: the same bits, no dW
 buffers, measured no faster than the standalone update at these shapes, so
 off by default: dW is stored in ``self.dw`` and fp8_adamw_multi updates the
-weights).  The optimizer keeps its step count on the device, so `step`
-issues the same calls every time and can be captured as a CUDA graph and
-replayed.
+weights after the backward; ``overlap_optimizer=True`` instead updates each
+weight on a second stream as soon as its gradient exists, beside the
+compute-bound GEMMs that remain -- the same bits, measured no faster on this
+GPU, whose step runs under its power cap).  The
+optimizer keeps its step count on the device, so `step` issues the same
+calls every time and can be captured as a CUDA graph (the second stream
+forks from and joins the capturing one) and replayed.
 
 Buffers are allocated once (device memory through torch); `step` issues the
 calls on the current stream.
@@ -60,11 +64,15 @@ class SwiGLUTrainer:
                  lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
                  history: int = HISTORY, weight_scaling: str = "delayed",
                  rescale_interval: int = 500, fuse_forward: bool = True,
-                 fuse_optimizer: bool = False):
+                 fuse_optimizer: bool = False, overlap_optimizer: bool = False):
         if weight_scaling not in ("delayed", "auto"):
             raise ValueError(weight_scaling)
         self.weight_scaling = weight_scaling
         self.fuse_forward, self.fuse_optimizer = fuse_forward, fuse_optimizer
+        # the standalone AdamW of each weight runs on a second stream as soon
+        # as that weight's gradient exists, beside the remaining GEMMs
+        self.overlap = overlap_optimizer and not fuse_optimizer
+        self.side = torch.cuda.Stream(device=w1.device) if self.overlap else None
         self.rescale_interval = rescale_interval
         dev = w1.device
         ffn, d = w1.shape
@@ -162,13 +170,15 @@ class SwiGLUTrainer:
                                           self._am(A2))
         run([P(self.aq, E4, self.w2q, E4, sc(A2), sc(K2), self.y)])         # y = a W2^T
         # backward
-        if self.fuse_optimizer:
+        if self.fuse_optimizer or self.overlap:
             F.fp8_adamw_multi([], self.step_dev, **self.hp)  # t of this step's updates
         ep = self.adamw_ep
         q(dy, E5, self.dyq, scale=sc(G2), amax_out=self._am(G2))
         run([P(self.dyq, E5, self.w2q, E4, sc(G2), sc(K2), self.da, b_layout=MN),   # da = dy W2
              P(self.dyq, E5, self.aq, E4, sc(G2), sc(A2), self.dw[2],               # dW2 = dy^T a
                a_layout=MN, b_layout=MN, adamw=ep[2])])
+        if self.overlap:
+            self._side_adamw([self.adamw_items[2]])                         # W2, beside the rest
         F.fp8_swiglu_backward_quantize(self.da, self.h, self.u, E5, sc(G1), sc(G3),  # dh, du
                                        self.dhq, self.duq, self._am(G1), self._am(G3))
         run([P(self.dhq, E5, self.w1q, E4, sc(G1), sc(K1), self.dx, b_layout=MN),   # dx = dh W1
@@ -176,14 +186,29 @@ class SwiGLUTrainer:
                a_layout=MN, b_layout=MN, adamw=ep[0]),
              P(self.duq, E5, self.xq, E4, sc(G3), sc(X1), self.dw[1],               # dW3 = du^T x
                a_layout=MN, b_layout=MN, adamw=ep[1])])
+        if self.overlap:
+            self._side_adamw(self.adamw_items[:2])                          # W1, W3
         run([P(self.duq, E5, self.w3q, E4, sc(G3), sc(K3), self.dx, b_layout=MN,    # dx += du W3
                accumulate=True)])
+
+    def _side_adamw(self, items):
+        """AdamW on `items` on the second stream once the current stream has
+        produced their gradients; t is the step's (already advanced) count.
+        Nothing later in the step reads those weights' masters, moments or bf16
+        copies (the GEMMs read the codes), so the update overlaps the GEMMs."""
+        ready = torch.cuda.Event()
+        ready.record()
+        self.side.wait_event(ready)
+        with torch.cuda.stream(self.side):
+            F.fp8_adamw_multi(items, self.step_dev, advance=False, **self.hp)
 
     def optimizer_and_state(self):
         """AdamW on the three weights (unless the weight-gradient GEMMs did it),
         then the nine amax-history pushes."""
         self.t += 1
-        if not self.fuse_optimizer:
+        if self.overlap:
+            torch.cuda.current_stream().wait_stream(self.side)  # the updates are done
+        elif not self.fuse_optimizer:
             F.fp8_adamw_multi(self.adamw_items, self.step_dev, **self.hp)
         auto = self.weight_scaling == "auto"
         if auto:

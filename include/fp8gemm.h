@@ -563,12 +563,15 @@ FP8_API int fp8_swiglu_backward_quantize(const void *da, const void *h, const vo
                                          float *amax_du, fp8_stream_t stream);
 
 /* fp8_adamw_multi: one AdamW step (as fp8_adamw_step) over `count` (0..8)
- * parameter tensors in one launch, with the step number kept on the device:
- * the call first increments *step (device int64, 8-byte aligned) and the
- * update uses the incremented value as t (bias corrections 1 - beta^t formed
- * in double on the device).  A captured training step therefore advances t
- * on every replay.  Start *step at 0 for a fresh optimizer.  count == 0 only
- * advances the counter (items may be null): for updates done by GEMM
+ * parameter tensors in one launch, with the step number kept on the device
+ * (*step: device int64, 8-byte aligned; bias corrections 1 - beta^t formed in
+ * double on the device).  advance = 1: the call first increments *step and
+ * the update uses the incremented value as t; advance = 0: the update uses
+ * t = *step as it stands (for the other updates of the same step, e.g. on a
+ * second stream).  A captured training step therefore advances t on every
+ * replay.  Start *step at 0 for a fresh optimizer.  count == 0 with
+ * advance = 1 only advances the counter (items may be null): for updates
+ * done later in the step, by further calls with advance = 0 or by GEMM
  * epilogues (fp8_adamw_epilogue_t), which read t without advancing it.
  *   items  HOST array of `count` descriptors (read during the call only);
  *          per item p, g, m, v fp32 [n] and p_bf16 (nullable) bf16 [n], all
@@ -582,9 +585,9 @@ typedef struct {
   void *p_bf16;
   int64_t n;
 } fp8_adamw_item_t;
-FP8_API int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, double lr,
-                            double beta1, double beta2, double eps, double weight_decay,
-                            fp8_stream_t stream);
+FP8_API int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step,
+                            int advance, double lr, double beta1, double beta2, double eps,
+                            double weight_decay, fp8_stream_t stream);
 
 /* ---------------------------------------------------------------- status --
  * fp8_status_string: static text for a status code.
@@ -621,13 +624,19 @@ FP8_API const char *fp8_version(void);
  *   FP8_OPT_GEMM_FEW_ROWS: 1 (default) runs fp8_gemm_group / _group_bias
  *     with a single activation row on the CUDA cores as a stream over the
  *     weights; 0 keeps it on the tensor cores.  Results agree within the
- *     GEMM bound. */
+ *     GEMM bound.
+ *   FP8_OPT_GEMM_BAND_ROWS: height, in 256-row tiles, of the bands in which
+ *     the CTA-pair per-tensor GEMM walks its output tiles column by column
+ *     (1..4096, default 8): taller bands read each B column block from DRAM
+ *     fewer times, at the price of a larger A working set in L2.  Same
+ *     results. */
 typedef enum {
   FP8_OPT_GEMM_CTA_PAIRS = 1,
   FP8_OPT_WAIT_LIMIT_US = 2,
   FP8_OPT_GEMM_MULTICAST = 3,
   FP8_OPT_GEMM_TMA_STORE = 4,
-  FP8_OPT_GEMM_FEW_ROWS = 5
+  FP8_OPT_GEMM_FEW_ROWS = 5,
+  FP8_OPT_GEMM_BAND_ROWS = 6
 } fp8_option_t;
 FP8_API int fp8_set_option(int option, int value);
 

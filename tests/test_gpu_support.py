@@ -131,7 +131,12 @@ def test_adamw_multi_device_step():
                  for n in sizes]
         for (p, g, m, v, pb), gr in zip(dev, grads):
             g.copy_(torch.from_numpy(gr))
-        F.fp8_adamw_multi(items, step)
+        if t % 2:
+            F.fp8_adamw_multi(items, step)
+        else:  # the advance alone, then the update at that t
+            F.fp8_adamw_multi([], step)
+            F.fp8_adamw_multi(items[:2], step, advance=False)
+            F.fp8_adamw_multi(items[2:], step, advance=False)
         torch.cuda.synchronize()
         assert int(step.item()) == t
         for k, n in enumerate(sizes):
