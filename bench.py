@@ -801,11 +801,39 @@ class GroupGemm:
         dt = time.perf_counter() - t0
         return 2.0 * r * self.n * self.k, dt, "%d of %d activation rows" % (r, self.m)
 
+    def graph_timing(self, flush, hbm, copies=14, steps=7):
+        """Decode-style timing: one CUDA graph of back-to-back calls, each on
+        its own copy of the weights (the copies together exceed L2), replayed
+        after an L2 flush; the mean per call of the GEMM alone and of a
+        quantize + GEMM pair (consecutive layers of a decode step)."""
+        F = self.F
+        wqs = [self.wq.clone() for _ in range(copies)]
+        wss = [self.ws.clone() for _ in range(copies)]
+        gemm = [(lambda i=i: F.fp8_gemm_group(self.aq, self.asc, wqs[i], wss[i], self.sfmt,
+                                              self.y)) for i in range(copies)] * 2
+        quant = lambda: F.fp8_quantize_token_group(self.ad, F.E4M3, self.sfmt, self.aq, self.asc)
+        pairs = []
+        for fn in gemm:
+            pairs += [quant, fn]
+        g_ms = sorted(time_graph(gemm, steps, flush))[steps // 2] / len(gemm)
+        p_ms = sorted(time_graph(pairs, steps, flush))[steps // 2] / len(gemm)
+        del wqs, wss
+        gb = self.gemm_bytes()
+        return {"gemm_us": round(g_ms * 1e3, 2), "gemm_gbs": round(gb / (g_ms / 1e3) / 1e9, 1),
+                "gemm_frac_hbm": round(gb / (g_ms / 1e3) / 1e9 / hbm, 4),
+                "quantize_plus_gemm_us": round(p_ms * 1e3, 2),
+                "how": "CUDA graph of %d back-to-back calls over %d weight copies (%.0f MB, "
+                       "more than L2), L2 flushed before each replay; median of %d replays, "
+                       "per call" % (len(gemm), copies, copies * self.n * self.k / 1e6, steps)}
+
+    def gemm_bytes(self):
+        return self.n * self.k + self.m * self.k + self.m * self.n * 2 + \
+            self.ws.numel() * self.ws.element_size() + self.asc.numel() * self.asc.element_size()
+
     def report(self, per, step, fp8_peak, hbm):
         m, k, n = self.m, self.k, self.n
         flops = 2.0 * m * n * k
-        gb = n * k + m * k + m * n * 2 + self.ws.numel() * self.ws.element_size() + \
-            self.asc.numel() * self.asc.element_size()
+        gb = self.gemm_bytes()
         return {"tflops_incl_quantize": round(flops / (step / 1e3) / 1e12, 2),
                 "gemm_tflops": round(flops / (per["gemm"] / 1e3) / 1e12, 2),
                 "gemm_frac_fp8_peak": round(flops / (per["gemm"] / 1e3) / 1e12 / fp8_peak, 4),
@@ -1047,10 +1075,20 @@ def run_extras(dev, flush, stream, peaks, args):
             wl = GroupGemm(dev, m, sname)
             per, step = time_launches(wl.launches(), 10, flush, stream)
             row = wl.report(per, step, fp8_peak, hbm)
+            if m <= 128:
+                row["graph"] = wl.graph_timing(flush, hbm)
             if not args.no_cpu_baseline:
                 row["cpu_baseline"] = cpu_baseline(wl.oracle_sample, args.cpu_seconds / 2)
             out[wl.name] = row
             del wl
+    # the decode-sized rows between 1 and 128 (the few-row kernel up to 64)
+    few = {}
+    for sname in ("f32", "ue8m0"):
+        for m in (16, 32, 64):
+            wl = GroupGemm(dev, m, sname)
+            few["%s_m%d" % (sname, m)] = wl.graph_timing(flush, hbm)
+            del wl
+    out["group_few_rows_graph"] = few
     for m in (128, 4096):
         wl = GroupGemm32(dev, m)
         per, step = time_launches(wl.launches(), 10, flush, stream)

@@ -424,7 +424,7 @@ def fp8_get_last_device_error(stream=None):
 
 
 (OPT_GEMM_CTA_PAIRS, OPT_WAIT_LIMIT_US, OPT_GEMM_MULTICAST, OPT_GEMM_TMA_STORE,
- OPT_GEMM_FEW_ROWS, OPT_GEMM_BAND_ROWS) = 1, 2, 3, 4, 5, 6
+ OPT_GEMM_FEW_ROWS, OPT_GEMM_BAND_ROWS, OPT_GEMM_SKINNY) = 1, 2, 3, 4, 5, 6, 7
 
 
 def fp8_set_option(option, value):

@@ -66,8 +66,13 @@ bool g_use_multicast = true;
 // measured 69.1 us on the Float8 linear's grouped launch against 70.2-73.3 us
 // through the TMA-store epilogue).
 bool g_use_tma_store = false;
-// CUDA-core path of the per-group GEMM for one to four rows (on by default).
-bool g_use_gemv = true;
+// CUDA-core path of the per-group GEMM for one row (off by default: inside
+// CUDA graphs the few-row tensor-core kernel measured faster, 5.7 against
+// 6.5 us at N 2048, K 7168, as it overlaps its start with the previous
+// kernel; single launches are about equal).
+bool g_use_gemv = false;
+// Few-row tensor-core kernel of the per-group GEMM (on by default).
+bool g_use_skinny = true;
 // 256-row tiles per band of the CTA-pair kernel's tile order.
 int64_t g_pair_band_rows = 8;
 // Bound of every device-side mbarrier wait (fp8_set_option).
@@ -740,6 +745,21 @@ int fp8_gemm_group_bias(const uint8_t *a, const void *sa, const uint8_t *b, cons
     return to_status(
         fp8k::launch_gemv_group(a, sa, b, sb, sfmt, M, N, K, bias, c, (cudaStream_t)stream));
   }
+  if (g_use_skinny && fp8k::gemm_skinny_rows(M) != 0) {
+    // 1-64 rows: the weights stream through the few-row kernel (its tile
+    // is 128 weight rows x the activation rows padded to 16, 32 or 64)
+    DeviceState *d = nullptr;
+    if ((rc = device_state(&d)) != FP8_OK) return rc;
+    args.err = d->err;
+    args.wait_limit_ns = g_wait_limit_ns;
+    args.vec_store = vector_store_ok(c, ldc, FP8_OUT_BF16);
+    args.ksplit = fp8k::gemm_skinny_ksplit(M, N, K, d->sms);
+    CUtensorMap tmw, tmx;
+    if ((rc = encode_operand(&tmw, b, K, N, 128)) != FP8_OK) return rc;
+    if ((rc = encode_operand(&tmx, a, K, M, fp8k::gemm_skinny_rows(M))) != FP8_OK) return rc;
+    return to_status(fp8k::launch_gemm_skinny(sfmt == FP8_SCALE_F32 ? 0 : 1, tmw, tmx, args,
+                                              (cudaStream_t)stream));
+  }
   if (mode == fp8k::kScaleGroupUe8m0 && M > 128) {
     // Beyond one row tile: the UE8M0 scales become E8M0 words (four equal
     // bytes per 128-wide K slice) that the block-scaled GEMM bulk-copies per
@@ -1035,6 +1055,10 @@ int fp8_set_option(int option, int value) {
   }
   if (option == FP8_OPT_GEMM_FEW_ROWS) {
     g_use_gemv = value != 0;
+    return FP8_OK;
+  }
+  if (option == FP8_OPT_GEMM_SKINNY) {
+    g_use_skinny = value != 0;
     return FP8_OK;
   }
   if (option == FP8_OPT_GEMM_TMA_STORE) {

@@ -150,6 +150,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
       : "memory");
 }
 
+// Bring one tensor-map box into L2 (no shared-memory destination, no
+// completion to wait for): a hint that warms the cache for a later load.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel in the stream has
+// finished.  grid_dependency_wait() blocks the calling thread until that
+// kernel has completed and its memory operations are visible (a no-op when
+// there is none); launch_dependents() lets the next such kernel start once
+// every CTA of this one has called it or exited.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // TMA load delivered to the same shared-memory offset in every CTA of the
 // cluster named by `mask`; each destination's mbarrier at `bar`'s offset
 // receives the bytes it got.
@@ -356,6 +378,15 @@ __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t 
         "=r"(r[31])                                                                           \
       : "r"(taddr))
 
+#define FP8K_TMEM_LD_X16(taddr, r)                                                            \
+  asm volatile(                                                                               \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
+      "%14,%15}, [%16];"                                                                      \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),   \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),            \
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                                                 \
+      : "r"(taddr))
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -377,6 +408,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Store four consecutive floats to another CTA's shared memory (16-byte
+// aligned shared::cluster address); made visible to that CTA by a cluster
+// barrier's release / acquire.
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, float a, float b,
+                                                     float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
 
 // arrive on an mbarrier anywhere in the cluster (shared::cluster address)

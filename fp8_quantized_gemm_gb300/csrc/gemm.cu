@@ -147,6 +147,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Programmatic dependent launch: the next kernel may start now; this one
+  // reads nothing a previous kernel may write (the expert offsets, the
+  // operands, the scales) and writes nothing before grid_dependency_wait()
+  // below (the grouped-expert kernels wait here, before their table).
+  launch_dependents();
+  if constexpr (EXPERTS) grid_dependency_wait();
 
   // Persistent tile loop: tile t covers rows (t / tiles_n) * 128 and columns
   // (t % tiles_n) * BN; CTA b takes tiles b, b + gridDim.x, ...  Consecutive
@@ -256,6 +262,19 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   auto unit_tile = [&](int64_t u) { return u % num_tiles; };
   auto kb_begin = [&](int64_t u) { return (int)((u / num_tiles) * KB / ks); };
   auto kb_end = [&](int64_t u) { return (int)((u / num_tiles + 1) * KB / ks); };
+
+  if constexpr (!EXPERTS) {
+    // the first unit's weight boxes into L2 while the previous kernel may
+    // still run (a cache hint: L2 is the device's point of coherence), then
+    // wait for that kernel
+    if (warp == 0 && lane == 0 && MC == 1 && !args.b_mn && u_first < num_units) {
+      const TileInfo ti = tile_info(unit_tile(u_first));
+      const int k0 = kb_begin(u_first), k1 = kb_end(u_first);
+      for (int kb = k0; kb < k1 && kb < k0 + STAGES; ++kb)
+        tma_prefetch_l2_2d(&tmb, kb * C::BK, (int32_t)ti.brow);
+    }
+    grid_dependency_wait();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -746,6 +765,11 @@ static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const Gem
   // (expert-grouped rows: at most one partial row tile per expert more)
   const int64_t row_tiles = (args.M + C::BM - 1) / C::BM + (args.experts > 0 ? args.experts : 0);
   const int64_t units = row_tiles * ((args.N + BN - 1) / BN) * args.ksplit;
+  // programmatic stream serialization: the kernel waits for the previous one
+  // itself (grid_dependency_wait) and may start before it ends
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   if (args.cluster_split || MC == 2) {
     cudaLaunchConfig_t cfg = {};
     unsigned csize = 0;
@@ -764,18 +788,22 @@ static cudaError_t run(const CUtensorMap &tma, const CUtensorMap &tmb, const Gem
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = csize;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tma, tmb, args);
   }
-  const int grid = (int)(units < sms ? units : sms);
-  kern<<<grid, C::kThreads, C::kSmem, st>>>(tma, tmb, args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units < sms ? units : sms));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tma, tmb, args);
 }
 
 // Tile width: 128 for the FP32-promotion mode; 256 for the per-tensor mode

@@ -259,12 +259,19 @@ __global__ void __launch_bounds__(256, 2)
 // 4c..4c+3: group 8w + c of window w) and each lane forms its group's scale
 // once for 32 elements.  Each warp takes kU windows at once (w, w + W, ...,
 // W warps in the grid) and issues all their loads first.
+//
+// Launched with programmatic stream serialization: it lets the next kernel
+// start at once (a GEMM that reads these codes then brings its weights into
+// L2 meanwhile, and waits for this kernel before it reads anything this
+// kernel writes) and waits itself for the kernel before it.
 template <typename T, int F, int GS>
 __global__ void __launch_bounds__(256, 3)
     quant_group_kernel(const T *__restrict__ x, int64_t M, int64_t K, int sfmt,
                        uint8_t *__restrict__ q, void *scales) {
   constexpr int kU = sizeof(T) == 2 ? 2 : 1;
   constexpr int kShift = GS == 128 ? 7 : 5;  // log2 of the group size
+  launch_dependents();
+  grid_dependency_wait();
   const float mx = fmt_max(F);
   const int64_t G = (K + GS - 1) / GS, wins = (K + 1023) / 1024, ntasks = M * wins;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -577,20 +584,38 @@ cudaError_t launch_quant_tensor(const void *x, int in_dt, int64_t rows, int64_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_group(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
-                               int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st) {
+// A launch with programmatic stream serialization (the kernel calls
+// grid_dependency_wait() before it touches memory).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), int blocks, int threads, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename T, int GS>
+static cudaError_t launch_group_kernel(const void *x, int64_t M, int64_t K, int fmt, int sfmt,
+                                       uint8_t *q, void *scales, int sms, cudaStream_t st) {
   // one resident wave (launch bounds: 3 CTAs per SM)
   const int threads = 256, blocks = grid_for(M * ((K + 1023) / 1024) * 32, threads, 3, sms);
-#define FP8K_QG(T, F)                                                                          \
-  quant_group_kernel<T, F, 128><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), M, K, sfmt, \
-                                                            q, scales)
-  if (in_dt == 0) {
-    if (fmt == 0) FP8K_QG(__nv_bfloat16, 0); else FP8K_QG(__nv_bfloat16, 1);
-  } else {
-    if (fmt == 0) FP8K_QG(float, 0); else FP8K_QG(float, 1);
-  }
-#undef FP8K_QG
-  return cudaGetLastError();
+  const T *xt = static_cast<const T *>(x);
+  if (fmt == 0) return launch_pdl(quant_group_kernel<T, 0, GS>, blocks, threads, st, xt, M, K, sfmt, q, scales);
+  return launch_pdl(quant_group_kernel<T, 1, GS>, blocks, threads, st, xt, M, K, sfmt, q, scales);
+}
+
+cudaError_t launch_quant_group(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
+                               int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st) {
+  if (in_dt == 0)
+    return launch_group_kernel<__nv_bfloat16, 128>(x, M, K, fmt, sfmt, q, scales, sms, st);
+  return launch_group_kernel<float, 128>(x, M, K, fmt, sfmt, q, scales, sms, st);
 }
 
 cudaError_t launch_quant_block(const void *w, int in_dt, int64_t N, int64_t K, int fmt,
@@ -736,17 +761,9 @@ cudaError_t launch_quant_block32_f32(const void *w, int in_dt, int64_t N, int64_
 
 cudaError_t launch_quant_group32(const void *x, int in_dt, int64_t M, int64_t K, int fmt,
                                  int sfmt, uint8_t *q, void *scales, int sms, cudaStream_t st) {
-  const int threads = 256, blocks = grid_for(M * ((K + 1023) / 1024) * 32, threads, 3, sms);
-#define FP8K_QG32(T, F)                                                                        \
-  quant_group_kernel<T, F, 32><<<blocks, threads, 0, st>>>(static_cast<const T *>(x), M, K, sfmt, \
-                                                           q, scales)
-  if (in_dt == 0) {
-    if (fmt == 0) FP8K_QG32(__nv_bfloat16, 0); else FP8K_QG32(__nv_bfloat16, 1);
-  } else {
-    if (fmt == 0) FP8K_QG32(float, 0); else FP8K_QG32(float, 1);
-  }
-#undef FP8K_QG32
-  return cudaGetLastError();
+  if (in_dt == 0)
+    return launch_group_kernel<__nv_bfloat16, 32>(x, M, K, fmt, sfmt, q, scales, sms, st);
+  return launch_group_kernel<float, 32>(x, M, K, fmt, sfmt, q, scales, sms, st);
 }
 
 // ------------------------------------------ UE8M0 group scales -> MX words --

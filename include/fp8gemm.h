@@ -621,22 +621,31 @@ FP8_API const char *fp8_version(void);
  *     through shared memory with TMA stores (when c and ldc allow 16-byte
  *     vectors and accumulate is 0); 0 (default) keeps plain per-thread row
  *     stores, which measured faster.  Same bytes.
- *   FP8_OPT_GEMM_FEW_ROWS: 1 (default) runs fp8_gemm_group / _group_bias
- *     with a single activation row on the CUDA cores as a stream over the
- *     weights; 0 keeps it on the tensor cores.  Results agree within the
- *     GEMM bound.
+ *   FP8_OPT_GEMM_FEW_ROWS: 1 runs fp8_gemm_group / _group_bias with a
+ *     single activation row on the CUDA cores as a stream over the weights;
+ *     0 (default) keeps it on the tensor cores (the few-row kernel of
+ *     FP8_OPT_GEMM_SKINNY, which measured faster inside CUDA graphs).
+ *     Results agree within the GEMM bound.
  *   FP8_OPT_GEMM_BAND_ROWS: height, in 256-row tiles, of the bands in which
  *     the CTA-pair per-tensor GEMM walks its output tiles column by column
  *     (1..4096, default 8): taller bands read each B column block from DRAM
  *     fewer times, at the price of a larger A working set in L2.  Same
- *     results. */
+ *     results.
+ *   FP8_OPT_GEMM_SKINNY: 1 (default) runs fp8_gemm_group / _group_bias with
+ *     1 to 64 activation rows (one row only while FP8_OPT_GEMM_FEW_ROWS is
+ *     0) on the few-row tensor-core kernel: 128 weight rows per tile on the
+ *     MMA's M side, the activation rows padded to 16, 32 or 64 on its N
+ *     side, K split over a thread-block cluster, launched so that it may
+ *     start before the previous kernel in the stream ends; 0 keeps them on
+ *     the general per-group kernel.  Results agree within the GEMM bound. */
 typedef enum {
   FP8_OPT_GEMM_CTA_PAIRS = 1,
   FP8_OPT_WAIT_LIMIT_US = 2,
   FP8_OPT_GEMM_MULTICAST = 3,
   FP8_OPT_GEMM_TMA_STORE = 4,
   FP8_OPT_GEMM_FEW_ROWS = 5,
-  FP8_OPT_GEMM_BAND_ROWS = 6
+  FP8_OPT_GEMM_BAND_ROWS = 6,
+  FP8_OPT_GEMM_SKINNY = 7
 } fp8_option_t;
 FP8_API int fp8_set_option(int option, int value);
 

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_options(lib):
     f = lib.fp8_set_option
     f.argtypes = [ctypes.c_int, ctypes.c_int]
-    for opt in (1, 3, 4, 5):  # CTA pairs, multicast, TMA-store epilogue, few rows
+    for opt in (1, 3, 4, 5, 7):  # CTA pairs, multicast, TMA-store epilogue, few rows, skinny
         assert f(opt, 0) == 0 and f(opt, 1) == 0
     assert f(6, 0) == -1 and f(6, 16) == 0 and f(6, 8) == 0  # band rows (1..4096)
     assert f(2, -1) == -1                           # negative wait bound

@@ -80,6 +80,22 @@ def test_timeout_in_group_gemm_resets_split_k_counters():
     assert ok, worst
 
 
+def test_timeout_in_few_row_kernel():
+    """The few-row per-group kernel bounds its waits the same way.  Its K
+    splits meet in a cluster exchange that every CTA still reaches after one
+    of its waits gave up, so the call ends, the timeout is reported, and the
+    next call is correct.  K 65536 over two weight tiles gives each CTA 64 k
+    blocks, so the producer refills its ring many times."""
+    F = lib()
+    qa, sa, qb, sb = group_operands(16, 256, 65536, "f32", seed=3)
+    rc, where = forced_timeout(lambda: run_group(qa, sa, qb, sb, "f32"))
+    assert rc == F.FP8_ERR_TIMEOUT and where in (1, 2, 3), (rc, where)
+    c, e = group_reference(qa, sa, qb, sb, "f32")
+    ok, worst = OG.check(run_group(qa, sa, qb, sb, "f32"), c, e, "bf16")
+    assert ok, worst
+    assert F.fp8_get_last_device_error()[0] == 0
+
+
 def test_timeout_in_multi_tensor_quantize():
     """The cooperative quantize waits on its copies and on the other CTAs'
     amax shares; with the bound at zero one of them runs out, the kernel

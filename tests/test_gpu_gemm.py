@@ -147,11 +147,11 @@ def test_gemm_group(mnk, sfmt):
 @pytest.mark.parametrize("m,k", [(1, 7168), (3, 7168), (1, 20480)])
 @pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
 def test_gemm_group_few_rows(m, k, sfmt):
-    """A single row runs on the CUDA cores (a stream over the weights), more
-    rows and the switch off on the tensor cores.  Ragged N (301: the last
-    block of the one-row kernel holds one valid column), a K with several
-    load steps per lane and a partial last one (20480), a bias, both scale
-    formats."""
+    """With the switch on a single row runs on the CUDA cores (a stream over
+    the weights); more rows, and one row by default, on the few-row
+    tensor-core kernel.  Ragged N (301: the last block of the one-row kernel
+    holds one valid column), a K with several load steps per lane and a
+    partial last one (20480), a bias, both scale formats."""
     F = lib()
     n = 301
     qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=m + 40)
@@ -171,7 +171,7 @@ def test_gemm_group_few_rows(m, k, sfmt):
             ok, worst = OG.check(out.float().cpu().numpy(), cb, eb, "bf16", extra=extra)
             assert ok, (few, worst)
     finally:
-        F.fp8_set_option(F.OPT_GEMM_FEW_ROWS, 1)
+        F.fp8_set_option(F.OPT_GEMM_FEW_ROWS, 0)  # the default
 
 
 @pytest.mark.parametrize("multicast", [0, 1])
@@ -366,6 +366,51 @@ def test_gemm_group_small_m_split_k(m, sfmt):
         got = run_group(qa, sa, qb, sb, sfmt)
         ok, worst = OG.check(got, c, e, "bf16")
         assert ok, worst
+
+
+@pytest.mark.parametrize("mnk", [(2, 300, 1024), (16, 2048, 7168), (17, 1000, 2048),
+                                 (33, 384, 7168), (64, 2048, 7168), (65, 200, 512),
+                                 (128, 2048, 7168), (100, 7168, 2048), (1, 2048, 256)])
+@pytest.mark.parametrize("sfmt", ["f32", "ue8m0"])
+def test_gemm_group_few_rows_kernel(mnk, sfmt):
+    """The few-row per-group kernel (weights on the MMA's M side, the M
+    activation rows padded to 16, 32, 64 or 128 on its N side, K split over
+    a cluster) against the oracle, with the switch on and off: every padded
+    width and its edges, ragged N (the last weight tile partly past N), K
+    shorter than the cluster (one k block per split), a bias and an output
+    pitch wider than N.  Past 64 rows (65, 100, 128) both settings run the
+    general kernel."""
+    F = lib()
+    m, n, k = mnk
+    qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=m + n)
+    c, e = group_reference(qa, sa, qb, sb, sfmt)
+    bias = _bias(n, m + 5)
+    cb, eb, extra = OG.gemm_bias(c, e, bias)
+    sa_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sa).T)).cuda()
+    sb_dev = torch.from_numpy(np.ascontiguousarray(np.asarray(sb))).cuda()
+    code = F.SCALE_F32 if sfmt == "f32" else F.SCALE_UE8M0
+    ldc = n + 24
+    try:
+        F.fp8_set_option(F.OPT_GEMM_FEW_ROWS, 0)
+        for skinny in (1, 0):
+            F.fp8_set_option(F.OPT_GEMM_SKINNY, skinny)
+            for with_bias in (False, True):
+                # (N comes from the weights; the output's row pitch is ldc)
+                buf = torch.full((m, ldc), float("nan"), dtype=torch.bfloat16, device="cuda")
+                F.fp8_gemm_group(dev_u8(qa), sa_dev, dev_u8(qb), sb_dev, code, buf,
+                                 bias=torch.from_numpy(bias).cuda() if with_bias else None)
+                torch.cuda.synchronize()
+                got = buf[:, :n].float().cpu().numpy()
+                if with_bias:
+                    ok, worst = OG.check(got, cb, eb, "bf16", extra=extra)
+                else:
+                    ok, worst = OG.check(got, c, e, "bf16")
+                assert ok, (skinny, with_bias, worst)
+                assert torch.isnan(buf[:, n:].float()).all()  # nothing past N
+        assert F.fp8_get_last_device_error()[0] == 0
+    finally:
+        F.fp8_set_option(F.OPT_GEMM_SKINNY, 1)
+        F.fp8_set_option(F.OPT_GEMM_FEW_ROWS, 0)
 
 
 @pytest.mark.parametrize("mnk", [(1, 2048, 4096), (100, 256, 8192), (33, 1000, 2048)])
