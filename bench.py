@@ -1185,7 +1185,7 @@ PROFILE_WORKLOADS = {
     "two_level_8192": lambda dev: TwoLevel(dev),
     "tiny": lambda dev: TinyPerTensor(dev),
     **{"group_%s_m%d" % (s_, m): (lambda dev, s_=s_, m=m: GroupGemm(dev, m, s_))
-       for s_ in ("f32", "ue8m0") for m in (1, 128, 4096)},
+       for s_ in ("f32", "ue8m0") for m in (1, 16, 64, 128, 4096)},
     **{"moe_%s" % s_: (lambda dev, s_=s_: MoeExperts(dev, s_)) for s_ in ("f32", "ue8m0")},
     **{"group32_f32_m%d" % m: (lambda dev, m=m: GroupGemm32(dev, m)) for m in (128, 4096)},
 }

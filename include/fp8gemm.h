@@ -391,8 +391,14 @@ FP8_API int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int coun
  *   b  [N, K] E4M3 codes, sb [ceil(N/128), K/128] (fp8_quantize_block).
  *   sfmt FP8_SCALE_F32: fp32 scales, partial sums promoted per 128-K group on
  *        the CUDA cores.  FP8_SCALE_UE8M0: byte scales, applied by the tensor
- *        core as block scale factors (no promotion).
+ *        core as block scale factors (no promotion); with 1-64 rows they are
+ *        promoted like fp32 scales (exact powers of two).
  *   K % 128 == 0.  c [M, ldc] bf16 as for fp8_gemm_tensor.
+ *   With 1-64 rows the call runs the few-row kernel (FP8_OPT_GEMM_SKINNY),
+ *   launched with programmatic stream serialization: it may start before the
+ *   previous kernel on `stream` ends, and then reads and writes nothing that
+ *   kernel may write until it has completed.  Every per-group GEMM launch and
+ *   fp8_quantize_token_group (/32) are launched that way.
  */
 FP8_API int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
                    int sfmt, int64_t M, int64_t N, int64_t K, void *c, int64_t ldc,
@@ -403,9 +409,10 @@ FP8_API int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, c
  * arguments, same definition, same bound) for callers that cannot allocate
  * device memory.  The pages have no counterpart to this entry point; it
  * exists for this library's users.  Its result agrees with fp8_gemm_group's
- * within the GEMM bound, not bit for bit: it always runs the tensor-core
- * per-group kernel, while fp8_gemm_group takes the CUDA-core path for one
- * row and converts UE8M0 scales to block-scale words for M > 128.
+ * within the GEMM bound, not bit for bit: it always runs the general
+ * tensor-core per-group kernel, while fp8_gemm_group runs 1-64 rows on its
+ * few-row kernel and converts UE8M0 scales to block-scale words for
+ * M > 128.
  *
  * Why: fp8_gemm_group allocates device memory on first use for some shapes
  * (the E8M0-word buffer of UE8M0 scales at M > 128).  Some callers cannot
