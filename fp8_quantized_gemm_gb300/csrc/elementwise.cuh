@@ -1,8 +1,8 @@
 // Element-wise arithmetic of the training step that runs both in standalone
 // kernels (support.cu) and inside GEMM epilogues (gemm_pair.cu): SwiGLU
 // forward / backward and the AdamW update.  Every operation is an explicitly
-// rounded intrinsic (no contraction left to the compiler), so each value is
-// the same wherever it is computed.
+// rounded intrinsic or a single hardware instruction (no contraction left to
+// the compiler), so each value is the same wherever it is computed.
 #pragma once
 
 #include "common.cuh"
@@ -11,11 +11,20 @@
 namespace fp8k {
 
 // logistic function 1 / (1 + e^-z): the hardware exponential (__expf, a
-// few fp32 ulps from e^-z) and the correctly rounded reciprocal.  The
-// SwiGLU values it feeds are rounded to bf16 (8 significant bits), far
-// coarser than that error.
+// few fp32 ulps from e^-z) and the hardware reciprocal (rcp.approx, one
+// instruction, within an fp32 ulp or so; subnormal results kept; 1 / inf =
+// 0 for very negative z).  The SwiGLU values it feeds are rounded to bf16
+// (8 significant bits), far coarser than either error.  (The correctly
+// rounded reciprocal is a sequence of several instructions; the gated
+// SwiGLU epilogue of the forward GEMM measured its arithmetic as the
+// launch's limiter.)
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 __device__ __forceinline__ float sigmoidf_(float z) {
-  return __frcp_rn(__fadd_rn(1.0f, __expf(-z)));
+  return rcp_approx(__fadd_rn(1.0f, __expf(-z)));
 }
 
 // a = silu(h) * u = (h * s(h)) * u
