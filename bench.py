@@ -289,13 +289,15 @@ class SwiGLUStep:
     # kernels each step launches: quantize x, W1, W3, W2, dy (5); GEMMs: the
     # gated h|u launch (its epilogue writes a's codes), y, da|dW2, dx|dW1|dW3
     # and the accumulating dx += du W3 (5); the fused SwiGLU-backward +
-    # quantize pass (1); AdamW (step advance + update: 2); nine amax-history
-    # updates (9).  The amax clears are memsets, not kernels.
-    kernels_per_step = 22
+    # quantize pass (1); AdamW (step advance + update: 2); the nine
+    # amax-history updates in one launch (1).  The amax clears are memsets,
+    # not kernels.
+    kernels_per_step = 14
     CALL_LABELS = {"fp8_gemm_tensor_grouped": "gemm", "fp8_quantize_tensor": "quantize",
                    "fp8_swiglu_forward_quantize": "swiglu_quantize",
                    "fp8_swiglu_backward_quantize": "swiglu_quantize",
-                   "fp8_adamw_multi": "adamw", "fp8_delayed_state_update": "state_update"}
+                   "fp8_adamw_multi": "adamw", "fp8_delayed_state_update": "state_update",
+                   "fp8_delayed_state_update_multi": "state_update"}
 
     def __init__(self, dev, n_dy=16, tokens=16384, d=4096, ffn=14336, weight_scaling="delayed"):
         from fp8_quantized_gemm_gb300.mlp import SwiGLUTrainer

@@ -56,6 +56,7 @@ _SIGS = {
     "fp8_gemm_mx": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _i64, _vp],
     "fp8_gemm_group_noalloc": [_vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp, _i64, _vp],
     "fp8_delayed_state_update": [_vp, _vp, _vp, _i64, _int, _vp],
+    "fp8_delayed_state_update_multi": [_vp, _int, _vp],
     "fp8_auto_weight_scale": [_vp, _i64, _d, _int, _vp, _vp],
     "fp8_swiglu_forward": [_vp, _vp, _vp, _i64, _vp],
     "fp8_swiglu_backward": [_vp, _vp, _vp, _vp, _vp, _i64, _vp],
@@ -356,6 +357,23 @@ def fp8_gemm_mx_rows(a, la, ga, b, lb, gb, out, *, out_dt=None, stream=None):
 
 def fp8_delayed_state_update(hist, scale, amax_cur, fmt, stream=None):
     _call("fp8_delayed_state_update", _p(hist), _p(scale), _p(amax_cur), hist.numel(), fmt,
+          _stream(stream))
+
+
+class DelayedItem(ctypes.Structure):
+    """fp8_delayed_item_t (include/fp8gemm.h)."""
+    _fields_ = [("hist", _vp), ("scale", _vp), ("amax_cur", _vp), ("L", ctypes.c_int64),
+                ("fmt", _int)]
+
+
+def delayed_item(hist, scale, amax_cur, fmt):
+    return DelayedItem(_p(hist), _p(scale), _p(amax_cur), hist.numel(), fmt)
+
+
+def fp8_delayed_state_update_multi(items, stream=None):
+    """Several amax-history steps in one launch (items from delayed_item)."""
+    arr = (DelayedItem * len(items))(*items)
+    _call("fp8_delayed_state_update_multi", ctypes.cast(arr, ctypes.c_void_p), len(items),
           _stream(stream))
 
 

@@ -886,6 +886,38 @@ int fp8_delayed_state_update(float *hist, float *scale, const float *amax_cur, i
   return to_status(fp8k::launch_delayed_update(hist, scale, amax_cur, L, fmt, (cudaStream_t)stream));
 }
 
+int fp8_delayed_state_update_multi(const fp8_delayed_item_t *items, int count,
+                                   fp8_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
+  if (items == nullptr || count < 1 || count > fp8k::kMaxDelayed) return FP8_ERR_INVALID_ARG;
+  fp8k::DelayedItems it{};
+  for (int i = 0; i < count; ++i) {
+    const fp8_delayed_item_t &d = items[i];
+    if (d.hist == nullptr || d.scale == nullptr || d.amax_cur == nullptr || !valid_fmt(d.fmt))
+      return FP8_ERR_INVALID_ARG;
+    if (d.L < 1 || d.L > 32768) return FP8_ERR_INVALID_ARG;
+    // no two items write the same memory (their updates run concurrently)
+    for (int j = 0; j < i; ++j) {
+      const fp8_delayed_item_t &e = items[j];
+      const bool hist_overlap = d.hist < e.hist + e.L && e.hist < d.hist + d.L;
+      const bool scale_in_hist = (d.scale >= e.hist && d.scale < e.hist + e.L) ||
+                                 (e.scale >= d.hist && e.scale < d.hist + d.L);
+      if (hist_overlap || scale_in_hist || d.scale == e.scale) return FP8_ERR_INVALID_ARG;
+    }
+    if (d.scale >= d.hist && d.scale < d.hist + d.L) return FP8_ERR_INVALID_ARG;
+    it.hist[i] = d.hist;
+    it.scale[i] = d.scale;
+    it.amax_cur[i] = d.amax_cur;
+    it.L[i] = d.L;
+    it.fmt[i] = d.fmt;
+  }
+  it.count = count;
+  DeviceState *dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc != FP8_OK) return rc;
+  return to_status(fp8k::launch_delayed_update_multi(it, (cudaStream_t)stream));
+}
+
 int fp8_auto_weight_scale(const float *amax0, int64_t t, double lr, int fmt, float *scale_out,
                           fp8_stream_t stream) {
   const NvtxRange nvtx_range(__func__);

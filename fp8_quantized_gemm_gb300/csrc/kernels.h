@@ -58,6 +58,17 @@ cudaError_t launch_auto_scale(const float *amax0, double grow, int fmt, float *s
                               cudaStream_t st);
 cudaError_t launch_delayed_update(float *hist, float *scale, const float *amax_cur, int64_t L,
                                   int fmt, cudaStream_t st);
+// Up to kMaxDelayed amax-history steps in one launch (one CTA each).
+constexpr int kMaxDelayed = 16;
+struct DelayedItems {
+  float *hist[kMaxDelayed];
+  float *scale[kMaxDelayed];
+  const float *amax_cur[kMaxDelayed];
+  int64_t L[kMaxDelayed];
+  int fmt[kMaxDelayed];
+  int count;
+};
+cudaError_t launch_delayed_update_multi(const DelayedItems &items, cudaStream_t st);
 
 // Current scaling of up to kMaxMulti tensors in one cooperative launch
 // (quantize_multi.cu).  `sync` is device scratch of 2 * kMaxMulti uint32

@@ -504,9 +504,11 @@ __global__ void __launch_bounds__(256, 3)
 // One CTA: roll the history by -1, write the new amax at index 0, then take
 // max(history) (NaN propagates, as a max over the array does) and update the
 // scale when it is positive and finite.
-__global__ void __launch_bounds__(1024)
-    delayed_update_kernel(float *hist, float *scale, const float *amax_cur, int64_t L, int fmt) {
-  extern __shared__ float old[];
+// One amax-history step (the body of both launches): `old` is L floats of
+// shared memory; every thread of the CTA takes part.
+__device__ __forceinline__ void delayed_update_one(float *hist, float *scale,
+                                                   const float *amax_cur, int64_t L, int fmt,
+                                                   float *old) {
   __shared__ uint32_t red_key[32];
   __shared__ int red_nan[32];
   for (int64_t i = threadIdx.x; i < L; i += blockDim.x) old[i] = hist[i];
@@ -539,6 +541,21 @@ __global__ void __launch_bounds__(1024)
       if (!nn && m > 0.0f && m <= 3.402823466e38f) *scale = __fdiv_rn(m, fmt_max(fmt));
     }
   }
+}
+
+__global__ void __launch_bounds__(1024)
+    delayed_update_kernel(float *hist, float *scale, const float *amax_cur, int64_t L, int fmt) {
+  extern __shared__ float old[];
+  delayed_update_one(hist, scale, amax_cur, L, fmt, old);
+}
+
+// Several histories in one launch, one CTA each.
+__global__ void __launch_bounds__(1024)
+    delayed_update_multi_kernel(const __grid_constant__ DelayedItems items) {
+  extern __shared__ float old[];
+  const int b = (int)blockIdx.x;
+  delayed_update_one(items.hist[b], items.scale[b], items.amax_cur[b], items.L[b], items.fmt[b],
+                     old);
 }
 
 // ----------------------------------------------------------- launchers --
@@ -1021,6 +1038,20 @@ cudaError_t launch_delayed_update(float *hist, float *scale, const float *amax_c
     if (e != cudaSuccess) return e;
   }
   delayed_update_kernel<<<1, 1024, smem, st>>>(hist, scale, amax_cur, L, fmt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_delayed_update_multi(const DelayedItems &items, cudaStream_t st) {
+  if (items.count < 1 || items.count > kMaxDelayed) return cudaErrorInvalidValue;
+  int64_t lmax = 1;
+  for (int i = 0; i < items.count; ++i) lmax = items.L[i] > lmax ? items.L[i] : lmax;
+  const size_t smem = (size_t)lmax * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(delayed_update_multi_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  delayed_update_multi_kernel<<<items.count, 1024, smem, st>>>(items);
   return cudaGetLastError();
 }
 

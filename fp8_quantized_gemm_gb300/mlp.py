@@ -215,12 +215,14 @@ class SwiGLUTrainer:
             self.t_since += 1
             if self.t_since >= self.rescale_interval:
                 self.refresh_weight_amax()
+        items = []
         for i in range(9):
             if auto and i in (K1, K3, K2):
                 continue  # weights follow eq. (10), not a history
             cur = X1 if i == X3 else i  # the x@W3 input state takes x's amax
             fmt = F.E5M2 if i in (G1, G3, G2) else F.E4M3
-            F.fp8_delayed_state_update(self.hist[i], self.scale[i:i + 1], self._am(cur), fmt)
+            items.append(F.delayed_item(self.hist[i], self.scale[i:i + 1], self._am(cur), fmt))
+        F.fp8_delayed_state_update_multi(items)  # the histories in one launch
 
     def step(self, x: torch.Tensor, dy: torch.Tensor):
         self.forward_backward(x, dy)

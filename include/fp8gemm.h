@@ -512,6 +512,23 @@ FP8_API int fp8_gemm_mx(const uint8_t *a, const uint32_t *la, const float *ga, c
 FP8_API int fp8_delayed_state_update(float *hist, float *scale, const float *amax_cur, int64_t L,
                              int fmt, fp8_stream_t stream);
 
+/* fp8_delayed_state_update_multi: the step above for `count` (1..16)
+ * independent histories in one launch (a training step keeps one per GEMM
+ * operand).  Each item's hist, scale, amax_cur, L and fmt mean what the
+ * arguments of fp8_delayed_state_update mean, with the same checks.  The
+ * items' hist ranges and scale words must not overlap each other
+ * (INVALID_ARG); an item's amax_cur may be another item's (it is only
+ * read).  The same results as `count` calls of fp8_delayed_state_update. */
+typedef struct {
+  float *hist;            /* [L] fp32, element 0 newest */
+  float *scale;           /* [1] fp32 */
+  const float *amax_cur;  /* [1] fp32 */
+  int64_t L;              /* 1 .. 32768 */
+  int fmt;                /* FP8_E4M3 / FP8_E5M2 */
+} fp8_delayed_item_t;
+FP8_API int fp8_delayed_state_update_multi(const fp8_delayed_item_t *items, int count,
+                                           fp8_stream_t stream);
+
 /* ------------------------------------------- automatic weight scaling --
  * fp8_auto_weight_scale: MOSS automatic scaling ([MOSS] 5, eq. 10): the scale
  * of a weight t optimizer steps after its last max-reduction is predicted,

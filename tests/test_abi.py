@@ -208,3 +208,32 @@ def test_gemm_group_experts_validation(lib):
     assert call(ldc=100) == -1
     if not torch.cuda.is_available():
         assert call() == -6
+
+
+def test_delayed_state_update_multi_validation(lib):
+    """Batched amax-history steps: item count 1..16, the single call's checks
+    per item, and no two items writing the same memory."""
+    import torch
+    import fp8_quantized_gemm_gb300 as F
+    f = lib.fp8_delayed_state_update_multi
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+
+    def call(items):
+        arr = (F.DelayedItem * max(len(items), 1))(*items)
+        return f(ctypes.cast(arr, ctypes.c_void_p), len(items), None)
+
+    ok = lambda h, s, L=1024, fmt=0: F.DelayedItem(h, s, 64, L, fmt)
+    assert call([]) == -1                                   # no items
+    assert call([ok(4096 * (i + 1), 16 + 16 * i) for i in range(17)]) == -1  # more than 16
+    assert call([F.DelayedItem(None, 16, 64, 1024, 0)]) == -1
+    assert call([F.DelayedItem(4096, 16, None, 1024, 0)]) == -1
+    assert call([ok(4096, 16, L=0)]) == -1
+    assert call([ok(4096, 16, L=32769)]) == -1
+    assert call([ok(4096, 16, fmt=2)]) == -1
+    assert call([ok(4096, 16), ok(4096 + 4 * 1000, 20)]) == -1  # histories overlap
+    assert call([ok(4096, 16), ok(16384, 16)]) == -1              # one scale word twice
+    assert call([ok(4096, 4096 + 8)]) == -1                       # scale inside a history
+    assert call([ok(4096, 16), ok(16384, 4096 + 8)]) == -1        # ... of another item
+    if not torch.cuda.is_available():
+        # disjoint items, one amax shared: valid (reaches the device check)
+        assert call([ok(4096, 16), ok(16384, 20)]) == -6

@@ -190,6 +190,39 @@ def test_delayed_scaling_sequence(length):
         assert np.array_equal(hist.cpu().numpy().view(np.uint32), st.history.view(np.uint32)), t
 
 
+def test_delayed_state_update_multi_matches_the_oracle():
+    """Nine histories (different lengths, both formats, one amax shared by
+    two items, a zero and a NaN amax) in one launch over 12 steps: every
+    history and scale bit-exact against the oracle's in_q order."""
+    F = lib()
+    lengths = [1024, 1024, 16, 1, 1024, 300, 1024, 7, 1024]
+    fmts = ["e4m3", "e4m3", "e5m2", "e4m3", "e5m2", "e5m2", "e4m3", "e5m2", "e4m3"]
+    code = {"e4m3": F.E4M3, "e5m2": F.E5M2}
+    hist = [torch.zeros(n, device="cuda") for n in lengths]
+    scale = torch.ones(len(lengths), device="cuda")
+    amax = torch.zeros(len(lengths), device="cuda")
+    src = [i if i != 1 else 0 for i in range(len(lengths))]  # item 1 reads item 0's amax
+    states = [OD.DelayedState.initial(n) for n in lengths]
+    items = [F.delayed_item(hist[i], scale[i:i + 1], amax[src[i]:src[i] + 1], code[fmts[i]])
+             for i in range(len(lengths))]
+    rng = np.random.default_rng(9)
+    for t in range(12):
+        cur = (rng.random(len(lengths)) * 10.0 ** rng.integers(-3, 4, len(lengths))).astype(np.float32)
+        cur[2] = 0.0 if t == 3 else cur[2]
+        cur[5] = np.nan if t == 5 else cur[5]
+        amax.copy_(torch.from_numpy(cur))
+        F.fp8_delayed_state_update_multi(items)
+        torch.cuda.synchronize()
+        for i, st in enumerate(states):
+            # the push, then the scale the next step uses (the order in which
+            # the oracle's in_q meets them)
+            h = OD.compute_amax_history(np.float32(cur[src[i]]), st.history)
+            states[i] = OD.DelayedState(h, OD.compute_scale(np.max(h), st.scale, fmts[i]))
+            assert np.array_equal(hist[i].cpu().numpy().view(np.uint32),
+                                  states[i].history.view(np.uint32)), (t, i)
+            assert f32_bits(scale[i].item()) == f32_bits(states[i].scale), (t, i)
+
+
 def test_delayed_update_keeps_scale_on_nonfinite():
     F = lib()
     hist = torch.zeros(8, device="cuda")
