@@ -704,6 +704,7 @@ class TinyPerTensor:
         self.qa, self.qb = torch.empty((16, 32), **u8), torch.empty((64, 32), **u8)
         self.am, self.bm, self.sa, self.sb = (torch.empty(1, device=dev) for _ in range(4))
         self.out = torch.empty((16, 64), dtype=torch.float32, device=dev)
+        self.sync = torch.zeros(F.QUANT_SYNC_WORDS, dtype=torch.int32, device=dev)
 
     def launches(self):
         F = self.F
@@ -713,6 +714,16 @@ class TinyPerTensor:
                                                            amax_in=self.am, scale_out=self.sa)),
                 ("quantize", lambda: F.fp8_quantize_tensor(self.bt, F.E4M3, self.qb,
                                                            amax_in=self.bm, scale_out=self.sb)),
+                ("gemm", lambda: F.fp8_gemm_tensor(self.qa, F.E4M3, self.qb, F.E4M3, self.sa,
+                                                   self.sb, self.out))]
+
+    def launches_fused(self):
+        """The same example with both operands' current scaling (amax, scale,
+        codes) in one launch."""
+        F = self.F
+        items = [F.quant_item(self.a, F.E4M3, self.qa, self.sa),
+                 F.quant_item(self.bt, F.E4M3, self.qb, self.sb)]
+        return [("quantize", lambda: F.fp8_quantize_tensors(items, self.sync)),
                 ("gemm", lambda: F.fp8_gemm_tensor(self.qa, F.E4M3, self.qb, F.E4M3, self.sa,
                                                    self.sb, self.out))]
 
@@ -730,9 +741,13 @@ def tiny_row(dev, flush, stream, args):
     wl = TinyPerTensor(dev)
     graph_ms = time_graph([fn for _, fn in wl.launches()], 200, flush)
     per, _ = time_launches(wl.launches(), 20, flush, stream)
+    fused_ms = time_graph([fn for _, fn in wl.launches_fused()], 200, flush)
     row = {"us_per_example": round(statistics.median(graph_ms) * 1e3, 2),
            "launch": "CUDA graph of the five API calls (2 amax, 2 quantize, 1 GEMM), median "
                      "of 200 replays after an L2 flush",
+           "us_per_example_two_calls": round(statistics.median(fused_ms) * 1e3, 2),
+           "two_calls": "CUDA graph of fp8_quantize_tensors (amax, scale and codes of both "
+                        "operands in one launch) and the GEMM, median of 200 replays",
            "eager_us_per_call": {k: round(v * 1e3, 2) for k, v in per.items()},
            "flop": 65536}
     if not args.no_cpu_baseline:
