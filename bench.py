@@ -286,13 +286,14 @@ class SwiGLUStep:
     16384 tokens): forward, backward, AdamW and the nine history updates."""
 
     name = "swiglu_training_delayed_d4096_ffn14336_t16384"
-    # kernels each step launches: quantize x, W1, W3, W2, dy (5); GEMMs: the
-    # gated h|u launch (its epilogue writes a's codes), y, da|dW2, dx|dW1|dW3
-    # and the accumulating dx += du W3 (5); the fused SwiGLU-backward +
-    # quantize pass (1); AdamW (step advance + update: 2); the nine
-    # amax-history updates in one launch (1).  The amax clears are memsets,
+    # kernels each step launches: quantize x, dy (2; the weights' codes come
+    # from the previous step's AdamW); GEMMs: the gated h|u launch (its
+    # epilogue writes a's codes), y, da|dW2, dx|dW1|dW3 and the accumulating
+    # dx += du W3 (5); the fused SwiGLU-backward + quantize pass (1); the nine
+    # amax-history updates in one launch (1); AdamW with the next step's
+    # weight codes (step advance + update: 2).  The amax clears are memsets,
     # not kernels.
-    kernels_per_step = 14
+    kernels_per_step = 11
     CALL_LABELS = {"fp8_gemm_tensor_grouped": "gemm", "fp8_quantize_tensor": "quantize",
                    "fp8_swiglu_forward_quantize": "swiglu_quantize",
                    "fp8_swiglu_backward_quantize": "swiglu_quantize",
@@ -466,7 +467,7 @@ def run_headline(args, dev, peaks):
     src = "MEASURED_PEAKS.json (%s)" % peaks["source"]
     T, d, ffn = wl.T, wl.d, wl.ffn
     # algorithmic HBM bytes of the standalone passes per step
-    qbytes = 3.0 * (2 * T * d + 3 * ffn * d)                 # x, dy, W1, W3, W2: 2 B in, 1 B out
+    qbytes = 3.0 * (2 * T * d)                               # x, dy: 2 B in, 1 B out
     sbytes = (3 * 2 + 2 * 1.0) * T * ffn                     # SwiGLU backward: da, h, u -> dh, du codes
     line = {
         "metric": METRIC,
@@ -501,13 +502,13 @@ def run_headline(args, dev, peaks):
         "passes_gbs": {
             "quantize": round(qbytes / (per["quantize"] / 1e3) / 1e9, 1),
             "swiglu_quantize": round(sbytes / (per["swiglu_quantize"] / 1e3) / 1e9, 1),
-            "adamw": round(30.0 * 3 * ffn * d / (per["adamw"] / 1e3) / 1e9, 1),
+            "adamw": round(31.0 * 3 * ffn * d / (per["adamw"] / 1e3) / 1e9, 1),
             "hbm_peak": peaks["hbm_gbs"],
-            "note": "algorithmic bytes of the standalone passes: quantize x, dy, W1, W3, W2 "
-                    "(2 B read, 1 B codes); the SwiGLU backward reads da, h, u and writes the "
-                    "codes of dh and du; AdamW 30 B per weight (p, m, v read and written, dW "
-                    "read, bf16 copy written).  The SwiGLU forward runs in the gated h|u "
-                    "GEMM's epilogue and is inside 'gemm'"},
+            "note": "algorithmic bytes of the standalone passes: quantize x, dy (2 B read, "
+                    "1 B codes); the SwiGLU backward reads da, h, u and writes the codes of dh "
+                    "and du; AdamW 31 B per weight (p, m, v read and written, dW read, bf16 "
+                    "copy and the next step's FP8 code written).  The SwiGLU forward runs in "
+                    "the gated h|u GEMM's epilogue and is inside 'gemm'"},
         "clocks": clk.summary(),
         "gpu_launches": wl.kernels_per_step * args.steps,
     }

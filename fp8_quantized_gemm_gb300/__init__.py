@@ -414,12 +414,17 @@ def fp8_swiglu_backward_quantize(da, h, u, fmt, scale_dh, scale_du, q_dh, q_du, 
 
 class AdamwItem(ctypes.Structure):
     """fp8_adamw_item_t (include/fp8gemm.h)."""
-    _fields_ = [("p", _vp), ("g", _vp), ("m", _vp), ("v", _vp), ("p_bf16", _vp), ("n", _i64)]
+    _fields_ = [("p", _vp), ("g", _vp), ("m", _vp), ("v", _vp), ("p_bf16", _vp), ("n", _i64),
+                ("q", _vp), ("q_scale", _vp), ("q_amax", _vp), ("q_fmt", _int)]
 
 
-def adamw_item(p, g, m, v, p_bf16=None):
+def adamw_item(p, g, m, v, p_bf16=None, *, q=None, q_scale=None, q_amax=None, q_fmt=E4M3):
+    """One tensor of fp8_adamw_multi; with q, also the codes of the updated
+    weights (as bf16) under q_scale and their amax (q_amax, nullable)."""
     assert p.numel() == g.numel() == m.numel() == v.numel()
-    return AdamwItem(_p(p), _p(g), _p(m), _p(v), _p(p_bf16), p.numel())
+    assert q is None or q.numel() == p.numel()
+    return AdamwItem(_p(p), _p(g), _p(m), _p(v), _p(p_bf16), p.numel(), _p(q), _p(q_scale),
+                     _p(q_amax), q_fmt)
 
 
 def fp8_adamw_multi(items, step, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,

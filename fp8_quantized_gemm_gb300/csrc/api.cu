@@ -1018,6 +1018,20 @@ int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step, int
                      !aligned16(it.v) ||
                      (it.p_bf16 != nullptr && (reinterpret_cast<uintptr_t>(it.p_bf16) & 7u) != 0)))
       return FP8_ERR_MISALIGNED;
+    if (it.q != nullptr) {
+      if (it.q_scale == nullptr || !valid_fmt(it.q_fmt)) return FP8_ERR_INVALID_ARG;
+      if (it.q_amax != nullptr && reinterpret_cast<const void *>(it.q_amax) ==
+                                      reinterpret_cast<const void *>(it.q_scale))
+        return FP8_ERR_INVALID_ARG;
+      for (int j = 0; j < k; ++j)
+        if (it.q_amax != nullptr && items[j].q != nullptr && items[j].q_amax == it.q_amax)
+          return FP8_ERR_INVALID_ARG;
+      if ((reinterpret_cast<uintptr_t>(it.q) & 3u) != 0) return FP8_ERR_MISALIGNED;
+      a.q[k] = it.q;
+      a.q_scale[k] = it.q_scale;
+      a.q_amax[k] = reinterpret_cast<uint32_t *>(it.q_amax);
+      a.q_fmt[k] = it.q_fmt;
+    }
     a.p[k] = it.p;
     a.g[k] = it.g;
     a.m[k] = it.m;

@@ -217,10 +217,25 @@ __global__ void __launch_bounds__(512)
 // captured training step advances it on every replay.
 __global__ void adamw_advance_step_kernel(int64_t *step) { *step += 1; }
 
+// Four codes (little-endian in a word) of four bf16 values held as fp32,
+// divided by d.s (correctly rounded quotient; IEEE division for scales
+// outside the fast range) and cast with saturation: the arithmetic of
+// fp8_quantize_tensor with a given scale.
+template <bool kFast>
+__device__ __forceinline__ uint32_t codes4(const float (&b)[4], const ScaleDiv &d, int fmt) {
+  const float y0 = d.div<kFast>(b[0]), y1 = d.div<kFast>(b[1]);
+  const float y2 = d.div<kFast>(b[2]), y3 = d.div<kFast>(b[3]);
+  const uint32_t lo = cvt_fp8x2(fmt, y0, y1), hi = cvt_fp8x2(fmt, y2, y3);
+  return __byte_perm(lo, hi, 0x5410);
+}
+
 // One launch over every parameter tensor; the bias corrections 1 - beta^t
-// are formed in double from the device step counter, once per block.
+// are formed in double from the device step counter, once per block.  An
+// item with codes also quantizes its updated weights (as bf16) with its
+// delayed scale and records their amax.
 __global__ void __launch_bounds__(512) adamw_multi_kernel(const __grid_constant__ AdamwMulti a) {
   __shared__ float bc[2];
+  __shared__ uint32_t red[16];
   if (threadIdx.x == 0) {
     const int64_t t = *a.step;
     bc[0] = bias_correction(a.b1d, t);
@@ -237,7 +252,23 @@ __global__ void __launch_bounds__(512) adamw_multi_kernel(const __grid_constant_
     float4 *__restrict__ m = reinterpret_cast<float4 *>(a.m[k]);
     float4 *__restrict__ v = reinterpret_cast<float4 *>(a.v[k]);
     uint2 *__restrict__ pb = reinterpret_cast<uint2 *>(a.pb[k]);
+    uint32_t *__restrict__ q = reinterpret_cast<uint32_t *>(a.q[k]);
     const int64_t nvec = a.n[k] / 4;
+    if (q == nullptr) {
+      for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        float4 pv = p[i], mv = m[i], vv = v[i];
+        const float4 gv = __ldcs(g + i);
+        adamw4(pv, mv, vv, gv, hp);
+        p[i] = pv;
+        m[i] = mv;
+        v[i] = vv;
+        if (pb != nullptr) pb[i] = f32x4_to_bf16(pv);
+      }
+      continue;
+    }
+    const ScaleDiv d(*a.q_scale[k]);
+    const int fmt = a.q_fmt[k];
+    uint32_t key = 0;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
       float4 pv = p[i], mv = m[i], vv = v[i];
       const float4 gv = __ldcs(g + i);
@@ -245,7 +276,24 @@ __global__ void __launch_bounds__(512) adamw_multi_kernel(const __grid_constant_
       p[i] = pv;
       m[i] = mv;
       v[i] = vv;
-      if (pb != nullptr) pb[i] = f32x4_to_bf16(pv);
+      const uint2 w = f32x4_to_bf16(pv);
+      if (pb != nullptr) pb[i] = w;
+      const float b[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                          __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) key = max(key, abs_key(b[j]));
+      q[i] = d.fast ? codes4<true>(b, d, fmt) : codes4<false>(b, d, fmt);
+    }
+    if (a.q_amax[k] != nullptr) {  // the block's max, then one atomicMax
+      key = warp_max_u32(key);
+      if (lane_id() == 0) red[threadIdx.x >> 5] = key;
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        uint32_t kk = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0u;
+        kk = warp_max_u32(kk);
+        if (threadIdx.x == 0 && kk != 0u) atomicMax(a.q_amax[k], kk);
+      }
+      __syncthreads();  // red is rewritten by the next item
     }
   }
 }
@@ -367,7 +415,10 @@ cudaError_t launch_adamw_multi(AdamwMulti a, bool advance, double lr, double b1,
   int64_t most = 0;
   for (int k = 0; k < a.count; ++k) most = a.n[k] > most ? a.n[k] : most;
   cudaError_t e = cudaSuccess;
-  if (advance) {
+  for (int k = 0; k < a.count && e == cudaSuccess; ++k)
+    if (a.q[k] != nullptr && a.q_amax[k] != nullptr)
+      e = cudaMemsetAsync(a.q_amax[k], 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess && advance) {
     adamw_advance_step_kernel<<<1, 1, 0, st>>>(a.step);
     e = cudaGetLastError();
   }

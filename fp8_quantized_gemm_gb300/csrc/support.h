@@ -35,6 +35,12 @@ struct AdamwMulti {
   float *v[kMaxAdamw];
   void *pb[kMaxAdamw];  // nullable bf16 copies
   int64_t n[kMaxAdamw];
+  // nullable: codes of bf16(p) under q_scale[0] (format q_fmt) and their
+  // amax (nullable; cleared by the launcher), the next step's quantization
+  uint8_t *q[kMaxAdamw];
+  const float *q_scale[kMaxAdamw];
+  uint32_t *q_amax[kMaxAdamw];
+  int q_fmt[kMaxAdamw];
   int count;
   int64_t *step;        // device: read as t (incremented first when advancing)
   AdamwHp hp;           // set by the launcher (bias corrections: in the kernel)

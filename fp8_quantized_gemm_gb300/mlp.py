@@ -44,6 +44,14 @@ optimizer keeps its step count on the device, so `step` issues the same
 calls every time and can be captured as a CUDA graph (the second stream
 forks from and joins the capturing one) and replayed.
 
+With delayed weight scaling and the standalone update (the defaults), the
+next step's weight quantization also moves into the optimizer: the amax
+histories are pushed first, which fixes the scales the next step quantizes
+the weights with, and fp8_adamw_multi then writes the codes of the updated
+weights (as bf16) under those scales and their amaxes -- what the next
+step's fp8_quantize_tensor calls on the bf16 copies would give -- so from
+the second step on the forward quantizes only x.
+
 Buffers are allocated once (device memory through torch); `step` issues the
 calls on the current stream.
 """
@@ -74,6 +82,10 @@ class SwiGLUTrainer:
         self.overlap = overlap_optimizer and not fuse_optimizer
         self.side = torch.cuda.Stream(device=w1.device) if self.overlap else None
         self.rescale_interval = rescale_interval
+        # the optimizer writes the next step's weight codes (see the module
+        # docstring); until the first update the forward quantizes them
+        self.fuse_wq = weight_scaling == "delayed" and not fuse_optimizer and not self.overlap
+        self.w_codes_ready = False
         dev = w1.device
         ffn, d = w1.shape
         assert w3.shape == (ffn, d) and w2.shape == (d, ffn)
@@ -117,8 +129,13 @@ class SwiGLUTrainer:
             self.dw = [torch.empty((ffn, d), **f32), torch.empty((ffn, d), **f32),
                        torch.empty((d, ffn), **f32)]
             self.adamw_ep = [None, None, None]
-            self.adamw_items = [F.adamw_item(self.w_master[i], self.dw[i], self.m[i], self.v[i],
-                                             self.w_bf[i]) for i in range(3)]
+            wq, slot = (self.w1q, self.w3q, self.w2q), (K1, K3, K2)
+            self.adamw_items = [
+                F.adamw_item(self.w_master[i], self.dw[i], self.m[i], self.v[i], self.w_bf[i],
+                             **(dict(q=wq[i], q_scale=self.scale[slot[i]:slot[i] + 1],
+                                     q_amax=self.amax[slot[i]:slot[i] + 1], q_fmt=F.E4M3)
+                                if self.fuse_wq else {}))
+                for i in range(3)]
         # gated forward: h | u in one launch whose epilogue also quantizes a
         self.swiglu_ep = (F.swiglu_epilogue(self.w3q, self.scale[K3:K3 + 1], self.u, self.aq,
                                             F.E4M3, self.scale[A2:A2 + 1],
@@ -157,9 +174,10 @@ class SwiGLUTrainer:
             wam = (None, None, None)
         else:
             wam = (self._am(K1), self._am(K3), self._am(K2))
-        q(w1, E4, self.w1q, scale=sc(K1), amax_out=wam[0])
-        q(w3, E4, self.w3q, scale=sc(K3), amax_out=wam[1])
-        q(w2, E4, self.w2q, scale=sc(K2), amax_out=wam[2])
+        if not (self.fuse_wq and self.w_codes_ready):  # else the optimizer wrote them
+            q(w1, E4, self.w1q, scale=sc(K1), amax_out=wam[0])
+            q(w3, E4, self.w3q, scale=sc(K3), amax_out=wam[1])
+            q(w2, E4, self.w2q, scale=sc(K2), amax_out=wam[2])
         if self.fuse_forward:
             run([P(self.xq, E4, self.w1q, E4, sc(X1), sc(K1), self.h,       # h, u = x W1^T, x W3^T
                    swiglu=self.swiglu_ep)])                                 # a = silu(h) u
@@ -204,8 +222,15 @@ class SwiGLUTrainer:
 
     def optimizer_and_state(self):
         """AdamW on the three weights (unless the weight-gradient GEMMs did it),
-        then the nine amax-history pushes."""
+        then the nine amax-history pushes; with the fused weight quantization
+        the pushes first, then AdamW (which quantizes the updated weights with
+        the scales the pushes left)."""
         self.t += 1
+        if self.fuse_wq:
+            self._push_histories(auto=False)
+            F.fp8_adamw_multi(self.adamw_items, self.step_dev, **self.hp)
+            self.w_codes_ready = True
+            return
         if self.overlap:
             torch.cuda.current_stream().wait_stream(self.side)  # the updates are done
         elif not self.fuse_optimizer:
@@ -215,6 +240,10 @@ class SwiGLUTrainer:
             self.t_since += 1
             if self.t_since >= self.rescale_interval:
                 self.refresh_weight_amax()
+        self._push_histories(auto)
+
+    def _push_histories(self, auto: bool):
+        """The amax-history pushes of every delayed-scaling state, one launch."""
         items = []
         for i in range(9):
             if auto and i in (K1, K3, K2):

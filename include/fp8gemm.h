@@ -600,7 +600,16 @@ FP8_API int fp8_swiglu_backward_quantize(const void *da, const void *h, const vo
  *   items  HOST array of `count` descriptors (read during the call only);
  *          per item p, g, m, v fp32 [n] and p_bf16 (nullable) bf16 [n], all
  *          device, 16-byte aligned (p_bf16 8-byte), n % 4 == 0; empty items
- *          (n == 0) may have null pointers. */
+ *          (n == 0) may have null pointers.
+ *          q (nullable): the item's next delayed-scaling quantization done
+ *          here, on the updated weights ([Flax] 2.3: the weight is quantized
+ *          with the scale its history left): q [n] receives the codes of
+ *          bf16(p) divided by q_scale[0] (format q_fmt), exactly what
+ *          fp8_quantize_tensor(bf16(p), scale = q_scale) gives, and
+ *          q_amax[0] (nullable) max |bf16(p)| (cleared by the call), the
+ *          amax that the weight's history then takes.  q 4-byte aligned;
+ *          q_scale required with q; q_amax must not alias q_scale or another
+ *          item's q_amax. */
 typedef struct {
   float *p;
   const float *g;
@@ -608,6 +617,10 @@ typedef struct {
   float *v;
   void *p_bf16;
   int64_t n;
+  uint8_t *q;
+  const float *q_scale;
+  float *q_amax;
+  int q_fmt;
 } fp8_adamw_item_t;
 FP8_API int fp8_adamw_multi(const fp8_adamw_item_t *items, int count, int64_t *step,
                             int advance, double lr, double beta1, double beta2, double eps,

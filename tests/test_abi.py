@@ -237,3 +237,33 @@ def test_delayed_state_update_multi_validation(lib):
     if not torch.cuda.is_available():
         # disjoint items, one amax shared: valid (reaches the device check)
         assert call([ok(4096, 16), ok(16384, 20)]) == -6
+
+
+def test_adamw_multi_codes_validation(lib):
+    """The fused weight quantization of fp8_adamw_multi: a scale is required
+    with codes, a valid format, 4-byte aligned codes, an amax that is neither
+    the scale nor another item's amax."""
+    import torch
+    import fp8_quantized_gemm_gb300 as F
+    f = lib.fp8_adamw_multi
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int] + \
+        [ctypes.c_double] * 5 + [ctypes.c_void_p]
+
+    def item(base, q=None, sc=None, am=None, fmt=0):
+        return F.AdamwItem(base, base + 4096, base + 8192, base + 12288, None, 1024, q, sc, am,
+                           fmt)
+
+    def call(items):
+        arr = (F.AdamwItem * len(items))(*items)
+        return f(ctypes.cast(arr, ctypes.c_void_p), len(items), 64, 1, 1e-4, 0.9, 0.999, 1e-8,
+                 0.01, None)
+
+    assert call([item(1 << 20, q=1 << 24)]) == -1                       # no scale
+    assert call([item(1 << 20, q=1 << 24, sc=16, fmt=2)]) == -1         # bad format
+    assert call([item(1 << 20, q=(1 << 24) + 2, sc=16)]) == -2          # misaligned codes
+    assert call([item(1 << 20, q=1 << 24, sc=16, am=16)]) == -1         # amax is the scale
+    assert call([item(1 << 20, q=1 << 24, sc=16, am=32),
+                 item(1 << 21, q=1 << 25, sc=20, am=32)]) == -1          # one amax twice
+    if not torch.cuda.is_available():
+        assert call([item(1 << 20, q=1 << 24, sc=16, am=32),
+                     item(1 << 21, q=1 << 25, sc=16, am=48)]) == -6      # valid (one scale shared)

@@ -9,7 +9,9 @@
   empty sizes.
 * Multi-tensor AdamW with the step counter on the device: every tensor
   against the oracle's AdamW at the advanced step, over several steps, with
-  an empty item.
+  an empty item; with the next step's weight codes: the codes and amax of
+  the updated bf16 weights bit-exact against the oracle quantizing them with
+  the given scale.
 """
 import numpy as np
 import pytest
@@ -151,3 +153,44 @@ def test_adamw_multi_device_step():
             # the next step continues from the GPU's own state
             host[k] = [p.double().cpu().numpy(), m.double().cpu().numpy(),
                        v.double().cpu().numpy()]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_adamw_multi_writes_the_next_weight_codes(fmt):
+    """The fused quantization of fp8_adamw_multi: items with codes (a scale
+    in the reciprocal-quotient range, one below it, one that clips), an item
+    without, an empty item; codes and amax bit-exact against the oracle's
+    quantize_with_scale / amax of the updated bf16 weights."""
+    F = lib()
+    code = F.E4M3 if fmt == "e4m3" else F.E5M2
+    sizes = [4096, 1000, 0, 65536 + 4, 2048]
+    scales = [3e-4, 2.0 ** -100, 1.0, 1e-5, 0.0]  # the fourth clips; the last has no codes
+    rng = np.random.default_rng(17)
+    dev = []
+    for n in sizes:
+        p = torch.from_numpy((rng.standard_normal(n) * 0.02).astype(np.float32)).cuda()
+        g = torch.from_numpy((rng.standard_normal(n) * 1e-3).astype(np.float32)).cuda()
+        dev.append([p, g, torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda"),
+                    torch.empty(n, dtype=torch.bfloat16, device="cuda"),
+                    torch.full((n,), 0xAB, dtype=torch.uint8, device="cuda")])
+    sc = torch.tensor(scales, dtype=torch.float32, device="cuda")
+    am = torch.full((len(sizes),), -1.0, device="cuda")
+    items = []
+    for k, (p, g, m, v, pb, q) in enumerate(dev):
+        kw = dict(q=q, q_scale=sc[k:k + 1], q_amax=am[k:k + 1], q_fmt=code) if k < 4 else {}
+        items.append(F.adamw_item(p, g, m, v, pb, **kw))
+    step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for t in range(2):
+        F.fp8_adamw_multi(items, step)
+        torch.cuda.synchronize()
+        for k, (p, g, m, v, pb, q) in enumerate(dev):
+            assert torch.equal(pb, p.to(torch.bfloat16))
+            if k >= 4:
+                assert np.all(to_np_u8(q) == 0xAB)  # no codes asked: untouched
+                continue
+            if sizes[k] == 0:
+                continue  # an empty item's codes pointer is null: nothing is written
+            wb = f32(pb)
+            assert np.array_equal(to_np_u8(q), OQ.quantize_with_scale(wb, np.float32(scales[k]),
+                                                                      fmt)), (t, k)
+            assert np.float32(am[k].item()) == OQ.amax(wb), (t, k)

@@ -276,14 +276,23 @@ def test_fused_epilogues_match_standalone_passes():
                           fuse_optimizer=True)
     plain = SwiGLUTrainer(w1.cuda(), w3.cuda(), w2.cuda(), tokens=T, fuse_forward=False,
                           fuse_optimizer=False)
+    from fp8_quantized_gemm_gb300.mlp import K1, K2, K3
+    assert plain.fuse_wq and not fused.fuse_wq
     xd = x.cuda()
     for t in range(4):
         dy = workloads.swiglu_grad(t, tokens=T, d=D).cuda()
         for tr in (fused, plain):
             tr.step(xd, dy)
         torch.cuda.synchronize()
-        for name in ("h", "u", "aq", "y", "da", "dhq", "duq", "dx", "amax", "scale", "hist"):
+        for name in ("h", "u", "aq", "y", "da", "dhq", "duq", "dx", "scale", "hist"):
             assert torch.equal(getattr(fused, name), getattr(plain, name)), (t, name)
+        # the weights' amax slots: the AdamW epilogue path leaves the amax of
+        # the weights this step used, the standalone update (which quantizes
+        # the next step's weights) the amax of the updated ones
+        others = [i for i in range(9) if i not in (K1, K3, K2)]
+        assert torch.equal(fused.amax[others], plain.amax[others]), t
+        for i, k in enumerate((K1, K3, K2)):
+            assert plain.amax[k].item() == plain.w_bf[i].abs().max().float().item(), (t, k)
         for name in ("w_master", "m", "v", "w_bf"):
             for i in range(3):
                 assert torch.equal(getattr(fused, name)[i], getattr(plain, name)[i]), (t, name, i)
