@@ -553,6 +553,11 @@ __device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // div_by_scale on two values at once: the same five rounded operations per
 // value, issued as packed pairs (y2 = {y, y}, ns2 = {-s, -s}).
@@ -590,12 +595,18 @@ __device__ __forceinline__ void div_by_scale2_bounded(float x0, float x1, uint64
 struct ScaleDiv {
   float s, y;
   uint64_t ns2, y2;  // {-s, -s}, {y, y} for div_by_scale2
+  // fast path: a magnitude from which on x / s saturates every FP8 format
+  // and up to which the quotient stays below 2^64 (no overflow): s 2^64,
+  // or 2^127 once that is larger (s > 2^63; with s <= 2^80, 2^127 / s >=
+  // 2^47, far beyond either format's MAX)
+  float bound;
   bool fast;
   __device__ __forceinline__ explicit ScaleDiv(float s_) {
     s = s_;
     y = __frcp_rn(s_);
     ns2 = f32x2_pack(-s_, -s_);
     y2 = f32x2_pack(y, y);
+    bound = fminf(__fmul_rn(s_, 0x1p64f), 0x1p127f);
     fast = s_ >= 0x1p-80f && s_ <= 0x1p80f;
   }
   // kFast: the caller has checked `fast` (uniformly, outside its loop)

@@ -183,19 +183,36 @@ __device__ __forceinline__ void gated_row32(const GemmArgs &a, int64_t row, int6
   }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const __nv_bfloat162 a2 = __floats2bfloat162_rn(swiglu_value(hb[2 * i], ub[2 * i]),
-                                                    swiglu_value(hb[2 * i + 1], ub[2 * i + 1]));
+    float a0, a1;
+    swiglu_value2(hb[2 * i], hb[2 * i + 1], ub[2 * i], ub[2 * i + 1], a0, a1);
+    const __nv_bfloat162 a2 = __floats2bfloat162_rn(a0, a1);
     aw[i] = *reinterpret_cast<const uint32_t *>(&a2);
-    ab[2 * i] = __uint_as_float(aw[i] << 16);
-    ab[2 * i + 1] = __uint_as_float(aw[i] & 0xFFFF0000u);
-    key = max(key, max(abs_key(ab[2 * i]), abs_key(ab[2 * i + 1])));
   }
   uint2 c[4];
+  if constexpr (kFast) {
+    // quotients of |a| clamped, signs from the bf16 words (quant_bf16x8)
+    uint32_t key2 = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float y[8];
-    d.div8<kFast>(*reinterpret_cast<const float(*)[8]>(ab + 8 * j), y);
-    c[j] = pack8(a.swi_fmt, y);
+    for (int j = 0; j < 4; ++j) {
+      const uint4 w = make_uint4(aw[4 * j], aw[4 * j + 1], aw[4 * j + 2], aw[4 * j + 3]);
+      float y[8];
+      bf16x8_quotients(w, d, key2, y);
+      c[j] = bf16x8_with_signs(pack8(a.swi_fmt, y), w);
+    }
+    key = max(key, bf16_key_merge(key2));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      ab[2 * i] = __uint_as_float(aw[i] << 16);
+      ab[2 * i + 1] = __uint_as_float(aw[i] & 0xFFFF0000u);
+      key = max(key, max(abs_key(ab[2 * i]), abs_key(ab[2 * i + 1])));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float y[8];
+      d.div8<false>(*reinterpret_cast<const float(*)[8]>(ab + 8 * j), y);
+      c[j] = pack8(a.swi_fmt, y);
+    }
   }
   uint4 *qd = reinterpret_cast<uint4 *>(a.swi_q + off);
   qd[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);

@@ -165,6 +165,56 @@ __device__ __forceinline__ uint2 pack8(int fmt, const float (&y)[8]) {
   return fmt == 0 ? pack8<0>(y) : pack8<1>(y);
 }
 
+// ---------------------------------------------- packed bf16 vectors --
+// Eight bf16 values held as a 16-byte vector of packed pairs (element 2i in
+// the low half of word i), quantized on a scale's fast path (ScaleDiv::fast)
+// with fewer instructions than decoding them and dividing signed values:
+//   - the running max of |x| is taken on the 16-bit halves (key2 holds two
+//     16-bit keys; bf16_key_merge folds them into the fp32 bits of |x|);
+//   - the quotient is formed from |x| clamped to ScaleDiv::bound (min.NaN:
+//     a NaN stays NaN), so the bounded quotient cannot overflow and every
+//     clamped value still saturates;
+//   - the sign is put back from the bf16 sign bits into the codes' bit 7
+//     (a NaN code keeps its input's sign).
+// The codes equal those of dividing the signed values (div_by_scale).
+__device__ __forceinline__ float min_nan_abs(float x, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(x)), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ void bf16x8_quotients(const uint4 w, const ScaleDiv &d, uint32_t &key2,
+                                                 float (&y)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    key2 = __vmaxu2(key2, u[i] & 0x7FFF7FFFu);
+    x[2 * i] = min_nan_abs(__uint_as_float(u[i] << 16), d.bound);
+    x[2 * i + 1] = min_nan_abs(__uint_as_float(u[i] & 0xFFFF0000u), d.bound);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) div_by_scale2_bounded(x[j], x[j + 1], d.ns2, d.y2, y[j], y[j + 1]);
+}
+
+// codes of non-negative quotients with the signs of the bf16 words put back
+__device__ __forceinline__ uint2 bf16x8_with_signs(const uint2 c, const uint4 w) {
+  return make_uint2(c.x | (__byte_perm(w.x, w.y, 0x7531) & 0x80808080u),
+                    c.y | (__byte_perm(w.z, w.w, 0x7531) & 0x80808080u));
+}
+
+template <int F>
+__device__ __forceinline__ uint2 quant_bf16x8(const uint4 w, const ScaleDiv &d, uint32_t &key2) {
+  float y[8];
+  bf16x8_quotients(w, d, key2, y);
+  return bf16x8_with_signs(pack8<F>(y), w);
+}
+
+// the two 16-bit |x| keys of key2 as one fp32 |x| key
+__device__ __forceinline__ uint32_t bf16_key_merge(uint32_t key2) {
+  return max(key2 & 0xFFFF0000u, key2 << 16);
+}
+
 // Eight quotients v[j] / s by one scale (ScaleDiv; the fast/slow choice is
 // per scale, so it diverges only between groups with extreme scales).
 __device__ __forceinline__ void div8(const ScaleDiv &d, const float *v, float (&y)[8]) {

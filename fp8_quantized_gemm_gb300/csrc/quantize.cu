@@ -89,11 +89,17 @@ __device__ __forceinline__ void quant_tensor_body(const T *__restrict__ x, int64
       uint2 c[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        if (kAmax) r[u][i].max_abs(key_a, key_b);  // zero-filled vectors add nothing
-        float v[8], y[8];
-        r[u][i].decode(v);
-        d.div8<kFast>(v, y);
-        c[i] = pack8<F>(y);
+        if constexpr (sizeof(T) == 2 && kFast) {
+          // bf16 on the fast path: quotients of |x| clamped, signs from the
+          // words; the same two-halfword key as max_abs (unused without kAmax)
+          c[i] = quant_bf16x8<F>(r[u][i].w[0], d, key_a);
+        } else {
+          if (kAmax) r[u][i].max_abs(key_a, key_b);  // zero-filled vectors add nothing
+          float v[8], y[8];
+          r[u][i].decode(v);
+          d.div8<kFast>(v, y);
+          c[i] = pack8<F>(y);
+        }
       }
       uint2 *dst = reinterpret_cast<uint2 *>(q) + v0;
       if (v0 + 4 <= nvec) {

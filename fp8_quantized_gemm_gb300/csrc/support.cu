@@ -40,16 +40,31 @@ __device__ __forceinline__ void bf16_roundtrip(const float (&v)[8], float (&o)[8
   bf16x8_to_f32(f32x8_to_bf16(v), o);
 }
 
+// SwiGLU of eight packed bf16 elements (packed arithmetic, elementwise.cuh)
+__device__ __forceinline__ void swiglu8(const uint4 hw, const uint4 uw, float (&av)[8]) {
+  float hv[8], uv[8];
+  bf16x8_to_f32(hw, hv);
+  bf16x8_to_f32(uw, uv);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) swiglu_value2(hv[j], hv[j + 1], uv[j], uv[j + 1], av[j], av[j + 1]);
+}
+
+__device__ __forceinline__ void swiglu_grad8(const uint4 daw, const uint4 hw, const uint4 uw,
+                                             float (&dhv)[8], float (&duv)[8]) {
+  float dav[8], hv[8], uv[8];
+  bf16x8_to_f32(daw, dav);
+  bf16x8_to_f32(hw, hv);
+  bf16x8_to_f32(uw, uv);
+  swiglu_grad8(dav, hv, uv, dhv, duv);
+}
+
 __global__ void __launch_bounds__(512)
     swiglu_fwd_kernel(const uint4 *__restrict__ h, const uint4 *__restrict__ u,
                       uint4 *__restrict__ a, int64_t nvec) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-    float hv[8], uv[8], av[8];
-    bf16x8_to_f32(__ldcs(h + i), hv);
-    bf16x8_to_f32(__ldcs(u + i), uv);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) av[j] = swiglu_value(hv[j], uv[j]);
+    float av[8];
+    swiglu8(__ldcs(h + i), __ldcs(u + i), av);
     __stcs(a + i, f32x8_to_bf16(av));
   }
 }
@@ -60,12 +75,8 @@ __global__ void __launch_bounds__(512)
                       uint4 *__restrict__ du, int64_t nvec) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-    float dav[8], hv[8], uv[8], dhv[8], duv[8];
-    bf16x8_to_f32(__ldcs(da + i), dav);
-    bf16x8_to_f32(__ldcs(h + i), hv);
-    bf16x8_to_f32(__ldcs(u + i), uv);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) swiglu_grad_values(dav[j], hv[j], uv[j], dhv[j], duv[j]);
+    float dhv[8], duv[8];
+    swiglu_grad8(__ldcs(da + i), __ldcs(h + i), __ldcs(u + i), dhv, duv);
     __stcs(dh + i, f32x8_to_bf16(dhv));
     __stcs(du + i, f32x8_to_bf16(duv));
   }
@@ -77,50 +88,27 @@ __global__ void __launch_bounds__(512)
 // the bf16 value is rounded as the plain kernel would store it, divided by
 // the scale (the same correctly rounded quotient as fp8_quantize_tensor),
 // cast with the saturating RNE conversion, and its |value| enters the fused
-// amax.  The bf16 tensor itself is never written.  kFast: the scale is in
-// the reciprocal-quotient range (checked once per launch).
-template <int F, bool kAmax, bool kFast>
-__device__ __forceinline__ void swiglu_fwd_quant_body(const uint4 *__restrict__ h,
-                                                      const uint4 *__restrict__ u, int64_t nvec,
-                                                      const ScaleDiv &d, uint2 *__restrict__ q,
-                                                      uint32_t &key) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  // two vectors of each input in flight per thread
-  for (; i + stride < nvec; i += 2 * stride) {
-    const uint4 hw0 = __ldcs(h + i), uw0 = __ldcs(u + i);
-    const uint4 hw1 = __ldcs(h + i + stride), uw1 = __ldcs(u + i + stride);
-    const uint4 hw[2] = {hw0, hw1}, uw[2] = {uw0, uw1};
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      float hv[8], uv[8], av[8], ab[8], y[8];
-      bf16x8_to_f32(hw[r], hv);
-      bf16x8_to_f32(uw[r], uv);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) av[j] = swiglu_value(hv[j], uv[j]);
-      bf16_roundtrip(av, ab);
-      if (kAmax) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) key = max(key, abs_key(ab[j]));
-      }
-      d.div8<kFast>(ab, y);
-      __stcs(q + i + r * stride, pack8<F>(y));
-    }
+// amax.  The bf16 tensor itself is never written.
+//
+// A scale in the reciprocal-quotient range (checked once per launch) takes
+// the fast loop: packed SwiGLU arithmetic and the packed-bf16 quantization
+// (quant_bf16x8), two vectors of each input in flight per thread.  Any
+// other scale takes a plain loop with IEEE division, one vector at a time,
+// kept small so that it does not raise the kernel's register count (the
+// two paths share one launch; 69 against 46 registers when the slow path
+// was a copy of the fast one, and 399 against 371 us at 16384 x 14336).
+
+// IEEE-division codes of eight values (the slow path) and their |x| key
+template <int F>
+__device__ __forceinline__ uint2 quant8_ieee_key(const float (&v)[8], float s, uint32_t &key) {
+  float b[8], y[8];
+  bf16_roundtrip(v, b);
+#pragma unroll 1
+  for (int j = 0; j < 8; ++j) {
+    key = max(key, abs_key(b[j]));
+    y[j] = __fdiv_rn(b[j], s);
   }
-  for (; i < nvec; i += stride) {
-    float hv[8], uv[8], av[8], ab[8], y[8];
-    bf16x8_to_f32(__ldcs(h + i), hv);
-    bf16x8_to_f32(__ldcs(u + i), uv);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) av[j] = swiglu_value(hv[j], uv[j]);
-    bf16_roundtrip(av, ab);
-    if (kAmax) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) key = max(key, abs_key(ab[j]));
-    }
-    d.div8<kFast>(ab, y);
-    __stcs(q + i, pack8<F>(y));
-  }
+  return pack8<F>(y);
 }
 
 template <int F, bool kAmax>
@@ -129,67 +117,84 @@ __global__ void __launch_bounds__(256, 6)
                             int64_t nvec, const float *scale, uint2 *__restrict__ q,
                             uint32_t *amax_out) {
   const ScaleDiv d(*scale);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   uint32_t key = 0;
-  if (d.fast)
-    swiglu_fwd_quant_body<F, kAmax, true>(h, u, nvec, d, q, key);
-  else
-    swiglu_fwd_quant_body<F, kAmax, false>(h, u, nvec, d, q, key);
+  if (d.fast) {
+    uint32_t key2 = 0;
+    auto one = [&](int64_t k, const uint4 hw, const uint4 uw) {
+      float av[8];
+      swiglu8(hw, uw, av);
+      __stcs(q + k, quant_bf16x8<F>(f32x8_to_bf16(av), d, key2));
+    };
+    for (; i + stride < nvec; i += 2 * stride) {
+      const uint4 h0 = __ldcs(h + i), u0 = __ldcs(u + i);
+      const uint4 h1 = __ldcs(h + i + stride), u1 = __ldcs(u + i + stride);
+      one(i, h0, u0);
+      one(i + stride, h1, u1);
+    }
+    for (; i < nvec; i += stride) one(i, __ldcs(h + i), __ldcs(u + i));
+    key = bf16_key_merge(key2);
+  } else {
+    for (; i < nvec; i += stride) {
+      float av[8];
+      swiglu8(__ldcs(h + i), __ldcs(u + i), av);
+      __stcs(q + i, quant8_ieee_key<F>(av, d.s, key));
+    }
+  }
   if (kAmax) block_max_to(key, amax_out);
+}
+
+// the slow path of the backward pass, out of line (its registers are not
+// the fast loop's)
+template <int F>
+__device__ __noinline__ void swiglu_bwd_quant_slow(const uint4 *__restrict__ da,
+                                                   const uint4 *__restrict__ h,
+                                                   const uint4 *__restrict__ u, int64_t nvec,
+                                                   int64_t i, int64_t stride, float sh, float su,
+                                                   uint2 *__restrict__ qh, uint2 *__restrict__ qu,
+                                                   uint32_t &key_h, uint32_t &key_u) {
+  for (; i < nvec; i += stride) {
+    float dhv[8], duv[8];
+    swiglu_grad8(__ldcs(da + i), __ldcs(h + i), __ldcs(u + i), dhv, duv);
+    __stcs(qh + i, quant8_ieee_key<F>(dhv, sh, key_h));
+    __stcs(qu + i, quant8_ieee_key<F>(duv, su, key_u));
+  }
 }
 
 // dh and du quantized with their own scales; one amax each.  Both scales'
 // fast checks are folded into one launch-uniform branch.
-template <int F, bool kAmax, bool kFast>
-__device__ __forceinline__ void swiglu_bwd_quant_body(
-    const uint4 *__restrict__ da, const uint4 *__restrict__ h, const uint4 *__restrict__ u,
-    int64_t nvec, const ScaleDiv &dsh, const ScaleDiv &dsu, uint2 *__restrict__ qh,
-    uint2 *__restrict__ qu, uint32_t &key_h, uint32_t &key_u) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  auto one = [&](int64_t i, const uint4 daw, const uint4 hw, const uint4 uw) {
-    float dav[8], hv[8], uv[8], dhv[8], duv[8], dhb[8], dub[8], y[8];
-    bf16x8_to_f32(daw, dav);
-    bf16x8_to_f32(hw, hv);
-    bf16x8_to_f32(uw, uv);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) swiglu_grad_values(dav[j], hv[j], uv[j], dhv[j], duv[j]);
-    bf16_roundtrip(dhv, dhb);
-    bf16_roundtrip(duv, dub);
-    if (kAmax) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        key_h = max(key_h, abs_key(dhb[j]));
-        key_u = max(key_u, abs_key(dub[j]));
-      }
-    }
-    dsh.div8<kFast>(dhb, y);
-    __stcs(qh + i, pack8<F>(y));
-    dsu.div8<kFast>(dub, y);
-    __stcs(qu + i, pack8<F>(y));
-  };
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  // two vectors of each input in flight per thread
-  for (; i + stride < nvec; i += 2 * stride) {
-    const uint4 da0 = __ldcs(da + i), h0 = __ldcs(h + i), u0 = __ldcs(u + i);
-    const uint4 da1 = __ldcs(da + i + stride), h1 = __ldcs(h + i + stride),
-                u1 = __ldcs(u + i + stride);
-    one(i, da0, h0, u0);
-    one(i + stride, da1, h1, u1);
-  }
-  for (; i < nvec; i += stride) one(i, __ldcs(da + i), __ldcs(h + i), __ldcs(u + i));
-}
-
 template <int F, bool kAmax>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 5)
     swiglu_bwd_quant_kernel(const uint4 *__restrict__ da, const uint4 *__restrict__ h,
                             const uint4 *__restrict__ u, int64_t nvec, const float *scale_h,
                             const float *scale_u, uint2 *__restrict__ qh, uint2 *__restrict__ qu,
                             uint32_t *amax_h, uint32_t *amax_u) {
   const ScaleDiv dsh(*scale_h), dsu(*scale_u);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   uint32_t key_h = 0, key_u = 0;
-  if (dsh.fast && dsu.fast)
-    swiglu_bwd_quant_body<F, kAmax, true>(da, h, u, nvec, dsh, dsu, qh, qu, key_h, key_u);
-  else
-    swiglu_bwd_quant_body<F, kAmax, false>(da, h, u, nvec, dsh, dsu, qh, qu, key_h, key_u);
+  if (dsh.fast && dsu.fast) {
+    uint32_t kh2 = 0, ku2 = 0;
+    auto one = [&](int64_t k, const uint4 daw, const uint4 hw, const uint4 uw) {
+      float dhv[8], duv[8];
+      swiglu_grad8(daw, hw, uw, dhv, duv);
+      __stcs(qh + k, quant_bf16x8<F>(f32x8_to_bf16(dhv), dsh, kh2));
+      __stcs(qu + k, quant_bf16x8<F>(f32x8_to_bf16(duv), dsu, ku2));
+    };
+    for (; i + stride < nvec; i += 2 * stride) {
+      const uint4 da0 = __ldcs(da + i), h0 = __ldcs(h + i), u0 = __ldcs(u + i);
+      const uint4 da1 = __ldcs(da + i + stride), h1 = __ldcs(h + i + stride),
+                  u1 = __ldcs(u + i + stride);
+      one(i, da0, h0, u0);
+      one(i + stride, da1, h1, u1);
+    }
+    for (; i < nvec; i += stride) one(i, __ldcs(da + i), __ldcs(h + i), __ldcs(u + i));
+    key_h = bf16_key_merge(kh2);
+    key_u = bf16_key_merge(ku2);
+  } else {
+    swiglu_bwd_quant_slow<F>(da, h, u, nvec, i, stride, dsh.s, dsu.s, qh, qu, key_h, key_u);
+  }
   if (kAmax) {
     block_max_to(key_h, amax_h);
     __syncthreads();  // block_max_to's shared scratch is reused
