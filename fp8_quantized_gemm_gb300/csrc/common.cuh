@@ -152,6 +152,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
 
 // Bring one tensor-map box into L2 (no shared-memory destination, no
 // completion to wait for): a hint that warms the cache for a later load.
+// Bring the line holding p into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int32_t c0, int32_t c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(m)),
@@ -390,6 +395,15 @@ __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t 
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// An empty volatile statement that "rewrites" 16 registers: placed after
+// tcgen05.wait::ld, it keeps every use of those tcgen05.ld results after the
+// wait in the compiler's order (no instruction is emitted).
+#define FP8K_REG_FENCE16(r)                                                                  \
+  asm volatile(""                                                                            \
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),     \
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),   \
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]))
 
 // ------------------------------------------- CTA pairs (cta_group::2) --
 __device__ __forceinline__ uint32_t cluster_ctarank() {

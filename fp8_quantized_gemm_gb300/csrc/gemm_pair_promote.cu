@@ -4,31 +4,28 @@
 //
 // FP32 scales are not powers of two, so the tensor core cannot apply them:
 // every 128-deep K slice is contracted into its own TMEM buffer and the
-// epilogue warps promote it, acc += sa * sb * partial, in registers.  On one
-// CTA with 128 x 128 tiles every k block moves 32 KB through shared memory
-// (16 KB of A, 16 KB of B, written by TMA and read by the tensor core) for
-// 4.2 MFLOP.  Here two CTAs on neighbouring SMs compute one 256 x 128 tile
-// with M = 256 MMAs issued by the even CTA (the leader):
+// epilogue warps promote it, acc += sa * sb * partial, in registers.  Two
+// CTAs on neighbouring SMs compute one 256 x 256 tile with M = 256 MMAs
+// issued by the even CTA (the leader):
 //
-//   - each CTA stages its own 128 rows of A and its own 64 rows of B per k
-//     block (24 KB a stage, eight stages), both CTAs' copies completing on
-//     the leader's full barrier;
+//   - each CTA stages its own 128 rows of A and its own 128 rows of B per k
+//     block (32 KB a stage, six stages), both CTAs' copies completing on the
+//     leader's full barrier;
 //   - the leader's MMAs read both CTAs' shared memory at the same offsets
 //     and write each CTA's 128 rows of the slice's partial product into that
-//     CTA's TMEM, one of four 128-column buffers in a ring;
+//     CTA's TMEM, one of two 256-column buffers;
 //   - tcgen05.commit multicasts each stage release and each "slice ready" to
 //     both CTAs; eight epilogue warps per CTA (two per TMEM lane quadrant,
-//     64 columns each) read the slice out, hand the buffer back on the
-//     leader's barrier (a relaxed arrive: a release one would first wait
-//     for the warp's scale prefetches in flight) and then promote it, so
-//     the tensor core runs the next slices meanwhile.
+//     128 columns each) read the slice out in 16-column chunks, each read in
+//     flight under the previous chunk's FMAs, and hand the buffer back on
+//     the leader's barrier after the last read, so the tensor core runs the
+//     next slice meanwhile.
 //
-// The promotion FMAs, 64 per warp and slice, bound the kernel: without them
-// the same launch runs about a quarter faster.
-//
-// The scales of a slice are loaded four slices ahead of its promotion.  The
-// 128-wide column tile lies inside one 128-row block of B, so one sb value
-// covers the whole tile for a slice.
+// The TMEM reads bound the kernel (the numbers are at the configuration
+// below).  A warp's 128 accumulators stay in registers for the whole tile;
+// its columns lie in one 128-row block of B, so one weight scale per slice.
+// The scales of the next slice are loaded one slice ahead, and their lines
+// four slices ahead are brought into L2.
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "kernels.h"
@@ -38,9 +35,10 @@ namespace fp8k {
 // 256-row tiles per band of the grouped tile order.
 constexpr int64_t kPromoteBandRows = 8;
 
-template <int STAGES, int EPI>
+template <int BN_, int STAGES, int EPI>
 struct PromoteCfg {
-  static constexpr int BM = 128, BN = 128, BK = 128;  // per CTA: 128 rows; pair: 256 x 128
+  // per CTA: 128 rows x BN columns; pair: 256 x BN
+  static constexpr int BM = 128, BN = BN_, BK = 128;
   // EPI epilogue warps, EPI / 4 per TMEM lane quadrant, each promoting
   // kCols columns of its 32 rows
   static constexpr int kEpiWarps = EPI;
@@ -50,21 +48,26 @@ struct PromoteCfg {
   static constexpr uint32_t kBBytes = (BN / 2) * BK;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTileBytes = STAGES * kStageBytes;
-  static constexpr int kAccBufs = 4;
-  static constexpr uint32_t kTmemCols = kAccBufs * BN;
+  static constexpr int kAccBufs = 512 / BN;  // 4 x 128, 2 x 192 or 2 x 256 columns
+  // the allocation: a power of two columns
+  static constexpr uint32_t kTmemCols = kAccBufs * BN <= 256 ? 256u : 512u;
   static constexpr int kNumBars = 2 * STAGES + 2 * kAccBufs + 1;
   static constexpr uint32_t kSmem = 1024 + kTileBytes + 8 * kNumBars + 16;
   static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kSmem <= 227 * 1024, "shared-memory budget");
   static_assert(EPI % 4 == 0 && kCols % 32 == 0, "whole 32-column chunks per warp");
+  // a warp's columns start at a multiple of kCols (BN is one), and kCols
+  // divides 128: they lie in one 128-row block of B, so one weight scale
+  // per warp and slice
+  static_assert(128 % kCols == 0 && BN % kCols == 0, "one 128-column B block of scales per warp");
 };
 
-template <int STAGES, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<STAGES, EPI>::kThreads, 1)
+template <int BN, int STAGES, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGES, EPI>::kThreads, 1)
     gemm_pair_promote_kernel(const __grid_constant__ CUtensorMap tma,
                              const __grid_constant__ CUtensorMap tmb, const GemmArgs args) {
-  using C = PromoteCfg<STAGES, EPI>;
+  using C = PromoteCfg<BN, STAGES, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -202,13 +205,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<STAGES, E
     __syncwarp();
   } else {
     // ---------------------------------------------- promotion epilogue (both)
-    constexpr int kCols = C::kCols, kChunks = kCols / 32;
+    constexpr int kCols = C::kCols;
     const uint32_t q = warp & 3u;                 // TMEM lane quadrant of this warp
-    const int col0 = ((int)(warp - 2) >> 2) * kCols;  // its columns of the 128-wide tile
+    const int col0 = ((int)(warp - 2) >> 2) * kCols;  // its columns of the BN-wide tile
     const uint32_t lane_base = tmem + ((32u * q) << 16) + (uint32_t)col0;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
-    const float *sa = static_cast<const float *>(args.sa);
-    const float *sb = static_cast<const float *>(args.sb);
     const int64_t G = args.K / 128;
     uint32_t it = 0;
     bool ok = true;
@@ -216,53 +217,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<STAGES, E
       int64_t m0, n0;
       tile_origin(t, m0, n0);
       const int64_t row = m0 + rank * C::BM + 32 * q + lane;
-      const float *sb_tile = sb + (n0 >> 7) * G;
+      // this warp's columns lie in one 128-row block of B; a warp wholly
+      // past N (or a lane past M) multiplies by a zero scale and stores
+      // nothing
+      const bool row_in = row < args.M, cols_in = n0 + col0 < args.N;
+      // scale of slice k: sa[k][row] * sb[block][k]; the next slice's pair
+      // is loaded one slice ahead, and the line four slices ahead is
+      // brought into L2 meanwhile (no registers held for it)
+      const float *sa_p = static_cast<const float *>(args.sa) + (row_in ? row : 0);
+      const float *sb_p = static_cast<const float *>(args.sb) + ((n0 + col0) >> 7) * G;
+      constexpr int kAhead = 4;
+      float na = row_in ? __ldg(sa_p) : 0.0f, nb = cols_in ? __ldg(sb_p) : 0.0f;
       float acc[kCols];
 #pragma unroll
       for (int i = 0; i < kCols; ++i) acc[i] = 0.0f;
-      // scales of slice k sit in register slot k % kQ, loaded kQ slices
-      // before the slice is promoted (constant indices: the loop over the
-      // slots is unrolled)
-      constexpr int kQ = 4;
-      float sa_q[kQ], sb_q[kQ];
-      auto load_s = [&](int k, float &fa, float &fb) {
-        fa = row < args.M ? __ldg(sa + (int64_t)k * args.M + row) : 0.0f;
-        fb = __ldg(sb_tile + k);
-      };
-#pragma unroll
-      for (int d = 0; d < kQ; ++d)
-        if (d < kb_count) load_s(d, sa_q[d], sb_q[d]);
-      for (int kb = 0; kb < kb_count && ok; kb += kQ) {
-#pragma unroll
-        for (int j = 0; j < kQ; ++j) {
-          const int k = kb + j;
-          if (k >= kb_count) break;
-          const uint32_t buf = it % C::kAccBufs, use = it / C::kAccBufs;
-          const float s_cur = sa_q[j] * sb_q[j];
-          if (k + kQ < kb_count) load_s(k + kQ, sa_q[j], sb_q[j]);
-          if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) {
-            ok = false;
-            break;
+      for (int k = 0; k < kb_count; ++k) {
+        const uint32_t buf = it % C::kAccBufs, use = it / C::kAccBufs;
+        const float s_cur = na * nb;
+        if (k + 1 < kb_count) {
+          sa_p += args.M;
+          ++sb_p;
+          na = row_in ? __ldg(sa_p) : 0.0f;
+          nb = cols_in ? __ldg(sb_p) : 0.0f;
+          if (k + kAhead < kb_count) {
+            if (row_in) prefetch_l2(sa_p + (kAhead - 1) * args.M);
+            if (cols_in && lane == 0) prefetch_l2(sb_p + (kAhead - 1));
           }
-          tc_fence_after();
-          uint32_t r[kCols];
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c) FP8K_TMEM_LD_X32(lane_base + buf * C::BN + 32 * c, (r + 32 * c));
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          // every lane's reads of the buffer are complete (wait::ld): a
-          // relaxed arrival hands it back without waiting for this thread's
-          // scale prefetches and output stores still in flight
-          if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader0 + 8u * buf);
-#pragma unroll
-          for (int i = 0; i < kCols; ++i) acc[i] = fmaf(s_cur, __uint_as_float(r[i]), acc[i]);
-          ++it;
         }
+        if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, err, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb = lane_base + buf * C::BN;
+        // 16-column chunks: chunk c + 1's read is in flight while chunk c's
+        // FMAs issue (tcgen05.wait::ld waits for every read of the thread, so
+        // one read overlaps the arithmetic at a time); the buffer goes back
+        // once the last chunk is read, before its FMAs.  A relaxed arrival:
+        // every lane's reads are complete (wait::ld), and a release would
+        // first wait for this thread's scale loads and stores in flight.
+        constexpr int kC16 = kCols / 16;
+        uint32_t r[2][16];
+        FP8K_TMEM_LD_X16(tb, r[0]);
+#pragma unroll
+        for (int c = 0; c < kC16; ++c) {
+          tmem_ld_wait();
+          FP8K_REG_FENCE16(r[c & 1]);
+          if (c + 1 < kC16) {
+            FP8K_TMEM_LD_X16(tb + 16 * (c + 1), r[(c + 1) & 1]);
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader0 + 8u * buf);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            acc[16 * c + i] = fmaf(s_cur, __uint_as_float(r[c & 1][i]), acc[16 * c + i]);
+        }
+        ++it;
       }
       if (!ok) break;
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
+      for (int c = 0; c < kCols / 32; ++c) {
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = acc[32 * c + i];
@@ -277,20 +293,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<STAGES, E
   if (warp == 1) tmem_dealloc_pair(tmem, C::kTmemCols);
 }
 
-// Eight stages of 24 KB; eight epilogue warps of 64 columns (sixteen of 32
-// columns measured slower: their register budget spills).
-constexpr int kPromoteStages = 8;
+// 256 x 256 pair tiles: six stages of 32 KB, two 256-column TMEM buffers,
+// eight epilogue warps (two per TMEM lane quadrant) of 128 columns.  The
+// promotion reads every slice's fp32 partial out of TMEM, 4 B per output
+// element and 128-deep K group; at the rate these reads reach (about 128 B
+// per cycle and SM in every layout measured) that takes 4 BN cycles per
+// slice against the tensor core's 2.5 BN, so the kernel tops out near 62% of
+// the dense FP8 rate whatever the tile shape.  Measured at 4096 x 2048 x
+// 7168 (2 rounds of tiles) / 16384 x 2048 x 7168 (7 rounds):
+//   - 256 x 128, eight 64-column warps: 78.5 / 248 us (each CTA's tensor
+//     core also reads 8 KB of shared memory, A and both halves of B, per
+//     128 x 128 x 32 MMA: its own limit at the same ~62%);
+//   - 256 x 256, eight 128-column warps, 16-column reads with the next one
+//     in flight under the FMAs: 68.3 / 214 us (this one);
+//   - the same with 32-column reads one at a time: 94.8 / 304 us;
+//   - 256 x 192, twelve 64-column warps (128 registers): 86.7 / 265 us.
+constexpr int kPromoteBN = 256;
+constexpr int kPromoteStages = 6;
 constexpr int kPromoteEpiWarps = 8;
-using PromoteC = PromoteCfg<kPromoteStages, kPromoteEpiWarps>;
+using PromoteC = PromoteCfg<kPromoteBN, kPromoteStages, kPromoteEpiWarps>;
 
 int gemm_pair_promote_b_rows() { return PromoteC::BN / 2; }
 
-// The pair kernel has no split K: it pays off when the 256 x 128 tiles give
-// every pair work.  K-major operands only (the group scales run along K).
+// The pair kernel has no split K: it pays off once the 256 x 256 tiles give
+// at least half of the pairs work (one round of them then takes less time
+// than the one-CTA kernel's two rounds of 128 x 128 tiles).  K-major
+// operands only (the group scales run along K).
 bool gemm_pair_promote_eligible(int64_t M, int64_t N, int64_t K, int sms) {
   if (K % 128 != 0) return false;
-  const int64_t tiles = ((M + 255) / 256) * ((N + 127) / 128);
-  return tiles >= sms / 2;
+  const int64_t tiles = ((M + 255) / 256) * ((N + PromoteC::BN - 1) / PromoteC::BN);
+  return tiles >= sms / 4;
 }
 
 cudaError_t launch_gemm_pair_promote(const CUtensorMap &tma, const CUtensorMap &tmb,
@@ -298,7 +330,7 @@ cudaError_t launch_gemm_pair_promote(const CUtensorMap &tma, const CUtensorMap &
   using C = PromoteC;
   if (args.K % 128 != 0 || args.a_mn || args.b_mn || args.ksplit != 1 || args.experts != 0)
     return cudaErrorInvalidValue;
-  auto kern = gemm_pair_promote_kernel<kPromoteStages, kPromoteEpiWarps>;
+  auto kern = gemm_pair_promote_kernel<kPromoteBN, kPromoteStages, kPromoteEpiWarps>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -195,12 +195,14 @@ def test_gemm_group_multicast_switch(mnk, sfmt, multicast):
     assert ok, worst
 
 
-@pytest.mark.parametrize("mnk", [(1800, 2000, 512), (1024, 9728, 256)])
+@pytest.mark.parametrize("mnk", [(1800, 2000, 512), (1024, 9728, 256), (2048, 1800, 384)])
 def test_gemm_group_f32_cta_pairs(mnk):
-    """FP32 group scales on CTA pairs (256 x 128 tiles, the promotion in both
-    CTAs): ragged M and N (1800 = 7 * 256 + 8: the last pair's second CTA
-    lies wholly past M; 2000 = 15 * 128 + 80) and a bias, against the oracle
-    with pairs on and off; the switch off runs the one-CTA kernel."""
+    """FP32 group scales on CTA pairs (256 x 256 tiles, the promotion in both
+    CTAs): ragged M and N (1800 rows = 7 * 256 + 8: the last pair's second CTA
+    lies wholly past M; 2000 = 7 * 256 + 208 columns; 1800 columns: the last
+    tile's second 128-column half lies wholly past N, with no weight scale
+    block of its own) and a bias, against the oracle with pairs on and off;
+    the switch off runs the one-CTA kernel."""
     F = lib()
     m, n, k = mnk
     qa, sa, qb, sb = group_operands(m, n, k, "f32", seed=9)

@@ -363,6 +363,31 @@ def test_given_scale_every_bf16_input(fmt, transpose):
             assert np.array_equal(to_np_u8(qt), ref.T), float(s)
 
 
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_nan_inputs_give_nan_codes(fmt):
+    """NaN inputs of either sign give a NaN code (the oracle defines codes for
+    finite and infinite inputs only; a NaN is not cast to a number), on the
+    reciprocal path and on the IEEE one, while the finite neighbours in the
+    same vectors keep the oracle's codes."""
+    from oracle import formats as OF
+    F = lib()
+    bits = np.full(64 * 32, 0x3F80, dtype=np.uint32)                  # 1.0
+    bits[::5] = 0x7FC0                                                # +NaN
+    bits[2::7] = 0xFFC1                                               # -NaN
+    bits[3::11] = 0xC2F6                                              # -123.0
+    x = torch.from_numpy((bits << 16).view(np.float32).reshape(64, 32)).to(torch.bfloat16)
+    xf = x.float().numpy()
+    nan = np.isnan(xf)
+    q = torch.empty((64, 32), dtype=torch.uint8, device="cuda")
+    for s in (np.float32(0.37), np.float32(2.0 ** 90)):
+        F.fp8_quantize_tensor(x.cuda(), FMT[fmt], q, scale=torch.tensor([s], device="cuda"))
+        codes = to_np_u8(q)
+        assert np.isnan(OF.decode(codes[nan], OF.fmt_of(fmt))).all(), float(s)
+        ref = OQ.quantize_with_scale(np.where(nan, 0, xf), s, fmt)
+        assert np.array_equal(codes[~nan], ref[~nan]), float(s)
+
+
 def midpoint_neighbours(fmt, scales):
     """fp32 inputs x whose quotient x / s lies on or within a few fp32 ulps of
     a rounding midpoint between two FP8 codes (the cases a quotient that is
