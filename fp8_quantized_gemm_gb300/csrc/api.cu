@@ -814,9 +814,17 @@ int fp8_gemm_group_experts(const uint8_t *a, const void *sa, const uint8_t *b, c
   args.sb_expert_stride = ((N + 127) / 128) * (K / 128);
   // tile width for the expected tile count (about half a row tile of
   // padding per expert)
-  const int bn = fp8k::gemm_tile_n(mode, M + 64 * (int64_t)experts, N, d->sms);
   CUtensorMap tma, tmb;
   if ((rc = encode_operand(&tma, a, K, M, 128)) != FP8_OK) return rc;
+  if (mode == fp8k::kScaleGroupF32 && g_use_pairs &&
+      fp8k::gemm_pair_promote_eligible(M, N, K, d->sms)) {
+    // FP32 scales on CTA pairs, expert row tiles of 256
+    if ((rc = encode_operand(&tmb, b, K, (int64_t)experts * N,
+                             fp8k::gemm_pair_promote_b_rows())) != FP8_OK)
+      return rc;
+    return to_status(fp8k::launch_gemm_pair_promote(tma, tmb, args, d->sms, (cudaStream_t)stream));
+  }
+  const int bn = fp8k::gemm_tile_n(mode, M + 64 * (int64_t)experts, N, d->sms);
   if ((rc = encode_operand(&tmb, b, K, (int64_t)experts * N, bn)) != FP8_OK) return rc;
   if (mode == fp8k::kScaleGroupUe8m0 && M > 256 && N % 128 == 0) {
     // as in fp8_gemm_group: the UE8M0 scales become E8M0 words for the

@@ -63,7 +63,7 @@ struct PromoteCfg {
   static_assert(128 % kCols == 0 && BN % kCols == 0, "one 128-column B block of scales per warp");
 };
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool EXPERTS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGES, EPI>::kThreads, 1)
     gemm_pair_promote_kernel(const __grid_constant__ CUtensorMap tma,
                              const __grid_constant__ CUtensorMap tmb, const GemmArgs args) {
@@ -107,26 +107,96 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGE
     tma_prefetch_desc(&tmb);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+
+  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int64_t rows = (args.M + 255) / 256, tiles_n = (args.N + C::BN - 1) / C::BN;
+  // Expert-grouped rows (MoE): a tile never spans two experts; expert e
+  // owns ceil(rows_e / 256) * tiles_n consecutive tile indices.  Warp 0 of
+  // each CTA turns the device offsets into that prefix (both CTAs of a pair
+  // read the same offsets, so they agree on every tile).
+  __shared__ int64_t ex_tile0[EXPERTS ? kMaxExperts + 1 : 1];
+  __shared__ int32_t ex_row0[EXPERTS ? kMaxExperts + 1 : 1];
+  const int E = EXPERTS ? args.experts : 0;
+  if constexpr (EXPERTS) {
+    if (warp == 0) {
+      // lane l takes experts [8l, 8l + 8)
+      int64_t cnt[8];
+      int64_t sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = 8 * (int)lane + i;
+        cnt[i] = 0;
+        if (e < E) {
+          const int32_t r0 = args.offsets[e], r1 = args.offsets[e + 1];
+          ex_row0[e] = r0;
+          cnt[i] = r1 > r0 ? (int64_t)((r1 - r0 + 255) / 256) * tiles_n : 0;
+          if (e == E - 1) ex_row0[E] = r1;
+        }
+        sum += cnt[i];
+      }
+      int64_t incl = sum;  // inclusive scan of the lane sums
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if ((int)lane >= o) incl += v;
+      }
+      int64_t run = incl - sum;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = 8 * (int)lane + i;
+        if (e < E) ex_tile0[e] = run;
+        run += cnt[i];
+        if (e == E - 1) ex_tile0[E] = run;
+      }
+    }
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // barrier inits visible to the peer before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // pair p takes tiles p, p + npairs, ... of the grouped order: bands of
-  // kPromoteBandRows 256-row tiles walked column by column, so the pairs in
-  // flight share A and B blocks in L2
-  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int64_t rows = (args.M + 255) / 256, tiles_n = (args.N + C::BN - 1) / C::BN;
-  const int64_t num_tiles = rows * tiles_n;
+  const int64_t num_tiles = EXPERTS ? ex_tile0[E] : rows * tiles_n;
   const int kb_count = (int)(args.K / C::BK);
-  auto tile_origin = [&](int64_t t, int64_t &m0, int64_t &n0) {
-    const int64_t band = t / (kPromoteBandRows * tiles_n);
-    const int64_t left = rows - band * kPromoteBandRows;
-    const int64_t band_rows = left < kPromoteBandRows ? left : kPromoteBandRows;
-    const int64_t local = t - band * kPromoteBandRows * tiles_n;
-    m0 = (band * kPromoteBandRows + local % band_rows) * 256;
-    n0 = (local / band_rows) * C::BN;
+  // Tile t: rows [m0, row_end) of A and C (row_end ends the expert's rows),
+  // columns [n0, n0 + BN), B tensor-map row brow, scale offset sbo.  Pair p
+  // takes tiles p, p + npairs, ...; plain rows go in the grouped order
+  // (bands of kPromoteBandRows 256-row tiles walked column by column, so
+  // the pairs in flight share A and B blocks in L2), expert rows expert by
+  // expert, row tile by row tile.
+  struct TileInfo {
+    int64_t m0, n0, row_end, brow, sbo;
+  };
+  auto tile_info = [&](int64_t t) {
+    TileInfo ti;
+    if constexpr (EXPERTS) {
+      int lo = 0, hi = E;  // the expert e with ex_tile0[e] <= t < ex_tile0[e + 1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ex_tile0[mid] <= t) lo = mid; else hi = mid;
+      }
+      while (lo + 1 < E && ex_tile0[lo + 1] <= t) ++lo;  // skip empty experts
+      const int64_t local = t - ex_tile0[lo];
+      ti.m0 = ex_row0[lo] + (local / tiles_n) * 256;
+      ti.n0 = (local % tiles_n) * C::BN;
+      ti.row_end = ex_row0[lo + 1];
+      ti.brow = (int64_t)lo * args.N + ti.n0;
+      ti.sbo = (int64_t)lo * args.sb_expert_stride;
+    } else {
+      // (32-bit: tile counts fit, and the 64-bit division's register needs
+      // would meet the accumulators)
+      const uint32_t tn = (uint32_t)tiles_n, t32 = (uint32_t)t;
+      const uint32_t band = t32 / ((uint32_t)kPromoteBandRows * tn);
+      const uint32_t left = (uint32_t)rows - band * (uint32_t)kPromoteBandRows;
+      const uint32_t band_rows = left < (uint32_t)kPromoteBandRows ? left : (uint32_t)kPromoteBandRows;
+      const uint32_t local = t32 - band * (uint32_t)kPromoteBandRows * tn;
+      ti.m0 = (int64_t)(band * (uint32_t)kPromoteBandRows + local % band_rows) * 256;
+      ti.n0 = (int64_t)(local / band_rows) * C::BN;
+      ti.row_end = args.M;
+      ti.brow = ti.n0;
+      ti.sbo = 0;
+    }
+    return ti;
   };
 
   if (warp == 0) {
@@ -135,10 +205,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGE
     uint32_t it = 0;
     bool ok = true;
     for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
-      int64_t m0, n0;
-      tile_origin(t, m0, n0);
-      const int32_t am = (int32_t)(m0 + rank * C::BM);
-      const int32_t bn = (int32_t)(n0 + rank * (C::BN / 2));
+      const TileInfo ti = tile_info(t);
+      const int32_t am = (int32_t)(ti.m0 + rank * C::BM);
+      const int32_t bn = (int32_t)(ti.brow + rank * (C::BN / 2));
       for (int kb = 0; kb < kb_count; ++kb, ++it) {
         const int s = (int)(it % STAGES);
         const uint32_t round = it / STAGES;
@@ -214,18 +283,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGE
     uint32_t it = 0;
     bool ok = true;
     for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
-      int64_t m0, n0;
-      tile_origin(t, m0, n0);
-      const int64_t row = m0 + rank * C::BM + 32 * q + lane;
+      const TileInfo ti = tile_info(t);
+      const int64_t n0 = ti.n0;
+      const int64_t row = ti.m0 + rank * C::BM + 32 * q + lane;
       // this warp's columns lie in one 128-row block of B; a warp wholly
-      // past N (or a lane past M) multiplies by a zero scale and stores
-      // nothing
-      const bool row_in = row < args.M, cols_in = n0 + col0 < args.N;
+      // past N (or a lane past its rows: past M, or in the next expert's)
+      // multiplies by a zero scale and stores nothing
+      const bool row_in = row < ti.row_end, cols_in = n0 + col0 < args.N;
       // scale of slice k: sa[k][row] * sb[block][k]; the next slice's pair
       // is loaded one slice ahead, and the line four slices ahead is
       // brought into L2 meanwhile (no registers held for it)
       const float *sa_p = static_cast<const float *>(args.sa) + (row_in ? row : 0);
-      const float *sb_p = static_cast<const float *>(args.sb) + ((n0 + col0) >> 7) * G;
+      const float *sb_p = static_cast<const float *>(args.sb) + ti.sbo + ((n0 + col0) >> 7) * G;
       constexpr int kAhead = 4;
       float na = row_in ? __ldg(sa_p) : 0.0f, nb = cols_in ? __ldg(sb_p) : 0.0f;
       float acc[kCols];
@@ -277,12 +346,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGE
         ++it;
       }
       if (!ok) break;
+      // the tile's origin once more (not held in registers across the slices)
+      const TileInfo to = tile_info(t);
+      const int64_t orow = to.m0 + rank * C::BM + 32 * q + lane;
 #pragma unroll
       for (int c = 0; c < kCols / 32; ++c) {
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = acc[32 * c + i];
-        store_row32(args, row, n0 + col0 + 32 * c, v);
+        // (store_row32 itself skips rows past M; expert rows end earlier)
+        if (!EXPERTS || orow < to.row_end) store_row32(args, orow, to.n0 + col0 + 32 * c, v);
       }
     }
   }
@@ -318,19 +391,20 @@ int gemm_pair_promote_b_rows() { return PromoteC::BN / 2; }
 // The pair kernel has no split K: it pays off once the 256 x 256 tiles give
 // at least half of the pairs work (one round of them then takes less time
 // than the one-CTA kernel's two rounds of 128 x 128 tiles).  K-major
-// operands only (the group scales run along K).
+// operands only (the group scales run along K).  Expert-grouped rows count
+// the tiles of the rows alone (at most one partial row tile per expert
+// more).
 bool gemm_pair_promote_eligible(int64_t M, int64_t N, int64_t K, int sms) {
   if (K % 128 != 0) return false;
   const int64_t tiles = ((M + 255) / 256) * ((N + PromoteC::BN - 1) / PromoteC::BN);
   return tiles >= sms / 4;
 }
 
-cudaError_t launch_gemm_pair_promote(const CUtensorMap &tma, const CUtensorMap &tmb,
-                                     const GemmArgs &args, int sms, cudaStream_t st) {
+template <bool EXPERTS>
+static cudaError_t run_pair_promote(const CUtensorMap &tma, const CUtensorMap &tmb,
+                                    const GemmArgs &args, int sms, cudaStream_t st) {
   using C = PromoteC;
-  if (args.K % 128 != 0 || args.a_mn || args.b_mn || args.ksplit != 1 || args.experts != 0)
-    return cudaErrorInvalidValue;
-  auto kern = gemm_pair_promote_kernel<kPromoteBN, kPromoteStages, kPromoteEpiWarps>;
+  auto kern = gemm_pair_promote_kernel<kPromoteBN, kPromoteStages, kPromoteEpiWarps, EXPERTS>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -341,10 +415,23 @@ cudaError_t launch_gemm_pair_promote(const CUtensorMap &tma, const CUtensorMap &
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const int64_t tiles = ((args.M + 255) / 256) * ((args.N + C::BN - 1) / C::BN);
+  // (expert-grouped rows: the tile count is known on the device only; the
+  // bound adds one partial row tile per expert)
+  const int64_t row_tiles = (args.M + 255) / 256 + (EXPERTS ? args.experts : 0);
+  const int64_t tiles = row_tiles * ((args.N + C::BN - 1) / C::BN);
   const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
   kern<<<(unsigned)(2 * pairs), C::kThreads, C::kSmem, st>>>(tma, tmb, args);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_pair_promote(const CUtensorMap &tma, const CUtensorMap &tmb,
+                                     const GemmArgs &args, int sms, cudaStream_t st) {
+  if (args.K % 128 != 0 || args.a_mn || args.b_mn || args.ksplit != 1) return cudaErrorInvalidValue;
+  if (args.experts > 0) {
+    if (args.experts > kMaxExperts || args.offsets == nullptr) return cudaErrorInvalidValue;
+    return run_pair_promote<true>(tma, tmb, args, sms, st);
+  }
+  return run_pair_promote<false>(tma, tmb, args, sms, st);
 }
 
 }  // namespace fp8k

@@ -213,9 +213,11 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tma, const CUtensorMap &tmb,
                              cudaStream_t st);
 
 // CTA-pair variant of the FP32-scale per-group GEMM (kScaleGroupF32):
-// 256 x 128 tiles, the per-slice promotion in both CTAs' epilogues; K-major
-// operands, K % 128 == 0, no split K, no experts.  The B tensor map box has
-// gemm_pair_promote_b_rows() rows.
+// 256 x 256 tiles, the per-slice promotion in both CTAs' epilogues; K-major
+// operands, K % 128 == 0, no split K; plain or expert-grouped rows
+// (args.experts, args.offsets, args.sb_expert_stride as for
+// launch_gemm_experts, B's tensor map over all experts' rows).  The B tensor
+// map box has gemm_pair_promote_b_rows() rows.
 bool gemm_pair_promote_eligible(int64_t M, int64_t N, int64_t K, int sms);
 int gemm_pair_promote_b_rows();
 cudaError_t launch_gemm_pair_promote(const CUtensorMap &tma, const CUtensorMap &tmb,

@@ -731,6 +731,30 @@ def test_gemm_group_experts(sfmt, case):
     assert F.fp8_get_last_device_error()[0] == 0
 
 
+def test_gemm_group_experts_f32_cta_pairs():
+    """FP32 expert-grouped rows on the CTA-pair kernel (256-row expert tiles):
+    an empty expert, a 1-row expert, experts of 255 and 257 rows (a tile
+    boundary just short of and just past the expert's end), ragged N (1000 =
+    3 * 256 + 232), against the oracle, with pairs on and off (off: the
+    one-CTA kernel)."""
+    F = lib()
+    counts = [700, 0, 1, 1100, 255, 257]
+    n, k = 1000, 384
+    qa, sa, qb, sb, offs, c, e, m = expert_operands(len(counts), sum(counts), n, k, "f32",
+                                                    seed=77, counts=counts)
+    try:
+        for pairs in (1, 0):
+            F.fp8_set_option(F.OPT_GEMM_CTA_PAIRS, pairs)
+            out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+            F.fp8_gemm_group_experts(qa, sa, qb, sb, F.SCALE_F32, offs, out)
+            torch.cuda.synchronize()
+            ok, worst = OG.check(out.float().cpu().numpy(), c, e, "bf16")
+            assert ok, (pairs, worst)
+    finally:
+        F.fp8_set_option(F.OPT_GEMM_CTA_PAIRS, 1)
+    assert F.fp8_get_last_device_error()[0] == 0
+
+
 # ------------------------------------------------------------ epilogue bias --
 
 def _bias(n, seed):
