@@ -746,8 +746,9 @@ int fp8_gemm_group_bias(const uint8_t *a, const void *sa, const uint8_t *b, cons
         fp8k::launch_gemv_group(a, sa, b, sb, sfmt, M, N, K, bias, c, (cudaStream_t)stream));
   }
   if (g_use_skinny && fp8k::gemm_skinny_rows(M) != 0) {
-    // 1-64 rows: the weights stream through the few-row kernel (its tile
-    // is 128 weight rows x the activation rows padded to 16, 32 or 64)
+    // 1-128 rows: the weights stream through the few-row kernel (its tile
+    // is 128 weight rows x the activation rows padded to 16, 32 or 64; two
+    // 64-row halves beyond 64)
     DeviceState *d = nullptr;
     if ((rc = device_state(&d)) != FP8_OK) return rc;
     args.err = d->err;

@@ -1,4 +1,4 @@
-// Per-K-group GEMM for few activation rows (M <= 64), the decode-sized
+// Per-K-group GEMM for few activation rows (M <= 128), the decode-sized
 // shape of fine-grained FP8 (Transformers fine-grained FP8, 一: C[m, n] =
 // sum over 128-wide K groups g of sa[m, g] * sb[n / 128, g] *
 // sum_{k in g} qa[m, k] qb[n, k]; 六: per-token dynamic activation scales).
@@ -16,9 +16,13 @@
 // the promotion after each 128-wide K slice is, per thread (one weight row),
 //   acc[m] += (sa[g, m] * sb[n0 / 128, g]) * D[n, m]
 // over MP columns only, and each lane fetches the activation scale of one
-// column that the warp then shares by shuffles.  (From 65 rows on, the
-// general per-group kernel measured as fast or faster: the exchange below
-// grows with the rows.)
+// column that the warp then shares by shuffles.  65-128 rows run as two
+// 64-row halves, a second row of CTAs along the grid's y that streams the
+// same weights (its reads hit L2): in CUDA graphs at N 2048, K 7168, M = 128
+// took 10.4 / 10.7 us (FP32 / UE8M0 scales) against 11.9 / 13.5 us on the
+// general kernel, where one CTA with MP = 128 took 12.6-13.7 us (the
+// exchange of a 128 x 128 fp32 partial per CTA, and a stage ring cut to
+// four to leave room for its receive buffer).
 //
 // Each output tile's K range is split over a thread-block cluster of up to
 // 8 CTAs (as many as fit beside the other tiles' clusters); each CTA issues
@@ -120,6 +124,11 @@ __global__ void __launch_bounds__(SkinnyCfg<MP>::kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const DevErr err{args.err, args.wait_limit_ns};
+  // activation rows [mb, mb + Mh) of this CTA: 65-128 rows run as two
+  // 64-row halves along the grid's y (each streams the same weights; the
+  // second read is an L2 hit)
+  const int64_t mb = (int64_t)blockIdx.y * MP;
+  const int64_t Mh = args.M - mb < MP ? args.M - mb : MP;
   const int ks = args.ksplit;  // 1..8
   const uint32_t rank = ks > 1 ? cluster_ctarank() : 0u;
   const int64_t n0 = (int64_t)(blockIdx.x / (uint32_t)ks) * 128;
@@ -172,7 +181,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP>::kThreads, 1)
         }
         mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
         tma_load_2d(sW(s), &tmw, full_bar(s), kb * 128, (int32_t)n0);
-        tma_load_2d(sX(s), &tmx, full_bar(s), kb * 128, 0);
+        tma_load_2d(sX(s), &tmx, full_bar(s), kb * 128, (int32_t)mb);
       }
       if (!ok) {  // let the copies already in flight land before the CTA can exit
         const uint32_t first = it > (uint32_t)C::kStages ? it - C::kStages : 0u;
@@ -233,7 +242,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP>::kThreads, 1)
 #pragma unroll
       for (int j = 0; j < C::kJ; ++j) {
         const int64_t m = mcol0 + 32 * j + lane;
-        v[j] = m < args.M ? skinny_scale_raw<SFMT>(args.sa, (int64_t)kb * args.M + m) : 0u;
+        v[j] = m < Mh ? skinny_scale_raw<SFMT>(args.sa, (int64_t)kb * args.M + mb + m) : 0u;
       }
       b = skinny_scale_raw<SFMT>(args.sb, sbo + kb);
     };
@@ -282,11 +291,11 @@ __global__ void __launch_bounds__(SkinnyCfg<MP>::kThreads, 1)
       const int64_t n = n0 + nl;
       if (ok && n < args.N) {
         const float bn = args.bias != nullptr ? __ldg(args.bias + n) : 0.0f;
-        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(args.c);
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(args.c) + mb * args.ldc;
 #pragma unroll
         for (int c = 0; c < C::kCols; ++c) {
           const int64_t m = mcol0 + c;
-          if (m < args.M) out[m * args.ldc + n] = __float2bfloat16_rn(acc[c] + bn);
+          if (m < Mh) out[m * args.ldc + n] = __float2bfloat16_rn(acc[c] + bn);
         }
       }
     } else {
@@ -299,7 +308,7 @@ __global__ void __launch_bounds__(SkinnyCfg<MP>::kThreads, 1)
                            ((rank * (uint32_t)W + j) * C::kRecvPitch + (uint32_t)mcol0) * 4u;
 #pragma unroll
       for (int c = 0; c < C::kCols; c += 4)
-        if (mcol0 + c < args.M)
+        if (mcol0 + c < Mh)
           st_shared_cluster_v4(dst + (uint32_t)c * 4u, acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
     }
   }
@@ -309,9 +318,9 @@ __global__ void __launch_bounds__(SkinnyCfg<MP>::kThreads, 1)
     // this CTA's weight rows [rank W, rank W + own): the sum over the splits,
     // in split order, plus the bias, to bf16; lanes walk the owned rows
     // (consecutive output columns), warps groups of four activation rows
-    const int rows = args.M < MP ? (int)args.M : MP;
+    const int rows = (int)Mh;
     const int own = 128 - (int)rank * W < W ? 128 - (int)rank * W : W;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(args.c);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(args.c) + mb * args.ldc;
     for (int m4 = (int)warp * 4; m4 < rows; m4 += C::kThreads / 32 * 4) {
       for (int j = (int)lane; j < own; j += 32) {
         const int64_t n = n0 + (int64_t)rank * W + j;
@@ -337,13 +346,16 @@ __global__ void __launch_bounds__(SkinnyCfg<MP>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// Padded activation rows for M rows (0: not a few-row shape).
+// Padded activation rows per CTA for M rows (0: not a few-row shape);
+// 65-128 rows take two 64-row halves.
 int gemm_skinny_rows(int64_t M) {
-  if (M < 1 || M > 64) return 0;
+  if (M < 1 || M > kSkinnyMaxRows) return 0;
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   return 64;
 }
+
+static int64_t skinny_halves(int64_t M) { return M > 64 ? (M + 63) / 64 : 1; }
 
 template <int SFMT, int MP>
 static cudaError_t skinny_attr(int dev) {
@@ -405,7 +417,7 @@ static int skinny_clusters_cached(int mp, int size) {
 int gemm_skinny_ksplit(int64_t M, int64_t N, int64_t K, int sms) {
   const int mp = gemm_skinny_rows(M);
   if (mp == 0) return 1;
-  const int64_t tiles = (N + 127) / 128, G = K / 128;
+  const int64_t tiles = (N + 127) / 128 * skinny_halves(M), G = K / 128;
   int ks = kMaxClusterSplit;
   while (ks > 1 && (tiles * ks > sms || ks > G || skinny_clusters_cached(mp, ks) < tiles)) --ks;
   return ks;
@@ -424,7 +436,7 @@ static cudaError_t run_skinny(const CUtensorMap &tmw, const CUtensorMap &tmx, co
     return cudaErrorInvalidValue;
   const int64_t tiles = (args.N + 127) / 128;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * ks));
+  cfg.gridDim = dim3((unsigned)(tiles * ks), (unsigned)skinny_halves(args.M));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;

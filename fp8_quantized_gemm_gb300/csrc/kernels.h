@@ -179,10 +179,12 @@ int gemm_ksplit(int mode, int64_t M, int64_t N, int64_t K, int sms, bool cluster
 // Output-tile width (N) of a mode at M rows; the B tensor map's box uses it.
 int gemm_tile_n(int mode, int64_t M, int64_t N, int sms);
 
-// Per-K-group GEMM for 1 <= M <= 64 activation rows (gemm_skinny.cu): bf16
+// Per-K-group GEMM for 1 <= M <= kSkinnyMaxRows activation rows
+// (gemm_skinny.cu; beyond 64 rows, 64-row halves along the grid's y): bf16
 // output, optional bias, K % 128 == 0.  tmw: the weights [N, K] with
 // 128 x 128 boxes; tmx: the activations [M, K] with boxes of
 // gemm_skinny_rows(M) rows x 128.  args.ksplit = gemm_skinny_ksplit(...).
+constexpr int64_t kSkinnyMaxRows = 128;
 int gemm_skinny_rows(int64_t M);
 int gemm_skinny_ksplit(int64_t M, int64_t N, int64_t K, int sms);
 cudaError_t launch_gemm_skinny(int sfmt, const CUtensorMap &tmw, const CUtensorMap &tmx,

@@ -391,10 +391,10 @@ FP8_API int fp8_gemm_tensor_grouped(const fp8_gemm_problem_t *problems, int coun
  *   b  [N, K] E4M3 codes, sb [ceil(N/128), K/128] (fp8_quantize_block).
  *   sfmt FP8_SCALE_F32: fp32 scales, partial sums promoted per 128-K group on
  *        the CUDA cores.  FP8_SCALE_UE8M0: byte scales, applied by the tensor
- *        core as block scale factors (no promotion); with 1-64 rows they are
- *        promoted like fp32 scales (exact powers of two).
+ *        core as block scale factors (no promotion); with 1-128 rows they
+ *        are promoted like fp32 scales (exact powers of two).
  *   K % 128 == 0.  c [M, ldc] bf16 as for fp8_gemm_tensor.
- *   With 1-64 rows the call runs the few-row kernel (FP8_OPT_GEMM_SKINNY),
+ *   With 1-128 rows the call runs the few-row kernel (FP8_OPT_GEMM_SKINNY),
  *   launched with programmatic stream serialization: it may start before the
  *   previous kernel on `stream` ends, and then reads and writes nothing that
  *   kernel may write until it has completed.  Every per-group GEMM launch and
@@ -410,7 +410,7 @@ FP8_API int fp8_gemm_group(const uint8_t *a, const void *sa, const uint8_t *b, c
  * device memory.  The pages have no counterpart to this entry point; it
  * exists for this library's users.  Its result agrees with fp8_gemm_group's
  * within the GEMM bound, not bit for bit: it always runs the general
- * tensor-core per-group kernel, while fp8_gemm_group runs 1-64 rows on its
+ * tensor-core per-group kernel, while fp8_gemm_group runs 1-128 rows on its
  * few-row kernel and converts UE8M0 scales to block-scale words for
  * M > 128.
  *
@@ -669,10 +669,11 @@ FP8_API const char *fp8_version(void);
  *     fewer times, at the price of a larger A working set in L2.  Same
  *     results.
  *   FP8_OPT_GEMM_SKINNY: 1 (default) runs fp8_gemm_group / _group_bias with
- *     1 to 64 activation rows (one row only while FP8_OPT_GEMM_FEW_ROWS is
+ *     1 to 128 activation rows (one row only while FP8_OPT_GEMM_FEW_ROWS is
  *     0) on the few-row tensor-core kernel: 128 weight rows per tile on the
  *     MMA's M side, the activation rows padded to 16, 32 or 64 on its N
- *     side, K split over a thread-block cluster, launched so that it may
+ *     side (65-128 rows as two 64-row halves of CTAs), K split over a
+ *     thread-block cluster, launched so that it may
  *     start before the previous kernel in the stream ends; 0 keeps them on
  *     the general per-group kernel.  Results agree within the GEMM bound. */
 typedef enum {

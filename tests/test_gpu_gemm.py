@@ -380,8 +380,8 @@ def test_gemm_group_few_rows_kernel(mnk, sfmt):
     a cluster) against the oracle, with the switch on and off: every padded
     width and its edges, ragged N (the last weight tile partly past N), K
     shorter than the cluster (one k block per split), a bias and an output
-    pitch wider than N.  Past 64 rows (65, 100, 128) both settings run the
-    general kernel."""
+    pitch wider than N.  Past 64 rows (65, 100, 128) the switch on runs two
+    64-row halves of CTAs (the second one ragged at 65 and 100)."""
     F = lib()
     m, n, k = mnk
     qa, sa, qb, sb = group_operands(m, n, k, sfmt, seed=m + n)
