@@ -127,7 +127,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGE
         const int e = 8 * (int)lane + i;
         cnt[i] = 0;
         if (e < E) {
-          const int32_t r0 = args.offsets[e], r1 = args.offsets[e + 1];
+          // (row starts clamped to [0, M]: no scale or output row past the
+          // last token even if the offsets break their contract)
+          const int32_t mm = (int32_t)args.M;
+          const int32_t r0 = min(max(args.offsets[e], 0), mm);
+          const int32_t r1 = min(max(args.offsets[e + 1], 0), mm);
           ex_row0[e] = r0;
           cnt[i] = r1 > r0 ? (int64_t)((r1 - r0 + 255) / 256) * tiles_n : 0;
           if (e == E - 1) ex_row0[E] = r1;

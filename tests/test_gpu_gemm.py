@@ -712,6 +712,7 @@ def expert_operands(experts, tokens, n, k, sfmt, seed, counts=None):
     (3, 0, 200, 256, [130, 0, 257]),             # N not a multiple of 128
     (16, 4096, 512, 2048, None),
     (8, 4096, 2048, 1024, None),                 # 128 x 256 tiles
+    (8, 4096, 2048, 7168, None),                 # the MoE workload bench.py times
 ])
 def test_gemm_group_experts(sfmt, case):
     """Beyond M = 256 with N % 128 == 0 the UE8M0 case runs as the
