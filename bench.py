@@ -502,12 +502,14 @@ def run_headline(args, dev, peaks):
         "passes_gbs": {
             "quantize": round(qbytes / (per["quantize"] / 1e3) / 1e9, 1),
             "swiglu_quantize": round(sbytes / (per["swiglu_quantize"] / 1e3) / 1e9, 1),
-            "adamw": round(31.0 * 3 * ffn * d / (per["adamw"] / 1e3) / 1e9, 1),
+            "adamw": round((29.0 if wl.tr.fuse_wq else 30.0) * 3 * ffn * d
+                           / (per["adamw"] / 1e3) / 1e9, 1),
             "hbm_peak": peaks["hbm_gbs"],
             "note": "algorithmic bytes of the standalone passes: quantize x, dy (2 B read, "
                     "1 B codes); the SwiGLU backward reads da, h, u and writes the codes of dh "
-                    "and du; AdamW 31 B per weight (p, m, v read and written, dW read, bf16 "
-                    "copy and the next step's FP8 code written).  The SwiGLU forward runs in "
+                    "and du; AdamW 29 B per weight (p, m, v read and written, dW read, the "
+                    "next step's FP8 code written; no bf16 copy, which nothing reads when the "
+                    "optimizer writes the codes).  The SwiGLU forward runs in "
                     "the gated h|u GEMM's epilogue and is inside 'gemm'"},
         "clocks": clk.summary(),
         "gpu_launches": wl.kernels_per_step * args.steps,

@@ -50,7 +50,9 @@ histories are pushed first, which fixes the scales the next step quantizes
 the weights with, and fp8_adamw_multi then writes the codes of the updated
 weights (as bf16) under those scales and their amaxes -- what the next
 step's fp8_quantize_tensor calls on the bf16 copies would give -- so from
-the second step on the forward quantizes only x.
+the second step on the forward quantizes only x, and no call reads a bf16
+copy of the weights: the update writes none (`w_bf` then returns the bf16
+rounding of the fp32 masters, the values such a copy would hold).
 
 Buffers are allocated once (device memory through torch); `step` issues the
 calls on the current stream.
@@ -96,8 +98,12 @@ class SwiGLUTrainer:
         u8 = dict(dtype=torch.uint8, device=dev)
         T = tokens
         # weights: fp32 masters, moments, bf16 copies
-        self.w_bf = [w1.contiguous().clone(), w3.contiguous().clone(), w2.contiguous().clone()]
-        self.w_master = [w.float() for w in self.w_bf]
+        # (bf16 copies kept up to date only where a later call reads them:
+        # when the optimizer writes the next step's codes itself, nothing
+        # does, and the copies stay the initial weights; see w_bf)
+        self._w_bf = [w1.contiguous().clone(), w3.contiguous().clone(), w2.contiguous().clone()]
+        self.keep_bf16 = not self.fuse_wq
+        self.w_master = [w.float() for w in self._w_bf]
         self.m = [torch.zeros_like(w) for w in self.w_master]
         self.v = [torch.zeros_like(w) for w in self.w_master]
         # delayed-scaling state
@@ -123,7 +129,7 @@ class SwiGLUTrainer:
             # the weight-gradient GEMMs update the weights in their epilogues
             self.dw = [None, None, None]
             self.adamw_ep = [F.adamw_epilogue(self.w_master[i], self.m[i], self.v[i],
-                                              self.w_bf[i], self.step_dev, **self.hp)
+                                              self._w_bf[i], self.step_dev, **self.hp)
                              for i in range(3)]
         else:
             self.dw = [torch.empty((ffn, d), **f32), torch.empty((ffn, d), **f32),
@@ -131,7 +137,8 @@ class SwiGLUTrainer:
             self.adamw_ep = [None, None, None]
             wq, slot = (self.w1q, self.w3q, self.w2q), (K1, K3, K2)
             self.adamw_items = [
-                F.adamw_item(self.w_master[i], self.dw[i], self.m[i], self.v[i], self.w_bf[i],
+                F.adamw_item(self.w_master[i], self.dw[i], self.m[i], self.v[i],
+                             self._w_bf[i] if self.keep_bf16 else None,
                              **(dict(q=wq[i], q_scale=self.scale[slot[i]:slot[i] + 1],
                                      q_amax=self.amax[slot[i]:slot[i] + 1], q_fmt=F.E4M3)
                                 if self.fuse_wq else {}))
@@ -149,8 +156,18 @@ class SwiGLUTrainer:
     def refresh_weight_amax(self):
         """The max-reduction of automatic scaling (fp8_amax of each weight)."""
         for i in range(3):
-            F.fp8_amax(self.w_bf[i], self.w_amax0[i:i + 1])
+            F.fp8_amax(self._w_bf[i], self.w_amax0[i:i + 1])
         self.t_since = 0
+
+    @property
+    def w_bf(self):
+        """The bf16 weights: the maintained copies, or, once the optimizer
+        writes the next step's codes itself (and keeps no bf16 copy), the bf16
+        rounding of the fp32 masters -- the same values the copies would hold
+        (plumbing for inspection; the step never reads it)."""
+        if self.keep_bf16 or not self.w_codes_ready:
+            return self._w_bf
+        return [w.to(torch.bfloat16) for w in self.w_master]
 
     def _sc(self, i):
         return self.scale[i:i + 1]
@@ -163,7 +180,7 @@ class SwiGLUTrainer:
         optimizer also the AdamW updates (in the weight-gradient GEMMs)."""
         E4, E5, MN = F.E4M3, F.E5M2, F.MN_MAJOR
         q, P, run = F.fp8_quantize_tensor, F.gemm_problem, F.fp8_gemm_tensor_grouped
-        w1, w3, w2 = self.w_bf
+        w1, w3, w2 = self._w_bf
         sc = self._sc
         # forward
         q(x, E4, self.xq, scale=sc(X1), amax_out=self._am(X1))
