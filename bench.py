@@ -418,6 +418,16 @@ class SwiGLUStep:
         ms = start.elapsed_time(end) / steps
         h2d = hx.numel() * hx.element_size() + hdy[0].numel() * hdy[0].element_size()
         d2h = 2 * 9 * 4
+        # the host link on its own: one step's input copies with nothing else
+        # running (the e2e step is link-bound when this takes longer than the
+        # device step)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(comp)
+        sets[0][0].copy_(hx, non_blocking=True)
+        sets[0][1].copy_(hdy[0], non_blocking=True)
+        c1.record(comp)
+        torch.cuda.synchronize()
+        self.h2d_copy_ms = c0.elapsed_time(c1)
         del sets, hx, hdy
         return ms, h2d, d2h
 
@@ -519,6 +529,8 @@ def run_headline(args, dev, peaks):
     line["e2e"] = {"value": round(wl.flops / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                    "ms_per_step": round(ms, 4), "steps": e2e_steps,
+                   "h2d_copy_alone_ms": round(wl.h2d_copy_ms, 4),
+                   "h2d_copy_alone_gbs": round(h2d / (wl.h2d_copy_ms / 1e3) / 1e9, 1),
                    "how": "pinned host -> device copy of the token batch x and the gradient dy "
                           "every step on a copy stream (two device input sets alternate, so "
                           "the next step's copies overlap this step's compute); eager API "
