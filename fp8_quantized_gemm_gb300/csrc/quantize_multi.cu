@@ -10,9 +10,9 @@
 //               into ring A: the amax stream, HBM-bound;
 //   warp 1      the same shares again into ring B: the quantize stream (mostly
 //               L2 hits: the tensor was read by the amax pass just before);
-//   warps 2-5   reduce ring A; after its last chunk of tensor t the CTA
+//   warps 2-13  reduce ring A; after its last chunk of tensor t the CTA
 //               publishes its max (atomicMax on a key) and counts itself in;
-//   warps 6-29 quantize ring B: before tensor t they wait until every CTA has
+//   warps 14-29 quantize ring B: before tensor t they wait until every CTA has
 //               counted in for t (a bounded spin on the counter), then divide
 //               by s_t, cast on store.  s_t comes from this tensor's own amax,
 //               so every quotient is finite and at most MAX (1 + 2^-23): the
@@ -35,7 +35,11 @@ constexpr uint32_t kMQChunk = 24576;
 // whose chunks go fastest: of the splits of nine stages, 4/5 measured best
 // (6/3 1.5% slower, 3/6 2%, 2/7 8%)
 constexpr int kMQStagesA = 4, kMQStagesB = 5;
-constexpr int kMQWarpsA = 4, kMQWarpsB = 24;
+// warps reducing ring A / casting ring B: with 4 / 24 the amax stream fell
+// to 3.5-4.4 TB/s while casts ran beside it (its 4 warps got few issue
+// slots); 12 / 16 measured 36.5 against 38.5 us for the Float8 linear's
+// three tensors (8 / 20 and 20 / 8: 38.5-38.6 us)
+constexpr int kMQWarpsA = 12, kMQWarpsB = 16;
 constexpr int kMQThreadsA = 32 * kMQWarpsA, kMQThreadsB = 32 * kMQWarpsB;
 constexpr int kMQThreads = 64 + kMQThreadsA + kMQThreadsB;
 constexpr int kMQNumBars = 2 * (kMQStagesA + kMQStagesB);
