@@ -101,6 +101,8 @@ FP8_API int fp8_amax(const void *x, int in_dt, int64_t n, float *amax_out, fp8_s
  *   amax_out nullable; receives max |x| (cleared first), the amax that the
  *           delayed-scaling history takes for this step.  Must not alias
  *           amax_in or scale (INVALID_ARG).
+ *   Codes: q = RNE_fp8(clip(fl32(x / s), -MAX, MAX)) for finite x; +-inf
+ *   gives +-MAX; a NaN x gives a NaN code (its sign bit may follow x's).
  */
 FP8_API int fp8_quantize_tensor(const void *x, int in_dt, int64_t rows, int64_t cols, int fmt,
                         const float *amax_in, const float *scale, float *scale_out,
