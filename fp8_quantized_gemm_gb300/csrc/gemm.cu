@@ -35,6 +35,7 @@
 //                                  32-deep K step, with the scales of each
 //                                  32-column weight block.
 #include "common.cuh"
+#include "expert_tiles.cuh"
 #include "gemm_common.cuh"
 #include "kernels.h"
 
@@ -159,50 +160,18 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   // CTAs share an A row block (L2 reuse of A; B is read by every row block).
   const int64_t tiles_n = (args.N + BN - 1) / BN;
   // Expert-grouped rows: a tile never spans two experts; expert e owns
-  // ceil(rows_e / 128) * tiles_n consecutive tile indices.  One warp turns
-  // the device offsets into that prefix (kept in shared memory) per CTA.
-  // The plain kernels compile this out (EXPERTS false).
-  __shared__ int64_t ex_tile0[EXPERTS ? kMaxExperts + 1 : 1];
-  __shared__ int32_t ex_row0[EXPERTS ? kMaxExperts + 1 : 1];
+  // ceil(rows_e / 128) * tiles_n consecutive tile indices (expert_tiles.cuh).
+  // The plain kernels keep no table (EXPERTS false).
+  __shared__ ExpertTiles<EXPERTS> ex;
   const int E = EXPERTS ? args.experts : 0;
   if constexpr (EXPERTS) {
-    if (warp == 0) {
-      // lane l takes experts [8l, 8l + 8)
-      int64_t cnt[8];
-      int64_t sum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = 8 * (int)lane + i;
-        cnt[i] = 0;
-        if (e < E) {
-          const int32_t r0 = args.offsets[e], r1 = args.offsets[e + 1];
-          ex_row0[e] = r0;
-          cnt[i] = r1 > r0 ? (int64_t)((r1 - r0 + C::BM - 1) / C::BM) * tiles_n : 0;
-          if (e == E - 1) ex_row0[E] = r1;
-        }
-        sum += cnt[i];
-      }
-      int64_t incl = sum;  // inclusive scan of the lane sums
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if ((int)lane >= o) incl += v;
-      }
-      int64_t run = incl - sum;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = 8 * (int)lane + i;
-        if (e < E) ex_tile0[e] = run;
-        run += cnt[i];
-        if (e == E - 1) ex_tile0[E] = run;
-      }
-    }
+    if (warp == 0) build_expert_tiles(args.offsets, E, args.M, tiles_n, C::BM, lane, ex);
     __syncthreads();
   }
   static_assert(MC == 1 || (MC == 2 && !EXPERTS), "multicast pairs plain row tiles");
   const int64_t row_tiles = (args.M + C::BM - 1) / C::BM;
   const int64_t num_tiles =
-      EXPERTS ? ex_tile0[E] : (MC == 2 ? (row_tiles + 1) / 2 : row_tiles) * tiles_n;
+      EXPERTS ? ex.tile0[E] : (MC == 2 ? (row_tiles + 1) / 2 : row_tiles) * tiles_n;
   const uint32_t mc_rank = MC == 2 ? cluster_ctarank() : 0u;
   const int KB = (int)((args.K + C::BK - 1) / C::BK);
   // work unit u = (tile u % num_tiles, K split u / num_tiles); with ksplit 1
@@ -219,19 +188,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, STAGES>::kThreads, 1)
   auto tile_info = [&](int64_t t) {
     TileInfo ti;
     if constexpr (EXPERTS) {
-      int lo = 0, hi = E;  // the expert e with ex_tile0[e] <= t < ex_tile0[e + 1]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (ex_tile0[mid] <= t) lo = mid; else hi = mid;
-      }
-      while (lo + 1 < E && ex_tile0[lo + 1] <= t) ++lo;  // skip empty experts
-      const int64_t local = t - ex_tile0[lo];
-      ti.m0 = ex_row0[lo] + (local / tiles_n) * C::BM;
+      const int lo = expert_of_tile(ex, E, t);
+      const int64_t local = t - ex.tile0[lo];
+      ti.m0 = ex.row0[lo] + (local / tiles_n) * C::BM;
       ti.n0 = (local % tiles_n) * BN;
-      ti.row_end = ex_row0[lo + 1];
+      ti.row_end = ex.row0[lo + 1];
       ti.brow = (int64_t)lo * args.N + ti.n0;
       ti.sbo = (int64_t)lo * args.sb_expert_stride;
-      ti.atile = ex_tile0[lo] / tiles_n + local / tiles_n;
+      ti.atile = ex.tile0[lo] / tiles_n + local / tiles_n;
     } else {
       // Grouped order: bands of kBandRows row tiles (row-tile pairs when
       // MC == 2), each walked column by column, so the CTAs in flight share

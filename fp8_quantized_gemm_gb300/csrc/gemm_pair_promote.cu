@@ -27,6 +27,7 @@
 // The scales of the next slice are loaded one slice ahead, and their lines
 // four slices ahead are brought into L2.
 #include "common.cuh"
+#include "expert_tiles.cuh"
 #include "gemm_common.cuh"
 #include "kernels.h"
 
@@ -111,48 +112,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGE
   const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int64_t rows = (args.M + 255) / 256, tiles_n = (args.N + C::BN - 1) / C::BN;
   // Expert-grouped rows (MoE): a tile never spans two experts; expert e
-  // owns ceil(rows_e / 256) * tiles_n consecutive tile indices.  Warp 0 of
-  // each CTA turns the device offsets into that prefix (both CTAs of a pair
-  // read the same offsets, so they agree on every tile).
-  __shared__ int64_t ex_tile0[EXPERTS ? kMaxExperts + 1 : 1];
-  __shared__ int32_t ex_row0[EXPERTS ? kMaxExperts + 1 : 1];
+  // owns ceil(rows_e / 256) * tiles_n consecutive tile indices
+  // (expert_tiles.cuh).  Both CTAs of a pair read the same offsets, so they
+  // agree on every tile.
+  __shared__ ExpertTiles<EXPERTS> ex;
   const int E = EXPERTS ? args.experts : 0;
   if constexpr (EXPERTS) {
-    if (warp == 0) {
-      // lane l takes experts [8l, 8l + 8)
-      int64_t cnt[8];
-      int64_t sum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = 8 * (int)lane + i;
-        cnt[i] = 0;
-        if (e < E) {
-          // (row starts clamped to [0, M]: no scale or output row past the
-          // last token even if the offsets break their contract)
-          const int32_t mm = (int32_t)args.M;
-          const int32_t r0 = min(max(args.offsets[e], 0), mm);
-          const int32_t r1 = min(max(args.offsets[e + 1], 0), mm);
-          ex_row0[e] = r0;
-          cnt[i] = r1 > r0 ? (int64_t)((r1 - r0 + 255) / 256) * tiles_n : 0;
-          if (e == E - 1) ex_row0[E] = r1;
-        }
-        sum += cnt[i];
-      }
-      int64_t incl = sum;  // inclusive scan of the lane sums
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if ((int)lane >= o) incl += v;
-      }
-      int64_t run = incl - sum;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = 8 * (int)lane + i;
-        if (e < E) ex_tile0[e] = run;
-        run += cnt[i];
-        if (e == E - 1) ex_tile0[E] = run;
-      }
-    }
+    if (warp == 0) build_expert_tiles(args.offsets, E, args.M, tiles_n, 256, lane, ex);
   }
   tc_fence_before();
   __syncthreads();
@@ -160,7 +126,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGE
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int64_t num_tiles = EXPERTS ? ex_tile0[E] : rows * tiles_n;
+  const int64_t num_tiles = EXPERTS ? ex.tile0[E] : rows * tiles_n;
   const int kb_count = (int)(args.K / C::BK);
   // Tile t: rows [m0, row_end) of A and C (row_end ends the expert's rows),
   // columns [n0, n0 + BN), B tensor-map row brow, scale offset sbo.  Pair p
@@ -174,16 +140,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PromoteCfg<BN, STAGE
   auto tile_info = [&](int64_t t) {
     TileInfo ti;
     if constexpr (EXPERTS) {
-      int lo = 0, hi = E;  // the expert e with ex_tile0[e] <= t < ex_tile0[e + 1]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (ex_tile0[mid] <= t) lo = mid; else hi = mid;
-      }
-      while (lo + 1 < E && ex_tile0[lo + 1] <= t) ++lo;  // skip empty experts
-      const int64_t local = t - ex_tile0[lo];
-      ti.m0 = ex_row0[lo] + (local / tiles_n) * 256;
+      const int lo = expert_of_tile(ex, E, t);
+      const int64_t local = t - ex.tile0[lo];
+      ti.m0 = ex.row0[lo] + (local / tiles_n) * 256;
       ti.n0 = (local % tiles_n) * C::BN;
-      ti.row_end = ex_row0[lo + 1];
+      ti.row_end = ex.row0[lo + 1];
       ti.brow = (int64_t)lo * args.N + ti.n0;
       ti.sbo = (int64_t)lo * args.sb_expert_stride;
     } else {
